@@ -1,0 +1,404 @@
+"""Benchmark: fused softmax cross-entropy forward+backward (gradient written
+over the logits) on one GB300, through the library's C ABI.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
+                    [--workload NAME]
+
+One step is one pass of the whole hot path over one batch: the online
+max/log-sum-exp forward, the target gather, the deterministic mean and the
+in-place gradient, i.e. one ce_fwd_bwd_inplace call on a fresh synthetic
+[M, V] logits matrix already resident in HBM.  Every timed step works on its
+own copy of the input (each larger than the 129 MB L2), so no step starts
+with a warm L2.  Prints ONE JSON line (rank 0).
+
+--impl reference times the float64 CPU oracle on the host cores on a bounded
+sample of the same workload (the slow, obviously correct baseline).
+Under torchrun (N > 1) each rank runs its own replica of the workload on its
+own GPU (weak scaling); the step time is the max over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from softmax_cross_entropy_online_gb300 import synthetic  # noqa: E402
+
+METRIC = "CE fwd+bwd GB/s and % of GB300 HBM roofline (ms per call) at 1 GPU"
+FALLBACK_HBM_GBS = 6800.0
+
+# DRAM traffic of the fused fwd+bwd kernel per launch on f32 [32768, 4096],
+# from `ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum` (summarised
+# under profiles/), valid only for the kernel source it was taken on: the
+# digest of csrc/ at that time.  Any change to the kernels nulls it.
+NCU_TRAFFIC = {
+    # "<sha256 of csrc/*>": {"workload": "...", "bytes_per_launch": int}
+}
+
+
+def algorithmic_bytes(M: int, V: int, es: int, bwd: bool) -> int:
+    """Bytes the method must move: one read of the logits (+ one write of the
+    gradient), the int64 targets, and the fp32 row_loss and lse outputs."""
+    x = M * V * es
+    return x * (2 if bwd else 1) + M * 8 + M * 4 * 2 + 4
+
+
+def csrc_digest() -> str:
+    d = os.path.join(ROOT, "softmax_cross_entropy_online_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(d)):
+        if f.endswith((".cu", ".cuh")):
+            with open(os.path.join(d, f), "rb") as fh:
+                h.update(f.encode() + b"\0" + fh.read())
+    return h.hexdigest()
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            d = json.load(fh)
+        if d.get("hbm_gbs"):
+            return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the float64 oracle on the host cores
+# ---------------------------------------------------------------------------
+def run_reference(args, w):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    es = synthetic.ELEM_BYTES[w.dtype]
+    sample_rows = max(16, min(w.M, args.ref_rows))
+    x = synthetic.make_logits(sample_rows, w.V, w.dtype, w.sigma, w.spike_prob, w.spike_value,
+                              w.seed)
+    t = synthetic.make_targets(sample_rows, w.V, w.seed)
+    x64 = oracle.to_f64(x, w.dtype)
+    for _ in range(args.warmup):
+        oracle.ce_fwd_bwd(x64[:16], t[:16], "mean")
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.ce_fwd_bwd(oracle.to_f64(x, w.dtype), t, "mean")
+        times.append(time.perf_counter() - t0)
+    step_s = sum(times) / len(times)
+    b = algorithmic_bytes(sample_rows, w.V, es, True)
+    gbs = b / step_s / 1e9
+    sample = f"{sample_rows} of {w.M} rows of {w.name} per step (float64 numpy, 1 thread)"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": workload_desc(w), "M": w.M, "V": w.V, "sample_rows": sample_rows},
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_desc(w):
+    return f"{w.name}: {w.desc}"
+
+
+def cpu_baseline(w, budget_s: float):
+    """Time the oracle (as it stands) on a bounded sample of the workload."""
+    import oracle
+    es = synthetic.ELEM_BYTES[w.dtype]
+    probe = max(8, min(w.M, (1 << 22) // w.V))
+    x = synthetic.make_logits(probe, w.V, w.dtype, w.sigma, w.spike_prob, w.spike_value, w.seed)
+    t = synthetic.make_targets(probe, w.V, w.seed)
+    t0 = time.perf_counter()
+    oracle.ce_fwd_bwd(oracle.to_f64(x, w.dtype), t, "mean")
+    dt = time.perf_counter() - t0
+    rows = int(min(w.M, max(probe, probe * budget_s / max(dt, 1e-6))))
+    x = synthetic.make_logits(rows, w.V, w.dtype, w.sigma, w.spike_prob, w.spike_value, w.seed)
+    t = synthetic.make_targets(rows, w.V, w.seed)
+    t0 = time.perf_counter()
+    oracle.ce_fwd_bwd(oracle.to_f64(x, w.dtype), t, "mean")
+    dt = time.perf_counter() - t0
+    gbs = algorithmic_bytes(rows, w.V, es, True) / dt / 1e9
+    return {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{rows} of {w.M} rows of {w.name}, fwd+bwd in float64 numpy "
+                      f"({dt:.1f} s on 1 host thread)"}
+
+
+# ---------------------------------------------------------------------------
+# native arm
+# ---------------------------------------------------------------------------
+def run_native(args, w):
+    import torch
+    import torch.distributed as dist
+
+    from softmax_cross_entropy_online_gb300 import api, build
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    build.build()
+    L = api.lib()
+
+    M, V = w.M, w.V
+    es = synthetic.ELEM_BYTES[w.dtype]
+    tdt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[w.dtype]
+    code = {"f32": 0, "f16": 1, "bf16": 2}[w.dtype]
+
+    x_np = synthetic.make_logits(M, V, w.dtype, w.sigma, w.spike_prob, w.spike_value, w.seed)
+    t_np = synthetic.make_targets(M, V, w.seed)
+    if w.dtype == "bf16":
+        host = torch.from_numpy(x_np.view(np.int16)).view(torch.bfloat16)
+    else:
+        host = torch.from_numpy(x_np)
+    host = host.pin_memory()
+    t_host = torch.from_numpy(t_np).pin_memory()
+    pristine = host.to(dev)
+    targets = t_host.to(dev)
+    step_bytes = M * V * es
+    n_bufs = args.steps + args.warmup
+    if n_bufs * step_bytes > args.max_resident_gb * 1e9:
+        n_bufs = max(2, int(args.max_resident_gb * 1e9 // step_bytes))
+    bufs = [pristine.clone() for _ in range(n_bufs)]
+    loss = torch.empty((), dtype=torch.float32, device=dev)
+    row_loss = torch.empty(M, dtype=torch.float32, device=dev)
+    lse = torch.empty(M, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+
+    def step(buf):
+        st = L.ce_fwd_bwd_inplace(buf.data_ptr(), targets.data_ptr(), M, V, code, 0,
+                                  loss.data_ptr(), row_loss.data_ptr(), lse.data_ptr(), sh)
+        if st != 0:
+            raise api.CEError(st, "ce_fwd_bwd_inplace")
+
+    for i in range(args.warmup):
+        step(bufs[(args.steps + i) % n_bufs])
+    # refresh every timed buffer with the pristine logits (untimed)
+    for b in bufs:
+        b.copy_(pristine)
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    region0 = torch.cuda.Event(enable_timing=True)
+    region1 = torch.cuda.Event(enable_timing=True)
+    launches0 = api.ce_launch_count()
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    region0.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        step(bufs[i % n_bufs])
+        ev[i][1].record(stream)
+    region1.record(stream)
+    torch.cuda.synchronize()
+    launches = api.ce_launch_count() - launches0
+    clocks = sampler.stop() if sampler else None
+    region_ms = region0.elapsed_time(region1)
+    kernel_ms = [a.elapsed_time(b) for a, b in ev]
+    if ws > 1:
+        tt = torch.tensor([region_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        region_ms = float(tt.item())
+    assert api.ce_check_errors() == 0
+
+    ms_per_step = region_ms / args.steps
+    b_step = algorithmic_bytes(M, V, es, True)
+    value = ws * b_step / (ms_per_step * 1e-3) / 1e9
+    avg_kernel_ms = sum(kernel_ms) / len(kernel_ms)
+    peak, peak_kind = measured_peaks()
+    achieved = b_step / (avg_kernel_ms * 1e-3) / 1e9
+    traffic = NCU_TRAFFIC.get(csrc_digest(), {}).get("bytes_per_launch")
+
+    # forward-only pass on the same workload (the first half of the config)
+    fwd_ms = None
+    if rank == 0:
+        for b in bufs[:2]:
+            b.copy_(pristine)
+        torch.cuda.synchronize()
+        fe0 = torch.cuda.Event(enable_timing=True)
+        fe1 = torch.cuda.Event(enable_timing=True)
+        nf = min(args.steps, n_bufs)
+        for i in range(3):
+            L.ce_forward(bufs[i % n_bufs].data_ptr(), targets.data_ptr(), M, V, code, 0,
+                         loss.data_ptr(), row_loss.data_ptr(), lse.data_ptr(), sh)
+        fe0.record(stream)
+        for i in range(nf):
+            L.ce_forward(bufs[i % n_bufs].data_ptr(), targets.data_ptr(), M, V, code, 0,
+                         loss.data_ptr(), row_loss.data_ptr(), lse.data_ptr(), sh)
+        fe1.record(stream)
+        torch.cuda.synchronize()
+        fwd_ms = fe0.elapsed_time(fe1) / nf
+
+    # end to end: host logits -> device, the call, loss -> host, every step
+    loss_host = torch.empty((), dtype=torch.float32).pin_memory()
+    dbuf = bufs[0]
+    for _ in range(2):
+        dbuf.copy_(host, non_blocking=True)
+        step(dbuf)
+        loss_host.copy_(loss, non_blocking=True)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(3, min(args.steps, 10))
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        dbuf.copy_(host, non_blocking=True)
+        targets.copy_(t_host, non_blocking=True)
+        step(dbuf)
+        loss_host.copy_(loss, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if ws > 1:
+        tt = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    e2e_value = ws * b_step / (e2e_ms * 1e-3) / 1e9
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": w.dtype, "data": "synthetic",
+            "config": {"workload": workload_desc(w), "M": M, "V": V,
+                       "call": "ce_fwd_bwd_inplace (mean)",
+                       "l2": f"inputs larger than L2: a distinct {step_bytes / 2**20:.0f} MiB "
+                             f"logits buffer per step ({n_bufs} resident buffers)",
+                       "parallelism": f"replicas x{ws}"},
+            "pct_of_hbm_roofline": 100.0 * achieved / peak,
+            "ms_per_call": avg_kernel_ms,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_source": peak_kind,
+                         "traffic": traffic,
+                         "bytes_per_launch": b_step},
+            "forward_only": None if fwd_ms is None else {
+                "ms_per_call": fwd_ms,
+                "gb_s": algorithmic_bytes(M, V, es, False) / (fwd_ms * 1e-3) / 1e9},
+            "e2e": {"value": e2e_value, "unit": "GB/s",
+                    "h2d_bytes_per_step": step_bytes + M * 8, "d2h_bytes_per_step": 4,
+                    "ms_per_step": e2e_ms},
+            "gpu_launches": launches,
+            "clocks": clocks,
+        }
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(w, args.cpu_budget_s)
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--workload", default="f32_32768x4096", choices=sorted(synthetic.WORKLOADS))
+    ap.add_argument("--max-resident-gb", type=float, default=64.0)
+    ap.add_argument("--cpu-budget-s", type=float, default=12.0)
+    ap.add_argument("--ref-rows", type=int, default=1024)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps, always
+    w = synthetic.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_native(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

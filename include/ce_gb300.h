@@ -1,0 +1,140 @@
+/*
+ * ce_gb300.h -- C ABI of the GB300 (sm_103a) softmax cross-entropy library.
+ *
+ * What is computed.  For logits x [M, V] (row-major, contiguous, row i at
+ * byte offset i*V*sizeof(dtype)) and integer targets t [M]:
+ *
+ *     m_i      = max_j x_ij
+ *     lse_i    = m_i + log sum_j exp(x_ij - m_i)
+ *     row_i    = lse_i - x_{i,t_i}
+ *     loss     = (1/M) sum_i row_i      (mean)   or   sum_i row_i   (sum)
+ *     g_ij     = (exp(x_ij - lse_i) - [j == t_i]) * scale
+ *
+ * with scale = 1/M for the mean and 1 for sum/none.  Sources: the per-row
+ * definition "max, subtract, exp, sum, log" with mean reduction in the
+ * "POPCORNBENCH level-1 problem 95 transcript" (cross-entropy CUDA kernel);
+ * the loss_kernel output formula (log(sumexp) + max - target logit) in
+ * "Cross Entropy Loss performance issue" (Triton issue #5509); the fused
+ * forward+backward that writes the gradient over the logits buffer in
+ * "9 Triton kernels in 9 weeks", week seven.
+ *
+ * Conventions shared by every entry point:
+ *  - Pointers named logits/targets/loss/row_loss/lse are DEVICE pointers on
+ *    the current CUDA device.  The caller owns all of them; the library
+ *    never frees or keeps them.  `stream` is a cudaStream_t (NULL = legacy
+ *    default stream); every call is asynchronous and stream-ordered.
+ *  - logits must be aligned to the element size, targets to 8 bytes and
+ *    the float outputs to 4 bytes.  Rows need not be 16-byte aligned.
+ *  - Arithmetic is fp32 (16-bit inputs widen exactly); loss, row_loss and
+ *    lse are fp32; gradients are rounded to the logits' dtype
+ *    (round-to-nearest-even, subnormals kept).
+ *  - The mean is deterministic: no floating-point atomics are used; for a
+ *    given device and shape the same inputs give bit-identical outputs.
+ *  - Errors detectable on the host return before anything is launched.  A
+ *    target outside [0, V) does not stop the call: that row's loss is NaN,
+ *    its gradient is softmax*scale (no one-hot term), and a device error
+ *    word is set; ce_check_errors reports it.  Nothing traps.
+ *  - The reducing calls use a small library-owned device buffer (one per
+ *    device and stream, created by cudaMalloc on the first reducing call
+ *    on that stream).  Make that first call outside CUDA graph capture.
+ */
+#ifndef CE_GB300_H
+#define CE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  CE_OK = 0,
+  CE_ERR_INVALID_ARG = 1,  /* bad size, null or misaligned pointer, bad enum */
+  CE_ERR_UNSUPPORTED = 2,  /* V beyond ce_max_vocab(dtype) */
+  CE_ERR_TARGET_RANGE = 3, /* (ce_check_errors) a target was outside [0, V) */
+  CE_ERR_CUDA = 4,         /* a CUDA runtime call or a launch failed */
+  CE_ERR_TIMEOUT = 5       /* (ce_check_errors) a bounded wait ran out */
+} ce_status;
+
+typedef enum { CE_F32 = 0, CE_F16 = 1, CE_BF16 = 2 } ce_dtype;
+
+typedef enum { CE_RED_MEAN = 0, CE_RED_SUM = 1, CE_RED_NONE = 2 } ce_reduction;
+
+/*
+ * ce_forward -- loss forward: one streaming pass over the logits with an
+ * online (max, sum-of-exp) per row, the target-logit gather, and the
+ * reduction.  The online recurrence and its pairwise merge are the ones
+ * the transcript derives ("online softmax algorithm", "This is
+ * associative").
+ *
+ *   logits    [M, V] of `dtype`, read only.
+ *   targets   [M] int64 class indices.
+ *   M >= 0, V >= 1.
+ *   reduction CE_RED_MEAN / CE_RED_SUM write *loss; CE_RED_NONE ignores it.
+ *   loss      [1] fp32 or NULL (then no reduction is computed).
+ *   row_loss  [M] fp32 or NULL.   lse [M] fp32 or NULL.
+ *   M == 0: mean writes NaN, sum writes 0.
+ */
+ce_status ce_forward(const void* logits, const int64_t* targets, int64_t M, int64_t V,
+                     ce_dtype dtype, ce_reduction reduction, float* loss, float* row_loss,
+                     float* lse, void* stream);
+
+/*
+ * ce_fwd_bwd_inplace -- fused forward + backward ("9 Triton kernels in 9
+ * weeks", week seven): computes everything ce_forward does and overwrites
+ * the logits with g = (softmax - onehot) * scale, scale = 1/M (mean) or 1
+ * (sum, none).  Each logit is read from HBM once and written once.
+ *
+ *   logits    [M, V] of `dtype`, read and overwritten with the gradient.
+ *   Other arguments as in ce_forward.  row_loss and lse must not alias
+ *   the logits.
+ */
+ce_status ce_fwd_bwd_inplace(void* logits, const int64_t* targets, int64_t M, int64_t V,
+                             ce_dtype dtype, ce_reduction reduction, float* loss,
+                             float* row_loss, float* lse, void* stream);
+
+/*
+ * ce_backward_from_lse -- gradient only, from a stored per-row lse:
+ * g = (exp(x - lse_i) - onehot) * scale written over the logits.  Use it
+ * when the forward ran earlier (ce_forward with lse != NULL); `scale` is
+ * the upstream gradient of each row loss (1/M for a mean).
+ *
+ *   logits [M, V] read and overwritten; targets [M] int64; lse [M] fp32.
+ */
+ce_status ce_backward_from_lse(void* logits, const int64_t* targets, const float* lse,
+                               int64_t M, int64_t V, ce_dtype dtype, float scale,
+                               void* stream);
+
+/*
+ * ce_check_errors -- wait (at most timeout_ms) for `stream` to drain, then
+ * read and clear the current device's error word.  Returns CE_OK,
+ * CE_ERR_TARGET_RANGE (some target was outside [0, V)), CE_ERR_TIMEOUT (the
+ * stream did not drain in time, or a kernel's bounded wait ran out), or
+ * CE_ERR_CUDA.
+ */
+ce_status ce_check_errors(void* stream, int timeout_ms);
+
+/* Human-readable name of a status. Never NULL. */
+const char* ce_status_string(ce_status status);
+
+/* Largest V the row kernels accept for `dtype` (0 for a bad dtype). */
+int64_t ce_max_vocab(ce_dtype dtype);
+
+/* Number of kernels this library has launched in this process (all devices). */
+uint64_t ce_launch_count(void);
+
+/*
+ * ce_selftest_wait_timeout -- test hook for the bounded-wait machinery:
+ * launches one tiny kernel that waits on a barrier nothing will complete,
+ * gives up after timeout_us microseconds and sets the device error word,
+ * so that a following ce_check_errors returns CE_ERR_TIMEOUT.  It never
+ * hangs the GPU.  1 <= timeout_us <= 1000000.
+ */
+ce_status ce_selftest_wait_timeout(void* stream, int timeout_us);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CE_GB300_H */

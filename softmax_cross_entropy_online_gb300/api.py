@@ -1,0 +1,164 @@
+"""Python binding of the C ABI in include/ce_gb300.h (ctypes).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of libce_gb300.so.  torch supplies device memory and streams.  There
+is no CPU fallback: without the built library every call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+CE_OK = 0
+CE_ERR_INVALID_ARG = 1
+CE_ERR_UNSUPPORTED = 2
+CE_ERR_TARGET_RANGE = 3
+CE_ERR_CUDA = 4
+CE_ERR_TIMEOUT = 5
+
+CE_F32, CE_F16, CE_BF16 = 0, 1, 2
+_DTYPES = {torch.float32: CE_F32, torch.float16: CE_F16, torch.bfloat16: CE_BF16}
+_DTYPE_NAMES = {"f32": CE_F32, "f16": CE_F16, "bf16": CE_BF16}
+_REDUCTIONS = {"mean": 0, "sum": 1, "none": 2}
+
+# (name, restype, argtypes) of every entry point declared in include/ce_gb300.h
+_vp, _i64, _i32, _f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
+SIGNATURES = {
+    "ce_forward": (_i32, [_vp, _vp, _i64, _i64, _i32, _i32, _vp, _vp, _vp, _vp]),
+    "ce_fwd_bwd_inplace": (_i32, [_vp, _vp, _i64, _i64, _i32, _i32, _vp, _vp, _vp, _vp]),
+    "ce_backward_from_lse": (_i32, [_vp, _vp, _vp, _i64, _i64, _i32, _f32, _vp]),
+    "ce_check_errors": (_i32, [_vp, _i32]),
+    "ce_status_string": (ctypes.c_char_p, [_i32]),
+    "ce_max_vocab": (_i64, [_i32]),
+    "ce_launch_count": (ctypes.c_uint64, []),
+    "ce_selftest_wait_timeout": (_i32, [_vp, _i32]),
+}
+
+
+class CEError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)}")
+
+
+_LIB = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libce_gb300.so (built in-tree by build.build()); raise if it is missing."""
+    global _LIB
+    if _LIB is None:
+        path = _build.LIB_PATH
+        if not os.path.exists(path):
+            raise ImportError(
+                f"{path} is missing: run softmax_cross_entropy_online_gb300.build.build() "
+                "(the library has no CPU fallback)")
+        L = ctypes.CDLL(path)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _LIB = L
+    return _LIB
+
+
+def status_string(status: int) -> str:
+    return lib().ce_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str):
+    if status != CE_OK:
+        raise CEError(status, where)
+
+
+def _stream_handle(stream, device) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check_inputs(logits: torch.Tensor, targets: torch.Tensor):
+    if not logits.is_cuda or logits.dim() != 2 or not logits.is_contiguous():
+        raise ValueError("logits must be a contiguous 2-D CUDA tensor [M, V]")
+    if logits.dtype not in _DTYPES:
+        raise ValueError(f"unsupported logits dtype {logits.dtype}")
+    if (not targets.is_cuda or targets.dtype != torch.int64 or targets.dim() != 1
+            or not targets.is_contiguous() or targets.numel() != logits.shape[0]
+            or targets.device != logits.device):
+        raise ValueError("targets must be a contiguous int64 CUDA tensor [M] on the logits' device")
+
+
+def _outputs(logits, reduction, row_loss, lse):
+    M = logits.shape[0]
+    dev = logits.device
+    loss_t = torch.empty((), dtype=torch.float32, device=dev) if reduction != "none" else None
+    rl_t = torch.empty(M, dtype=torch.float32, device=dev) if row_loss else None
+    lse_t = torch.empty(M, dtype=torch.float32, device=dev) if lse else None
+    return loss_t, rl_t, lse_t
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def ce_forward(logits: torch.Tensor, targets: torch.Tensor, reduction: str = "mean", *,
+               row_loss: bool = True, lse: bool = True, stream=None):
+    """Loss forward.  Returns (loss, row_loss, lse); unrequested entries are None."""
+    _check_inputs(logits, targets)
+    loss_t, rl_t, lse_t = _outputs(logits, reduction, row_loss, lse)
+    M, V = logits.shape
+    st = lib().ce_forward(logits.data_ptr(), targets.data_ptr(), M, V, _DTYPES[logits.dtype],
+                          _REDUCTIONS[reduction], _ptr(loss_t), _ptr(rl_t), _ptr(lse_t),
+                          _stream_handle(stream, logits.device))
+    _check(st, "ce_forward")
+    return loss_t, rl_t, lse_t
+
+
+def ce_fwd_bwd_inplace(logits: torch.Tensor, targets: torch.Tensor, reduction: str = "mean", *,
+                       row_loss: bool = True, lse: bool = True, stream=None):
+    """Fused forward + backward; `logits` is overwritten with the gradient."""
+    _check_inputs(logits, targets)
+    loss_t, rl_t, lse_t = _outputs(logits, reduction, row_loss, lse)
+    M, V = logits.shape
+    st = lib().ce_fwd_bwd_inplace(logits.data_ptr(), targets.data_ptr(), M, V,
+                                  _DTYPES[logits.dtype], _REDUCTIONS[reduction], _ptr(loss_t),
+                                  _ptr(rl_t), _ptr(lse_t), _stream_handle(stream, logits.device))
+    _check(st, "ce_fwd_bwd_inplace")
+    return loss_t, rl_t, lse_t
+
+
+def ce_backward_from_lse(logits: torch.Tensor, targets: torch.Tensor, lse: torch.Tensor,
+                         scale: float, *, stream=None):
+    """Gradient from a stored lse, written over `logits`."""
+    _check_inputs(logits, targets)
+    if (not lse.is_cuda or lse.dtype != torch.float32 or not lse.is_contiguous()
+            or lse.numel() != logits.shape[0]):
+        raise ValueError("lse must be a contiguous fp32 CUDA tensor [M]")
+    M, V = logits.shape
+    st = lib().ce_backward_from_lse(logits.data_ptr(), targets.data_ptr(), lse.data_ptr(), M, V,
+                                    _DTYPES[logits.dtype], float(scale),
+                                    _stream_handle(stream, logits.device))
+    _check(st, "ce_backward_from_lse")
+
+
+def ce_check_errors(stream=None, timeout_ms: int = 10000, device=None) -> int:
+    """Wait (bounded) for the stream and return the device error status (0 = CE_OK)."""
+    return lib().ce_check_errors(_stream_handle(stream, device), int(timeout_ms))
+
+
+def ce_max_vocab(dtype) -> int:
+    code = _DTYPES[dtype] if isinstance(dtype, torch.dtype) else _DTYPE_NAMES[dtype]
+    return int(lib().ce_max_vocab(code))
+
+
+def ce_launch_count() -> int:
+    return int(lib().ce_launch_count())
+
+
+def ce_selftest_wait_timeout(timeout_us: int, stream=None, device=None) -> int:
+    return lib().ce_selftest_wait_timeout(_stream_handle(stream, device), int(timeout_us))

@@ -1,0 +1,380 @@
+// ce_api.cu -- the C ABI (include/ce_gb300.h): argument checks, the choice
+// of launch shape for each (dtype, V, M), the per-stream reduction scratch,
+// the device error word, and the launches.  Every computation happens in the
+// kernels of ce_rows.cuh; this file only validates, plans and launches.
+#include <atomic>
+#include <chrono>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <thread>
+#include <utility>
+
+#include "../../include/ce_gb300.h"
+#include "ce_rows.cuh"
+
+namespace ce {
+template <typename T>
+cudaError_t rows_launch(int mode, int NC, const RowParams& p, int grid, int smem_bytes,
+                        cudaStream_t stream);
+template <typename T>
+cudaError_t rows_max_active(int mode, int NC, int smem_bytes, int CL, int sm_count, int* out);
+}  // namespace ce
+
+namespace ce {
+// Test hook: wait on a barrier that nothing completes; give up after limit_ns.
+__global__ void ce_selftest_wait_kernel(unsigned int* err, unsigned long long limit_ns) {
+  __shared__ __align__(8) unsigned long long bar;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    bool failed = false;
+    mbar_wait<false>(smem_u32(&bar), 0u, err, failed, limit_ns);
+    mbar_arrive(smem_u32(&bar));  // leave the barrier in a completed phase
+  }
+}
+
+}  // namespace ce
+
+// The device error word: bit 0 = a target outside [0, V), bit 1 = a bounded
+// wait ran out.  One per device (each device's module has its own copy).
+__device__ unsigned int g_ce_err_word;
+
+namespace {
+
+std::atomic<uint64_t> g_launches{0};
+
+constexpr int kSmemBudget = 200 * 1024;  // dynamic shared memory per CTA for the stages
+constexpr int kScratchPartials = 8192;   // > any persistent grid (152 SMs x 2 CTAs)
+
+struct DeviceInfo {
+  int sm_count = 0;
+  unsigned int* err = nullptr;
+};
+
+std::mutex g_mu;
+std::map<int, DeviceInfo> g_dev;
+struct Scratch {
+  double* partials = nullptr;
+  unsigned int* ticket = nullptr;
+};
+std::map<std::pair<int, void*>, Scratch> g_scratch;
+
+ce_status device_info(DeviceInfo& out, int* dev_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return CE_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  auto it = g_dev.find(dev);
+  if (it == g_dev.end()) {
+    DeviceInfo d;
+    if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return CE_ERR_CUDA;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_ce_err_word) != cudaSuccess) return CE_ERR_CUDA;
+    d.err = static_cast<unsigned int*>(p);
+    it = g_dev.emplace(dev, d).first;
+  }
+  out = it->second;
+  *dev_out = dev;
+  return CE_OK;
+}
+
+// Reduction scratch for (device, stream): calls on one stream are ordered, so
+// they can share it; different streams get their own.
+ce_status scratch_for(int dev, void* stream, Scratch& out) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  auto key = std::make_pair(dev, stream);
+  auto it = g_scratch.find(key);
+  if (it == g_scratch.end()) {
+    void* mem = nullptr;
+    const size_t bytes = 256 + sizeof(double) * kScratchPartials;
+    if (cudaMalloc(&mem, bytes) != cudaSuccess) return CE_ERR_CUDA;
+    if (cudaMemset(mem, 0, 256) != cudaSuccess) return CE_ERR_CUDA;
+    Scratch s;
+    s.ticket = static_cast<unsigned int*>(mem);
+    s.partials = reinterpret_cast<double*>(static_cast<char*>(mem) + 256);
+    it = g_scratch.emplace(key, s).first;
+  }
+  out = it->second;
+  return CE_OK;
+}
+
+int elem_size(ce_dtype d) {
+  switch (d) {
+    case CE_F32: return 4;
+    case CE_F16: return 2;
+    case CE_BF16: return 2;
+    default: return 0;
+  }
+}
+
+struct Plan {
+  int NC = 0, R = 1, CL = 1, S = 0, stage_bytes = 0;
+};
+
+// Upper bound of the 16-byte chunks one row (or R rows) can straddle.
+long long chunks_for(long long bytes, bool aligned) {
+  return aligned ? (bytes + 15) / 16 : (bytes + 15) / 16 + 1;
+}
+
+// Launch shape for rows of `rb` bytes.  A CTA holds NC*CPT = 2048 chunks
+// (32 KB) of a unit in registers.  Rows up to that size live in one CTA (R rows
+// per unit, a group of NC/R consumer threads per row); longer rows are split
+// over a cluster of CL = 2..8 CTAs.
+bool choose_plan(long long rb, bool aligned, long long M, int sm_count, int NC, Plan& pl) {
+  const int CPT = ce::cpt_for(NC);
+  const long long cap = static_cast<long long>(NC) * CPT;
+  const long long cpr = chunks_for(rb, aligned);
+  if (cpr <= cap) {
+    // the smallest power-of-two group (>= one warp) that covers a row
+    int GT = 32;
+    while (static_cast<long long>(GT) * CPT < cpr) GT *= 2;
+    int R = NC / GT;
+    // small problems: more units (CTAs) before more rows per unit
+    while (R > 1 && (M + R - 1) / R < sm_count) R /= 2;
+    for (; R >= 1; R /= 2) {
+      const long long stage = chunks_for(static_cast<long long>(R) * rb, aligned) * 16;
+      const int S = static_cast<int>(kSmemBudget / stage);
+      if (S >= 3 || (R == 1 && S >= 2)) {
+        pl.NC = NC;
+        pl.R = R;
+        pl.CL = 1;
+        pl.S = S > ce::kMaxStages ? ce::kMaxStages : S;
+        pl.stage_bytes = static_cast<int>(stage);
+        return true;
+      }
+    }
+  }
+  for (int CL = 2; CL <= ce::kMaxCluster; ++CL) {
+    const long long per_cta = (cpr + CL - 1) / CL;
+    if (per_cta > cap) continue;
+    const long long stage = per_cta * 16;
+    const int S = static_cast<int>(kSmemBudget / stage);
+    if (S < 2) continue;
+    pl.NC = NC;
+    pl.R = 1;
+    pl.CL = CL;
+    pl.S = S > ce::kMaxStages ? ce::kMaxStages : S;
+    pl.stage_bytes = static_cast<int>(stage);
+    return true;
+  }
+  return false;
+}
+
+// Optional override for tuning sweeps: CE_PLAN="NC,R,CL,S".  It is checked
+// against the same limits as the automatic choice and ignored when it does
+// not fit them.
+void apply_env_plan(long long rb, bool aligned, Plan& pl) {
+  const char* env = std::getenv("CE_PLAN");
+  if (env == nullptr || *env == 0) return;
+  int NC = 0, R = 0, CL = 0, S = 0;
+  if (std::sscanf(env, "%d,%d,%d,%d", &NC, &R, &CL, &S) != 4) return;
+  const int CPT = ce::cpt_for(NC);
+  if (CPT == 0) return;
+  if (R < 1 || NC % R != 0 || (NC / R) % 32 != 0) return;
+  if (CL < 1 || CL > ce::kMaxCluster) return;
+  if (CL > 1 && R != 1) return;
+  const long long cpr = chunks_for(rb, aligned);
+  const long long GT = NC / R;
+  long long stage = 0;
+  if (CL == 1) {
+    if (GT * CPT < cpr) return;
+    stage = chunks_for(static_cast<long long>(R) * rb, aligned) * 16;
+  } else {
+    const long long per_cta = (cpr + CL - 1) / CL;
+    if (per_cta > static_cast<long long>(NC) * CPT) return;
+    stage = per_cta * 16;
+  }
+  if (S < 1 || S > ce::kMaxStages || stage * S > 220 * 1024) return;
+  pl.NC = NC;
+  pl.R = R;
+  pl.CL = CL;
+  pl.S = S;
+  pl.stage_bytes = static_cast<int>(stage);
+}
+
+ce_status launch_rows(int mode, const void* logits, const int64_t* targets, const float* lse_in,
+                      int64_t M, int64_t V, ce_dtype dtype, ce_reduction red, float* loss,
+                      float* row_loss, float* lse_out, float grad_scale, void* stream) {
+  const int es = elem_size(dtype);
+  if (es == 0) return CE_ERR_INVALID_ARG;
+  if (red != CE_RED_MEAN && red != CE_RED_SUM && red != CE_RED_NONE) return CE_ERR_INVALID_ARG;
+  if (M < 0 || V < 1) return CE_ERR_INVALID_ARG;
+  if (M > 0 && (logits == nullptr || targets == nullptr)) return CE_ERR_INVALID_ARG;
+  if (mode == ce::BWD && M > 0 && lse_in == nullptr) return CE_ERR_INVALID_ARG;
+  const uintptr_t lb = reinterpret_cast<uintptr_t>(logits);
+  if (lb % es) return CE_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(targets) % 8) return CE_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(loss) % 4 || reinterpret_cast<uintptr_t>(row_loss) % 4 ||
+      reinterpret_cast<uintptr_t>(lse_out) % 4 || reinterpret_cast<uintptr_t>(lse_in) % 4)
+    return CE_ERR_INVALID_ARG;
+  if (V > (INT64_MAX / 4) / es) return CE_ERR_INVALID_ARG;
+  const long long rb = static_cast<long long>(V) * es;
+  if (M > 0 && M > INT64_MAX / rb) return CE_ERR_INVALID_ARG;
+  if (red == CE_RED_NONE) loss = nullptr;
+  if (mode == ce::BWD) loss = nullptr;
+  if (M == 0 && loss == nullptr) return CE_OK;
+
+  DeviceInfo di;
+  int dev = 0;
+  ce_status st = device_info(di, &dev);
+  if (st != CE_OK) return st;
+
+  const bool aligned = (lb % 16 == 0) && (rb % 16 == 0);
+  Plan pl;
+  if (!choose_plan(rb, aligned, M, di.sm_count, 256, pl)) return CE_ERR_UNSUPPORTED;
+  apply_env_plan(rb, aligned, pl);
+
+  ce::RowParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.base = static_cast<char*>(const_cast<void*>(logits));
+  p.targets = targets;
+  p.lse_in = lse_in;
+  p.row_loss = row_loss;
+  p.lse_out = lse_out;
+  p.loss = loss;
+  p.err = di.err;
+  p.M = M;
+  p.V = V;
+  p.row_bytes = rb;
+  p.R = pl.R;
+  p.CL = pl.CL;
+  p.S = pl.S;
+  p.stage_bytes = pl.stage_bytes;
+  p.n_units = (M + pl.R - 1) / pl.R;
+  p.grad_scale = grad_scale;
+  p.mean = (red == CE_RED_MEAN) ? 1 : 0;
+
+  const int smem = pl.S * pl.stage_bytes;
+  int max_active = 0;
+  cudaError_t ce_err = cudaSuccess;
+  switch (dtype) {
+    case CE_F32: ce_err = ce::rows_max_active<float>(mode, pl.NC, smem, pl.CL, di.sm_count, &max_active); break;
+    case CE_F16: ce_err = ce::rows_max_active<__half>(mode, pl.NC, smem, pl.CL, di.sm_count, &max_active); break;
+    default: ce_err = ce::rows_max_active<__nv_bfloat16>(mode, pl.NC, smem, pl.CL, di.sm_count, &max_active); break;
+  }
+  if (ce_err != cudaSuccess || max_active < 1) return CE_ERR_CUDA;
+  long long nclusters = p.n_units < max_active ? p.n_units : max_active;
+  if (nclusters < 1) nclusters = 1;  // M == 0: one cluster writes the empty reduction
+  const int grid = static_cast<int>(nclusters * pl.CL);
+
+  if (loss != nullptr) {
+    if (grid > kScratchPartials) return CE_ERR_UNSUPPORTED;
+    Scratch sc;
+    st = scratch_for(dev, stream, sc);
+    if (st != CE_OK) return st;
+    p.partials = sc.partials;
+    p.ticket = sc.ticket;
+  }
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  switch (dtype) {
+    case CE_F32: ce_err = ce::rows_launch<float>(mode, pl.NC, p, grid, smem, s); break;
+    case CE_F16: ce_err = ce::rows_launch<__half>(mode, pl.NC, p, grid, smem, s); break;
+    default: ce_err = ce::rows_launch<__nv_bfloat16>(mode, pl.NC, p, grid, smem, s); break;
+  }
+  if (ce_err != cudaSuccess) return CE_ERR_CUDA;
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return CE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+ce_status ce_forward(const void* logits, const int64_t* targets, int64_t M, int64_t V,
+                     ce_dtype dtype, ce_reduction reduction, float* loss, float* row_loss,
+                     float* lse, void* stream) {
+  return launch_rows(ce::FWD, logits, targets, nullptr, M, V, dtype, reduction, loss, row_loss,
+                     lse, 1.0f, stream);
+}
+
+ce_status ce_fwd_bwd_inplace(void* logits, const int64_t* targets, int64_t M, int64_t V,
+                             ce_dtype dtype, ce_reduction reduction, float* loss,
+                             float* row_loss, float* lse, void* stream) {
+  const float scale = (reduction == CE_RED_MEAN && M > 0) ? 1.0f / static_cast<float>(M) : 1.0f;
+  return launch_rows(ce::FWD_BWD, logits, targets, nullptr, M, V, dtype, reduction, loss,
+                     row_loss, lse, scale, stream);
+}
+
+ce_status ce_backward_from_lse(void* logits, const int64_t* targets, const float* lse, int64_t M,
+                               int64_t V, ce_dtype dtype, float scale, void* stream) {
+  return launch_rows(ce::BWD, logits, targets, lse, M, V, dtype, CE_RED_NONE, nullptr, nullptr,
+                     nullptr, scale, stream);
+}
+
+ce_status ce_check_errors(void* stream, int timeout_ms) {
+  DeviceInfo di;
+  int dev = 0;
+  ce_status st = device_info(di, &dev);
+  if (st != CE_OK) return st;
+  static std::mutex mu;
+  static std::map<int, unsigned int*> host_words;
+  std::lock_guard<std::mutex> lk(mu);
+  unsigned int*& hw = host_words[dev];
+  if (hw == nullptr) {
+    if (cudaHostAlloc(reinterpret_cast<void**>(&hw), sizeof(unsigned int), cudaHostAllocDefault) !=
+        cudaSuccess)
+      return CE_ERR_CUDA;
+  }
+  *hw = 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(hw, di.err, sizeof(unsigned int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return CE_ERR_CUDA;
+  const auto t0 = std::chrono::steady_clock::now();
+  for (;;) {
+    cudaError_t q = cudaStreamQuery(s);
+    if (q == cudaSuccess) break;
+    if (q != cudaErrorNotReady) return CE_ERR_CUDA;
+    if (std::chrono::steady_clock::now() - t0 > std::chrono::milliseconds(timeout_ms))
+      return CE_ERR_TIMEOUT;
+    std::this_thread::sleep_for(std::chrono::microseconds(50));
+  }
+  const unsigned int w = *hw;
+  if (w != 0) {
+    if (cudaMemsetAsync(di.err, 0, sizeof(unsigned int), s) != cudaSuccess) return CE_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return CE_ERR_CUDA;
+  }
+  if (w & ce::ERR_WAIT_TIMEOUT) return CE_ERR_TIMEOUT;
+  if (w & ce::ERR_TARGET_RANGE) return CE_ERR_TARGET_RANGE;
+  return CE_OK;
+}
+
+const char* ce_status_string(ce_status status) {
+  switch (status) {
+    case CE_OK: return "CE_OK";
+    case CE_ERR_INVALID_ARG: return "CE_ERR_INVALID_ARG";
+    case CE_ERR_UNSUPPORTED: return "CE_ERR_UNSUPPORTED";
+    case CE_ERR_TARGET_RANGE: return "CE_ERR_TARGET_RANGE";
+    case CE_ERR_CUDA: return "CE_ERR_CUDA";
+    case CE_ERR_TIMEOUT: return "CE_ERR_TIMEOUT";
+    default: return "CE_ERR_UNKNOWN";
+  }
+}
+
+int64_t ce_max_vocab(ce_dtype dtype) {
+  const int es = elem_size(dtype);
+  if (es == 0) return 0;
+  // 8 CTAs x 2048 register-resident chunks; a misaligned row straddles one more
+  const long long chunks = static_cast<long long>(ce::kMaxCluster) * 2048;
+  return (chunks - 2) * 16 / es;
+}
+
+uint64_t ce_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+ce_status ce_selftest_wait_timeout(void* stream, int timeout_us) {
+  if (timeout_us < 1 || timeout_us > 1000000) return CE_ERR_INVALID_ARG;
+  DeviceInfo di;
+  int dev = 0;
+  ce_status st = device_info(di, &dev);
+  if (st != CE_OK) return st;
+  ce::ce_selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      di.err, static_cast<unsigned long long>(timeout_us) * 1000ull);
+  if (cudaGetLastError() != cudaSuccess) return CE_ERR_CUDA;
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return CE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,99 @@
+// ce_launch.cuh -- launch helpers for the row kernels, instantiated once per
+// element type in ce_rows_f32.cu / ce_rows_f16.cu / ce_rows_bf16.cu so the
+// three translation units compile in parallel.
+#pragma once
+
+#include "ce_rows.cuh"
+
+namespace ce {
+
+// Instantiated shapes: NC consumer threads x CPT register-resident 16-byte
+// chunks per thread.  Both hold 2048 chunks (32 KB) of a row slice per CTA.
+//   NC = 256, CPT = 8: 9 warps, fewer threads with more elements each
+//   NC = 512, CPT = 4: 17 warps, more threads with fewer elements each
+
+template <typename T, int MODE, int NC, int CPT>
+static const void* kptr() {
+  return reinterpret_cast<const void*>(&ce_rows_kernel<T, MODE, NC, CPT>);
+}
+
+template <typename T, int NC, int CPT>
+static const void* kptr_mode(int mode) {
+  switch (mode) {
+    case FWD: return kptr<T, FWD, NC, CPT>();
+    case FWD_BWD: return kptr<T, FWD_BWD, NC, CPT>();
+    case BWD: return kptr<T, BWD, NC, CPT>();
+    default: return nullptr;
+  }
+}
+
+// Kernel entry for (T, mode, NC); NC is the number of consumer threads.
+template <typename T>
+const void* rows_kernel_ptr(int mode, int NC) {
+  if (NC == 256) return kptr_mode<T, 256, 8>(mode);
+  if (NC == 512) return kptr_mode<T, 512, 4>(mode);
+  return nullptr;
+}
+
+template <typename T>
+cudaError_t rows_launch(int mode, int NC, const RowParams& p, int grid, int smem_bytes,
+                        cudaStream_t stream) {
+  const void* fn = rows_kernel_ptr<T>(mode, NC);
+  if (fn == nullptr) return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(NC + 32), 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem_bytes);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  if (p.CL > 1) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(p.CL);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  void* args[] = {const_cast<RowParams*>(&p)};
+  return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+// How many clusters (CTAs when CL == 1) of this kernel fit on the device at once.
+template <typename T>
+cudaError_t rows_max_active(int mode, int NC, int smem_bytes, int CL, int sm_count, int* out) {
+  const void* fn = rows_kernel_ptr<T>(mode, NC);
+  if (fn == nullptr) return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+  if (e != cudaSuccess) return e;
+  if (CL <= 1) {
+    int occ = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, NC + 32,
+                                                      static_cast<size_t>(smem_bytes));
+    *out = occ * sm_count;
+    return e;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(CL), 1, 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(NC + 32), 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem_bytes);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(CL);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int ncl = 0;
+  e = cudaOccupancyMaxActiveClusters(&ncl, fn, &cfg);
+  *out = ncl;
+  return e;
+}
+
+#define CE_INSTANTIATE_ROWS(T)                                                                  \
+  template const void* rows_kernel_ptr<T>(int, int);                                            \
+  template cudaError_t rows_launch<T>(int, int, const RowParams&, int, int, cudaStream_t);      \
+  template cudaError_t rows_max_active<T>(int, int, int, int, int, int*);
+
+}  // namespace ce

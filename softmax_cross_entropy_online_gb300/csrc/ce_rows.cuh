@@ -1,0 +1,699 @@
+// ce_rows.cuh -- the row kernels of the softmax cross-entropy library (sm_103a).
+//
+// One kernel template covers the three row operations:
+//   FWD      per-row lse and loss, deterministic mean        (ce_forward)
+//   FWD_BWD  the same, then g = (softmax - onehot)*scale
+//            written over the logits from the on-chip copy    (ce_fwd_bwd_inplace)
+//   BWD      g from a stored lse, written over the logits      (ce_backward_from_lse)
+//
+// Definitions followed: the per-row "max, subtract, exp, sum, log" of the
+// "POPCORNBENCH level-1 problem 95 transcript", its online (max, sum) pair
+// and the associative merge of two pairs ("This is associative"); the row
+// output log(sumexp) + max - x_target of the loss_kernel in "Cross Entropy
+// Loss performance issue"; the fused in-place backward of "9 Triton kernels
+// in 9 weeks" (week seven).  exp is evaluated as exp2(x * log2 e), the
+// identity the flash-attention discussion on the Triton forum uses.
+//
+// Design (GB300-first, not a port of the pages' kernels):
+//  * Persistent grid.  A "unit" is R consecutive rows (small V) or one row
+//    split over a thread-block cluster of CL CTAs (large V).  Cluster c
+//    processes units c, c + nclusters, ...; CTA `rank` of the cluster owns
+//    the rank-th slice of every unit.
+//  * Warp specialisation.  The last warp is the producer: it streams units
+//    into an S-deep ring of shared-memory stages with 1-D TMA bulk copies
+//    (cp.async.bulk, completion on an mbarrier), and writes gradients back
+//    with bulk stores from the same stage.  The NC consumer threads compute.
+//  * Rows need not be 16-byte aligned (odd V in 16-bit types).  A unit's
+//    bytes [as, ae) are cut into 16-byte "chunks" aligned to absolute
+//    addresses: chunk c covers [A0 - 16 + 16c, A0 + 16c) with A0 =
+//    ceil16(as).  Interior chunks 1..nI move by TMA; the partial head chunk
+//    (0) and tail chunk (nI + 1) are read and written element by element by
+//    the consumer thread that owns them.  No byte outside the unit is ever
+//    touched, so neighbouring units never race.
+//  * Each consumer thread keeps its elements in registers: it takes its own
+//    max m_t first, so every element costs one exp2 (not two), keeps
+//    e = exp(x - m_t), and after the row's lse is known writes
+//    g = e * exp(m_t - lse) * scale.  Thread pairs (m_t, s_t) merge by warp
+//    shuffles, then across the row's warps through shared memory, then
+//    across the cluster through distributed shared memory (each CTA stores
+//    its pair into every peer's slot and arrives on the peer's mbarrier).
+//  * Mean: each CTA sums its rows' losses in row order (fp64); the last CTA
+//    to finish (integer ticket) adds the per-CTA partials in index order.
+//    No floating-point atomics, bit-reproducible for a given grid.
+//  * Every wait is bounded (mbarrier try_wait against %globaltimer).  On
+//    timeout the thread records an error bit and carries on without
+//    waiting again, so every launch ends and no barrier is left unmatched.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace ce {
+
+constexpr unsigned ERR_TARGET_RANGE = 1u;
+constexpr unsigned ERR_WAIT_TIMEOUT = 2u;
+constexpr unsigned long long WAIT_LIMIT_NS = 4000000000ull;  // 4 s per wait
+constexpr float kLog2e = 1.4426950408889634f;
+
+enum Mode : int { FWD = 0, FWD_BWD = 1, BWD = 2 };
+
+constexpr int kMaxStages = 16;
+constexpr int kMaxCluster = 8;
+
+// Chunks (16 B) each consumer thread keeps in registers, for the two
+// instantiated consumer sizes: both hold 2048 chunks (32 KB) per CTA.
+inline int cpt_for(int NC) { return NC == 256 ? 8 : (NC == 512 ? 4 : 0); }
+
+struct RowParams {
+  char* base;                 // logits (byte address)
+  const int64_t* targets;     // [M]
+  const float* lse_in;        // [M], BWD only
+  float* row_loss;            // [M] or null
+  float* lse_out;             // [M] or null
+  float* loss;                // [1] or null
+  double* partials;           // [gridDim.x] scratch when loss != null
+  unsigned int* ticket;       // scratch counter when loss != null
+  unsigned int* err;          // device error word
+  long long M, V;
+  long long row_bytes;        // V * sizeof(T)
+  long long n_units;          // ceil(M / R)
+  int R;                      // rows per unit (1 in cluster mode)
+  int CL;                     // CTAs per cluster
+  int S;                      // pipeline stages
+  int stage_bytes;            // bytes of one stage (multiple of 16)
+  float grad_scale;           // FWD_BWD / BWD
+  int mean;                   // 1: loss = sum / M, 0: loss = sum
+};
+
+// ---------------------------------------------------------------------------
+// PTX helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ unsigned long long global_timer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t tx) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+               "r"(tx)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(
+                   bar_cluster_addr)
+               : "memory");
+}
+template <bool kClusterScope>
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  if (kClusterScope) {
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+  }
+  return ok != 0;
+}
+// Bounded wait.  After this thread has once timed out (`failed`), later waits
+// only poll once, so a launch that lost a barrier still ends promptly.
+template <bool kClusterScope>
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned int* err,
+                                          bool& failed, unsigned long long limit_ns) {
+  if (mbar_try_wait<kClusterScope>(bar, parity)) return true;
+  if (failed) return false;
+  const unsigned long long t0 = global_timer_ns();
+  while (!mbar_try_wait<kClusterScope>(bar, parity)) {
+    if (global_timer_ns() - t0 > limit_ns) {
+      atomicOr(err, ERR_WAIT_TIMEOUT);
+      failed = true;
+      return false;
+    }
+  }
+  return true;
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void fence_mbar_init_cluster() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_load(uint32_t dst_smem, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst_smem),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_store(void* dst, uint32_t src_smem, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+               "r"(src_smem), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+__device__ __forceinline__ void consumer_sync(int nthreads) {
+  asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t smem_addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void st_cluster_f4(uint32_t addr, float a, float b, float c, float d) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b),
+               "f"(c), "f"(d)
+               : "memory");
+}
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float lg2(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Element formats: 16 bytes = EPC elements; widen to fp32, narrow with RN.
+// ---------------------------------------------------------------------------
+template <typename T>
+struct Elem;
+
+template <>
+struct Elem<float> {
+  static constexpr int EPC = 4;
+  static constexpr int ES = 4;
+  __device__ static __forceinline__ void unpack(uint4 q, float* v) {
+    v[0] = __uint_as_float(q.x);
+    v[1] = __uint_as_float(q.y);
+    v[2] = __uint_as_float(q.z);
+    v[3] = __uint_as_float(q.w);
+  }
+  __device__ static __forceinline__ uint4 pack(const float* g) {
+    return make_uint4(__float_as_uint(g[0]), __float_as_uint(g[1]), __float_as_uint(g[2]),
+                      __float_as_uint(g[3]));
+  }
+  __device__ static __forceinline__ float ld(const void* p) {
+    return *static_cast<const volatile float*>(p);
+  }
+  __device__ static __forceinline__ void st(void* p, float g) { *static_cast<float*>(p) = g; }
+};
+
+template <>
+struct Elem<__half> {
+  static constexpr int EPC = 8;
+  static constexpr int ES = 2;
+  __device__ static __forceinline__ float2 w2(uint32_t u) {
+    __half2 h = *reinterpret_cast<__half2*>(&u);
+    return __half22float2(h);
+  }
+  __device__ static __forceinline__ uint32_t n2(float a, float b) {
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+  __device__ static __forceinline__ void unpack(uint4 q, float* v) {
+    float2 a = w2(q.x), b = w2(q.y), c = w2(q.z), d = w2(q.w);
+    v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
+    v[4] = c.x; v[5] = c.y; v[6] = d.x; v[7] = d.y;
+  }
+  __device__ static __forceinline__ uint4 pack(const float* g) {
+    return make_uint4(n2(g[0], g[1]), n2(g[2], g[3]), n2(g[4], g[5]), n2(g[6], g[7]));
+  }
+  __device__ static __forceinline__ float ld(const void* p) {
+    unsigned short u = *static_cast<const volatile unsigned short*>(p);
+    return __half2float(__ushort_as_half(u));
+  }
+  __device__ static __forceinline__ void st(void* p, float g) {
+    *static_cast<unsigned short*>(p) = __half_as_ushort(__float2half_rn(g));
+  }
+};
+
+template <>
+struct Elem<__nv_bfloat16> {
+  static constexpr int EPC = 8;
+  static constexpr int ES = 2;
+  __device__ static __forceinline__ uint32_t n2(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+  __device__ static __forceinline__ void unpack(uint4 q, float* v) {
+    // bf16 is the upper half of an fp32: widening is a shift
+    v[0] = __uint_as_float(q.x << 16); v[1] = __uint_as_float(q.x & 0xffff0000u);
+    v[2] = __uint_as_float(q.y << 16); v[3] = __uint_as_float(q.y & 0xffff0000u);
+    v[4] = __uint_as_float(q.z << 16); v[5] = __uint_as_float(q.z & 0xffff0000u);
+    v[6] = __uint_as_float(q.w << 16); v[7] = __uint_as_float(q.w & 0xffff0000u);
+  }
+  __device__ static __forceinline__ uint4 pack(const float* g) {
+    return make_uint4(n2(g[0], g[1]), n2(g[2], g[3]), n2(g[4], g[5]), n2(g[6], g[7]));
+  }
+  __device__ static __forceinline__ float ld(const void* p) {
+    unsigned short u = *static_cast<const volatile unsigned short*>(p);
+    return __uint_as_float(static_cast<uint32_t>(u) << 16);
+  }
+  __device__ static __forceinline__ void st(void* p, float g) {
+    *static_cast<unsigned short*>(p) = __bfloat16_as_ushort(__float2bfloat16_rn(g));
+  }
+};
+
+// ---------------------------------------------------------------------------
+// Unit geometry (identical on producer and consumers)
+// ---------------------------------------------------------------------------
+struct UnitGeo {
+  long long row0;   // first row of the unit
+  int rows;         // rows in the unit
+  long long as;     // absolute address of the unit's first byte
+  long long A0;     // ceil16(as): start of interior chunk 1
+  int nI;           // interior chunks (1..nI)
+  int w0, w1;       // this CTA's chunk window [w0, w1)
+};
+
+__device__ __forceinline__ UnitGeo unit_geo(const RowParams& p, long long u, int rank) {
+  UnitGeo g;
+  g.row0 = u * p.R;
+  long long rows = p.M - g.row0;
+  g.rows = static_cast<int>(rows < p.R ? rows : p.R);
+  g.as = reinterpret_cast<long long>(p.base) + g.row0 * p.row_bytes;
+  const long long ae = g.as + static_cast<long long>(g.rows) * p.row_bytes;
+  g.A0 = (g.as + 15) & ~15LL;
+  long long A1 = ae & ~15LL;
+  if (A1 < g.A0) A1 = g.A0;
+  g.nI = static_cast<int>((A1 - g.A0) >> 4);
+  const int c_first = (g.as < g.A0) ? 0 : 1;
+  const int c_last = (ae > A1) ? g.nI + 1 : g.nI;
+  const int nC = c_last - c_first + 1;
+  const int Q = (nC + p.CL - 1) / p.CL;
+  g.w0 = c_first + rank * Q;
+  int w1 = g.w0 + Q;
+  g.w1 = w1 < c_last + 1 ? w1 : c_last + 1;
+  if (g.w1 < g.w0) g.w1 = g.w0;
+  return g;
+}
+
+// interior chunk range [lo, hi) of this CTA's window, moved by TMA
+__device__ __forceinline__ void bulk_range(const UnitGeo& g, int& lo, int& hi) {
+  lo = g.w0 > 1 ? g.w0 : 1;
+  hi = g.w1 < g.nI + 1 ? g.w1 : g.nI + 1;
+}
+
+// ---------------------------------------------------------------------------
+// The kernel
+// ---------------------------------------------------------------------------
+template <typename T, int MODE, int NC, int CPT>
+__global__ void __launch_bounds__(NC + 32, 1) ce_rows_kernel(const RowParams p) {
+  using E = Elem<T>;
+  constexpr int EPC = E::EPC;
+  constexpr int ES = E::ES;
+  constexpr int NW = NC / 32;
+
+  extern __shared__ __align__(128) unsigned char stage_mem[];
+  __shared__ __align__(8) unsigned long long full_bar[kMaxStages];
+  __shared__ __align__(8) unsigned long long done_bar[kMaxStages];
+  __shared__ __align__(8) unsigned long long xbar[2];
+  __shared__ __align__(16) float4 xslot[2][kMaxCluster];
+  __shared__ float2 red[2][NW];
+  __shared__ float xt_slot[2][NW];
+  __shared__ double acc_slot[NW];
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int CL = p.CL;
+  const int rank = static_cast<int>(blockIdx.x) % CL;
+  const long long cid = blockIdx.x / CL;
+  const long long ncl = gridDim.x / CL;
+  const long long n_iter = (cid < p.n_units) ? (p.n_units - 1 - cid) / ncl + 1 : 0;
+  const int S = p.S;
+  const uint32_t stage0 = smem_u32(stage_mem);
+  bool failed = false;
+
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(smem_u32(&full_bar[s]), 1);
+      mbar_init(smem_u32(&done_bar[s]), NC);
+    }
+    mbar_init(smem_u32(&xbar[0]), CL);
+    mbar_init(smem_u32(&xbar[1]), CL);
+    fence_mbar_init_cluster();
+  }
+  __syncthreads();
+  if (CL > 1) cluster_sync_all();  // peers' barriers exist before any remote arrive
+
+  if (warp == NW) {
+    // ======================= producer warp =======================
+    if (lane == 0) {
+      for (long long i = 0; i < n_iter; ++i) {
+        const int s = static_cast<int>(i % S);
+        if (i >= S) {
+          const uint32_t par = static_cast<uint32_t>(((i / S) - 1) & 1);
+          mbar_wait<false>(smem_u32(&done_bar[s]), par, p.err, failed, WAIT_LIMIT_NS);
+          if (MODE != FWD) {
+            const UnitGeo go = unit_geo(p, cid + (i - S) * ncl, rank);
+            int lo, hi;
+            bulk_range(go, lo, hi);
+            if (hi > lo) {
+              bulk_store(reinterpret_cast<void*>(go.A0 - 16 + 16LL * lo),
+                         stage0 + s * p.stage_bytes + (lo - go.w0) * 16, (hi - lo) * 16);
+              bulk_commit();
+              bulk_wait_read_all();
+            }
+          }
+        }
+        fence_proxy_async_smem();
+        const UnitGeo g = unit_geo(p, cid + i * ncl, rank);
+        int lo, hi;
+        bulk_range(g, lo, hi);
+        const uint32_t fb = smem_u32(&full_bar[s]);
+        if (hi > lo) {
+          mbar_arrive_expect_tx(fb, static_cast<uint32_t>((hi - lo) * 16));
+          bulk_load(stage0 + s * p.stage_bytes + (lo - g.w0) * 16,
+                    reinterpret_cast<const void*>(g.A0 - 16 + 16LL * lo),
+                    static_cast<uint32_t>((hi - lo) * 16), fb);
+        } else {
+          mbar_arrive(fb);
+        }
+      }
+      if (MODE != FWD) {
+        const long long first = n_iter > S ? n_iter - S : 0;
+        for (long long i = first; i < n_iter; ++i) {
+          const int s = static_cast<int>(i % S);
+          const uint32_t par = static_cast<uint32_t>((i / S) & 1);
+          mbar_wait<false>(smem_u32(&done_bar[s]), par, p.err, failed, WAIT_LIMIT_NS);
+          const UnitGeo go = unit_geo(p, cid + i * ncl, rank);
+          int lo, hi;
+          bulk_range(go, lo, hi);
+          if (hi > lo) {
+            bulk_store(reinterpret_cast<void*>(go.A0 - 16 + 16LL * lo),
+                       stage0 + s * p.stage_bytes + (lo - go.w0) * 16, (hi - lo) * 16);
+            bulk_commit();
+          }
+        }
+        bulk_wait_all();
+      } else {
+        // every issued load must land before the CTA may exit
+        const long long first = n_iter > S ? n_iter - S : 0;
+        for (long long i = first; i < n_iter; ++i) {
+          const int s = static_cast<int>(i % S);
+          mbar_wait<false>(smem_u32(&full_bar[s]), static_cast<uint32_t>((i / S) & 1), p.err,
+                           failed, WAIT_LIMIT_NS);
+        }
+      }
+    }
+  } else {
+    // ======================= consumer warps =======================
+    constexpr int LOG_ES = (ES == 4) ? 2 : 1;
+    const int R = p.R;
+    const int GT = NC / R;     // threads per row group
+    const int GW = GT / 32;    // warps per row group
+    const int grp = tid / GT;  // row of the unit this thread works on
+    const int gt = tid - grp * GT;
+    const int V = static_cast<int>(p.V);          // the host caps V * sizeof(T) far below 2^31
+    const int rb = static_cast<int>(p.row_bytes);
+    double acc = 0.0;  // this group's running loss sum (leader only)
+    const bool leader = (gt == 0) && (rank == 0);
+
+    for (long long i = 0; i < n_iter; ++i) {
+      const int s = static_cast<int>(i % S);
+      const int b = static_cast<int>(i & 1);
+      const UnitGeo g = unit_geo(p, cid + i * ncl, rank);
+      const bool row_ok = grp < g.rows;
+      const long long row = g.row0 + grp;
+      const long long t = row_ok ? __ldg(p.targets + row) : -1;
+      float lse_given = 0.f;
+      if (MODE == BWD && row_ok) lse_given = __ldg(p.lse_in + row);
+      const bool t_ok = row_ok && t >= 0 && t < V;
+
+      // Offsets are taken from the start of chunk 0 (absolute A0 - 16):
+      // element e of this row lies at byte e*ES - d0 of that frame.
+      const long long rs = g.as + static_cast<long long>(grp) * rb;  // row start (absolute)
+      const int d0 = static_cast<int>(g.A0 - 16 - rs);                // in (-16 - grp*rb, 0]
+      int lo = (-d0) >> 4;                 // chunk holding the row's first byte
+      int hi = ((rb - 1 - d0) >> 4) + 1;   // one past the chunk holding its last byte
+      if (lo < g.w0) lo = g.w0;
+      if (hi > g.w1) hi = g.w1;
+      if (!row_ok) hi = lo;
+      const uint32_t sbase = stage0 + s * p.stage_bytes - g.w0 * 16;  // chunk c at sbase + 16c
+
+      // target owner: the thread whose chunk holds x[row, t]
+      const int tbo = t_ok ? static_cast<int>(t) * ES - d0 : 0;
+      const int tc = t_ok ? (tbo >> 4) : -1;
+      const bool t_smem = tc >= 1 && tc <= g.nI;
+      const bool owner = t_ok && tc >= lo && tc < hi && ((tc - lo) % GT) == gt;
+
+      auto elem_ptr_global = [&](int e) -> char* {
+        return reinterpret_cast<char*>(rs + static_cast<long long>(e) * ES);
+      };
+      auto smem_ptr = [&](int byte_off) -> char* {
+        return static_cast<char*>(__cvta_shared_to_generic(sbase + byte_off));
+      };
+      // write EPC gradient values of chunk c (vector store when the chunk is
+      // whole, element stores at a row edge, global stores for head/tail)
+      auto store_chunk = [&](int c, const float* gv) {
+        const int e0 = (d0 + 16 * c) >> LOG_ES;
+        if (c >= 1 && c <= g.nI) {
+          if (e0 >= 0 && e0 + EPC <= V) {
+            sts128(sbase + 16 * c, E::pack(gv));
+          } else {
+#pragma unroll
+            for (int q = 0; q < EPC; ++q)
+              if (e0 + q >= 0 && e0 + q < V) E::st(smem_ptr(16 * c + q * ES), gv[q]);
+          }
+        } else {
+#pragma unroll
+          for (int q = 0; q < EPC; ++q)
+            if (e0 + q >= 0 && e0 + q < V) E::st(elem_ptr_global(e0 + q), gv[q]);
+        }
+      };
+
+      mbar_wait<false>(smem_u32(&full_bar[s]), static_cast<uint32_t>((i / S) & 1), p.err, failed,
+                       WAIT_LIMIT_NS);
+
+      float v[CPT][EPC];
+#pragma unroll
+      for (int k = 0; k < CPT; ++k) {
+        const int c = lo + gt + k * GT;
+        if (c < hi) {
+          const int e0 = (d0 + 16 * c) >> LOG_ES;  // element index of the chunk's first slot
+          if (c >= 1 && c <= g.nI) {
+            E::unpack(lds128(sbase + 16 * c), v[k]);
+            if (e0 < 0 || e0 + EPC > V) {
+#pragma unroll
+              for (int q = 0; q < EPC; ++q)
+                if (e0 + q < 0 || e0 + q >= V) v[k][q] = -INFINITY;
+            }
+          } else {
+#pragma unroll
+            for (int q = 0; q < EPC; ++q)
+              v[k][q] = (e0 + q >= 0 && e0 + q < V) ? E::ld(elem_ptr_global(e0 + q)) : -INFINITY;
+          }
+        } else {
+#pragma unroll
+          for (int q = 0; q < EPC; ++q) v[k][q] = -INFINITY;
+        }
+      }
+      float xt = 0.f;
+      if (owner) xt = t_smem ? E::ld(smem_ptr(tbo)) : E::ld(elem_ptr_global(static_cast<int>(t)));
+      if (MODE == FWD) {
+        // the stage is no longer needed: hand it back to the producer early
+        mbar_arrive(smem_u32(&done_bar[s]));
+      }
+
+      if (MODE == BWD) {
+        const float sc = p.grad_scale;
+        const float off = lse_given * kLog2e;
+#pragma unroll
+        for (int k = 0; k < CPT; ++k) {
+          const int c = lo + gt + k * GT;
+          if (c < hi) {
+            float gv[EPC];
+#pragma unroll
+            for (int q = 0; q < EPC; ++q) gv[q] = ex2(fmaf(v[k][q], kLog2e, -off)) * sc;
+            store_chunk(c, gv);
+          }
+        }
+        if (owner) {
+          const float gval = (ex2(fmaf(xt, kLog2e, -off)) - 1.f) * sc;
+          if (t_smem) E::st(smem_ptr(tbo), gval);
+          else E::st(elem_ptr_global(static_cast<int>(t)), gval);
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(smem_u32(&done_bar[s]));
+        if (row_ok && !t_ok && gt == 0 && rank == 0) atomicOr(p.err, ERR_TARGET_RANGE);
+        continue;
+      }
+
+      // ---- per-thread max, then one exp2 per element ----
+      float mt = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < CPT; ++k)
+#pragma unroll
+        for (int q = 0; q < EPC; ++q) mt = fmaxf(mt, v[k][q]);
+      const float mts = (mt == -INFINITY) ? 0.f : mt * kLog2e;
+      float st = 0.f;
+#pragma unroll
+      for (int k = 0; k < CPT; ++k)
+#pragma unroll
+        for (int q = 0; q < EPC; ++q) {
+          const float e = ex2(fmaf(v[k][q], kLog2e, -mts));
+          v[k][q] = e;
+          st += e;
+        }
+
+      // ---- merge (m, s): warp, then the row's warps ----
+      float mw = mt;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, o));
+      float sw = (mt == -INFINITY) ? 0.f : st * ex2((mt - mw) * kLog2e);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sw += __shfl_down_sync(0xffffffffu, sw, o);
+      if (lane == 0) red[b][warp] = make_float2(mw, sw);
+      if (owner) xt_slot[b][grp] = xt;
+      consumer_sync(NC);
+
+      float2 r = (lane < GW) ? red[b][grp * GW + lane] : make_float2(-INFINITY, 0.f);
+      float Mg = r.x;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) Mg = fmaxf(Mg, __shfl_xor_sync(0xffffffffu, Mg, o));
+      float Sg = (r.x == -INFINITY) ? 0.f : r.y * ex2((r.x - Mg) * kLog2e);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) Sg += __shfl_down_sync(0xffffffffu, Sg, o);
+      Sg = __shfl_sync(0xffffffffu, Sg, 0);
+      const bool have_t = t_ok && tc >= g.w0 && tc < g.w1;  // this CTA holds x[row, t]
+      float xrow = have_t ? xt_slot[b][grp] : 0.f;
+
+      // ---- merge across the cluster through distributed shared memory ----
+      if (CL > 1) {
+        if (tid == 0) {
+          const uint32_t my_slot = smem_u32(&xslot[b][rank]);
+          const uint32_t my_bar = smem_u32(&xbar[b]);
+          for (int k = 0; k < CL; ++k) {
+            st_cluster_f4(map_to_rank(my_slot, k), Mg, Sg, xrow, have_t ? 1.f : 0.f);
+            mbar_arrive_remote(map_to_rank(my_bar, k));
+          }
+        }
+        mbar_wait<true>(smem_u32(&xbar[b]), static_cast<uint32_t>((i >> 1) & 1), p.err, failed,
+                        WAIT_LIMIT_NS);
+        float4 xs = (lane < CL) ? xslot[b][lane] : make_float4(-INFINITY, 0.f, 0.f, 0.f);
+        float Mc = xs.x;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) Mc = fmaxf(Mc, __shfl_xor_sync(0xffffffffu, Mc, o));
+        float Sc = (xs.x == -INFINITY) ? 0.f : xs.y * ex2((xs.x - Mc) * kLog2e);
+        float Xc = xs.w != 0.f ? xs.z : 0.f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          Sc += __shfl_down_sync(0xffffffffu, Sc, o);
+          Xc += __shfl_down_sync(0xffffffffu, Xc, o);
+        }
+        Mg = Mc;
+        Sg = __shfl_sync(0xffffffffu, Sc, 0);
+        xrow = __shfl_sync(0xffffffffu, Xc, 0);
+      }
+
+      // ---- row outputs (one thread per row) ----
+      if (leader && row_ok) {
+        const float lse = Mg + logf(Sg);
+        const float rl = t_ok ? lse - xrow : __int_as_float(0x7fc00000);
+        if (p.row_loss) p.row_loss[row] = rl;
+        if (p.lse_out) p.lse_out[row] = lse;
+        acc += static_cast<double>(rl);
+        if (!t_ok) atomicOr(p.err, ERR_TARGET_RANGE);
+      }
+
+      if (MODE == FWD_BWD) {
+        // g = e * exp(m_t - lse) * scale, with lse in log2 units from the merged pair
+        const float lse2 = Mg * kLog2e + lg2(Sg);
+        const float sc = p.grad_scale;
+        const float f = ex2(mts - lse2) * sc;
+#pragma unroll
+        for (int k = 0; k < CPT; ++k) {
+          const int c = lo + gt + k * GT;
+          if (c < hi) {
+            float gv[EPC];
+#pragma unroll
+            for (int q = 0; q < EPC; ++q) gv[q] = v[k][q] * f;
+            store_chunk(c, gv);
+          }
+        }
+        if (owner) {
+          const float gval = (ex2(fmaf(xt, kLog2e, -lse2)) - 1.f) * sc;
+          if (t_smem) E::st(smem_ptr(tbo), gval);
+          else E::st(elem_ptr_global(static_cast<int>(t)), gval);
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(smem_u32(&done_bar[s]));
+      }
+    }
+
+    // ---- deterministic reduction of the loss ----
+    if (p.loss != nullptr) {
+      if (gt == 0) acc_slot[grp] = acc;
+      consumer_sync(NC);
+      if (tid == 0) {
+        double part = 0.0;
+        for (int j = 0; j < R; ++j) part += acc_slot[j];
+        p.partials[blockIdx.x] = part;
+        __threadfence();
+        const unsigned prev = atomicAdd(p.ticket, 1u);
+        if (prev == gridDim.x - 1) {
+          __threadfence();
+          double total = 0.0;
+          for (unsigned j = 0; j < gridDim.x; ++j) total += __ldcg(p.partials + j);
+          *p.loss = static_cast<float>(p.mean ? total / static_cast<double>(p.M) : total);
+          *p.ticket = 0u;  // ready for the next launch on this stream
+        }
+      }
+    }
+  }
+
+  if (CL > 1) {
+    __syncwarp();
+    cluster_sync_all();  // no CTA leaves while a peer may still write into its shared memory
+  }
+}
+
+}  // namespace ce

@@ -1,0 +1,101 @@
+"""Helpers for GPU-vs-oracle parity tests (test infrastructure).
+
+Tolerances (from the stated targets; the arithmetic behind them is in the
+design notes):
+  * fp32 logits: per-row loss and lse |err| <= 1e-4; reduced loss relative
+    error <= 1e-5; gradient |M*g_gpu - M*g_ref| <= 1e-5 (i.e. |g err| <=
+    1e-5 * scale).
+  * fp16/bf16 logits (fp32 accumulation): per-row loss and lse |err| <= 2e-3;
+    gradient within one unit in the last place of the output dtype of the
+    float64 reference (|g_gpu - RN(g_ref)| <= ulp(g_ref)), which also keeps
+    it inside the stated 2e-3 absolute bound.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+
+ROW_TOL = {"f32": 1e-4, "f16": 2e-3, "bf16": 2e-3}
+LOSS_REL_TOL_F32 = 1e-5
+GRAD_TOL_F32 = 1e-5  # on M*g (scale-normalised)
+TORCH_DT = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
+
+
+def to_device(x: np.ndarray, dtype: str, device="cuda", offset_elems: int = 0) -> torch.Tensor:
+    """Upload storage-dtype logits; with offset_elems > 0 the tensor starts that
+    many elements into a larger buffer (a base pointer off the 16-byte grid)."""
+    if dtype == "bf16":
+        src = torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16)
+    else:
+        src = torch.from_numpy(np.ascontiguousarray(x))
+    if offset_elems == 0:
+        return src.to(device)
+    M, V = x.shape
+    buf = torch.empty(M * V + offset_elems, dtype=TORCH_DT[dtype], device=device)
+    view = buf[offset_elems:].view(M, V)
+    view.copy_(src.to(device))
+    return view
+
+
+def to_host(t: torch.Tensor, dtype: str) -> np.ndarray:
+    t = t.detach().cpu().contiguous()
+    if dtype == "bf16":
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()
+
+
+def widen(x_storage: np.ndarray, dtype: str) -> np.ndarray:
+    return oracle.to_f64(x_storage, dtype)
+
+
+def check_rows(name, got, ref, tol, rows=None):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    if rows is not None:
+        got = got[rows]
+    both_nan = np.isnan(got) & np.isnan(ref)
+    err = np.where(both_nan, 0.0, np.abs(got - ref))
+    bad = ~(err <= tol)
+    assert not bad.any(), (f"{name}: {bad.sum()} rows beyond {tol}; worst "
+                           f"{np.nanmax(err):.3e} at {int(np.argmax(np.where(np.isnan(err), np.inf, err)))}")
+
+
+def check_loss(got: float, ref: float, dtype: str, M: int):
+    if np.isnan(ref):
+        assert np.isnan(got)
+        return
+    if dtype == "f32":
+        assert abs(got - ref) <= LOSS_REL_TOL_F32 * max(abs(ref), 1e-30) + 1e-7, (got, ref)
+    else:
+        # the mean of per-row errors bounded by the per-row tolerance
+        assert abs(got - ref) <= ROW_TOL[dtype] * max(1.0, 1.0 if M else 0.0), (got, ref)
+
+
+def check_grad(g_storage: np.ndarray, x64: np.ndarray, t: np.ndarray, lse_ref: np.ndarray,
+               scale: float, dtype: str):
+    """Compare gradient rows (storage dtype) with the float64 reference rows."""
+    g_ref = oracle.ce_grad(x64, t, lse_ref, scale)
+    g = oracle.to_f64(g_storage, dtype)
+    if dtype == "f32":
+        err = np.abs(g - g_ref)
+        tol = GRAD_TOL_F32 * abs(scale)
+        assert np.all(err <= tol), f"grad: worst |err| {err.max():.3e} > {tol:.3e}"
+    else:
+        r = oracle.round_to_format(g_ref, dtype)
+        err = np.abs(g - r)
+        u = oracle.ulp(g_ref, dtype)
+        bad = err > u
+        assert not bad.any(), (f"grad: {bad.sum()} elements beyond 1 ulp; e.g. got {g[bad][:4]} "
+                               f"ref {g_ref[bad][:4]}")
+        assert np.all(np.abs(g - g_ref) <= 2e-3 + u)
+
+
+def sample_rows(M: int, n: int, seed: int = 7) -> np.ndarray:
+    if M <= n:
+        return np.arange(M)
+    rng = np.random.default_rng(seed)
+    rows = rng.choice(M, size=n - 2, replace=False)
+    return np.unique(np.concatenate([[0, M - 1], rows]))

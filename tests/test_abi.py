@@ -1,0 +1,114 @@
+"""The C ABI without a GPU: the library builds, loads, exports every symbol the
+header declares, and rejects bad arguments on the host before any launch."""
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from tests.conftest import ROOT
+
+HEADER_DIR = os.path.join(ROOT, "include")
+
+
+def _declared_functions():
+    names = []
+    for h in sorted(os.listdir(HEADER_DIR)):
+        if not h.endswith(".h"):
+            continue
+        text = open(os.path.join(HEADER_DIR, h)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][\w]*\s*\*?\s+(\w+)\s*\(", text, re.M):
+            if m.group(1) not in ("if", "return"):
+                names.append(m.group(1))
+    return names
+
+
+@pytest.fixture(scope="module")
+def cdll():
+    from softmax_cross_entropy_online_gb300 import api, build
+    build.build()
+    return api.lib()
+
+
+def test_header_declares_the_boundary():
+    names = set(_declared_functions())
+    for required in ("ce_forward", "ce_fwd_bwd_inplace", "ce_backward_from_lse",
+                     "ce_check_errors", "ce_status_string"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(cdll):
+    from softmax_cross_entropy_online_gb300 import build
+    names = _declared_functions()
+    assert names
+    exported = subprocess.run(["nm", "-D", "--defined-only", build.LIB_PATH],
+                              capture_output=True, text=True, check=True).stdout
+    for n in names:
+        assert re.search(rf"\bT {n}$", exported, re.M), f"{n} not exported"
+        assert hasattr(cdll, n)
+
+
+def test_binding_covers_every_declared_symbol():
+    from softmax_cross_entropy_online_gb300 import api
+    assert set(_declared_functions()) == set(api.SIGNATURES)
+
+
+def test_status_strings(cdll):
+    from softmax_cross_entropy_online_gb300 import api
+    names = [api.status_string(i) for i in range(6)]
+    assert names == ["CE_OK", "CE_ERR_INVALID_ARG", "CE_ERR_UNSUPPORTED", "CE_ERR_TARGET_RANGE",
+                     "CE_ERR_CUDA", "CE_ERR_TIMEOUT"]
+    assert api.status_string(99) == "CE_ERR_UNKNOWN"
+
+
+def test_max_vocab(cdll):
+    assert cdll.ce_max_vocab(0) * 4 == cdll.ce_max_vocab(1) * 2 == cdll.ce_max_vocab(2) * 2
+    # 8 CTAs x 2048 chunks of 16 B, less one chunk of slack for a misaligned row
+    assert cdll.ce_max_vocab(1) == (8 * 2048 - 2) * 8 and cdll.ce_max_vocab(0) == (8 * 2048 - 2) * 4
+    assert cdll.ce_max_vocab(7) == 0
+
+
+@pytest.mark.parametrize("args", [
+    # (logits, targets, M, V, dtype, red, loss, row_loss, lse)
+    (16, 16, -1, 4, 0, 0, 16, None, None),      # M < 0
+    (16, 16, 4, 0, 0, 0, 16, None, None),       # V < 1
+    (16, 16, 4, 4, 3, 0, 16, None, None),       # bad dtype
+    (16, 16, 4, 4, 0, 5, 16, None, None),       # bad reduction
+    (None, 16, 4, 4, 0, 0, 16, None, None),     # null logits
+    (16, None, 4, 4, 0, 0, 16, None, None),     # null targets
+    (18, 16, 4, 4, 0, 0, 16, None, None),       # fp32 logits not 4-byte aligned
+    (17, 16, 4, 4, 1, 0, 16, None, None),       # fp16 logits not 2-byte aligned
+    (16, 12, 4, 4, 0, 0, 16, None, None),       # targets not 8-byte aligned
+    (16, 16, 4, 4, 0, 0, 18, None, None),       # loss not 4-byte aligned
+    (16, 16, 4, 4, 0, 0, 16, 2, None),          # row_loss misaligned
+    (16, 16, 1 << 40, 1 << 30, 0, 0, 16, None, None),  # M*V*4 overflows
+])
+def test_host_validation_rejects(cdll, args):
+    for fn in (cdll.ce_forward, cdll.ce_fwd_bwd_inplace):
+        assert fn(*args, None) == 1  # CE_ERR_INVALID_ARG, returned before any CUDA call
+
+
+def test_host_validation_backward(cdll):
+    assert cdll.ce_backward_from_lse(16, 16, None, 4, 4, 0, 1.0, None) == 1  # null lse
+    assert cdll.ce_backward_from_lse(16, 16, 16, 4, 0, 0, 1.0, None) == 1    # V = 0
+    assert cdll.ce_selftest_wait_timeout(None, 0) == 1
+    assert cdll.ce_selftest_wait_timeout(None, 2000000) == 1
+
+
+def test_empty_problem_without_loss_is_a_no_op(cdll):
+    # M == 0 with nothing to write returns before touching the device
+    assert cdll.ce_forward(None, None, 0, 5, 0, 2, None, None, None, None) == 0
+    assert cdll.ce_fwd_bwd_inplace(None, None, 0, 5, 2, 0, None, None, None, None) == 0
+
+
+def test_product_path_never_imports_the_oracle():
+    pkg = os.path.join(ROOT, "softmax_cross_entropy_online_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(from|import)\s+oracle\b", text, re.M), f
+                assert "ce_oracle" not in text, f
