@@ -20,6 +20,7 @@ own GPU (weak scaling); the step time is the max over ranks.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -392,9 +393,13 @@ def main():
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     ap.add_argument("--ref-rows", type=int, default=1024)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--rows", type=int, default=None,
+                    help="override the workload's row count (smaller cases for profiling)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps, always
     w = synthetic.WORKLOADS[args.workload]
+    if args.rows is not None:
+        w = dataclasses.replace(w, M=args.rows, name=f"{w.name}[rows={args.rows}]")
     if args.impl == "reference":
         return run_reference(args, w)
     return run_native(args, w)

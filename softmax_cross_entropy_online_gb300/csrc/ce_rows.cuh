@@ -173,8 +173,9 @@ __device__ __forceinline__ void bulk_store(void* dst, uint32_t src_smem, uint32_
 __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
-__device__ __forceinline__ void bulk_wait_read_all() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
 }
 __device__ __forceinline__ void bulk_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
@@ -386,29 +387,18 @@ __global__ void __launch_bounds__(NC + 32, 1) ce_rows_kernel(const RowParams p) 
 
   if (warp == NW) {
     // ======================= producer warp =======================
+    // Loads run S units ahead of the consumers.  In the modes that write, the
+    // gradient of unit j is stored as soon as the consumers release its stage,
+    // and a stage is refilled LAG units later, once its store has been read
+    // out of shared memory, so a store never stalls the next load.
     if (lane == 0) {
-      for (long long i = 0; i < n_iter; ++i) {
+      auto issue_load = [&](long long i) {
         const int s = static_cast<int>(i % S);
-        if (i >= S) {
-          const uint32_t par = static_cast<uint32_t>(((i / S) - 1) & 1);
-          mbar_wait<false>(smem_u32(&done_bar[s]), par, p.err, failed, WAIT_LIMIT_NS);
-          if (MODE != FWD) {
-            const UnitGeo go = unit_geo(p, cid + (i - S) * ncl, rank);
-            int lo, hi;
-            bulk_range(go, lo, hi);
-            if (hi > lo) {
-              bulk_store(reinterpret_cast<void*>(go.A0 - 16 + 16LL * lo),
-                         stage0 + s * p.stage_bytes + (lo - go.w0) * 16, (hi - lo) * 16);
-              bulk_commit();
-              bulk_wait_read_all();
-            }
-          }
-        }
-        fence_proxy_async_smem();
         const UnitGeo g = unit_geo(p, cid + i * ncl, rank);
         int lo, hi;
         bulk_range(g, lo, hi);
         const uint32_t fb = smem_u32(&full_bar[s]);
+        fence_proxy_async_smem();
         if (hi > lo) {
           mbar_arrive_expect_tx(fb, static_cast<uint32_t>((hi - lo) * 16));
           bulk_load(stage0 + s * p.stage_bytes + (lo - g.w0) * 16,
@@ -417,32 +407,33 @@ __global__ void __launch_bounds__(NC + 32, 1) ce_rows_kernel(const RowParams p) 
         } else {
           mbar_arrive(fb);
         }
-      }
-      if (MODE != FWD) {
-        const long long first = n_iter > S ? n_iter - S : 0;
-        for (long long i = first; i < n_iter; ++i) {
-          const int s = static_cast<int>(i % S);
-          const uint32_t par = static_cast<uint32_t>((i / S) & 1);
-          mbar_wait<false>(smem_u32(&done_bar[s]), par, p.err, failed, WAIT_LIMIT_NS);
-          const UnitGeo go = unit_geo(p, cid + i * ncl, rank);
+      };
+      const long long pre = n_iter < S ? n_iter : S;
+      for (long long i = 0; i < pre; ++i) issue_load(i);
+      const int lag = (S >= 3) ? 2 : 1;
+      for (long long j = 0; j < n_iter; ++j) {
+        const int s = static_cast<int>(j % S);
+        mbar_wait<false>(smem_u32(&done_bar[s]), static_cast<uint32_t>((j / S) & 1), p.err,
+                         failed, WAIT_LIMIT_NS);
+        if (MODE == FWD) {
+          if (j + S < n_iter) issue_load(j + S);
+        } else {
+          const UnitGeo go = unit_geo(p, cid + j * ncl, rank);
           int lo, hi;
           bulk_range(go, lo, hi);
-          if (hi > lo) {
+          if (hi > lo)
             bulk_store(reinterpret_cast<void*>(go.A0 - 16 + 16LL * lo),
                        stage0 + s * p.stage_bytes + (lo - go.w0) * 16, (hi - lo) * 16);
-            bulk_commit();
+          bulk_commit();  // one group per unit (possibly empty) keeps the count exact
+          const long long r = j - lag;
+          if (r >= 0 && r + S < n_iter) {
+            if (lag == 2) bulk_wait_read<2>();
+            else bulk_wait_read<1>();
+            issue_load(r + S);
           }
         }
-        bulk_wait_all();
-      } else {
-        // every issued load must land before the CTA may exit
-        const long long first = n_iter > S ? n_iter - S : 0;
-        for (long long i = first; i < n_iter; ++i) {
-          const int s = static_cast<int>(i % S);
-          mbar_wait<false>(smem_u32(&full_bar[s]), static_cast<uint32_t>((i / S) & 1), p.err,
-                           failed, WAIT_LIMIT_NS);
-        }
       }
+      if (MODE != FWD) bulk_wait_all();
     }
   } else {
     // ======================= consumer warps =======================
@@ -545,19 +536,19 @@ __global__ void __launch_bounds__(NC + 32, 1) ce_rows_kernel(const RowParams p) 
 
       if (MODE == BWD) {
         const float sc = p.grad_scale;
-        const float off = lse_given * kLog2e;
 #pragma unroll
         for (int k = 0; k < CPT; ++k) {
           const int c = lo + gt + k * GT;
           if (c < hi) {
             float gv[EPC];
 #pragma unroll
-            for (int q = 0; q < EPC; ++q) gv[q] = ex2(fmaf(v[k][q], kLog2e, -off)) * sc;
+            for (int q = 0; q < EPC; ++q) gv[q] = ex2((v[k][q] - lse_given) * kLog2e) * sc;
             store_chunk(c, gv);
           }
         }
         if (owner) {
-          const float gval = (ex2(fmaf(xt, kLog2e, -off)) - 1.f) * sc;
+          // exp(x_t - lse) - 1 without cancellation when the target dominates
+          const float gval = expm1f(xt - lse_given) * sc;
           if (t_smem) E::st(smem_ptr(tbo), gval);
           else E::st(elem_ptr_global(static_cast<int>(t)), gval);
         }
@@ -573,13 +564,15 @@ __global__ void __launch_bounds__(NC + 32, 1) ce_rows_kernel(const RowParams p) 
       for (int k = 0; k < CPT; ++k)
 #pragma unroll
         for (int q = 0; q < EPC; ++q) mt = fmaxf(mt, v[k][q]);
-      const float mts = (mt == -INFINITY) ? 0.f : mt * kLog2e;
+      // differences first, then the scale to log2 units: exact for logits that
+      // share a large offset (shift invariance holds in fp32 too)
+      const float mref = (mt == -INFINITY) ? 0.f : mt;
       float st = 0.f;
 #pragma unroll
       for (int k = 0; k < CPT; ++k)
 #pragma unroll
         for (int q = 0; q < EPC; ++q) {
-          const float e = ex2(fmaf(v[k][q], kLog2e, -mts));
+          const float e = ex2((v[k][q] - mref) * kLog2e);
           v[k][q] = e;
           st += e;
         }
@@ -636,8 +629,10 @@ __global__ void __launch_bounds__(NC + 32, 1) ce_rows_kernel(const RowParams p) 
 
       // ---- row outputs (one thread per row) ----
       if (leader && row_ok) {
-        const float lse = Mg + logf(Sg);
-        const float rl = t_ok ? lse - xrow : __int_as_float(0x7fc00000);
+        const float lnS = logf(Sg);
+        const float lse = Mg + lnS;
+        // (m - x_t) + log S keeps the loss accurate when m and x_t are large
+        const float rl = t_ok ? (Mg - xrow) + lnS : __int_as_float(0x7fc00000);
         if (p.row_loss) p.row_loss[row] = rl;
         if (p.lse_out) p.lse_out[row] = lse;
         acc += static_cast<double>(rl);
@@ -645,10 +640,9 @@ __global__ void __launch_bounds__(NC + 32, 1) ce_rows_kernel(const RowParams p) 
       }
 
       if (MODE == FWD_BWD) {
-        // g = e * exp(m_t - lse) * scale, with lse in log2 units from the merged pair
-        const float lse2 = Mg * kLog2e + lg2(Sg);
+        // g = e * exp(m_t - lse) * scale with exp(m_t - lse) = 2^((m_t - M) log2 e - log2 S)
         const float sc = p.grad_scale;
-        const float f = ex2(mts - lse2) * sc;
+        const float f = ex2((mt - Mg) * kLog2e - lg2(Sg)) * sc;
 #pragma unroll
         for (int k = 0; k < CPT; ++k) {
           const int c = lo + gt + k * GT;
@@ -660,7 +654,8 @@ __global__ void __launch_bounds__(NC + 32, 1) ce_rows_kernel(const RowParams p) 
           }
         }
         if (owner) {
-          const float gval = (ex2(fmaf(xt, kLog2e, -lse2)) - 1.f) * sc;
+          // exp(x_t - lse) - 1 without cancellation when the target dominates
+          const float gval = expm1f((xt - Mg) - logf(Sg)) * sc;
           if (t_smem) E::st(smem_ptr(tbo), gval);
           else E::st(elem_ptr_global(static_cast<int>(t)), gval);
         }

@@ -7,8 +7,17 @@ design notes):
     1e-5 * scale).
   * fp16/bf16 logits (fp32 accumulation): per-row loss and lse |err| <= 2e-3;
     gradient within one unit in the last place of the output dtype of the
-    float64 reference (|g_gpu - RN(g_ref)| <= ulp(g_ref)), which also keeps
-    it inside the stated 2e-3 absolute bound.
+    float64 reference plus the fp32 evaluation error of softmax, scaled:
+    |g_gpu - RN(g_ref)| <= ulp(g_ref) + 4e-6 * scale.  This stays far inside
+    the stated bound (2e-3 absolute plus one ulp).
+  * lse is an fp32 output: its own rounding (2^-23 relative) is added to the
+    row tolerance.
+
+The 4e-6 * scale term is the absolute error of p = exp(x - lse) in fp32: the
+row sum near 1 is rounded at 2^-24 per addition over a few tens of additions
+(<= ~70 * 2^-24 = 4.2e-6), and exp2/log2 are evaluated to ~2^-22.  It only
+matters where the exact gradient is smaller than that error, e.g. the target
+entry of a row whose target dominates (p_t -> 1, g_t -> 0).
 """
 
 from __future__ import annotations
@@ -21,6 +30,7 @@ import oracle
 ROW_TOL = {"f32": 1e-4, "f16": 2e-3, "bf16": 2e-3}
 LOSS_REL_TOL_F32 = 1e-5
 GRAD_TOL_F32 = 1e-5  # on M*g (scale-normalised)
+GRAD_ABS_EPS = 4e-6  # fp32 evaluation error of softmax, times scale
 TORCH_DT = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
 
 
@@ -59,8 +69,13 @@ def check_rows(name, got, ref, tol, rows=None):
     both_nan = np.isnan(got) & np.isnan(ref)
     err = np.where(both_nan, 0.0, np.abs(got - ref))
     bad = ~(err <= tol)
-    assert not bad.any(), (f"{name}: {bad.sum()} rows beyond {tol}; worst "
+    assert not bad.any(), (f"{name}: {bad.sum()} rows beyond tolerance; worst "
                            f"{np.nanmax(err):.3e} at {int(np.argmax(np.where(np.isnan(err), np.inf, err)))}")
+
+
+def check_lse(name, got, ref, tol, rows=None):
+    ref = np.asarray(ref, dtype=np.float64)
+    check_rows(name, got, ref, tol + 2.0**-22 * np.abs(ref), rows)
 
 
 def check_loss(got: float, ref: float, dtype: str, M: int):
@@ -87,7 +102,7 @@ def check_grad(g_storage: np.ndarray, x64: np.ndarray, t: np.ndarray, lse_ref: n
         r = oracle.round_to_format(g_ref, dtype)
         err = np.abs(g - r)
         u = oracle.ulp(g_ref, dtype)
-        bad = err > u
+        bad = err > u + GRAD_ABS_EPS * abs(scale)
         assert not bad.any(), (f"grad: {bad.sum()} elements beyond 1 ulp; e.g. got {g[bad][:4]} "
                                f"ref {g_ref[bad][:4]}")
         assert np.all(np.abs(g - g_ref) <= 2e-3 + u)

@@ -34,7 +34,7 @@ def api():
 
 
 def run_all(x_np, t_np, dtype, reduction="mean", offset_elems=0, stream=None):
-    """Run forward, fused fwd+bwd and backward-from-lse on the same input."""
+    """Run the forward and the fused fwd+bwd on the same input."""
     a = api()
     t_dev = torch.from_numpy(t_np).cuda()
     xf = P.to_device(x_np, dtype, offset_elems=offset_elems)
@@ -43,12 +43,22 @@ def run_all(x_np, t_np, dtype, reduction="mean", offset_elems=0, stream=None):
     loss_b, rl_b, lse_b = a.ce_fwd_bwd_inplace(xb, t_dev, reduction, stream=stream)
     M = x_np.shape[0]
     scale = oracle.grad_scale(reduction, M) if M else 1.0
-    xl = P.to_device(x_np, dtype, offset_elems=offset_elems)
-    if M:
-        a.ce_backward_from_lse(xl, t_dev, lse_f, scale, stream=stream)
     torch.cuda.synchronize()
     return dict(loss_f=loss_f, rl_f=rl_f, lse_f=lse_f, loss_b=loss_b, rl_b=rl_b, lse_b=lse_b,
-                grad_b=xb, grad_l=xl, scale=scale)
+                grad_b=xb, scale=scale)
+
+
+def check_backward_from_lse(x_rows, t_rows, lse_ref, scale, dtype, offset_elems=0):
+    """ce_backward_from_lse on the given rows, fed the oracle's lse rounded to
+    fp32; the reference gradient uses that same fp32 lse."""
+    a = api()
+    lse32 = lse_ref.astype(np.float32)
+    xl = P.to_device(x_rows, dtype, offset_elems=offset_elems)
+    a.ce_backward_from_lse(xl, torch.from_numpy(t_rows).cuda(), torch.from_numpy(lse32).cuda(),
+                           scale)
+    torch.cuda.synchronize()
+    P.check_grad(P.to_host(xl, dtype), P.widen(x_rows, dtype), t_rows,
+                 lse32.astype(np.float64), scale, dtype)
 
 
 def check_case(x_np, t_np, dtype, reduction="mean", offset_elems=0, rows=None):
@@ -62,7 +72,7 @@ def check_case(x_np, t_np, dtype, reduction="mean", offset_elems=0, rows=None):
     for key in ("rl_f", "rl_b"):
         P.check_rows(key, out[key].cpu().numpy(), ref["row_loss"], tol, rows)
     for key in ("lse_f", "lse_b"):
-        P.check_rows(key, out[key].cpu().numpy(), ref["lse"], tol, rows)
+        P.check_lse(key, out[key].cpu().numpy(), ref["lse"], tol, rows)
     if reduction != "none":
         if len(rows) == M:
             P.check_loss(out["loss_f"].item(), ref["loss"], dtype, M)
@@ -80,9 +90,11 @@ def check_case(x_np, t_np, dtype, reduction="mean", offset_elems=0, rows=None):
     else:
         assert out["loss_f"] is None
     ridx = torch.from_numpy(rows).to(out["grad_b"].device)
-    for key in ("grad_b", "grad_l"):
-        g = P.to_host(out[key][ridx], dtype)
-        P.check_grad(g, x64, t_np[rows], ref["lse"], out["scale"], dtype)
+    g = P.to_host(out["grad_b"][ridx], dtype)
+    P.check_grad(g, x64, t_np[rows], ref["lse"], out["scale"], dtype)
+    if M:
+        check_backward_from_lse(x_np[rows], t_np[rows], ref["lse"], out["scale"], dtype,
+                                offset_elems)
     return out
 
 
