@@ -17,10 +17,11 @@
 
 namespace ce {
 template <typename T>
-cudaError_t rows_launch(int mode, int NC, const RowParams& p, int grid, int smem_bytes,
+cudaError_t rows_launch(int mode, int variant, const RowParams& p, int grid, int smem_bytes,
                         cudaStream_t stream);
 template <typename T>
-cudaError_t rows_max_active(int mode, int NC, int smem_bytes, int CL, int sm_count, int* out);
+cudaError_t rows_max_active(int mode, int variant, int smem_bytes, int CL, int sm_count,
+                            int* out);
 }  // namespace ce
 
 namespace ce {
@@ -47,7 +48,7 @@ namespace {
 std::atomic<uint64_t> g_launches{0};
 
 constexpr int kSmemBudget = 200 * 1024;  // dynamic shared memory per CTA for the stages
-constexpr int kScratchPartials = 8192;   // > any persistent grid (152 SMs x 2 CTAs)
+constexpr int kScratchPartials = 8192;   // > any persistent grid (152 SMs x 4 CTAs)
 
 struct DeviceInfo {
   int sm_count = 0;
@@ -111,88 +112,88 @@ int elem_size(ce_dtype d) {
 }
 
 struct Plan {
-  int NC = 0, R = 1, CL = 1, S = 0, stage_bytes = 0;
+  int variant = 0, R = 1, CL = 1, S = 0, stage_bytes = 0;
 };
+
+constexpr int kMaxSliceBytes = 200 * 1024;  // one stage of one CTA, at most
 
 // Upper bound of the 16-byte chunks one row (or R rows) can straddle.
 long long chunks_for(long long bytes, bool aligned) {
   return aligned ? (bytes + 15) / 16 : (bytes + 15) / 16 + 1;
 }
 
-// Launch shape for rows of `rb` bytes.  A CTA holds NC*CPT = 2048 chunks
-// (32 KB) of a unit in registers.  Rows up to that size live in one CTA (R rows
-// per unit, a group of NC/R consumer threads per row); longer rows are split
-// over a cluster of CL = 2..8 CTAs.
-bool choose_plan(long long rb, bool aligned, long long M, int sm_count, int NC, Plan& pl) {
-  const int CPT = ce::cpt_for(NC);
-  const long long cap = static_cast<long long>(NC) * CPT;
+// Stage size of a launch shape, or 0 when the shape cannot hold the rows.
+long long stage_bytes_for(int variant, int R, int CL, long long rb, bool aligned) {
+  const int NC = ce::kVariants[variant].NC;
+  const int CPT = ce::kVariants[variant].CPT;
+  if (R < 1 || NC % R != 0 || (NC / R) % 32 != 0) return 0;
+  if (CL < 1 || CL > ce::kMaxCluster || (CL > 1 && R != 1)) return 0;
   const long long cpr = chunks_for(rb, aligned);
-  if (cpr <= cap) {
-    // the smallest power-of-two group (>= one warp) that covers a row
+  if (CL == 1) {
+    if (CPT > 0 && static_cast<long long>(NC / R) * CPT < cpr) return 0;
+    return chunks_for(static_cast<long long>(R) * rb, aligned) * 16;
+  }
+  const long long per_cta = (cpr + CL - 1) / CL;
+  if (CPT > 0 && per_cta > static_cast<long long>(NC) * CPT) return 0;
+  return per_cta * 16;
+}
+
+// Default launch shape: the shared-memory streaming consumers (variant 3, 256
+// threads) with two CTAs per SM.  Rows of up to 32 KB are packed R per unit in
+// one CTA; longer rows are split over a cluster of up to 8 CTAs.
+bool choose_plan(long long rb, bool aligned, long long M, int sm_count, Plan& pl) {
+  const int variant = 3;
+  const int NC = ce::kVariants[variant].NC;
+  const long long per_cta_smem = 96 * 1024;
+  const long long cpr = chunks_for(rb, aligned);
+  if (cpr * 16 <= 32 * 1024) {
+    // about 8 chunks per thread and pass: GT = cpr / 8 rounded up to a power of two
     int GT = 32;
-    while (static_cast<long long>(GT) * CPT < cpr) GT *= 2;
+    while (GT < NC && static_cast<long long>(GT) * 8 < cpr) GT *= 2;
     int R = NC / GT;
-    // small problems: more units (CTAs) before more rows per unit
-    while (R > 1 && (M + R - 1) / R < sm_count) R /= 2;
+    while (R > 1 && (M + R - 1) / R < 2LL * sm_count) R /= 2;
     for (; R >= 1; R /= 2) {
-      const long long stage = chunks_for(static_cast<long long>(R) * rb, aligned) * 16;
-      const int S = static_cast<int>(kSmemBudget / stage);
-      if (S >= 3 || (R == 1 && S >= 2)) {
-        pl.NC = NC;
-        pl.R = R;
-        pl.CL = 1;
-        pl.S = S > ce::kMaxStages ? ce::kMaxStages : S;
-        pl.stage_bytes = static_cast<int>(stage);
+      const long long stage = stage_bytes_for(variant, R, 1, rb, aligned);
+      if (stage == 0) continue;
+      long long S = per_cta_smem / stage;
+      if (S > ce::kMaxStages) S = ce::kMaxStages;
+      if (S >= 2) {
+        pl = Plan{variant, R, 1, static_cast<int>(S), static_cast<int>(stage)};
         return true;
       }
     }
   }
   for (int CL = 2; CL <= ce::kMaxCluster; ++CL) {
-    const long long per_cta = (cpr + CL - 1) / CL;
-    if (per_cta > cap) continue;
-    const long long stage = per_cta * 16;
-    const int S = static_cast<int>(kSmemBudget / stage);
-    if (S < 2) continue;
-    pl.NC = NC;
-    pl.R = 1;
-    pl.CL = CL;
-    pl.S = S > ce::kMaxStages ? ce::kMaxStages : S;
-    pl.stage_bytes = static_cast<int>(stage);
+    const long long stage = stage_bytes_for(variant, 1, CL, rb, aligned);
+    if (stage == 0 || stage > 32 * 1024) continue;
+    long long S = per_cta_smem / stage;
+    if (S > ce::kMaxStages) S = ce::kMaxStages;
+    pl = Plan{variant, 1, CL, static_cast<int>(S), static_cast<int>(stage)};
     return true;
   }
-  return false;
+  // very long rows: 8 CTAs, larger slices, fewer stages
+  const long long stage = stage_bytes_for(variant, 1, ce::kMaxCluster, rb, aligned);
+  if (stage == 0 || stage > kMaxSliceBytes) return false;
+  long long S = (2 * per_cta_smem) / stage;
+  if (S < 1) S = 1;
+  if (S > 2) S = 2;
+  if (S * stage > 220 * 1024) S = 1;
+  pl = Plan{variant, 1, ce::kMaxCluster, static_cast<int>(S), static_cast<int>(stage)};
+  return true;
 }
 
-// Optional override for tuning sweeps: CE_PLAN="NC,R,CL,S".  It is checked
-// against the same limits as the automatic choice and ignored when it does
-// not fit them.
+// Optional override for tuning sweeps: CE_PLAN="variant,R,CL,S" (variant
+// indexes kVariants).  It is checked against the same limits as the automatic
+// choice and ignored when it does not fit them.
 void apply_env_plan(long long rb, bool aligned, Plan& pl) {
   const char* env = std::getenv("CE_PLAN");
   if (env == nullptr || *env == 0) return;
-  int NC = 0, R = 0, CL = 0, S = 0;
-  if (std::sscanf(env, "%d,%d,%d,%d", &NC, &R, &CL, &S) != 4) return;
-  const int CPT = ce::cpt_for(NC);
-  if (CPT == 0) return;
-  if (R < 1 || NC % R != 0 || (NC / R) % 32 != 0) return;
-  if (CL < 1 || CL > ce::kMaxCluster) return;
-  if (CL > 1 && R != 1) return;
-  const long long cpr = chunks_for(rb, aligned);
-  const long long GT = NC / R;
-  long long stage = 0;
-  if (CL == 1) {
-    if (GT * CPT < cpr) return;
-    stage = chunks_for(static_cast<long long>(R) * rb, aligned) * 16;
-  } else {
-    const long long per_cta = (cpr + CL - 1) / CL;
-    if (per_cta > static_cast<long long>(NC) * CPT) return;
-    stage = per_cta * 16;
-  }
-  if (S < 1 || S > ce::kMaxStages || stage * S > 220 * 1024) return;
-  pl.NC = NC;
-  pl.R = R;
-  pl.CL = CL;
-  pl.S = S;
-  pl.stage_bytes = static_cast<int>(stage);
+  int var = 0, R = 0, CL = 0, S = 0;
+  if (std::sscanf(env, "%d,%d,%d,%d", &var, &R, &CL, &S) != 4) return;
+  if (var < 0 || var >= ce::kNumVariants) return;
+  const long long stage = stage_bytes_for(var, R, CL, rb, aligned);
+  if (stage == 0 || S < 1 || S > ce::kMaxStages || stage * S > 220 * 1024) return;
+  pl = Plan{var, R, CL, S, static_cast<int>(stage)};
 }
 
 ce_status launch_rows(int mode, const void* logits, const int64_t* targets, const float* lse_in,
@@ -224,7 +225,7 @@ ce_status launch_rows(int mode, const void* logits, const int64_t* targets, cons
 
   const bool aligned = (lb % 16 == 0) && (rb % 16 == 0);
   Plan pl;
-  if (!choose_plan(rb, aligned, M, di.sm_count, 256, pl)) return CE_ERR_UNSUPPORTED;
+  if (!choose_plan(rb, aligned, M, di.sm_count, pl)) return CE_ERR_UNSUPPORTED;
   apply_env_plan(rb, aligned, pl);
 
   ce::RowParams p;
@@ -251,9 +252,9 @@ ce_status launch_rows(int mode, const void* logits, const int64_t* targets, cons
   int max_active = 0;
   cudaError_t ce_err = cudaSuccess;
   switch (dtype) {
-    case CE_F32: ce_err = ce::rows_max_active<float>(mode, pl.NC, smem, pl.CL, di.sm_count, &max_active); break;
-    case CE_F16: ce_err = ce::rows_max_active<__half>(mode, pl.NC, smem, pl.CL, di.sm_count, &max_active); break;
-    default: ce_err = ce::rows_max_active<__nv_bfloat16>(mode, pl.NC, smem, pl.CL, di.sm_count, &max_active); break;
+    case CE_F32: ce_err = ce::rows_max_active<float>(mode, pl.variant, smem, pl.CL, di.sm_count, &max_active); break;
+    case CE_F16: ce_err = ce::rows_max_active<__half>(mode, pl.variant, smem, pl.CL, di.sm_count, &max_active); break;
+    default: ce_err = ce::rows_max_active<__nv_bfloat16>(mode, pl.variant, smem, pl.CL, di.sm_count, &max_active); break;
   }
   if (ce_err != cudaSuccess || max_active < 1) return CE_ERR_CUDA;
   long long nclusters = p.n_units < max_active ? p.n_units : max_active;
@@ -271,9 +272,9 @@ ce_status launch_rows(int mode, const void* logits, const int64_t* targets, cons
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   switch (dtype) {
-    case CE_F32: ce_err = ce::rows_launch<float>(mode, pl.NC, p, grid, smem, s); break;
-    case CE_F16: ce_err = ce::rows_launch<__half>(mode, pl.NC, p, grid, smem, s); break;
-    default: ce_err = ce::rows_launch<__nv_bfloat16>(mode, pl.NC, p, grid, smem, s); break;
+    case CE_F32: ce_err = ce::rows_launch<float>(mode, pl.variant, p, grid, smem, s); break;
+    case CE_F16: ce_err = ce::rows_launch<__half>(mode, pl.variant, p, grid, smem, s); break;
+    default: ce_err = ce::rows_launch<__nv_bfloat16>(mode, pl.variant, p, grid, smem, s); break;
   }
   if (ce_err != cudaSuccess) return CE_ERR_CUDA;
   g_launches.fetch_add(1, std::memory_order_relaxed);
@@ -357,8 +358,8 @@ const char* ce_status_string(ce_status status) {
 int64_t ce_max_vocab(ce_dtype dtype) {
   const int es = elem_size(dtype);
   if (es == 0) return 0;
-  // 8 CTAs x 2048 register-resident chunks; a misaligned row straddles one more
-  const long long chunks = static_cast<long long>(ce::kMaxCluster) * 2048;
+  // 8 CTAs x one stage of at most kMaxSliceBytes; a misaligned row straddles one more chunk
+  const long long chunks = static_cast<long long>(ce::kMaxCluster) * (kMaxSliceBytes / 16);
   return (chunks - 2) * 16 / es;
 }
 

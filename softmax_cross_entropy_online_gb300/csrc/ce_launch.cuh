@@ -27,18 +27,24 @@ static const void* kptr_mode(int mode) {
   }
 }
 
-// Kernel entry for (T, mode, NC); NC is the number of consumer threads.
+// Kernel entry for (T, mode, variant); see kVariants.
 template <typename T>
-const void* rows_kernel_ptr(int mode, int NC) {
-  if (NC == 256) return kptr_mode<T, 256, 8>(mode);
-  if (NC == 512) return kptr_mode<T, 512, 4>(mode);
-  return nullptr;
+const void* rows_kernel_ptr(int mode, int variant) {
+  switch (variant) {
+    case 0: return kptr_mode<T, 256, 8>(mode);
+    case 1: return kptr_mode<T, 512, 4>(mode);
+    case 2: return kptr_mode<T, 128, 0>(mode);
+    case 3: return kptr_mode<T, 256, 0>(mode);
+    case 4: return kptr_mode<T, 512, 0>(mode);
+    default: return nullptr;
+  }
 }
 
 template <typename T>
-cudaError_t rows_launch(int mode, int NC, const RowParams& p, int grid, int smem_bytes,
+cudaError_t rows_launch(int mode, int variant, const RowParams& p, int grid, int smem_bytes,
                         cudaStream_t stream) {
-  const void* fn = rows_kernel_ptr<T>(mode, NC);
+  const void* fn = rows_kernel_ptr<T>(mode, variant);
+  const int NC = kVariants[variant].NC;
   if (fn == nullptr) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
   if (e != cudaSuccess) return e;
@@ -62,8 +68,10 @@ cudaError_t rows_launch(int mode, int NC, const RowParams& p, int grid, int smem
 
 // How many clusters (CTAs when CL == 1) of this kernel fit on the device at once.
 template <typename T>
-cudaError_t rows_max_active(int mode, int NC, int smem_bytes, int CL, int sm_count, int* out) {
-  const void* fn = rows_kernel_ptr<T>(mode, NC);
+cudaError_t rows_max_active(int mode, int variant, int smem_bytes, int CL, int sm_count,
+                            int* out) {
+  const void* fn = rows_kernel_ptr<T>(mode, variant);
+  const int NC = kVariants[variant].NC;
   if (fn == nullptr) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
   if (e != cudaSuccess) return e;

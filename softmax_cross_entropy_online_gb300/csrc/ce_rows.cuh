@@ -62,9 +62,13 @@ enum Mode : int { FWD = 0, FWD_BWD = 1, BWD = 2 };
 constexpr int kMaxStages = 16;
 constexpr int kMaxCluster = 8;
 
-// Chunks (16 B) each consumer thread keeps in registers, for the two
-// instantiated consumer sizes: both hold 2048 chunks (32 KB) per CTA.
-inline int cpt_for(int NC) { return NC == 256 ? 8 : (NC == 512 ? 4 : 0); }
+// The instantiated consumer shapes (NC consumer threads, CPT register-resident
+// 16-byte chunks per thread; CPT == 0 re-reads shared memory instead).
+struct Variant {
+  int NC, CPT;
+};
+constexpr Variant kVariants[] = {{256, 8}, {512, 4}, {128, 0}, {256, 0}, {512, 0}};
+constexpr int kNumVariants = 5;
 
 struct RowParams {
   char* base;                 // logits (byte address)
@@ -345,8 +349,18 @@ __device__ __forceinline__ void bulk_range(const UnitGeo& g, int& lo, int& hi) {
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
+// CPT > 0: each consumer thread keeps up to CPT full chunks of exp values in
+// registers (one exp2 per element).  CPT == 0: the stage in shared memory is
+// re-read for the backward (two exp2 per element, few registers, several CTAs
+// per SM, and no register limit on the slice length).
+template <int NC, int CPT>
+struct MinBlocks {
+  static constexpr int value = CPT > 0 ? 1 : (NC <= 128 ? 4 : (NC <= 256 ? 2 : 1));
+};
+
 template <typename T, int MODE, int NC, int CPT>
-__global__ void __launch_bounds__(NC + 32, 1) ce_rows_kernel(const RowParams p) {
+__global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
+    ce_rows_kernel(const RowParams p) {
   using E = Elem<T>;
   constexpr int EPC = E::EPC;
   constexpr int ES = E::ES;
@@ -438,6 +452,8 @@ __global__ void __launch_bounds__(NC + 32, 1) ce_rows_kernel(const RowParams p) 
   } else {
     // ======================= consumer warps =======================
     constexpr int LOG_ES = (ES == 4) ? 2 : 1;
+    constexpr bool RESIDENT = CPT > 0;  // keep exp values in registers (else re-read smem)
+    constexpr int KR = RESIDENT ? CPT : 1;
     const int R = p.R;
     const int GT = NC / R;     // threads per row group
     const int GW = GT / 32;    // warps per row group
@@ -468,13 +484,27 @@ __global__ void __launch_bounds__(NC + 32, 1) ce_rows_kernel(const RowParams p) 
       if (lo < g.w0) lo = g.w0;
       if (hi > g.w1) hi = g.w1;
       if (!row_ok) hi = lo;
+      // "full" chunks: interior (moved by TMA) with all EPC slots inside the row;
+      // the at most two edge chunks at either end, [lo, f0) and [f1, hi), are
+      // handled element by element by threads gt = 0, 1.
+      int f0 = (-d0 + 15) >> 4;
+      if (f0 < 1) f0 = 1;
+      int f1 = (rb - d0) >> 4;
+      if (f1 > g.nI + 1) f1 = g.nI + 1;
+      f0 = f0 < lo ? lo : (f0 > hi ? hi : f0);
+      f1 = f1 < f0 ? f0 : (f1 > hi ? hi : f1);
+      const int ce_front = (gt < f0 - lo) ? lo + gt : -1;  // this thread's edge chunks
+      const int ce_back = (gt < hi - f1) ? f1 + gt : -1;
       const uint32_t sbase = stage0 + s * p.stage_bytes - g.w0 * 16;  // chunk c at sbase + 16c
 
-      // target owner: the thread whose chunk holds x[row, t]
+      // target owner: the thread that processes the chunk holding x[row, t]
       const int tbo = t_ok ? static_cast<int>(t) * ES - d0 : 0;
       const int tc = t_ok ? (tbo >> 4) : -1;
       const bool t_smem = tc >= 1 && tc <= g.nI;
-      const bool owner = t_ok && tc >= lo && tc < hi && ((tc - lo) % GT) == gt;
+      bool owner = false;
+      if (t_ok && tc >= lo && tc < hi) {
+        owner = (tc < f0) ? (tc - lo == gt) : (tc >= f1 ? tc - f1 == gt : (tc - f0) % GT == gt);
+      }
 
       auto elem_ptr_global = [&](int e) -> char* {
         return reinterpret_cast<char*>(rs + static_cast<long long>(e) * ES);
@@ -482,68 +512,55 @@ __global__ void __launch_bounds__(NC + 32, 1) ce_rows_kernel(const RowParams p) 
       auto smem_ptr = [&](int byte_off) -> char* {
         return static_cast<char*>(__cvta_shared_to_generic(sbase + byte_off));
       };
-      // write EPC gradient values of chunk c (vector store when the chunk is
-      // whole, element stores at a row edge, global stores for head/tail)
-      auto store_chunk = [&](int c, const float* gv) {
+      // values of an edge chunk, -inf outside the row
+      auto edge_load = [&](int c, float* v) {
         const int e0 = (d0 + 16 * c) >> LOG_ES;
-        if (c >= 1 && c <= g.nI) {
-          if (e0 >= 0 && e0 + EPC <= V) {
-            sts128(sbase + 16 * c, E::pack(gv));
-          } else {
+        const bool in_smem = c >= 1 && c <= g.nI;
 #pragma unroll
-            for (int q = 0; q < EPC; ++q)
-              if (e0 + q >= 0 && e0 + q < V) E::st(smem_ptr(16 * c + q * ES), gv[q]);
+        for (int q = 0; q < EPC; ++q) {
+          const int e = e0 + q;
+          v[q] = (e >= 0 && e < V)
+                     ? (in_smem ? E::ld(smem_ptr(16 * c + q * ES)) : E::ld(elem_ptr_global(e)))
+                     : -INFINITY;
+        }
+      };
+      auto edge_store = [&](int c, const float* gv) {
+        const int e0 = (d0 + 16 * c) >> LOG_ES;
+        const bool in_smem = c >= 1 && c <= g.nI;
+#pragma unroll
+        for (int q = 0; q < EPC; ++q) {
+          const int e = e0 + q;
+          if (e >= 0 && e < V) {
+            if (in_smem) E::st(smem_ptr(16 * c + q * ES), gv[q]);
+            else E::st(elem_ptr_global(e), gv[q]);
           }
-        } else {
-#pragma unroll
-          for (int q = 0; q < EPC; ++q)
-            if (e0 + q >= 0 && e0 + q < V) E::st(elem_ptr_global(e0 + q), gv[q]);
         }
       };
 
       mbar_wait<false>(smem_u32(&full_bar[s]), static_cast<uint32_t>((i / S) & 1), p.err, failed,
                        WAIT_LIMIT_NS);
 
-      float v[CPT][EPC];
-#pragma unroll
-      for (int k = 0; k < CPT; ++k) {
-        const int c = lo + gt + k * GT;
-        if (c < hi) {
-          const int e0 = (d0 + 16 * c) >> LOG_ES;  // element index of the chunk's first slot
-          if (c >= 1 && c <= g.nI) {
-            E::unpack(lds128(sbase + 16 * c), v[k]);
-            if (e0 < 0 || e0 + EPC > V) {
-#pragma unroll
-              for (int q = 0; q < EPC; ++q)
-                if (e0 + q < 0 || e0 + q >= V) v[k][q] = -INFINITY;
-            }
-          } else {
-#pragma unroll
-            for (int q = 0; q < EPC; ++q)
-              v[k][q] = (e0 + q >= 0 && e0 + q < V) ? E::ld(elem_ptr_global(e0 + q)) : -INFINITY;
-          }
-        } else {
-#pragma unroll
-          for (int q = 0; q < EPC; ++q) v[k][q] = -INFINITY;
-        }
-      }
       float xt = 0.f;
       if (owner) xt = t_smem ? E::ld(smem_ptr(tbo)) : E::ld(elem_ptr_global(static_cast<int>(t)));
-      if (MODE == FWD) {
-        // the stage is no longer needed: hand it back to the producer early
-        mbar_arrive(smem_u32(&done_bar[s]));
-      }
 
       if (MODE == BWD) {
         const float sc = p.grad_scale;
+        for (int c = f0 + gt; c < f1; c += GT) {
+          float x[EPC], gv[EPC];
+          E::unpack(lds128(sbase + 16 * c), x);
 #pragma unroll
-        for (int k = 0; k < CPT; ++k) {
-          const int c = lo + gt + k * GT;
-          if (c < hi) {
-            float gv[EPC];
+          for (int q = 0; q < EPC; ++q) gv[q] = ex2((x[q] - lse_given) * kLog2e) * sc;
+          sts128(sbase + 16 * c, E::pack(gv));
+        }
 #pragma unroll
-            for (int q = 0; q < EPC; ++q) gv[q] = ex2((v[k][q] - lse_given) * kLog2e) * sc;
-            store_chunk(c, gv);
+        for (int h = 0; h < 2; ++h) {
+          const int c = h ? ce_back : ce_front;
+          if (c >= 0) {
+            float x[EPC], gv[EPC];
+            edge_load(c, x);
+#pragma unroll
+            for (int q = 0; q < EPC; ++q) gv[q] = ex2((x[q] - lse_given) * kLog2e) * sc;
+            edge_store(c, gv);
           }
         }
         if (owner) {
@@ -558,24 +575,76 @@ __global__ void __launch_bounds__(NC + 32, 1) ce_rows_kernel(const RowParams p) 
         continue;
       }
 
-      // ---- per-thread max, then one exp2 per element ----
+      // ---- per-thread max ----
+      float v[KR][EPC];
       float mt = -INFINITY;
+      if (RESIDENT) {
 #pragma unroll
-      for (int k = 0; k < CPT; ++k)
+        for (int k = 0; k < KR; ++k) {
+          const int c = f0 + gt + k * GT;
+          if (c < f1) {
+            E::unpack(lds128(sbase + 16 * c), v[k]);
+          } else {
 #pragma unroll
-        for (int q = 0; q < EPC; ++q) mt = fmaxf(mt, v[k][q]);
-      // differences first, then the scale to log2 units: exact for logits that
-      // share a large offset (shift invariance holds in fp32 too)
+            for (int q = 0; q < EPC; ++q) v[k][q] = -INFINITY;
+          }
+#pragma unroll
+          for (int q = 0; q < EPC; ++q) mt = fmaxf(mt, v[k][q]);
+        }
+      } else {
+        for (int c = f0 + gt; c < f1; c += GT) {
+          float x[EPC];
+          E::unpack(lds128(sbase + 16 * c), x);
+#pragma unroll
+          for (int q = 0; q < EPC; ++q) mt = fmaxf(mt, x[q]);
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int c = h ? ce_back : ce_front;
+        if (c >= 0) {
+          float x[EPC];
+          edge_load(c, x);
+#pragma unroll
+          for (int q = 0; q < EPC; ++q) mt = fmaxf(mt, x[q]);
+        }
+      }
+
+      // ---- one exp2 per element: e = exp(x - m_t), formed as (x - m_t) * log2 e so
+      // that logits sharing a large offset keep full fp32 accuracy ----
       const float mref = (mt == -INFINITY) ? 0.f : mt;
       float st = 0.f;
+      if (RESIDENT) {
 #pragma unroll
-      for (int k = 0; k < CPT; ++k)
+        for (int k = 0; k < KR; ++k)
 #pragma unroll
-        for (int q = 0; q < EPC; ++q) {
-          const float e = ex2((v[k][q] - mref) * kLog2e);
-          v[k][q] = e;
-          st += e;
+          for (int q = 0; q < EPC; ++q) {
+            const float e = ex2((v[k][q] - mref) * kLog2e);
+            v[k][q] = e;
+            st += e;
+          }
+      } else {
+        for (int c = f0 + gt; c < f1; c += GT) {
+          float x[EPC];
+          E::unpack(lds128(sbase + 16 * c), x);
+#pragma unroll
+          for (int q = 0; q < EPC; ++q) st += ex2((x[q] - mref) * kLog2e);
         }
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int c = h ? ce_back : ce_front;
+        if (c >= 0) {
+          float x[EPC];
+          edge_load(c, x);
+#pragma unroll
+          for (int q = 0; q < EPC; ++q) st += ex2((x[q] - mref) * kLog2e);
+        }
+      }
+      if (MODE == FWD) {
+        // every read of the stage is done: hand it back to the producer early
+        mbar_arrive(smem_u32(&done_bar[s]));
+      }
 
       // ---- merge (m, s): warp, then the row's warps ----
       float mw = mt;
@@ -643,14 +712,35 @@ __global__ void __launch_bounds__(NC + 32, 1) ce_rows_kernel(const RowParams p) 
         // g = e * exp(m_t - lse) * scale with exp(m_t - lse) = 2^((m_t - M) log2 e - log2 S)
         const float sc = p.grad_scale;
         const float f = ex2((mt - Mg) * kLog2e - lg2(Sg)) * sc;
+        if (RESIDENT) {
 #pragma unroll
-        for (int k = 0; k < CPT; ++k) {
-          const int c = lo + gt + k * GT;
-          if (c < hi) {
-            float gv[EPC];
+          for (int k = 0; k < KR; ++k) {
+            const int c = f0 + gt + k * GT;
+            if (c < f1) {
+              float gv[EPC];
 #pragma unroll
-            for (int q = 0; q < EPC; ++q) gv[q] = v[k][q] * f;
-            store_chunk(c, gv);
+              for (int q = 0; q < EPC; ++q) gv[q] = v[k][q] * f;
+              sts128(sbase + 16 * c, E::pack(gv));
+            }
+          }
+        } else {
+          for (int c = f0 + gt; c < f1; c += GT) {
+            float x[EPC], gv[EPC];
+            E::unpack(lds128(sbase + 16 * c), x);
+#pragma unroll
+            for (int q = 0; q < EPC; ++q) gv[q] = ex2((x[q] - mref) * kLog2e) * f;
+            sts128(sbase + 16 * c, E::pack(gv));
+          }
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int c = h ? ce_back : ce_front;
+          if (c >= 0) {
+            float x[EPC], gv[EPC];
+            edge_load(c, x);
+#pragma unroll
+            for (int q = 0; q < EPC; ++q) gv[q] = ex2((x[q] - mref) * kLog2e) * f;
+            edge_store(c, gv);
           }
         }
         if (owner) {

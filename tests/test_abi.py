@@ -66,8 +66,10 @@ def test_status_strings(cdll):
 
 def test_max_vocab(cdll):
     assert cdll.ce_max_vocab(0) * 4 == cdll.ce_max_vocab(1) * 2 == cdll.ce_max_vocab(2) * 2
-    # 8 CTAs x 2048 chunks of 16 B, less one chunk of slack for a misaligned row
-    assert cdll.ce_max_vocab(1) == (8 * 2048 - 2) * 8 and cdll.ce_max_vocab(0) == (8 * 2048 - 2) * 4
+    # 8 CTAs x one 200 KB stage of 16-byte chunks, less two chunks of slack for a
+    # misaligned row
+    chunks = 8 * (200 * 1024 // 16) - 2
+    assert cdll.ce_max_vocab(1) == chunks * 8 and cdll.ce_max_vocab(0) == chunks * 4
     assert cdll.ce_max_vocab(7) == 0
 
 
