@@ -244,6 +244,13 @@ ce_status launch_rows(int mode, const void* logits, const int64_t* targets, cons
   p.CL = pl.CL;
   p.S = pl.S;
   p.stage_bytes = pl.stage_bytes;
+  p.q_chunks = pl.stage_bytes / 16;
+  {
+    const int GT = ce::kVariants[pl.variant].NC / pl.R;  // a power of two
+    int lg = 0;
+    while ((1 << lg) < GT) ++lg;
+    p.log_gt = lg;
+  }
   p.n_units = (M + pl.R - 1) / pl.R;
   p.grad_scale = grad_scale;
   p.mean = (red == CE_RED_MEAN) ? 1 : 0;

@@ -87,6 +87,8 @@ struct RowParams {
   int CL;                     // CTAs per cluster
   int S;                      // pipeline stages
   int stage_bytes;            // bytes of one stage (multiple of 16)
+  int q_chunks;               // chunk window of one CTA per unit (stage_bytes / 16)
+  int log_gt;                 // log2 of the consumer threads per row group
   float grad_scale;           // FWD_BWD / BWD
   int mean;                   // 1: loss = sum / M, 0: loss = sum
 };
@@ -320,7 +322,7 @@ struct UnitGeo {
 
 __device__ __forceinline__ UnitGeo unit_geo(const RowParams& p, long long u, int rank) {
   UnitGeo g;
-  g.row0 = u * p.R;
+  g.row0 = u * p.R;  // the host guarantees CL * q_chunks covers every unit's chunks
   long long rows = p.M - g.row0;
   g.rows = static_cast<int>(rows < p.R ? rows : p.R);
   g.as = reinterpret_cast<long long>(p.base) + g.row0 * p.row_bytes;
@@ -331,8 +333,7 @@ __device__ __forceinline__ UnitGeo unit_geo(const RowParams& p, long long u, int
   g.nI = static_cast<int>((A1 - g.A0) >> 4);
   const int c_first = (g.as < g.A0) ? 0 : 1;
   const int c_last = (ae > A1) ? g.nI + 1 : g.nI;
-  const int nC = c_last - c_first + 1;
-  const int Q = (nC + p.CL - 1) / p.CL;
+  const int Q = p.q_chunks;
   g.w0 = c_first + rank * Q;
   int w1 = g.w0 + Q;
   g.w1 = w1 < c_last + 1 ? w1 : c_last + 1;
@@ -406,8 +407,7 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
     // and a stage is refilled LAG units later, once its store has been read
     // out of shared memory, so a store never stalls the next load.
     if (lane == 0) {
-      auto issue_load = [&](long long i) {
-        const int s = static_cast<int>(i % S);
+      auto issue_load = [&](long long i, int s) {
         const UnitGeo g = unit_geo(p, cid + i * ncl, rank);
         int lo, hi;
         bulk_range(g, lo, hi);
@@ -423,14 +423,17 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
         }
       };
       const long long pre = n_iter < S ? n_iter : S;
-      for (long long i = 0; i < pre; ++i) issue_load(i);
-      const int lag = (S >= 3) ? 2 : 1;
+      for (long long i = 0; i < pre; ++i) issue_load(i, static_cast<int>(i));
+      // a stage is refilled `lag` units after its store was issued; the refill
+      // brings unit r + S, which must be a unit not yet loaded: lag <= S - 1
+      const int lag = (S >= 3) ? 2 : S - 1;
+      int s = 0, sr = S - lag;  // stages of unit j and of unit j - lag (mod S)
+      if (sr == S) sr = 0;
+      uint32_t phase = 0;
       for (long long j = 0; j < n_iter; ++j) {
-        const int s = static_cast<int>(j % S);
-        mbar_wait<false>(smem_u32(&done_bar[s]), static_cast<uint32_t>((j / S) & 1), p.err,
-                         failed, WAIT_LIMIT_NS);
+        mbar_wait<false>(smem_u32(&done_bar[s]), phase, p.err, failed, WAIT_LIMIT_NS);
         if (MODE == FWD) {
-          if (j + S < n_iter) issue_load(j + S);
+          if (j + S < n_iter) issue_load(j + S, s);
         } else {
           const UnitGeo go = unit_geo(p, cid + j * ncl, rank);
           int lo, hi;
@@ -442,10 +445,13 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
           const long long r = j - lag;
           if (r >= 0 && r + S < n_iter) {
             if (lag == 2) bulk_wait_read<2>();
-            else bulk_wait_read<1>();
-            issue_load(r + S);
+            else if (lag == 1) bulk_wait_read<1>();
+            else bulk_wait_read<0>();
+            issue_load(r + S, sr);
           }
         }
+        if (++s == S) { s = 0; phase ^= 1u; }
+        if (++sr == S) sr = 0;
       }
       if (MODE != FWD) bulk_wait_all();
     }
@@ -457,15 +463,18 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
     const int R = p.R;
     const int GT = NC / R;     // threads per row group
     const int GW = GT / 32;    // warps per row group
-    const int grp = tid / GT;  // row of the unit this thread works on
-    const int gt = tid - grp * GT;
+    const int grp = tid >> p.log_gt;  // row of the unit this thread works on
+    const int gt = tid & (GT - 1);
     const int V = static_cast<int>(p.V);          // the host caps V * sizeof(T) far below 2^31
     const int rb = static_cast<int>(p.row_bytes);
     double acc = 0.0;  // this group's running loss sum (leader only)
     const bool leader = (gt == 0) && (rank == 0);
 
+    int s = -1;
+    uint32_t phase = 1;
     for (long long i = 0; i < n_iter; ++i) {
-      const int s = static_cast<int>(i % S);
+      if (++s == S) s = 0;
+      if (s == 0) phase ^= 1u;
       const int b = static_cast<int>(i & 1);
       const UnitGeo g = unit_geo(p, cid + i * ncl, rank);
       const bool row_ok = grp < g.rows;
@@ -503,7 +512,7 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
       const bool t_smem = tc >= 1 && tc <= g.nI;
       bool owner = false;
       if (t_ok && tc >= lo && tc < hi) {
-        owner = (tc < f0) ? (tc - lo == gt) : (tc >= f1 ? tc - f1 == gt : (tc - f0) % GT == gt);
+        owner = (tc < f0) ? (tc - lo == gt) : (tc >= f1 ? tc - f1 == gt : ((tc - f0) & (GT - 1)) == gt);
       }
 
       auto elem_ptr_global = [&](int e) -> char* {
@@ -537,8 +546,7 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
         }
       };
 
-      mbar_wait<false>(smem_u32(&full_bar[s]), static_cast<uint32_t>((i / S) & 1), p.err, failed,
-                       WAIT_LIMIT_NS);
+      mbar_wait<false>(smem_u32(&full_bar[s]), phase, p.err, failed, WAIT_LIMIT_NS);
 
       float xt = 0.f;
       if (owner) xt = t_smem ? E::ld(smem_ptr(tbo)) : E::ld(elem_ptr_global(static_cast<int>(t)));

@@ -301,3 +301,14 @@ def test_large_workloads_sampled(name):
     x, t = synthetic.make_workload(w)
     rows = P.sample_rows(w.M, 128)
     check_case(x, t, w.dtype, rows=rows)
+
+
+@pytest.mark.parametrize("plan", ["3,1,1,1", "2,2,1,1", "0,1,1,1", "3,1,2,1"])
+def test_single_stage_pipeline_many_units_per_cta(plan, monkeypatch):
+    # one stage: every refill waits for the previous store to be read out;
+    # enough rows that each CTA runs many units
+    monkeypatch.setenv("CE_PLAN", plan)
+    M, V = 20000, 1000
+    x = synthetic.make_logits(M, V, "f32", 2.0, seed=77)
+    t = synthetic.make_targets(M, V, seed=78)
+    check_case(x, t, "f32", rows=P.sample_rows(M, 400))
