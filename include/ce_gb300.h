@@ -95,6 +95,37 @@ ce_status ce_fwd_bwd_inplace(void* logits, const int64_t* targets, int64_t M, in
                              float* row_loss, float* lse, void* stream);
 
 /*
+ * ce_fwd_bwd_inplace_noalloc -- ce_fwd_bwd_inplace for callers that must not
+ * allocate device memory.  (The source pages have no counterpart; this is a
+ * deployment variant of the fused kernel.)
+ *
+ * Who needs it: a caller whose allocator owns the whole device memory budget
+ * and forbids stray allocations, or one that cannot afford the implicit
+ * device synchronisation a cudaMalloc/cudaFree may cause in a timed loop.
+ * ce_fwd_bwd_inplace creates a small reduction buffer with cudaMalloc on the
+ * first reducing call on each stream; this entry point never calls
+ * cudaMalloc, cudaFree or any other allocating routine.
+ *
+ * Same arguments, results and errors as ce_fwd_bwd_inplace.  The reduction
+ * scratch is a fixed array inside the library's device code (one fp64
+ * partial sum per CTA, at most 1024 CTAs, about 8 KB), held by every device
+ * that loads the library until the process exits.  A launch that would need
+ * more than 1024 CTAs returns CE_ERR_UNSUPPORTED (no GB300 launch shape does).
+ *
+ *  - Set-up: the first call on each device (with that device current) looks
+ *    up the array's device address once; make that first call before any
+ *    stream capture.
+ *  - Every call on a device shares the one array.  Each call clears its
+ *    counter on `stream` before the launch, so a call never depends on the
+ *    previous call's leftovers, but calls whose executions overlap on the GPU
+ *    (different streams, no ordering between them) race and can produce a
+ *    wrong loss.  Order them on one stream or with events.
+ */
+ce_status ce_fwd_bwd_inplace_noalloc(void* logits, const int64_t* targets, int64_t M, int64_t V,
+                                     ce_dtype dtype, ce_reduction reduction, float* loss,
+                                     float* row_loss, float* lse, void* stream);
+
+/*
  * ce_backward_from_lse -- gradient only, from a stored per-row lse:
  * g = (exp(x - lse_i) - onehot) * scale written over the logits.  Use it
  * when the forward ran earlier (ce_forward with lse != NULL); `scale` is

@@ -9,7 +9,8 @@ The binding (``api``) needs torch and the in-tree library built by
 """
 
 __all__ = [
-    "ce_forward", "ce_fwd_bwd_inplace", "ce_backward_from_lse", "ce_check_errors",
+    "ce_forward", "ce_fwd_bwd_inplace", "ce_fwd_bwd_inplace_noalloc", "ce_backward_from_lse",
+    "ce_check_errors",
     "ce_max_vocab", "ce_launch_count", "ce_selftest_wait_timeout", "CEError",
 ]
 

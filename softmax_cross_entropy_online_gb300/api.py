@@ -31,6 +31,7 @@ _vp, _i64, _i32, _f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_
 SIGNATURES = {
     "ce_forward": (_i32, [_vp, _vp, _i64, _i64, _i32, _i32, _vp, _vp, _vp, _vp]),
     "ce_fwd_bwd_inplace": (_i32, [_vp, _vp, _i64, _i64, _i32, _i32, _vp, _vp, _vp, _vp]),
+    "ce_fwd_bwd_inplace_noalloc": (_i32, [_vp, _vp, _i64, _i64, _i32, _i32, _vp, _vp, _vp, _vp]),
     "ce_backward_from_lse": (_i32, [_vp, _vp, _vp, _i64, _i64, _i32, _f32, _vp]),
     "ce_check_errors": (_i32, [_vp, _i32]),
     "ce_status_string": (ctypes.c_char_p, [_i32]),
@@ -130,6 +131,27 @@ def ce_fwd_bwd_inplace(logits: torch.Tensor, targets: torch.Tensor, reduction: s
                                   _ptr(rl_t), _ptr(lse_t), _stream_handle(stream, logits.device))
     _check(st, "ce_fwd_bwd_inplace")
     return loss_t, rl_t, lse_t
+
+
+def ce_fwd_bwd_inplace_noalloc(logits: torch.Tensor, targets: torch.Tensor,
+                               reduction: str = "mean", *, loss: torch.Tensor | None = None,
+                               row_loss: torch.Tensor | None = None,
+                               lse: torch.Tensor | None = None, stream=None):
+    """ce_fwd_bwd_inplace for callers that cannot allocate device memory: the
+    library allocates nothing, and the caller passes every output buffer
+    (fp32 loss [], row_loss [M], lse [M]; any may be None).  Returns them."""
+    _check_inputs(logits, targets)
+    M, V = logits.shape
+    for t_, n in ((loss, 1), (row_loss, M), (lse, M)):
+        if t_ is not None and (not t_.is_cuda or t_.dtype != torch.float32
+                               or t_.numel() != n or not t_.is_contiguous()):
+            raise ValueError("outputs must be contiguous fp32 CUDA tensors of the right size")
+    st = lib().ce_fwd_bwd_inplace_noalloc(logits.data_ptr(), targets.data_ptr(), M, V,
+                                          _DTYPES[logits.dtype], _REDUCTIONS[reduction],
+                                          _ptr(loss), _ptr(row_loss), _ptr(lse),
+                                          _stream_handle(stream, logits.device))
+    _check(st, "ce_fwd_bwd_inplace_noalloc")
+    return loss, row_loss, lse
 
 
 def ce_backward_from_lse(logits: torch.Tensor, targets: torch.Tensor, lse: torch.Tensor,

@@ -196,9 +196,45 @@ void apply_env_plan(long long rb, bool aligned, Plan& pl) {
   pl = Plan{var, R, CL, S, static_cast<int>(stage)};
 }
 
+// ---------------------------------------------------------------------------
+// Reduction scratch for ce_fwd_bwd_inplace_noalloc.  It lives in the module's
+// own device memory (a file-scope array), so that entry point never allocates:
+// the first 256 bytes hold the ticket, then one fp64 partial sum per CTA.
+// Every device that loads this library holds it until the process exits.
+// ---------------------------------------------------------------------------
+constexpr int kNoAllocPartials = 1024;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[256 + sizeof(double) * kNoAllocPartials];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_base[kMaxDevices] = {};
+
+// The array's device address for the current device.  Host code only knows
+// a host-side stand-in for the symbol, so the address is looked up once per
+// device (with that device current) and kept.
+ce_status noalloc_scratch(Scratch& out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return CE_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return CE_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (g_noalloc_base[dev] == nullptr) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr)
+      return CE_ERR_CUDA;
+    g_noalloc_base[dev] = ptr;
+  }
+  char* base = static_cast<char*>(g_noalloc_base[dev]);
+  out.ticket = reinterpret_cast<unsigned int*>(base);
+  out.partials = reinterpret_cast<double*>(base + 256);
+  return CE_OK;
+}
+
+// static_scratch: reduce through g_noalloc_scratch (its ticket is cleared on
+// the stream before the launch) instead of the per-stream buffer.
 ce_status launch_rows(int mode, const void* logits, const int64_t* targets, const float* lse_in,
                       int64_t M, int64_t V, ce_dtype dtype, ce_reduction red, float* loss,
-                      float* row_loss, float* lse_out, float grad_scale, void* stream) {
+                      float* row_loss, float* lse_out, float grad_scale, void* stream,
+                      bool static_scratch = false) {
   const int es = elem_size(dtype);
   if (es == 0) return CE_ERR_INVALID_ARG;
   if (red != CE_RED_MEAN && red != CE_RED_SUM && red != CE_RED_NONE) return CE_ERR_INVALID_ARG;
@@ -268,7 +304,17 @@ ce_status launch_rows(int mode, const void* logits, const int64_t* targets, cons
   if (nclusters < 1) nclusters = 1;  // M == 0: one cluster writes the empty reduction
   const int grid = static_cast<int>(nclusters * pl.CL);
 
-  if (loss != nullptr) {
+  if (loss != nullptr && static_scratch) {
+    if (grid > kNoAllocPartials) return CE_ERR_UNSUPPORTED;
+    Scratch sc;
+    st = noalloc_scratch(sc);
+    if (st != CE_OK) return st;
+    if (cudaMemsetAsync(sc.ticket, 0, sizeof(unsigned int), static_cast<cudaStream_t>(stream)) !=
+        cudaSuccess)
+      return CE_ERR_CUDA;
+    p.partials = sc.partials;
+    p.ticket = sc.ticket;
+  } else if (loss != nullptr) {
     if (grid > kScratchPartials) return CE_ERR_UNSUPPORTED;
     Scratch sc;
     st = scratch_for(dev, stream, sc);
@@ -305,6 +351,14 @@ ce_status ce_fwd_bwd_inplace(void* logits, const int64_t* targets, int64_t M, in
   const float scale = (reduction == CE_RED_MEAN && M > 0) ? 1.0f / static_cast<float>(M) : 1.0f;
   return launch_rows(ce::FWD_BWD, logits, targets, nullptr, M, V, dtype, reduction, loss,
                      row_loss, lse, scale, stream);
+}
+
+ce_status ce_fwd_bwd_inplace_noalloc(void* logits, const int64_t* targets, int64_t M, int64_t V,
+                                     ce_dtype dtype, ce_reduction reduction, float* loss,
+                                     float* row_loss, float* lse, void* stream) {
+  const float scale = (reduction == CE_RED_MEAN && M > 0) ? 1.0f / static_cast<float>(M) : 1.0f;
+  return launch_rows(ce::FWD_BWD, logits, targets, nullptr, M, V, dtype, reduction, loss,
+                     row_loss, lse, scale, stream, /*static_scratch=*/true);
 }
 
 ce_status ce_backward_from_lse(void* logits, const int64_t* targets, const float* lse, int64_t M,
