@@ -138,18 +138,19 @@ long long stage_bytes_for(int variant, int R, int CL, long long rb, bool aligned
   return per_cta * 16;
 }
 
-// Default launch shape: the shared-memory streaming consumers (variant 3, 256
-// threads) with two CTAs per SM.  Rows of up to 32 KB are packed R per unit in
-// one CTA; longer rows are split over a cluster of up to 8 CTAs.
+// Default launch shape (from sweeps on GB300): the shared-memory streaming
+// consumers (variant 3, 256 threads), about 64 KB of stages per CTA so three
+// CTAs share an SM.  Rows of up to 32 KB are packed R per unit in one CTA with
+// ~4 chunks per thread and pass; longer rows are split over a cluster of up to
+// 8 CTAs with two stages each.
 bool choose_plan(long long rb, bool aligned, long long M, int sm_count, Plan& pl) {
   const int variant = 3;
   const int NC = ce::kVariants[variant].NC;
-  const long long per_cta_smem = 96 * 1024;
+  const long long per_cta_smem = 64 * 1024;
   const long long cpr = chunks_for(rb, aligned);
   if (cpr * 16 <= 32 * 1024) {
-    // about 8 chunks per thread and pass: GT = cpr / 8 rounded up to a power of two
     int GT = 32;
-    while (GT < NC && static_cast<long long>(GT) * 8 < cpr) GT *= 2;
+    while (GT < NC && static_cast<long long>(GT) * 4 < cpr) GT *= 2;
     int R = NC / GT;
     while (R > 1 && (M + R - 1) / R < 2LL * sm_count) R /= 2;
     for (; R >= 1; R /= 2) {
@@ -166,19 +167,14 @@ bool choose_plan(long long rb, bool aligned, long long M, int sm_count, Plan& pl
   for (int CL = 2; CL <= ce::kMaxCluster; ++CL) {
     const long long stage = stage_bytes_for(variant, 1, CL, rb, aligned);
     if (stage == 0 || stage > 32 * 1024) continue;
-    long long S = per_cta_smem / stage;
-    if (S > ce::kMaxStages) S = ce::kMaxStages;
-    pl = Plan{variant, 1, CL, static_cast<int>(S), static_cast<int>(stage)};
+    pl = Plan{variant, 1, CL, 2, static_cast<int>(stage)};
     return true;
   }
   // very long rows: 8 CTAs, larger slices, fewer stages
   const long long stage = stage_bytes_for(variant, 1, ce::kMaxCluster, rb, aligned);
   if (stage == 0 || stage > kMaxSliceBytes) return false;
-  long long S = (2 * per_cta_smem) / stage;
-  if (S < 1) S = 1;
-  if (S > 2) S = 2;
-  if (S * stage > 220 * 1024) S = 1;
-  pl = Plan{variant, 1, ce::kMaxCluster, static_cast<int>(S), static_cast<int>(stage)};
+  const int S = (2 * stage <= 220 * 1024) ? 2 : 1;
+  pl = Plan{variant, 1, ce::kMaxCluster, S, static_cast<int>(stage)};
   return true;
 }
 

@@ -318,6 +318,8 @@ struct UnitGeo {
   long long A0;     // ceil16(as): start of interior chunk 1
   int nI;           // interior chunks (1..nI)
   int w0, w1;       // this CTA's chunk window [w0, w1)
+  bool head_ok;     // the partial head chunk 0 lies inside the tensor: load it by TMA
+  bool tail_ok;     // the partial tail chunk nI + 1 lies inside the tensor: load it by TMA
 };
 
 __device__ __forceinline__ UnitGeo unit_geo(const RowParams& p, long long u, int rank) {
@@ -333,6 +335,13 @@ __device__ __forceinline__ UnitGeo unit_geo(const RowParams& p, long long u, int
   g.nI = static_cast<int>((A1 - g.A0) >> 4);
   const int c_first = (g.as < g.A0) ? 0 : 1;
   const int c_last = (ae > A1) ? g.nI + 1 : g.nI;
+  // A partial chunk also holds bytes of the neighbouring unit.  Reading those
+  // (and ignoring them) is harmless as long as the 16 bytes lie inside the
+  // tensor; writes to a partial chunk are always element by element.
+  const long long base = reinterpret_cast<long long>(p.base);
+  const long long end = base + p.M * p.row_bytes;
+  g.head_ok = c_first == 0 && g.A0 - 16 >= base && g.A0 <= end;
+  g.tail_ok = c_last == g.nI + 1 && A1 + 16 <= end;
   const int Q = p.q_chunks;
   g.w0 = c_first + rank * Q;
   int w1 = g.w0 + Q;
@@ -341,10 +350,18 @@ __device__ __forceinline__ UnitGeo unit_geo(const RowParams& p, long long u, int
   return g;
 }
 
-// interior chunk range [lo, hi) of this CTA's window, moved by TMA
+// chunk range [lo, hi) of this CTA's window written back by TMA: the interior
 __device__ __forceinline__ void bulk_range(const UnitGeo& g, int& lo, int& hi) {
   lo = g.w0 > 1 ? g.w0 : 1;
   hi = g.w1 < g.nI + 1 ? g.w1 : g.nI + 1;
+}
+// chunk range read by TMA: the interior plus the partial head/tail chunks
+// that lie inside the tensor
+__device__ __forceinline__ void load_range(const UnitGeo& g, int& lo, int& hi) {
+  const int l = g.head_ok ? 0 : 1;
+  const int h = g.tail_ok ? g.nI + 2 : g.nI + 1;
+  lo = g.w0 > l ? g.w0 : l;
+  hi = g.w1 < h ? g.w1 : h;
 }
 
 // ---------------------------------------------------------------------------
@@ -410,7 +427,7 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
       auto issue_load = [&](long long i, int s) {
         const UnitGeo g = unit_geo(p, cid + i * ncl, rank);
         int lo, hi;
-        bulk_range(g, lo, hi);
+        load_range(g, lo, hi);
         const uint32_t fb = smem_u32(&full_bar[s]);
         fence_proxy_async_smem();
         if (hi > lo) {
@@ -472,6 +489,17 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
 
     int s = -1;
     uint32_t phase = 1;
+    // the target (and, for BWD, the lse) of the next unit's row is fetched one
+    // unit ahead, so its global-memory latency hides behind this unit's work
+    long long t_next = -1;
+    float lse_next = 0.f;
+    {
+      const long long row_first = cid * R + grp;
+      if (n_iter > 0 && row_first < p.M) {
+        t_next = __ldg(p.targets + row_first);
+        if (MODE == BWD) lse_next = __ldg(p.lse_in + row_first);
+      }
+    }
     for (long long i = 0; i < n_iter; ++i) {
       if (++s == S) s = 0;
       if (s == 0) phase ^= 1u;
@@ -479,9 +507,15 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
       const UnitGeo g = unit_geo(p, cid + i * ncl, rank);
       const bool row_ok = grp < g.rows;
       const long long row = g.row0 + grp;
-      const long long t = row_ok ? __ldg(p.targets + row) : -1;
-      float lse_given = 0.f;
-      if (MODE == BWD && row_ok) lse_given = __ldg(p.lse_in + row);
+      const long long t = row_ok ? t_next : -1;
+      const float lse_given = lse_next;
+      if (i + 1 < n_iter) {
+        const long long row_n = (cid + (i + 1) * ncl) * R + grp;
+        if (row_n < p.M) {
+          t_next = __ldg(p.targets + row_n);
+          if (MODE == BWD) lse_next = __ldg(p.lse_in + row_n);
+        }
+      }
       const bool t_ok = row_ok && t >= 0 && t < V;
 
       // Offsets are taken from the start of chunk 0 (absolute A0 - 16):
@@ -509,7 +543,11 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
       // target owner: the thread that processes the chunk holding x[row, t]
       const int tbo = t_ok ? static_cast<int>(t) * ES - d0 : 0;
       const int tc = t_ok ? (tbo >> 4) : -1;
-      const bool t_smem = tc >= 1 && tc <= g.nI;
+      const bool t_smem = tc >= 1 && tc <= g.nI;  // written back through shared memory
+      // chunk c's bytes are in the stage (interior, or a partial chunk loaded by TMA)
+      auto in_stage = [&](int c) -> bool {
+        return (c >= 1 && c <= g.nI) || (c == 0 && g.head_ok) || (c == g.nI + 1 && g.tail_ok);
+      };
       bool owner = false;
       if (t_ok && tc >= lo && tc < hi) {
         owner = (tc < f0) ? (tc - lo == gt) : (tc >= f1 ? tc - f1 == gt : ((tc - f0) & (GT - 1)) == gt);
@@ -524,7 +562,7 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
       // values of an edge chunk, -inf outside the row
       auto edge_load = [&](int c, float* v) {
         const int e0 = (d0 + 16 * c) >> LOG_ES;
-        const bool in_smem = c >= 1 && c <= g.nI;
+        const bool in_smem = in_stage(c);
 #pragma unroll
         for (int q = 0; q < EPC; ++q) {
           const int e = e0 + q;
@@ -549,7 +587,8 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
       mbar_wait<false>(smem_u32(&full_bar[s]), phase, p.err, failed, WAIT_LIMIT_NS);
 
       float xt = 0.f;
-      if (owner) xt = t_smem ? E::ld(smem_ptr(tbo)) : E::ld(elem_ptr_global(static_cast<int>(t)));
+      if (owner)
+        xt = in_stage(tc) ? E::ld(smem_ptr(tbo)) : E::ld(elem_ptr_global(static_cast<int>(t)));
 
       if (MODE == BWD) {
         const float sc = p.grad_scale;
