@@ -373,7 +373,9 @@ __device__ __forceinline__ void load_range(const UnitGeo& g, int& lo, int& hi) {
 // per SM, and no register limit on the slice length).
 template <int NC, int CPT>
 struct MinBlocks {
-  static constexpr int value = CPT > 0 ? 1 : (NC <= 128 ? 4 : (NC <= 256 ? 2 : 1));
+  // streaming consumers: registers capped so that 5 (128 threads) or 3 (256
+  // threads) CTAs fit on an SM; occupancy hides each CTA's per-unit latency
+  static constexpr int value = CPT > 0 ? 1 : (NC <= 128 ? 5 : (NC <= 256 ? 3 : 1));
 };
 
 template <typename T, int MODE, int NC, int CPT>
