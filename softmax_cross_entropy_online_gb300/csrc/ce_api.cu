@@ -225,6 +225,17 @@ ce_status noalloc_scratch(Scratch& out) {
   return CE_OK;
 }
 
+// Suspend-time hint of the kernels' mbarrier waits (ns); CE_WAIT_HINT_NS
+// overrides it for tuning sweeps.
+unsigned int wait_hint_ns() {
+  static const unsigned int hint = [] {
+    const char* env = std::getenv("CE_WAIT_HINT_NS");
+    long v = env ? std::strtol(env, nullptr, 10) : 0;
+    return (v > 0 && v <= 1000000) ? static_cast<unsigned int>(v) : 20000u;
+  }();
+  return hint;
+}
+
 // static_scratch: reduce through g_noalloc_scratch (its ticket is cleared on
 // the stream before the launch) instead of the per-stream buffer.
 ce_status launch_rows(int mode, const void* logits, const int64_t* targets, const float* lse_in,
@@ -277,6 +288,7 @@ ce_status launch_rows(int mode, const void* logits, const int64_t* targets, cons
   p.S = pl.S;
   p.stage_bytes = pl.stage_bytes;
   p.q_chunks = pl.stage_bytes / 16;
+  p.wait_hint_ns = wait_hint_ns();
   {
     const int GT = ce::kVariants[pl.variant].NC / pl.R;  // a power of two
     int lg = 0;

@@ -89,6 +89,7 @@ struct RowParams {
   int stage_bytes;            // bytes of one stage (multiple of 16)
   int q_chunks;               // chunk window of one CTA per unit (stage_bytes / 16)
   int log_gt;                 // log2 of the consumer threads per row group
+  unsigned int wait_hint_ns;  // suspend-time hint of the mbarrier waits
   float grad_scale;           // FWD_BWD / BWD
   int mean;                   // 1: loss = sum / M, 0: loss = sum
 };
@@ -120,22 +121,27 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_cluster_addr) {
                    bar_cluster_addr)
                : "memory");
 }
+// try_wait with a suspend-time hint: a waiting thread sleeps (up to hint_ns)
+// until the phase completes instead of spinning and taking issue slots from
+// the warps that are computing.
 template <bool kClusterScope>
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
   uint32_t ok;
   if (kClusterScope) {
     asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+        "{\n .reg .pred p;\n"
+        " mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n"
         " selp.u32 %0, 1, 0, p;\n}\n"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
         : "memory");
   } else {
     asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+        "{\n .reg .pred p;\n"
+        " mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n"
         " selp.u32 %0, 1, 0, p;\n}\n"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
         : "memory");
   }
   return ok != 0;
@@ -144,11 +150,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // only poll once, so a launch that lost a barrier still ends promptly.
 template <bool kClusterScope>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned int* err,
-                                          bool& failed, unsigned long long limit_ns) {
-  if (mbar_try_wait<kClusterScope>(bar, parity)) return true;
+                                          bool& failed, unsigned long long limit_ns,
+                                          uint32_t hint_ns = 20000u) {
+  if (mbar_try_wait<kClusterScope>(bar, parity, hint_ns)) return true;
   if (failed) return false;
   const unsigned long long t0 = global_timer_ns();
-  while (!mbar_try_wait<kClusterScope>(bar, parity)) {
+  while (!mbar_try_wait<kClusterScope>(bar, parity, hint_ns)) {
     if (global_timer_ns() - t0 > limit_ns) {
       atomicOr(err, ERR_WAIT_TIMEOUT);
       failed = true;
@@ -450,7 +457,7 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
       if (sr == S) sr = 0;
       uint32_t phase = 0;
       for (long long j = 0; j < n_iter; ++j) {
-        mbar_wait<false>(smem_u32(&done_bar[s]), phase, p.err, failed, WAIT_LIMIT_NS);
+        mbar_wait<false>(smem_u32(&done_bar[s]), phase, p.err, failed, WAIT_LIMIT_NS, p.wait_hint_ns);
         if (MODE == FWD) {
           if (j + S < n_iter) issue_load(j + S, s);
         } else {
@@ -586,7 +593,7 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
         }
       };
 
-      mbar_wait<false>(smem_u32(&full_bar[s]), phase, p.err, failed, WAIT_LIMIT_NS);
+      mbar_wait<false>(smem_u32(&full_bar[s]), phase, p.err, failed, WAIT_LIMIT_NS, p.wait_hint_ns);
 
       float xt = 0.f;
       if (owner)
@@ -728,7 +735,7 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
           }
         }
         mbar_wait<true>(smem_u32(&xbar[b]), static_cast<uint32_t>((i >> 1) & 1), p.err, failed,
-                        WAIT_LIMIT_NS);
+                        WAIT_LIMIT_NS, p.wait_hint_ns);
         float4 xs = (lane < CL) ? xslot[b][lane] : make_float4(-INFINITY, 0.f, 0.f, 0.f);
         float Mc = xs.x;
 #pragma unroll
