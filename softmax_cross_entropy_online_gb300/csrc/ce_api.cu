@@ -47,7 +47,6 @@ namespace {
 
 std::atomic<uint64_t> g_launches{0};
 
-constexpr int kSmemBudget = 200 * 1024;  // dynamic shared memory per CTA for the stages
 constexpr int kScratchPartials = 8192;   // > any persistent grid (152 SMs x 4 CTAs)
 
 struct DeviceInfo {
@@ -143,14 +142,16 @@ long long stage_bytes_for(int variant, int R, int CL, long long rb, bool aligned
 // CTAs share an SM.  Rows of up to 32 KB are packed R per unit in one CTA with
 // ~4 chunks per thread and pass; longer rows are split over a cluster of up to
 // 8 CTAs with two stages each.
-bool choose_plan(long long rb, bool aligned, long long M, int sm_count, Plan& pl) {
+bool choose_plan(long long rb, int es, bool aligned, long long M, int sm_count, Plan& pl) {
   const int variant = 3;
   const int NC = ce::kVariants[variant].NC;
   const long long per_cta_smem = 64 * 1024;
   const long long cpr = chunks_for(rb, aligned);
   if (cpr * 16 <= 32 * 1024) {
+    // at least ~32 elements per thread and pass: 8 chunks of fp32, 4 of 16-bit
+    const int per_thread = static_cast<int>(2 * es);
     int GT = 32;
-    while (GT < NC && static_cast<long long>(GT) * 4 < cpr) GT *= 2;
+    while (GT < NC && static_cast<long long>(GT) * per_thread < cpr) GT *= 2;
     int R = NC / GT;
     while (R > 1 && (M + R - 1) / R < 2LL * sm_count) R /= 2;
     for (; R >= 1; R /= 2) {
@@ -268,7 +269,7 @@ ce_status launch_rows(int mode, const void* logits, const int64_t* targets, cons
 
   const bool aligned = (lb % 16 == 0) && (rb % 16 == 0);
   Plan pl;
-  if (!choose_plan(rb, aligned, M, di.sm_count, pl)) return CE_ERR_UNSUPPORTED;
+  if (!choose_plan(rb, es, aligned, M, di.sm_count, pl)) return CE_ERR_UNSUPPORTED;
   apply_env_plan(rb, aligned, pl);
 
   ce::RowParams p;

@@ -210,6 +210,12 @@ __device__ __forceinline__ void st_cluster_f4(uint32_t addr, float a, float b, f
                "f"(c), "f"(d)
                : "memory");
 }
+// warp-wide max of a float in one instruction (NaN-ignoring, like fmaxf)
+__device__ __forceinline__ float warp_max(float v) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
+}
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -256,6 +262,10 @@ struct Elem<float> {
   __device__ static __forceinline__ float ld(const void* p) {
     return *static_cast<const volatile float*>(p);
   }
+  __device__ static __forceinline__ float chunk_max(uint4 q) {
+    return fmaxf(fmaxf(__uint_as_float(q.x), __uint_as_float(q.y)),
+                 fmaxf(__uint_as_float(q.z), __uint_as_float(q.w)));
+  }
   __device__ static __forceinline__ void st(void* p, float g) { *static_cast<float*>(p) = g; }
 };
 
@@ -282,6 +292,13 @@ struct Elem<__half> {
   __device__ static __forceinline__ float ld(const void* p) {
     unsigned short u = *static_cast<const volatile unsigned short*>(p);
     return __half2float(__ushort_as_half(u));
+  }
+  // max of the 8 elements with packed half2 max (exact; NaN-ignoring like fmaxf)
+  __device__ static __forceinline__ float chunk_max(uint4 q) {
+    __half2 a = *reinterpret_cast<__half2*>(&q.x), b = *reinterpret_cast<__half2*>(&q.y);
+    __half2 c = *reinterpret_cast<__half2*>(&q.z), d = *reinterpret_cast<__half2*>(&q.w);
+    __half2 m = __hmax2(__hmax2(a, b), __hmax2(c, d));
+    return fmaxf(__low2float(m), __high2float(m));
   }
   __device__ static __forceinline__ void st(void* p, float g) {
     *static_cast<unsigned short*>(p) = __half_as_ushort(__float2half_rn(g));
@@ -310,6 +327,15 @@ struct Elem<__nv_bfloat16> {
     unsigned short u = *static_cast<const volatile unsigned short*>(p);
     return __uint_as_float(static_cast<uint32_t>(u) << 16);
   }
+  // max of the 8 elements with packed bf16x2 max (exact; NaN-ignoring like fmaxf)
+  __device__ static __forceinline__ float chunk_max(uint4 q) {
+    __nv_bfloat162 a = *reinterpret_cast<__nv_bfloat162*>(&q.x);
+    __nv_bfloat162 b = *reinterpret_cast<__nv_bfloat162*>(&q.y);
+    __nv_bfloat162 c = *reinterpret_cast<__nv_bfloat162*>(&q.z);
+    __nv_bfloat162 d = *reinterpret_cast<__nv_bfloat162*>(&q.w);
+    __nv_bfloat162 m = __hmax2(__hmax2(a, b), __hmax2(c, d));
+    return fmaxf(__low2float(m), __high2float(m));
+  }
   __device__ static __forceinline__ void st(void* p, float g) {
     *static_cast<unsigned short*>(p) = __bfloat16_as_ushort(__float2bfloat16_rn(g));
   }
@@ -322,7 +348,7 @@ struct UnitGeo {
   long long row0;   // first row of the unit
   int rows;         // rows in the unit
   long long as;     // absolute address of the unit's first byte
-  long long A0;     // ceil16(as): start of interior chunk 1
+  int hb;           // bytes from `as` to the next 16-byte boundary A0 = as + hb
   int nI;           // interior chunks (1..nI)
   int w0, w1;       // this CTA's chunk window [w0, w1)
   bool head_ok;     // the partial head chunk 0 lies inside the tensor: load it by TMA
@@ -332,28 +358,32 @@ struct UnitGeo {
 __device__ __forceinline__ UnitGeo unit_geo(const RowParams& p, long long u, int rank) {
   UnitGeo g;
   g.row0 = u * p.R;  // the host guarantees CL * q_chunks covers every unit's chunks
-  long long rows = p.M - g.row0;
+  const long long rows = p.M - g.row0;
   g.rows = static_cast<int>(rows < p.R ? rows : p.R);
-  g.as = reinterpret_cast<long long>(p.base) + g.row0 * p.row_bytes;
-  const long long ae = g.as + static_cast<long long>(g.rows) * p.row_bytes;
-  g.A0 = (g.as + 15) & ~15LL;
-  long long A1 = ae & ~15LL;
-  if (A1 < g.A0) A1 = g.A0;
-  g.nI = static_cast<int>((A1 - g.A0) >> 4);
-  const int c_first = (g.as < g.A0) ? 0 : 1;
-  const int c_last = (ae > A1) ? g.nI + 1 : g.nI;
-  // A partial chunk also holds bytes of the neighbouring unit.  Reading those
-  // (and ignoring them) is harmless as long as the 16 bytes lie inside the
-  // tensor; writes to a partial chunk are always element by element.
-  const long long base = reinterpret_cast<long long>(p.base);
-  const long long end = base + p.M * p.row_bytes;
-  g.head_ok = c_first == 0 && g.A0 - 16 >= base && g.A0 <= end;
-  g.tail_ok = c_last == g.nI + 1 && A1 + 16 <= end;
+  const long long off = g.row0 * p.row_bytes;  // unit start, from the tensor base
+  g.as = reinterpret_cast<long long>(p.base) + off;
+  const int ub = g.rows * static_cast<int>(p.row_bytes);  // unit bytes (< 2^31)
+  g.hb = static_cast<int>((-g.as) & 15);
+  int c_first, c_last;
+  if (ub > g.hb) {
+    g.nI = (ub - g.hb) >> 4;
+    c_last = ((ub - g.hb) & 15) ? g.nI + 1 : g.nI;
+  } else {  // the whole unit sits before the first 16-byte boundary
+    g.nI = 0;
+    c_last = 0;
+  }
+  c_first = g.hb ? 0 : 1;
   const int Q = p.q_chunks;
   g.w0 = c_first + rank * Q;
   int w1 = g.w0 + Q;
   g.w1 = w1 < c_last + 1 ? w1 : c_last + 1;
   if (g.w1 < g.w0) g.w1 = g.w0;
+  // A partial chunk also holds bytes of the neighbouring unit.  Reading those
+  // (and ignoring them) is harmless as long as the 16 bytes lie inside the
+  // tensor; writes to a partial chunk are always element by element.
+  const long long total = p.M * p.row_bytes;
+  g.head_ok = c_first == 0 && off + g.hb - 16 >= 0 && off + g.hb <= total;
+  g.tail_ok = c_last == g.nI + 1 && off + g.hb + 16LL * (g.nI + 1) <= total;
   return g;
 }
 
@@ -442,7 +472,7 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
         if (hi > lo) {
           mbar_arrive_expect_tx(fb, static_cast<uint32_t>((hi - lo) * 16));
           bulk_load(stage0 + s * p.stage_bytes + (lo - g.w0) * 16,
-                    reinterpret_cast<const void*>(g.A0 - 16 + 16LL * lo),
+                    reinterpret_cast<const void*>(g.as + g.hb - 16 + 16LL * lo),
                     static_cast<uint32_t>((hi - lo) * 16), fb);
         } else {
           mbar_arrive(fb);
@@ -465,7 +495,7 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
           int lo, hi;
           bulk_range(go, lo, hi);
           if (hi > lo)
-            bulk_store(reinterpret_cast<void*>(go.A0 - 16 + 16LL * lo),
+            bulk_store(reinterpret_cast<void*>(go.as + go.hb - 16 + 16LL * lo),
                        stage0 + s * p.stage_bytes + (lo - go.w0) * 16, (hi - lo) * 16);
           bulk_commit();  // one group per unit (possibly empty) keeps the count exact
           const long long r = j - lag;
@@ -527,10 +557,9 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
       }
       const bool t_ok = row_ok && t >= 0 && t < V;
 
-      // Offsets are taken from the start of chunk 0 (absolute A0 - 16):
+      // Offsets are taken from the start of chunk 0 (absolute as + hb - 16):
       // element e of this row lies at byte e*ES - d0 of that frame.
-      const long long rs = g.as + static_cast<long long>(grp) * rb;  // row start (absolute)
-      const int d0 = static_cast<int>(g.A0 - 16 - rs);                // in (-16 - grp*rb, 0]
+      const int d0 = g.hb - 16 - grp * rb;  // in (-16 - grp*rb, 0]
       int lo = (-d0) >> 4;                 // chunk holding the row's first byte
       int hi = ((rb - 1 - d0) >> 4) + 1;   // one past the chunk holding its last byte
       if (lo < g.w0) lo = g.w0;
@@ -563,7 +592,8 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
       }
 
       auto elem_ptr_global = [&](int e) -> char* {
-        return reinterpret_cast<char*>(rs + static_cast<long long>(e) * ES);
+        return reinterpret_cast<char*>(g.as + static_cast<long long>(grp) * rb +
+                                       static_cast<long long>(e) * ES);
       };
       auto smem_ptr = [&](int byte_off) -> char* {
         return static_cast<char*>(__cvta_shared_to_generic(sbase + byte_off));
@@ -601,11 +631,16 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
 
       if (MODE == BWD) {
         const float sc = p.grad_scale;
+        // g = 2^(x log2e - lse log2e) * scale; the rounding of lse*log2e (lh)
+        // is a common factor 2^(-ll) folded into the scale
+        const float lh = lse_given * kLog2e;
+        const float ll = fmaf(lse_given, kLog2e, -lh);
+        const float scf = ex2(-ll) * sc;
         for (int c = f0 + gt; c < f1; c += GT) {
           float x[EPC], gv[EPC];
           E::unpack(lds128(sbase + 16 * c), x);
 #pragma unroll
-          for (int q = 0; q < EPC; ++q) gv[q] = ex2((x[q] - lse_given) * kLog2e) * sc;
+          for (int q = 0; q < EPC; ++q) gv[q] = ex2(fmaf(x[q], kLog2e, -lh)) * scf;
           sts128(sbase + 16 * c, E::pack(gv));
         }
 #pragma unroll
@@ -639,21 +674,16 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
         for (int k = 0; k < KR; ++k) {
           const int c = f0 + gt + k * GT;
           if (c < f1) {
-            E::unpack(lds128(sbase + 16 * c), v[k]);
+            const uint4 q = lds128(sbase + 16 * c);
+            mt = fmaxf(mt, E::chunk_max(q));
+            E::unpack(q, v[k]);
           } else {
 #pragma unroll
             for (int q = 0; q < EPC; ++q) v[k][q] = -INFINITY;
           }
-#pragma unroll
-          for (int q = 0; q < EPC; ++q) mt = fmaxf(mt, v[k][q]);
         }
       } else {
-        for (int c = f0 + gt; c < f1; c += GT) {
-          float x[EPC];
-          E::unpack(lds128(sbase + 16 * c), x);
-#pragma unroll
-          for (int q = 0; q < EPC; ++q) mt = fmaxf(mt, x[q]);
-        }
+        for (int c = f0 + gt; c < f1; c += GT) mt = fmaxf(mt, E::chunk_max(lds128(sbase + 16 * c)));
       }
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -666,16 +696,22 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
         }
       }
 
-      // ---- one exp2 per element: e = exp(x - m_t), formed as (x - m_t) * log2 e so
-      // that logits sharing a large offset keep full fp32 accuracy ----
+      // ---- one exp2 per element ----
+      // e' = 2^(x log2e - mh) with mh = RN(m_t log2e) is a single FFMA + EX2.
+      // Since x log2e - mh = (x - m_t) log2e + ml exactly up to the FFMA's own
+      // rounding (ml = m_t log2e - mh, the same for every element of the
+      // thread), e' = e * 2^ml: the common factor is divided out once per
+      // thread, so logits sharing a large offset lose no accuracy.
       const float mref = (mt == -INFINITY) ? 0.f : mt;
+      const float mh = mref * kLog2e;
+      const float ml = fmaf(mref, kLog2e, -mh);
       float st = 0.f;
       if (RESIDENT) {
 #pragma unroll
         for (int k = 0; k < KR; ++k)
 #pragma unroll
           for (int q = 0; q < EPC; ++q) {
-            const float e = ex2((v[k][q] - mref) * kLog2e);
+            const float e = ex2(fmaf(v[k][q], kLog2e, -mh));
             v[k][q] = e;
             st += e;
           }
@@ -684,7 +720,7 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
           float x[EPC];
           E::unpack(lds128(sbase + 16 * c), x);
 #pragma unroll
-          for (int q = 0; q < EPC; ++q) st += ex2((x[q] - mref) * kLog2e);
+          for (int q = 0; q < EPC; ++q) st += ex2(fmaf(x[q], kLog2e, -mh));
         }
       }
 #pragma unroll
@@ -694,7 +730,7 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
           float x[EPC];
           edge_load(c, x);
 #pragma unroll
-          for (int q = 0; q < EPC; ++q) st += ex2((x[q] - mref) * kLog2e);
+          for (int q = 0; q < EPC; ++q) st += ex2(fmaf(x[q], kLog2e, -mh));
         }
       }
       if (MODE == FWD) {
@@ -703,10 +739,10 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
       }
 
       // ---- merge (m, s): warp, then the row's warps ----
-      float mw = mt;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, o));
-      float sw = (mt == -INFINITY) ? 0.f : st * ex2((mt - mw) * kLog2e);
+      // (st carries the factor 2^ml; it is removed in the same exp2 that
+      // rescales the thread's sum to the warp max)
+      const float mw = warp_max(mt);
+      float sw = (mt == -INFINITY) ? 0.f : st * ex2((mt - mw) * kLog2e - ml);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) sw += __shfl_down_sync(0xffffffffu, sw, o);
       if (lane == 0) red[b][warp] = make_float2(mw, sw);
@@ -714,9 +750,7 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
       consumer_sync(NC);
 
       float2 r = (lane < GW) ? red[b][grp * GW + lane] : make_float2(-INFINITY, 0.f);
-      float Mg = r.x;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) Mg = fmaxf(Mg, __shfl_xor_sync(0xffffffffu, Mg, o));
+      float Mg = warp_max(r.x);
       float Sg = (r.x == -INFINITY) ? 0.f : r.y * ex2((r.x - Mg) * kLog2e);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) Sg += __shfl_down_sync(0xffffffffu, Sg, o);
@@ -737,9 +771,7 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
         mbar_wait<true>(smem_u32(&xbar[b]), static_cast<uint32_t>((i >> 1) & 1), p.err, failed,
                         WAIT_LIMIT_NS, p.wait_hint_ns);
         float4 xs = (lane < CL) ? xslot[b][lane] : make_float4(-INFINITY, 0.f, 0.f, 0.f);
-        float Mc = xs.x;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) Mc = fmaxf(Mc, __shfl_xor_sync(0xffffffffu, Mc, o));
+        const float Mc = warp_max(xs.x);
         float Sc = (xs.x == -INFINITY) ? 0.f : xs.y * ex2((xs.x - Mc) * kLog2e);
         float Xc = xs.w != 0.f ? xs.z : 0.f;
 #pragma unroll
@@ -765,9 +797,9 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
       }
 
       if (MODE == FWD_BWD) {
-        // g = e * exp(m_t - lse) * scale with exp(m_t - lse) = 2^((m_t - M) log2 e - log2 S)
+        // g = e' * 2^-ml * exp(m_t - lse) * scale, exp(m_t - lse) = 2^((m_t - M) log2e - log2 S)
         const float sc = p.grad_scale;
-        const float f = ex2((mt - Mg) * kLog2e - lg2(Sg)) * sc;
+        const float f = ex2((mt - Mg) * kLog2e - lg2(Sg) - ml) * sc;
         if (RESIDENT) {
 #pragma unroll
           for (int k = 0; k < KR; ++k) {
@@ -784,7 +816,7 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
             float x[EPC], gv[EPC];
             E::unpack(lds128(sbase + 16 * c), x);
 #pragma unroll
-            for (int q = 0; q < EPC; ++q) gv[q] = ex2((x[q] - mref) * kLog2e) * f;
+            for (int q = 0; q < EPC; ++q) gv[q] = ex2(fmaf(x[q], kLog2e, -mh)) * f;
             sts128(sbase + 16 * c, E::pack(gv));
           }
         }
@@ -795,7 +827,7 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
             float x[EPC], gv[EPC];
             edge_load(c, x);
 #pragma unroll
-            for (int q = 0; q < EPC; ++q) gv[q] = ex2((x[q] - mref) * kLog2e) * f;
+            for (int q = 0; q < EPC; ++q) gv[q] = ex2(fmaf(x[q], kLog2e, -mh)) * f;
             edge_store(c, gv);
           }
         }
