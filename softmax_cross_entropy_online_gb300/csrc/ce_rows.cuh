@@ -458,10 +458,9 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
 
   if (warp == NW) {
     // ======================= producer warp =======================
-    // Loads run S units ahead of the consumers.  In the modes that write, the
-    // gradient of unit j is stored as soon as the consumers release its stage,
-    // and a stage is refilled LAG units later, once its store has been read
-    // out of shared memory, so a store never stalls the next load.
+    // Loads run up to S - 1 units ahead of the consumers.  In the modes that
+    // write, the gradient of unit j is stored as soon as the consumers release
+    // its stage, and the stage is refilled once that store has been read out.
     if (lane == 0) {
       auto issue_load = [&](long long i, int s) {
         const UnitGeo g = unit_geo(p, cid + i * ncl, rank);
@@ -480,9 +479,12 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
       };
       const long long pre = n_iter < S ? n_iter : S;
       for (long long i = 0; i < pre; ++i) issue_load(i, static_cast<int>(i));
-      // a stage is refilled `lag` units after its store was issued; the refill
-      // brings unit r + S, which must be a unit not yet loaded: lag <= S - 1
-      const int lag = (S >= 3) ? 2 : S - 1;
+      // A stage is refilled as soon as the store of its unit has been read out
+      // of shared memory (lag 0): the loads then run S - 1 units ahead of the
+      // consumers.  (The refill brings unit r + S, r = j - lag, which must not
+      // be loaded yet, so any lag <= S - 1 is valid; a larger lag only shortens
+      // the lookahead to S - 1 - lag units.)
+      const int lag = 0;
       int s = 0, sr = S - lag;  // stages of unit j and of unit j - lag (mod S)
       if (sr == S) sr = 0;
       uint32_t phase = 0;
