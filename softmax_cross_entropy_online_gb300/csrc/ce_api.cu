@@ -137,45 +137,55 @@ long long stage_bytes_for(int variant, int R, int CL, long long rb, bool aligned
   return per_cta * 16;
 }
 
-// Default launch shape (from sweeps on GB300): the shared-memory streaming
-// consumers (variant 3, 256 threads), about 64 KB of stages per CTA so three
-// CTAs share an SM.  Rows of up to 32 KB are packed R per unit in one CTA with
-// ~4 chunks per thread and pass; longer rows are split over a cluster of up to
-// 8 CTAs with two stages each.
-bool choose_plan(long long rb, int es, bool aligned, long long M, int sm_count, Plan& pl) {
-  const int variant = 3;
-  const int NC = ce::kVariants[variant].NC;
-  const long long per_cta_smem = 64 * 1024;
+// Default launch shapes, from sweeps of every shape on GB300:
+//  * rows up to 32 KB: R rows per unit of up to 64 KB.  The forward (read
+//    only) uses 256 streaming consumer threads with one stage, three CTAs
+//    per SM; the writing modes use 512 consumer threads with two stages, one
+//    CTA per SM.
+//  * rows that fit one CTA twice over (up to ~108 KB): one row per unit, 512
+//    threads, two stages, no cluster and so no cross-CTA exchange.
+//  * longer rows: split over a cluster into slices of at most 52 KB, 256
+//    threads, two stages (two CTAs per SM); beyond 8 x 52 KB the slices grow.
+bool choose_plan(int mode, long long rb, bool aligned, long long M, int sm_count, Plan& pl) {
   const long long cpr = chunks_for(rb, aligned);
   if (cpr * 16 <= 32 * 1024) {
-    // at least ~32 elements per thread and pass: 8 chunks of fp32, 4 of 16-bit
-    const int per_thread = static_cast<int>(2 * es);
-    int GT = 32;
-    while (GT < NC && static_cast<long long>(GT) * per_thread < cpr) GT *= 2;
-    int R = NC / GT;
-    while (R > 1 && (M + R - 1) / R < 2LL * sm_count) R /= 2;
+    const bool fwd = mode == ce::FWD;
+    const int variant = fwd ? 3 : 4;
+    const int NC = ce::kVariants[variant].NC;
+    const long long budget = fwd ? 64 * 1024 : 128 * 1024;  // stage bytes per CTA
+    int R = 1;
+    while (R * 2 <= NC / 32 && static_cast<long long>(R) * 2 * rb <= 64 * 1024) R *= 2;
+    const long long min_units = (fwd ? 3LL : 1LL) * sm_count;
+    while (R > 1 && (M + R - 1) / R < min_units) R /= 2;
     for (; R >= 1; R /= 2) {
       const long long stage = stage_bytes_for(variant, R, 1, rb, aligned);
       if (stage == 0) continue;
-      long long S = per_cta_smem / stage;
+      long long S = budget / stage;
       if (S > ce::kMaxStages) S = ce::kMaxStages;
-      if (S >= 2) {
-        pl = Plan{variant, R, 1, static_cast<int>(S), static_cast<int>(stage)};
-        return true;
-      }
+      if (S < 1) S = 1;
+      if (S * stage > 216 * 1024) continue;
+      pl = Plan{variant, R, 1, static_cast<int>(S), static_cast<int>(stage)};
+      return true;
+    }
+  }
+  {
+    const long long stage = stage_bytes_for(4, 1, 1, rb, aligned);
+    if (stage != 0 && 2 * stage <= 216 * 1024) {
+      pl = Plan{4, 1, 1, 2, static_cast<int>(stage)};
+      return true;
     }
   }
   for (int CL = 2; CL <= ce::kMaxCluster; ++CL) {
-    const long long stage = stage_bytes_for(variant, 1, CL, rb, aligned);
-    if (stage == 0 || stage > 32 * 1024) continue;
-    pl = Plan{variant, 1, CL, 2, static_cast<int>(stage)};
+    const long long stage = stage_bytes_for(3, 1, CL, rb, aligned);
+    if (stage == 0 || stage > 52 * 1024) continue;
+    pl = Plan{3, 1, CL, 2, static_cast<int>(stage)};
     return true;
   }
   // very long rows: 8 CTAs, larger slices, fewer stages
-  const long long stage = stage_bytes_for(variant, 1, ce::kMaxCluster, rb, aligned);
+  const long long stage = stage_bytes_for(3, 1, ce::kMaxCluster, rb, aligned);
   if (stage == 0 || stage > kMaxSliceBytes) return false;
-  const int S = (2 * stage <= 220 * 1024) ? 2 : 1;
-  pl = Plan{variant, 1, ce::kMaxCluster, S, static_cast<int>(stage)};
+  const int S = (2 * stage <= 216 * 1024) ? 2 : 1;
+  pl = Plan{3, 1, ce::kMaxCluster, S, static_cast<int>(stage)};
   return true;
 }
 
@@ -269,7 +279,7 @@ ce_status launch_rows(int mode, const void* logits, const int64_t* targets, cons
 
   const bool aligned = (lb % 16 == 0) && (rb % 16 == 0);
   Plan pl;
-  if (!choose_plan(rb, es, aligned, M, di.sm_count, pl)) return CE_ERR_UNSUPPORTED;
+  if (!choose_plan(mode, rb, aligned, M, di.sm_count, pl)) return CE_ERR_UNSUPPORTED;
   apply_env_plan(rb, aligned, pl);
 
   ce::RowParams p;
