@@ -45,7 +45,9 @@ FALLBACK_HBM_GBS = 6800.0
 # under profiles/), valid only for the kernel source it was taken on: the
 # digest of csrc/ at that time.  Any change to the kernels nulls it.
 NCU_TRAFFIC = {
-    # "<sha256 of csrc/*>": {"workload": "...", "bytes_per_launch": int}
+    # profiles/ce_rows_fwd_bwd_f32_32768x4096.md: a 16384-row capture, scaled 2x
+    "a49986c8c7b745c097223a82c0173ce019d121277670bfdfde67cecece81ee8f": {
+        "workload": "f32_32768x4096", "bytes_per_launch": 953085440},
 }
 
 
@@ -299,7 +301,8 @@ def run_native(args, w):
     avg_kernel_ms = sum(kernel_ms) / len(kernel_ms)
     peak, peak_kind = measured_peaks()
     achieved = b_step / (avg_kernel_ms * 1e-3) / 1e9
-    traffic = NCU_TRAFFIC.get(csrc_digest(), {}).get("bytes_per_launch")
+    rec = NCU_TRAFFIC.get(csrc_digest(), {})
+    traffic = rec.get("bytes_per_launch") if rec.get("workload") == w.name else None
 
     # forward-only pass on the same workload (the first half of the config)
     fwd_ms = None
