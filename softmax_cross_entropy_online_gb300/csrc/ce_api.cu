@@ -142,8 +142,10 @@ long long stage_bytes_for(int variant, int R, int CL, long long rb, bool aligned
 //    only) uses 256 streaming consumer threads with one stage, three CTAs
 //    per SM; the writing modes use 512 consumer threads with two stages, one
 //    CTA per SM.
-//  * rows that fit one CTA twice over (up to ~108 KB): one row per unit, 512
-//    threads, two stages, no cluster and so no cross-CTA exchange.
+//  * rows that fit one CTA twice over (up to ~108 KB): one row per unit and
+//    no cluster, so no cross-CTA exchange: 512 threads with two stages for
+//    the writing modes, 256 threads with one stage (two CTAs per SM) for the
+//    forward.
 //  * longer rows: split over a cluster into slices of at most 52 KB, 256
 //    threads, two stages (two CTAs per SM); beyond 8 x 52 KB the slices grow.
 bool choose_plan(int mode, long long rb, bool aligned, long long M, int sm_count, Plan& pl) {
@@ -169,9 +171,12 @@ bool choose_plan(int mode, long long rb, bool aligned, long long M, int sm_count
     }
   }
   {
-    const long long stage = stage_bytes_for(4, 1, 1, rb, aligned);
+    // the forward does best with two 256-thread CTAs per SM and one stage each
+    const bool fwd = mode == ce::FWD;
+    const int variant = fwd ? 3 : 4;
+    const long long stage = stage_bytes_for(variant, 1, 1, rb, aligned);
     if (stage != 0 && 2 * stage <= 216 * 1024) {
-      pl = Plan{4, 1, 1, 2, static_cast<int>(stage)};
+      pl = Plan{variant, 1, 1, fwd ? 1 : 2, static_cast<int>(stage)};
       return true;
     }
   }

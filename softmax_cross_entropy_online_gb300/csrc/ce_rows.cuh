@@ -196,6 +196,11 @@ __device__ __forceinline__ void bulk_wait_all() {
 __device__ __forceinline__ void consumer_sync(int nthreads) {
   asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
 }
+// named barrier `id` (1..15) over `nthreads` threads: one per row group, so
+// the groups of a CTA do not wait for each other
+__device__ __forceinline__ void group_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;" ::
                    : "memory");
@@ -747,18 +752,29 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
       float sw = (mt == -INFINITY) ? 0.f : st * ex2((mt - mw) * kLog2e - ml);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) sw += __shfl_down_sync(0xffffffffu, sw, o);
-      if (lane == 0) red[b][warp] = make_float2(mw, sw);
-      if (owner) xt_slot[b][grp] = xt;
-      consumer_sync(NC);
-
-      float2 r = (lane < GW) ? red[b][grp * GW + lane] : make_float2(-INFINITY, 0.f);
-      float Mg = warp_max(r.x);
-      float Sg = (r.x == -INFINITY) ? 0.f : r.y * ex2((r.x - Mg) * kLog2e);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) Sg += __shfl_down_sync(0xffffffffu, Sg, o);
-      Sg = __shfl_sync(0xffffffffu, Sg, 0);
       const bool have_t = t_ok && tc >= g.w0 && tc < g.w1;  // this CTA holds x[row, t]
-      float xrow = have_t ? xt_slot[b][grp] : 0.f;
+      float Mg, Sg, xrow = 0.f;
+      if (GW == 1) {
+        // a row handled by one warp: the warp's pair is the row's pair, and the
+        // target logit comes from the owner lane, with no shared memory or barrier
+        Mg = mw;
+        Sg = __shfl_sync(0xffffffffu, sw, 0);
+        const unsigned own = __ballot_sync(0xffffffffu, owner);
+        if (have_t && own != 0u) xrow = __shfl_sync(0xffffffffu, xt, __ffs(own) - 1);
+      } else {
+        if (lane == 0) red[b][warp] = make_float2(mw, sw);
+        if (owner) xt_slot[b][grp] = xt;
+        if (R == 1) consumer_sync(NC);
+        else group_sync(1 + grp, GT);
+
+        float2 r = (lane < GW) ? red[b][grp * GW + lane] : make_float2(-INFINITY, 0.f);
+        Mg = warp_max(r.x);
+        Sg = (r.x == -INFINITY) ? 0.f : r.y * ex2((r.x - Mg) * kLog2e);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) Sg += __shfl_down_sync(0xffffffffu, Sg, o);
+        Sg = __shfl_sync(0xffffffffu, Sg, 0);
+        xrow = have_t ? xt_slot[b][grp] : 0.f;
+      }
 
       // ---- merge across the cluster through distributed shared memory ----
       if (CL > 1) {
@@ -847,7 +863,7 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
     // ---- deterministic reduction of the loss ----
     if (p.loss != nullptr) {
       if (gt == 0) acc_slot[grp] = acc;
-      consumer_sync(NC);
+      group_sync(15, NC);  // an id no row group uses
       if (tid == 0) {
         double part = 0.0;
         for (int j = 0; j < R; ++j) part += acc_slot[j];
