@@ -51,7 +51,7 @@ extern "C" {
 typedef enum {
   CE_OK = 0,
   CE_ERR_INVALID_ARG = 1,  /* bad size, null or misaligned pointer, bad enum */
-  CE_ERR_UNSUPPORTED = 2,  /* V beyond ce_max_vocab(dtype) */
+  CE_ERR_UNSUPPORTED = 2,  /* V beyond ce_max_vocab(dtype), or a layout a kernel cannot take */
   CE_ERR_TARGET_RANGE = 3, /* (ce_check_errors) a target was outside [0, V) */
   CE_ERR_CUDA = 4,         /* a CUDA runtime call or a launch failed */
   CE_ERR_TIMEOUT = 5       /* (ce_check_errors) a bounded wait ran out */
@@ -136,6 +136,50 @@ ce_status ce_fwd_bwd_inplace_noalloc(void* logits, const int64_t* targets, int64
 ce_status ce_backward_from_lse(void* logits, const int64_t* targets, const float* lse,
                                int64_t M, int64_t V, ce_dtype dtype, float scale,
                                void* stream);
+
+/*
+ * linear_ce_fwd_bwd -- fused linear + cross-entropy ("9 Triton kernels in 9
+ * weeks", week eight: the lm_head projection chunked into the loss so the
+ * full logits matrix never exists).  For hidden states h [M, H] and the
+ * lm_head weight W [V, H], with logits = h W^T:
+ *
+ *     loss = mean_i CE(logits_i, t_i)
+ *     dH   = G W          [M, H]      G = (softmax(logits) - onehot) / M
+ *     dW   = G^T h        [V, H]
+ *
+ * Rows are processed in chunks: each chunk's logits are produced by a
+ * tcgen05 GEMM into the workspace, turned into G in place by the row
+ * kernel, and contracted into dH and dW (accumulated over chunks) by two
+ * more tcgen05 GEMMs with bf16 operands and fp32 accumulation.
+ *
+ *   h        [M, H] bf16, row-major; W [V, H] bf16, row-major (device).
+ *            H must be a multiple of 8; h and W 16-byte aligned.
+ *   targets  [M] int64.   loss [1] fp32.   dH [M, H] fp32.   dW [V, H] fp32.
+ *   workspace  device memory of workspace_bytes >= linear_ce_workspace_size
+ *            for some chunk size (256-byte aligned, owned by the caller); a
+ *            smaller workspace is used with a smaller row chunk, down to 128
+ *            rows, else CE_ERR_INVALID_ARG.
+ *   G is rounded to bf16 before the two gradient GEMMs; logits, the loss
+ *   and every accumulation are fp32.
+ */
+ce_status linear_ce_fwd_bwd(const void* h, const void* W, const int64_t* targets, int64_t M,
+                            int64_t H, int64_t V, float* loss, float* dH, float* dW,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace bytes of linear_ce_fwd_bwd at its default row chunk (0 on bad sizes). */
+size_t linear_ce_workspace_size(int64_t M, int64_t H, int64_t V);
+
+/*
+ * ce_gemm_bf16_tn -- the tensor-core contraction under linear_ce_fwd_bwd,
+ * exposed on its own: D[M, N] = A[M, K] B[N, K]^T (beta = 0) or
+ * D += A B^T (beta = 1), A and B bf16 with K contiguous (row strides lda,
+ * ldb elements, multiples of 8, bases 16-byte aligned), D fp32 with row
+ * stride ldd.  A persistent tcgen05 kernel: TMA into shared memory, MMAs
+ * into TMEM accumulators, fp32 epilogue.
+ */
+ce_status ce_gemm_bf16_tn(const void* A, int64_t lda, const void* B, int64_t ldb, float* D,
+                          int64_t ldd, int64_t M, int64_t N, int64_t K, float beta,
+                          void* stream);
 
 /*
  * ce_check_errors -- wait (at most timeout_ms) for `stream` to drain, then

@@ -33,6 +33,10 @@ SIGNATURES = {
     "ce_fwd_bwd_inplace": (_i32, [_vp, _vp, _i64, _i64, _i32, _i32, _vp, _vp, _vp, _vp]),
     "ce_fwd_bwd_inplace_noalloc": (_i32, [_vp, _vp, _i64, _i64, _i32, _i32, _vp, _vp, _vp, _vp]),
     "ce_backward_from_lse": (_i32, [_vp, _vp, _vp, _i64, _i64, _i32, _f32, _vp]),
+    "linear_ce_fwd_bwd": (_i32, [_vp, _vp, _vp, _i64, _i64, _i64, _vp, _vp, _vp, _vp,
+                                 ctypes.c_size_t, _vp]),
+    "linear_ce_workspace_size": (ctypes.c_size_t, [_i64, _i64, _i64]),
+    "ce_gemm_bf16_tn": (_i32, [_vp, _i64, _vp, _i64, _vp, _i64, _i64, _i64, _i64, _f32, _vp]),
     "ce_check_errors": (_i32, [_vp, _i32]),
     "ce_status_string": (ctypes.c_char_p, [_i32]),
     "ce_max_vocab": (_i64, [_i32]),
@@ -166,6 +170,57 @@ def ce_backward_from_lse(logits: torch.Tensor, targets: torch.Tensor, lse: torch
                                     _DTYPES[logits.dtype], float(scale),
                                     _stream_handle(stream, logits.device))
     _check(st, "ce_backward_from_lse")
+
+
+def linear_ce_fwd_bwd(h: torch.Tensor, W: torch.Tensor, targets: torch.Tensor, *,
+                      workspace: torch.Tensor | None = None, stream=None):
+    """Fused linear + cross-entropy: returns (loss, dH, dW) for bf16 h [M, H] and
+    W [V, H]; the mean loss's gradients are fp32.  The workspace (uint8 CUDA
+    tensor) defaults to linear_ce_workspace_size(M, H, V) bytes."""
+    if h.dtype != torch.bfloat16 or W.dtype != torch.bfloat16 or not h.is_cuda or not W.is_cuda:
+        raise ValueError("h and W must be bf16 CUDA tensors")
+    if h.dim() != 2 or W.dim() != 2 or h.shape[1] != W.shape[1]:
+        raise ValueError("h must be [M, H] and W [V, H]")
+    if not h.is_contiguous() or not W.is_contiguous():
+        raise ValueError("h and W must be contiguous")
+    M, H = h.shape
+    V = W.shape[0]
+    if (targets.dtype != torch.int64 or targets.numel() != M or not targets.is_cuda
+            or not targets.is_contiguous()):
+        raise ValueError("targets must be a contiguous int64 CUDA tensor [M]")
+    dev = h.device
+    if workspace is None:
+        workspace = torch.empty(int(lib().linear_ce_workspace_size(M, H, V)), dtype=torch.uint8,
+                                device=dev)
+    loss = torch.empty((), dtype=torch.float32, device=dev)
+    dH = torch.empty((M, H), dtype=torch.float32, device=dev)
+    dW = torch.empty((V, H), dtype=torch.float32, device=dev)
+    st = lib().linear_ce_fwd_bwd(h.data_ptr(), W.data_ptr(), targets.data_ptr(), M, H, V,
+                                 loss.data_ptr(), dH.data_ptr(), dW.data_ptr(),
+                                 workspace.data_ptr(), workspace.numel(),
+                                 _stream_handle(stream, dev))
+    _check(st, "linear_ce_fwd_bwd")
+    return loss, dH, dW
+
+
+def linear_ce_workspace_size(M: int, H: int, V: int) -> int:
+    return int(lib().linear_ce_workspace_size(M, H, V))
+
+
+def ce_gemm_bf16_tn(A: torch.Tensor, B: torch.Tensor, D: torch.Tensor | None = None,
+                    beta: float = 0.0, *, stream=None) -> torch.Tensor:
+    """D = A B^T (beta 0) or D += A B^T (beta 1): A [M, K], B [N, K] bf16, D fp32."""
+    if A.dtype != torch.bfloat16 or B.dtype != torch.bfloat16 or A.shape[1] != B.shape[1]:
+        raise ValueError("A [M, K] and B [N, K] must be bf16 with the same K")
+    M, K = A.shape
+    N = B.shape[0]
+    if D is None:
+        D = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    st = lib().ce_gemm_bf16_tn(A.data_ptr(), A.stride(0), B.data_ptr(), B.stride(0),
+                               D.data_ptr(), D.stride(0), M, N, K, float(beta),
+                               _stream_handle(stream, A.device))
+    _check(st, "ce_gemm_bf16_tn")
+    return D
 
 
 def ce_check_errors(stream=None, timeout_ms: int = 10000, device=None) -> int:

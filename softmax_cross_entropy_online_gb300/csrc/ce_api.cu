@@ -22,6 +22,15 @@ cudaError_t rows_launch(int mode, int variant, const RowParams& p, int grid, int
 template <typename T>
 cudaError_t rows_max_active(int mode, int variant, int smem_bytes, int CL, int sm_count,
                             int* out);
+ce_status gemm_bf16_tn(const void* A, long long lda, const void* B, long long ldb, float* D,
+                       long long ldd, int M, int N, int K, float beta, cudaStream_t stream,
+                       unsigned int* err, int sm_count, unsigned int wait_hint_ns);
+ce_status launch_convert_transpose(const float* G, int R, int C, long long ldg,
+                                   __nv_bfloat16* G16, long long ldo, __nv_bfloat16* Gt16,
+                                   long long ldt, cudaStream_t st, int sm_count);
+ce_status launch_transpose_bf16(const void* X, int R, int C, long long ldx, void* T,
+                                long long ldt, cudaStream_t st, int sm_count);
+ce_status launch_mean_rows(const float* rl, long long M, float* loss, cudaStream_t st);
 }  // namespace ce
 
 namespace ce {
@@ -358,6 +367,36 @@ ce_status launch_rows(int mode, const void* logits, const int64_t* targets, cons
   return CE_OK;
 }
 
+// Workspace of the fused linear + cross-entropy for row chunks of `mc` rows:
+// Wt [H, ldv] bf16, logits/G [mc, V] fp32, G16 [mc, ldv] bf16, Gt16 [V, ldk]
+// bf16, ht [H, ldk] bf16, row losses [M] fp32 (ldv = V and ldk = mc rounded up
+// to a multiple of 8, padded with zeros).
+struct LinearWs {
+  size_t wt, logits, g16, gt16, ht, rl, total;
+};
+size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+LinearWs linear_ws_layout(long long M, long long H, long long V, long long mc) {
+  const long long ldv = (V + 7) / 8 * 8;
+  const long long ldk = (mc + 7) / 8 * 8;
+  LinearWs w;
+  size_t off = 0;
+  w.wt = off;
+  off += round256(static_cast<size_t>(H) * ldv * 2);
+  w.logits = off;
+  off += round256(static_cast<size_t>(mc) * V * 4);
+  w.g16 = off;
+  off += round256(static_cast<size_t>(mc) * ldv * 2);
+  w.gt16 = off;
+  off += round256(static_cast<size_t>(V) * ldk * 2);
+  w.ht = off;
+  off += round256(static_cast<size_t>(H) * ldk * 2);
+  w.rl = off;
+  off += round256(static_cast<size_t>(M) * 4);
+  w.total = off;
+  return w;
+}
+constexpr long long kLinearDefaultChunk = 2048;
+
 }  // namespace
 
 extern "C" {
@@ -389,6 +428,109 @@ ce_status ce_backward_from_lse(void* logits, const int64_t* targets, const float
                                int64_t V, ce_dtype dtype, float scale, void* stream) {
   return launch_rows(ce::BWD, logits, targets, lse, M, V, dtype, CE_RED_NONE, nullptr, nullptr,
                      nullptr, scale, stream);
+}
+
+ce_status ce_gemm_bf16_tn(const void* A, int64_t lda, const void* B, int64_t ldb, float* D,
+                          int64_t ldd, int64_t M, int64_t N, int64_t K, float beta,
+                          void* stream) {
+  if (M < 0 || N < 0 || K < 0 || (M > 0 && N > 0 && (A == nullptr || B == nullptr || D == nullptr)))
+    return CE_ERR_INVALID_ARG;
+  if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return CE_ERR_UNSUPPORTED;
+  if (beta != 0.f && beta != 1.f) return CE_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(D) % 4) return CE_ERR_INVALID_ARG;
+  DeviceInfo di;
+  int dev = 0;
+  ce_status st = device_info(di, &dev);
+  if (st != CE_OK) return st;
+  st = ce::gemm_bf16_tn(A, lda, B, ldb, D, ldd, static_cast<int>(M), static_cast<int>(N),
+                        static_cast<int>(K), beta, static_cast<cudaStream_t>(stream), di.err,
+                        di.sm_count, wait_hint_ns());
+  if (st == CE_OK) g_launches.fetch_add(1, std::memory_order_relaxed);
+  return st;
+}
+
+size_t linear_ce_workspace_size(int64_t M, int64_t H, int64_t V) {
+  if (M < 0 || H < 1 || V < 1) return 0;
+  const long long mc = M < kLinearDefaultChunk ? (M > 0 ? M : 1) : kLinearDefaultChunk;
+  return linear_ws_layout(M, H, V, mc).total;
+}
+
+ce_status linear_ce_fwd_bwd(const void* h, const void* W, const int64_t* targets, int64_t M,
+                            int64_t H, int64_t V, float* loss, float* dH, float* dW,
+                            void* workspace, size_t workspace_bytes, void* stream) {
+  if (M < 1 || H < 1 || V < 1) return CE_ERR_INVALID_ARG;
+  if (!h || !W || !targets || !loss || !dH || !dW || !workspace) return CE_ERR_INVALID_ARG;
+  if ((H % 8) || (reinterpret_cast<uintptr_t>(h) % 16) || (reinterpret_cast<uintptr_t>(W) % 16))
+    return CE_ERR_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(workspace) % 256) || (reinterpret_cast<uintptr_t>(dH) % 16) ||
+      (reinterpret_cast<uintptr_t>(dW) % 16) || (reinterpret_cast<uintptr_t>(targets) % 8) ||
+      (reinterpret_cast<uintptr_t>(loss) % 4))
+    return CE_ERR_INVALID_ARG;
+  if (M > INT32_MAX || H > INT32_MAX || V > INT32_MAX) return CE_ERR_UNSUPPORTED;
+  // the largest row chunk (a multiple of 128, or all of M) whose workspace fits
+  long long mc = M < kLinearDefaultChunk ? M : kLinearDefaultChunk;
+  while (linear_ws_layout(M, H, V, mc).total > workspace_bytes) {
+    if (mc <= 128) return CE_ERR_INVALID_ARG;
+    mc = (mc / 2 + 127) / 128 * 128;
+  }
+  DeviceInfo di;
+  int dev = 0;
+  ce_status st = device_info(di, &dev);
+  if (st != CE_OK) return st;
+  const LinearWs L = linear_ws_layout(M, H, V, mc);
+  char* ws = static_cast<char*>(workspace);
+  auto* wt = reinterpret_cast<__nv_bfloat16*>(ws + L.wt);
+  auto* logits = reinterpret_cast<float*>(ws + L.logits);
+  auto* g16 = reinterpret_cast<__nv_bfloat16*>(ws + L.g16);
+  auto* gt16 = reinterpret_cast<__nv_bfloat16*>(ws + L.gt16);
+  auto* ht = reinterpret_cast<__nv_bfloat16*>(ws + L.ht);
+  auto* rl = reinterpret_cast<float*>(ws + L.rl);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const long long ldv = (V + 7) / 8 * 8;
+  const unsigned hint = wait_hint_ns();
+  const int sms = di.sm_count;
+  uint64_t launches = 0;
+  // W^T [H, ldv] for dH = G W
+  if ((st = ce::launch_transpose_bf16(W, static_cast<int>(V), static_cast<int>(H), H, wt, ldv, s,
+                                      sms)) != CE_OK)
+    return st;
+  ++launches;
+  const float scale = 1.0f / static_cast<float>(M);
+  for (long long m0 = 0; m0 < M; m0 += mc) {
+    const long long rows = (M - m0) < mc ? (M - m0) : mc;
+    const long long ldk = (rows + 7) / 8 * 8;
+    const auto* hc = static_cast<const __nv_bfloat16*>(h) + m0 * H;
+    // logits[rows, V] = h_c W^T
+    if ((st = ce::gemm_bf16_tn(hc, H, W, H, logits, V, static_cast<int>(rows),
+                               static_cast<int>(V), static_cast<int>(H), 0.f, s, di.err, sms,
+                               hint)) != CE_OK)
+      return st;
+    // in place: row losses and G = (softmax - onehot) / M
+    if ((st = launch_rows(ce::FWD_BWD, logits, targets + m0, nullptr, rows, V, CE_F32,
+                          CE_RED_NONE, nullptr, rl + m0, nullptr, scale, stream)) != CE_OK)
+      return st;
+    // G16 [rows, ldv] and G^T [V, ldk] in bf16, h_c^T [H, ldk]
+    if ((st = ce::launch_convert_transpose(logits, static_cast<int>(rows), static_cast<int>(V), V,
+                                           g16, ldv, gt16, ldk, s, sms)) != CE_OK)
+      return st;
+    if ((st = ce::launch_transpose_bf16(hc, static_cast<int>(rows), static_cast<int>(H), H, ht,
+                                        ldk, s, sms)) != CE_OK)
+      return st;
+    // dH[rows] = G W = G16 (W^T)^T ; dW (+)= G^T h_c = Gt16 (h_c^T)^T
+    if ((st = ce::gemm_bf16_tn(g16, ldv, wt, ldv, dH + m0 * H, H, static_cast<int>(rows),
+                               static_cast<int>(H), static_cast<int>(ldv), 0.f, s, di.err, sms,
+                               hint)) != CE_OK)
+      return st;
+    if ((st = ce::gemm_bf16_tn(gt16, ldk, ht, ldk, dW, H, static_cast<int>(V), static_cast<int>(H),
+                               static_cast<int>(ldk), m0 == 0 ? 0.f : 1.f, s, di.err, sms,
+                               hint)) != CE_OK)
+      return st;
+    launches += 4;  // the row kernel counts itself
+  }
+  if ((st = ce::launch_mean_rows(rl, M, loss, s)) != CE_OK) return st;
+  ++launches;
+  g_launches.fetch_add(launches, std::memory_order_relaxed);
+  return CE_OK;
 }
 
 ce_status ce_check_errors(void* stream, int timeout_ms) {

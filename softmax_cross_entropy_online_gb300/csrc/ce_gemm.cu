@@ -1,0 +1,415 @@
+// ce_gemm.cu -- the dense contractions of the fused linear + cross-entropy
+// ("9 Triton kernels in 9 weeks", week eight: the lm_head projection chunked
+// into the loss), on the 5th-generation tensor cores of sm_103a:
+//
+//     D[M, N] (fp32)  =  A[M, K] . B[N, K]^T  (+ beta * D)
+//
+// with A and B bf16 and K contiguous in memory ("K-major" for both operands).
+//
+// Design: a persistent kernel, one CTA per SM, warp-specialised.
+//  * warp 0 (one thread) streams 128x64 tiles of A and 256x64 tiles of B into a
+//    ring of shared-memory stages with TMA (cp.async.bulk.tensor, 128-byte
+//    swizzle), completion counted on an mbarrier per stage;
+//  * warp 1 allocates 512 TMEM columns (two 128x256 fp32 accumulators) and one
+//    of its threads issues tcgen05.mma (M=128, N=256, K=16, bf16 -> fp32) from
+//    the shared-memory descriptors; tcgen05.commit frees a stage when the MMAs
+//    that read it are done and signals a full accumulator after the last k-tile;
+//  * warps 2..5 are the epilogue: each reads its 32 TMEM lanes (tile rows) with
+//    tcgen05.ld, adds beta * D when asked, and stores fp32 to global memory,
+//    then hands the accumulator back.  With two accumulators the epilogue of
+//    one tile overlaps the main loop of the next.
+// Every mbarrier wait is bounded (see ce_rows.cuh); TMEM is freed on every path.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "../../include/ce_gb300.h"
+#include "ce_rows.cuh"
+
+namespace ce {
+
+constexpr int kGemmBM = 128;
+constexpr int kGemmBN = 256;
+constexpr int kGemmBK = 64;  // one 128-byte swizzle row of bf16
+constexpr int kGemmStages = 4;
+constexpr int kGemmThreads = 192;
+constexpr int kTileABytes = kGemmBM * kGemmBK * 2;  // 16 KB
+constexpr int kTileBBytes = kGemmBN * kGemmBK * 2;  // 32 KB
+constexpr int kStageBytes = kTileABytes + kTileBBytes;
+constexpr int kGemmSmem = kGemmStages * kStageBytes + 1024;  // + alignment slack
+constexpr uint32_t kTmemCols = 512;
+
+struct GemmParams {
+  int M, N, K;
+  float* D;
+  long long ldd;  // elements between rows of D
+  float beta;     // 0: D = A B^T; 1: D += A B^T
+  int tiles_m, tiles_n, k_tiles;
+  unsigned int* err;
+  unsigned int wait_hint_ns;
+};
+
+// --- tcgen05 / TMA helpers ---------------------------------------------------
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+// shared-memory matrix descriptor: K-major operand, 128-byte swizzle, 8-row
+// groups 1024 bytes apart (SBO); the leading-byte offset is unused for a
+// swizzled K-major layout and set to 1
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
+  return static_cast<uint64_t>((addr >> 4) & 0x3FFFu) | (static_cast<uint64_t>(1) << 16) |
+         (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
+         (static_cast<uint64_t>(2) << 61);
+}
+// instruction descriptor of kind::f16: D fp32, A and B bf16, both K-major, N=256, M=128
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((kGemmBN >> 3) << 17) |
+                            ((kGemmBM >> 4) << 24);
+
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(kIdesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+// 32 consecutive fp32 columns of this thread's TMEM lane
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+      "%28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+}
+
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    gemm_bf16_tn_kernel(const __grid_constant__ CUtensorMap tma_a,
+                        const __grid_constant__ CUtensorMap tma_b, const GemmParams p) {
+  extern __shared__ unsigned char gsm[];
+  __shared__ __align__(8) unsigned long long full_bar[kGemmStages];
+  __shared__ __align__(8) unsigned long long empty_bar[kGemmStages];
+  __shared__ __align__(8) unsigned long long accf_bar[2];
+  __shared__ __align__(8) unsigned long long acce_bar[2];
+  __shared__ uint32_t tmem_slot;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t sbase = (smem_u32(gsm) + 1023u) & ~1023u;  // swizzle atoms need 1024 B
+  bool failed = false;
+  const unsigned int hint = p.wait_hint_ns;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kGemmStages; ++s) {
+      mbar_init(smem_u32(&full_bar[s]), 1);
+      mbar_init(smem_u32(&empty_bar[s]), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(smem_u32(&accf_bar[a]), 1);
+      mbar_init(smem_u32(&acce_bar[a]), 128);
+    }
+    fence_mbar_init_cluster();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&tmem_slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  const int num_tiles = p.tiles_m * p.tiles_n;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer ----------------
+      int s = 0;
+      uint32_t ph = 0;
+      uint32_t filled = 0;  // stages that received at least one load
+      for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+        const int tm = tile % p.tiles_m;
+        const int tn = tile / p.tiles_m;
+        for (int kt = 0; kt < p.k_tiles; ++kt) {
+          mbar_wait<false>(smem_u32(&empty_bar[s]), ph ^ 1u, p.err, failed, WAIT_LIMIT_NS, hint);
+          const uint32_t fb = smem_u32(&full_bar[s]);
+          const uint32_t sa = sbase + s * kStageBytes;
+          mbar_arrive_expect_tx(fb, kStageBytes);
+          tma_load_2d(sa, &tma_a, kt * kGemmBK, tm * kGemmBM, fb);
+          tma_load_2d(sa + kTileABytes, &tma_b, kt * kGemmBK, tn * kGemmBN, fb);
+          filled |= 1u << s;
+          if (++s == kGemmStages) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      // the CTA may not exit with a load in flight: wait (bounded) for the last
+      // load of every stage (already complete unless a wait above timed out)
+      for (int k = 0; k < kGemmStages; ++k) {
+        if (!(filled & (1u << k))) continue;
+        const uint32_t last_ph = (k < s) ? ph : (ph ^ 1u);
+        mbar_wait<false>(smem_u32(&full_bar[k]), last_ph, p.err, failed, WAIT_LIMIT_NS, hint);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer ----------------
+      int s = 0, a = 0;
+      uint32_t ph = 0, aph = 0;
+      for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+        mbar_wait<false>(smem_u32(&acce_bar[a]), aph ^ 1u, p.err, failed, WAIT_LIMIT_NS, hint);
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + static_cast<uint32_t>(a * kGemmBN);
+        for (int kt = 0; kt < p.k_tiles; ++kt) {
+          mbar_wait<false>(smem_u32(&full_bar[s]), ph, p.err, failed, WAIT_LIMIT_NS, hint);
+          tc_fence_after();
+          const uint32_t sa = sbase + s * kStageBytes;
+          const uint64_t da = smem_desc_sw128(sa);
+          const uint64_t db = smem_desc_sw128(sa + kTileABytes);
+#pragma unroll
+          for (int kk = 0; kk < kGemmBK / 16; ++kk) {
+            // advance 16 bf16 (32 bytes) along K inside the swizzled rows
+            umma_bf16(d_tmem, da + 2 * kk, db + 2 * kk, (kt | kk) != 0 ? 1u : 0u);
+          }
+          umma_commit(smem_u32(&empty_bar[s]));
+          if (++s == kGemmStages) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+        umma_commit(smem_u32(&accf_bar[a]));
+        a ^= 1;
+        if (a == 0) aph ^= 1u;
+      }
+    }
+  } else {
+    // ---------------- epilogue: warps 2..5 ----------------
+    const int q = warp & 3;  // the TMEM lane quarter this warp may access
+    int a = 0;
+    uint32_t aph = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+      const int tm = tile % p.tiles_m;
+      const int tn = tile / p.tiles_m;
+      mbar_wait<false>(smem_u32(&accf_bar[a]), aph, p.err, failed, WAIT_LIMIT_NS, hint);
+      tc_fence_after();
+      const int row = tm * kGemmBM + 32 * q + lane;
+      float* drow = p.D + static_cast<long long>(row) * p.ldd;
+#pragma unroll 1
+      for (int cc = 0; cc < kGemmBN / 32; ++cc) {
+        float v[32];
+        tmem_ld32(tmem + static_cast<uint32_t>(a * kGemmBN + cc * 32) +
+                      (static_cast<uint32_t>(32 * q) << 16),
+                  v);
+        const int col0 = tn * kGemmBN + cc * 32;
+        if (row < p.M && col0 < p.N) {
+          if (col0 + 32 <= p.N && (p.ldd & 3) == 0 &&
+              (reinterpret_cast<uintptr_t>(drow) & 15) == 0) {
+            float4* dst = reinterpret_cast<float4*>(drow + col0);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              float4 o = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+              if (p.beta != 0.f) {
+                const float4 old = dst[j];
+                o.x += old.x;
+                o.y += old.y;
+                o.z += old.z;
+                o.w += old.w;
+              }
+              dst[j] = o;
+            }
+          } else {
+            for (int j = 0; j < 32 && col0 + j < p.N; ++j)
+              drow[col0 + j] = (p.beta != 0.f) ? drow[col0 + j] + v[j] : v[j];
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(smem_u32(&acce_bar[a]));
+      a ^= 1;
+      if (a == 0) aph ^= 1u;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kTmemCols)
+                 : "memory");
+  }
+}
+
+// --- host side ---------------------------------------------------------------
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2-D bf16 tensor map over `rows` x `cols` (cols contiguous, row stride ld
+// elements) with a box of box_rows x 64 and 128-byte swizzle
+static bool make_map(CUtensorMap* map, const void* base, long long rows, long long cols,
+                     long long ld, int box_rows) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kGemmBK), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// D[M,N] = A[M,K] B[N,K]^T (+ beta D); bf16 inputs with K contiguous, fp32 D.
+// Requires K, lda, ldb multiples of 8 and 16-byte aligned A and B.
+ce_status gemm_bf16_tn(const void* A, long long lda, const void* B, long long ldb, float* D,
+                       long long ldd, int M, int N, int K, float beta, cudaStream_t stream,
+                       unsigned int* err, int sm_count, unsigned int wait_hint_ns) {
+  if (M <= 0 || N <= 0 || K <= 0) return CE_OK;
+  if ((K % 8) || (lda % 8) || (ldb % 8) || lda < K || ldb < K || ldd < N) return CE_ERR_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(A) & 15) || (reinterpret_cast<uintptr_t>(B) & 15))
+    return CE_ERR_UNSUPPORTED;
+  CUtensorMap ma, mb;
+  if (!make_map(&ma, A, M, K, lda, kGemmBM) || !make_map(&mb, B, N, K, ldb, kGemmBN))
+    return CE_ERR_CUDA;
+  GemmParams p;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.D = D;
+  p.ldd = ldd;
+  p.beta = beta;
+  p.tiles_m = (M + kGemmBM - 1) / kGemmBM;
+  p.tiles_n = (N + kGemmBN - 1) / kGemmBN;
+  p.k_tiles = (K + kGemmBK - 1) / kGemmBK;
+  p.err = err;
+  p.wait_hint_ns = wait_hint_ns;
+  if (cudaFuncSetAttribute(gemm_bf16_tn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kGemmSmem) != cudaSuccess)
+    return CE_ERR_CUDA;
+  const int tiles = p.tiles_m * p.tiles_n;
+  const int grid = tiles < sm_count ? tiles : sm_count;
+  gemm_bf16_tn_kernel<<<grid, kGemmThreads, kGemmSmem, stream>>>(ma, mb, p);
+  return cudaGetLastError() == cudaSuccess ? CE_OK : CE_ERR_CUDA;
+}
+
+}  // namespace ce
+
+namespace ce {
+
+// --- layout helpers of the fused linear + cross-entropy ------------------------
+// G16[r, c] = bf16(G[r, c]) for c < C (zero in the padding columns up to ldo) and
+// Gt16[c, r] = bf16(G[r, c]) (zero in the padding columns r >= R up to ldt).
+__global__ void convert_transpose_kernel(const float* __restrict__ G, int R, int C, long long ldg,
+                                         __nv_bfloat16* __restrict__ G16, long long ldo,
+                                         __nv_bfloat16* __restrict__ Gt16, long long ldt) {
+  __shared__ float tile[32][33];
+  const long long tiles_c = (ldo + 31) / 32;
+  const long long tiles_r = (ldt + 31) / 32;
+  for (long long tt = blockIdx.x; tt < tiles_r * tiles_c; tt += gridDim.x) {
+    const long long r0 = (tt / tiles_c) * 32, c0 = (tt % tiles_c) * 32;
+    for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+      const long long r = r0 + i, c = c0 + threadIdx.x;
+      const float v = (r < R && c < C) ? G[r * ldg + c] : 0.f;
+      tile[i][threadIdx.x] = v;
+      if (r < R && c < ldo) G16[r * ldo + c] = __float2bfloat16_rn(v);
+    }
+    __syncthreads();
+    for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+      const long long c = c0 + i, r = r0 + threadIdx.x;
+      if (c < C && r < ldt) Gt16[c * ldt + r] = __float2bfloat16_rn(tile[threadIdx.x][i]);
+    }
+    __syncthreads();
+  }
+}
+
+// T[c, r] = X[r, c] for bf16, r < R, c < C (zero in the padding columns r >= R up to ldt)
+__global__ void transpose_bf16_kernel(const __nv_bfloat16* __restrict__ X, int R, int C,
+                                      long long ldx, __nv_bfloat16* __restrict__ T, long long ldt) {
+  __shared__ __nv_bfloat16 tile[32][34];
+  const long long tiles_c = (C + 31) / 32;
+  const long long tiles_r = (ldt + 31) / 32;
+  for (long long tt = blockIdx.x; tt < tiles_r * tiles_c; tt += gridDim.x) {
+    const long long r0 = (tt / tiles_c) * 32, c0 = (tt % tiles_c) * 32;
+    for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+      const long long r = r0 + i, c = c0 + threadIdx.x;
+      tile[i][threadIdx.x] = (r < R && c < C) ? X[r * ldx + c] : __float2bfloat16_rn(0.f);
+    }
+    __syncthreads();
+    for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+      const long long c = c0 + i, r = r0 + threadIdx.x;
+      if (c < C && r < ldt) T[c * ldt + r] = tile[threadIdx.x][i];
+    }
+    __syncthreads();
+  }
+}
+
+// loss = (sum of rl[0..M)) / M: one CTA, each thread sums a fixed stride in
+// fp64, then a fixed-order tree; deterministic, no atomics
+__global__ void mean_rows_kernel(const float* __restrict__ rl, long long M, float* loss) {
+  __shared__ double part[1024];
+  double s = 0.0;
+  for (long long i = threadIdx.x; i < M; i += blockDim.x) s += static_cast<double>(rl[i]);
+  part[threadIdx.x] = s;
+  __syncthreads();
+  for (int w = blockDim.x / 2; w > 0; w >>= 1) {
+    if (threadIdx.x < w) part[threadIdx.x] += part[threadIdx.x + w];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) *loss = static_cast<float>(part[0] / static_cast<double>(M));
+}
+
+ce_status launch_convert_transpose(const float* G, int R, int C, long long ldg,
+                                   __nv_bfloat16* G16, long long ldo, __nv_bfloat16* Gt16,
+                                   long long ldt, cudaStream_t st, int sm_count) {
+  convert_transpose_kernel<<<sm_count * 8, dim3(32, 8), 0, st>>>(G, R, C, ldg, G16, ldo, Gt16,
+                                                                  ldt);
+  return cudaGetLastError() == cudaSuccess ? CE_OK : CE_ERR_CUDA;
+}
+ce_status launch_transpose_bf16(const void* X, int R, int C, long long ldx, void* T,
+                                long long ldt, cudaStream_t st, int sm_count) {
+  transpose_bf16_kernel<<<sm_count * 8, dim3(32, 8), 0, st>>>(
+      static_cast<const __nv_bfloat16*>(X), R, C, ldx, static_cast<__nv_bfloat16*>(T), ldt);
+  return cudaGetLastError() == cudaSuccess ? CE_OK : CE_ERR_CUDA;
+}
+ce_status launch_mean_rows(const float* rl, long long M, float* loss, cudaStream_t st) {
+  mean_rows_kernel<<<1, 1024, 0, st>>>(rl, M, loss);
+  return cudaGetLastError() == cudaSuccess ? CE_OK : CE_ERR_CUDA;
+}
+
+}  // namespace ce

@@ -1,0 +1,99 @@
+"""GPU parity of the tensor-core GEMM and of the fused linear + cross-entropy
+against float64 references (numpy matmul for the GEMM, the oracle's
+linear_ce for the fused path).
+
+Tolerances.  h and W are exact bf16 values, so every product is exact in
+fp32; the GEMM accumulates in fp32 on the tensor cores: |D - D_ref| <=
+1e-5 * (|A| |B|^T) covers K up to several thousand terms at 2^-24 per step.
+The gradients use G rounded to bf16 (relative 2^-9) and fp32 accumulation:
+|dH - dH_ref| <= 2^-8 (|G| |W|) and |dW - dW_ref| <= 2^-8 (|G|^T |h|),
+elementwise, with G the float64 reference gradient.  The loss follows the
+16-bit-input rule (2e-3).
+"""
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import oracle  # noqa: E402
+from softmax_cross_entropy_online_gb300 import synthetic  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def api():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from softmax_cross_entropy_online_gb300 import api as a, build
+    build.build()
+    a.lib()
+    return a
+
+
+def bf16_dev(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (200, 300, 136), (1, 1, 8), (513, 1000, 4096),
+                                   (1024, 2048, 1024), (130, 520, 72)])
+def test_gemm_against_float64(api, M, N, K):
+    rng = np.random.default_rng(M * 7 + N)
+    A = synthetic.f32_to_bf16_bits(rng.standard_normal((M, K), dtype=np.float32))
+    B = synthetic.f32_to_bf16_bits(rng.standard_normal((N, K), dtype=np.float32))
+    A64, B64 = oracle.decode_bf16(A), oracle.decode_bf16(B)
+    ref = A64 @ B64.T
+    bound = 1e-5 * (np.abs(A64) @ np.abs(B64).T) + 1e-30
+    D = api.ce_gemm_bf16_tn(bf16_dev(A), bf16_dev(B))
+    torch.cuda.synchronize()
+    err = np.abs(D.cpu().numpy().astype(np.float64) - ref)
+    assert np.all(err <= bound), f"worst {np.max(err / bound):.3g} x bound"
+    # beta = 1 accumulates into D
+    api.ce_gemm_bf16_tn(bf16_dev(A), bf16_dev(B), D, beta=1.0)
+    torch.cuda.synchronize()
+    err = np.abs(D.cpu().numpy().astype(np.float64) - 2 * ref)
+    assert np.all(err <= 2 * bound)
+    assert api.ce_check_errors() == 0
+
+
+def check_linear(api, M, H, V, seed, workspace_bytes=None):
+    h, W, t = synthetic.make_linear_ce_inputs(M, H, V, seed=seed)
+    ws = None
+    if workspace_bytes is not None:
+        ws = torch.empty(workspace_bytes, dtype=torch.uint8, device="cuda")
+    loss, dH, dW = api.linear_ce_fwd_bwd(bf16_dev(h), bf16_dev(W), torch.from_numpy(t).cuda(),
+                                         workspace=ws)
+    torch.cuda.synchronize()
+    assert api.ce_check_errors() == 0
+    h64, W64 = oracle.decode_bf16(h), oracle.decode_bf16(W)
+    ref = oracle.linear_ce(h64, W64, t, "mean")
+    assert abs(loss.item() - ref["loss"]) <= 2e-3
+    G = np.abs(ref["grad"])
+    bH = 2.0**-8 * (G @ np.abs(W64)) + 1e-30
+    eH = np.abs(dH.cpu().numpy().astype(np.float64) - ref["dH"])
+    assert np.all(eH <= bH), f"dH worst {np.max(eH / bH):.3g} x bound"
+    bW = 2.0**-8 * (G.T @ np.abs(h64)) + 1e-30
+    eW = np.abs(dW.cpu().numpy().astype(np.float64) - ref["dW"])
+    assert np.all(eW <= bW), f"dW worst {np.max(eW / bW):.3g} x bound"
+
+
+@pytest.mark.parametrize("M,H,V", [(300, 256, 1000), (257, 64, 777), (128, 4096, 2048),
+                                   (1, 8, 3), (64, 512, 50257)])
+def test_linear_ce_against_oracle(api, M, H, V):
+    check_linear(api, M, H, V, seed=M + H + V)
+
+
+def test_linear_ce_in_row_chunks(api):
+    # a workspace too small for one chunk: rows go through in chunks of 128
+    M, H, V = 700, 128, 1500
+    ws = api.linear_ce_workspace_size(128, H, V) + 4 * M + 4096
+    check_linear(api, M, H, V, seed=5, workspace_bytes=ws)
+
+
+def test_linear_ce_rejects_bad_layouts(api):
+    h = torch.zeros((4, 12), dtype=torch.bfloat16, device="cuda")  # H not a multiple of 8
+    W = torch.zeros((5, 12), dtype=torch.bfloat16, device="cuda")
+    t = torch.zeros(4, dtype=torch.int64, device="cuda")
+    with pytest.raises(api.CEError):
+        api.linear_ce_fwd_bwd(h, W, t)
