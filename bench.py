@@ -385,13 +385,135 @@ def run_native(args, w):
     return 0
 
 
+# ---------------------------------------------------------------------------
+# fused linear + cross-entropy (bf16 h [8192, 4096], W [128256, 4096])
+# ---------------------------------------------------------------------------
+LINEAR_SHAPES = {"linear_ce_8192x4096x128256": (8192, 4096, 128256)}
+
+
+def measured_tflops():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            d = json.load(fh)
+        if d.get("bf16_tflops_sustained"):
+            return float(d["bf16_tflops_sustained"]), "measured (sustained)"
+    return 1700.0, "fallback (sustained)"
+
+
+def run_linear(args):
+    import torch
+    from softmax_cross_entropy_online_gb300 import api, build
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", init_method="env://")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    build.build()
+    L = api.lib()
+    M, H, V = LINEAR_SHAPES[args.workload]
+    if args.rows is not None:
+        M = args.rows
+    h_np, W_np, t_np = synthetic.make_linear_ce_inputs(M, H, V, seed=0)
+    as_bf16 = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)  # noqa: E731
+    h_host, W_host = as_bf16(h_np).pin_memory(), as_bf16(W_np).pin_memory()
+    t_host = torch.from_numpy(t_np).pin_memory()
+    h, W, t = h_host.to(dev), W_host.to(dev), t_host.to(dev)
+    wsb = int(L.linear_ce_workspace_size(M, H, V))
+    work = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    loss = torch.empty((), dtype=torch.float32, device=dev)
+    dH = torch.empty((M, H), dtype=torch.float32, device=dev)
+    dW = torch.empty((V, H), dtype=torch.float32, device=dev)
+    sh = torch.cuda.current_stream(dev).cuda_stream
+
+    def step():
+        st = L.linear_ce_fwd_bwd(h.data_ptr(), W.data_ptr(), t.data_ptr(), M, H, V,
+                                 loss.data_ptr(), dH.data_ptr(), dW.data_ptr(),
+                                 work.data_ptr(), wsb, sh)
+        if st != 0:
+            raise api.CEError(st, "linear_ce_fwd_bwd")
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n0 = api.ce_launch_count()
+    e0.record()
+    for _ in range(args.steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    launches = api.ce_launch_count() - n0
+    clocks = sampler.stop() if sampler else None
+    ms = e0.elapsed_time(e1) / args.steps
+    flops = 6.0 * M * V * H  # logits, dH and dW GEMMs
+    value = ws * flops / (ms * 1e-3) / 1e12
+    assert api.ce_check_errors() == 0
+    # the dominant kernel (the logits GEMM of one row chunk), timed live
+    mc = min(M, 2048)
+    logits = torch.empty((mc, V), dtype=torch.float32, device=dev)
+    for _ in range(2):
+        L.ce_gemm_bf16_tn(h.data_ptr(), H, W.data_ptr(), H, logits.data_ptr(), V, mc, V, H, 0.0, sh)
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    g0.record()
+    for _ in range(5):
+        L.ce_gemm_bf16_tn(h.data_ptr(), H, W.data_ptr(), H, logits.data_ptr(), V, mc, V, H, 0.0, sh)
+    g1.record()
+    torch.cuda.synchronize()
+    gemm_ms = g0.elapsed_time(g1) / 5
+    gemm_tf = 2.0 * mc * V * H / (gemm_ms * 1e-3) / 1e12
+    peak, peak_kind = measured_tflops()
+    del logits
+    # end to end: host h, W, targets -> device, the call, loss -> host
+    loss_host = torch.empty((), dtype=torch.float32).pin_memory()
+    x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    x0.record()
+    e2e_steps = max(2, min(args.steps, 4))
+    for _ in range(e2e_steps):
+        h.copy_(h_host, non_blocking=True)
+        W.copy_(W_host, non_blocking=True)
+        t.copy_(t_host, non_blocking=True)
+        step()
+        loss_host.copy_(loss, non_blocking=True)
+    x1.record()
+    torch.cuda.synchronize()
+    e2e_ms = x0.elapsed_time(x1) / e2e_steps
+    if rank == 0:
+        line = {
+            "metric": "fused linear+CE fwd+bwd TFLOP/s (6 M V H per step)", "value": value,
+            "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"{args.workload}: bf16 h [{M}, {H}] N(0,1), W [{V}, {H}] "
+                                   "N(0, 0.02^2), int64 targets; loss, dH, dW (fp32)",
+                       "M": M, "H": H, "V": V, "workspace_bytes": wsb, "row_chunk": mc},
+            "roofline": {"bound": "tensor", "achieved": gemm_tf, "peak": peak,
+                         "unit": "TFLOP/s", "frac": gemm_tf / peak, "peak_source": peak_kind,
+                         "traffic": None, "kernel": f"logits GEMM [{mc}, {V}, {H}]",
+                         "ms_per_launch": gemm_ms},
+            "e2e": {"value": ws * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": (M * H + V * H) * 2 + M * 8, "d2h_bytes_per_step": 4,
+                    "ms_per_step": e2e_ms},
+            "gpu_launches": launches, "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
-    ap.add_argument("--workload", default="f32_32768x4096", choices=sorted(synthetic.WORKLOADS))
+    ap.add_argument("--workload", default="f32_32768x4096",
+                    choices=sorted(synthetic.WORKLOADS) + sorted(LINEAR_SHAPES))
     ap.add_argument("--max-resident-gb", type=float, default=64.0)
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     ap.add_argument("--ref-rows", type=int, default=1024)
@@ -400,6 +522,12 @@ def main():
                     help="override the workload's row count (smaller cases for profiling)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps, always
+    if args.workload in LINEAR_SHAPES:
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable":
+                              "the float64 linear+CE oracle is timed only on the CE workloads"}))
+            return 0
+        return run_linear(args)
     w = synthetic.WORKLOADS[args.workload]
     if args.rows is not None:
         w = dataclasses.replace(w, M=args.rows, name=f"{w.name}[rows={args.rows}]")

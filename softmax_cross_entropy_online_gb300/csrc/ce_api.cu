@@ -156,7 +156,8 @@ long long stage_bytes_for(int variant, int R, int CL, long long rb, bool aligned
 //    the writing modes, 256 threads with one stage (two CTAs per SM) for the
 //    forward.
 //  * longer rows: split over a cluster into slices of at most 52 KB, 256
-//    threads, two stages (two CTAs per SM); beyond 8 x 52 KB the slices grow.
+//    threads, two stages (two CTAs per SM); beyond 8 x 52 KB the slices grow
+//    and each CTA keeps one stage.
 bool choose_plan(int mode, long long rb, bool aligned, long long M, int sm_count, Plan& pl) {
   const long long cpr = chunks_for(rb, aligned);
   if (cpr * 16 <= 32 * 1024) {
@@ -195,11 +196,12 @@ bool choose_plan(int mode, long long rb, bool aligned, long long M, int sm_count
     pl = Plan{3, 1, CL, 2, static_cast<int>(stage)};
     return true;
   }
-  // very long rows: 8 CTAs, larger slices, fewer stages
+  // very long rows: 8 CTAs with larger slices and one stage each, so that
+  // several CTAs share an SM (measured: 513 KB rows run 1.6x faster than with
+  // two stages and one CTA per SM)
   const long long stage = stage_bytes_for(3, 1, ce::kMaxCluster, rb, aligned);
   if (stage == 0 || stage > kMaxSliceBytes) return false;
-  const int S = (2 * stage <= 216 * 1024) ? 2 : 1;
-  pl = Plan{3, 1, ce::kMaxCluster, S, static_cast<int>(stage)};
+  pl = Plan{3, 1, ce::kMaxCluster, 1, static_cast<int>(stage)};
   return true;
 }
 

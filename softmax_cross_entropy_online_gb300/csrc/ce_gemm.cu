@@ -335,45 +335,119 @@ namespace ce {
 // --- layout helpers of the fused linear + cross-entropy ------------------------
 // G16[r, c] = bf16(G[r, c]) for c < C (zero in the padding columns up to ldo) and
 // Gt16[c, r] = bf16(G[r, c]) (zero in the padding columns r >= R up to ldt).
-__global__ void convert_transpose_kernel(const float* __restrict__ G, int R, int C, long long ldg,
-                                         __nv_bfloat16* __restrict__ G16, long long ldo,
-                                         __nv_bfloat16* __restrict__ Gt16, long long ldt) {
-  __shared__ float tile[32][33];
-  const long long tiles_c = (ldo + 31) / 32;
-  const long long tiles_r = (ldt + 31) / 32;
+// 64x64 tiles: 16-byte loads of G, 8-byte stores of G16, and 16-byte stores
+// of Gt16 from a padded bf16 tile in shared memory (scalar loads when rows of
+// G are not 16-byte aligned).  ldo and ldt are multiples of 8.
+constexpr int kTT = 64;       // tile edge
+constexpr int kTP = kTT + 8;  // padded pitch (bf16) of the shared tile
+__global__ void __launch_bounds__(256) convert_transpose_kernel(
+    const float* __restrict__ G, int R, int C, long long ldg, __nv_bfloat16* __restrict__ G16,
+    long long ldo, __nv_bfloat16* __restrict__ Gt16, long long ldt) {
+  __shared__ __align__(16) __nv_bfloat16 tile[kTT][kTP];
+  // 16-byte loads need rows of G on the 16-byte grid
+  const bool vec = (ldg % 4 == 0) && ((reinterpret_cast<uintptr_t>(G) & 15) == 0);
+  const long long tiles_c = (ldo + kTT - 1) / kTT;
+  const long long tiles_r = (ldt + kTT - 1) / kTT;
+  const int tid = threadIdx.x;
   for (long long tt = blockIdx.x; tt < tiles_r * tiles_c; tt += gridDim.x) {
-    const long long r0 = (tt / tiles_c) * 32, c0 = (tt % tiles_c) * 32;
-    for (int i = threadIdx.y; i < 32; i += blockDim.y) {
-      const long long r = r0 + i, c = c0 + threadIdx.x;
-      const float v = (r < R && c < C) ? G[r * ldg + c] : 0.f;
-      tile[i][threadIdx.x] = v;
-      if (r < R && c < ldo) G16[r * ldo + c] = __float2bfloat16_rn(v);
+    const long long r0 = (tt / tiles_c) * kTT, c0 = (tt % tiles_c) * kTT;
+    // load: 64 rows x 16 float4, four per thread
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int idx = tid + k * 256;
+      const int rr = idx >> 4, cq = (idx & 15) * 4;
+      const long long r = r0 + rr, c = c0 + cq;
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (r < R) {
+        if (vec && c + 3 < C) {
+          v = *reinterpret_cast<const float4*>(G + r * ldg + c);
+        } else {
+          if (c + 3 < C) v.w = G[r * ldg + c + 3];
+          if (c < C) v.x = G[r * ldg + c];
+          if (c + 1 < C) v.y = G[r * ldg + c + 1];
+          if (c + 2 < C) v.z = G[r * ldg + c + 2];
+        }
+      }
+      __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+      if (r < R && c < ldo) {  // padding columns (c >= C) are written as zeros
+        uint2 pk;
+        pk.x = *reinterpret_cast<uint32_t*>(&lo);
+        pk.y = *reinterpret_cast<uint32_t*>(&hi);
+        *reinterpret_cast<uint2*>(G16 + r * ldo + c) = pk;
+      }
+      *reinterpret_cast<__nv_bfloat162*>(&tile[rr][cq]) = lo;
+      *reinterpret_cast<__nv_bfloat162*>(&tile[rr][cq + 2]) = hi;
     }
     __syncthreads();
-    for (int i = threadIdx.y; i < 32; i += blockDim.y) {
-      const long long c = c0 + i, r = r0 + threadIdx.x;
-      if (c < C && r < ldt) Gt16[c * ldt + r] = __float2bfloat16_rn(tile[threadIdx.x][i]);
+    // transposed store: 64 columns x 8 groups of 8 rows, two per thread
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int idx = tid + k * 256;
+      const int cc = idx >> 3, rg = (idx & 7) * 8;
+      const long long c = c0 + cc, r = r0 + rg;
+      if (c < C && r < ldt) {
+        uint32_t w[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          __nv_bfloat162 pr;
+          pr.x = tile[rg + 2 * j][cc];
+          pr.y = tile[rg + 2 * j + 1][cc];
+          w[j] = *reinterpret_cast<uint32_t*>(&pr);
+        }
+        *reinterpret_cast<uint4*>(Gt16 + c * ldt + r) = make_uint4(w[0], w[1], w[2], w[3]);
+      }
     }
     __syncthreads();
   }
 }
 
-// T[c, r] = X[r, c] for bf16, r < R, c < C (zero in the padding columns r >= R up to ldt)
-__global__ void transpose_bf16_kernel(const __nv_bfloat16* __restrict__ X, int R, int C,
-                                      long long ldx, __nv_bfloat16* __restrict__ T, long long ldt) {
-  __shared__ __nv_bfloat16 tile[32][34];
-  const long long tiles_c = (C + 31) / 32;
-  const long long tiles_r = (ldt + 31) / 32;
+// T[c, r] = X[r, c] for bf16, r < R, c < C (zero in the padding columns r >= R up
+// to ldt); 64x64 tiles with 16-byte loads and stores (ldx, ldt multiples of 8)
+__global__ void __launch_bounds__(256) transpose_bf16_kernel(const __nv_bfloat16* __restrict__ X,
+                                                             int R, int C, long long ldx,
+                                                             __nv_bfloat16* __restrict__ T,
+                                                             long long ldt) {
+  __shared__ __align__(16) __nv_bfloat16 tile[kTT][kTP];
+  const long long tiles_c = (C + kTT - 1) / kTT;
+  const long long tiles_r = (ldt + kTT - 1) / kTT;
+  const int tid = threadIdx.x;
   for (long long tt = blockIdx.x; tt < tiles_r * tiles_c; tt += gridDim.x) {
-    const long long r0 = (tt / tiles_c) * 32, c0 = (tt % tiles_c) * 32;
-    for (int i = threadIdx.y; i < 32; i += blockDim.y) {
-      const long long r = r0 + i, c = c0 + threadIdx.x;
-      tile[i][threadIdx.x] = (r < R && c < C) ? X[r * ldx + c] : __float2bfloat16_rn(0.f);
+    const long long r0 = (tt / tiles_c) * kTT, c0 = (tt % tiles_c) * kTT;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int idx = tid + k * 256;
+      const int rr = idx >> 3, cq = (idx & 7) * 8;
+      const long long r = r0 + rr, c = c0 + cq;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (r < R) {
+        if (c + 7 < C) {
+          v = *reinterpret_cast<const uint4*>(X + r * ldx + c);
+        } else {
+          __nv_bfloat16 e[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) e[j] = (c + j < C) ? X[r * ldx + c + j] : __float2bfloat16_rn(0.f);
+          v = *reinterpret_cast<uint4*>(e);
+        }
+      }
+      *reinterpret_cast<uint4*>(&tile[rr][cq]) = v;
     }
     __syncthreads();
-    for (int i = threadIdx.y; i < 32; i += blockDim.y) {
-      const long long c = c0 + i, r = r0 + threadIdx.x;
-      if (c < C && r < ldt) T[c * ldt + r] = tile[threadIdx.x][i];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int idx = tid + k * 256;
+      const int cc = idx >> 3, rg = (idx & 7) * 8;
+      const long long c = c0 + cc, r = r0 + rg;
+      if (c < C && r < ldt) {
+        uint32_t w[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          __nv_bfloat162 pr;
+          pr.x = tile[rg + 2 * j][cc];
+          pr.y = tile[rg + 2 * j + 1][cc];
+          w[j] = *reinterpret_cast<uint32_t*>(&pr);
+        }
+        *reinterpret_cast<uint4*>(T + c * ldt + r) = make_uint4(w[0], w[1], w[2], w[3]);
+      }
     }
     __syncthreads();
   }
@@ -397,13 +471,13 @@ __global__ void mean_rows_kernel(const float* __restrict__ rl, long long M, floa
 ce_status launch_convert_transpose(const float* G, int R, int C, long long ldg,
                                    __nv_bfloat16* G16, long long ldo, __nv_bfloat16* Gt16,
                                    long long ldt, cudaStream_t st, int sm_count) {
-  convert_transpose_kernel<<<sm_count * 8, dim3(32, 8), 0, st>>>(G, R, C, ldg, G16, ldo, Gt16,
+  convert_transpose_kernel<<<sm_count * 8, 256, 0, st>>>(G, R, C, ldg, G16, ldo, Gt16,
                                                                   ldt);
   return cudaGetLastError() == cudaSuccess ? CE_OK : CE_ERR_CUDA;
 }
 ce_status launch_transpose_bf16(const void* X, int R, int C, long long ldx, void* T,
                                 long long ldt, cudaStream_t st, int sm_count) {
-  transpose_bf16_kernel<<<sm_count * 8, dim3(32, 8), 0, st>>>(
+  transpose_bf16_kernel<<<sm_count * 8, 256, 0, st>>>(
       static_cast<const __nv_bfloat16*>(X), R, C, ldx, static_cast<__nv_bfloat16*>(T), ldt);
   return cudaGetLastError() == cudaSuccess ? CE_OK : CE_ERR_CUDA;
 }

@@ -97,3 +97,24 @@ def test_linear_ce_rejects_bad_layouts(api):
     t = torch.zeros(4, dtype=torch.int64, device="cuda")
     with pytest.raises(api.CEError):
         api.linear_ce_fwd_bwd(h, W, t)
+
+
+def test_linear_ce_full_width_sampled(api):
+    # the bench shapes' H and V at 512 rows: all of loss and dH, sampled rows of dW
+    M, H, V = 512, 4096, 128256
+    h, W, t = synthetic.make_linear_ce_inputs(M, H, V, seed=0)
+    loss, dH, dW = api.linear_ce_fwd_bwd(bf16_dev(h), bf16_dev(W), torch.from_numpy(t).cuda())
+    torch.cuda.synchronize()
+    assert api.ce_check_errors() == 0
+    h64, W64 = oracle.decode_bf16(h), oracle.decode_bf16(W)
+    logits = h64 @ W64.T
+    f = oracle.ce_fwd_bwd(logits, t, "mean")
+    assert abs(loss.item() - f["loss"]) <= 2e-3
+    G = f["grad"]
+    eH = np.abs(dH.cpu().numpy().astype(np.float64) - G @ W64)
+    assert np.all(eH <= 2.0**-8 * (np.abs(G) @ np.abs(W64)) + 1e-30)
+    rng = np.random.default_rng(1)
+    vs = np.unique(np.concatenate([t[:64], rng.choice(V, 192, replace=False), [0, V - 1]]))
+    dW_ref = G[:, vs].T @ h64
+    eW = np.abs(dW[torch.from_numpy(vs).cuda()].cpu().numpy().astype(np.float64) - dW_ref)
+    assert np.all(eW <= 2.0**-8 * (np.abs(G[:, vs]).T @ np.abs(h64)) + 1e-30)
