@@ -95,6 +95,19 @@ ce_status ce_fwd_bwd_inplace(void* logits, const int64_t* targets, int64_t M, in
                              float* row_loss, float* lse, void* stream);
 
 /*
+ * ce_softmax_forward -- fused softmax, p = exp(x - lse) per row, in one read
+ * and one write of HBM ("9 Triton kernels in 9 weeks", week one: the three
+ * passes of a softmax fused into one).  Same row machinery as ce_forward.
+ *
+ *   logits [M, V] of `dtype`, read.  probs [M, V] of `dtype`: either the
+ *   logits pointer itself (in place) or a buffer that does not overlap it and
+ *   whose address differs from the logits' by a multiple of 16 bytes (else
+ *   CE_ERR_UNSUPPORTED).  lse [M] fp32 or NULL.  No targets.
+ */
+ce_status ce_softmax_forward(const void* logits, void* probs, int64_t M, int64_t V,
+                             ce_dtype dtype, float* lse, void* stream);
+
+/*
  * ce_fwd_bwd_inplace_noalloc -- ce_fwd_bwd_inplace for callers that must not
  * allocate device memory.  (The source pages have no counterpart; this is a
  * deployment variant of the fused kernel.)

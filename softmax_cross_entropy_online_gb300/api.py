@@ -33,6 +33,7 @@ SIGNATURES = {
     "ce_fwd_bwd_inplace": (_i32, [_vp, _vp, _i64, _i64, _i32, _i32, _vp, _vp, _vp, _vp]),
     "ce_fwd_bwd_inplace_noalloc": (_i32, [_vp, _vp, _i64, _i64, _i32, _i32, _vp, _vp, _vp, _vp]),
     "ce_backward_from_lse": (_i32, [_vp, _vp, _vp, _i64, _i64, _i32, _f32, _vp]),
+    "ce_softmax_forward": (_i32, [_vp, _vp, _i64, _i64, _i32, _vp, _vp]),
     "linear_ce_fwd_bwd": (_i32, [_vp, _vp, _vp, _i64, _i64, _i64, _vp, _vp, _vp, _vp,
                                  ctypes.c_size_t, _vp]),
     "linear_ce_workspace_size": (ctypes.c_size_t, [_i64, _i64, _i64]),
@@ -221,6 +222,27 @@ def ce_gemm_bf16_tn(A: torch.Tensor, B: torch.Tensor, D: torch.Tensor | None = N
                                _stream_handle(stream, A.device))
     _check(st, "ce_gemm_bf16_tn")
     return D
+
+
+def ce_softmax_forward(logits: torch.Tensor, probs: torch.Tensor | None = None, *,
+                       lse: bool = False, stream=None):
+    """Row softmax of `logits` into `probs` (a new tensor by default; pass
+    `logits` itself for in place).  Returns (probs, lse or None)."""
+    if not logits.is_cuda or logits.dim() != 2 or not logits.is_contiguous():
+        raise ValueError("logits must be a contiguous 2-D CUDA tensor [M, V]")
+    if logits.dtype not in _DTYPES:
+        raise ValueError(f"unsupported logits dtype {logits.dtype}")
+    if probs is None:
+        probs = torch.empty_like(logits)
+    if probs.shape != logits.shape or probs.dtype != logits.dtype or not probs.is_contiguous():
+        raise ValueError("probs must match logits")
+    M, V = logits.shape
+    lse_t = torch.empty(M, dtype=torch.float32, device=logits.device) if lse else None
+    st = lib().ce_softmax_forward(logits.data_ptr(), probs.data_ptr(), M, V,
+                                  _DTYPES[logits.dtype], _ptr(lse_t),
+                                  _stream_handle(stream, logits.device))
+    _check(st, "ce_softmax_forward")
+    return probs, lse_t
 
 
 def ce_check_errors(stream=None, timeout_ms: int = 10000, device=None) -> int:

@@ -268,12 +268,13 @@ unsigned int wait_hint_ns() {
 ce_status launch_rows(int mode, const void* logits, const int64_t* targets, const float* lse_in,
                       int64_t M, int64_t V, ce_dtype dtype, ce_reduction red, float* loss,
                       float* row_loss, float* lse_out, float grad_scale, void* stream,
-                      bool static_scratch = false) {
+                      bool static_scratch = false, void* out_buf = nullptr) {
   const int es = elem_size(dtype);
   if (es == 0) return CE_ERR_INVALID_ARG;
   if (red != CE_RED_MEAN && red != CE_RED_SUM && red != CE_RED_NONE) return CE_ERR_INVALID_ARG;
   if (M < 0 || V < 1) return CE_ERR_INVALID_ARG;
-  if (M > 0 && (logits == nullptr || targets == nullptr)) return CE_ERR_INVALID_ARG;
+  if (M > 0 && (logits == nullptr || (targets == nullptr && mode != ce::SOFTMAX)))
+    return CE_ERR_INVALID_ARG;
   if (mode == ce::BWD && M > 0 && lse_in == nullptr) return CE_ERR_INVALID_ARG;
   const uintptr_t lb = reinterpret_cast<uintptr_t>(logits);
   if (lb % es) return CE_ERR_INVALID_ARG;
@@ -324,6 +325,9 @@ ce_status launch_rows(int mode, const void* logits, const int64_t* targets, cons
   }
   p.n_units = (M + pl.R - 1) / pl.R;
   p.grad_scale = grad_scale;
+  p.out_delta = (out_buf == nullptr) ? 0
+                                     : static_cast<long long>(reinterpret_cast<uintptr_t>(out_buf) -
+                                                              reinterpret_cast<uintptr_t>(logits));
   p.mean = (red == CE_RED_MEAN) ? 1 : 0;
 
   const int smem = pl.S * pl.stage_bytes;
@@ -424,6 +428,22 @@ ce_status ce_fwd_bwd_inplace_noalloc(void* logits, const int64_t* targets, int64
   const float scale = (reduction == CE_RED_MEAN && M > 0) ? 1.0f / static_cast<float>(M) : 1.0f;
   return launch_rows(ce::FWD_BWD, logits, targets, nullptr, M, V, dtype, reduction, loss,
                      row_loss, lse, scale, stream, /*static_scratch=*/true);
+}
+
+ce_status ce_softmax_forward(const void* logits, void* probs, int64_t M, int64_t V,
+                             ce_dtype dtype, float* lse, void* stream) {
+  const int es = elem_size(dtype);
+  if (es == 0 || M < 0 || V < 1) return CE_ERR_INVALID_ARG;
+  if (M > 0 && (logits == nullptr || probs == nullptr)) return CE_ERR_INVALID_ARG;
+  if (M > 0 && probs != logits) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(logits), b = reinterpret_cast<uintptr_t>(probs);
+    if (V > (INT64_MAX / 4) / es || M > (INT64_MAX / 4) / (V * es)) return CE_ERR_INVALID_ARG;
+    const uintptr_t n = static_cast<uintptr_t>(M) * static_cast<uintptr_t>(V) * es;
+    if (a < b + n && b < a + n) return CE_ERR_INVALID_ARG;  // partial overlap
+    if ((a - b) % 16) return CE_ERR_UNSUPPORTED;  // both buffers on the same 16-byte phase
+  }
+  return launch_rows(ce::SOFTMAX, logits, nullptr, nullptr, M, V, dtype, CE_RED_NONE, nullptr,
+                     nullptr, lse, 1.0f, stream, false, probs == logits ? nullptr : probs);
 }
 
 ce_status ce_backward_from_lse(void* logits, const int64_t* targets, const float* lse, int64_t M,

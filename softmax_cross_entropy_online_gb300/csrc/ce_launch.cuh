@@ -23,6 +23,7 @@ static const void* kptr_mode(int mode) {
     case FWD: return kptr<T, FWD, NC, CPT>();
     case FWD_BWD: return kptr<T, FWD_BWD, NC, CPT>();
     case BWD: return kptr<T, BWD, NC, CPT>();
+    case SOFTMAX: return kptr<T, SOFTMAX, NC, CPT>();
     default: return nullptr;
   }
 }

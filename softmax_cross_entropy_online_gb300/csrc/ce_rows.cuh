@@ -57,7 +57,9 @@ constexpr unsigned ERR_WAIT_TIMEOUT = 2u;
 constexpr unsigned long long WAIT_LIMIT_NS = 4000000000ull;  // 4 s per wait
 constexpr float kLog2e = 1.4426950408889634f;
 
-enum Mode : int { FWD = 0, FWD_BWD = 1, BWD = 2 };
+// SOFTMAX: p = exp(x - lse) (the fused softmax of "9 Triton kernels in 9
+// weeks", week one), written over the logits or into a second buffer.
+enum Mode : int { FWD = 0, FWD_BWD = 1, BWD = 2, SOFTMAX = 3 };
 
 constexpr int kMaxStages = 16;
 constexpr int kMaxCluster = 8;
@@ -90,6 +92,7 @@ struct RowParams {
   int q_chunks;               // chunk window of one CTA per unit (stage_bytes / 16)
   int log_gt;                 // log2 of the consumer threads per row group
   unsigned int wait_hint_ns;  // suspend-time hint of the mbarrier waits
+  long long out_delta;        // writes go to (address + out_delta); 0 = in place
   float grad_scale;           // FWD_BWD / BWD
   int mean;                   // 1: loss = sum / M, 0: loss = sum
 };
@@ -502,7 +505,7 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
           int lo, hi;
           bulk_range(go, lo, hi);
           if (hi > lo)
-            bulk_store(reinterpret_cast<void*>(go.as + go.hb - 16 + 16LL * lo),
+            bulk_store(reinterpret_cast<void*>(go.as + go.hb - 16 + 16LL * lo + p.out_delta),
                        stage0 + s * p.stage_bytes + (lo - go.w0) * 16, (hi - lo) * 16);
           bulk_commit();  // one group per unit (possibly empty) keeps the count exact
           const long long r = j - lag;
@@ -541,7 +544,7 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
     float lse_next = 0.f;
     {
       const long long row_first = cid * R + grp;
-      if (n_iter > 0 && row_first < p.M) {
+      if (MODE != SOFTMAX && n_iter > 0 && row_first < p.M) {
         t_next = __ldg(p.targets + row_first);
         if (MODE == BWD) lse_next = __ldg(p.lse_in + row_first);
       }
@@ -557,7 +560,7 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
       const float lse_given = lse_next;
       if (i + 1 < n_iter) {
         const long long row_n = (cid + (i + 1) * ncl) * R + grp;
-        if (row_n < p.M) {
+        if (MODE != SOFTMAX && row_n < p.M) {
           t_next = __ldg(p.targets + row_n);
           if (MODE == BWD) lse_next = __ldg(p.lse_in + row_n);
         }
@@ -625,7 +628,7 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
           const int e = e0 + q;
           if (e >= 0 && e < V) {
             if (in_smem) E::st(smem_ptr(16 * c + q * ES), gv[q]);
-            else E::st(elem_ptr_global(e), gv[q]);
+            else E::st(elem_ptr_global(e) + p.out_delta, gv[q]);
           }
         }
       };
@@ -811,10 +814,10 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
         if (p.row_loss) p.row_loss[row] = rl;
         if (p.lse_out) p.lse_out[row] = lse;
         acc += static_cast<double>(rl);
-        if (!t_ok) atomicOr(p.err, ERR_TARGET_RANGE);
+        if (!t_ok && MODE != SOFTMAX) atomicOr(p.err, ERR_TARGET_RANGE);
       }
 
-      if (MODE == FWD_BWD) {
+      if (MODE == FWD_BWD || MODE == SOFTMAX) {
         // g = e' * 2^-ml * exp(m_t - lse) * scale, exp(m_t - lse) = 2^((m_t - M) log2e - log2 S)
         const float sc = p.grad_scale;
         const float f = ex2((mt - Mg) * kLog2e - lg2(Sg) - ml) * sc;

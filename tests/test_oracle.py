@@ -356,3 +356,10 @@ def test_planted_mistakes_are_caught(kind, golden_dir):
     # and the unmutated variant passes them all
     row, loss = _forward_variant("none")(np.array([g["logits"]]), np.array([1]))
     assert abs(loss - g["loss"]) <= g["printed_tolerance"]
+
+
+def test_softmax_matches_torch_float64():
+    torch = pytest.importorskip("torch")
+    x = RNG.normal(0, 5, size=(17, 301))
+    ref = torch.softmax(torch.tensor(x, dtype=torch.float64), dim=1).numpy()
+    np.testing.assert_allclose(oracle.softmax_rows(x), ref, rtol=1e-13, atol=1e-300)
