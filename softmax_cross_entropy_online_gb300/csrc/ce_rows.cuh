@@ -693,7 +693,15 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
           }
         }
       } else {
-        for (int c = f0 + gt; c < f1; c += GT) mt = fmaxf(mt, E::chunk_max(lds128(sbase + 16 * c)));
+        // four chunks per iteration: independent shared-memory loads in flight
+        int c = f0 + gt;
+        for (; c + 3 * GT < f1; c += 4 * GT) {
+          const uint4 q0 = lds128(sbase + 16 * c), q1 = lds128(sbase + 16 * (c + GT));
+          const uint4 q2 = lds128(sbase + 16 * (c + 2 * GT)), q3 = lds128(sbase + 16 * (c + 3 * GT));
+          mt = fmaxf(mt, fmaxf(fmaxf(E::chunk_max(q0), E::chunk_max(q1)),
+                               fmaxf(E::chunk_max(q2), E::chunk_max(q3))));
+        }
+        for (; c < f1; c += GT) mt = fmaxf(mt, E::chunk_max(lds128(sbase + 16 * c)));
       }
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -726,12 +734,27 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
             st += e;
           }
       } else {
-        for (int c = f0 + gt; c < f1; c += GT) {
+        int c = f0 + gt;
+        float st1 = 0.f;  // a second partial sum shortens the dependency chain
+        for (; c + 3 * GT < f1; c += 4 * GT) {
+          float x0[EPC], x1[EPC], x2[EPC], x3[EPC];
+          E::unpack(lds128(sbase + 16 * c), x0);
+          E::unpack(lds128(sbase + 16 * (c + GT)), x1);
+          E::unpack(lds128(sbase + 16 * (c + 2 * GT)), x2);
+          E::unpack(lds128(sbase + 16 * (c + 3 * GT)), x3);
+#pragma unroll
+          for (int q = 0; q < EPC; ++q) {
+            st += ex2(fmaf(x0[q], kLog2e, -mh)) + ex2(fmaf(x1[q], kLog2e, -mh));
+            st1 += ex2(fmaf(x2[q], kLog2e, -mh)) + ex2(fmaf(x3[q], kLog2e, -mh));
+          }
+        }
+        for (; c < f1; c += GT) {
           float x[EPC];
           E::unpack(lds128(sbase + 16 * c), x);
 #pragma unroll
           for (int q = 0; q < EPC; ++q) st += ex2(fmaf(x[q], kLog2e, -mh));
         }
+        st += st1;
       }
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -833,7 +856,20 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
             }
           }
         } else {
-          for (int c = f0 + gt; c < f1; c += GT) {
+          int c = f0 + gt;
+          for (; c + 3 * GT < f1; c += 4 * GT) {
+            float x[4][EPC];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) E::unpack(lds128(sbase + 16 * (c + u * GT)), x[u]);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              float gv[EPC];
+#pragma unroll
+              for (int q = 0; q < EPC; ++q) gv[q] = ex2(fmaf(x[u][q], kLog2e, -mh)) * f;
+              sts128(sbase + 16 * (c + u * GT), E::pack(gv));
+            }
+          }
+          for (; c < f1; c += GT) {
             float x[EPC], gv[EPC];
             E::unpack(lds128(sbase + 16 * c), x);
 #pragma unroll
