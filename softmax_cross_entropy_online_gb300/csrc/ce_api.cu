@@ -3,6 +3,7 @@
 // the device error word, and the launches.  Every computation happens in the
 // kernels of ce_rows.cuh; this file only validates, plans and launches.
 #include <atomic>
+#include <cmath>
 #include <chrono>
 #include <cstdio>
 #include <cstdlib>
@@ -14,6 +15,7 @@
 
 #include "../../include/ce_gb300.h"
 #include "ce_rows.cuh"
+#include "ce_stream.cuh"
 
 namespace ce {
 template <typename T>
@@ -22,6 +24,11 @@ cudaError_t rows_launch(int mode, int variant, const RowParams& p, int grid, int
 template <typename T>
 cudaError_t rows_max_active(int mode, int variant, int smem_bytes, int CL, int sm_count,
                             int* out);
+template <typename T>
+cudaError_t stream_launch(int mode, const StreamParams& p, int grid, int nwarps, int smem_bytes,
+                          cudaStream_t stream);
+template <typename T>
+cudaError_t stream_max_active(int mode, int nwarps, int smem_bytes, int* per_sm);
 ce_status gemm_bf16_tn(const void* A, long long lda, const void* B, long long ldb, float* D,
                        long long ldd, int M, int N, int K, float beta, cudaStream_t stream,
                        unsigned int* err, int sm_count, unsigned int wait_hint_ns);
@@ -220,6 +227,81 @@ void apply_env_plan(long long rb, bool aligned, Plan& pl) {
 }
 
 // ---------------------------------------------------------------------------
+// Launch shape of the warp-streaming kernel: nw warps per CTA (one CTA per
+// SM), G warps per row, S ring slots of seg bytes per warp.
+// ---------------------------------------------------------------------------
+struct StreamPlan {
+  int nw = 16, G = 1, S = 3, seg = 4096;
+};
+
+constexpr long long kStreamSmemBudget = 200 * 1024;
+// Two-pass modes re-read each row from L2: the rows in flight at once (one per
+// group) must stay well inside the 126 MB cache.
+constexpr long long kL2ReuseBytes = 48LL << 20;
+
+int stream_slots(int nw, int seg) {
+  long long S = kStreamSmemBudget / (static_cast<long long>(nw) * seg);
+  if (S > ce::kStreamMaxSlots) S = ce::kStreamMaxSlots;
+  return static_cast<int>(S);
+}
+
+// Picks (nw, G) for the best balance of the persistent grid: each group runs
+// ceil(M / groups) rows, so the efficiency is q / ceil(q) with q = M / groups.
+// Among shapes within 1% of the best, fewer warps per row (fewer merges) and
+// then more warps per CTA win.
+bool choose_stream_plan(int mode, long long rb, long long M, int sm_count, StreamPlan& sp) {
+  const bool two_pass = mode == ce::FWD_BWD || mode == ce::SOFTMAX;
+  const long long chunks = rb / 16 + 2;
+  const int seg = 4096;
+  double best_eff = -1.0;
+  StreamPlan best;
+  bool found = false;
+  for (int pass = 0; pass < 2; ++pass) {
+    for (int G = 1; G <= ce::kStreamMaxWarps; G *= 2) {
+      if (G > 1 && chunks / G < 64) break;  // every warp streams at least 1 KB
+      for (int nw = ce::kStreamMaxWarps; nw >= 8; --nw) {
+        if (nw % G) continue;
+        const long long groups = static_cast<long long>(sm_count) * (nw / G);
+        if (two_pass && groups * rb > kL2ReuseBytes && G < ce::kStreamMaxWarps) continue;
+        const int S = stream_slots(nw, seg);
+        if (S < 2) continue;
+        const double q = static_cast<double>(M > 0 ? M : 1) / static_cast<double>(groups);
+        const double eff = q / std::ceil(q);
+        if (pass == 0) {
+          if (eff > best_eff) best_eff = eff;
+        } else if (!found && eff >= 0.99 * best_eff) {
+          best = StreamPlan{nw, G, S, seg};
+          found = true;
+        }
+      }
+    }
+  }
+  if (!found) return false;
+  sp = best;
+  return true;
+}
+
+// Tuning overrides: CE_KERNEL=stream|unit forces a kernel; CE_SPLAN="nw,G,S,seg"
+// sets the streaming shape (ignored unless it fits the kernel's limits).
+int env_kernel_choice() {
+  const char* env = std::getenv("CE_KERNEL");
+  if (env == nullptr) return 0;
+  if (std::strcmp(env, "stream") == 0) return 1;
+  if (std::strcmp(env, "unit") == 0) return 2;
+  return 0;
+}
+void apply_env_stream_plan(StreamPlan& sp) {
+  const char* env = std::getenv("CE_SPLAN");
+  if (env == nullptr || *env == 0) return;
+  int nw = 0, G = 0, S = 0, seg = 0;
+  if (std::sscanf(env, "%d,%d,%d,%d", &nw, &G, &S, &seg) != 4) return;
+  if (nw < 1 || nw > ce::kStreamMaxWarps || G < 1 || (G & (G - 1)) != 0 || nw % G != 0) return;
+  if (S < 1 || S > ce::kStreamMaxSlots || seg < 512 || seg % 512 != 0) return;
+  if (static_cast<long long>(nw) * S * seg > 220 * 1024) return;
+  sp = StreamPlan{nw, G, S, seg};
+}
+
+// ---------------------------------------------------------------------------
 // Reduction scratch for ce_fwd_bwd_inplace_noalloc.  It lives in the module's
 // own device memory (a file-scope array), so that entry point never allocates:
 // the first 256 bytes hold the ticket, then one fp64 partial sum per CTA.
@@ -263,6 +345,97 @@ unsigned int wait_hint_ns() {
   return hint;
 }
 
+// Reduction scratch for a launch of `grid` CTAs: the module's static array
+// (its ticket cleared on the stream first) or the per-stream buffer.
+ce_status reduction_scratch(bool static_scratch, int dev, void* stream, int grid, Scratch& sc) {
+  if (static_scratch) {
+    if (grid > kNoAllocPartials) return CE_ERR_UNSUPPORTED;
+    ce_status st = noalloc_scratch(sc);
+    if (st != CE_OK) return st;
+    if (cudaMemsetAsync(sc.ticket, 0, sizeof(unsigned int), static_cast<cudaStream_t>(stream)) !=
+        cudaSuccess)
+      return CE_ERR_CUDA;
+    return CE_OK;
+  }
+  if (grid > kScratchPartials) return CE_ERR_UNSUPPORTED;
+  return scratch_for(dev, stream, sc);
+}
+
+// The warp-streaming kernel; arguments already validated by launch_rows.
+ce_status launch_stream(int mode, const void* logits, const int64_t* targets, const float* lse_in,
+                        int64_t M, int64_t V, ce_dtype dtype, ce_reduction red, float* loss,
+                        float* row_loss, float* lse_out, float grad_scale, void* stream,
+                        const DeviceInfo& di, int dev, bool static_scratch, void* out_buf,
+                        const StreamPlan& sp) {
+  const long long rb = static_cast<long long>(V) * elem_size(dtype);
+  ce::StreamParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.base = static_cast<char*>(const_cast<void*>(logits));
+  p.targets = targets;
+  p.lse_in = lse_in;
+  p.row_loss = row_loss;
+  p.lse_out = lse_out;
+  p.loss = loss;
+  p.err = di.err;
+  p.M = M;
+  p.V = V;
+  p.row_bytes = rb;
+  p.G = sp.G;
+  int lg = 0;
+  while ((1 << lg) < sp.G) ++lg;
+  p.log_g = lg;
+  p.S = sp.S;
+  p.seg_bytes = sp.seg;
+  p.wait_hint_ns = wait_hint_ns();
+  p.out_delta = (out_buf == nullptr) ? 0
+                                     : static_cast<long long>(reinterpret_cast<uintptr_t>(out_buf) -
+                                                              reinterpret_cast<uintptr_t>(logits));
+  p.grad_scale = grad_scale;
+  p.mean = (red == CE_RED_MEAN) ? 1 : 0;
+
+  const int smem = sp.nw * sp.S * sp.seg;
+  int per_sm = 0;
+  cudaError_t e = cudaSuccess;
+  switch (dtype) {
+    case CE_F32: e = ce::stream_max_active<float>(mode, sp.nw, smem, &per_sm); break;
+    case CE_F16: e = ce::stream_max_active<__half>(mode, sp.nw, smem, &per_sm); break;
+    default: e = ce::stream_max_active<__nv_bfloat16>(mode, sp.nw, smem, &per_sm); break;
+  }
+  if (e != cudaSuccess || per_sm < 1) return CE_ERR_CUDA;
+  const long long groups_per_cta = sp.nw / sp.G;
+  long long grid = static_cast<long long>(per_sm) * di.sm_count;
+  const long long need = (M + groups_per_cta - 1) / groups_per_cta;  // CTAs with a row
+  if (grid > need) grid = need;
+  if (grid < 1) grid = 1;  // M == 0: one CTA writes the empty reduction
+
+  if (loss != nullptr) {
+    Scratch sc;
+    const ce_status st = reduction_scratch(static_scratch, dev, stream, static_cast<int>(grid), sc);
+    if (st != CE_OK) return st;
+    p.partials = sc.partials;
+    p.ticket = sc.ticket;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int g = static_cast<int>(grid);
+  switch (dtype) {
+    case CE_F32: e = ce::stream_launch<float>(mode, p, g, sp.nw, smem, s); break;
+    case CE_F16: e = ce::stream_launch<__half>(mode, p, g, sp.nw, smem, s); break;
+    default: e = ce::stream_launch<__nv_bfloat16>(mode, p, g, sp.nw, smem, s); break;
+  }
+  if (e != cudaSuccess) return CE_ERR_CUDA;
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return CE_OK;
+}
+
+// Which row kernel runs a call: the unit kernel (whole rows or slices resident
+// in shared memory) or the warp-streaming kernel.
+bool default_use_stream(int mode, long long rb, long long M) {
+  (void)mode;
+  (void)rb;
+  (void)M;
+  return false;
+}
+
 // static_scratch: reduce through g_noalloc_scratch (its ticket is cleared on
 // the stream before the launch) instead of the per-stream buffer.
 ce_status launch_rows(int mode, const void* logits, const int64_t* targets, const float* lse_in,
@@ -295,6 +468,16 @@ ce_status launch_rows(int mode, const void* logits, const int64_t* targets, cons
   if (st != CE_OK) return st;
 
   const bool aligned = (lb % 16 == 0) && (rb % 16 == 0);
+  {
+    const int forced = env_kernel_choice();
+    const bool use_stream = forced == 1 || (forced == 0 && default_use_stream(mode, rb, M));
+    StreamPlan sp;
+    if (use_stream && choose_stream_plan(mode, rb, M, di.sm_count, sp)) {
+      apply_env_stream_plan(sp);
+      return launch_stream(mode, logits, targets, lse_in, M, V, dtype, red, loss, row_loss,
+                           lse_out, grad_scale, stream, di, dev, static_scratch, out_buf, sp);
+    }
+  }
   Plan pl;
   if (!choose_plan(mode, rb, aligned, M, di.sm_count, pl)) return CE_ERR_UNSUPPORTED;
   apply_env_plan(rb, aligned, pl);
@@ -343,20 +526,9 @@ ce_status launch_rows(int mode, const void* logits, const int64_t* targets, cons
   if (nclusters < 1) nclusters = 1;  // M == 0: one cluster writes the empty reduction
   const int grid = static_cast<int>(nclusters * pl.CL);
 
-  if (loss != nullptr && static_scratch) {
-    if (grid > kNoAllocPartials) return CE_ERR_UNSUPPORTED;
+  if (loss != nullptr) {
     Scratch sc;
-    st = noalloc_scratch(sc);
-    if (st != CE_OK) return st;
-    if (cudaMemsetAsync(sc.ticket, 0, sizeof(unsigned int), static_cast<cudaStream_t>(stream)) !=
-        cudaSuccess)
-      return CE_ERR_CUDA;
-    p.partials = sc.partials;
-    p.ticket = sc.ticket;
-  } else if (loss != nullptr) {
-    if (grid > kScratchPartials) return CE_ERR_UNSUPPORTED;
-    Scratch sc;
-    st = scratch_for(dev, stream, sc);
+    st = reduction_scratch(static_scratch, dev, stream, grid, sc);
     if (st != CE_OK) return st;
     p.partials = sc.partials;
     p.ticket = sc.ticket;

@@ -4,6 +4,7 @@
 #pragma once
 
 #include "ce_rows.cuh"
+#include "ce_stream.cuh"
 
 namespace ce {
 
@@ -100,9 +101,51 @@ cudaError_t rows_max_active(int mode, int variant, int smem_bytes, int CL, int s
   return e;
 }
 
+// ---- the warp-streaming kernel (ce_stream.cuh) ----
+template <typename T>
+const void* stream_kernel_ptr(int mode) {
+  switch (mode) {
+    case FWD: return reinterpret_cast<const void*>(&ce_stream_kernel<T, FWD>);
+    case FWD_BWD: return reinterpret_cast<const void*>(&ce_stream_kernel<T, FWD_BWD>);
+    case BWD: return reinterpret_cast<const void*>(&ce_stream_kernel<T, BWD>);
+    case SOFTMAX: return reinterpret_cast<const void*>(&ce_stream_kernel<T, SOFTMAX>);
+    default: return nullptr;
+  }
+}
+
+template <typename T>
+cudaError_t stream_launch(int mode, const StreamParams& p, int grid, int nwarps, int smem_bytes,
+                          cudaStream_t stream) {
+  const void* fn = stream_kernel_ptr<T>(mode);
+  if (fn == nullptr || nwarps < 1 || nwarps > kStreamMaxWarps) return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(nwarps * 32), 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem_bytes);
+  cfg.stream = stream;
+  void* args[] = {const_cast<StreamParams*>(&p)};
+  return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+// CTAs of the streaming kernel that fit on one SM at once.
+template <typename T>
+cudaError_t stream_max_active(int mode, int nwarps, int smem_bytes, int* per_sm) {
+  const void* fn = stream_kernel_ptr<T>(mode);
+  if (fn == nullptr) return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+  if (e != cudaSuccess) return e;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, fn, nwarps * 32,
+                                                       static_cast<size_t>(smem_bytes));
+}
+
 #define CE_INSTANTIATE_ROWS(T)                                                                  \
   template const void* rows_kernel_ptr<T>(int, int);                                            \
   template cudaError_t rows_launch<T>(int, int, const RowParams&, int, int, cudaStream_t);      \
-  template cudaError_t rows_max_active<T>(int, int, int, int, int, int*);
+  template cudaError_t rows_max_active<T>(int, int, int, int, int, int*);                       \
+  template const void* stream_kernel_ptr<T>(int);                                               \
+  template cudaError_t stream_launch<T>(int, const StreamParams&, int, int, int, cudaStream_t); \
+  template cudaError_t stream_max_active<T>(int, int, int, int*);
 
 }  // namespace ce

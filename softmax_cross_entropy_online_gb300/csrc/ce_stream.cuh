@@ -1,0 +1,478 @@
+// ce_stream.cuh -- the warp-streaming row kernel (sm_103a).
+//
+// Same operations and outputs as ce_rows_kernel (FWD, FWD_BWD, BWD, SOFTMAX),
+// organised for a continuous stream instead of whole units in shared memory:
+//
+//  * Every warp is its own producer and consumer.  It owns a ring of S
+//    shared-memory slots of `seg_bytes` each; lane 0 fills them with 1-D TMA
+//    bulk copies (cp.async.bulk, completion on the slot's mbarrier) and
+//    refills a slot as soon as the warp has read it.  No CTA-wide barrier
+//    ever waits for the slowest warp, and the warp starts computing as soon
+//    as the first segment of a row has landed.
+//  * A row is handled by a group of G warps (G = 1: a warp per row).  The
+//    row's 16-byte chunks (the same absolute-address chunk frame as the unit
+//    kernel: chunk c covers [A0 - 16 + 16c, A0 + 16c), A0 = ceil16(row start),
+//    partial head/tail chunks handled element by element) are split into G
+//    contiguous pieces, and each warp streams its piece in segments.
+//  * Statistics pass: each lane keeps an online pair (m, s) -- the running
+//    max and the sum of exp(x - m), rescaled when m grows (the online
+//    softmax recurrence of the "POPCORNBENCH level-1 problem 95 transcript"
+//    and its merge of two pairs).  Lanes merge by shuffles, the group's warps
+//    through shared memory and one named barrier.
+//  * Gradient pass (FWD_BWD, SOFTMAX, and the only pass of BWD): the piece is
+//    streamed again -- from L2, where the statistics pass left it (its loads
+//    carry an evict_last policy, the second pass evict_first) -- and
+//    g = exp(x - lse) * scale (the target's g = expm1(x_t - lse) * scale) is
+//    written with 16-byte stores.  The second pass's loads are issued before
+//    the group's merge completes, so the barrier never drains the stream.
+//  * Mean: per-group fp64 sums in row order, per-CTA partials, the last CTA
+//    (integer ticket) adds them in index order: no floating-point atomics.
+#pragma once
+
+#include "ce_rows.cuh"
+
+namespace ce {
+
+constexpr int kStreamMaxWarps = 16;
+constexpr int kStreamMaxSlots = 8;
+constexpr int kStreamKPL = 8;  // 16-byte chunks a lane holds in registers per sub-block
+
+struct StreamParams {
+  char* base;                 // logits (byte address)
+  const int64_t* targets;     // [M] (null for SOFTMAX)
+  const float* lse_in;        // [M], BWD only
+  float* row_loss;            // [M] or null
+  float* lse_out;             // [M] or null
+  float* loss;                // [1] or null
+  double* partials;           // [gridDim.x] scratch when loss != null
+  unsigned int* ticket;       // scratch counter when loss != null
+  unsigned int* err;          // device error word
+  long long M, V;
+  long long row_bytes;        // V * sizeof(T)
+  int G;                      // warps per row (a power of two dividing the warps per CTA)
+  int log_g;                  // log2(G)
+  int S;                      // ring slots per warp
+  int seg_bytes;              // bytes per slot (a multiple of 16)
+  unsigned int wait_hint_ns;  // suspend-time hint of the mbarrier waits
+  long long out_delta;        // writes go to (address + out_delta); 0 = in place
+  float grad_scale;           // FWD_BWD / BWD
+  int mean;                   // 1: loss = sum / M, 0: loss = sum
+};
+
+// Chunk frame of one row and this warp's piece of it.
+struct StreamGeo {
+  long long as;     // absolute address of the row's first byte
+  int hb;           // bytes from `as` to the next 16-byte boundary
+  int nI;           // interior (full) chunks 1..nI
+  int p0, p1;       // this warp's piece [p0, p1) of the row's chunks
+  int ld_lo, ld_hi; // chunks that TMA may read: [ld_lo, ld_hi)
+  int ns;           // segments of the piece
+};
+
+__device__ __forceinline__ StreamGeo stream_geo(const StreamParams& p, long long r, int kw,
+                                                int seg_chunks) {
+  StreamGeo g;
+  const long long off = r * p.row_bytes;
+  g.as = reinterpret_cast<long long>(p.base) + off;
+  g.hb = static_cast<int>((-g.as) & 15);
+  const int rb = static_cast<int>(p.row_bytes);
+  int c_last;
+  if (rb > g.hb) {
+    g.nI = (rb - g.hb) >> 4;
+    c_last = ((rb - g.hb) & 15) ? g.nI + 1 : g.nI;
+  } else {  // the whole row sits before the first 16-byte boundary
+    g.nI = 0;
+    c_last = 0;
+  }
+  const int c_first = g.hb ? 0 : 1;
+  const int nc = c_last - c_first + 1;
+  const int Q = (nc + p.G - 1) >> p.log_g;
+  int a = c_first + kw * Q;
+  int b = a + Q;
+  if (a > c_last + 1) a = c_last + 1;
+  if (b > c_last + 1) b = c_last + 1;
+  g.p0 = a;
+  g.p1 = b;
+  g.ns = (b - a + seg_chunks - 1) / seg_chunks;
+  // A partial chunk also holds bytes of the neighbouring row.  Reading them
+  // (and ignoring them) is harmless while the 16 bytes lie inside the tensor;
+  // writes to a partial chunk are always element by element.
+  const long long total = p.M * p.row_bytes;
+  const bool head_ok = c_first == 0 && off + g.hb - 16 >= 0 && off + g.hb <= total;
+  const bool tail_ok = c_last == g.nI + 1 && off + g.hb + 16LL * (g.nI + 1) <= total;
+  g.ld_lo = head_ok ? 0 : 1;
+  g.ld_hi = tail_ok ? g.nI + 2 : g.nI + 1;
+  return g;
+}
+
+__device__ __forceinline__ unsigned long long l2_policy_evict_last() {
+  unsigned long long pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ unsigned long long l2_policy_evict_first() {
+  unsigned long long pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ void bulk_load_hint(uint32_t dst_smem, const void* src, uint32_t bytes,
+                                               uint32_t bar, unsigned long long pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(dst_smem),
+      "l"(src), "r"(bytes), "r"(bar), "l"(pol)
+      : "memory");
+}
+__device__ __forceinline__ void stg128_hint(void* dst, uint4 v, unsigned long long pol) {
+  asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(dst),
+               "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "l"(pol)
+               : "memory");
+}
+
+// Online update of a lane's pair with a block of values whose max is lm.
+// s and s1 (two partial sums, for a shorter dependency chain) hold
+// sum 2^(x log2e - mh) with mh = RN(m log2e); while m = -inf, mh = 0, so
+// -inf logits give exp2(-inf) = 0 rather than NaN.
+__device__ __forceinline__ void online_rescale(float lm, float& m, float& mh, float& s, float& s1) {
+  if (lm > m) {
+    const float mhn = lm * kLog2e;
+    const float f = (m == -INFINITY) ? 0.f : ex2(mh - mhn);
+    s *= f;
+    s1 *= f;
+    m = lm;
+    mh = mhn;
+  }
+}
+
+template <typename T, int MODE>
+__global__ void __launch_bounds__(kStreamMaxWarps * 32, 1) ce_stream_kernel(const StreamParams p) {
+  using E = Elem<T>;
+  constexpr int EPC = E::EPC;
+  constexpr int ES = E::ES;
+  constexpr int LOG_ES = (ES == 4) ? 2 : 1;
+  constexpr bool STATS = MODE != BWD;                  // a statistics pass
+  constexpr bool GRAD = MODE != FWD;                   // a gradient / probability pass
+  constexpr bool TARGETS = MODE != SOFTMAX;
+  constexpr int NPASS = (STATS && GRAD) ? 2 : 1;
+
+  extern __shared__ __align__(128) unsigned char ring_mem[];
+  __shared__ __align__(8) unsigned long long full_bar[kStreamMaxWarps][kStreamMaxSlots];
+  __shared__ float2 red[2][kStreamMaxWarps];
+  __shared__ double acc_slot[kStreamMaxWarps];
+
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int nwarps = blockDim.x >> 5;
+  const int G = p.G;
+  const int kw = warp & (G - 1);       // this warp's piece of the group's rows
+  const int grp = warp >> p.log_g;     // row group within the CTA
+  const int ngrp_cta = nwarps >> p.log_g;
+  const long long gidx = static_cast<long long>(blockIdx.x) * ngrp_cta + grp;
+  const long long ngroups = static_cast<long long>(gridDim.x) * ngrp_cta;
+  const long long n_rows = gidx < p.M ? (p.M - 1 - gidx) / ngroups + 1 : 0;
+  const int S = p.S;
+  const int SB = p.seg_bytes;
+  const int SC = SB >> 4;  // chunks per segment
+  const uint32_t ring = smem_u32(ring_mem) + static_cast<uint32_t>(warp * S * SB);
+  const int V = static_cast<int>(p.V);  // the host caps V * sizeof(T) far below 2^31
+  bool failed = false;
+
+  if (lane == 0) {
+    for (int s = 0; s < S; ++s) mbar_init(smem_u32(&full_bar[warp][s]), 1);
+    fence_mbar_init_cluster();
+  }
+  __syncthreads();
+
+  const unsigned long long pol_keep = l2_policy_evict_last();
+  const unsigned long long pol_drop = l2_policy_evict_first();
+
+  // ---- the load cursor (lane 0): the k-th load fills slot k % S ----
+  long long i_ri = 0;
+  int i_pass = 0, i_seg = 0, i_slot = 0;
+  StreamGeo ig;
+  if (lane == 0 && n_rows > 0) ig = stream_geo(p, gidx, kw, SC);
+  auto issue_next = [&]() {
+    while (i_ri < n_rows && i_seg >= ig.ns) {
+      i_seg = 0;
+      if (++i_pass == NPASS) {
+        i_pass = 0;
+        if (++i_ri < n_rows) ig = stream_geo(p, gidx + i_ri * ngroups, kw, SC);
+      }
+    }
+    if (i_ri >= n_rows) return;
+    const int c0 = ig.p0 + i_seg * SC;
+    int c1 = c0 + SC;
+    if (c1 > ig.p1) c1 = ig.p1;
+    const int lo = c0 > ig.ld_lo ? c0 : ig.ld_lo;
+    const int hi = c1 < ig.ld_hi ? c1 : ig.ld_hi;
+    const uint32_t fb = smem_u32(&full_bar[warp][i_slot]);
+    fence_proxy_async_smem();  // the warp's reads of this slot precede the refill
+    if (hi > lo) {
+      mbar_arrive_expect_tx(fb, static_cast<uint32_t>((hi - lo) * 16));
+      // kept in L2 only when a second pass will read it again
+      const bool keep = NPASS == 2 && i_pass == 0;
+      bulk_load_hint(ring + i_slot * SB + (lo - c0) * 16,
+                     reinterpret_cast<const void*>(ig.as + ig.hb - 16 + 16LL * lo),
+                     static_cast<uint32_t>((hi - lo) * 16), fb, keep ? pol_keep : pol_drop);
+    } else {
+      mbar_arrive(fb);
+    }
+    ++i_seg;
+    if (++i_slot == S) i_slot = 0;
+  };
+  if (lane == 0)
+    for (int k = 0; k < S; ++k) issue_next();
+
+  // the consumer side: the k-th segment sits in slot k % S, phase (k / S) & 1
+  int c_slot = 0;
+  uint32_t c_phase = 0;
+  auto wait_segment = [&]() -> uint32_t {
+    mbar_wait<false>(smem_u32(&full_bar[warp][c_slot]), c_phase, p.err, failed, WAIT_LIMIT_NS,
+                     p.wait_hint_ns);
+    return ring + c_slot * SB;
+  };
+  auto release_segment = [&]() {
+    __syncwarp();
+    if (lane == 0) issue_next();
+    if (++c_slot == S) {
+      c_slot = 0;
+      c_phase ^= 1u;
+    }
+  };
+
+  double acc = 0.0;  // the group's loss sum (warp kw == 0, lane 0)
+  long long t_next = -1;
+  float lse_next = 0.f;
+  if (TARGETS && n_rows > 0) t_next = __ldg(p.targets + gidx);
+  if (MODE == BWD && n_rows > 0) lse_next = __ldg(p.lse_in + gidx);
+
+  for (long long ri = 0; ri < n_rows; ++ri) {
+    const long long r = gidx + ri * ngroups;
+    const StreamGeo g = stream_geo(p, r, kw, SC);
+    const long long t = t_next;
+    const float lse_given = lse_next;
+    if (ri + 1 < n_rows) {
+      if (TARGETS) t_next = __ldg(p.targets + r + ngroups);
+      if (MODE == BWD) lse_next = __ldg(p.lse_in + r + ngroups);
+    }
+    const bool t_ok = TARGETS && t >= 0 && t < V;
+    // the target's chunk and its slot in the chunk
+    const int tbo = t_ok ? static_cast<int>(t) * ES + 16 - g.hb : -1;
+    const int tc = t_ok ? (tbo >> 4) : -1;
+    const int tq = t_ok ? ((tbo & 15) >> LOG_ES) : 0;
+    const int b = static_cast<int>(ri & 1);
+    const bool row_leader = kw == 0 && lane == 0;
+    // the target logit, read before any gradient of this row is written
+    float xt = 0.f;
+    if (MODE != BWD && MODE != SOFTMAX && row_leader && t_ok)
+      xt = E::ld(reinterpret_cast<const char*>(g.as) + t * ES);
+
+    // element e of the row, -inf outside it; from the slot when TMA loaded it
+    auto edge_vals = [&](int c, int c0, uint32_t sbase, float* v) {
+      const int e0 = (g.hb - 16 + 16 * c) >> LOG_ES;
+      const bool in_smem = c >= g.ld_lo && c < g.ld_hi;
+#pragma unroll
+      for (int q = 0; q < EPC; ++q) {
+        const int e = e0 + q;
+        float x = -INFINITY;
+        if (e >= 0 && e < V) {
+          x = in_smem ? E::ld(static_cast<char*>(__cvta_shared_to_generic(sbase + 16 * (c - c0) + q * ES)))
+                      : E::ld(reinterpret_cast<const char*>(g.as) + static_cast<long long>(e) * ES);
+        }
+        v[q] = x;
+      }
+    };
+
+    float Mrow = 0.f, Srow = 1.f;  // row max and sum of exp(x - max)
+    if (STATS) {
+      float m = -INFINITY, mh = 0.f, s = 0.f, s1 = 0.f;
+      for (int sg = 0; sg < g.ns; ++sg) {
+        const int c0 = g.p0 + sg * SC;
+        const int c1 = (c0 + SC < g.p1) ? c0 + SC : g.p1;
+        const uint32_t sbase = wait_segment();
+        const int fa = c0 > 1 ? c0 : 1;                      // full chunks [fa, fb)
+        const int fb = c1 < g.nI + 1 ? c1 : g.nI + 1;
+        for (int cb = fa; cb < fb; cb += 32 * kStreamKPL) {
+          uint4 q[kStreamKPL];
+          float lm = -INFINITY;
+#pragma unroll
+          for (int j = 0; j < kStreamKPL; ++j) {
+            const int c = cb + lane + 32 * j;
+            if (c < fb) {
+              q[j] = lds128(sbase + 16 * (c - c0));
+              lm = fmaxf(lm, E::chunk_max(q[j]));
+            }
+          }
+          online_rescale(lm, m, mh, s, s1);
+#pragma unroll
+          for (int j = 0; j < kStreamKPL; ++j) {
+            const int c = cb + lane + 32 * j;
+            if (c < fb) {
+              float x[EPC];
+              E::unpack(q[j], x);
+#pragma unroll
+              for (int e = 0; e < EPC; e += 2) {
+                s += ex2(fmaf(x[e], kLog2e, -mh));
+                s1 += ex2(fmaf(x[e + 1], kLog2e, -mh));
+              }
+            }
+          }
+        }
+        // the partial head and tail chunks of the row, element by element
+        if (c0 <= 0 && 0 < c1 && lane == 0) {
+          float x[EPC];
+          edge_vals(0, c0, sbase, x);
+          float lm = -INFINITY;
+#pragma unroll
+          for (int e = 0; e < EPC; ++e) lm = fmaxf(lm, x[e]);
+          online_rescale(lm, m, mh, s, s1);
+#pragma unroll
+          for (int e = 0; e < EPC; ++e) s += ex2(fmaf(x[e], kLog2e, -mh));
+        }
+        if (g.nI + 1 >= c0 && g.nI + 1 < c1 && lane == 1) {
+          float x[EPC];
+          edge_vals(g.nI + 1, c0, sbase, x);
+          float lm = -INFINITY;
+#pragma unroll
+          for (int e = 0; e < EPC; ++e) lm = fmaxf(lm, x[e]);
+          online_rescale(lm, m, mh, s, s1);
+#pragma unroll
+          for (int e = 0; e < EPC; ++e) s += ex2(fmaf(x[e], kLog2e, -mh));
+        }
+        release_segment();
+      }
+      s += s1;
+      // ---- merge: lanes, then the group's warps ----
+      const float mref = (m == -INFINITY) ? 0.f : m;
+      const float ml = fmaf(mref, kLog2e, -mh);
+      const float mw = warp_max(m);
+      float sw = (m == -INFINITY) ? 0.f : s * ex2((m - mw) * kLog2e - ml);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sw += __shfl_xor_sync(0xffffffffu, sw, o);
+      if (G == 1) {
+        Mrow = mw;
+        Srow = sw;
+      } else {
+        if (lane == 0) red[b][warp] = make_float2(mw, sw);
+        group_sync(1 + grp, G * 32);
+        const float2 rr = (lane < G) ? red[b][grp * G + lane] : make_float2(-INFINITY, 0.f);
+        Mrow = warp_max(rr.x);
+        float sg2 = (rr.x == -INFINITY) ? 0.f : rr.y * ex2((rr.x - Mrow) * kLog2e);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sg2 += __shfl_xor_sync(0xffffffffu, sg2, o);
+        Srow = sg2;
+      }
+      if (row_leader) {
+        const float lnS = logf(Srow);
+        const float rl = t_ok ? (Mrow - xt) + lnS : __int_as_float(0x7fc00000);
+        if (p.row_loss) p.row_loss[r] = rl;
+        if (p.lse_out) p.lse_out[r] = Mrow + lnS;
+        acc += static_cast<double>(rl);
+        if (TARGETS && !t_ok) atomicOr(p.err, ERR_TARGET_RANGE);
+      }
+    } else if (row_leader && !t_ok) {
+      atomicOr(p.err, ERR_TARGET_RANGE);
+    }
+
+    if (GRAD) {
+      const float sc = p.grad_scale;
+      // g = 2^(x log2e - Lh - Lc) * scale with Lh + Lc = lse log2e split into
+      // a float and a small correction: the FFMA gives x log2e - Lh with one
+      // rounding, the correction is a factor taken once per row.
+      float Lh, Lc, lnS = 0.f;
+      if (MODE == BWD) {
+        Lh = lse_given * kLog2e;
+        Lc = fmaf(lse_given, kLog2e, -Lh);
+      } else {
+        const float mref = (Mrow == -INFINITY) ? 0.f : Mrow;
+        const float mhr = mref * kLog2e;
+        const float mlr = fmaf(mref, kLog2e, -mhr);
+        const float l2s = lg2(Srow);
+        Lh = mhr + l2s;
+        // two-sum: (mhr + l2s) - Lh exactly
+        const float bv = Lh - mhr;
+        const float rem = (mhr - (Lh - bv)) + (l2s - bv);
+        Lc = mlr + rem;
+        lnS = logf(Srow);
+      }
+      const float scf = ex2(-Lc) * sc;
+      // g_t = expm1(x_t - lse) * scale, evaluated from the target's own value
+      auto target_grad = [&](float x) -> float {
+        return MODE == BWD ? expm1f(x - lse_given) * sc : expm1f((x - Mrow) - lnS) * sc;
+      };
+      char* const out_row = reinterpret_cast<char*>(g.as) + p.out_delta;
+      for (int sg = 0; sg < g.ns; ++sg) {
+        const int c0 = g.p0 + sg * SC;
+        const int c1 = (c0 + SC < g.p1) ? c0 + SC : g.p1;
+        const uint32_t sbase = wait_segment();
+        const int fa = c0 > 1 ? c0 : 1;
+        const int fb = c1 < g.nI + 1 ? c1 : g.nI + 1;
+        for (int cb = fa + lane; cb < fb; cb += 128) {
+          uint4 q[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (cb + 32 * j < fb) q[j] = lds128(sbase + 16 * (cb + 32 * j - c0));
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int c = cb + 32 * j;
+            if (c < fb) {
+              float x[EPC], gv[EPC];
+              E::unpack(q[j], x);
+#pragma unroll
+              for (int e = 0; e < EPC; ++e) gv[e] = ex2(fmaf(x[e], kLog2e, -Lh)) * scf;
+              if (c == tc) {
+#pragma unroll
+                for (int e = 0; e < EPC; ++e)
+                  if (e == tq) gv[e] = target_grad(x[e]);
+              }
+              stg128_hint(out_row + (g.hb - 16 + 16LL * c), E::pack(gv), pol_drop);
+            }
+          }
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int c = h ? g.nI + 1 : 0;
+          const bool mine = h ? (lane == 1 && c >= c0 && c < c1) : (lane == 0 && c0 <= 0 && 0 < c1);
+          if (mine) {
+            float x[EPC];
+            edge_vals(c, c0, sbase, x);
+            const int e0 = (g.hb - 16 + 16 * c) >> LOG_ES;
+#pragma unroll
+            for (int q = 0; q < EPC; ++q) {
+              const int e = e0 + q;
+              if (e >= 0 && e < V) {
+                const float gv = (t_ok && e == static_cast<int>(t))
+                                     ? target_grad(x[q])
+                                     : ex2(fmaf(x[q], kLog2e, -Lh)) * scf;
+                E::st(out_row + static_cast<long long>(e) * ES, gv);
+              }
+            }
+          }
+        }
+        release_segment();
+      }
+    }
+  }
+
+  // ---- deterministic reduction of the loss ----
+  if (STATS && p.loss != nullptr) {
+    if (kw == 0 && lane == 0) acc_slot[grp] = acc;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      double part = 0.0;
+      for (int j = 0; j < ngrp_cta; ++j) part += acc_slot[j];
+      p.partials[blockIdx.x] = part;
+      __threadfence();
+      const unsigned prev = atomicAdd(p.ticket, 1u);
+      if (prev == gridDim.x - 1) {
+        __threadfence();
+        double total = 0.0;
+        for (unsigned j = 0; j < gridDim.x; ++j) total += __ldcg(p.partials + j);
+        *p.loss = static_cast<float>(p.mean ? total / static_cast<double>(p.M) : total);
+        *p.ticket = 0u;  // ready for the next launch on this stream
+      }
+    }
+  }
+}
+
+}  // namespace ce
