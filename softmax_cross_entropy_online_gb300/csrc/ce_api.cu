@@ -235,9 +235,6 @@ struct StreamPlan {
 };
 
 constexpr long long kStreamSmemBudget = 200 * 1024;
-// Two-pass modes re-read each row from L2: the rows in flight at once (one per
-// group) must stay well inside the 126 MB cache.
-constexpr long long kL2ReuseBytes = 48LL << 20;
 
 int stream_slots(int nw, int seg) {
   long long S = kStreamSmemBudget / (static_cast<long long>(nw) * seg);
@@ -245,39 +242,30 @@ int stream_slots(int nw, int seg) {
   return static_cast<int>(S);
 }
 
-// Picks (nw, G) for the best balance of the persistent grid: each group runs
-// ceil(M / groups) rows, so the efficiency is q / ceil(q) with q = M / groups.
-// Among shapes within 1% of the best, fewer warps per row (fewer merges) and
-// then more warps per CTA win.
+// Launch shape of the streaming kernel, from sweeps on GB300 (16 warps per CTA
+// with three 4 KB slots each beat every smaller CTA, deeper ring and other
+// segment size measured):
+//  * one pass (FWD, BWD): a warp per row while every warp gets at least six
+//    rows; otherwise the fewest warps per row that give each group twelve,
+//    keeping at least 8 KB of the row per warp.  Long pieces with enough rows
+//    per group won (fp16 256 KB rows: 4 warps per row 97%, 16 warps 88%).
+//  * two passes (FWD_BWD, SOFTMAX): 16 warps per row, so that the rows in
+//    flight (one per CTA) stay in L2 until the second pass re-reads them.
 bool choose_stream_plan(int mode, long long rb, long long M, int sm_count, StreamPlan& sp) {
-  const bool two_pass = mode == ce::FWD_BWD || mode == ce::SOFTMAX;
-  const long long chunks = rb / 16 + 2;
+  const int nw = ce::kStreamMaxWarps;
   const int seg = 4096;
-  double best_eff = -1.0;
-  StreamPlan best;
-  bool found = false;
-  for (int pass = 0; pass < 2; ++pass) {
-    for (int G = 1; G <= ce::kStreamMaxWarps; G *= 2) {
-      if (G > 1 && chunks / G < 64) break;  // every warp streams at least 1 KB
-      for (int nw = ce::kStreamMaxWarps; nw >= 8; --nw) {
-        if (nw % G) continue;
-        const long long groups = static_cast<long long>(sm_count) * (nw / G);
-        if (two_pass && groups * rb > kL2ReuseBytes && G < ce::kStreamMaxWarps) continue;
-        const int S = stream_slots(nw, seg);
-        if (S < 2) continue;
-        const double q = static_cast<double>(M > 0 ? M : 1) / static_cast<double>(groups);
-        const double eff = q / std::ceil(q);
-        if (pass == 0) {
-          if (eff > best_eff) best_eff = eff;
-        } else if (!found && eff >= 0.99 * best_eff) {
-          best = StreamPlan{nw, G, S, seg};
-          found = true;
-        }
-      }
+  const bool two_pass = mode == ce::FWD_BWD || mode == ce::SOFTMAX;
+  int G = 1;
+  if (two_pass) {
+    G = nw;
+  } else {
+    const long long warps = static_cast<long long>(sm_count) * nw;
+    if (M < 6 * warps) {
+      while (G < nw && M * G < 12 * warps) G *= 2;
     }
+    while (G > 1 && rb / G < 8192) G /= 2;
   }
-  if (!found) return false;
-  sp = best;
+  sp = StreamPlan{nw, G, stream_slots(nw, seg), seg};
   return true;
 }
 
@@ -427,13 +415,16 @@ ce_status launch_stream(int mode, const void* logits, const int64_t* targets, co
   return CE_OK;
 }
 
-// Which row kernel runs a call: the unit kernel (whole rows or slices resident
-// in shared memory) or the warp-streaming kernel.
-bool default_use_stream(int mode, long long rb, long long M) {
-  (void)mode;
-  (void)rb;
-  (void)M;
-  return false;
+// Which row kernel runs a call (from sweeps on GB300): the streaming kernel
+// for the forward at every row length (1.1x to 2.3x the unit kernel) and for
+// the writing modes once a row no longer fits one CTA's shared memory twice
+// (where the unit kernel would split it over a cluster); the unit kernel for
+// the writing modes on shorter rows, where its single read of each row
+// (against the streaming kernel's read and L2 re-read) wins.
+bool default_use_stream(int mode, long long rb, bool aligned) {
+  if (mode == ce::FWD) return true;
+  const long long cpr = chunks_for(rb, aligned);
+  return 2 * cpr * 16 > 216 * 1024;
 }
 
 // static_scratch: reduce through g_noalloc_scratch (its ticket is cleared on
@@ -468,9 +459,10 @@ ce_status launch_rows(int mode, const void* logits, const int64_t* targets, cons
   if (st != CE_OK) return st;
 
   const bool aligned = (lb % 16 == 0) && (rb % 16 == 0);
+  if (V > ce_max_vocab(dtype)) return CE_ERR_UNSUPPORTED;  // the same limit for both kernels
   {
     const int forced = env_kernel_choice();
-    const bool use_stream = forced == 1 || (forced == 0 && default_use_stream(mode, rb, M));
+    const bool use_stream = forced == 1 || (forced == 0 && default_use_stream(mode, rb, aligned));
     StreamPlan sp;
     if (use_stream && choose_stream_plan(mode, rb, M, di.sm_count, sp)) {
       apply_env_stream_plan(sp);

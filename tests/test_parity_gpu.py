@@ -117,6 +117,18 @@ def test_sweep_vocab(dtype, V):
     check_case(x, t, dtype)
 
 
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("V", [1, 7, 129, 4097, 50257, 131072, 300007])
+def test_unit_kernel_in_every_mode(dtype, V, monkeypatch):
+    # the forward (and the longest rows) default to the streaming kernel; the
+    # unit kernel stays selectable and must agree with the oracle everywhere
+    monkeypatch.setenv("CE_KERNEL", "unit")
+    M = max(2, min(200, (2 << 20) // V))
+    x = synthetic.make_logits(M, V, dtype, 2.0, seed=V + 7)
+    t = synthetic.make_targets(M, V, seed=V + 8)
+    check_case(x, t, dtype)
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("M", [1, 2, 3, 5, 151, 152, 153, 1000, 4099])
 def test_sweep_rows(dtype, M):
@@ -262,6 +274,7 @@ def test_side_stream():
     ("4,4,1,3", "f16", 1000), ("4,1,2,2", "f32", 65539), ("3,8,1,2", "bf16", 7),
 ])
 def test_other_launch_shapes(plan, dtype, V, monkeypatch):
+    monkeypatch.setenv("CE_KERNEL", "unit")  # the unit kernel in every mode
     monkeypatch.setenv("CE_PLAN", plan)
     M = max(2, min(64, (2 << 20) // V))
     x = synthetic.make_logits(M, V, dtype, 2.0, seed=V)
@@ -307,6 +320,7 @@ def test_large_workloads_sampled(name):
 def test_single_stage_pipeline_many_units_per_cta(plan, monkeypatch):
     # one stage: every refill waits for the previous store to be read out;
     # enough rows that each CTA runs many units
+    monkeypatch.setenv("CE_KERNEL", "unit")
     monkeypatch.setenv("CE_PLAN", plan)
     M, V = 20000, 1000
     x = synthetic.make_logits(M, V, "f32", 2.0, seed=77)
