@@ -157,7 +157,7 @@ __global__ void __launch_bounds__(kStreamMaxWarps * 32, 1) ce_stream_kernel(cons
 
   extern __shared__ __align__(128) unsigned char ring_mem[];
   __shared__ __align__(8) unsigned long long full_bar[kStreamMaxWarps][kStreamMaxSlots];
-  __shared__ float2 red[2][kStreamMaxWarps];
+  __shared__ __align__(16) float4 red[2][kStreamMaxWarps];
   __shared__ double acc_slot[kStreamMaxWarps];
 
   const int lane = threadIdx.x & 31;
@@ -241,20 +241,34 @@ __global__ void __launch_bounds__(kStreamMaxWarps * 32, 1) ce_stream_kernel(cons
   };
 
   double acc = 0.0;  // the group's loss sum (warp kw == 0, lane 0)
-  long long t_next = -1;
-  float lse_next = 0.f;
-  if (TARGETS && n_rows > 0) t_next = __ldg(p.targets + gidx);
-  if (MODE == BWD && n_rows > 0) lse_next = __ldg(p.lse_in + gidx);
+  // Targets (and, for BWD, the stored lse) of the group's rows are fetched 32
+  // rows at a time, lane j holding row ri0 + j, one batch ahead, so their
+  // latency never sits on a row's path.
+  auto fetch = [&](long long ri0, long long& tv, float& lv) {
+    const long long ri = ri0 + lane;
+    tv = -1;
+    lv = 0.f;
+    if (ri < n_rows) {
+      if (TARGETS) tv = __ldg(p.targets + gidx + ri * ngroups);
+      if (MODE == BWD) lv = __ldg(p.lse_in + gidx + ri * ngroups);
+    }
+  };
+  long long t_cur, t_nxt;
+  float l_cur, l_nxt;
+  fetch(0, t_cur, l_cur);
+  fetch(32, t_nxt, l_nxt);
 
   for (long long ri = 0; ri < n_rows; ++ri) {
     const long long r = gidx + ri * ngroups;
     const StreamGeo g = stream_geo(p, r, kw, SC);
-    const long long t = t_next;
-    const float lse_given = lse_next;
-    if (ri + 1 < n_rows) {
-      if (TARGETS) t_next = __ldg(p.targets + r + ngroups);
-      if (MODE == BWD) lse_next = __ldg(p.lse_in + r + ngroups);
+    const int bl = static_cast<int>(ri & 31);
+    if (bl == 0 && ri > 0) {
+      t_cur = t_nxt;
+      l_cur = l_nxt;
+      fetch(ri + 32, t_nxt, l_nxt);
     }
+    const long long t = TARGETS ? __shfl_sync(0xffffffffu, t_cur, bl) : -1;
+    const float lse_given = (MODE == BWD) ? __shfl_sync(0xffffffffu, l_cur, bl) : 0.f;
     const bool t_ok = TARGETS && t >= 0 && t < V;
     // the target's chunk and its slot in the chunk
     const int tbo = t_ok ? static_cast<int>(t) * ES + 16 - g.hb : -1;
@@ -262,10 +276,11 @@ __global__ void __launch_bounds__(kStreamMaxWarps * 32, 1) ce_stream_kernel(cons
     const int tq = t_ok ? ((tbo & 15) >> LOG_ES) : 0;
     const int b = static_cast<int>(ri & 1);
     const bool row_leader = kw == 0 && lane == 0;
-    // the target logit, read before any gradient of this row is written
+    // the target logit: taken by lane 0 of the warp whose piece holds it,
+    // from the slot (or, for a partial chunk TMA did not load, from memory)
+    // while the statistics pass streams that segment
     float xt = 0.f;
-    if (MODE != BWD && MODE != SOFTMAX && row_leader && t_ok)
-      xt = E::ld(reinterpret_cast<const char*>(g.as) + t * ES);
+    bool have_xt = false;
 
     // element e of the row, -inf outside it; from the slot when TMA loaded it
     auto edge_vals = [&](int c, int c0, uint32_t sbase, float* v) {
@@ -318,6 +333,12 @@ __global__ void __launch_bounds__(kStreamMaxWarps * 32, 1) ce_stream_kernel(cons
             }
           }
         }
+        if (TARGETS && lane == 0 && t_ok && tc >= c0 && tc < c1) {
+          xt = (tc >= g.ld_lo && tc < g.ld_hi)
+                   ? E::ld(static_cast<char*>(__cvta_shared_to_generic(sbase + 16 * (tc - c0) + tq * ES)))
+                   : E::ld(reinterpret_cast<const char*>(g.as) + t * ES);
+          have_xt = true;
+        }
         // the partial head and tail chunks of the row, element by element
         if (c0 <= 0 && 0 < c1 && lane == 0) {
           float x[EPC];
@@ -353,14 +374,20 @@ __global__ void __launch_bounds__(kStreamMaxWarps * 32, 1) ce_stream_kernel(cons
         Mrow = mw;
         Srow = sw;
       } else {
-        if (lane == 0) red[b][warp] = make_float2(mw, sw);
+        if (lane == 0) red[b][warp] = make_float4(mw, sw, xt, have_xt ? 1.f : 0.f);
         group_sync(1 + grp, G * 32);
-        const float2 rr = (lane < G) ? red[b][grp * G + lane] : make_float2(-INFINITY, 0.f);
+        const float4 rr =
+            (lane < G) ? red[b][grp * G + lane] : make_float4(-INFINITY, 0.f, 0.f, 0.f);
         Mrow = warp_max(rr.x);
         float sg2 = (rr.x == -INFINITY) ? 0.f : rr.y * ex2((rr.x - Mrow) * kLog2e);
+        float xg = rr.w != 0.f ? rr.z : 0.f;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) sg2 += __shfl_xor_sync(0xffffffffu, sg2, o);
+        for (int o = 16; o > 0; o >>= 1) {
+          sg2 += __shfl_xor_sync(0xffffffffu, sg2, o);
+          xg += __shfl_xor_sync(0xffffffffu, xg, o);
+        }
         Srow = sg2;
+        xt = xg;
       }
       if (row_leader) {
         const float lnS = logf(Srow);
