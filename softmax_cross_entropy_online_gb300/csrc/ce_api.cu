@@ -2,6 +2,7 @@
 // of launch shape for each (dtype, V, M), the per-stream reduction scratch,
 // the device error word, and the launches.  Every computation happens in the
 // kernels of ce_rows.cuh; this file only validates, plans and launches.
+#include <array>
 #include <atomic>
 #include <cmath>
 #include <chrono>
@@ -51,6 +52,21 @@ __global__ void ce_selftest_wait_kernel(unsigned int* err, unsigned long long li
     mbar_wait<false>(smem_u32(&bar), 0u, err, failed, limit_ns);
     mbar_arrive(smem_u32(&bar));  // leave the barrier in a completed phase
   }
+}
+
+cudaError_t ensure_max_smem(const void* fn, int smem_bytes) {
+  static std::mutex mu;
+  static std::map<std::pair<int, const void*>, int> raised;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(mu);
+  const auto key = std::make_pair(dev, fn);
+  auto it = raised.find(key);
+  if (it != raised.end() && it->second >= smem_bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+  if (e == cudaSuccess) raised[key] = smem_bytes;
+  return e;
 }
 
 }  // namespace ce
@@ -129,6 +145,28 @@ int elem_size(ce_dtype d) {
 struct Plan {
   int variant = 0, R = 1, CL = 1, S = 0, stage_bytes = 0;
 };
+
+// Occupancy of a launch shape, looked up once per (device, kernel, shape):
+// the runtime's occupancy query costs more host time than a small launch.
+std::mutex g_occ_mu;
+std::map<std::array<long long, 7>, int> g_occ;
+template <typename F>
+cudaError_t cached_occupancy(const std::array<long long, 7>& key, F query, int* out) {
+  {
+    std::lock_guard<std::mutex> lk(g_occ_mu);
+    auto it = g_occ.find(key);
+    if (it != g_occ.end()) {
+      *out = it->second;
+      return cudaSuccess;
+    }
+  }
+  const cudaError_t e = query(out);
+  if (e == cudaSuccess) {
+    std::lock_guard<std::mutex> lk(g_occ_mu);
+    g_occ[key] = *out;
+  }
+  return e;
+}
 
 constexpr int kMaxSliceBytes = 200 * 1024;  // one stage of one CTA, at most
 
@@ -388,12 +426,16 @@ ce_status launch_stream(int mode, const void* logits, const int64_t* targets, co
 
   const int smem = sp.nw * sp.S * sp.seg;
   int per_sm = 0;
-  cudaError_t e = cudaSuccess;
-  switch (dtype) {
-    case CE_F32: e = ce::stream_max_active<float>(mode, sp.nw, smem, &per_sm); break;
-    case CE_F16: e = ce::stream_max_active<__half>(mode, sp.nw, smem, &per_sm); break;
-    default: e = ce::stream_max_active<__nv_bfloat16>(mode, sp.nw, smem, &per_sm); break;
-  }
+  cudaError_t e = cached_occupancy(
+      {dev, 1, static_cast<long long>(dtype), mode, sp.nw, smem, 1},
+      [&](int* out) {
+        switch (dtype) {
+          case CE_F32: return ce::stream_max_active<float>(mode, sp.nw, smem, out);
+          case CE_F16: return ce::stream_max_active<__half>(mode, sp.nw, smem, out);
+          default: return ce::stream_max_active<__nv_bfloat16>(mode, sp.nw, smem, out);
+        }
+      },
+      &per_sm);
   if (e != cudaSuccess || per_sm < 1) return CE_ERR_CUDA;
   const long long groups_per_cta = sp.nw / sp.G;
   long long grid = static_cast<long long>(per_sm) * di.sm_count;
@@ -512,12 +554,16 @@ ce_status launch_rows(int mode, const void* logits, const int64_t* targets, cons
 
   const int smem = pl.S * pl.stage_bytes;
   int max_active = 0;
-  cudaError_t ce_err = cudaSuccess;
-  switch (dtype) {
-    case CE_F32: ce_err = ce::rows_max_active<float>(mode, pl.variant, smem, pl.CL, di.sm_count, &max_active); break;
-    case CE_F16: ce_err = ce::rows_max_active<__half>(mode, pl.variant, smem, pl.CL, di.sm_count, &max_active); break;
-    default: ce_err = ce::rows_max_active<__nv_bfloat16>(mode, pl.variant, smem, pl.CL, di.sm_count, &max_active); break;
-  }
+  cudaError_t ce_err = cached_occupancy(
+      {dev, 0, static_cast<long long>(dtype), mode, pl.variant, smem, pl.CL},
+      [&](int* out) {
+        switch (dtype) {
+          case CE_F32: return ce::rows_max_active<float>(mode, pl.variant, smem, pl.CL, di.sm_count, out);
+          case CE_F16: return ce::rows_max_active<__half>(mode, pl.variant, smem, pl.CL, di.sm_count, out);
+          default: return ce::rows_max_active<__nv_bfloat16>(mode, pl.variant, smem, pl.CL, di.sm_count, out);
+        }
+      },
+      &max_active);
   if (ce_err != cudaSuccess || max_active < 1) return CE_ERR_CUDA;
   long long nclusters = p.n_units < max_active ? p.n_units : max_active;
   if (nclusters < 1) nclusters = 1;  // M == 0: one cluster writes the empty reduction

@@ -8,6 +8,11 @@
 
 namespace ce {
 
+// Raises a kernel's dynamic shared-memory limit to at least smem_bytes on the
+// current device; remembered per (device, kernel), so repeated launches make
+// no runtime call (defined in ce_api.cu).
+cudaError_t ensure_max_smem(const void* fn, int smem_bytes);
+
 // Instantiated shapes: NC consumer threads x CPT register-resident 16-byte
 // chunks per thread.  Both hold 2048 chunks (32 KB) of a row slice per CTA.
 //   NC = 256, CPT = 8: 9 warps, fewer threads with more elements each
@@ -48,7 +53,7 @@ cudaError_t rows_launch(int mode, int variant, const RowParams& p, int grid, int
   const void* fn = rows_kernel_ptr<T>(mode, variant);
   const int NC = kVariants[variant].NC;
   if (fn == nullptr) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+  cudaError_t e = ensure_max_smem(fn, smem_bytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
@@ -75,7 +80,7 @@ cudaError_t rows_max_active(int mode, int variant, int smem_bytes, int CL, int s
   const void* fn = rows_kernel_ptr<T>(mode, variant);
   const int NC = kVariants[variant].NC;
   if (fn == nullptr) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+  cudaError_t e = ensure_max_smem(fn, smem_bytes);
   if (e != cudaSuccess) return e;
   if (CL <= 1) {
     int occ = 0;
@@ -118,7 +123,7 @@ cudaError_t stream_launch(int mode, const StreamParams& p, int grid, int nwarps,
                           cudaStream_t stream) {
   const void* fn = stream_kernel_ptr<T>(mode);
   if (fn == nullptr || nwarps < 1 || nwarps > kStreamMaxWarps) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+  cudaError_t e = ensure_max_smem(fn, smem_bytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
@@ -134,7 +139,7 @@ template <typename T>
 cudaError_t stream_max_active(int mode, int nwarps, int smem_bytes, int* per_sm) {
   const void* fn = stream_kernel_ptr<T>(mode);
   if (fn == nullptr) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+  cudaError_t e = ensure_max_smem(fn, smem_bytes);
   if (e != cudaSuccess) return e;
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, fn, nwarps * 32,
                                                        static_cast<size_t>(smem_bytes));

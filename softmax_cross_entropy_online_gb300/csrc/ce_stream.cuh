@@ -37,6 +37,14 @@ constexpr int kStreamMaxWarps = 16;
 constexpr int kStreamMaxSlots = 8;
 constexpr int kStreamKPL = 8;  // 16-byte chunks a lane holds in registers per sub-block
 
+// compile-time flags for the full / last-block variants of the inner loops
+struct kTrue {
+  static constexpr bool value = true;
+};
+struct kFalse {
+  static constexpr bool value = false;
+};
+
 struct StreamParams {
   char* base;                 // logits (byte address)
   const int64_t* targets;     // [M] (null for SOFTMAX)
@@ -105,6 +113,14 @@ __device__ __forceinline__ StreamGeo stream_geo(const StreamParams& p, long long
   return g;
 }
 
+// Position of a warp's load cursor: row (index into the group's rows), pass,
+// segment, next slot, and that row's frame.
+struct IssueCursor {
+  long long ri;
+  int pass, seg, slot;
+  StreamGeo g;
+};
+
 __device__ __forceinline__ unsigned long long l2_policy_evict_last() {
   unsigned long long pol;
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
@@ -154,11 +170,15 @@ __global__ void __launch_bounds__(kStreamMaxWarps * 32, 1) ce_stream_kernel(cons
   constexpr bool GRAD = MODE != FWD;                   // a gradient / probability pass
   constexpr bool TARGETS = MODE != SOFTMAX;
   constexpr int NPASS = (STATS && GRAD) ? 2 : 1;
+  // chunks per lane in a statistics sub-block: fewer in the two-pass modes,
+  // whose gradient pass needs registers of its own
+  constexpr int KPL = NPASS == 2 ? kStreamKPL / 2 : kStreamKPL;
 
   extern __shared__ __align__(128) unsigned char ring_mem[];
   __shared__ __align__(8) unsigned long long full_bar[kStreamMaxWarps][kStreamMaxSlots];
   __shared__ __align__(16) float4 red[2][kStreamMaxWarps];
   __shared__ double acc_slot[kStreamMaxWarps];
+  __shared__ IssueCursor cursor[kStreamMaxWarps];
 
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
@@ -187,38 +207,46 @@ __global__ void __launch_bounds__(kStreamMaxWarps * 32, 1) ce_stream_kernel(cons
   const unsigned long long pol_drop = l2_policy_evict_first();
 
   // ---- the load cursor (lane 0): the k-th load fills slot k % S ----
-  long long i_ri = 0;
-  int i_pass = 0, i_seg = 0, i_slot = 0;
-  StreamGeo ig;
-  if (lane == 0 && n_rows > 0) ig = stream_geo(p, gidx, kw, SC);
+  // It lives in shared memory: only lane 0 uses it, and in registers it would
+  // take a dozen from every lane of the warp.
+  IssueCursor& cur = cursor[warp];
+  if (lane == 0) {
+    cur.ri = 0;
+    cur.pass = 0;
+    cur.seg = 0;
+    cur.slot = 0;
+    if (n_rows > 0) cur.g = stream_geo(p, gidx, kw, SC);
+  }
   auto issue_next = [&]() {
-    while (i_ri < n_rows && i_seg >= ig.ns) {
-      i_seg = 0;
-      if (++i_pass == NPASS) {
-        i_pass = 0;
-        if (++i_ri < n_rows) ig = stream_geo(p, gidx + i_ri * ngroups, kw, SC);
+    while (cur.ri < n_rows && cur.seg >= cur.g.ns) {
+      cur.seg = 0;
+      if (++cur.pass == NPASS) {
+        cur.pass = 0;
+        if (++cur.ri < n_rows) cur.g = stream_geo(p, gidx + cur.ri * ngroups, kw, SC);
       }
     }
-    if (i_ri >= n_rows) return;
-    const int c0 = ig.p0 + i_seg * SC;
+    if (cur.ri >= n_rows) return;
+    const StreamGeo& ig = cur.g;
+    const int c0 = ig.p0 + cur.seg * SC;
     int c1 = c0 + SC;
     if (c1 > ig.p1) c1 = ig.p1;
     const int lo = c0 > ig.ld_lo ? c0 : ig.ld_lo;
     const int hi = c1 < ig.ld_hi ? c1 : ig.ld_hi;
-    const uint32_t fb = smem_u32(&full_bar[warp][i_slot]);
+    const int slot = cur.slot;
+    const uint32_t fb = smem_u32(&full_bar[warp][slot]);
     fence_proxy_async_smem();  // the warp's reads of this slot precede the refill
     if (hi > lo) {
       mbar_arrive_expect_tx(fb, static_cast<uint32_t>((hi - lo) * 16));
       // kept in L2 only when a second pass will read it again
-      const bool keep = NPASS == 2 && i_pass == 0;
-      bulk_load_hint(ring + i_slot * SB + (lo - c0) * 16,
+      const bool keep = NPASS == 2 && cur.pass == 0;
+      bulk_load_hint(ring + slot * SB + (lo - c0) * 16,
                      reinterpret_cast<const void*>(ig.as + ig.hb - 16 + 16LL * lo),
                      static_cast<uint32_t>((hi - lo) * 16), fb, keep ? pol_keep : pol_drop);
     } else {
       mbar_arrive(fb);
     }
-    ++i_seg;
-    if (++i_slot == S) i_slot = 0;
+    ++cur.seg;
+    cur.slot = (slot + 1 == S) ? 0 : slot + 1;
   };
   if (lane == 0)
     for (int k = 0; k < S; ++k) issue_next();
@@ -307,22 +335,23 @@ __global__ void __launch_bounds__(kStreamMaxWarps * 32, 1) ce_stream_kernel(cons
         const uint32_t sbase = wait_segment();
         const int fa = c0 > 1 ? c0 : 1;                      // full chunks [fa, fb)
         const int fb = c1 < g.nI + 1 ? c1 : g.nI + 1;
-        for (int cb = fa; cb < fb; cb += 32 * kStreamKPL) {
-          uint4 q[kStreamKPL];
+        // sub-blocks of 32 x KPL chunks; the checks against fb only in the last
+        auto stats_block = [&](int cb, auto full_tag) {
+          constexpr bool FULL = decltype(full_tag)::value;
+          const uint32_t a0 = sbase + 16 * (cb + lane - c0);
+          uint4 q[KPL];
           float lm = -INFINITY;
 #pragma unroll
-          for (int j = 0; j < kStreamKPL; ++j) {
-            const int c = cb + lane + 32 * j;
-            if (c < fb) {
-              q[j] = lds128(sbase + 16 * (c - c0));
+          for (int j = 0; j < KPL; ++j) {
+            if (FULL || cb + lane + 32 * j < fb) {
+              q[j] = lds128(a0 + 512 * j);
               lm = fmaxf(lm, E::chunk_max(q[j]));
             }
           }
           online_rescale(lm, m, mh, s, s1);
 #pragma unroll
-          for (int j = 0; j < kStreamKPL; ++j) {
-            const int c = cb + lane + 32 * j;
-            if (c < fb) {
+          for (int j = 0; j < KPL; ++j) {
+            if (FULL || cb + lane + 32 * j < fb) {
               float x[EPC];
               E::unpack(q[j], x);
 #pragma unroll
@@ -332,7 +361,10 @@ __global__ void __launch_bounds__(kStreamMaxWarps * 32, 1) ce_stream_kernel(cons
               }
             }
           }
-        }
+        };
+        int cb = fa;
+        for (; cb + 32 * KPL <= fb; cb += 32 * KPL) stats_block(cb, kTrue{});
+        if (cb < fb) stats_block(cb, kFalse{});
         if (TARGETS && lane == 0 && t_ok && tc >= c0 && tc < c1) {
           xt = (tc >= g.ld_lo && tc < g.ld_hi)
                    ? E::ld(static_cast<char*>(__cvta_shared_to_generic(sbase + 16 * (tc - c0) + tq * ES)))
@@ -434,28 +466,36 @@ __global__ void __launch_bounds__(kStreamMaxWarps * 32, 1) ce_stream_kernel(cons
         const uint32_t sbase = wait_segment();
         const int fa = c0 > 1 ? c0 : 1;
         const int fb = c1 < g.nI + 1 ? c1 : g.nI + 1;
-        for (int cb = fa + lane; cb < fb; cb += 128) {
+        // blocks of 128 chunks, four per lane; the checks against fb only in the last
+        auto grad_block = [&](int cb, auto full_tag) {
+          constexpr bool FULL = decltype(full_tag)::value;
+          const int cl = cb + lane;
+          const uint32_t a0 = sbase + 16 * (cl - c0);
+          char* const o0 = out_row + (g.hb - 16 + 16LL * cl);
+          const bool t_here = tc >= cb && tc < cb + 128;  // the target's chunk is in this block
           uint4 q[4];
 #pragma unroll
           for (int j = 0; j < 4; ++j)
-            if (cb + 32 * j < fb) q[j] = lds128(sbase + 16 * (cb + 32 * j - c0));
+            if (FULL || cl + 32 * j < fb) q[j] = lds128(a0 + 512 * j);
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            const int c = cb + 32 * j;
-            if (c < fb) {
+            if (FULL || cl + 32 * j < fb) {
               float x[EPC], gv[EPC];
               E::unpack(q[j], x);
 #pragma unroll
               for (int e = 0; e < EPC; ++e) gv[e] = ex2(fmaf(x[e], kLog2e, -Lh)) * scf;
-              if (c == tc) {
+              if (t_here && cl + 32 * j == tc) {
 #pragma unroll
                 for (int e = 0; e < EPC; ++e)
                   if (e == tq) gv[e] = target_grad(x[e]);
               }
-              stg128_hint(out_row + (g.hb - 16 + 16LL * c), E::pack(gv), pol_drop);
+              stg128_hint(o0 + 512 * j, E::pack(gv), pol_drop);
             }
           }
-        }
+        };
+        int cb = fa;
+        for (; cb + 128 <= fb; cb += 128) grad_block(cb, kTrue{});
+        if (cb < fb) grad_block(cb, kFalse{});
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int c = h ? g.nI + 1 : 0;
