@@ -303,16 +303,19 @@ bool choose_stream_plan(int mode, long long rb, long long M, int sm_count, Strea
     }
     while (G > 1 && rb / G < 8192) G /= 2;
   }
-  // rows shorter than a segment: one row per slot, up to eight slots a warp
+  // rows shorter than a segment: one row per slot (the power of two that
+  // holds every chunk a row can straddle), up to eight slots a warp
   int sg = seg;
-  const long long row_span = (rb / 16 + 2) * 16;  // chunks a row can straddle
-  if (G == 1 && row_span < seg) sg = static_cast<int>(row_span);
+  const long long row_span = (rb / 16 + 2) * 16;
+  if (G == 1) {
+    while (sg / 2 >= row_span && sg > 16) sg /= 2;
+  }
   sp = StreamPlan{nw, G, stream_slots(nw, sg), sg};
   return true;
 }
 
 // Tuning overrides: CE_KERNEL=stream|unit forces a kernel; CE_SPLAN="nw,G,S,seg"
-// (seg a multiple of 16 bytes)
+// (seg a power of two, at least 16 bytes)
 // sets the streaming shape (ignored unless it fits the kernel's limits).
 int env_kernel_choice() {
   const char* env = std::getenv("CE_KERNEL");
@@ -327,7 +330,7 @@ void apply_env_stream_plan(StreamPlan& sp) {
   int nw = 0, G = 0, S = 0, seg = 0;
   if (std::sscanf(env, "%d,%d,%d,%d", &nw, &G, &S, &seg) != 4) return;
   if (nw < 1 || nw > ce::kStreamMaxWarps || G < 1 || (G & (G - 1)) != 0 || nw % G != 0) return;
-  if (S < 1 || S > ce::kStreamMaxSlots || seg < 16 || seg % 16 != 0) return;
+  if (S < 1 || S > ce::kStreamMaxSlots || seg < 16 || (seg & (seg - 1)) != 0) return;
   if (static_cast<long long>(nw) * S * seg > 220 * 1024) return;
   sp = StreamPlan{nw, G, S, seg};
 }
@@ -417,6 +420,12 @@ ce_status launch_stream(int mode, const void* logits, const int64_t* targets, co
   p.log_g = lg;
   p.S = sp.S;
   p.seg_bytes = sp.seg;
+  {
+    int sh = 0;
+    while ((16 << sh) < sp.seg) ++sh;
+    p.seg_shift = sh;
+  }
+  p.total_bytes = static_cast<long long>(M) * rb;
   p.wait_hint_ns = wait_hint_ns();
   p.out_delta = (out_buf == nullptr) ? 0
                                      : static_cast<long long>(reinterpret_cast<uintptr_t>(out_buf) -

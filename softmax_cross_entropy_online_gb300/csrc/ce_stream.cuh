@@ -60,7 +60,9 @@ struct StreamParams {
   int G;                      // warps per row (a power of two dividing the warps per CTA)
   int log_g;                  // log2(G)
   int S;                      // ring slots per warp
-  int seg_bytes;              // bytes per slot (a multiple of 16)
+  int seg_bytes;              // bytes per slot (a power of two, at least 16)
+  int seg_shift;              // log2(seg_bytes / 16): chunks per slot as a shift
+  long long total_bytes;      // M * row_bytes
   unsigned int wait_hint_ns;  // suspend-time hint of the mbarrier waits
   long long out_delta;        // writes go to (address + out_delta); 0 = in place
   float grad_scale;           // FWD_BWD / BWD
@@ -77,8 +79,7 @@ struct StreamGeo {
   int ns;           // segments of the piece
 };
 
-__device__ __forceinline__ StreamGeo stream_geo(const StreamParams& p, long long r, int kw,
-                                                int seg_chunks) {
+__device__ __forceinline__ StreamGeo stream_geo(const StreamParams& p, long long r, int kw) {
   StreamGeo g;
   const long long off = r * p.row_bytes;
   g.as = reinterpret_cast<long long>(p.base) + off;
@@ -101,11 +102,11 @@ __device__ __forceinline__ StreamGeo stream_geo(const StreamParams& p, long long
   if (b > c_last + 1) b = c_last + 1;
   g.p0 = a;
   g.p1 = b;
-  g.ns = (b - a + seg_chunks - 1) / seg_chunks;
+  g.ns = (b - a + (1 << p.seg_shift) - 1) >> p.seg_shift;
   // A partial chunk also holds bytes of the neighbouring row.  Reading them
   // (and ignoring them) is harmless while the 16 bytes lie inside the tensor;
   // writes to a partial chunk are always element by element.
-  const long long total = p.M * p.row_bytes;
+  const long long total = p.total_bytes;
   const bool head_ok = c_first == 0 && off + g.hb - 16 >= 0 && off + g.hb <= total;
   const bool tail_ok = c_last == g.nI + 1 && off + g.hb + 16LL * (g.nI + 1) <= total;
   g.ld_lo = head_ok ? 0 : 1;
@@ -145,20 +146,19 @@ __device__ __forceinline__ void stg128_hint(void* dst, uint4 v, unsigned long lo
                : "memory");
 }
 
-// Online update of a lane's pair with a block of values whose max is lm.
-// s and s1 (two partial sums, for a shorter dependency chain) hold
-// sum 2^(x log2e - mh) with mh = RN(m log2e); while m = -inf, mh = 0, so
-// -inf logits give exp2(-inf) = 0 rather than NaN.
-__device__ __forceinline__ void online_rescale(float lm, float& m, float& mh, float& s, float& s1) {
+// Online update of a lane's pair with a block of values whose max is lm:
+// s holds sum 2^(x log2e - mh) with mh = RN(m log2e); while m = -inf, mh = 0,
+// so -inf logits give exp2(-inf) = 0 rather than NaN.
+__device__ __forceinline__ void online_rescale(float lm, float& m, float& mh, float& s) {
   if (lm > m) {
     const float mhn = lm * kLog2e;
-    const float f = (m == -INFINITY) ? 0.f : ex2(mh - mhn);
-    s *= f;
-    s1 *= f;
+    s = (m == -INFINITY) ? 0.f : s * ex2(mh - mhn);
     m = lm;
     mh = mhn;
   }
 }
+
+constexpr float kLn2 = 0.6931471805599453f;
 
 template <typename T, int MODE>
 __global__ void __launch_bounds__(kStreamMaxWarps * 32, 1) ce_stream_kernel(const StreamParams p) {
@@ -215,38 +215,50 @@ __global__ void __launch_bounds__(kStreamMaxWarps * 32, 1) ce_stream_kernel(cons
     cur.pass = 0;
     cur.seg = 0;
     cur.slot = 0;
-    if (n_rows > 0) cur.g = stream_geo(p, gidx, kw, SC);
+    if (n_rows > 0) cur.g = stream_geo(p, gidx, kw);
   }
   auto issue_next = [&]() {
-    while (cur.ri < n_rows && cur.seg >= cur.g.ns) {
-      cur.seg = 0;
-      if (++cur.pass == NPASS) {
-        cur.pass = 0;
-        if (++cur.ri < n_rows) cur.g = stream_geo(p, gidx + cur.ri * ngroups, kw, SC);
+    // the cursor is read into registers once and written back once
+    long long ri = cur.ri;
+    int pass = cur.pass, seg = cur.seg;
+    const int slot = cur.slot;
+    StreamGeo ig = cur.g;
+    bool moved = false;
+    while (ri < n_rows && seg >= ig.ns) {
+      seg = 0;
+      if (++pass == NPASS) {
+        pass = 0;
+        if (++ri < n_rows) {
+          ig = stream_geo(p, gidx + ri * ngroups, kw);
+          moved = true;
+        }
       }
     }
-    if (cur.ri >= n_rows) return;
-    const StreamGeo& ig = cur.g;
-    const int c0 = ig.p0 + cur.seg * SC;
-    int c1 = c0 + SC;
-    if (c1 > ig.p1) c1 = ig.p1;
-    const int lo = c0 > ig.ld_lo ? c0 : ig.ld_lo;
-    const int hi = c1 < ig.ld_hi ? c1 : ig.ld_hi;
-    const int slot = cur.slot;
-    const uint32_t fb = smem_u32(&full_bar[warp][slot]);
-    fence_proxy_async_smem();  // the warp's reads of this slot precede the refill
-    if (hi > lo) {
-      mbar_arrive_expect_tx(fb, static_cast<uint32_t>((hi - lo) * 16));
-      // kept in L2 only when a second pass will read it again
-      const bool keep = NPASS == 2 && cur.pass == 0;
-      bulk_load_hint(ring + slot * SB + (lo - c0) * 16,
-                     reinterpret_cast<const void*>(ig.as + ig.hb - 16 + 16LL * lo),
-                     static_cast<uint32_t>((hi - lo) * 16), fb, keep ? pol_keep : pol_drop);
-    } else {
-      mbar_arrive(fb);
+    if (ri < n_rows) {
+      const int c0 = ig.p0 + (seg << p.seg_shift);
+      int c1 = c0 + SC;
+      if (c1 > ig.p1) c1 = ig.p1;
+      const int lo = c0 > ig.ld_lo ? c0 : ig.ld_lo;
+      const int hi = c1 < ig.ld_hi ? c1 : ig.ld_hi;
+      const uint32_t fb = smem_u32(&full_bar[warp][slot]);
+      fence_proxy_async_smem();  // the warp's reads of this slot precede the refill
+      if (hi > lo) {
+        mbar_arrive_expect_tx(fb, static_cast<uint32_t>((hi - lo) * 16));
+        // kept in L2 only when a second pass will read it again
+        const bool keep = NPASS == 2 && pass == 0;
+        bulk_load_hint(ring + slot * SB + (lo - c0) * 16,
+                       reinterpret_cast<const void*>(ig.as + ig.hb - 16 + 16LL * lo),
+                       static_cast<uint32_t>((hi - lo) * 16), fb, keep ? pol_keep : pol_drop);
+      } else {
+        mbar_arrive(fb);
+      }
+      ++seg;
+      cur.slot = (slot + 1 == S) ? 0 : slot + 1;
     }
-    ++cur.seg;
-    cur.slot = (slot + 1 == S) ? 0 : slot + 1;
+    cur.ri = ri;
+    cur.pass = pass;
+    cur.seg = seg;
+    if (moved) cur.g = ig;
   };
   if (lane == 0)
     for (int k = 0; k < S; ++k) issue_next();
@@ -288,7 +300,7 @@ __global__ void __launch_bounds__(kStreamMaxWarps * 32, 1) ce_stream_kernel(cons
 
   for (long long ri = 0; ri < n_rows; ++ri) {
     const long long r = gidx + ri * ngroups;
-    const StreamGeo g = stream_geo(p, r, kw, SC);
+    const StreamGeo g = stream_geo(p, r, kw);
     const int bl = static_cast<int>(ri & 31);
     if (bl == 0 && ri > 0) {
       t_cur = t_nxt;
@@ -328,9 +340,9 @@ __global__ void __launch_bounds__(kStreamMaxWarps * 32, 1) ce_stream_kernel(cons
 
     float Mrow = 0.f, Srow = 1.f;  // row max and sum of exp(x - max)
     if (STATS) {
-      float m = -INFINITY, mh = 0.f, s = 0.f, s1 = 0.f;
+      float m = -INFINITY, mh = 0.f, s = 0.f;
       for (int sg = 0; sg < g.ns; ++sg) {
-        const int c0 = g.p0 + sg * SC;
+        const int c0 = g.p0 + (sg << p.seg_shift);
         const int c1 = (c0 + SC < g.p1) ? c0 + SC : g.p1;
         const uint32_t sbase = wait_segment();
         const int fa = c0 > 1 ? c0 : 1;                      // full chunks [fa, fb)
@@ -340,27 +352,32 @@ __global__ void __launch_bounds__(kStreamMaxWarps * 32, 1) ce_stream_kernel(cons
           constexpr bool FULL = decltype(full_tag)::value;
           const uint32_t a0 = sbase + 16 * (cb + lane - c0);
           uint4 q[KPL];
-          float lm = -INFINITY;
+          float cm[KPL];
 #pragma unroll
           for (int j = 0; j < KPL; ++j) {
+            cm[j] = -INFINITY;
             if (FULL || cb + lane + 32 * j < fb) {
               q[j] = lds128(a0 + 512 * j);
-              lm = fmaxf(lm, E::chunk_max(q[j]));
+              cm[j] = E::chunk_max(q[j]);
             }
           }
-          online_rescale(lm, m, mh, s, s1);
+          // tree max, then four partial sums: short dependency chains
+#pragma unroll
+          for (int w = KPL / 2; w >= 1; w /= 2)
+#pragma unroll
+            for (int j = 0; j < w; ++j) cm[j] = fmaxf(cm[j], cm[j + w]);
+          online_rescale(cm[0], m, mh, s);
+          float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
           for (int j = 0; j < KPL; ++j) {
             if (FULL || cb + lane + 32 * j < fb) {
               float x[EPC];
               E::unpack(q[j], x);
 #pragma unroll
-              for (int e = 0; e < EPC; e += 2) {
-                s += ex2(fmaf(x[e], kLog2e, -mh));
-                s1 += ex2(fmaf(x[e + 1], kLog2e, -mh));
-              }
+              for (int e = 0; e < EPC; ++e) ps[e & 3] += ex2(fmaf(x[e], kLog2e, -mh));
             }
           }
+          s += (ps[0] + ps[1]) + (ps[2] + ps[3]);
         };
         int cb = fa;
         for (; cb + 32 * KPL <= fb; cb += 32 * KPL) stats_block(cb, kTrue{});
@@ -378,7 +395,7 @@ __global__ void __launch_bounds__(kStreamMaxWarps * 32, 1) ce_stream_kernel(cons
           float lm = -INFINITY;
 #pragma unroll
           for (int e = 0; e < EPC; ++e) lm = fmaxf(lm, x[e]);
-          online_rescale(lm, m, mh, s, s1);
+          online_rescale(lm, m, mh, s);
 #pragma unroll
           for (int e = 0; e < EPC; ++e) s += ex2(fmaf(x[e], kLog2e, -mh));
         }
@@ -388,13 +405,12 @@ __global__ void __launch_bounds__(kStreamMaxWarps * 32, 1) ce_stream_kernel(cons
           float lm = -INFINITY;
 #pragma unroll
           for (int e = 0; e < EPC; ++e) lm = fmaxf(lm, x[e]);
-          online_rescale(lm, m, mh, s, s1);
+          online_rescale(lm, m, mh, s);
 #pragma unroll
           for (int e = 0; e < EPC; ++e) s += ex2(fmaf(x[e], kLog2e, -mh));
         }
         release_segment();
       }
-      s += s1;
       // ---- merge: lanes, then the group's warps ----
       const float mref = (m == -INFINITY) ? 0.f : m;
       const float ml = fmaf(mref, kLog2e, -mh);
@@ -422,7 +438,7 @@ __global__ void __launch_bounds__(kStreamMaxWarps * 32, 1) ce_stream_kernel(cons
         xt = xg;
       }
       if (row_leader) {
-        const float lnS = logf(Srow);
+        const float lnS = lg2(Srow) * kLn2;
         const float rl = t_ok ? (Mrow - xt) + lnS : __int_as_float(0x7fc00000);
         if (p.row_loss) p.row_loss[r] = rl;
         if (p.lse_out) p.lse_out[r] = Mrow + lnS;
@@ -452,7 +468,7 @@ __global__ void __launch_bounds__(kStreamMaxWarps * 32, 1) ce_stream_kernel(cons
         const float bv = Lh - mhr;
         const float rem = (mhr - (Lh - bv)) + (l2s - bv);
         Lc = mlr + rem;
-        lnS = logf(Srow);
+        lnS = l2s * kLn2;
       }
       const float scf = ex2(-Lc) * sc;
       // g_t = expm1(x_t - lse) * scale, evaluated from the target's own value
@@ -461,7 +477,7 @@ __global__ void __launch_bounds__(kStreamMaxWarps * 32, 1) ce_stream_kernel(cons
       };
       char* const out_row = reinterpret_cast<char*>(g.as) + p.out_delta;
       for (int sg = 0; sg < g.ns; ++sg) {
-        const int c0 = g.p0 + sg * SC;
+        const int c0 = g.p0 + (sg << p.seg_shift);
         const int c1 = (c0 + SC < g.p1) ? c0 + SC : g.p1;
         const uint32_t sbase = wait_segment();
         const int fa = c0 > 1 ? c0 : 1;

@@ -79,7 +79,8 @@ def test_stream_base_off_the_16_byte_grid(dtype, offset, V):
     ("16,1,3,4096", "f32", 4096), ("8,2,4,2048", "bf16", 1999), ("12,4,3,4096", "f16", 50257),
     ("16,16,3,4096", "f16", 131072), ("4,4,2,512", "f32", 3001), ("16,1,1,512", "bf16", 4099),
     ("9,1,5,1024", "f32", 100), ("16,8,2,8192", "bf16", 50257), ("2,2,8,512", "f16", 17),
-    ("16,16,1,512", "f32", 30000), ("8,8,3,1024", "bf16", 7),
+    ("16,16,1,512", "f32", 30000), ("8,8,3,1024", "bf16", 7), ("16,1,8,64", "f32", 9),
+    ("16,1,8,16", "bf16", 3), ("4,1,8,32", "f16", 30),
 ])
 def test_stream_launch_shapes(splan, dtype, V, monkeypatch):
     monkeypatch.setenv("CE_SPLAN", splan)
