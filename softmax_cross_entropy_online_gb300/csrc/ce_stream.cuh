@@ -206,11 +206,15 @@ __global__ void __launch_bounds__(kStreamMaxWarps * 32, 1) ce_stream_kernel(cons
   const unsigned long long pol_keep = l2_policy_evict_last();
   const unsigned long long pol_drop = l2_policy_evict_first();
 
-  // ---- the load cursor (lane 0): the k-th load fills slot k % S ----
-  // It lives in shared memory: only lane 0 uses it, and in registers it would
-  // take a dozen from every lane of the warp.
-  IssueCursor& cur = cursor[warp];
-  if (lane == 0) {
+  // ---- the load cursor: the k-th load fills slot k % S ----
+  // One-pass modes keep it in registers and every lane advances it in step
+  // (no divergent bookkeeping on the warp's path; only lane 0 issues the
+  // copy).  Two-pass modes need those registers elsewhere: lane 0 alone keeps
+  // it in shared memory.
+  constexpr bool REG_CURSOR = NPASS == 1;
+  IssueCursor reg_cur;
+  IssueCursor& cur = REG_CURSOR ? reg_cur : cursor[warp];
+  if (REG_CURSOR || lane == 0) {
     cur.ri = 0;
     cur.pass = 0;
     cur.seg = 0;
@@ -240,17 +244,19 @@ __global__ void __launch_bounds__(kStreamMaxWarps * 32, 1) ce_stream_kernel(cons
       if (c1 > ig.p1) c1 = ig.p1;
       const int lo = c0 > ig.ld_lo ? c0 : ig.ld_lo;
       const int hi = c1 < ig.ld_hi ? c1 : ig.ld_hi;
-      const uint32_t fb = smem_u32(&full_bar[warp][slot]);
-      fence_proxy_async_smem();  // the warp's reads of this slot precede the refill
-      if (hi > lo) {
-        mbar_arrive_expect_tx(fb, static_cast<uint32_t>((hi - lo) * 16));
-        // kept in L2 only when a second pass will read it again
-        const bool keep = NPASS == 2 && pass == 0;
-        bulk_load_hint(ring + slot * SB + (lo - c0) * 16,
-                       reinterpret_cast<const void*>(ig.as + ig.hb - 16 + 16LL * lo),
-                       static_cast<uint32_t>((hi - lo) * 16), fb, keep ? pol_keep : pol_drop);
-      } else {
-        mbar_arrive(fb);
+      if (lane == 0) {
+        const uint32_t fb = smem_u32(&full_bar[warp][slot]);
+        fence_proxy_async_smem();  // the warp's reads of this slot precede the refill
+        if (hi > lo) {
+          mbar_arrive_expect_tx(fb, static_cast<uint32_t>((hi - lo) * 16));
+          // kept in L2 only when a second pass will read it again
+          const bool keep = NPASS == 2 && pass == 0;
+          bulk_load_hint(ring + slot * SB + (lo - c0) * 16,
+                         reinterpret_cast<const void*>(ig.as + ig.hb - 16 + 16LL * lo),
+                         static_cast<uint32_t>((hi - lo) * 16), fb, keep ? pol_keep : pol_drop);
+        } else {
+          mbar_arrive(fb);
+        }
       }
       ++seg;
       cur.slot = (slot + 1 == S) ? 0 : slot + 1;
@@ -260,7 +266,7 @@ __global__ void __launch_bounds__(kStreamMaxWarps * 32, 1) ce_stream_kernel(cons
     cur.seg = seg;
     if (moved) cur.g = ig;
   };
-  if (lane == 0)
+  if (REG_CURSOR || lane == 0)
     for (int k = 0; k < S; ++k) issue_next();
 
   // the consumer side: the k-th segment sits in slot k % S, phase (k / S) & 1
@@ -273,7 +279,7 @@ __global__ void __launch_bounds__(kStreamMaxWarps * 32, 1) ce_stream_kernel(cons
   };
   auto release_segment = [&]() {
     __syncwarp();
-    if (lane == 0) issue_next();
+    if (REG_CURSOR || lane == 0) issue_next();
     if (++c_slot == S) {
       c_slot = 0;
       c_phase ^= 1u;
