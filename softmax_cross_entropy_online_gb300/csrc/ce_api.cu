@@ -26,10 +26,11 @@ template <typename T>
 cudaError_t rows_max_active(int mode, int variant, int smem_bytes, int CL, int sm_count,
                             int* out);
 template <typename T>
-cudaError_t stream_launch(int mode, const StreamParams& p, int grid, int nwarps, int smem_bytes,
-                          cudaStream_t stream);
+cudaError_t stream_launch(int mode, bool resident, const StreamParams& p, int grid, int nwarps,
+                          int smem_bytes, cudaStream_t stream);
 template <typename T>
-cudaError_t stream_max_active(int mode, int nwarps, int smem_bytes, int* per_sm);
+cudaError_t stream_max_active(int mode, bool resident, int nwarps, int smem_bytes, int* per_sm);
+constexpr int kStreamKRes = 16;  // as in ce_launch.cuh
 ce_status gemm_bf16_tn(const void* A, long long lda, const void* B, long long ldb, float* D,
                        long long ldd, int M, int N, int K, float beta, cudaStream_t stream,
                        unsigned int* err, int sm_count, unsigned int wait_hint_ns);
@@ -270,19 +271,19 @@ void apply_env_plan(long long rb, bool aligned, Plan& pl) {
 // ---------------------------------------------------------------------------
 struct StreamPlan {
   int nw = 16, G = 1, S = 3, seg = 4096;
+  bool res = false;  // resident rows (writing modes): one read of each row
 };
 
-constexpr long long kStreamSmemBudget = 200 * 1024;
-
-int stream_slots(int nw, int seg) {
-  long long S = kStreamSmemBudget / (static_cast<long long>(nw) * seg);
-  if (S > ce::kStreamMaxSlots) S = ce::kStreamMaxSlots;
-  return static_cast<int>(S);
+// A resident plan holds every piece of a row in registers: 4 KB slots and at
+// most 32 x kStreamKRes chunks a warp (the row's chunk count: exact for rows
+// on the 16-byte grid, else an upper bound).
+bool resident_fits(long long rb, bool aligned, int G, int seg) {
+  const long long chunks = chunks_for(rb, aligned) + (aligned ? 0 : 1);
+  return seg == 4096 && (chunks + G - 1) / G <= 32LL * ce::kStreamKRes;
 }
 
 // Launch shape of the streaming kernel, from sweeps on GB300 (16 warps per CTA
-// with three 4 KB slots each beat every smaller CTA, deeper ring and other
-// segment size measured):
+// with 4 KB slots beat every smaller CTA and other segment size measured):
 //  * one pass (FWD, BWD): a warp per row while every warp gets at least six
 //    rows; otherwise the fewest warps per row that give each group twelve,
 //    keeping at least 8 KB of the row per warp.  Long pieces with enough rows
@@ -310,7 +311,14 @@ bool choose_stream_plan(int mode, long long rb, long long M, int sm_count, Strea
   if (G == 1) {
     while (sg / 2 >= row_span && sg > 16) sg /= 2;
   }
-  sp = StreamPlan{nw, G, stream_slots(nw, sg), sg};
+  // ring depth per warp: two 4 KB slots for one pass, three for two passes
+  // (measured: a third slot costs the one-pass modes up to 7%, and gains the
+  // two-pass modes 2%); short rows take up to eight smaller slots
+  const long long per_warp = two_pass ? 3 * 4096 : 2 * 4096;
+  long long S = per_warp / sg;
+  if (S < 2) S = 2;
+  if (S > ce::kStreamMaxSlots) S = ce::kStreamMaxSlots;
+  sp = StreamPlan{nw, G, static_cast<int>(S), sg};
   return true;
 }
 
@@ -324,15 +332,18 @@ int env_kernel_choice() {
   if (std::strcmp(env, "unit") == 0) return 2;
   return 0;
 }
-void apply_env_stream_plan(StreamPlan& sp) {
+void apply_env_stream_plan(int mode, long long rb, bool aligned, StreamPlan& sp) {
   const char* env = std::getenv("CE_SPLAN");
   if (env == nullptr || *env == 0) return;
-  int nw = 0, G = 0, S = 0, seg = 0;
-  if (std::sscanf(env, "%d,%d,%d,%d", &nw, &G, &S, &seg) != 4) return;
+  int nw = 0, G = 0, S = 0, seg = 0, res = 0;
+  const int n = std::sscanf(env, "%d,%d,%d,%d,%d", &nw, &G, &S, &seg, &res);
+  if (n != 4 && n != 5) return;
   if (nw < 1 || nw > ce::kStreamMaxWarps || G < 1 || (G & (G - 1)) != 0 || nw % G != 0) return;
   if (S < 1 || S > ce::kStreamMaxSlots || seg < 16 || (seg & (seg - 1)) != 0) return;
   if (static_cast<long long>(nw) * S * seg > 220 * 1024) return;
-  sp = StreamPlan{nw, G, S, seg};
+  const bool resident = res != 0 && (mode == ce::FWD_BWD || mode == ce::SOFTMAX);
+  if (resident && !resident_fits(rb, aligned, G, seg)) return;
+  sp = StreamPlan{nw, G, S, seg, resident};
 }
 
 // ---------------------------------------------------------------------------
@@ -436,12 +447,12 @@ ce_status launch_stream(int mode, const void* logits, const int64_t* targets, co
   const int smem = sp.nw * sp.S * sp.seg;
   int per_sm = 0;
   cudaError_t e = cached_occupancy(
-      {dev, 1, static_cast<long long>(dtype), mode, sp.nw, smem, 1},
+      {dev, sp.res ? 2 : 1, static_cast<long long>(dtype), mode, sp.nw, smem, 1},
       [&](int* out) {
         switch (dtype) {
-          case CE_F32: return ce::stream_max_active<float>(mode, sp.nw, smem, out);
-          case CE_F16: return ce::stream_max_active<__half>(mode, sp.nw, smem, out);
-          default: return ce::stream_max_active<__nv_bfloat16>(mode, sp.nw, smem, out);
+          case CE_F32: return ce::stream_max_active<float>(mode, sp.res, sp.nw, smem, out);
+          case CE_F16: return ce::stream_max_active<__half>(mode, sp.res, sp.nw, smem, out);
+          default: return ce::stream_max_active<__nv_bfloat16>(mode, sp.res, sp.nw, smem, out);
         }
       },
       &per_sm);
@@ -462,9 +473,9 @@ ce_status launch_stream(int mode, const void* logits, const int64_t* targets, co
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int g = static_cast<int>(grid);
   switch (dtype) {
-    case CE_F32: e = ce::stream_launch<float>(mode, p, g, sp.nw, smem, s); break;
-    case CE_F16: e = ce::stream_launch<__half>(mode, p, g, sp.nw, smem, s); break;
-    default: e = ce::stream_launch<__nv_bfloat16>(mode, p, g, sp.nw, smem, s); break;
+    case CE_F32: e = ce::stream_launch<float>(mode, sp.res, p, g, sp.nw, smem, s); break;
+    case CE_F16: e = ce::stream_launch<__half>(mode, sp.res, p, g, sp.nw, smem, s); break;
+    default: e = ce::stream_launch<__nv_bfloat16>(mode, sp.res, p, g, sp.nw, smem, s); break;
   }
   if (e != cudaSuccess) return CE_ERR_CUDA;
   g_launches.fetch_add(1, std::memory_order_relaxed);
@@ -521,7 +532,7 @@ ce_status launch_rows(int mode, const void* logits, const int64_t* targets, cons
     const bool use_stream = forced == 1 || (forced == 0 && default_use_stream(mode, rb, aligned));
     StreamPlan sp;
     if (use_stream && choose_stream_plan(mode, rb, M, di.sm_count, sp)) {
-      apply_env_stream_plan(sp);
+      apply_env_stream_plan(mode, rb, aligned, sp);
       return launch_stream(mode, logits, targets, lse_in, M, V, dtype, red, loss, row_loss,
                            lse_out, grad_scale, stream, di, dev, static_scratch, out_buf, sp);
     }

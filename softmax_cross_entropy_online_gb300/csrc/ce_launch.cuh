@@ -107,21 +107,29 @@ cudaError_t rows_max_active(int mode, int variant, int smem_bytes, int CL, int s
 }
 
 // ---- the warp-streaming kernel (ce_stream.cuh) ----
+// kStreamKRes: register chunks a lane holds in the resident rows of the
+// writing modes (0: stream the row twice)
+constexpr int kStreamKRes = 16;
+
 template <typename T>
-const void* stream_kernel_ptr(int mode) {
+const void* stream_kernel_ptr(int mode, bool resident) {
   switch (mode) {
-    case FWD: return reinterpret_cast<const void*>(&ce_stream_kernel<T, FWD>);
-    case FWD_BWD: return reinterpret_cast<const void*>(&ce_stream_kernel<T, FWD_BWD>);
-    case BWD: return reinterpret_cast<const void*>(&ce_stream_kernel<T, BWD>);
-    case SOFTMAX: return reinterpret_cast<const void*>(&ce_stream_kernel<T, SOFTMAX>);
+    case FWD: return reinterpret_cast<const void*>(&ce_stream_kernel<T, FWD, 0>);
+    case FWD_BWD:
+      return resident ? reinterpret_cast<const void*>(&ce_stream_kernel<T, FWD_BWD, kStreamKRes>)
+                      : reinterpret_cast<const void*>(&ce_stream_kernel<T, FWD_BWD, 0>);
+    case BWD: return reinterpret_cast<const void*>(&ce_stream_kernel<T, BWD, 0>);
+    case SOFTMAX:
+      return resident ? reinterpret_cast<const void*>(&ce_stream_kernel<T, SOFTMAX, kStreamKRes>)
+                      : reinterpret_cast<const void*>(&ce_stream_kernel<T, SOFTMAX, 0>);
     default: return nullptr;
   }
 }
 
 template <typename T>
-cudaError_t stream_launch(int mode, const StreamParams& p, int grid, int nwarps, int smem_bytes,
-                          cudaStream_t stream) {
-  const void* fn = stream_kernel_ptr<T>(mode);
+cudaError_t stream_launch(int mode, bool resident, const StreamParams& p, int grid, int nwarps,
+                          int smem_bytes, cudaStream_t stream) {
+  const void* fn = stream_kernel_ptr<T>(mode, resident);
   if (fn == nullptr || nwarps < 1 || nwarps > kStreamMaxWarps) return cudaErrorInvalidValue;
   cudaError_t e = ensure_max_smem(fn, smem_bytes);
   if (e != cudaSuccess) return e;
@@ -136,8 +144,8 @@ cudaError_t stream_launch(int mode, const StreamParams& p, int grid, int nwarps,
 
 // CTAs of the streaming kernel that fit on one SM at once.
 template <typename T>
-cudaError_t stream_max_active(int mode, int nwarps, int smem_bytes, int* per_sm) {
-  const void* fn = stream_kernel_ptr<T>(mode);
+cudaError_t stream_max_active(int mode, bool resident, int nwarps, int smem_bytes, int* per_sm) {
+  const void* fn = stream_kernel_ptr<T>(mode, resident);
   if (fn == nullptr) return cudaErrorInvalidValue;
   cudaError_t e = ensure_max_smem(fn, smem_bytes);
   if (e != cudaSuccess) return e;
@@ -149,8 +157,9 @@ cudaError_t stream_max_active(int mode, int nwarps, int smem_bytes, int* per_sm)
   template const void* rows_kernel_ptr<T>(int, int);                                            \
   template cudaError_t rows_launch<T>(int, int, const RowParams&, int, int, cudaStream_t);      \
   template cudaError_t rows_max_active<T>(int, int, int, int, int, int*);                       \
-  template const void* stream_kernel_ptr<T>(int);                                               \
-  template cudaError_t stream_launch<T>(int, const StreamParams&, int, int, int, cudaStream_t); \
-  template cudaError_t stream_max_active<T>(int, int, int, int*);
+  template const void* stream_kernel_ptr<T>(int, bool);                                         \
+  template cudaError_t stream_launch<T>(int, bool, const StreamParams&, int, int, int,          \
+                                        cudaStream_t);                                          \
+  template cudaError_t stream_max_active<T>(int, bool, int, int, int*);
 
 }  // namespace ce

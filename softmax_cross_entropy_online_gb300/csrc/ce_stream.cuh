@@ -160,7 +160,12 @@ __device__ __forceinline__ void online_rescale(float lm, float& m, float& mh, fl
 
 constexpr float kLn2 = 0.6931471805599453f;
 
-template <typename T, int MODE>
+// KRES > 0 (FWD_BWD, SOFTMAX): "resident" rows.  Each lane copies its chunks
+// of the piece (at most KRES, lane + 32 k) from the ring into registers and
+// releases the slots at once; the gradient is computed from those registers
+// after the merge, so a row is read once and the ring keeps loading the next
+// row meanwhile.  The host picks it when the row's pieces fit, with 4 KB slots.
+template <typename T, int MODE, int KRES>
 __global__ void __launch_bounds__(kStreamMaxWarps * 32, 1) ce_stream_kernel(const StreamParams p) {
   using E = Elem<T>;
   constexpr int EPC = E::EPC;
@@ -169,7 +174,9 @@ __global__ void __launch_bounds__(kStreamMaxWarps * 32, 1) ce_stream_kernel(cons
   constexpr bool STATS = MODE != BWD;                  // a statistics pass
   constexpr bool GRAD = MODE != FWD;                   // a gradient / probability pass
   constexpr bool TARGETS = MODE != SOFTMAX;
-  constexpr int NPASS = (STATS && GRAD) ? 2 : 1;
+  constexpr bool RES = KRES > 0 && STATS && GRAD;
+  constexpr int KSEG = 8;  // resident: chunks per lane in one 4 KB slot
+  constexpr int NPASS = (STATS && GRAD && !RES) ? 2 : 1;
   // chunks per lane in a statistics sub-block: fewer in the two-pass modes,
   // whose gradient pass needs registers of its own
   constexpr int KPL = NPASS == 2 ? kStreamKPL / 2 : kStreamKPL;
@@ -179,6 +186,10 @@ __global__ void __launch_bounds__(kStreamMaxWarps * 32, 1) ce_stream_kernel(cons
   __shared__ __align__(16) float4 red[2][kStreamMaxWarps];
   __shared__ double acc_slot[kStreamMaxWarps];
   __shared__ IssueCursor cursor[kStreamMaxWarps];
+  // resident rows: the values of the row's partial head and tail chunks, kept
+  // by lanes 0 and 1 between the two halves of the row (shared memory, so
+  // they cost no registers on the other lanes)
+  __shared__ float edge_buf[RES ? kStreamMaxWarps : 1][2][8];
 
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
@@ -211,7 +222,7 @@ __global__ void __launch_bounds__(kStreamMaxWarps * 32, 1) ce_stream_kernel(cons
   // (no divergent bookkeeping on the warp's path; only lane 0 issues the
   // copy).  Two-pass modes need those registers elsewhere: lane 0 alone keeps
   // it in shared memory.
-  constexpr bool REG_CURSOR = NPASS == 1;
+  constexpr bool REG_CURSOR = NPASS == 1 && !RES;
   IssueCursor reg_cur;
   IssueCursor& cur = REG_CURSOR ? reg_cur : cursor[warp];
   if (REG_CURSOR || lane == 0) {
@@ -345,9 +356,74 @@ __global__ void __launch_bounds__(kStreamMaxWarps * 32, 1) ce_stream_kernel(cons
     };
 
     float Mrow = 0.f, Srow = 1.f;  // row max and sum of exp(x - max)
+    float m = -INFINITY, mh = 0.f, s = 0.f;  // this lane's pair
+    uint4 qr[RES ? KRES : 1];                // resident: the lane's raw chunks
+    const int fa_row = g.p0 > 1 ? g.p0 : 1;  // the piece's full chunks [fa_row, fb_row)
+    const int fb_row = g.p1 < g.nI + 1 ? g.p1 : g.nI + 1;
+    if constexpr (STATS && RES) {
+      float (*ev)[8] = edge_buf[warp];
+      if (lane < 2) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) ev[lane][q] = -INFINITY;
+      }
+      uint32_t sbase = 0;
+      int c0 = g.p0;
+      float cm = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < KRES; ++k) {
+        if (k % KSEG == 0 && k / KSEG < g.ns) {
+          if (k > 0) release_segment();
+          sbase = wait_segment();
+          c0 = g.p0 + (k / KSEG) * SC;
+          const int c1 = (c0 + SC < g.p1) ? c0 + SC : g.p1;
+          if (TARGETS && lane == 0 && t_ok && tc >= c0 && tc < c1) {
+            xt = (tc >= g.ld_lo && tc < g.ld_hi)
+                     ? E::ld(static_cast<char*>(__cvta_shared_to_generic(sbase + 16 * (tc - c0) + tq * ES)))
+                     : E::ld(reinterpret_cast<const char*>(g.as) + t * ES);
+            have_xt = true;
+          }
+          if (c0 <= 0 && 0 < c1 && lane == 0) edge_vals(0, c0, sbase, ev[0]);
+          if (g.nI + 1 >= c0 && g.nI + 1 < c1 && lane == 1) edge_vals(g.nI + 1, c0, sbase, ev[1]);
+        }
+        const int c = g.p0 + lane + 32 * k;
+        if (c >= fa_row && c < fb_row) {
+          qr[k] = lds128(sbase + 16 * (c - c0));
+          cm = fmaxf(cm, E::chunk_max(qr[k]));
+        }
+      }
+      if (g.ns > 0) release_segment();
+      // (the host keeps every piece within KRES chunks a lane; any further
+      // segment is still consumed, so the ring stays in step)
+      for (int sg = KRES / KSEG; sg < g.ns; ++sg) {
+        wait_segment();
+        release_segment();
+      }
+      float pe = 0.f;  // lanes 0 and 1: the partial chunk's share of the sum
+      if (lane < 2) {
+#pragma unroll
+        for (int q = 0; q < EPC; ++q) cm = fmaxf(cm, ev[lane][q]);
+      }
+      m = cm;
+      mh = (m == -INFINITY) ? 0.f : m * kLog2e;
+      float ps[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int k = 0; k < KRES; ++k) {
+        const int c = g.p0 + lane + 32 * k;
+        if (c >= fa_row && c < fb_row) {
+          float x[EPC];
+          E::unpack(qr[k], x);
+#pragma unroll
+          for (int e = 0; e < EPC; ++e) ps[e & 3] += ex2(fmaf(x[e], kLog2e, -mh));
+        }
+      }
+      if (lane < 2) {
+#pragma unroll
+        for (int q = 0; q < EPC; ++q) pe += ex2(fmaf(ev[lane][q], kLog2e, -mh));
+      }
+      s = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + pe;
+    }
     if (STATS) {
-      float m = -INFINITY, mh = 0.f, s = 0.f;
-      for (int sg = 0; sg < g.ns; ++sg) {
+      for (int sg = 0; sg < (RES ? 0 : g.ns); ++sg) {
         const int c0 = g.p0 + (sg << p.seg_shift);
         const int c1 = (c0 + SC < g.p1) ? c0 + SC : g.p1;
         const uint32_t sbase = wait_segment();
@@ -482,7 +558,49 @@ __global__ void __launch_bounds__(kStreamMaxWarps * 32, 1) ce_stream_kernel(cons
         return MODE == BWD ? expm1f(x - lse_given) * sc : expm1f((x - Mrow) - lnS) * sc;
       };
       char* const out_row = reinterpret_cast<char*>(g.as) + p.out_delta;
-      for (int sg = 0; sg < g.ns; ++sg) {
+      if constexpr (RES) {
+        // g = e' * f with e' = 2^(x log2e - mh), this lane's own reference,
+        // and f = exp(m - lse) * 2^-ml * scale taken once
+        const float mref = (m == -INFINITY) ? 0.f : m;
+        const float ml = fmaf(mref, kLog2e, -mh);
+        const float f = ex2((m - Mrow) * kLog2e - lg2(Srow) - ml) * sc;
+        char* const o0 = out_row + (g.hb - 16);
+#pragma unroll
+        for (int k = 0; k < KRES; ++k) {
+          const int c = g.p0 + lane + 32 * k;
+          if (c >= fa_row && c < fb_row) {
+            float x[EPC], gv[EPC];
+            E::unpack(qr[k], x);
+#pragma unroll
+            for (int e = 0; e < EPC; ++e) gv[e] = ex2(fmaf(x[e], kLog2e, -mh)) * f;
+            if (c == tc) {
+#pragma unroll
+              for (int e = 0; e < EPC; ++e)
+                if (e == tq) gv[e] = target_grad(x[e]);
+            }
+            stg128_hint(o0 + 16LL * c, E::pack(gv), pol_drop);
+          }
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int c = h ? g.nI + 1 : 0;
+          const bool mine = h ? (lane == 1 && c >= g.p0 && c < g.p1) : (lane == 0 && g.p0 <= 0 && 0 < g.p1);
+          if (mine) {
+            const int e0 = (g.hb - 16 + 16 * c) >> LOG_ES;
+#pragma unroll
+            for (int q = 0; q < EPC; ++q) {
+              const int e = e0 + q;
+              if (e >= 0 && e < V) {
+                const float x = edge_buf[RES ? warp : 0][h][q];
+                const float gv = (t_ok && e == static_cast<int>(t)) ? target_grad(x)
+                                                                    : ex2(fmaf(x, kLog2e, -mh)) * f;
+                E::st(out_row + static_cast<long long>(e) * ES, gv);
+              }
+            }
+          }
+        }
+      }
+      for (int sg = 0; sg < (RES ? 0 : g.ns); ++sg) {
         const int c0 = g.p0 + (sg << p.seg_shift);
         const int c1 = (c0 + SC < g.p1) ? c0 + SC : g.p1;
         const uint32_t sbase = wait_segment();

@@ -90,6 +90,34 @@ def test_stream_launch_shapes(splan, dtype, V, monkeypatch):
     check_case(x, t, dtype)
 
 
+# resident rows (fifth field 1): every lane holds its chunks of the row in
+# registers; fused fwd+bwd and softmax, across piece sizes, alignments and
+# the partial head / tail chunks
+@pytest.mark.parametrize("splan,dtype,V,offset", [
+    ("16,16,3,4096,1", "bf16", 50257, 0), ("16,16,3,4096,1", "f16", 50257, 3),
+    ("16,4,3,4096,1", "f32", 4096, 0), ("16,2,3,4096,1", "f32", 4096, 0),
+    ("16,2,2,4096,1", "f32", 4097, 1), ("16,1,2,4096,1", "bf16", 1999, 5),
+    ("16,1,3,4096,1", "f16", 7, 1), ("8,8,3,4096,1", "bf16", 30011, 0),
+    ("16,16,2,4096,1", "f32", 32768, 0), ("16,4,3,4096,1", "bf16", 16387, 2),
+])
+def test_stream_resident_rows(splan, dtype, V, offset, monkeypatch):
+    monkeypatch.setenv("CE_SPLAN", splan)
+    M = max(2, min(80, (2 << 20) // V))
+    x = synthetic.make_logits(M, V, dtype, 3.0, seed=V + 3)
+    t = synthetic.make_targets(M, V, seed=V + 4)
+    check_case(x, t, dtype, offset_elems=offset)
+    xd = P.to_device(x, dtype, offset_elems=offset)
+    probs, _ = api().ce_softmax_forward(xd, xd)
+    torch.cuda.synchronize()
+    p_ref = oracle.softmax_rows(P.widen(x, dtype))
+    pg = oracle.to_f64(P.to_host(probs, dtype), dtype)
+    if dtype == "f32":
+        assert np.all(np.abs(pg - p_ref) <= 1e-5)
+    else:
+        err = np.abs(pg - oracle.round_to_format(p_ref, dtype))
+        assert np.all(err <= oracle.ulp(p_ref, dtype) + 4e-6)
+
+
 @pytest.mark.parametrize("reduction", ["mean", "sum", "none"])
 def test_stream_reductions(reduction):
     x = synthetic.make_logits(64, 4096, "f32", 2.0, seed=3)
