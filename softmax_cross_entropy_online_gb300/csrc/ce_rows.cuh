@@ -485,6 +485,43 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
           mbar_arrive(fb);
         }
       };
+      // Writing modes move a stage in kParts parts of fixed stage offsets: part
+      // q of the refill is loaded as soon as part q of the previous unit's
+      // store has been read out, so the store's tail and the load's head
+      // overlap instead of following each other.
+      constexpr int kParts = 4;
+      auto part_of = [&](int a, int b, int q, int& pa, int& pb) {
+        const int lo_q = (q * p.q_chunks) / kParts, hi_q = ((q + 1) * p.q_chunks) / kParts;
+        pa = a > lo_q ? a : lo_q;
+        pb = b < hi_q ? b : hi_q;
+      };
+      auto refill_in_parts = [&](long long i, int s) {
+        const UnitGeo g = unit_geo(p, cid + i * ncl, rank);
+        int lo, hi;
+        load_range(g, lo, hi);
+        const uint32_t fb = smem_u32(&full_bar[s]);
+        if (hi > lo) {
+          mbar_arrive_expect_tx(fb, static_cast<uint32_t>((hi - lo) * 16));
+        } else {
+          mbar_arrive(fb);
+        }
+#pragma unroll
+        for (int q = 0; q < kParts; ++q) {
+          // parts 0..q of the store of this stage's previous unit are read out
+          if (q == 0) bulk_wait_read<kParts - 1>();
+          else if (q == 1) bulk_wait_read<kParts - 2>();
+          else if (q == 2) bulk_wait_read<kParts - 3>();
+          else bulk_wait_read<0>();
+          int a, b;
+          part_of(lo - g.w0, hi - g.w0, q, a, b);
+          if (b > a) {
+            fence_proxy_async_smem();
+            bulk_load(stage0 + s * p.stage_bytes + a * 16,
+                      reinterpret_cast<const void*>(g.as + g.hb - 16 + 16LL * (g.w0 + a)),
+                      static_cast<uint32_t>((b - a) * 16), fb);
+          }
+        }
+      };
       const long long pre = n_iter < S ? n_iter : S;
       for (long long i = 0; i < pre; ++i) issue_load(i, static_cast<int>(i));
       // A stage is refilled as soon as the store of its unit has been read out
@@ -492,7 +529,7 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
       // consumers.  (The refill brings unit r + S, r = j - lag, which must not
       // be loaded yet, so any lag <= S - 1 is valid; a larger lag only shortens
       // the lookahead to S - 1 - lag units.)
-      const int lag = 0;
+      constexpr int lag = 0;  // the stage just stored is the one refilled
       int s = 0, sr = S - lag;  // stages of unit j and of unit j - lag (mod S)
       if (sr == S) sr = 0;
       uint32_t phase = 0;
@@ -504,17 +541,17 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
           const UnitGeo go = unit_geo(p, cid + j * ncl, rank);
           int lo, hi;
           bulk_range(go, lo, hi);
-          if (hi > lo)
-            bulk_store(reinterpret_cast<void*>(go.as + go.hb - 16 + 16LL * lo + p.out_delta),
-                       stage0 + s * p.stage_bytes + (lo - go.w0) * 16, (hi - lo) * 16);
-          bulk_commit();  // one group per unit (possibly empty) keeps the count exact
-          const long long r = j - lag;
-          if (r >= 0 && r + S < n_iter) {
-            if (lag == 2) bulk_wait_read<2>();
-            else if (lag == 1) bulk_wait_read<1>();
-            else bulk_wait_read<0>();
-            issue_load(r + S, sr);
+#pragma unroll
+          for (int q = 0; q < kParts; ++q) {
+            int a, b;
+            part_of(lo - go.w0, hi - go.w0, q, a, b);
+            if (b > a)
+              bulk_store(reinterpret_cast<void*>(go.as + go.hb - 16 + 16LL * (go.w0 + a) + p.out_delta),
+                         stage0 + s * p.stage_bytes + a * 16, (b - a) * 16);
+            bulk_commit();  // one group per part (possibly empty) keeps the count exact
           }
+          const long long r = j - lag;
+          if (r >= 0 && r + S < n_iter) refill_in_parts(r + S, sr);
         }
         if (++s == S) { s = 0; phase ^= 1u; }
         if (++sr == S) sr = 0;
