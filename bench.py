@@ -43,7 +43,7 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM traffic of the fused fwd+bwd kernel per launch on f32 [32768, 4096],
 # from `ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum` (summarised
 # under profiles/), valid only for the kernel source it was taken on: the
-# digest of csrc/ at that time.  Any change to the kernels nulls it.
+# digest of the row-kernel sources at that time.  Any change to them nulls it.
 NCU_TRAFFIC = {
     # profiles/ce_rows_fwd_bwd_f32_32768x4096.md: a 16384-row capture, scaled 2x
     "a49986c8c7b745c097223a82c0173ce019d121277670bfdfde67cecece81ee8f": {
@@ -58,13 +58,18 @@ def algorithmic_bytes(M: int, V: int, es: int, bwd: bool) -> int:
     return x * (2 if bwd else 1) + M * 8 + M * 4 * 2 + 4
 
 
+# The sources that decide which row kernel runs and what it does; the
+# tensor-core GEMM of the fused linear path does not enter the record.
+ROW_KERNEL_SOURCES = ("ce_rows.cuh", "ce_stream.cuh", "ce_launch.cuh", "ce_rows_f32.cu",
+                      "ce_rows_f16.cu", "ce_rows_bf16.cu", "ce_api.cu")
+
+
 def csrc_digest() -> str:
     d = os.path.join(ROOT, "softmax_cross_entropy_online_gb300", "csrc")
     h = hashlib.sha256()
-    for f in sorted(os.listdir(d)):
-        if f.endswith((".cu", ".cuh")):
-            with open(os.path.join(d, f), "rb") as fh:
-                h.update(f.encode() + b"\0" + fh.read())
+    for f in ROW_KERNEL_SOURCES:
+        with open(os.path.join(d, f), "rb") as fh:
+            h.update(f.encode() + b"\0" + fh.read())
     return h.hexdigest()
 
 

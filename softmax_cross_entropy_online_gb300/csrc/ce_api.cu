@@ -1,7 +1,8 @@
 // ce_api.cu -- the C ABI (include/ce_gb300.h): argument checks, the choice
-// of launch shape for each (dtype, V, M), the per-stream reduction scratch,
-// the device error word, and the launches.  Every computation happens in the
-// kernels of ce_rows.cuh; this file only validates, plans and launches.
+// of kernel and launch shape for each (mode, dtype, V, M), the per-stream
+// reduction scratch, the device error word, and the launches.  Every
+// computation happens in the kernels (ce_rows.cuh, ce_stream.cuh,
+// ce_gemm.cu); this file only validates, plans and launches.
 #include <array>
 #include <atomic>
 #include <cmath>
@@ -192,7 +193,9 @@ long long stage_bytes_for(int variant, int R, int CL, long long rb, bool aligned
   return per_cta * 16;
 }
 
-// Default launch shapes, from sweeps of every shape on GB300:
+// Default launch shapes of the unit kernel, from sweeps of every shape on
+// GB300 (the forward and the longest rows default to the streaming kernel;
+// these shapes serve them when the unit kernel is forced):
 //  * rows up to 32 KB: R rows per unit of up to 64 KB.  The forward (read
 //    only) uses 256 streaming consumer threads with one stage, three CTAs
 //    per SM; the writing modes use 512 consumer threads with two stages, one
@@ -322,9 +325,13 @@ bool choose_stream_plan(int mode, long long rb, long long M, int sm_count, Strea
   return true;
 }
 
-// Tuning overrides: CE_KERNEL=stream|unit forces a kernel; CE_SPLAN="nw,G,S,seg"
-// (seg a power of two, at least 16 bytes)
-// sets the streaming shape (ignored unless it fits the kernel's limits).
+// Tuning overrides: CE_KERNEL=stream|unit forces a kernel; CE_SPLAN=
+// "nw,G,S,seg[,res]" sets the streaming shape (seg a power of two of at least
+// 16 bytes; res = 1 asks for resident rows in the writing modes), ignored
+// unless it fits the kernel's limits.  Resident rows are never the default:
+// measured, they tie with the unit kernel where pieces span two slots (fp32
+// 4096: 90.3% against 90.1%) and lose where a row needs a whole CTA (bf16
+// 50257: 54% against 78%, the CTA-wide merge stalls every warp's ring).
 int env_kernel_choice() {
   const char* env = std::getenv("CE_KERNEL");
   if (env == nullptr) return 0;
