@@ -160,27 +160,6 @@ __device__ __forceinline__ void online_rescale(float lm, float& m, float& mh, fl
 
 constexpr float kLn2 = 0.6931471805599453f;
 
-// Order of a group's steps in the two-pass modes: the statistics of row i + 1
-// run before the gradient of row i, so a warp never waits for the group's merge
-// of a row it has just finished (by the time it needs row i's merged pair,
-// every warp has long published it).  Steps: S0, S1, G0, S2, G1, ..., S(n-1),
-// G(n-2), G(n-1).
-__device__ __forceinline__ void skew_step(long long k, long long n, long long& ri, int& pass) {
-  if (k == 0) {
-    ri = 0;
-    pass = 0;
-  } else if (k == 2 * n - 1) {
-    ri = n - 1;
-    pass = 1;
-  } else if (k & 1) {
-    ri = (k + 1) >> 1;
-    pass = 0;
-  } else {
-    ri = (k >> 1) - 1;
-    pass = 1;
-  }
-}
-
 // KRES > 0 (FWD_BWD, SOFTMAX): "resident" rows.  Each lane copies its chunks
 // of the piece (at most KRES, lane + 32 k) from the ring into registers and
 // releases the slots at once; the gradient is computed from those registers
@@ -201,8 +180,6 @@ __global__ void __launch_bounds__(kStreamMaxWarps * 32, 1) ce_stream_kernel(cons
   // chunks per lane in a statistics sub-block: fewer in the two-pass modes,
   // whose gradient pass needs registers of its own
   constexpr int KPL = NPASS == 2 ? kStreamKPL / 2 : kStreamKPL;
-  // two passes: the skewed step order and split-phase merges (see skew_step)
-  constexpr bool SKEW = NPASS == 2;
 
   extern __shared__ __align__(128) unsigned char ring_mem[];
   __shared__ __align__(8) unsigned long long full_bar[kStreamMaxWarps][kStreamMaxSlots];
@@ -213,11 +190,6 @@ __global__ void __launch_bounds__(kStreamMaxWarps * 32, 1) ce_stream_kernel(cons
   // by lanes 0 and 1 between the two halves of the row (shared memory, so
   // they cost no registers on the other lanes)
   __shared__ float edge_buf[RES ? kStreamMaxWarps : 1][2][8];
-  // skewed merges: each warp's (m, s, x_t, has x_t) of a row, four rows deep,
-  // and per group one mbarrier per row slot (count G): a warp arrives after
-  // publishing its pair and waits only when it needs the row's merged pair
-  __shared__ __align__(16) float4 mslot[SKEW ? kStreamMaxWarps : 1][4];
-  __shared__ __align__(8) unsigned long long row_bar[SKEW ? kStreamMaxWarps : 1][4];
 
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
@@ -238,21 +210,9 @@ __global__ void __launch_bounds__(kStreamMaxWarps * 32, 1) ce_stream_kernel(cons
 
   if (lane == 0) {
     for (int s = 0; s < S; ++s) mbar_init(smem_u32(&full_bar[warp][s]), 1);
-    if (SKEW && kw == 0)
-      for (int j = 0; j < 4; ++j) mbar_init(smem_u32(&row_bar[SKEW ? grp : 0][j]), G);
     fence_mbar_init_cluster();
   }
   __syncthreads();
-  const long long nsteps = NPASS * n_rows;
-  // the row and pass of step k
-  auto step_of = [&](long long k, long long& ri, int& pass) {
-    if (SKEW) {
-      skew_step(k, n_rows, ri, pass);
-    } else {
-      ri = k;
-      pass = 0;
-    }
-  };
 
   const unsigned long long pol_keep = l2_policy_evict_last();
   const unsigned long long pol_drop = l2_policy_evict_first();
@@ -266,7 +226,7 @@ __global__ void __launch_bounds__(kStreamMaxWarps * 32, 1) ce_stream_kernel(cons
   IssueCursor reg_cur;
   IssueCursor& cur = REG_CURSOR ? reg_cur : cursor[warp];
   if (REG_CURSOR || lane == 0) {
-    cur.ri = 0;  // the step (see step_of)
+    cur.ri = 0;
     cur.pass = 0;
     cur.seg = 0;
     cur.slot = 0;
@@ -274,21 +234,22 @@ __global__ void __launch_bounds__(kStreamMaxWarps * 32, 1) ce_stream_kernel(cons
   }
   auto issue_next = [&]() {
     // the cursor is read into registers once and written back once
-    long long ks = cur.ri;
+    long long ri = cur.ri;
     int pass = cur.pass, seg = cur.seg;
     const int slot = cur.slot;
     StreamGeo ig = cur.g;
     bool moved = false;
-    while (ks < nsteps && seg >= ig.ns) {
+    while (ri < n_rows && seg >= ig.ns) {
       seg = 0;
-      if (++ks < nsteps) {
-        long long rk;
-        step_of(ks, rk, pass);
-        ig = stream_geo(p, gidx + rk * ngroups, kw);
-        moved = true;
+      if (++pass == NPASS) {
+        pass = 0;
+        if (++ri < n_rows) {
+          ig = stream_geo(p, gidx + ri * ngroups, kw);
+          moved = true;
+        }
       }
     }
-    if (ks < nsteps) {
+    if (ri < n_rows) {
       const int c0 = ig.p0 + (seg << p.seg_shift);
       int c1 = c0 + SC;
       if (c1 > ig.p1) c1 = ig.p1;
@@ -311,7 +272,7 @@ __global__ void __launch_bounds__(kStreamMaxWarps * 32, 1) ce_stream_kernel(cons
       ++seg;
       cur.slot = (slot + 1 == S) ? 0 : slot + 1;
     }
-    cur.ri = ks;
+    cur.ri = ri;
     cur.pass = pass;
     cur.seg = seg;
     if (moved) cur.g = ig;
@@ -354,35 +315,17 @@ __global__ void __launch_bounds__(kStreamMaxWarps * 32, 1) ce_stream_kernel(cons
   fetch(0, t_cur, l_cur);
   fetch(32, t_nxt, l_nxt);
 
-  // skewed steps: the targets of the last two rows whose statistics ran
-  long long t_last = -1, t_prev = -1, last_stats_ri = -1;
-  for (long long k = 0; k < nsteps; ++k) {
-    long long ri;
-    int pass;
-    step_of(k, ri, pass);
-    const bool do_stats = STATS && pass == 0;
-    const bool do_grad = GRAD && (pass == 1 || !SKEW);
+  for (long long ri = 0; ri < n_rows; ++ri) {
     const long long r = gidx + ri * ngroups;
     const StreamGeo g = stream_geo(p, r, kw);
-    long long t = -1;
-    float lse_given = 0.f;
-    if (!SKEW || pass == 0) {
-      const int bl = static_cast<int>(ri & 31);
-      if (bl == 0 && ri > 0) {
-        t_cur = t_nxt;
-        l_cur = l_nxt;
-        fetch(ri + 32, t_nxt, l_nxt);
-      }
-      t = TARGETS ? __shfl_sync(0xffffffffu, t_cur, bl) : -1;
-      lse_given = (MODE == BWD) ? __shfl_sync(0xffffffffu, l_cur, bl) : 0.f;
-      if (SKEW) {
-        t_prev = t_last;
-        t_last = t;
-        last_stats_ri = ri;
-      }
-    } else {
-      t = (ri == last_stats_ri) ? t_last : t_prev;
+    const int bl = static_cast<int>(ri & 31);
+    if (bl == 0 && ri > 0) {
+      t_cur = t_nxt;
+      l_cur = l_nxt;
+      fetch(ri + 32, t_nxt, l_nxt);
     }
+    const long long t = TARGETS ? __shfl_sync(0xffffffffu, t_cur, bl) : -1;
+    const float lse_given = (MODE == BWD) ? __shfl_sync(0xffffffffu, l_cur, bl) : 0.f;
     const bool t_ok = TARGETS && t >= 0 && t < V;
     // the target's chunk and its slot in the chunk
     const int tbo = t_ok ? static_cast<int>(t) * ES + 16 - g.hb : -1;
@@ -479,7 +422,7 @@ __global__ void __launch_bounds__(kStreamMaxWarps * 32, 1) ce_stream_kernel(cons
       }
       s = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + pe;
     }
-    if (do_stats) {
+    if (STATS) {
       for (int sg = 0; sg < (RES ? 0 : g.ns); ++sg) {
         const int c0 = g.p0 + (sg << p.seg_shift);
         const int c1 = (c0 + SC < g.p1) ? c0 + SC : g.p1;
@@ -557,13 +500,7 @@ __global__ void __launch_bounds__(kStreamMaxWarps * 32, 1) ce_stream_kernel(cons
       float sw = (m == -INFINITY) ? 0.f : s * ex2((m - mw) * kLog2e - ml);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) sw += __shfl_xor_sync(0xffffffffu, sw, o);
-      if (SKEW) {
-        // publish; the merge happens at this row's gradient step
-        if (lane == 0) {
-          mslot[SKEW ? warp : 0][ri & 3] = make_float4(mw, sw, xt, have_xt ? 1.f : 0.f);
-          mbar_arrive(smem_u32(&row_bar[SKEW ? grp : 0][ri & 3]));
-        }
-      } else if (G == 1) {
+      if (G == 1) {
         Mrow = mw;
         Srow = sw;
       } else {
@@ -582,34 +519,6 @@ __global__ void __launch_bounds__(kStreamMaxWarps * 32, 1) ce_stream_kernel(cons
         Srow = sg2;
         xt = xg;
       }
-      if (!SKEW && row_leader) {
-        const float lnS = lg2(Srow) * kLn2;
-        const float rl = t_ok ? (Mrow - xt) + lnS : __int_as_float(0x7fc00000);
-        if (p.row_loss) p.row_loss[r] = rl;
-        if (p.lse_out) p.lse_out[r] = Mrow + lnS;
-        acc += static_cast<double>(rl);
-        if (TARGETS && !t_ok) atomicOr(p.err, ERR_TARGET_RANGE);
-      }
-    }
-    if (!STATS && row_leader && !t_ok) atomicOr(p.err, ERR_TARGET_RANGE);
-
-    if (SKEW && do_grad) {
-      // the group's merged pair of this row (every warp published it one step ago)
-      mbar_wait<false>(smem_u32(&row_bar[SKEW ? grp : 0][ri & 3]),
-                       static_cast<uint32_t>((ri >> 2) & 1), p.err, failed, WAIT_LIMIT_NS,
-                       p.wait_hint_ns);
-      const float4 rr = (lane < G) ? mslot[SKEW ? grp * G + lane : 0][ri & 3]
-                                   : make_float4(-INFINITY, 0.f, 0.f, 0.f);
-      Mrow = warp_max(rr.x);
-      float sg2 = (rr.x == -INFINITY) ? 0.f : rr.y * ex2((rr.x - Mrow) * kLog2e);
-      float xg = rr.w != 0.f ? rr.z : 0.f;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        sg2 += __shfl_xor_sync(0xffffffffu, sg2, o);
-        xg += __shfl_xor_sync(0xffffffffu, xg, o);
-      }
-      Srow = sg2;
-      xt = xg;
       if (row_leader) {
         const float lnS = lg2(Srow) * kLn2;
         const float rl = t_ok ? (Mrow - xt) + lnS : __int_as_float(0x7fc00000);
@@ -618,9 +527,11 @@ __global__ void __launch_bounds__(kStreamMaxWarps * 32, 1) ce_stream_kernel(cons
         acc += static_cast<double>(rl);
         if (TARGETS && !t_ok) atomicOr(p.err, ERR_TARGET_RANGE);
       }
+    } else if (row_leader && !t_ok) {
+      atomicOr(p.err, ERR_TARGET_RANGE);
     }
 
-    if (do_grad) {
+    if (GRAD) {
       const float sc = p.grad_scale;
       // g = 2^(x log2e - Lh - Lc) * scale with Lh + Lc = lse log2e split into
       // a float and a small correction: the FFMA gives x log2e - Lh with one
