@@ -35,9 +35,6 @@ constexpr int kStreamKRes = 16;  // as in ce_launch.cuh
 ce_status gemm_bf16_tn(const void* A, long long lda, const void* B, long long ldb, float* D,
                        long long ldd, int M, int N, int K, float beta, cudaStream_t stream,
                        unsigned int* err, int sm_count, unsigned int wait_hint_ns);
-ce_status launch_convert_transpose(const float* G, int R, int C, long long ldg,
-                                   __nv_bfloat16* G16, long long ldo, __nv_bfloat16* Gt16,
-                                   long long ldt, cudaStream_t st, int sm_count);
 ce_status launch_transpose_bf16(const void* X, int R, int C, long long ldx, void* T,
                                 long long ldt, cudaStream_t st, int sm_count);
 ce_status launch_mean_rows(const float* rl, long long M, float* loss, cudaStream_t st);
@@ -418,7 +415,8 @@ ce_status launch_stream(int mode, const void* logits, const int64_t* targets, co
                         int64_t M, int64_t V, ce_dtype dtype, ce_reduction red, float* loss,
                         float* row_loss, float* lse_out, float grad_scale, void* stream,
                         const DeviceInfo& di, int dev, bool static_scratch, void* out_buf,
-                        const StreamPlan& sp) {
+                        const StreamPlan& sp, __nv_bfloat16* g16 = nullptr,
+                        long long g16_ld = 0) {
   const long long rb = static_cast<long long>(V) * elem_size(dtype);
   ce::StreamParams p;
   std::memset(&p, 0, sizeof(p));
@@ -450,6 +448,8 @@ ce_status launch_stream(int mode, const void* logits, const int64_t* targets, co
                                                               reinterpret_cast<uintptr_t>(logits));
   p.grad_scale = grad_scale;
   p.mean = (red == CE_RED_MEAN) ? 1 : 0;
+  p.g16 = g16;
+  p.g16_ld = g16_ld;
 
   const int smem = sp.nw * sp.S * sp.seg;
   int per_sm = 0;
@@ -503,10 +503,13 @@ bool default_use_stream(int mode, long long rb, bool aligned) {
 
 // static_scratch: reduce through g_noalloc_scratch (its ticket is cleared on
 // the stream before the launch) instead of the per-stream buffer.
+// g16 (FWD_BWD on fp32 logits only): the gradient is written as bf16 rows of
+// g16_ld elements into g16 instead of over the logits (streaming kernel).
 ce_status launch_rows(int mode, const void* logits, const int64_t* targets, const float* lse_in,
                       int64_t M, int64_t V, ce_dtype dtype, ce_reduction red, float* loss,
                       float* row_loss, float* lse_out, float grad_scale, void* stream,
-                      bool static_scratch = false, void* out_buf = nullptr) {
+                      bool static_scratch = false, void* out_buf = nullptr,
+                      __nv_bfloat16* g16 = nullptr, long long g16_ld = 0) {
   const int es = elem_size(dtype);
   if (es == 0) return CE_ERR_INVALID_ARG;
   if (red != CE_RED_MEAN && red != CE_RED_SUM && red != CE_RED_NONE) return CE_ERR_INVALID_ARG;
@@ -534,6 +537,16 @@ ce_status launch_rows(int mode, const void* logits, const int64_t* targets, cons
 
   const bool aligned = (lb % 16 == 0) && (rb % 16 == 0);
   if (V > ce_max_vocab(dtype)) return CE_ERR_UNSUPPORTED;  // the same limit for both kernels
+  if (g16 != nullptr) {
+    if (mode != ce::FWD_BWD || dtype != CE_F32 || out_buf != nullptr || g16_ld < V ||
+        (g16_ld % 4) || (reinterpret_cast<uintptr_t>(g16) % 16))
+      return CE_ERR_INVALID_ARG;
+    StreamPlan sp;
+    if (!choose_stream_plan(mode, rb, M, di.sm_count, sp)) return CE_ERR_UNSUPPORTED;
+    sp.res = false;
+    return launch_stream(mode, logits, targets, lse_in, M, V, dtype, red, loss, row_loss, lse_out,
+                         grad_scale, stream, di, dev, static_scratch, out_buf, sp, g16, g16_ld);
+  }
   {
     const int forced = env_kernel_choice();
     const bool use_stream = forced == 1 || (forced == 0 && default_use_stream(mode, rb, aligned));
@@ -616,7 +629,7 @@ ce_status launch_rows(int mode, const void* logits, const int64_t* targets, cons
 }
 
 // Workspace of the fused linear + cross-entropy for row chunks of `mc` rows:
-// Wt [H, ldv] bf16, logits/G [mc, V] fp32, G16 [mc, ldv] bf16, Gt16 [V, ldk]
+// Wt [H, ldv] bf16, logits [mc, V] fp32, G16 [mc, ldv] bf16, Gt16 [V, ldk]
 // bf16, ht [H, ldk] bf16, row losses [M] fp32 (ldv = V and ldk = mc rounded up
 // to a multiple of 8, padded with zeros).
 struct LinearWs {
@@ -759,6 +772,9 @@ ce_status linear_ce_fwd_bwd(const void* h, const void* W, const int64_t* targets
                                       sms)) != CE_OK)
     return st;
   ++launches;
+  // the padding columns [V, ldv) of G16 are never written by the row kernel
+  if (ldv > V && cudaMemset2DAsync(g16 + V, ldv * 2, 0, (ldv - V) * 2, mc, s) != cudaSuccess)
+    return CE_ERR_CUDA;
   const float scale = 1.0f / static_cast<float>(M);
   for (long long m0 = 0; m0 < M; m0 += mc) {
     const long long rows = (M - m0) < mc ? (M - m0) : mc;
@@ -769,13 +785,15 @@ ce_status linear_ce_fwd_bwd(const void* h, const void* W, const int64_t* targets
                                static_cast<int>(V), static_cast<int>(H), 0.f, s, di.err, sms,
                                hint)) != CE_OK)
       return st;
-    // in place: row losses and G = (softmax - onehot) / M
+    // row losses, and G16 [rows, ldv] = bf16 of G = (softmax - onehot) / M
+    // written by the row kernel straight from the fp32 logits
     if ((st = launch_rows(ce::FWD_BWD, logits, targets + m0, nullptr, rows, V, CE_F32,
-                          CE_RED_NONE, nullptr, rl + m0, nullptr, scale, stream)) != CE_OK)
+                          CE_RED_NONE, nullptr, rl + m0, nullptr, scale, stream, false, nullptr,
+                          g16, ldv)) != CE_OK)
       return st;
-    // G16 [rows, ldv] and G^T [V, ldk] in bf16, h_c^T [H, ldk]
-    if ((st = ce::launch_convert_transpose(logits, static_cast<int>(rows), static_cast<int>(V), V,
-                                           g16, ldv, gt16, ldk, s, sms)) != CE_OK)
+    // G^T [V, ldk] and h_c^T [H, ldk] in bf16
+    if ((st = ce::launch_transpose_bf16(g16, static_cast<int>(rows), static_cast<int>(V), ldv,
+                                        gt16, ldk, s, sms)) != CE_OK)
       return st;
     if ((st = ce::launch_transpose_bf16(hc, static_cast<int>(rows), static_cast<int>(H), H, ht,
                                         ldk, s, sms)) != CE_OK)

@@ -333,73 +333,8 @@ ce_status gemm_bf16_tn(const void* A, long long lda, const void* B, long long ld
 namespace ce {
 
 // --- layout helpers of the fused linear + cross-entropy ------------------------
-// G16[r, c] = bf16(G[r, c]) for c < C (zero in the padding columns up to ldo) and
-// Gt16[c, r] = bf16(G[r, c]) (zero in the padding columns r >= R up to ldt).
-// 64x64 tiles: 16-byte loads of G, 8-byte stores of G16, and 16-byte stores
-// of Gt16 from a padded bf16 tile in shared memory (scalar loads when rows of
-// G are not 16-byte aligned).  ldo and ldt are multiples of 8.
 constexpr int kTT = 64;       // tile edge
 constexpr int kTP = kTT + 8;  // padded pitch (bf16) of the shared tile
-__global__ void __launch_bounds__(256) convert_transpose_kernel(
-    const float* __restrict__ G, int R, int C, long long ldg, __nv_bfloat16* __restrict__ G16,
-    long long ldo, __nv_bfloat16* __restrict__ Gt16, long long ldt) {
-  __shared__ __align__(16) __nv_bfloat16 tile[kTT][kTP];
-  // 16-byte loads need rows of G on the 16-byte grid
-  const bool vec = (ldg % 4 == 0) && ((reinterpret_cast<uintptr_t>(G) & 15) == 0);
-  const long long tiles_c = (ldo + kTT - 1) / kTT;
-  const long long tiles_r = (ldt + kTT - 1) / kTT;
-  const int tid = threadIdx.x;
-  for (long long tt = blockIdx.x; tt < tiles_r * tiles_c; tt += gridDim.x) {
-    const long long r0 = (tt / tiles_c) * kTT, c0 = (tt % tiles_c) * kTT;
-    // load: 64 rows x 16 float4, four per thread
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int idx = tid + k * 256;
-      const int rr = idx >> 4, cq = (idx & 15) * 4;
-      const long long r = r0 + rr, c = c0 + cq;
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (r < R) {
-        if (vec && c + 3 < C) {
-          v = *reinterpret_cast<const float4*>(G + r * ldg + c);
-        } else {
-          if (c + 3 < C) v.w = G[r * ldg + c + 3];
-          if (c < C) v.x = G[r * ldg + c];
-          if (c + 1 < C) v.y = G[r * ldg + c + 1];
-          if (c + 2 < C) v.z = G[r * ldg + c + 2];
-        }
-      }
-      __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
-      if (r < R && c < ldo) {  // padding columns (c >= C) are written as zeros
-        uint2 pk;
-        pk.x = *reinterpret_cast<uint32_t*>(&lo);
-        pk.y = *reinterpret_cast<uint32_t*>(&hi);
-        *reinterpret_cast<uint2*>(G16 + r * ldo + c) = pk;
-      }
-      *reinterpret_cast<__nv_bfloat162*>(&tile[rr][cq]) = lo;
-      *reinterpret_cast<__nv_bfloat162*>(&tile[rr][cq + 2]) = hi;
-    }
-    __syncthreads();
-    // transposed store: 64 columns x 8 groups of 8 rows, two per thread
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const int idx = tid + k * 256;
-      const int cc = idx >> 3, rg = (idx & 7) * 8;
-      const long long c = c0 + cc, r = r0 + rg;
-      if (c < C && r < ldt) {
-        uint32_t w[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          __nv_bfloat162 pr;
-          pr.x = tile[rg + 2 * j][cc];
-          pr.y = tile[rg + 2 * j + 1][cc];
-          w[j] = *reinterpret_cast<uint32_t*>(&pr);
-        }
-        *reinterpret_cast<uint4*>(Gt16 + c * ldt + r) = make_uint4(w[0], w[1], w[2], w[3]);
-      }
-    }
-    __syncthreads();
-  }
-}
 
 // T[c, r] = X[r, c] for bf16, r < R, c < C (zero in the padding columns r >= R up
 // to ldt); 64x64 tiles with 16-byte loads and stores (ldx, ldt multiples of 8)
@@ -468,13 +403,6 @@ __global__ void mean_rows_kernel(const float* __restrict__ rl, long long M, floa
   if (threadIdx.x == 0) *loss = static_cast<float>(part[0] / static_cast<double>(M));
 }
 
-ce_status launch_convert_transpose(const float* G, int R, int C, long long ldg,
-                                   __nv_bfloat16* G16, long long ldo, __nv_bfloat16* Gt16,
-                                   long long ldt, cudaStream_t st, int sm_count) {
-  convert_transpose_kernel<<<sm_count * 8, 256, 0, st>>>(G, R, C, ldg, G16, ldo, Gt16,
-                                                                  ldt);
-  return cudaGetLastError() == cudaSuccess ? CE_OK : CE_ERR_CUDA;
-}
 ce_status launch_transpose_bf16(const void* X, int R, int C, long long ldx, void* T,
                                 long long ldt, cudaStream_t st, int sm_count) {
   transpose_bf16_kernel<<<sm_count * 8, 256, 0, st>>>(

@@ -67,6 +67,10 @@ struct StreamParams {
   long long out_delta;        // writes go to (address + out_delta); 0 = in place
   float grad_scale;           // FWD_BWD / BWD
   int mean;                   // 1: loss = sum / M, 0: loss = sum
+  // fp32 logits only: the gradient goes to g16 + row * g16_ld + e as bf16 (the
+  // operand of the fused linear path's gradient GEMMs) instead of in place
+  __nv_bfloat16* g16;
+  long long g16_ld;
 };
 
 // Chunk frame of one row and this warp's piece of it.
@@ -558,6 +562,33 @@ __global__ void __launch_bounds__(kStreamMaxWarps * 32, 1) ce_stream_kernel(cons
         return MODE == BWD ? expm1f(x - lse_given) * sc : expm1f((x - Mrow) - lnS) * sc;
       };
       char* const out_row = reinterpret_cast<char*>(g.as) + p.out_delta;
+      // bf16 gradient rows (fp32 logits): chunk c holds elements e0 .. e0 + 3,
+      // e0 = (hb - 16 + 16 c) / 4, 8-byte aligned in g16 when the row is on the
+      // 16-byte grid (g16_ld a multiple of 4)
+      constexpr bool CAN16 = ES == 4;
+      __nv_bfloat16* const g16_row = CAN16 && p.g16 ? p.g16 + r * p.g16_ld : nullptr;
+      auto store_chunk = [&](char* dst, int c, const float* gv) {
+        if (CAN16 && g16_row) {
+          __nv_bfloat16* const d = g16_row + ((g.hb - 16 + 16 * c) >> 2);
+          if (g.hb == 0) {
+            const __nv_bfloat162 lo = __floats2bfloat162_rn(gv[0], gv[1]);
+            const __nv_bfloat162 hi = __floats2bfloat162_rn(gv[2], gv[3 % EPC]);
+            uint2 w;
+            w.x = *reinterpret_cast<const uint32_t*>(&lo);
+            w.y = *reinterpret_cast<const uint32_t*>(&hi);
+            *reinterpret_cast<uint2*>(d) = w;
+          } else {
+#pragma unroll
+            for (int e = 0; e < 4 && e < EPC; ++e) d[e] = __float2bfloat16_rn(gv[e]);
+          }
+        } else {
+          stg128_hint(dst, E::pack(gv), pol_drop);
+        }
+      };
+      auto store_elem = [&](int e, float gv) {
+        if (CAN16 && g16_row) g16_row[e] = __float2bfloat16_rn(gv);
+        else E::st(out_row + static_cast<long long>(e) * ES, gv);
+      };
       if constexpr (RES) {
         // g = e' * f with e' = 2^(x log2e - mh), this lane's own reference,
         // and f = exp(m - lse) * 2^-ml * scale taken once
@@ -578,7 +609,7 @@ __global__ void __launch_bounds__(kStreamMaxWarps * 32, 1) ce_stream_kernel(cons
               for (int e = 0; e < EPC; ++e)
                 if (e == tq) gv[e] = target_grad(x[e]);
             }
-            stg128_hint(o0 + 16LL * c, E::pack(gv), pol_drop);
+            store_chunk(o0 + 16LL * c, c, gv);
           }
         }
 #pragma unroll
@@ -594,7 +625,7 @@ __global__ void __launch_bounds__(kStreamMaxWarps * 32, 1) ce_stream_kernel(cons
                 const float x = edge_buf[RES ? warp : 0][h][q];
                 const float gv = (t_ok && e == static_cast<int>(t)) ? target_grad(x)
                                                                     : ex2(fmaf(x, kLog2e, -mh)) * f;
-                E::st(out_row + static_cast<long long>(e) * ES, gv);
+                store_elem(e, gv);
               }
             }
           }
@@ -629,7 +660,7 @@ __global__ void __launch_bounds__(kStreamMaxWarps * 32, 1) ce_stream_kernel(cons
                 for (int e = 0; e < EPC; ++e)
                   if (e == tq) gv[e] = target_grad(x[e]);
               }
-              stg128_hint(o0 + 512 * j, E::pack(gv), pol_drop);
+              store_chunk(o0 + 512 * j, cl + 32 * j, gv);
             }
           }
         };
@@ -651,7 +682,7 @@ __global__ void __launch_bounds__(kStreamMaxWarps * 32, 1) ce_stream_kernel(cons
                 const float gv = (t_ok && e == static_cast<int>(t))
                                      ? target_grad(x[q])
                                      : ex2(fmaf(x[q], kLog2e, -Lh)) * scf;
-                E::st(out_row + static_cast<long long>(e) * ES, gv);
+                store_elem(e, gv);
               }
             }
           }
