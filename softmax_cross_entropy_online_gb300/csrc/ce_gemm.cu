@@ -15,9 +15,10 @@
 //    the shared-memory descriptors; tcgen05.commit frees a stage when the MMAs
 //    that read it are done and signals a full accumulator after the last k-tile;
 //  * warps 2..5 are the epilogue: each reads its 32 TMEM lanes (tile rows) with
-//    tcgen05.ld, adds beta * D when asked, and stores fp32 to global memory,
-//    then hands the accumulator back.  With two accumulators the epilogue of
-//    one tile overlaps the main loop of the next.
+//    tcgen05.ld, 32 columns at a time, turns the 32 x 32 block around in shared
+//    memory so that every global access covers one 128-byte row segment, adds
+//    beta * D when asked, and stores fp32, then hands the accumulator back.  With
+//    two accumulators the epilogue of one tile overlaps the main loop of the next.
 // Every mbarrier wait is bounded (see ce_rows.cuh); TMEM is freed on every path.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -115,6 +116,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   __shared__ __align__(8) unsigned long long accf_bar[2];
   __shared__ __align__(8) unsigned long long acce_bar[2];
   __shared__ uint32_t tmem_slot;
+  // epilogue staging: each epilogue warp turns its 32 x 32 block around here
+  // (pitch 33 floats: conflict-free in both directions) so that its global
+  // loads and stores cover one 128-byte row segment per instruction
+  __shared__ float stg[4][32][33];
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -218,36 +223,38 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int tn = tile / p.tiles_m;
       mbar_wait<false>(smem_u32(&accf_bar[a]), aph, p.err, failed, WAIT_LIMIT_NS, hint);
       tc_fence_after();
-      const int row = tm * kGemmBM + 32 * q + lane;
-      float* drow = p.D + static_cast<long long>(row) * p.ldd;
+      const int rbase = tm * kGemmBM + 32 * q;  // this warp's 32 rows of the tile
+      float (*sb)[33] = stg[q];
 #pragma unroll 1
       for (int cc = 0; cc < kGemmBN / 32; ++cc) {
         float v[32];
         tmem_ld32(tmem + static_cast<uint32_t>(a * kGemmBN + cc * 32) +
                       (static_cast<uint32_t>(32 * q) << 16),
                   v);
-        const int col0 = tn * kGemmBN + cc * 32;
-        if (row < p.M && col0 < p.N) {
-          if (col0 + 32 <= p.N && (p.ldd & 3) == 0 &&
-              (reinterpret_cast<uintptr_t>(drow) & 15) == 0) {
-            float4* dst = reinterpret_cast<float4*>(drow + col0);
+        // lane = row on the way in, lane = column on the way out
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              float4 o = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-              if (p.beta != 0.f) {
-                const float4 old = dst[j];
-                o.x += old.x;
-                o.y += old.y;
-                o.z += old.z;
-                o.w += old.w;
-              }
-              dst[j] = o;
-            }
-          } else {
-            for (int j = 0; j < 32 && col0 + j < p.N; ++j)
-              drow[col0 + j] = (p.beta != 0.f) ? drow[col0 + j] + v[j] : v[j];
-          }
+        for (int j = 0; j < 32; ++j) sb[lane][j] = v[j];
+        __syncwarp();
+        const int col = tn * kGemmBN + cc * 32 + lane;
+        const bool col_ok = col < p.N;
+        float* const dcol = p.D + col;
+        if (p.beta != 0.f) {
+          float old[32];
+#pragma unroll
+          for (int r = 0; r < 32; ++r)
+            old[r] = (col_ok && rbase + r < p.M)
+                         ? dcol[static_cast<long long>(rbase + r) * p.ldd]
+                         : 0.f;
+#pragma unroll
+          for (int r = 0; r < 32; ++r)
+            if (col_ok && rbase + r < p.M)
+              dcol[static_cast<long long>(rbase + r) * p.ldd] = sb[r][lane] + old[r];
+        } else {
+#pragma unroll
+          for (int r = 0; r < 32; ++r)
+            if (col_ok && rbase + r < p.M) dcol[static_cast<long long>(rbase + r) * p.ldd] = sb[r][lane];
         }
+        __syncwarp();  // the block is read out before the next one is written
       }
       tc_fence_before();
       mbar_arrive(smem_u32(&acce_bar[a]));
