@@ -15,11 +15,15 @@
 //    the shared-memory descriptors; tcgen05.commit frees a stage when the MMAs
 //    that read it are done and signals a full accumulator after the last k-tile;
 //  * warps 2..5 are the epilogue: each reads its 32 TMEM lanes (tile rows) with
-//    tcgen05.ld, 32 columns at a time, turns the 32 x 32 block around in shared
-//    memory so that every global access covers one 128-byte row segment, adds
-//    beta * D when asked, and stores fp32, then hands the accumulator back.  With
-//    two accumulators the epilogue of one tile overlaps the main loop of the next.
+//    tcgen05.ld, 32 columns at a time, writes the 32 x 32 block into shared
+//    memory (128-byte swizzle) and hands it to a TMA tensor store, or, to
+//    accumulate (D += ...), a TMA tensor reduce-add done in L2; rows of D off the
+//    16-byte grid are written by the warp instead, one row segment per access.
+//    With two accumulators the epilogue of one tile overlaps the main loop of
+//    the next.
 // Every mbarrier wait is bounded (see ce_rows.cuh); TMEM is freed on every path.
+#include <cstring>
+
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -36,7 +40,8 @@ constexpr int kGemmThreads = 192;
 constexpr int kTileABytes = kGemmBM * kGemmBK * 2;  // 16 KB
 constexpr int kTileBBytes = kGemmBN * kGemmBK * 2;  // 32 KB
 constexpr int kStageBytes = kTileABytes + kTileBBytes;
-constexpr int kGemmSmem = kGemmStages * kStageBytes + 1024;  // + alignment slack
+constexpr int kEpiBytes = 32 * 32 * 4;  // one epilogue warp's 32 x 32 fp32 block
+constexpr int kGemmSmem = kGemmStages * kStageBytes + 4 * kEpiBytes + 1024;  // + alignment slack
 constexpr uint32_t kTmemCols = 512;
 
 struct GemmParams {
@@ -44,6 +49,7 @@ struct GemmParams {
   float* D;
   long long ldd;  // elements between rows of D
   float beta;     // 0: D = A B^T; 1: D += A B^T
+  int use_tma;    // D written by TMA tensor stores / reduce-adds (rows 16-byte aligned)
   int tiles_m, tiles_n, k_tiles;
   unsigned int* err;
   unsigned int wait_hint_ns;
@@ -69,6 +75,24 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
 // instruction descriptor of kind::f16: D fp32, A and B bf16, both K-major, N=256, M=128
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((kGemmBN >> 3) << 17) |
                             ((kGemmBM >> 4) << 24);
+
+// D blocks leave shared memory by TMA: a tensor store (D = ...) or a tensor
+// reduce-add performed in L2 (D += ...), so the accumulation reads nothing back
+// into the SM.  Elements outside D are clipped by the tensor map.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(src)
+               : "memory");
+}
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, uint32_t src, int x,
+                                                  int y) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(x), "r"(y), "r"(src)
+      : "memory");
+}
 
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                           uint32_t accumulate) {
@@ -109,17 +133,14 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
 
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_bf16_tn_kernel(const __grid_constant__ CUtensorMap tma_a,
-                        const __grid_constant__ CUtensorMap tma_b, const GemmParams p) {
+                        const __grid_constant__ CUtensorMap tma_b,
+                        const __grid_constant__ CUtensorMap tma_d, const GemmParams p) {
   extern __shared__ unsigned char gsm[];
   __shared__ __align__(8) unsigned long long full_bar[kGemmStages];
   __shared__ __align__(8) unsigned long long empty_bar[kGemmStages];
   __shared__ __align__(8) unsigned long long accf_bar[2];
   __shared__ __align__(8) unsigned long long acce_bar[2];
   __shared__ uint32_t tmem_slot;
-  // epilogue staging: each epilogue warp turns its 32 x 32 block around here
-  // (pitch 33 floats: conflict-free in both directions) so that its global
-  // loads and stores cover one 128-byte row segment per instruction
-  __shared__ float stg[4][32][33];
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -216,6 +237,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else {
     // ---------------- epilogue: warps 2..5 ----------------
     const int q = warp & 3;  // the TMEM lane quarter this warp may access
+    // this warp's 32 x 32 fp32 block in shared memory, in the 128-byte swizzled
+    // layout of the D tensor map: row r at 128 r, its 16-byte chunk c at chunk
+    // c ^ (r & 7) (written by lane = row without more than 4-way conflicts,
+    // read by lane = column without any)
+    const uint32_t ebuf = sbase + kGemmStages * kStageBytes + q * kEpiBytes;
     int a = 0;
     uint32_t aph = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
@@ -224,43 +250,69 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_wait<false>(smem_u32(&accf_bar[a]), aph, p.err, failed, WAIT_LIMIT_NS, hint);
       tc_fence_after();
       const int rbase = tm * kGemmBM + 32 * q;  // this warp's 32 rows of the tile
-      float (*sb)[33] = stg[q];
 #pragma unroll 1
       for (int cc = 0; cc < kGemmBN / 32; ++cc) {
         float v[32];
         tmem_ld32(tmem + static_cast<uint32_t>(a * kGemmBN + cc * 32) +
                       (static_cast<uint32_t>(32 * q) << 16),
                   v);
-        // lane = row on the way in, lane = column on the way out
-#pragma unroll
-        for (int j = 0; j < 32; ++j) sb[lane][j] = v[j];
-        __syncwarp();
-        const int col = tn * kGemmBN + cc * 32 + lane;
-        const bool col_ok = col < p.N;
-        float* const dcol = p.D + col;
-        if (p.beta != 0.f) {
-          float old[32];
-#pragma unroll
-          for (int r = 0; r < 32; ++r)
-            old[r] = (col_ok && rbase + r < p.M)
-                         ? dcol[static_cast<long long>(rbase + r) * p.ldd]
-                         : 0.f;
-#pragma unroll
-          for (int r = 0; r < 32; ++r)
-            if (col_ok && rbase + r < p.M)
-              dcol[static_cast<long long>(rbase + r) * p.ldd] = sb[r][lane] + old[r];
-        } else {
-#pragma unroll
-          for (int r = 0; r < 32; ++r)
-            if (col_ok && rbase + r < p.M) dcol[static_cast<long long>(rbase + r) * p.ldd] = sb[r][lane];
+        const int col0 = tn * kGemmBN + cc * 32;
+        if (p.use_tma) {
+          // the previous block's store has read the buffer
+          if (lane == 0) bulk_wait_read<0>();
+          __syncwarp();
         }
-        __syncwarp();  // the block is read out before the next one is written
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(
+                           ebuf + lane * 128 + 16 * (j ^ (lane & 7))),
+                       "f"(v[4 * j]), "f"(v[4 * j + 1]), "f"(v[4 * j + 2]), "f"(v[4 * j + 3])
+                       : "memory");
+        if (p.use_tma) {
+          fence_proxy_async_smem();  // the block is visible to the TMA engine
+          __syncwarp();
+          if (lane == 0) {
+            if (p.beta != 0.f) tma_reduce_add_2d(&tma_d, ebuf, col0, rbase);
+            else tma_store_2d(&tma_d, ebuf, col0, rbase);
+            bulk_commit();
+          }
+        } else {
+          // rows of D off the 16-byte grid: lane = column, one row segment per access
+          __syncwarp();
+          const int col = col0 + lane;
+          const bool col_ok = col < p.N;
+          float* const dcol = p.D + col;
+          const uint32_t rd = ebuf + 16 * (lane >> 2) + 4 * (lane & 3);
+          float val[32];
+#pragma unroll
+          for (int r = 0; r < 32; ++r) {
+            asm volatile("ld.shared.f32 %0, [%1];"
+                         : "=f"(val[r])
+                         : "r"((rd + r * 128) ^ (static_cast<uint32_t>(r & 7) << 4)));
+          }
+          if (p.beta != 0.f) {
+            float old[32];
+#pragma unroll
+            for (int r = 0; r < 32; ++r)
+              old[r] = (col_ok && rbase + r < p.M)
+                           ? dcol[static_cast<long long>(rbase + r) * p.ldd]
+                           : 0.f;
+#pragma unroll
+            for (int r = 0; r < 32; ++r) val[r] += old[r];
+          }
+#pragma unroll
+          for (int r = 0; r < 32; ++r)
+            if (col_ok && rbase + r < p.M) dcol[static_cast<long long>(rbase + r) * p.ldd] = val[r];
+          __syncwarp();  // the block is read out before the next one is written
+        }
       }
       tc_fence_before();
       mbar_arrive(smem_u32(&acce_bar[a]));
       a ^= 1;
       if (a == 0) aph ^= 1u;
     }
+    // no CTA exits while a TMA store still reads its shared memory
+    if (p.use_tma && lane == 0) bulk_wait_all();
   }
 
   tc_fence_before();
@@ -302,6 +354,21 @@ static bool make_map(CUtensorMap* map, const void* base, long long rows, long lo
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D fp32 tensor map over D (rows x cols, row stride ld elements, a multiple
+// of 4) with a box of 32 x 32 and 128-byte swizzle: the epilogue's blocks
+static bool make_map_f32(CUtensorMap* map, void* base, long long rows, long long cols,
+                         long long ld) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 4};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // D[M,N] = A[M,K] B[N,K]^T (+ beta D); bf16 inputs with K contiguous, fp32 D.
 // Requires K, lda, ldb multiples of 8 and 16-byte aligned A and B.
 ce_status gemm_bf16_tn(const void* A, long long lda, const void* B, long long ldb, float* D,
@@ -311,9 +378,13 @@ ce_status gemm_bf16_tn(const void* A, long long lda, const void* B, long long ld
   if ((K % 8) || (lda % 8) || (ldb % 8) || lda < K || ldb < K || ldd < N) return CE_ERR_UNSUPPORTED;
   if ((reinterpret_cast<uintptr_t>(A) & 15) || (reinterpret_cast<uintptr_t>(B) & 15))
     return CE_ERR_UNSUPPORTED;
-  CUtensorMap ma, mb;
+  CUtensorMap ma, mb, md;
   if (!make_map(&ma, A, M, K, lda, kGemmBM) || !make_map(&mb, B, N, K, ldb, kGemmBN))
     return CE_ERR_CUDA;
+  // D by TMA when its rows sit on the 16-byte grid (the tensor map's stride rule)
+  const bool use_tma = (ldd % 4 == 0) && ((reinterpret_cast<uintptr_t>(D) & 15) == 0);
+  std::memset(&md, 0, sizeof(md));
+  if (use_tma && !make_map_f32(&md, D, M, N, ldd)) return CE_ERR_CUDA;
   GemmParams p;
   p.M = M;
   p.N = N;
@@ -321,6 +392,7 @@ ce_status gemm_bf16_tn(const void* A, long long lda, const void* B, long long ld
   p.D = D;
   p.ldd = ldd;
   p.beta = beta;
+  p.use_tma = use_tma ? 1 : 0;
   p.tiles_m = (M + kGemmBM - 1) / kGemmBM;
   p.tiles_n = (N + kGemmBN - 1) / kGemmBN;
   p.k_tiles = (K + kGemmBK - 1) / kGemmBK;
@@ -331,7 +403,7 @@ ce_status gemm_bf16_tn(const void* A, long long lda, const void* B, long long ld
     return CE_ERR_CUDA;
   const int tiles = p.tiles_m * p.tiles_n;
   const int grid = tiles < sm_count ? tiles : sm_count;
-  gemm_bf16_tn_kernel<<<grid, kGemmThreads, kGemmSmem, stream>>>(ma, mb, p);
+  gemm_bf16_tn_kernel<<<grid, kGemmThreads, kGemmSmem, stream>>>(ma, mb, md, p);
   return cudaGetLastError() == cudaSuccess ? CE_OK : CE_ERR_CUDA;
 }
 
