@@ -51,6 +51,7 @@ struct GemmParams {
   float beta;     // 0: D = A B^T; 1: D += A B^T
   int use_tma;    // D written by TMA tensor stores / reduce-adds (rows 16-byte aligned)
   int tiles_m, tiles_n, k_tiles;
+  int n_fast;     // tile order: 1 = N varies fastest (A the larger operand), 0 = M
   unsigned int* err;
   unsigned int wait_hint_ns;
 };
@@ -92,6 +93,19 @@ __device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, uint32
           reinterpret_cast<uint64_t>(map)),
       "r"(x), "r"(y), "r"(src)
       : "memory");
+}
+
+// Tile order of the persistent grid: the CTAs running at the same time share
+// the tiles of the smaller operand through L2 while the larger operand streams
+// from HBM once (M fastest when B is the larger, N fastest when A is).
+__device__ __forceinline__ void tile_coords(const GemmParams& p, int tile, int& tm, int& tn) {
+  if (p.n_fast) {
+    tn = tile % p.tiles_n;
+    tm = tile / p.tiles_n;
+  } else {
+    tm = tile % p.tiles_m;
+    tn = tile / p.tiles_m;
+  }
 }
 
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
@@ -179,8 +193,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t ph = 0;
       uint32_t filled = 0;  // stages that received at least one load
       for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-        const int tm = tile % p.tiles_m;
-        const int tn = tile / p.tiles_m;
+        int tm, tn;
+        tile_coords(p, tile, tm, tn);
         for (int kt = 0; kt < p.k_tiles; ++kt) {
           mbar_wait<false>(smem_u32(&empty_bar[s]), ph ^ 1u, p.err, failed, WAIT_LIMIT_NS, hint);
           const uint32_t fb = smem_u32(&full_bar[s]);
@@ -245,8 +259,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     int a = 0;
     uint32_t aph = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-      const int tm = tile % p.tiles_m;
-      const int tn = tile / p.tiles_m;
+      int tm, tn;
+      tile_coords(p, tile, tm, tn);
       mbar_wait<false>(smem_u32(&accf_bar[a]), aph, p.err, failed, WAIT_LIMIT_NS, hint);
       tc_fence_after();
       const int rbase = tm * kGemmBM + 32 * q;  // this warp's 32 rows of the tile
@@ -396,6 +410,7 @@ ce_status gemm_bf16_tn(const void* A, long long lda, const void* B, long long ld
   p.tiles_m = (M + kGemmBM - 1) / kGemmBM;
   p.tiles_n = (N + kGemmBN - 1) / kGemmBN;
   p.k_tiles = (K + kGemmBK - 1) / kGemmBK;
+  p.n_fast = M > N ? 1 : 0;  // A [M, K] the larger operand
   p.err = err;
   p.wait_hint_ns = wait_hint_ns;
   if (cudaFuncSetAttribute(gemm_bf16_tn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
