@@ -431,7 +431,9 @@ constexpr int kTT = 64;       // tile edge
 constexpr int kTP = kTT + 8;  // padded pitch (bf16) of the shared tile
 
 // T[c, r] = X[r, c] for bf16, r < R, c < C (zero in the padding columns r >= R up
-// to ldt); 64x64 tiles with 16-byte loads and stores (ldx, ldt multiples of 8)
+// to ldt); 64x64 tiles with 16-byte loads and stores (ldx, ldt multiples of 8),
+// the shared tile XOR-swizzled by 16-byte chunk so that neither direction has
+// bank conflicts
 __global__ void __launch_bounds__(256) transpose_bf16_kernel(const __nv_bfloat16* __restrict__ X,
                                                              int R, int C, long long ldx,
                                                              __nv_bfloat16* __restrict__ T,
@@ -458,7 +460,9 @@ __global__ void __launch_bounds__(256) transpose_bf16_kernel(const __nv_bfloat16
           v = *reinterpret_cast<uint4*>(e);
         }
       }
-      *reinterpret_cast<uint4*>(&tile[rr][cq]) = v;
+      // 16-byte chunk (cq / 8) of row rr at chunk (cq / 8) ^ (rr / 8 % 8): the
+      // column reads below then spread over all banks
+      *reinterpret_cast<uint4*>(&tile[rr][8 * ((cq >> 3) ^ ((rr >> 3) & 7))]) = v;
     }
     __syncthreads();
 #pragma unroll
@@ -471,8 +475,9 @@ __global__ void __launch_bounds__(256) transpose_bf16_kernel(const __nv_bfloat16
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           __nv_bfloat162 pr;
-          pr.x = tile[rg + 2 * j][cc];
-          pr.y = tile[rg + 2 * j + 1][cc];
+          const int sw = 8 * ((cc >> 3) ^ ((rg >> 3) & 7)) + (cc & 7);  // rows rg..rg+7 share rg / 8
+          pr.x = tile[rg + 2 * j][sw];
+          pr.y = tile[rg + 2 * j + 1][sw];
           w[j] = *reinterpret_cast<uint32_t*>(&pr);
         }
         *reinterpret_cast<uint4*>(T + c * ldt + r) = make_uint4(w[0], w[1], w[2], w[3]);
