@@ -645,16 +645,22 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
       auto smem_ptr = [&](int byte_off) -> char* {
         return static_cast<char*>(__cvta_shared_to_generic(sbase + byte_off));
       };
-      // values of an edge chunk, -inf outside the row
+      // values of an edge chunk, -inf outside the row: one 16-byte shared load
+      // when the chunk is in the stage (the partial head/tail chunks normally
+      // are), element loads from memory otherwise
       auto edge_load = [&](int c, float* v) {
         const int e0 = (d0 + 16 * c) >> LOG_ES;
-        const bool in_smem = in_stage(c);
+        if (in_stage(c)) {
+          E::unpack(lds128(sbase + 16 * c), v);
 #pragma unroll
-        for (int q = 0; q < EPC; ++q) {
-          const int e = e0 + q;
-          v[q] = (e >= 0 && e < V)
-                     ? (in_smem ? E::ld(smem_ptr(16 * c + q * ES)) : E::ld(elem_ptr_global(e)))
-                     : -INFINITY;
+          for (int q = 0; q < EPC; ++q)
+            if (!(e0 + q >= 0 && e0 + q < V)) v[q] = -INFINITY;
+        } else {
+#pragma unroll
+          for (int q = 0; q < EPC; ++q) {
+            const int e = e0 + q;
+            v[q] = (e >= 0 && e < V) ? E::ld(elem_ptr_global(e)) : -INFINITY;
+          }
         }
       };
       auto edge_store = [&](int c, const float* gv) {

@@ -344,18 +344,22 @@ __global__ void __launch_bounds__(kStreamMaxWarps * 32, 1) ce_stream_kernel(cons
     bool have_xt = false;
 
     // element e of the row, -inf outside it; from the slot when TMA loaded it
+    // (one 16-byte shared load), element loads from memory otherwise
     auto edge_vals = [&](int c, int c0, uint32_t sbase, float* v) {
       const int e0 = (g.hb - 16 + 16 * c) >> LOG_ES;
-      const bool in_smem = c >= g.ld_lo && c < g.ld_hi;
+      if (c >= g.ld_lo && c < g.ld_hi) {
+        E::unpack(lds128(sbase + 16 * (c - c0)), v);
 #pragma unroll
-      for (int q = 0; q < EPC; ++q) {
-        const int e = e0 + q;
-        float x = -INFINITY;
-        if (e >= 0 && e < V) {
-          x = in_smem ? E::ld(static_cast<char*>(__cvta_shared_to_generic(sbase + 16 * (c - c0) + q * ES)))
-                      : E::ld(reinterpret_cast<const char*>(g.as) + static_cast<long long>(e) * ES);
+        for (int q = 0; q < EPC; ++q)
+          if (!(e0 + q >= 0 && e0 + q < V)) v[q] = -INFINITY;
+      } else {
+#pragma unroll
+        for (int q = 0; q < EPC; ++q) {
+          const int e = e0 + q;
+          v[q] = (e >= 0 && e < V)
+                     ? E::ld(reinterpret_cast<const char*>(g.as) + static_cast<long long>(e) * ES)
+                     : -INFINITY;
         }
-        v[q] = x;
       }
     };
 
