@@ -129,6 +129,17 @@ def test_unit_kernel_in_every_mode(dtype, V, monkeypatch):
     check_case(x, t, dtype)
 
 
+@pytest.mark.parametrize("dtype,V", [("f32", 9000), ("f32", 13000), ("bf16", 25013),
+                                     ("f16", 27001), ("bf16", 16387), ("f32", 8193)])
+def test_two_rows_per_unit_mid_rows(dtype, V):
+    # rows of 32-54 KB in the writing modes run two rows per unit when there are
+    # enough rows (M >= 2 x SMs): both rows of a unit, aligned or not
+    M = 400
+    x = synthetic.make_logits(M, V, dtype, 2.0, seed=V + 11)
+    t = synthetic.make_targets(M, V, seed=V + 12)
+    check_case(x, t, dtype, rows=P.sample_rows(M, 160))
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("M", [1, 2, 3, 5, 151, 152, 153, 1000, 4099])
 def test_sweep_rows(dtype, M):
