@@ -141,6 +141,24 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def max_over_ranks(x: float, device) -> float:
+    """The slowest rank's value of x (the step time of a replica run): an
+    all-reduce of one scalar, on `device` (CUDA under NCCL, CPU under gloo)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_gbs(world_size: int, bytes_per_step: int, ms_per_step: float) -> float:
+    """Whole-job throughput of N replicas: every rank moves bytes_per_step per
+    step and the step takes the slowest rank's ms_per_step."""
+    return world_size * bytes_per_step / (ms_per_step * 1e-3) / 1e9
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -294,15 +312,12 @@ def run_native(args, w):
     clocks = sampler.stop() if sampler else None
     region_ms = region0.elapsed_time(region1)
     kernel_ms = [a.elapsed_time(b) for a, b in ev]
-    if ws > 1:
-        tt = torch.tensor([region_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        region_ms = float(tt.item())
+    region_ms = max_over_ranks(region_ms, dev)
     assert api.ce_check_errors() == 0
 
     ms_per_step = region_ms / args.steps
     b_step = algorithmic_bytes(M, V, es, True)
-    value = ws * b_step / (ms_per_step * 1e-3) / 1e9
+    value = aggregate_gbs(ws, b_step, ms_per_step)
     avg_kernel_ms = sum(kernel_ms) / len(kernel_ms)
     peak, peak_kind = measured_peaks()
     achieved = b_step / (avg_kernel_ms * 1e-3) / 1e9
@@ -349,11 +364,8 @@ def run_native(args, w):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if ws > 1:
-        tt = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
-    e2e_value = ws * b_step / (e2e_ms * 1e-3) / 1e9
+    e2e_ms = max_over_ranks(e2e_ms, dev)
+    e2e_value = aggregate_gbs(ws, b_step, e2e_ms)
 
     if rank == 0:
         line = {

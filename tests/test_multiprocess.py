@@ -1,0 +1,74 @@
+"""The multi-GPU path without GPUs: world-size-2 process groups on CPU (gloo).
+
+The row operations shard over rows with no data exchange, so several GPUs run
+independent replicas ("replicas only"): the only cross-rank steps are the
+barrier and the max over ranks of the step time, and `value` is the whole-job
+throughput.  These run here on the gloo backend; the reference arm under
+torchrun prints from rank 0 alone."""
+
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+
+torch = pytest.importorskip("torch")
+
+from tests.conftest import ROOT  # noqa: E402
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out_dir):
+    import torch.distributed as dist
+    sys.path.insert(0, ROOT)
+    import bench
+    dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank,
+                            world_size=world)
+    # each replica's step time differs; every rank must see the slowest
+    ms = bench.max_over_ranks(1.0 + rank * 0.5, "cpu")
+    dist.barrier()
+    with open(os.path.join(out_dir, f"rank{rank}.json"), "w") as fh:
+        json.dump({"ms": ms, "gbs": bench.aggregate_gbs(world, 10**9, ms)}, fh)
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_and_aggregate_gloo(tmp_path):
+    import torch.multiprocessing as mp
+    world, port = 2, _free_port()
+    mp.start_processes(_rank_main, args=(world, port, str(tmp_path)), nprocs=world,
+                       join=True, start_method="spawn")
+    got = [json.load(open(tmp_path / f"rank{r}.json")) for r in range(world)]
+    for g in got:
+        assert g["ms"] == 1.5  # the slower rank's time on every rank
+        # two replicas of 1 GB each in 1.5 ms
+        assert abs(g["gbs"] - 2 * 1e9 / 1.5e-3 / 1e9) < 1e-9
+
+
+def test_single_process_needs_no_group():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.max_over_ranks(3.25, "cpu") == 3.25
+    assert bench.aggregate_gbs(1, 2 * 10**9, 2.0) == 1000.0
+
+
+def test_reference_arm_under_torchrun_prints_from_rank_zero_only():
+    port = _free_port()
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), "bench.py",
+           "--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "3",
+           "--ref-rows", "16", "--workload", "small_f32_256x1024"]
+    r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2
+    assert d["cpu_baseline"]["kind"] == "oracle"
+    assert d["e2e"]["h2d_bytes_per_step"] == 0
