@@ -178,7 +178,11 @@ long long chunks_for(long long bytes, bool aligned) {
 long long stage_bytes_for(int variant, int R, int CL, long long rb, bool aligned) {
   const int NC = ce::kVariants[variant].NC;
   const int CPT = ce::kVariants[variant].CPT;
-  if (R < 1 || NC % R != 0 || (NC / R) % 32 != 0) return 0;
+  // a row group is a power of two of at least kMinGroupThreads threads: a
+  // quarter warp, half a warp, or whole warps
+  if (R < 1 || NC % R != 0) return 0;
+  const int GT = NC / R;
+  if (GT < ce::kMinGroupThreads || (GT & (GT - 1)) != 0) return 0;
   if (CL < 1 || CL > ce::kMaxCluster || (CL > 1 && R != 1)) return 0;
   const long long cpr = chunks_for(rb, aligned);
   if (CL == 1) {
@@ -213,7 +217,9 @@ bool choose_plan(int mode, long long rb, bool aligned, long long M, int sm_count
     const int NC = ce::kVariants[variant].NC;
     const long long budget = fwd ? 64 * 1024 : 128 * 1024;  // stage bytes per CTA
     int R = 1;
-    while (R * 2 <= NC / 32 && static_cast<long long>(R) * 2 * rb <= 64 * 1024) R *= 2;
+    // short rows share a warp: as few as kMinGroupThreads threads per row
+    while (R * 2 <= NC / ce::kMinGroupThreads && static_cast<long long>(R) * 2 * rb <= 64 * 1024)
+      R *= 2;
     const long long min_units = (fwd ? 3LL : 1LL) * sm_count;
     while (R > 1 && (M + R - 1) / R < min_units) R /= 2;
     for (; R >= 1; R /= 2) {

@@ -63,6 +63,10 @@ enum Mode : int { FWD = 0, FWD_BWD = 1, BWD = 2, SOFTMAX = 3 };
 
 constexpr int kMaxStages = 16;
 constexpr int kMaxCluster = 8;
+// row groups of a CTA: a row takes GT = NC / R threads, at least 8 (a quarter
+// warp: short rows put several rows in one warp)
+constexpr int kMinGroupThreads = 8;
+constexpr int kMaxRowGroups = 512 / kMinGroupThreads;
 
 // The instantiated consumer shapes (NC consumer threads, CPT register-resident
 // 16-byte chunks per thread; CPT == 0 re-reads shared memory instead).
@@ -438,7 +442,7 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
   __shared__ __align__(16) float4 xslot[2][kMaxCluster];
   __shared__ float2 red[2][NW];
   __shared__ float xt_slot[2][NW];
-  __shared__ double acc_slot[NW];
+  __shared__ double acc_slot[kMaxRowGroups];
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -565,7 +569,7 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
     constexpr int KR = RESIDENT ? CPT : 1;
     const int R = p.R;
     const int GT = NC / R;     // threads per row group
-    const int GW = GT / 32;    // warps per row group
+    const int GW = GT / 32;    // warps per row group (0: several rows in a warp)
     const int grp = tid >> p.log_gt;  // row of the unit this thread works on
     const int gt = tid & (GT - 1);
     const int V = static_cast<int>(p.V);          // the host caps V * sizeof(T) far below 2^31
@@ -817,13 +821,26 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
       // ---- merge (m, s): warp, then the row's warps ----
       // (st carries the factor 2^ml; it is removed in the same exp2 that
       // rescales the thread's sum to the warp max)
-      const float mw = warp_max(mt);
-      float sw = (mt == -INFINITY) ? 0.f : st * ex2((mt - mw) * kLog2e - ml);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) sw += __shfl_down_sync(0xffffffffu, sw, o);
       const bool have_t = t_ok && tc >= g.w0 && tc < g.w1;  // this CTA holds x[row, t]
       float Mg, Sg, xrow = 0.f;
-      if (GW == 1) {
+      if (GW == 0) {
+        // GT lanes per row, groups aligned to GT lanes: butterflies over lane
+        // distances below GT stay inside the row's group
+        float mg = mt;
+        for (int o = GT >> 1; o > 0; o >>= 1) mg = fmaxf(mg, __shfl_xor_sync(0xffffffffu, mg, o));
+        float sg = (mt == -INFINITY) ? 0.f : st * ex2((mt - mg) * kLog2e - ml);
+        for (int o = GT >> 1; o > 0; o >>= 1) sg += __shfl_xor_sync(0xffffffffu, sg, o);
+        Mg = mg;
+        Sg = sg;
+        const unsigned gmask = ((GT == 32) ? 0xffffffffu : ((1u << GT) - 1u)) << (lane & ~(GT - 1));
+        const unsigned own = __ballot_sync(0xffffffffu, owner) & gmask;
+        const float xo = __shfl_sync(0xffffffffu, xt, own ? __ffs(own) - 1 : lane);
+        if (have_t && own != 0u) xrow = xo;
+      } else if (GW == 1) {
+        const float mw = warp_max(mt);
+        float sw = (mt == -INFINITY) ? 0.f : st * ex2((mt - mw) * kLog2e - ml);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sw += __shfl_down_sync(0xffffffffu, sw, o);
         // a row handled by one warp: the warp's pair is the row's pair, and the
         // target logit comes from the owner lane, with no shared memory or barrier
         Mg = mw;
@@ -831,6 +848,10 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
         const unsigned own = __ballot_sync(0xffffffffu, owner);
         if (have_t && own != 0u) xrow = __shfl_sync(0xffffffffu, xt, __ffs(own) - 1);
       } else {
+        const float mw = warp_max(mt);
+        float sw = (mt == -INFINITY) ? 0.f : st * ex2((mt - mw) * kLog2e - ml);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sw += __shfl_down_sync(0xffffffffu, sw, o);
         if (lane == 0) red[b][warp] = make_float2(mw, sw);
         if (owner) xt_slot[b][grp] = xt;
         if (R == 1) consumer_sync(NC);

@@ -117,6 +117,23 @@ def test_sweep_vocab(dtype, V):
     check_case(x, t, dtype)
 
 
+@pytest.mark.parametrize("plan,dtype,V", [("3,32,1,2", "f32", 256), ("4,64,1,2", "bf16", 100),
+                                          ("3,16,1,3", "f16", 999), ("4,32,1,2", "f32", 31)])
+def test_sub_warp_row_groups_many_units(plan, dtype, V, monkeypatch):
+    # 8 or 16 threads per row, many units per CTA and a ragged last unit
+    monkeypatch.setenv("CE_KERNEL", "unit")
+    monkeypatch.setenv("CE_PLAN", plan)
+    M = 5003
+    x = synthetic.make_logits(M, V, dtype, 3.0, seed=V + 21)
+    t = synthetic.make_targets(M, V, seed=V + 22)
+    t[17] = V  # one target out of range in the middle of a warp's rows
+    a = api()
+    assert a.ce_check_errors() == 0
+    rows = np.unique(np.concatenate([P.sample_rows(M, 400), [16, 17, 18]]))
+    check_case(x, t, dtype, "sum", rows=rows)
+    assert a.ce_check_errors() == a.CE_ERR_TARGET_RANGE
+
+
 @pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
 @pytest.mark.parametrize("V", [1, 7, 129, 4097, 50257, 131072, 300007])
 def test_unit_kernel_in_every_mode(dtype, V, monkeypatch):
@@ -283,6 +300,9 @@ def test_side_stream():
     ("0,1,8,3", "f16", 131072), ("0,1,4,4", "bf16", 50257), ("1,1,8,2", "f32", 30000),
     ("1,16,1,6", "f32", 100), ("2,1,1,4", "f32", 4096), ("2,1,6,2", "bf16", 50257),
     ("4,4,1,3", "f16", 1000), ("4,1,2,2", "f32", 65539), ("3,8,1,2", "bf16", 7),
+    # several rows in one warp: 16 or 8 threads per row
+    ("3,16,1,2", "f32", 1000), ("3,32,1,2", "bf16", 333), ("4,64,1,2", "f16", 100),
+    ("0,32,1,2", "f32", 200), ("1,32,1,3", "bf16", 500), ("2,16,1,4", "f16", 77),
 ])
 def test_other_launch_shapes(plan, dtype, V, monkeypatch):
     monkeypatch.setenv("CE_KERNEL", "unit")  # the unit kernel in every mode
