@@ -212,7 +212,9 @@ long long stage_bytes_for(int variant, int R, int CL, long long rb, bool aligned
 bool choose_plan(int mode, long long rb, bool aligned, long long M, int sm_count, Plan& pl) {
   const long long cpr = chunks_for(rb, aligned);
   if (cpr * 16 <= 32 * 1024) {
-    const bool fwd = mode == ce::FWD;
+    // rows of up to 2 KB take the writing modes' shape in the forward too
+    // (512 threads, 8-16 per row: 59% against 50% for fp32 V = 256)
+    const bool fwd = mode == ce::FWD && rb > 2048;
     const int variant = fwd ? 3 : 4;
     const int NC = ce::kVariants[variant].NC;
     const long long budget = fwd ? 64 * 1024 : 128 * 1024;  // stage bytes per CTA
@@ -507,13 +509,15 @@ ce_status launch_stream(int mode, const void* logits, const int64_t* targets, co
 }
 
 // Which row kernel runs a call (from sweeps on GB300): the streaming kernel
-// for the forward at every row length (1.1x to 2.3x the unit kernel) and for
+// for the forward on rows above 2 KB (1.1x to 2.3x the unit kernel) and for
 // the writing modes once a row no longer fits one CTA's shared memory twice
 // (where the unit kernel would split it over a cluster); the unit kernel for
 // the writing modes on shorter rows, where its single read of each row
 // (against the streaming kernel's read and L2 re-read) wins.
 bool default_use_stream(int mode, long long rb, bool aligned) {
-  if (mode == ce::FWD) return true;
+  // the forward: the unit kernel's sub-warp row groups for rows of up to 2 KB
+  // (fp32 V = 256: 59% against the streaming kernel's 20%), streaming above
+  if (mode == ce::FWD) return rb > 2048;
   const long long cpr = chunks_for(rb, aligned);
   return 2 * cpr * 16 > 216 * 1024;
 }
