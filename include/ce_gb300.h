@@ -161,9 +161,10 @@ ce_status ce_backward_from_lse(void* logits, const int64_t* targets, const float
  *     dW   = G^T h        [V, H]
  *
  * Rows are processed in chunks: each chunk's logits are produced by a
- * tcgen05 GEMM into the workspace, turned into G in place by the row
- * kernel, and contracted into dH and dW (accumulated over chunks) by two
- * more tcgen05 GEMMs with bf16 operands and fp32 accumulation.
+ * tcgen05 GEMM into the workspace, turned by the row kernel into the bf16
+ * gradient rows G (never written in fp32), and contracted into dH and dW
+ * (accumulated over chunks) by two more tcgen05 GEMMs that read W, G and h in
+ * their stored layouts, with fp32 accumulation.
  *
  *   h        [M, H] bf16, row-major; W [V, H] bf16, row-major (device).
  *            H must be a multiple of 8; h and W 16-byte aligned.
@@ -183,12 +184,25 @@ ce_status linear_ce_fwd_bwd(const void* h, const void* W, const int64_t* targets
 size_t linear_ce_workspace_size(int64_t M, int64_t H, int64_t V);
 
 /*
- * ce_gemm_bf16_tn -- the tensor-core contraction under linear_ce_fwd_bwd,
- * exposed on its own: D[M, N] = A[M, K] B[N, K]^T (beta = 0) or
- * D += A B^T (beta = 1), A and B bf16 with K contiguous (row strides lda,
- * ldb elements, multiples of 8, bases 16-byte aligned), D fp32 with row
- * stride ldd.  A persistent tcgen05 kernel: TMA into shared memory, MMAs
- * into TMEM accumulators, fp32 epilogue.
+ * ce_gemm_bf16 -- the tensor-core contraction under linear_ce_fwd_bwd, exposed
+ * on its own: D[M, N] = sum_k A(m, k) B(n, k) (beta = 0) or D += ... (beta = 1)
+ * in fp32, A and B bf16.  a_mn = 0: A is [M, lda] with K contiguous,
+ * A(m, k) = A[m * lda + k]; a_mn = 1: A is stored transposed, [K, lda] with M
+ * contiguous, A(m, k) = A[k * lda + m].  The same for B with N (b_mn).  Row
+ * strides lda, ldb in elements, multiples of 8; A and B 16-byte aligned; D
+ * fp32 with row stride ldd >= N.  A persistent tcgen05 kernel: TMA into shared
+ * memory, MMAs into TMEM accumulators, an epilogue through shared memory and
+ * TMA tensor stores (or tensor reduce-adds for beta = 1).  Errors: null
+ * pointers, a_mn / b_mn outside {0, 1}, beta outside {0, 1} ->
+ * CE_ERR_INVALID_ARG; bad strides or alignment -> CE_ERR_UNSUPPORTED.
+ */
+ce_status ce_gemm_bf16(const void* A, int64_t lda, int a_mn, const void* B, int64_t ldb,
+                       int b_mn, float* D, int64_t ldd, int64_t M, int64_t N, int64_t K,
+                       float beta, void* stream);
+
+/*
+ * ce_gemm_bf16_tn -- ce_gemm_bf16 with both operands K-major:
+ * D[M, N] = A[M, K] B[N, K]^T (beta = 0) or D += A B^T (beta = 1).
  */
 ce_status ce_gemm_bf16_tn(const void* A, int64_t lda, const void* B, int64_t ldb, float* D,
                           int64_t ldd, int64_t M, int64_t N, int64_t K, float beta,

@@ -38,6 +38,8 @@ SIGNATURES = {
                                  ctypes.c_size_t, _vp]),
     "linear_ce_workspace_size": (ctypes.c_size_t, [_i64, _i64, _i64]),
     "ce_gemm_bf16_tn": (_i32, [_vp, _i64, _vp, _i64, _vp, _i64, _i64, _i64, _i64, _f32, _vp]),
+    "ce_gemm_bf16": (_i32, [_vp, _i64, _i32, _vp, _i64, _i32, _vp, _i64, _i64, _i64, _i64, _f32,
+                            _vp]),
     "ce_check_errors": (_i32, [_vp, _i32]),
     "ce_status_string": (ctypes.c_char_p, [_i32]),
     "ce_max_vocab": (_i64, [_i32]),
@@ -221,6 +223,29 @@ def ce_gemm_bf16_tn(A: torch.Tensor, B: torch.Tensor, D: torch.Tensor | None = N
                                D.data_ptr(), D.stride(0), M, N, K, float(beta),
                                _stream_handle(stream, A.device))
     _check(st, "ce_gemm_bf16_tn")
+    return D
+
+
+def ce_gemm_bf16(A: torch.Tensor, B: torch.Tensor, D: torch.Tensor | None = None,
+                 beta: float = 0.0, *, a_mn: bool = False, b_mn: bool = False,
+                 stream=None) -> torch.Tensor:
+    """D[M, N] = sum_k A(m, k) B(n, k) (beta 0) or D += ... (beta 1), fp32.
+    A is [M, K] (a_mn False) or its transpose stored [K, M] (a_mn True); B is
+    [N, K] (b_mn False) or stored [K, N] (b_mn True); both bf16, rows contiguous."""
+    if A.dtype != torch.bfloat16 or B.dtype != torch.bfloat16 or A.dim() != 2 or B.dim() != 2:
+        raise ValueError("A and B must be 2-D bf16 tensors")
+    if A.stride(1) != 1 or B.stride(1) != 1:
+        raise ValueError("A and B must have contiguous rows")
+    K, M = A.shape if a_mn else (A.shape[1], A.shape[0])
+    Kb, N = B.shape if b_mn else (B.shape[1], B.shape[0])
+    if Kb != K:
+        raise ValueError("A and B must share K")
+    if D is None:
+        D = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    st = lib().ce_gemm_bf16(A.data_ptr(), A.stride(0), int(a_mn), B.data_ptr(), B.stride(0),
+                            int(b_mn), D.data_ptr(), D.stride(0), M, N, K, float(beta),
+                            _stream_handle(stream, A.device))
+    _check(st, "ce_gemm_bf16")
     return D
 
 

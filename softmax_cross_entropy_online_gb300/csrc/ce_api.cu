@@ -32,11 +32,10 @@ cudaError_t stream_launch(int mode, bool resident, const StreamParams& p, int gr
 template <typename T>
 cudaError_t stream_max_active(int mode, bool resident, int nwarps, int smem_bytes, int* per_sm);
 constexpr int kStreamKRes = 16;  // as in ce_launch.cuh
-ce_status gemm_bf16_tn(const void* A, long long lda, const void* B, long long ldb, float* D,
-                       long long ldd, int M, int N, int K, float beta, cudaStream_t stream,
-                       unsigned int* err, int sm_count, unsigned int wait_hint_ns);
-ce_status launch_transpose_bf16(const void* X, int R, int C, long long ldx, void* T,
-                                long long ldt, cudaStream_t st, int sm_count);
+ce_status gemm_bf16(const void* A, long long lda, bool a_mn, const void* B, long long ldb,
+                    bool b_mn, float* D, long long ldd, int M, int N, int K, float beta,
+                    cudaStream_t stream, unsigned int* err, int sm_count,
+                    unsigned int wait_hint_ns);
 ce_status launch_mean_rows(const float* rl, long long M, float* loss, cudaStream_t st);
 }  // namespace ce
 
@@ -650,28 +649,22 @@ ce_status launch_rows(int mode, const void* logits, const int64_t* targets, cons
 }
 
 // Workspace of the fused linear + cross-entropy for row chunks of `mc` rows:
-// Wt [H, ldv] bf16, logits [mc, V] fp32, G16 [mc, ldv] bf16, Gt16 [V, ldk]
-// bf16, ht [H, ldk] bf16, row losses [M] fp32 (ldv = V and ldk = mc rounded up
-// to a multiple of 8, padded with zeros).
+// logits [mc, V] fp32, G16 [mc, ldv] bf16 (ldv = V rounded up to a multiple of
+// 8), row losses [M] fp32.  The GEMMs read W, G16 and h in their stored
+// layouts (MN-major operands where K is not contiguous), so nothing is
+// transposed.
 struct LinearWs {
-  size_t wt, logits, g16, gt16, ht, rl, total;
+  size_t logits, g16, rl, total;
 };
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
-LinearWs linear_ws_layout(long long M, long long H, long long V, long long mc) {
+LinearWs linear_ws_layout(long long M, long long V, long long mc) {
   const long long ldv = (V + 7) / 8 * 8;
-  const long long ldk = (mc + 7) / 8 * 8;
   LinearWs w;
   size_t off = 0;
-  w.wt = off;
-  off += round256(static_cast<size_t>(H) * ldv * 2);
   w.logits = off;
   off += round256(static_cast<size_t>(mc) * V * 4);
   w.g16 = off;
   off += round256(static_cast<size_t>(mc) * ldv * 2);
-  w.gt16 = off;
-  off += round256(static_cast<size_t>(V) * ldk * 2);
-  w.ht = off;
-  off += round256(static_cast<size_t>(H) * ldk * 2);
   w.rl = off;
   off += round256(static_cast<size_t>(M) * 4);
   w.total = off;
@@ -728,11 +721,12 @@ ce_status ce_backward_from_lse(void* logits, const int64_t* targets, const float
                      nullptr, scale, stream);
 }
 
-ce_status ce_gemm_bf16_tn(const void* A, int64_t lda, const void* B, int64_t ldb, float* D,
-                          int64_t ldd, int64_t M, int64_t N, int64_t K, float beta,
-                          void* stream) {
+ce_status ce_gemm_bf16(const void* A, int64_t lda, int a_mn, const void* B, int64_t ldb,
+                       int b_mn, float* D, int64_t ldd, int64_t M, int64_t N, int64_t K,
+                       float beta, void* stream) {
   if (M < 0 || N < 0 || K < 0 || (M > 0 && N > 0 && (A == nullptr || B == nullptr || D == nullptr)))
     return CE_ERR_INVALID_ARG;
+  if ((a_mn != 0 && a_mn != 1) || (b_mn != 0 && b_mn != 1)) return CE_ERR_INVALID_ARG;
   if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return CE_ERR_UNSUPPORTED;
   if (beta != 0.f && beta != 1.f) return CE_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(D) % 4) return CE_ERR_INVALID_ARG;
@@ -740,17 +734,24 @@ ce_status ce_gemm_bf16_tn(const void* A, int64_t lda, const void* B, int64_t ldb
   int dev = 0;
   ce_status st = device_info(di, &dev);
   if (st != CE_OK) return st;
-  st = ce::gemm_bf16_tn(A, lda, B, ldb, D, ldd, static_cast<int>(M), static_cast<int>(N),
-                        static_cast<int>(K), beta, static_cast<cudaStream_t>(stream), di.err,
-                        di.sm_count, wait_hint_ns());
+  st = ce::gemm_bf16(A, lda, a_mn != 0, B, ldb, b_mn != 0, D, ldd, static_cast<int>(M),
+                     static_cast<int>(N), static_cast<int>(K), beta,
+                     static_cast<cudaStream_t>(stream), di.err, di.sm_count, wait_hint_ns());
   if (st == CE_OK) g_launches.fetch_add(1, std::memory_order_relaxed);
   return st;
+}
+
+ce_status ce_gemm_bf16_tn(const void* A, int64_t lda, const void* B, int64_t ldb, float* D,
+                          int64_t ldd, int64_t M, int64_t N, int64_t K, float beta,
+                          void* stream) {
+  return ce_gemm_bf16(A, lda, 0, B, ldb, 0, D, ldd, M, N, K, beta, stream);
 }
 
 size_t linear_ce_workspace_size(int64_t M, int64_t H, int64_t V) {
   if (M < 0 || H < 1 || V < 1) return 0;
   const long long mc = M < kLinearDefaultChunk ? (M > 0 ? M : 1) : kLinearDefaultChunk;
-  return linear_ws_layout(M, H, V, mc).total;
+  (void)H;
+  return linear_ws_layout(M, V, mc).total;
 }
 
 ce_status linear_ce_fwd_bwd(const void* h, const void* W, const int64_t* targets, int64_t M,
@@ -767,7 +768,7 @@ ce_status linear_ce_fwd_bwd(const void* h, const void* W, const int64_t* targets
   if (M > INT32_MAX || H > INT32_MAX || V > INT32_MAX) return CE_ERR_UNSUPPORTED;
   // the largest row chunk (a multiple of 128, or all of M) whose workspace fits
   long long mc = M < kLinearDefaultChunk ? M : kLinearDefaultChunk;
-  while (linear_ws_layout(M, H, V, mc).total > workspace_bytes) {
+  while (linear_ws_layout(M, V, mc).total > workspace_bytes) {
     if (mc <= 128) return CE_ERR_INVALID_ARG;
     mc = (mc / 2 + 127) / 128 * 128;
   }
@@ -775,36 +776,25 @@ ce_status linear_ce_fwd_bwd(const void* h, const void* W, const int64_t* targets
   int dev = 0;
   ce_status st = device_info(di, &dev);
   if (st != CE_OK) return st;
-  const LinearWs L = linear_ws_layout(M, H, V, mc);
+  const LinearWs L = linear_ws_layout(M, V, mc);
   char* ws = static_cast<char*>(workspace);
-  auto* wt = reinterpret_cast<__nv_bfloat16*>(ws + L.wt);
   auto* logits = reinterpret_cast<float*>(ws + L.logits);
   auto* g16 = reinterpret_cast<__nv_bfloat16*>(ws + L.g16);
-  auto* gt16 = reinterpret_cast<__nv_bfloat16*>(ws + L.gt16);
-  auto* ht = reinterpret_cast<__nv_bfloat16*>(ws + L.ht);
   auto* rl = reinterpret_cast<float*>(ws + L.rl);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const long long ldv = (V + 7) / 8 * 8;
   const unsigned hint = wait_hint_ns();
   const int sms = di.sm_count;
+  const auto* Wb = static_cast<const __nv_bfloat16*>(W);
   uint64_t launches = 0;
-  // W^T [H, ldv] for dH = G W
-  if ((st = ce::launch_transpose_bf16(W, static_cast<int>(V), static_cast<int>(H), H, wt, ldv, s,
-                                      sms)) != CE_OK)
-    return st;
-  ++launches;
-  // the padding columns [V, ldv) of G16 are never written by the row kernel
-  if (ldv > V && cudaMemset2DAsync(g16 + V, ldv * 2, 0, (ldv - V) * 2, mc, s) != cudaSuccess)
-    return CE_ERR_CUDA;
   const float scale = 1.0f / static_cast<float>(M);
   for (long long m0 = 0; m0 < M; m0 += mc) {
     const long long rows = (M - m0) < mc ? (M - m0) : mc;
-    const long long ldk = (rows + 7) / 8 * 8;
     const auto* hc = static_cast<const __nv_bfloat16*>(h) + m0 * H;
-    // logits[rows, V] = h_c W^T
-    if ((st = ce::gemm_bf16_tn(hc, H, W, H, logits, V, static_cast<int>(rows),
-                               static_cast<int>(V), static_cast<int>(H), 0.f, s, di.err, sms,
-                               hint)) != CE_OK)
+    // logits[rows, V] = h_c W^T: both operands K-major (K = H)
+    if ((st = ce::gemm_bf16(hc, H, false, Wb, H, false, logits, V, static_cast<int>(rows),
+                            static_cast<int>(V), static_cast<int>(H), 0.f, s, di.err, sms,
+                            hint)) != CE_OK)
       return st;
     // row losses, and G16 [rows, ldv] = bf16 of G = (softmax - onehot) / M
     // written by the row kernel straight from the fp32 logits
@@ -812,23 +802,18 @@ ce_status linear_ce_fwd_bwd(const void* h, const void* W, const int64_t* targets
                           CE_RED_NONE, nullptr, rl + m0, nullptr, scale, stream, false, nullptr,
                           g16, ldv)) != CE_OK)
       return st;
-    // G^T [V, ldk] and h_c^T [H, ldk] in bf16
-    if ((st = ce::launch_transpose_bf16(g16, static_cast<int>(rows), static_cast<int>(V), ldv,
-                                        gt16, ldk, s, sms)) != CE_OK)
+    // dH[rows] = G W: A = G16 K-major (K = V), B = W read MN-major ([V, H], H contiguous)
+    if ((st = ce::gemm_bf16(g16, ldv, false, Wb, H, true, dH + m0 * H, H, static_cast<int>(rows),
+                            static_cast<int>(H), static_cast<int>(V), 0.f, s, di.err, sms,
+                            hint)) != CE_OK)
       return st;
-    if ((st = ce::launch_transpose_bf16(hc, static_cast<int>(rows), static_cast<int>(H), H, ht,
-                                        ldk, s, sms)) != CE_OK)
+    // dW (+)= G^T h_c: A = G16 read MN-major ([rows, V], V contiguous), B = h_c read
+    // MN-major ([rows, H], H contiguous), K = rows
+    if ((st = ce::gemm_bf16(g16, ldv, true, hc, H, true, dW, H, static_cast<int>(V),
+                            static_cast<int>(H), static_cast<int>(rows), m0 == 0 ? 0.f : 1.f, s,
+                            di.err, sms, hint)) != CE_OK)
       return st;
-    // dH[rows] = G W = G16 (W^T)^T ; dW (+)= G^T h_c = Gt16 (h_c^T)^T
-    if ((st = ce::gemm_bf16_tn(g16, ldv, wt, ldv, dH + m0 * H, H, static_cast<int>(rows),
-                               static_cast<int>(H), static_cast<int>(ldv), 0.f, s, di.err, sms,
-                               hint)) != CE_OK)
-      return st;
-    if ((st = ce::gemm_bf16_tn(gt16, ldk, ht, ldk, dW, H, static_cast<int>(V), static_cast<int>(H),
-                               static_cast<int>(ldk), m0 == 0 ? 0.f : 1.f, s, di.err, sms,
-                               hint)) != CE_OK)
-      return st;
-    launches += 4;  // the row kernel counts itself
+    launches += 3;  // the row kernel counts itself
   }
   if ((st = ce::launch_mean_rows(rl, M, loss, s)) != CE_OK) return st;
   ++launches;

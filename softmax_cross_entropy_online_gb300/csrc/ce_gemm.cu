@@ -4,7 +4,9 @@
 //
 //     D[M, N] (fp32)  =  A[M, K] . B[N, K]^T  (+ beta * D)
 //
-// with A and B bf16 and K contiguous in memory ("K-major" for both operands).
+// with A and B bf16, each stored either K-major (K contiguous) or MN-major (M or
+// N contiguous, i.e. the transpose): the fused path reads W, G and h in the
+// layout they have, with no transpose pass.
 //
 // Design: a persistent kernel, one CTA per SM, warp-specialised.
 //  * warp 0 (one thread) streams 128x64 tiles of A and 256x64 tiles of B into a
@@ -52,6 +54,7 @@ struct GemmParams {
   int use_tma;    // D written by TMA tensor stores / reduce-adds (rows 16-byte aligned)
   int tiles_m, tiles_n, k_tiles;
   int n_fast;     // tile order: 1 = N varies fastest (A the larger operand), 0 = M
+  int a_mn, b_mn; // operand stored MN-major (M or N contiguous) instead of K-major
   unsigned int* err;
   unsigned int wait_hint_ns;
 };
@@ -73,7 +76,19 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
          (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
          (static_cast<uint64_t>(2) << 61);
 }
-// instruction descriptor of kind::f16: D fp32, A and B bf16, both K-major, N=256, M=128
+// MN-major operand (M or N contiguous), 128-byte swizzle: the tile is built
+// from 64-element (128-byte) wide TMA boxes of 64 K-rows, 8 KB each; inside a
+// box K-row r sits at 128 r (8-row swizzle atoms, 1024 bytes).  Descriptor: the
+// next 64 elements of M / N are 8 KB on (leading-byte offset), the next 8
+// K-rows 1024 bytes on (stride-byte offset); one MMA's 16 K-rows are 2048
+// bytes.
+__device__ __forceinline__ uint64_t smem_desc_sw128_mn(uint32_t addr) {
+  return static_cast<uint64_t>((addr >> 4) & 0x3FFFu) |
+         (static_cast<uint64_t>(8192 >> 4) << 16) | (static_cast<uint64_t>(1024 >> 4) << 32) |
+         (static_cast<uint64_t>(1) << 46) | (static_cast<uint64_t>(2) << 61);
+}
+// instruction descriptor of kind::f16: D fp32, A and B bf16, N=256, M=128; bits
+// 15 and 16 mark A and B as MN-major
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((kGemmBN >> 3) << 17) |
                             ((kGemmBM >> 4) << 24);
 
@@ -109,11 +124,11 @@ __device__ __forceinline__ void tile_coords(const GemmParams& p, int tile, int& 
 }
 
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                          uint32_t accumulate) {
+                                          uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
       " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(kIdesc), "r"(accumulate)
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
@@ -146,7 +161,7 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
 }
 
 __global__ void __launch_bounds__(kGemmThreads, 1)
-    gemm_bf16_tn_kernel(const __grid_constant__ CUtensorMap tma_a,
+    gemm_bf16_kernel(const __grid_constant__ CUtensorMap tma_a,
                         const __grid_constant__ CUtensorMap tma_b,
                         const __grid_constant__ CUtensorMap tma_d, const GemmParams p) {
   extern __shared__ unsigned char gsm[];
@@ -200,8 +215,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint32_t fb = smem_u32(&full_bar[s]);
           const uint32_t sa = sbase + s * kStageBytes;
           mbar_arrive_expect_tx(fb, kStageBytes);
-          tma_load_2d(sa, &tma_a, kt * kGemmBK, tm * kGemmBM, fb);
-          tma_load_2d(sa + kTileABytes, &tma_b, kt * kGemmBK, tn * kGemmBN, fb);
+          if (p.a_mn) {
+            for (int j = 0; j < kGemmBM / 64; ++j)
+              tma_load_2d(sa + j * 8192, &tma_a, tm * kGemmBM + 64 * j, kt * kGemmBK, fb);
+          } else {
+            tma_load_2d(sa, &tma_a, kt * kGemmBK, tm * kGemmBM, fb);
+          }
+          if (p.b_mn) {
+            for (int j = 0; j < kGemmBN / 64; ++j)
+              tma_load_2d(sa + kTileABytes + j * 8192, &tma_b, tn * kGemmBN + 64 * j,
+                          kt * kGemmBK, fb);
+          } else {
+            tma_load_2d(sa + kTileABytes, &tma_b, kt * kGemmBK, tn * kGemmBN, fb);
+          }
           filled |= 1u << s;
           if (++s == kGemmStages) {
             s = 0;
@@ -222,6 +248,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       // ---------------- MMA issuer ----------------
       int s = 0, a = 0;
       uint32_t ph = 0, aph = 0;
+      const uint32_t idesc = kIdesc | (p.a_mn ? (1u << 15) : 0u) | (p.b_mn ? (1u << 16) : 0u);
+      // one MMA's K = 16 step: 32 bytes inside a K-major row, 2048 bytes (16
+      // K-rows) in an MN-major tile; descriptors count 16-byte units
+      const uint64_t a_step = p.a_mn ? 128 : 2, b_step = p.b_mn ? 128 : 2;
       for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
         mbar_wait<false>(smem_u32(&acce_bar[a]), aph ^ 1u, p.err, failed, WAIT_LIMIT_NS, hint);
         tc_fence_after();
@@ -230,13 +260,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           mbar_wait<false>(smem_u32(&full_bar[s]), ph, p.err, failed, WAIT_LIMIT_NS, hint);
           tc_fence_after();
           const uint32_t sa = sbase + s * kStageBytes;
-          const uint64_t da = smem_desc_sw128(sa);
-          const uint64_t db = smem_desc_sw128(sa + kTileABytes);
+          const uint64_t da = p.a_mn ? smem_desc_sw128_mn(sa) : smem_desc_sw128(sa);
+          const uint64_t db =
+              p.b_mn ? smem_desc_sw128_mn(sa + kTileABytes) : smem_desc_sw128(sa + kTileABytes);
 #pragma unroll
-          for (int kk = 0; kk < kGemmBK / 16; ++kk) {
-            // advance 16 bf16 (32 bytes) along K inside the swizzled rows
-            umma_bf16(d_tmem, da + 2 * kk, db + 2 * kk, (kt | kk) != 0 ? 1u : 0u);
-          }
+          for (int kk = 0; kk < kGemmBK / 16; ++kk)
+            umma_bf16(d_tmem, da + a_step * kk, db + b_step * kk, idesc, (kt | kk) != 0 ? 1u : 0u);
           umma_commit(smem_u32(&empty_bar[s]));
           if (++s == kGemmStages) {
             s = 0;
@@ -354,14 +383,15 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // 2-D bf16 tensor map over `rows` x `cols` (cols contiguous, row stride ld
-// elements) with a box of box_rows x 64 and 128-byte swizzle
+// elements) with a box of box_rows x 64 and 128-byte swizzle: K-major tiles take
+// box_rows = 128 / 256 rows of 64 K; MN-major tiles take 64 K-rows of 64
 static bool make_map(CUtensorMap* map, const void* base, long long rows, long long cols,
                      long long ld, int box_rows) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(kGemmBK), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[2] = {1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -383,18 +413,24 @@ static bool make_map_f32(CUtensorMap* map, void* base, long long rows, long long
             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// D[M,N] = A[M,K] B[N,K]^T (+ beta D); bf16 inputs with K contiguous, fp32 D.
-// Requires K, lda, ldb multiples of 8 and 16-byte aligned A and B.
-ce_status gemm_bf16_tn(const void* A, long long lda, const void* B, long long ldb, float* D,
-                       long long ldd, int M, int N, int K, float beta, cudaStream_t stream,
-                       unsigned int* err, int sm_count, unsigned int wait_hint_ns) {
+// D[M,N] = op(A) op(B)^T (+ beta D), bf16 inputs, fp32 D.  a_mn = false: A is
+// [M, lda] with K contiguous; a_mn = true: A is stored [K, lda] with M contiguous
+// (the transpose of a K-major A).  The same for B with N.  Requires lda, ldb
+// multiples of 8 (16-byte row strides for TMA) and 16-byte aligned A and B;
+// tiles reaching past M, N or K are zero-filled by TMA.
+ce_status gemm_bf16(const void* A, long long lda, bool a_mn, const void* B, long long ldb,
+                    bool b_mn, float* D, long long ldd, int M, int N, int K, float beta,
+                    cudaStream_t stream, unsigned int* err, int sm_count,
+                    unsigned int wait_hint_ns) {
   if (M <= 0 || N <= 0 || K <= 0) return CE_OK;
-  if ((K % 8) || (lda % 8) || (ldb % 8) || lda < K || ldb < K || ldd < N) return CE_ERR_UNSUPPORTED;
+  if ((lda % 8) || (ldb % 8) || ldd < N) return CE_ERR_UNSUPPORTED;
+  if ((a_mn ? lda < M : lda < K) || (b_mn ? ldb < N : ldb < K)) return CE_ERR_UNSUPPORTED;
   if ((reinterpret_cast<uintptr_t>(A) & 15) || (reinterpret_cast<uintptr_t>(B) & 15))
     return CE_ERR_UNSUPPORTED;
   CUtensorMap ma, mb, md;
-  if (!make_map(&ma, A, M, K, lda, kGemmBM) || !make_map(&mb, B, N, K, ldb, kGemmBN))
-    return CE_ERR_CUDA;
+  const bool ok_a = a_mn ? make_map(&ma, A, K, M, lda, 64) : make_map(&ma, A, M, K, lda, kGemmBM);
+  const bool ok_b = b_mn ? make_map(&mb, B, K, N, ldb, 64) : make_map(&mb, B, N, K, ldb, kGemmBN);
+  if (!ok_a || !ok_b) return CE_ERR_CUDA;
   // D by TMA when its rows sit on the 16-byte grid (the tensor map's stride rule)
   const bool use_tma = (ldd % 4 == 0) && ((reinterpret_cast<uintptr_t>(D) & 15) == 0);
   std::memset(&md, 0, sizeof(md));
@@ -411,14 +447,16 @@ ce_status gemm_bf16_tn(const void* A, long long lda, const void* B, long long ld
   p.tiles_n = (N + kGemmBN - 1) / kGemmBN;
   p.k_tiles = (K + kGemmBK - 1) / kGemmBK;
   p.n_fast = M > N ? 1 : 0;  // A [M, K] the larger operand
+  p.a_mn = a_mn ? 1 : 0;
+  p.b_mn = b_mn ? 1 : 0;
   p.err = err;
   p.wait_hint_ns = wait_hint_ns;
-  if (cudaFuncSetAttribute(gemm_bf16_tn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(gemm_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kGemmSmem) != cudaSuccess)
     return CE_ERR_CUDA;
   const int tiles = p.tiles_m * p.tiles_n;
   const int grid = tiles < sm_count ? tiles : sm_count;
-  gemm_bf16_tn_kernel<<<grid, kGemmThreads, kGemmSmem, stream>>>(ma, mb, md, p);
+  gemm_bf16_kernel<<<grid, kGemmThreads, kGemmSmem, stream>>>(ma, mb, md, p);
   return cudaGetLastError() == cudaSuccess ? CE_OK : CE_ERR_CUDA;
 }
 
@@ -426,66 +464,7 @@ ce_status gemm_bf16_tn(const void* A, long long lda, const void* B, long long ld
 
 namespace ce {
 
-// --- layout helpers of the fused linear + cross-entropy ------------------------
-constexpr int kTT = 64;       // tile edge
-constexpr int kTP = kTT + 8;  // padded pitch (bf16) of the shared tile
-
-// T[c, r] = X[r, c] for bf16, r < R, c < C (zero in the padding columns r >= R up
-// to ldt); 64x64 tiles with 16-byte loads and stores (ldx, ldt multiples of 8),
-// the shared tile XOR-swizzled by 16-byte chunk so that neither direction has
-// bank conflicts
-__global__ void __launch_bounds__(256) transpose_bf16_kernel(const __nv_bfloat16* __restrict__ X,
-                                                             int R, int C, long long ldx,
-                                                             __nv_bfloat16* __restrict__ T,
-                                                             long long ldt) {
-  __shared__ __align__(16) __nv_bfloat16 tile[kTT][kTP];
-  const long long tiles_c = (C + kTT - 1) / kTT;
-  const long long tiles_r = (ldt + kTT - 1) / kTT;
-  const int tid = threadIdx.x;
-  for (long long tt = blockIdx.x; tt < tiles_r * tiles_c; tt += gridDim.x) {
-    const long long r0 = (tt / tiles_c) * kTT, c0 = (tt % tiles_c) * kTT;
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const int idx = tid + k * 256;
-      const int rr = idx >> 3, cq = (idx & 7) * 8;
-      const long long r = r0 + rr, c = c0 + cq;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (r < R) {
-        if (c + 7 < C) {
-          v = *reinterpret_cast<const uint4*>(X + r * ldx + c);
-        } else {
-          __nv_bfloat16 e[8];
-#pragma unroll
-          for (int j = 0; j < 8; ++j) e[j] = (c + j < C) ? X[r * ldx + c + j] : __float2bfloat16_rn(0.f);
-          v = *reinterpret_cast<uint4*>(e);
-        }
-      }
-      // 16-byte chunk (cq / 8) of row rr at chunk (cq / 8) ^ (rr / 8 % 8): the
-      // column reads below then spread over all banks
-      *reinterpret_cast<uint4*>(&tile[rr][8 * ((cq >> 3) ^ ((rr >> 3) & 7))]) = v;
-    }
-    __syncthreads();
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const int idx = tid + k * 256;
-      const int cc = idx >> 3, rg = (idx & 7) * 8;
-      const long long c = c0 + cc, r = r0 + rg;
-      if (c < C && r < ldt) {
-        uint32_t w[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          __nv_bfloat162 pr;
-          const int sw = 8 * ((cc >> 3) ^ ((rg >> 3) & 7)) + (cc & 7);  // rows rg..rg+7 share rg / 8
-          pr.x = tile[rg + 2 * j][sw];
-          pr.y = tile[rg + 2 * j + 1][sw];
-          w[j] = *reinterpret_cast<uint32_t*>(&pr);
-        }
-        *reinterpret_cast<uint4*>(T + c * ldt + r) = make_uint4(w[0], w[1], w[2], w[3]);
-      }
-    }
-    __syncthreads();
-  }
-}
+// --- the mean of the row losses of the fused linear + cross-entropy ------------
 
 // loss = (sum of rl[0..M)) / M: one CTA, each thread sums a fixed stride in
 // fp64, then a fixed-order tree; deterministic, no atomics
@@ -502,12 +481,6 @@ __global__ void mean_rows_kernel(const float* __restrict__ rl, long long M, floa
   if (threadIdx.x == 0) *loss = static_cast<float>(part[0] / static_cast<double>(M));
 }
 
-ce_status launch_transpose_bf16(const void* X, int R, int C, long long ldx, void* T,
-                                long long ldt, cudaStream_t st, int sm_count) {
-  transpose_bf16_kernel<<<sm_count * 8, 256, 0, st>>>(
-      static_cast<const __nv_bfloat16*>(X), R, C, ldx, static_cast<__nv_bfloat16*>(T), ldt);
-  return cudaGetLastError() == cudaSuccess ? CE_OK : CE_ERR_CUDA;
-}
 ce_status launch_mean_rows(const float* rl, long long M, float* loss, cudaStream_t st) {
   mean_rows_kernel<<<1, 1024, 0, st>>>(rl, M, loss);
   return cudaGetLastError() == cudaSuccess ? CE_OK : CE_ERR_CUDA;

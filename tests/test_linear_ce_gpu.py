@@ -57,6 +57,39 @@ def test_gemm_against_float64(api, M, N, K):
     assert api.ce_check_errors() == 0
 
 
+@pytest.mark.parametrize("a_mn,b_mn", [(False, False), (False, True), (True, False), (True, True)])
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (200, 300, 136), (1, 1, 8), (513, 1000, 777),
+                                   (130, 520, 2049), (1024, 768, 72)])
+def test_gemm_operand_layouts_against_float64(api, a_mn, b_mn, M, N, K):
+    # A read K-major ([M, K]) or MN-major (stored [K, M]); the same for B
+    rng = np.random.default_rng(M * 13 + N + K)
+    A = synthetic.f32_to_bf16_bits(rng.standard_normal((M, K), dtype=np.float32))
+    B = synthetic.f32_to_bf16_bits(rng.standard_normal((N, K), dtype=np.float32))
+    A64, B64 = oracle.decode_bf16(A), oracle.decode_bf16(B)
+    ref = A64 @ B64.T
+    bound = 1e-5 * (np.abs(A64) @ np.abs(B64).T) + 1e-30
+
+    def stored(X, mn):
+        # rows padded to a multiple of 8 elements, as the strides require
+        Xs = np.ascontiguousarray(X.T) if mn else X
+        cols = Xs.shape[1]
+        pad = (cols + 7) // 8 * 8
+        buf = np.zeros((Xs.shape[0], pad), dtype=Xs.dtype)
+        buf[:, :cols] = Xs
+        return bf16_dev(buf)[:, :cols]
+
+    Ad, Bd = stored(A, a_mn), stored(B, b_mn)
+    D = api.ce_gemm_bf16(Ad, Bd, a_mn=a_mn, b_mn=b_mn)
+    torch.cuda.synchronize()
+    err = np.abs(D.cpu().numpy().astype(np.float64) - ref)
+    assert np.all(err <= bound), f"worst {np.max(err / bound):.3g} x bound"
+    api.ce_gemm_bf16(Ad, Bd, D, beta=1.0, a_mn=a_mn, b_mn=b_mn)
+    torch.cuda.synchronize()
+    err = np.abs(D.cpu().numpy().astype(np.float64) - 2 * ref)
+    assert np.all(err <= 2 * bound)
+    assert api.ce_check_errors() == 0
+
+
 def check_linear(api, M, H, V, seed, workspace_bytes=None):
     h, W, t = synthetic.make_linear_ce_inputs(M, H, V, seed=seed)
     ws = None
