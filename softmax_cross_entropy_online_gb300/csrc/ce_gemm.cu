@@ -55,11 +55,20 @@ struct GemmParams {
   int tiles_m, tiles_n, k_tiles;
   int n_fast;     // tile order: 1 = N varies fastest (A the larger operand), 0 = M
   int a_mn, b_mn; // operand stored MN-major (M or N contiguous) instead of K-major
+  int a_3d, b_3d; // MN-major operand loaded by one 3-D box per stage (M / N % 64 == 0)
   unsigned int* err;
   unsigned int wait_hint_ns;
 };
 
 // --- tcgen05 / TMA helpers ---------------------------------------------------
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            int z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
                                             uint32_t bar) {
   asm volatile(
@@ -215,13 +224,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint32_t fb = smem_u32(&full_bar[s]);
           const uint32_t sa = sbase + s * kStageBytes;
           mbar_arrive_expect_tx(fb, kStageBytes);
-          if (p.a_mn) {
+          if (p.a_3d) {
+            tma_load_3d(sa, &tma_a, 0, kt * kGemmBK, tm * (kGemmBM / 64), fb);
+          } else if (p.a_mn) {
             for (int j = 0; j < kGemmBM / 64; ++j)
               tma_load_2d(sa + j * 8192, &tma_a, tm * kGemmBM + 64 * j, kt * kGemmBK, fb);
           } else {
             tma_load_2d(sa, &tma_a, kt * kGemmBK, tm * kGemmBM, fb);
           }
-          if (p.b_mn) {
+          if (p.b_3d) {
+            tma_load_3d(sa + kTileABytes, &tma_b, 0, kt * kGemmBK, tn * (kGemmBN / 64), fb);
+          } else if (p.b_mn) {
             for (int j = 0; j < kGemmBN / 64; ++j)
               tma_load_2d(sa + kTileABytes + j * 8192, &tma_b, tn * kGemmBN + 64 * j,
                           kt * kGemmBK, fb);
@@ -398,6 +411,23 @@ static bool make_map(CUtensorMap* map, const void* base, long long rows, long lo
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D bf16 tensor map of an MN-major operand whose MN extent is a multiple of
+// 64: element (mn, k) at (mn % 64, k, mn / 64); one box of 64 x 64 x blocks
+// lands the 64-wide blocks of a tile one after another (8 KB apart), the
+// layout the MN-major descriptor expects, in a single copy
+static bool make_map_mn3d(CUtensorMap* map, const void* base, long long k_rows, long long mn,
+                          long long ld, int blocks) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(k_rows), static_cast<cuuint64_t>(mn / 64)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * 2, 128};
+  cuuint32_t box[3] = {64u, 64u, static_cast<cuuint32_t>(blocks)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 2-D fp32 tensor map over D (rows x cols, row stride ld elements, a multiple
 // of 4) with a box of 32 x 32 and 128-byte swizzle: the epilogue's blocks
 static bool make_map_f32(CUtensorMap* map, void* base, long long rows, long long cols,
@@ -428,8 +458,12 @@ ce_status gemm_bf16(const void* A, long long lda, bool a_mn, const void* B, long
   if ((reinterpret_cast<uintptr_t>(A) & 15) || (reinterpret_cast<uintptr_t>(B) & 15))
     return CE_ERR_UNSUPPORTED;
   CUtensorMap ma, mb, md;
-  const bool ok_a = a_mn ? make_map(&ma, A, K, M, lda, 64) : make_map(&ma, A, M, K, lda, kGemmBM);
-  const bool ok_b = b_mn ? make_map(&mb, B, K, N, ldb, 64) : make_map(&mb, B, N, K, ldb, kGemmBN);
+  // MN-major with an MN extent of whole 64-element blocks: one 3-D box per tile
+  const bool a_3d = a_mn && (M % 64 == 0), b_3d = b_mn && (N % 64 == 0);
+  const bool ok_a = a_3d ? make_map_mn3d(&ma, A, K, M, lda, kGemmBM / 64)
+                         : (a_mn ? make_map(&ma, A, K, M, lda, 64) : make_map(&ma, A, M, K, lda, kGemmBM));
+  const bool ok_b = b_3d ? make_map_mn3d(&mb, B, K, N, ldb, kGemmBN / 64)
+                         : (b_mn ? make_map(&mb, B, K, N, ldb, 64) : make_map(&mb, B, N, K, ldb, kGemmBN));
   if (!ok_a || !ok_b) return CE_ERR_CUDA;
   // D by TMA when its rows sit on the 16-byte grid (the tensor map's stride rule)
   const bool use_tma = (ldd % 4 == 0) && ((reinterpret_cast<uintptr_t>(D) & 15) == 0);
@@ -449,6 +483,8 @@ ce_status gemm_bf16(const void* A, long long lda, bool a_mn, const void* B, long
   p.n_fast = M > N ? 1 : 0;  // A [M, K] the larger operand
   p.a_mn = a_mn ? 1 : 0;
   p.b_mn = b_mn ? 1 : 0;
+  p.a_3d = a_3d ? 1 : 0;
+  p.b_3d = b_3d ? 1 : 0;
   p.err = err;
   p.wait_hint_ns = wait_hint_ns;
   if (cudaFuncSetAttribute(gemm_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

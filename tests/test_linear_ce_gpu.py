@@ -59,8 +59,11 @@ def test_gemm_against_float64(api, M, N, K):
 
 @pytest.mark.parametrize("a_mn,b_mn", [(False, False), (False, True), (True, False), (True, True)])
 @pytest.mark.parametrize("M,N,K", [(128, 256, 64), (200, 300, 136), (1, 1, 8), (513, 1000, 777),
-                                   (130, 520, 2049), (1024, 768, 72)])
+                                   (130, 520, 2049), (1024, 768, 72), (192, 320, 200),
+                                   (640, 64, 1000)])
 def test_gemm_operand_layouts_against_float64(api, a_mn, b_mn, M, N, K):
+    # (M, N multiples of 64 load MN-major tiles with one 3-D box, others in
+    # 64-wide 2-D boxes)
     # A read K-major ([M, K]) or MN-major (stored [K, M]); the same for B
     rng = np.random.default_rng(M * 13 + N + K)
     A = synthetic.f32_to_bf16_bits(rng.standard_normal((M, K), dtype=np.float32))
