@@ -169,6 +169,9 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
   for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
 }
 
+// A_MN / B_MN: the operands' layouts, fixed at compile time so that the
+// K-major form runs exactly the code it would alone
+template <bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap tma_a,
                         const __grid_constant__ CUtensorMap tma_b,
@@ -224,17 +227,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint32_t fb = smem_u32(&full_bar[s]);
           const uint32_t sa = sbase + s * kStageBytes;
           mbar_arrive_expect_tx(fb, kStageBytes);
-          if (p.a_3d) {
+          if (A_MN && p.a_3d) {
             tma_load_3d(sa, &tma_a, 0, kt * kGemmBK, tm * (kGemmBM / 64), fb);
-          } else if (p.a_mn) {
+          } else if (A_MN) {
             for (int j = 0; j < kGemmBM / 64; ++j)
               tma_load_2d(sa + j * 8192, &tma_a, tm * kGemmBM + 64 * j, kt * kGemmBK, fb);
           } else {
             tma_load_2d(sa, &tma_a, kt * kGemmBK, tm * kGemmBM, fb);
           }
-          if (p.b_3d) {
+          if (B_MN && p.b_3d) {
             tma_load_3d(sa + kTileABytes, &tma_b, 0, kt * kGemmBK, tn * (kGemmBN / 64), fb);
-          } else if (p.b_mn) {
+          } else if (B_MN) {
             for (int j = 0; j < kGemmBN / 64; ++j)
               tma_load_2d(sa + kTileABytes + j * 8192, &tma_b, tn * kGemmBN + 64 * j,
                           kt * kGemmBK, fb);
@@ -261,10 +264,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       // ---------------- MMA issuer ----------------
       int s = 0, a = 0;
       uint32_t ph = 0, aph = 0;
-      const uint32_t idesc = kIdesc | (p.a_mn ? (1u << 15) : 0u) | (p.b_mn ? (1u << 16) : 0u);
+      constexpr uint32_t idesc = kIdesc | (A_MN ? (1u << 15) : 0u) | (B_MN ? (1u << 16) : 0u);
       // one MMA's K = 16 step: 32 bytes inside a K-major row, 2048 bytes (16
       // K-rows) in an MN-major tile; descriptors count 16-byte units
-      const uint64_t a_step = p.a_mn ? 128 : 2, b_step = p.b_mn ? 128 : 2;
+      constexpr uint64_t a_step = A_MN ? 128 : 2, b_step = B_MN ? 128 : 2;
       for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
         mbar_wait<false>(smem_u32(&acce_bar[a]), aph ^ 1u, p.err, failed, WAIT_LIMIT_NS, hint);
         tc_fence_after();
@@ -273,9 +276,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           mbar_wait<false>(smem_u32(&full_bar[s]), ph, p.err, failed, WAIT_LIMIT_NS, hint);
           tc_fence_after();
           const uint32_t sa = sbase + s * kStageBytes;
-          const uint64_t da = p.a_mn ? smem_desc_sw128_mn(sa) : smem_desc_sw128(sa);
+          const uint64_t da = A_MN ? smem_desc_sw128_mn(sa) : smem_desc_sw128(sa);
           const uint64_t db =
-              p.b_mn ? smem_desc_sw128_mn(sa + kTileABytes) : smem_desc_sw128(sa + kTileABytes);
+              B_MN ? smem_desc_sw128_mn(sa + kTileABytes) : smem_desc_sw128(sa + kTileABytes);
 #pragma unroll
           for (int kk = 0; kk < kGemmBK / 16; ++kk)
             umma_bf16(d_tmem, da + a_step * kk, db + b_step * kk, idesc, (kt | kk) != 0 ? 1u : 0u);
@@ -487,12 +490,14 @@ ce_status gemm_bf16(const void* A, long long lda, bool a_mn, const void* B, long
   p.b_3d = b_3d ? 1 : 0;
   p.err = err;
   p.wait_hint_ns = wait_hint_ns;
-  if (cudaFuncSetAttribute(gemm_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kGemmSmem) != cudaSuccess)
+  auto kern = a_mn ? (b_mn ? gemm_bf16_kernel<true, true> : gemm_bf16_kernel<true, false>)
+                   : (b_mn ? gemm_bf16_kernel<false, true> : gemm_bf16_kernel<false, false>);
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem) !=
+      cudaSuccess)
     return CE_ERR_CUDA;
   const int tiles = p.tiles_m * p.tiles_n;
   const int grid = tiles < sm_count ? tiles : sm_count;
-  gemm_bf16_kernel<<<grid, kGemmThreads, kGemmSmem, stream>>>(ma, mb, md, p);
+  kern<<<grid, kGemmThreads, kGemmSmem, stream>>>(ma, mb, md, p);
   return cudaGetLastError() == cudaSuccess ? CE_OK : CE_ERR_CUDA;
 }
 
