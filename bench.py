@@ -408,14 +408,17 @@ def run_native(args, w):
 LINEAR_SHAPES = {"linear_ce_8192x4096x128256": (8192, 4096, 128256)}
 
 
-def measured_tflops():
+def measured_tflops(burst: bool = False):
+    """bf16 tensor peak: the sustained figure for a kernel timed inside a long
+    step, the burst figure for one timed alone."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    key = "bf16_tflops" if burst else "bf16_tflops_sustained"
     if os.path.exists(p):
         with open(p) as fh:
             d = json.load(fh)
-        if d.get("bf16_tflops_sustained"):
-            return float(d["bf16_tflops_sustained"]), "measured (sustained)"
-    return 1700.0, "fallback (sustained)"
+        if d.get(key):
+            return float(d[key]), f"measured ({'burst' if burst else 'sustained'})"
+    return (1900.0, "fallback (burst)") if burst else (1700.0, "fallback (sustained)")
 
 
 def run_linear(args):
@@ -523,6 +526,168 @@ def run_linear(args):
     return 0
 
 
+# ---------------------------------------------------------------------------
+# blockwise attention forward (the flash-attention page's benchmark shape)
+# ---------------------------------------------------------------------------
+ATTN_SHAPES = {"attn_causal_32x96x512x128": (32, 96, 512, 128, True)}
+
+
+def attention_flops(B: int, NH: int, T: int, D: int, causal: bool, heads: int | None = None) -> float:
+    """FLOPs the method must do: 2 D for each visible (query, key) pair in
+    Q K^T and again in P V (T (T + 1) / 2 pairs per head under the causal
+    mask, T^2 without)."""
+    pairs = T * (T + 1) // 2 if causal else T * T
+    return 4.0 * D * pairs * (B * NH if heads is None else heads)
+
+
+def attention_desc(name, B, NH, T, D, causal):
+    return (f"{name}: q, k, v bf16 [{B}, {NH}, {T}, {D}] N(0,1), "
+            f"{'causal' if causal else 'no'} mask, sm_scale 1/sqrt({D}); out fp32 + lse")
+
+
+def attention_oracle_sample(B, NH, T, D, causal, budget_s):
+    """Time the float64 oracle on whole heads of the workload (about budget_s
+    of CPU work); returns (TFLOP/s, heads, seconds)."""
+    from oracle import attention_oracle as AO
+    q, k, v = synthetic.make_attention_inputs(1, 4, T, D, seed=0)
+    widen = lambda b: (b.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)  # noqa: E731
+    q, k, v = widen(q)[0], widen(k)[0], widen(v)[0]
+    mask = AO.causal_mask(T) if causal else None
+    t0 = time.perf_counter()
+    AO.attention_forward(q[:1], k[:1], v[:1], mask)
+    one = max(time.perf_counter() - t0, 1e-6)
+    heads = int(max(1, min(B * NH, budget_s / one)))
+    reps = (heads + 3) // 4
+    t0 = time.perf_counter()
+    done = 0
+    for _ in range(reps):
+        n = min(4, heads - done)
+        AO.attention_forward(q[:n], k[:n], v[:n], mask)
+        done += n
+    dt = time.perf_counter() - t0
+    return attention_flops(B, NH, T, D, causal, heads) / dt / 1e12, heads, dt
+
+
+def run_attention(args):
+    import torch
+    from softmax_cross_entropy_online_gb300 import api, build
+
+    ws, rank, local = dist_env()
+    B, NH, T, D, causal = ATTN_SHAPES[args.workload]
+    desc = attention_desc(args.workload, B, NH, T, D, causal)
+    metric = "blockwise attention forward TFLOP/s (4 D per visible query-key pair)"
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        vals, hs, secs = [], 0, 0.0
+        for _ in range(args.warmup):
+            attention_oracle_sample(B, NH, T, D, causal, 0.2)
+        for _ in range(args.steps):
+            v, hs, secs = attention_oracle_sample(B, NH, T, D, causal, args.cpu_budget_s / 4)
+            vals.append(v)
+        val = sum(vals) / len(vals)
+        sample = f"{hs} of {B * NH} heads per step (float64 numpy oracle, 1 thread)"
+        print(json.dumps({
+            "impl": "reference", "metric": metric, "value": val, "unit": "TFLOP/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": desc, "B": B, "NH": NH, "T": T, "D": D},
+            "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}), flush=True)
+        return 0
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", init_method="env://")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    build.build()
+    L = api.lib()
+    qb, kb, vb = synthetic.make_attention_inputs(B, NH, T, D, seed=0)
+    as_bf16 = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)  # noqa: E731
+    hosts = [as_bf16(a).pin_memory() for a in (qb, kb, vb)]
+    del qb, kb, vb
+    q, k, v = (h.to(dev) for h in hosts)
+    out = torch.empty((B, NH, T, D), dtype=torch.float32, device=dev)
+    lse = torch.empty((B, NH, T), dtype=torch.float32, device=dev)
+    sh = torch.cuda.current_stream(dev).cuda_stream
+    scale = 1.0 / float(np.sqrt(D))
+
+    def step():
+        st = L.ce_attention_forward(q.data_ptr(), k.data_ptr(), v.data_ptr(), None, int(causal),
+                                    B, NH, T, D, scale, out.data_ptr(), lse.data_ptr(), sh)
+        if st != 0:
+            raise api.CEError(st, "ce_attention_forward")
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n0 = api.ce_launch_count()
+    e0.record()
+    for _ in range(args.steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    launches = api.ce_launch_count() - n0
+    clocks = sampler.stop() if sampler else None
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dev)
+    if ws > 1:
+        dist.barrier()
+    flops = attention_flops(B, NH, T, D, causal)
+    value = ws * flops / (ms * 1e-3) / 1e12
+    assert api.ce_check_errors() == 0
+    peak, peak_kind = measured_tflops(burst=True)
+    # end to end: q, k, v from pinned host memory, the call, out and lse back
+    out_host = torch.empty((B, NH, T, D), dtype=torch.float32).pin_memory()
+    lse_host = torch.empty((B, NH, T), dtype=torch.float32).pin_memory()
+    x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(2, min(args.steps, 5))
+    x0.record()
+    for _ in range(e2e_steps):
+        for d_, h_ in zip((q, k, v), hosts):
+            d_.copy_(h_, non_blocking=True)
+        step()
+        out_host.copy_(out, non_blocking=True)
+        lse_host.copy_(lse, non_blocking=True)
+    x1.record()
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(x0.elapsed_time(x1) / e2e_steps, dev)
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        cv, hs, secs = attention_oracle_sample(B, NH, T, D, causal, args.cpu_budget_s)
+        cpu = {"value": cv, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+               "sample": f"{hs} of {B * NH} heads in float64 numpy ({secs:.1f} s on 1 host "
+                         "thread)"}
+    if rank == 0:
+        print(json.dumps({
+            "metric": metric, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": desc, "B": B, "NH": NH, "T": T, "D": D, "causal": causal,
+                       "l2": "inputs (3 x 403 MB) larger than L2"},
+            "roofline": {"bound": "tensor", "achieved": flops / (ms * 1e-3) / 1e12, "peak": peak,
+                         "unit": "TFLOP/s", "frac": flops / (ms * 1e-3) / 1e12 / peak,
+                         "peak_source": peak_kind, "traffic": None,
+                         "kernel": "attention_fwd_kernel<128>", "ms_per_launch": ms},
+            "e2e": {"value": ws * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": 3 * B * NH * T * D * 2,
+                    "d2h_bytes_per_step": B * NH * T * (D + 1) * 4, "ms_per_step": e2e_ms},
+            "cpu_baseline": cpu, "gpu_launches": launches, "clocks": clocks}), flush=True)
+    if ws > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -530,7 +695,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workload", default="f32_32768x4096",
-                    choices=sorted(synthetic.WORKLOADS) + sorted(LINEAR_SHAPES))
+                    choices=sorted(synthetic.WORKLOADS) + sorted(LINEAR_SHAPES)
+                    + sorted(ATTN_SHAPES))
     ap.add_argument("--max-resident-gb", type=float, default=64.0)
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     ap.add_argument("--ref-rows", type=int, default=1024)
@@ -539,6 +705,8 @@ def main():
                     help="override the workload's row count (smaller cases for profiling)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps, always
+    if args.workload in ATTN_SHAPES:
+        return run_attention(args)
     if args.workload in LINEAR_SHAPES:
         if args.impl == "reference":
             print(json.dumps({"impl": "reference", "unavailable":

@@ -209,6 +209,38 @@ ce_status ce_gemm_bf16_tn(const void* A, int64_t lda, const void* B, int64_t ldb
                           void* stream);
 
 /*
+ * ce_attention_forward -- blockwise (flash-attention-2 style) attention
+ * forward on the tensor cores: the workload of "How to optimize an existing
+ * Triton Kernel to make it faster?" (Triton discussion #8261), whose forward
+ * keeps a running row max and a running normaliser over blocks of keys, the
+ * same online (max, sum) pair as the cross-entropy rows.  Per head:
+ *
+ *     S   = Q K^T * sm_scale + mask        (+ the causal mask if causal != 0)
+ *     out = softmax_rows(S) V
+ *     lse = log sum_j exp(S_ij)            (per query row)
+ *
+ *   q, k, v  [B, NH, T, D] bf16, contiguous, 16-byte aligned (device).
+ *            D is 64 or 128.
+ *   mask     [T, T] fp32 additive mask (row = query), or NULL.  -inf hides
+ *            a key.  Combined with causal it is added before the causal mask.
+ *   causal   1: key j is hidden from query i when j > i (and the key blocks
+ *            wholly above the diagonal are skipped); 0: no causal mask.
+ *   sm_scale the score scale (the page uses 1/sqrt(D)); finite.
+ *   out      [B, NH, T, D] fp32, 16-byte aligned (device, caller-owned).
+ *   lse      [B, NH, T] fp32 (device) or NULL.
+ * Arithmetic: bf16 products with fp32 accumulation for Q K^T; the softmax in
+ * fp32 (exponentials in base 2 of the score times log2(e)); P is rounded to
+ * bf16 for P V, accumulated in fp32.  A row whose every key is hidden gives
+ * NaN outputs and lse = -inf (the definition's 0/0).
+ * Errors: null pointers, B, NH or T < 0, causal outside {0, 1}, a non-finite
+ * sm_scale, misaligned pointers -> CE_ERR_INVALID_ARG; D not 64 or 128, or T
+ * or B*NH above 2^31-1 -> CE_ERR_UNSUPPORTED.
+ */
+ce_status ce_attention_forward(const void* q, const void* k, const void* v, const float* mask,
+                               int causal, int64_t B, int64_t NH, int64_t T, int64_t D,
+                               float sm_scale, float* out, float* lse, void* stream);
+
+/*
  * ce_check_errors -- wait (at most timeout_ms) for `stream` to drain, then
  * read and clear the current device's error word.  Returns CE_OK,
  * CE_ERR_TARGET_RANGE (some target was outside [0, V)), CE_ERR_TIMEOUT (the

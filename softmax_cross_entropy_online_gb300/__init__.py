@@ -12,7 +12,8 @@ __all__ = [
     "ce_forward", "ce_fwd_bwd_inplace", "ce_fwd_bwd_inplace_noalloc", "ce_backward_from_lse",
     "ce_check_errors",
     "ce_max_vocab", "ce_launch_count", "ce_selftest_wait_timeout", "CEError",
-    "linear_ce_fwd_bwd", "linear_ce_workspace_size", "ce_gemm_bf16_tn", "ce_softmax_forward",
+    "linear_ce_fwd_bwd", "linear_ce_workspace_size", "ce_gemm_bf16_tn", "ce_gemm_bf16",
+    "ce_softmax_forward", "ce_attention_forward",
 ]
 
 

@@ -37,6 +37,10 @@ ce_status gemm_bf16(const void* A, long long lda, bool a_mn, const void* B, long
                     cudaStream_t stream, unsigned int* err, int sm_count,
                     unsigned int wait_hint_ns);
 ce_status launch_mean_rows(const float* rl, long long M, float* loss, cudaStream_t st);
+ce_status attention_forward(const void* Q, const void* K, const void* V, const float* mask,
+                            int causal, int BH, int T, int D, float sm_scale, float* O, float* lse,
+                            cudaStream_t stream, unsigned int* err, int sm_count,
+                            unsigned int wait_hint_ns);
 }  // namespace ce
 
 namespace ce {
@@ -737,6 +741,32 @@ ce_status ce_gemm_bf16(const void* A, int64_t lda, int a_mn, const void* B, int6
   st = ce::gemm_bf16(A, lda, a_mn != 0, B, ldb, b_mn != 0, D, ldd, static_cast<int>(M),
                      static_cast<int>(N), static_cast<int>(K), beta,
                      static_cast<cudaStream_t>(stream), di.err, di.sm_count, wait_hint_ns());
+  if (st == CE_OK) g_launches.fetch_add(1, std::memory_order_relaxed);
+  return st;
+}
+
+ce_status ce_attention_forward(const void* q, const void* k, const void* v, const float* mask,
+                               int causal, int64_t B, int64_t NH, int64_t T, int64_t D,
+                               float sm_scale, float* out, float* lse, void* stream) {
+  if (B < 0 || NH < 0 || T < 0 || (causal != 0 && causal != 1) || !std::isfinite(sm_scale))
+    return CE_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return CE_ERR_UNSUPPORTED;
+  const int64_t BH = B * NH;
+  if (BH == 0 || T == 0) return CE_OK;
+  if (q == nullptr || k == nullptr || v == nullptr || out == nullptr) return CE_ERR_INVALID_ARG;
+  if (T > INT32_MAX || BH > INT32_MAX || (B > 0 && BH / B != NH)) return CE_ERR_UNSUPPORTED;
+  auto mis = [](const void* ptr, uintptr_t a) { return reinterpret_cast<uintptr_t>(ptr) % a != 0; };
+  if (mis(q, 16) || mis(k, 16) || mis(v, 16) || mis(out, 16) || (mask && mis(mask, 4)) ||
+      (lse && mis(lse, 4)))
+    return CE_ERR_INVALID_ARG;
+  DeviceInfo di;
+  int dev = 0;
+  ce_status st = device_info(di, &dev);
+  if (st != CE_OK) return st;
+  st = ce::attention_forward(q, k, v, mask, causal, static_cast<int>(BH), static_cast<int>(T),
+                             static_cast<int>(D), sm_scale, out, lse,
+                             static_cast<cudaStream_t>(stream), di.err, di.sm_count,
+                             wait_hint_ns());
   if (st == CE_OK) g_launches.fetch_add(1, std::memory_order_relaxed);
   return st;
 }

@@ -1,0 +1,470 @@
+// ce_attention.cu -- the blockwise attention forward on the tcgen05 tensor
+// cores of sm_103a: the workload of "How to optimize an existing Triton Kernel
+// to make it faster?" (Triton discussion #8261), whose flash-attention-2
+// listing keeps, per query row, a running max and a running normaliser over
+// blocks of keys and rescales the output accumulator when the max grows --
+// the same online (max, sum) pair as the cross-entropy rows.  For Q, K, V of
+// shape [B * NH, T, D] (bf16), an optional additive mask [T, T] and/or the
+// causal mask, and sm_scale:
+//
+//     O = softmax(Q K^T * sm_scale + mask) V        (fp32)
+//     lse_i = log sum_j exp(S_ij)                    (fp32, optional)
+//
+// Design (persistent, one CTA per SM, 192 threads; a work item is 128 query
+// rows of one head):
+//  * warp 0 (one thread) loads the item's Q tile and streams K and V tiles of
+//    128 keys into a two-stage ring with TMA (128-byte swizzle; K K-major for
+//    S = Q K^T, V MN-major for O = P V, so neither is transposed);
+//  * warp 1 allocates 512 TMEM columns -- two 128 x 128 fp32 score buffers
+//    and the D-column output accumulator -- and one thread issues the MMAs:
+//    S_{j+1} = Q K_{j+1}^T is issued before O += P_j V_j, so the tensor cores
+//    compute the next scores while the softmax warps work on these;
+//  * warps 2..5 own one query row per thread (TMEM lane = row): from S_j they
+//    take the row max, the correction alpha = 2^(m_old - m_new), rescale the
+//    row of O in TMEM when some alpha != 1 (after the previous O += P V has
+//    finished), write P = 2^(s - m_new) as bf16 into a 128-byte swizzled
+//    shared tile (the K-major A operand of O += P V), and keep the running
+//    normaliser l = alpha l + sum P in fp32.  At the end of the item they
+//    divide O by l and store it through shared memory with TMA tensor stores
+//    (rows past T are clipped by the tensor map), and write lse.
+//  * exp is exp2 of the score in log2 units: s * sm_scale * log2(e).
+// Every mbarrier wait is bounded; TMEM is freed on every path.
+#include <cstring>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "../../include/ce_gb300.h"
+#include "ce_rows.cuh"
+#include "ce_tc.cuh"
+
+namespace ce {
+
+constexpr int kAttBQ = 128;  // query rows of a work item
+constexpr int kAttBK = 128;  // keys of a tile
+constexpr int kAttThreads = 192;
+constexpr uint32_t kAttTmemCols = 512;  // S0 [0, 128), S1 [128, 256), O [256, 256 + D)
+
+struct AttnParams {
+  const float* mask;   // [T, T] additive, or null
+  float* lse;          // [BH, T], or null
+  int T, BH;
+  int causal;          // 1: keys after the query are masked (and their tiles skipped)
+  float scale_log2;    // sm_scale * log2(e)
+  int q_tiles;         // ceil(T / 128)
+  int n_items;         // BH * q_tiles
+  unsigned int* err;
+  unsigned int wait_hint_ns;
+};
+
+template <int D>
+struct AttnSmem {
+  static constexpr int kQ = kAttBQ * D * 2;       // Q: D / 64 K-major blocks of 128 rows x 128 B
+  static constexpr int kK = kAttBK * D * 2;       // K: the same layout
+  static constexpr int kV = kAttBK * D * 2;       // V: D / 64 MN-major blocks of 128 keys x 128 B
+  static constexpr int kStage = kK + kV;
+  static constexpr int kP = kAttBQ * kAttBK * 2;  // P: 2 K-major blocks of 128 rows x 128 B
+  static constexpr int kTotal = kQ + 2 * kStage + kP + 1024;  // + alignment slack
+};
+
+__device__ __forceinline__ uint4 pack8_bf16(const float* v) {
+  uint4 w;
+  __nv_bfloat162 h0 = __floats2bfloat162_rn(v[0], v[1]), h1 = __floats2bfloat162_rn(v[2], v[3]);
+  __nv_bfloat162 h2 = __floats2bfloat162_rn(v[4], v[5]), h3 = __floats2bfloat162_rn(v[6], v[7]);
+  w.x = *reinterpret_cast<uint32_t*>(&h0);
+  w.y = *reinterpret_cast<uint32_t*>(&h1);
+  w.z = *reinterpret_cast<uint32_t*>(&h2);
+  w.w = *reinterpret_cast<uint32_t*>(&h3);
+  return w;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kAttThreads, 1)
+    attention_fwd_kernel(const __grid_constant__ CUtensorMap map_q,
+                         const __grid_constant__ CUtensorMap map_k,
+                         const __grid_constant__ CUtensorMap map_v,
+                         const __grid_constant__ CUtensorMap map_o, const AttnParams p) {
+  using L = AttnSmem<D>;
+  extern __shared__ unsigned char att_smem[];
+  __shared__ __align__(8) unsigned long long q_full, q_empty, p_full, o_done, o_free;
+  __shared__ __align__(8) unsigned long long kv_full[2], kv_empty[2], s_full[2], s_free[2];
+  __shared__ uint32_t tmem_slot;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t base = (smem_u32(att_smem) + 1023u) & ~1023u;  // swizzle atoms need 1024 B
+  const uint32_t sq = base;
+  const uint32_t skv = sq + L::kQ;
+  const uint32_t sp = skv + 2 * L::kStage;
+  bool failed = false;
+  const unsigned int hint = p.wait_hint_ns;
+
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&q_full), 1);
+    mbar_init(smem_u32(&q_empty), 1);
+    mbar_init(smem_u32(&p_full), 128);
+    mbar_init(smem_u32(&o_done), 1);
+    mbar_init(smem_u32(&o_free), 128);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_u32(&kv_full[s]), 1);
+      mbar_init(smem_u32(&kv_empty[s]), 1);
+      mbar_init(smem_u32(&s_full[s]), 1);
+      mbar_init(smem_u32(&s_free[s]), 128);
+    }
+    fence_mbar_init_cluster();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&tmem_slot)),
+                 "r"(kAttTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+
+  // work item w: head bh, query tile qt; the causal items with the most key
+  // tiles come first so the persistent grid ends evenly
+  auto item_of = [&](int w, int& bh, int& qt) {
+    bh = w % p.BH;
+    qt = p.q_tiles - 1 - w / p.BH;
+  };
+  auto tiles_of = [&](int qt) {
+    const int kv_end = p.causal ? min(p.T, (qt + 1) * kAttBQ) : p.T;
+    return (kv_end + kAttBK - 1) / kAttBK;
+  };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer ----------------
+      long long g = 0;  // key tiles loaded, over all items
+      int it = 0;
+      for (int w = blockIdx.x; w < p.n_items; w += gridDim.x, ++it) {
+        int bh, qt;
+        item_of(w, bh, qt);
+        const int n = tiles_of(qt);
+        // the previous item's score MMAs have read its Q
+        if (it > 0)
+          mbar_wait<false>(smem_u32(&q_empty), static_cast<uint32_t>((it - 1) & 1), p.err, failed,
+                           WAIT_LIMIT_NS, hint);
+        mbar_arrive_expect_tx(smem_u32(&q_full), L::kQ);
+        for (int kb = 0; kb < D / 64; ++kb)
+          tma_load_3d(sq + kb * 16384, &map_q, 64 * kb, qt * kAttBQ, bh, smem_u32(&q_full));
+        for (int j = 0; j < n; ++j, ++g) {
+          const int st = static_cast<int>(g & 1);
+          if (g >= 2)
+            mbar_wait<false>(smem_u32(&kv_empty[st]), static_cast<uint32_t>(((g >> 1) - 1) & 1),
+                             p.err, failed, WAIT_LIMIT_NS, hint);
+          const uint32_t sk = skv + st * L::kStage;
+          const uint32_t sv = sk + L::kK;
+          const uint32_t fb = smem_u32(&kv_full[st]);
+          mbar_arrive_expect_tx(fb, L::kStage);
+          for (int kb = 0; kb < D / 64; ++kb)
+            tma_load_3d(sk + kb * 16384, &map_k, 64 * kb, j * kAttBK, bh, fb);
+          for (int db = 0; db < D / 64; ++db)
+            for (int kh = 0; kh < 2; ++kh)
+              tma_load_3d(sv + db * 16384 + kh * 8192, &map_v, 64 * db, j * kAttBK + 64 * kh, bh,
+                          fb);
+        }
+      }
+      // drain: no copy into this CTA's shared memory is in flight when it exits
+      // (the MMA thread has waited on these phases already unless a wait failed)
+      bool drain_failed = false;
+      if (it > 0)
+        mbar_wait<false>(smem_u32(&q_full), static_cast<uint32_t>((it - 1) & 1), p.err,
+                         drain_failed, WAIT_LIMIT_NS, hint);
+      for (long long t = g - 2 < 0 ? 0 : g - 2; t < g; ++t)
+        mbar_wait<false>(smem_u32(&kv_full[t & 1]), static_cast<uint32_t>((t >> 1) & 1), p.err,
+                         drain_failed, WAIT_LIMIT_NS, hint);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer ----------------
+      // S = Q K^T: M = 128 queries, N = 128 keys, both operands K-major (K = D)
+      constexpr uint32_t idesc_s = (1u << 4) | (1u << 7) | (1u << 10) | ((128u >> 3) << 17) |
+                                   ((128u >> 4) << 24);
+      // O += P V: M = 128 queries, N = D, A = P K-major (K = keys), B = V MN-major
+      constexpr uint32_t idesc_o = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) |
+                                   ((static_cast<uint32_t>(D) >> 3) << 17) | ((128u >> 4) << 24);
+      long long g = 0;   // score tiles issued, over all items
+      long long gp = 0;  // P V tiles issued, over all items
+      int it = 0;
+      auto issue_s = [&](long long gs) {
+        const int st = static_cast<int>(gs & 1);  // key stage and score buffer alternate alike
+        mbar_wait<false>(smem_u32(&kv_full[st]), static_cast<uint32_t>((gs >> 1) & 1), p.err,
+                         failed, WAIT_LIMIT_NS, hint);
+        if (gs >= 2)
+          mbar_wait<false>(smem_u32(&s_free[st]), static_cast<uint32_t>(((gs >> 1) - 1) & 1),
+                           p.err, failed, WAIT_LIMIT_NS, hint);
+        tc_fence_after();
+        const uint32_t sk = skv + st * L::kStage;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          umma_bf16(tmem + st * 128, smem_desc_sw128(sq + off), smem_desc_sw128(sk + off), idesc_s,
+                    kk > 0 ? 1u : 0u);
+        }
+        umma_commit(smem_u32(&s_full[st]));
+      };
+      for (int w = blockIdx.x; w < p.n_items; w += gridDim.x, ++it) {
+        int bh, qt;
+        item_of(w, bh, qt);
+        const int n = tiles_of(qt);
+        mbar_wait<false>(smem_u32(&q_full), static_cast<uint32_t>(it & 1), p.err, failed,
+                         WAIT_LIMIT_NS, hint);
+        tc_fence_after();
+        issue_s(g++);
+        for (int j = 0; j < n; ++j) {
+          if (j + 1 < n) issue_s(g++);
+          if (j + 1 == n) umma_commit(smem_u32(&q_empty));  // every MMA reading Q is issued
+          // the previous item's output has been read out of TMEM
+          if (j == 0 && it > 0)
+            mbar_wait<false>(smem_u32(&o_free), static_cast<uint32_t>((it - 1) & 1), p.err, failed,
+                             WAIT_LIMIT_NS, hint);
+          mbar_wait<false>(smem_u32(&p_full), static_cast<uint32_t>(gp & 1), p.err, failed,
+                           WAIT_LIMIT_NS, hint);
+          tc_fence_after();
+          const int st = static_cast<int>(gp & 1);
+          const uint32_t sv = skv + st * L::kStage + L::kK;
+#pragma unroll
+          for (int kk = 0; kk < kAttBK / 16; ++kk) {
+            const uint32_t pa = sp + (kk >> 2) * 16384 + (kk & 3) * 32;
+            // V: 64-wide D blocks 128 keys x 128 B = 16 KB apart, 16 keys = 2 KB
+            umma_bf16(tmem + 256, smem_desc_sw128(pa), smem_desc_sw128_mn(sv + kk * 2048, 16384),
+                      idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(smem_u32(&o_done));
+          umma_commit(smem_u32(&kv_empty[st]));
+          ++gp;
+        }
+      }
+      // drain: every MMA has finished before TMEM is released
+      bool drain_failed = false;
+      if (gp > 0)
+        mbar_wait<false>(smem_u32(&o_done), static_cast<uint32_t>((gp - 1) & 1), p.err,
+                         drain_failed, WAIT_LIMIT_NS, hint);
+    }
+  } else {
+    // ---------------- softmax warps 2..5: one query row per thread ----------------
+    const int q = warp & 3;  // the TMEM lane quarter this warp may access
+    const int r = 32 * q + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(32 * q) << 16;
+    const uint32_t ebuf = sp + q * 4096;  // this warp's output staging block (inside P)
+    long long g = 0;                       // score tiles consumed, over all items
+    int it = 0;
+    for (int w = blockIdx.x; w < p.n_items; w += gridDim.x, ++it) {
+      int bh, qt;
+      item_of(w, bh, qt);
+      const int n = tiles_of(qt);
+      const int row = qt * kAttBQ + r;
+      const bool row_ok = row < p.T;
+      const float* mrow = (p.mask != nullptr && row_ok) ? p.mask + static_cast<long long>(row) * p.T
+                                                        : nullptr;
+      // score of key kv in log2 units; -inf where masked or past T
+      auto score = [&](float x, int kv) -> float {
+        if (kv >= p.T || (p.causal && kv > row)) return -INFINITY;
+        float y = x * p.scale_log2;
+        if (mrow != nullptr) y = fmaf(__ldg(mrow + kv), kLog2e, y);
+        return y;
+      };
+      float m = -INFINITY;  // running max (log2 units)
+      float l = 0.f;        // running normaliser
+      for (int j = 0; j < n; ++j, ++g) {
+        const int st = static_cast<int>(g & 1);
+        mbar_wait<false>(smem_u32(&s_full[st]), static_cast<uint32_t>((g >> 1) & 1), p.err,
+                         failed, WAIT_LIMIT_NS, hint);
+        tc_fence_after();
+        const uint32_t ts = tmem + st * 128 + lane_off;
+        const int kv0 = j * kAttBK;
+        float mx = -INFINITY;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          float x[32];
+          tmem_ld32(ts + 32 * c, x);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) mx = fmaxf(mx, score(x[i], kv0 + 32 * c + i));
+        }
+        const float m_new = fmaxf(m, mx);
+        const float ref = (m_new == -INFINITY) ? 0.f : m_new;
+        const float alpha = (m == -INFINITY) ? 0.f : ex2(m - ref);
+        if (j > 0) {
+          // the previous O += P V is done: O may be rescaled and P rewritten
+          mbar_wait<false>(smem_u32(&o_done), static_cast<uint32_t>((g - 1) & 1), p.err, failed,
+                           WAIT_LIMIT_NS, hint);
+          tc_fence_after();
+          if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+            for (int cc = 0; cc < D / 32; ++cc) {
+              float o[32];
+              tmem_ld32(tmem + 256 + 32 * cc + lane_off, o);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) o[i] *= alpha;
+              tmem_st32(tmem + 256 + 32 * cc + lane_off, o);
+            }
+          }
+        } else if (it > 0) {
+          // P doubles as the previous item's output staging: its stores have read it
+          if (lane == 0) bulk_wait_read<0>();
+          __syncwarp();
+        }
+        float sum = 0.f;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          float x[32];
+          tmem_ld32(ts + 32 * c, x);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            x[i] = ex2(score(x[i], kv0 + 32 * c + i) - ref);
+            sum += x[i];
+          }
+          // keys 32c .. 32c + 31 of row r: K-block (32c / 64), 16-byte chunks
+          // ((32c % 64) / 8 + u) at chunk ^ (r % 8) -- the 128-byte swizzle
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int kk = 32 * c + 8 * u;
+            const uint32_t addr = sp + (kk >> 6) * 16384 + r * 128 + 16 * (((kk & 63) >> 3) ^ (r & 7));
+            sts128(addr, pack8_bf16(x + 8 * u));
+          }
+        }
+        l = fmaf(l, alpha, sum);
+        m = m_new;
+        fence_proxy_async_smem();  // P is read by the tensor cores (async proxy)
+        tc_fence_before();
+        mbar_arrive(smem_u32(&p_full));
+        mbar_arrive(smem_u32(&s_free[st]));
+      }
+      // ---- the item's output: O / l through shared memory and TMA ----
+      mbar_wait<false>(smem_u32(&o_done), static_cast<uint32_t>((g - 1) & 1), p.err, failed,
+                       WAIT_LIMIT_NS, hint);
+      tc_fence_after();
+      if (p.lse != nullptr && row_ok) {
+        const float mref = (m == -INFINITY) ? 0.f : m;
+        p.lse[static_cast<long long>(bh) * p.T + row] = (mref + lg2(l)) * 0.6931471805599453f;
+      }
+      const float inv_l = 1.f / l;
+#pragma unroll 1
+      for (int cc = 0; cc < D / 32; ++cc) {
+        float o[32];
+        tmem_ld32(tmem + 256 + 32 * cc + lane_off, o);
+        if (cc > 0) {
+          if (lane == 0) bulk_wait_read<0>();
+          __syncwarp();
+        }
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj)
+          asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(
+                           ebuf + lane * 128 + 16 * (jj ^ (lane & 7))),
+                       "f"(o[4 * jj] * inv_l), "f"(o[4 * jj + 1] * inv_l),
+                       "f"(o[4 * jj + 2] * inv_l), "f"(o[4 * jj + 3] * inv_l)
+                       : "memory");
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && qt * kAttBQ + 32 * q < p.T) {  // blocks wholly past T are not stored
+          tma_store_3d(&map_o, ebuf, 32 * cc, qt * kAttBQ + 32 * q, bh);
+          bulk_commit();
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(smem_u32(&o_free));
+    }
+    // no CTA exits while a TMA store still reads its shared memory
+    if (lane == 0) bulk_wait_all();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kAttTmemCols)
+                 : "memory");
+  }
+}
+
+// --- host side ---------------------------------------------------------------
+static PFN_cuTensorMapEncodeTiled_v12000 att_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }
+  return fn;
+}
+
+// 3-D map over [BH, T, D] (D contiguous) with a box of box_d x box_t x 1
+static bool att_map(CUtensorMap* map, CUtensorMapDataType type, int esize, const void* base,
+                    int BH, int T, int D, int box_d, int box_t) {
+  auto fn = att_encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(T),
+                        static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * esize,
+                           static_cast<cuuint64_t>(T) * D * esize};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(box_d), static_cast<cuuint32_t>(box_t), 1u};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, type, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D>
+static ce_status attention_launch(const void* Q, const void* K, const void* V, const float* mask,
+                                  int causal, int BH, int T, float sm_scale, float* O, float* lse,
+                                  cudaStream_t stream, unsigned int* err, int sm_count,
+                                  unsigned int wait_hint_ns) {
+  CUtensorMap mq, mk, mv, mo;
+  if (!att_map(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Q, BH, T, D, 64, kAttBQ) ||
+      !att_map(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, BH, T, D, 64, kAttBK) ||
+      !att_map(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, V, BH, T, D, 64, 64) ||
+      !att_map(&mo, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, O, BH, T, D, 32, 32))
+    return CE_ERR_CUDA;
+  AttnParams p;
+  p.mask = mask;
+  p.lse = lse;
+  p.T = T;
+  p.BH = BH;
+  p.causal = causal;
+  p.scale_log2 = sm_scale * kLog2e;
+  p.q_tiles = (T + kAttBQ - 1) / kAttBQ;
+  p.n_items = BH * p.q_tiles;
+  p.err = err;
+  p.wait_hint_ns = wait_hint_ns;
+  if (BH == 0 || T == 0) return CE_OK;
+  // 512 TMEM columns per CTA: the shared-memory request keeps one CTA per SM,
+  // so no CTA ever waits in tcgen05.alloc for a neighbour to finish
+  const int smem = AttnSmem<D>::kTotal > (128 << 10) ? AttnSmem<D>::kTotal : (128 << 10);
+  if (cudaFuncSetAttribute(attention_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           smem) != cudaSuccess)
+    return CE_ERR_CUDA;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attention_fwd_kernel<D>, kAttThreads,
+                                                    smem) != cudaSuccess ||
+      per_sm < 1)
+    return CE_ERR_CUDA;
+  if (per_sm != 1) return CE_ERR_UNSUPPORTED;
+  long long grid = sm_count;
+  if (grid > p.n_items) grid = p.n_items;
+  attention_fwd_kernel<D><<<static_cast<int>(grid), kAttThreads, smem, stream>>>(mq, mk, mv, mo, p);
+  return cudaGetLastError() == cudaSuccess ? CE_OK : CE_ERR_CUDA;
+}
+
+ce_status attention_forward(const void* Q, const void* K, const void* V, const float* mask,
+                            int causal, int BH, int T, int D, float sm_scale, float* O, float* lse,
+                            cudaStream_t stream, unsigned int* err, int sm_count,
+                            unsigned int wait_hint_ns) {
+  if (D == 64)
+    return attention_launch<64>(Q, K, V, mask, causal, BH, T, sm_scale, O, lse, stream, err,
+                                sm_count, wait_hint_ns);
+  if (D == 128)
+    return attention_launch<128>(Q, K, V, mask, causal, BH, T, sm_scale, O, lse, stream, err,
+                                 sm_count, wait_hint_ns);
+  return CE_ERR_UNSUPPORTED;
+}
+
+}  // namespace ce

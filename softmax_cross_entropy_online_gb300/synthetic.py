@@ -135,3 +135,31 @@ def make_linear_ce_inputs(M: int, H: int, V: int, seed: int = 0):
                                     * np.float32(0.02))
     t = gt.integers(0, V, size=M, dtype=np.int64)
     return h, W, t
+
+
+def make_attention_inputs(B: int, NH: int, T: int, D: int, seed: int = 0,
+                          q_sigma: float = 1.0):
+    """Queries, keys and values [B, NH, T, D] ~ N(0, 1) (queries N(0, q_sigma^2)),
+    the distribution of the flash-attention page's harness; bf16 bit patterns."""
+    gq, gk, gv = (np.random.Generator(np.random.PCG64(s))
+                  for s in np.random.SeedSequence(seed).spawn(3))
+    shape = (B, NH, T, D)
+    q = gq.standard_normal(shape, dtype=np.float32)
+    if q_sigma != 1.0:
+        q *= np.float32(q_sigma)
+    return (f32_to_bf16_bits(q), f32_to_bf16_bits(gk.standard_normal(shape, dtype=np.float32)),
+            f32_to_bf16_bits(gv.standard_normal(shape, dtype=np.float32)))
+
+
+def make_attention_mask(T: int, seed: int = 0, sigma: float = 1.0,
+                        hide_prob: float = 0.0) -> np.ndarray:
+    """An additive fp32 mask [T, T] ~ N(0, sigma^2) whose off-diagonal entries
+    are -inf with probability `hide_prob` (the diagonal stays finite, so every
+    query sees at least one key)."""
+    g = np.random.Generator(np.random.PCG64(np.random.SeedSequence(seed).spawn(2)[1]))
+    m = g.standard_normal((T, T), dtype=np.float32) * np.float32(sigma)
+    if hide_prob > 0.0:
+        hide = g.random((T, T), dtype=np.float32) < np.float32(hide_prob)
+        np.fill_diagonal(hide, False)
+        m[hide] = -np.inf
+    return m
