@@ -225,15 +225,17 @@ ce_status ce_gemm_bf16_tn(const void* A, int64_t lda, const void* B, int64_t ldb
  *            a key.  Combined with causal it is added before the causal mask.
  *   causal   1: key j is hidden from query i when j > i (and the key blocks
  *            wholly above the diagonal are skipped); 0: no causal mask.
- *   sm_scale the score scale (the page uses 1/sqrt(D)); finite.
+ *   sm_scale the score scale (the page uses 1/sqrt(D)); positive, with a finite
+ *            reciprocal (a mask entry enters as mask / sm_scale on the unscaled
+ *            score, so finite entries must stay below 2^127 sm_scale in size).
  *   out      [B, NH, T, D] fp32, 16-byte aligned (device, caller-owned).
  *   lse      [B, NH, T] fp32 (device) or NULL.
  * Arithmetic: bf16 products with fp32 accumulation for Q K^T; the softmax in
  * fp32 (exponentials in base 2 of the score times log2(e)); P is rounded to
  * bf16 for P V, accumulated in fp32.  A row whose every key is hidden gives
  * NaN outputs and lse = -inf (the definition's 0/0).
- * Errors: null pointers, B, NH or T < 0, causal outside {0, 1}, a non-finite
- * sm_scale, misaligned pointers -> CE_ERR_INVALID_ARG; D not 64 or 128, or T
+ * Errors: null pointers, B, NH or T < 0, causal outside {0, 1}, sm_scale not
+ * positive with a finite reciprocal, misaligned pointers -> CE_ERR_INVALID_ARG; D not 64 or 128, or T
  * or B*NH above 2^31-1 -> CE_ERR_UNSUPPORTED.
  */
 ce_status ce_attention_forward(const void* q, const void* k, const void* v, const float* mask,

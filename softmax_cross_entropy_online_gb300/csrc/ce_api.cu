@@ -748,7 +748,8 @@ ce_status ce_gemm_bf16(const void* A, int64_t lda, int a_mn, const void* B, int6
 ce_status ce_attention_forward(const void* q, const void* k, const void* v, const float* mask,
                                int causal, int64_t B, int64_t NH, int64_t T, int64_t D,
                                float sm_scale, float* out, float* lse, void* stream) {
-  if (B < 0 || NH < 0 || T < 0 || (causal != 0 && causal != 1) || !std::isfinite(sm_scale))
+  if (B < 0 || NH < 0 || T < 0 || (causal != 0 && causal != 1) || !std::isfinite(sm_scale) ||
+      !(sm_scale > 0.f) || !std::isfinite(1.f / sm_scale))
     return CE_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return CE_ERR_UNSUPPORTED;
   const int64_t BH = B * NH;

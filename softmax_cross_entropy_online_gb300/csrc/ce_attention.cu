@@ -51,6 +51,7 @@ struct AttnParams {
   int T, BH;
   int causal;          // 1: keys after the query are masked (and their tiles skipped)
   float scale_log2;    // sm_scale * log2(e)
+  float inv_scale;     // 1 / sm_scale: a mask entry in units of the unscaled score
   int q_tiles;         // ceil(T / 128)
   int n_items;         // BH * q_tiles
   unsigned int* err;
@@ -64,8 +65,13 @@ struct AttnSmem {
   static constexpr int kV = kAttBK * D * 2;       // V: D / 64 MN-major blocks of 128 keys x 128 B
   static constexpr int kStage = kK + kV;
   static constexpr int kP = kAttBQ * kAttBK * 2;  // P: 2 K-major blocks of 128 rows x 128 B
-  static constexpr int kTotal = kQ + 2 * kStage + kP + 1024;  // + alignment slack
+  static constexpr int kTotal = kQ + 2 * kStage + 2 * kP + 1024;  // + alignment slack
 };
+
+// The reference max of a row moves only when a tile's max exceeds it by more
+// than this (log2 units): until then the weights 2^(y - ref) stay below 2^8,
+// exact enough in fp32 and bf16, and the accumulator is not rescaled.
+constexpr float kRescaleLog2 = 8.f;
 
 __device__ __forceinline__ uint4 pack8_bf16(const float* v) {
   uint4 w;
@@ -86,8 +92,9 @@ __global__ void __launch_bounds__(kAttThreads, 1)
                          const __grid_constant__ CUtensorMap map_o, const AttnParams p) {
   using L = AttnSmem<D>;
   extern __shared__ unsigned char att_smem[];
-  __shared__ __align__(8) unsigned long long q_full, q_empty, p_full, o_done, o_free;
+  __shared__ __align__(8) unsigned long long q_full, q_empty, o_free;
   __shared__ __align__(8) unsigned long long kv_full[2], kv_empty[2], s_full[2], s_free[2];
+  __shared__ __align__(8) unsigned long long p_full[2], pv_done[2];
   __shared__ uint32_t tmem_slot;
 
   const int warp = threadIdx.x >> 5;
@@ -95,21 +102,21 @@ __global__ void __launch_bounds__(kAttThreads, 1)
   const uint32_t base = (smem_u32(att_smem) + 1023u) & ~1023u;  // swizzle atoms need 1024 B
   const uint32_t sq = base;
   const uint32_t skv = sq + L::kQ;
-  const uint32_t sp = skv + 2 * L::kStage;
+  const uint32_t sp = skv + 2 * L::kStage;  // two P buffers
   bool failed = false;
   const unsigned int hint = p.wait_hint_ns;
 
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&q_full), 1);
     mbar_init(smem_u32(&q_empty), 1);
-    mbar_init(smem_u32(&p_full), 128);
-    mbar_init(smem_u32(&o_done), 1);
     mbar_init(smem_u32(&o_free), 128);
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&kv_full[s]), 1);
       mbar_init(smem_u32(&kv_empty[s]), 1);
       mbar_init(smem_u32(&s_full[s]), 1);
       mbar_init(smem_u32(&s_free[s]), 128);
+      mbar_init(smem_u32(&p_full[s]), 128);
+      mbar_init(smem_u32(&pv_done[s]), 1);
     }
     fence_mbar_init_cluster();
   }
@@ -223,36 +230,43 @@ __global__ void __launch_bounds__(kAttThreads, 1)
           if (j == 0 && it > 0)
             mbar_wait<false>(smem_u32(&o_free), static_cast<uint32_t>((it - 1) & 1), p.err, failed,
                              WAIT_LIMIT_NS, hint);
-          mbar_wait<false>(smem_u32(&p_full), static_cast<uint32_t>(gp & 1), p.err, failed,
-                           WAIT_LIMIT_NS, hint);
+          const int pb = static_cast<int>(gp & 1);  // P buffer, and the K/V stage of this tile
+          mbar_wait<false>(smem_u32(&p_full[pb]), static_cast<uint32_t>((gp >> 1) & 1), p.err,
+                           failed, WAIT_LIMIT_NS, hint);
           tc_fence_after();
-          const int st = static_cast<int>(gp & 1);
-          const uint32_t sv = skv + st * L::kStage + L::kK;
+          const uint32_t sv = skv + pb * L::kStage + L::kK;
+          const uint32_t pbase = sp + pb * L::kP;
 #pragma unroll
           for (int kk = 0; kk < kAttBK / 16; ++kk) {
-            const uint32_t pa = sp + (kk >> 2) * 16384 + (kk & 3) * 32;
+            const uint32_t pa = pbase + (kk >> 2) * 16384 + (kk & 3) * 32;
             // V: 64-wide D blocks 128 keys x 128 B = 16 KB apart, 16 keys = 2 KB
             umma_bf16(tmem + 256, smem_desc_sw128(pa), smem_desc_sw128_mn(sv + kk * 2048, 16384),
                       idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
           }
-          umma_commit(smem_u32(&o_done));
-          umma_commit(smem_u32(&kv_empty[st]));
+          umma_commit(smem_u32(&pv_done[pb]));
+          umma_commit(smem_u32(&kv_empty[pb]));
           ++gp;
         }
       }
       // drain: every MMA has finished before TMEM is released
       bool drain_failed = false;
       if (gp > 0)
-        mbar_wait<false>(smem_u32(&o_done), static_cast<uint32_t>((gp - 1) & 1), p.err,
-                         drain_failed, WAIT_LIMIT_NS, hint);
+        mbar_wait<false>(smem_u32(&pv_done[(gp - 1) & 1]), static_cast<uint32_t>(((gp - 1) >> 1) & 1),
+                         p.err, drain_failed, WAIT_LIMIT_NS, hint);
     }
   } else {
     // ---------------- softmax warps 2..5: one query row per thread ----------------
     const int q = warp & 3;  // the TMEM lane quarter this warp may access
     const int r = 32 * q + lane;
     const uint32_t lane_off = static_cast<uint32_t>(32 * q) << 16;
-    const uint32_t ebuf = sp + q * 4096;  // this warp's output staging block (inside P)
-    long long g = 0;                       // score tiles consumed, over all items
+    const uint32_t ebuf = sp + q * 4096;  // this warp's output staging block (inside P buffer 0)
+    const float c = p.scale_log2;          // > 0: the max of s * c is c * max(s)
+    // wait until P V of global tile t has finished
+    auto wait_pv = [&](long long t) {
+      mbar_wait<false>(smem_u32(&pv_done[t & 1]), static_cast<uint32_t>((t >> 1) & 1), p.err,
+                       failed, WAIT_LIMIT_NS, hint);
+    };
+    long long g = 0;  // score tiles consumed, over all items
     int it = 0;
     for (int w = blockIdx.x; w < p.n_items; w += gridDim.x, ++it) {
       int bh, qt;
@@ -262,85 +276,106 @@ __global__ void __launch_bounds__(kAttThreads, 1)
       const bool row_ok = row < p.T;
       const float* mrow = (p.mask != nullptr && row_ok) ? p.mask + static_cast<long long>(row) * p.T
                                                         : nullptr;
-      // score of key kv in log2 units; -inf where masked or past T
-      auto score = [&](float x, int kv) -> float {
-        if (kv >= p.T || (p.causal && kv > row)) return -INFINITY;
-        float y = x * p.scale_log2;
-        if (mrow != nullptr) y = fmaf(__ldg(mrow + kv), kLog2e, y);
-        return y;
-      };
-      float m = -INFINITY;  // running max (log2 units)
-      float l = 0.f;        // running normaliser
+      float m_ref = -INFINITY;  // reference max of O and l (log2 units)
+      float l = 0.f;            // running normaliser, relative to m_ref
       for (int j = 0; j < n; ++j, ++g) {
         const int st = static_cast<int>(g & 1);
         mbar_wait<false>(smem_u32(&s_full[st]), static_cast<uint32_t>((g >> 1) & 1), p.err,
                          failed, WAIT_LIMIT_NS, hint);
         tc_fence_after();
+        uint32_t sr[128];
         const uint32_t ts = tmem + st * 128 + lane_off;
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) tmem_ld32_nowait(ts + 32 * c4, sr + 32 * c4);
+        tmem_wait_ld<128>(sr);
+        // the scores are in registers: the buffer may take the next tile's scores
+        tc_fence_before();
+        mbar_arrive(smem_u32(&s_free[st]));
+        float* x = reinterpret_cast<float*>(sr);
         const int kv0 = j * kAttBK;
-        float mx = -INFINITY;
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          float x[32];
-          tmem_ld32(ts + 32 * c, x);
+        // one decision for the whole CTA: does any key of this tile need a mask?
+        const bool masked =
+            p.mask != nullptr || kv0 + kAttBK > p.T || (p.causal && kv0 + kAttBK - 1 > qt * kAttBQ);
+        float mt;  // the tile's max (log2 units)
+        if (!masked) {
+          float mx[8];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) mx = fmaxf(mx, score(x[i], kv0 + 32 * c + i));
-        }
-        const float m_new = fmaxf(m, mx);
-        const float ref = (m_new == -INFINITY) ? 0.f : m_new;
-        const float alpha = (m == -INFINITY) ? 0.f : ex2(m - ref);
-        if (j > 0) {
-          // the previous O += P V is done: O may be rescaled and P rewritten
-          mbar_wait<false>(smem_u32(&o_done), static_cast<uint32_t>((g - 1) & 1), p.err, failed,
-                           WAIT_LIMIT_NS, hint);
-          tc_fence_after();
-          if (__any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll 1
-            for (int cc = 0; cc < D / 32; ++cc) {
-              float o[32];
-              tmem_ld32(tmem + 256 + 32 * cc + lane_off, o);
+          for (int i = 0; i < 8; ++i) mx[i] = x[i];
 #pragma unroll
-              for (int i = 0; i < 32; ++i) o[i] *= alpha;
-              tmem_st32(tmem + 256 + 32 * cc + lane_off, o);
-            }
+          for (int i = 8; i < 128; ++i) mx[i & 7] = fmaxf(mx[i & 7], x[i]);
+          mt = c * fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                         fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        } else {
+          // keys kv0 + i with i > lim are hidden (past T, or after the query);
+          // the additive mask joins the unscaled score as mask / sm_scale, so
+          // both paths share one exponent, and a zero entry changes no bit
+          const int lim = (p.causal ? min(row, p.T - 1) : p.T - 1) - kv0;
+          float mx[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
+#pragma unroll
+          for (int i = 0; i < 128; ++i) {
+            float y = x[i];
+            if (mrow != nullptr) y = fmaf(__ldg(mrow + min(kv0 + i, p.T - 1)), p.inv_scale, y);
+            x[i] = (i > lim) ? -INFINITY : y;
+            mx[i & 7] = fmaxf(mx[i & 7], x[i]);
           }
-        } else if (it > 0) {
-          // P doubles as the previous item's output staging: its stores have read it
+          mt = c * fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                         fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        }
+        if (j == 0) {
+          m_ref = mt;  // this tile's P V overwrites O
+        } else if (__any_sync(0xffffffffu, mt > m_ref + kRescaleLog2)) {
+          // move the reference: O and l are rescaled by alpha = 2^(old - new),
+          // after the previous P V has finished and before this tile's is issued
+          const float m_new = fmaxf(m_ref, mt);
+          const float alpha = (m_ref == -INFINITY) ? 0.f : ex2(m_ref - m_new);
+          wait_pv(g - 1);
+          tc_fence_after();
+#pragma unroll 1
+          for (int cc = 0; cc < D / 32; ++cc) {
+            float o[32];
+            tmem_ld32(tmem + 256 + 32 * cc + lane_off, o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] *= alpha;
+            tmem_st32(tmem + 256 + 32 * cc + lane_off, o);
+          }
+          l *= alpha;
+          m_ref = m_new;
+        }
+        const float ref = (m_ref == -INFINITY) ? 0.f : m_ref;
+        float sm[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) sm[i] = 0.f;
+#pragma unroll
+        for (int i = 0; i < 128; ++i) {
+          x[i] = ex2(fmaf(x[i], c, -ref));
+          sm[i & 7] += x[i];
+        }
+        l += ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
+        // P buffer g % 2 is free once P V of tile g - 2 has finished; at an
+        // item's first tile the previous item's output stores (staged in P
+        // buffer 0) have also read their rows
+        if (g >= 2) wait_pv(g - 2);
+        if (j == 0 && it > 0) {
           if (lane == 0) bulk_wait_read<0>();
           __syncwarp();
         }
-        float sum = 0.f;
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          float x[32];
-          tmem_ld32(ts + 32 * c, x);
+        const uint32_t pbase = sp + st * L::kP;
+        // keys 8u .. 8u + 7 of row r: K-block u / 8, 16-byte chunk (u % 8) ^ (r % 8)
+        // -- the 128-byte swizzle
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            x[i] = ex2(score(x[i], kv0 + 32 * c + i) - ref);
-            sum += x[i];
-          }
-          // keys 32c .. 32c + 31 of row r: K-block (32c / 64), 16-byte chunks
-          // ((32c % 64) / 8 + u) at chunk ^ (r % 8) -- the 128-byte swizzle
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int kk = 32 * c + 8 * u;
-            const uint32_t addr = sp + (kk >> 6) * 16384 + r * 128 + 16 * (((kk & 63) >> 3) ^ (r & 7));
-            sts128(addr, pack8_bf16(x + 8 * u));
-          }
-        }
-        l = fmaf(l, alpha, sum);
-        m = m_new;
+        for (int u = 0; u < 16; ++u)
+          sts128(pbase + (u >> 3) * 16384 + r * 128 + 16 * ((u & 7) ^ (r & 7)), pack8_bf16(x + 8 * u));
         fence_proxy_async_smem();  // P is read by the tensor cores (async proxy)
         tc_fence_before();
-        mbar_arrive(smem_u32(&p_full));
-        mbar_arrive(smem_u32(&s_free[st]));
+        mbar_arrive(smem_u32(&p_full[st]));
       }
       // ---- the item's output: O / l through shared memory and TMA ----
-      mbar_wait<false>(smem_u32(&o_done), static_cast<uint32_t>((g - 1) & 1), p.err, failed,
-                       WAIT_LIMIT_NS, hint);
+      wait_pv(g - 1);
       tc_fence_after();
       if (p.lse != nullptr && row_ok) {
-        const float mref = (m == -INFINITY) ? 0.f : m;
+        const float mref = (m_ref == -INFINITY) ? 0.f : m_ref;
         p.lse[static_cast<long long>(bh) * p.T + row] = (mref + lg2(l)) * 0.6931471805599453f;
       }
       const float inv_l = 1.f / l;
@@ -431,6 +466,7 @@ static ce_status attention_launch(const void* Q, const void* K, const void* V, c
   p.BH = BH;
   p.causal = causal;
   p.scale_log2 = sm_scale * kLog2e;
+  p.inv_scale = 1.f / sm_scale;
   p.q_tiles = (T + kAttBQ - 1) / kAttBQ;
   p.n_items = BH * p.q_tiles;
   p.err = err;

@@ -123,6 +123,9 @@ def test_product_path_never_imports_the_oracle():
     ((16, 16, 16, None, 0, 1, 1, -8, 64, 0.125, 16, None), 1),          # T < 0
     ((16, 16, 16, None, 0, 1, 1, 8, 64, float("nan"), 16, None), 1),    # sm_scale not finite
     ((16, 16, 16, None, 0, 1, 1, 8, 64, float("inf"), 16, None), 1),
+    ((16, 16, 16, None, 0, 1, 1, 8, 64, 0.0, 16, None), 1),             # sm_scale not > 0
+    ((16, 16, 16, None, 0, 1, 1, 8, 64, -0.125, 16, None), 1),
+    ((16, 16, 16, None, 0, 1, 1, 8, 64, 1e-39, 16, None), 1),           # 1 / sm_scale overflows
     ((16, 16, 16, None, 0, 1, 1, 8, 96, 0.125, 16, None), 2),           # D not 64 / 128
     ((16, 16, 16, None, 0, 1, 1, 8, 32, 0.125, 16, None), 2),
     ((None, 16, 16, None, 0, 1, 1, 8, 64, 0.125, 16, None), 1),         # null q

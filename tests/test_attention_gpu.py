@@ -4,7 +4,9 @@ inputs.
 
 Tolerances, from the arithmetic of the kernel:
   * scores: exact bf16 products summed in fp32 by the tensor cores, so
-    |S - S_ref| <= d_s = sm_scale * D * 2^-24 * max_j sum_d |q_d k_jd| per row;
+    |S - S_ref| <= d_s = sm_scale * D * 2^-24 * max_j sum_d |q_d k_jd| per row
+    (+ 2^-22 max_j |mask_ij| with an additive mask, which joins the unscaled
+    score as fma(mask, 1/sm_scale, s));
     exp turns that into a relative error of at most d_s in each weight, on
     the numerator and on the normaliser alike;
   * P is rounded to bf16 (relative 2^-9) before P V; the normaliser sums the
@@ -57,6 +59,10 @@ def check(out, lse, q, k, v, mask, sm_scale, heads=None):
         ref = AO.attention_forward(qh, kh, vh, mask, sm_scale)
         pv = AO.attention_forward(qh, kh, np.abs(vh), mask, sm_scale)["out"]
         d_s = sm_scale * D * 2.0 ** -24 * np.max(np.abs(qh) @ np.abs(kh).T, axis=1)
+        if mask is not None:
+            # the mask enters as fma(mask, 1/sm_scale, s): two more roundings
+            fin = np.where(np.isfinite(mask), np.abs(mask), 0.0)
+            d_s = d_s + 2.0 ** -22 * np.max(fin, axis=1)
         bound = (2.0 ** -8 + 2 * d_s[:, None] + T * 2.0 ** -24) * pv + 1e-6
         err = np.abs(out[h].astype(np.float64) - ref["out"])
         assert np.all(err <= bound), (
