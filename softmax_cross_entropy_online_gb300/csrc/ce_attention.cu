@@ -53,7 +53,8 @@ struct AttnParams {
   float scale_log2;    // sm_scale * log2(e)
   float inv_scale;     // 1 / sm_scale: a mask entry in units of the unscaled score
   int q_tiles;         // ceil(T / 128)
-  int n_items;         // BH * q_tiles
+  int n_pairs;         // ceil(q_tiles / 2)
+  int n_units;         // work units: BH * n_pairs (causal) or BH * q_tiles
   unsigned int* err;
   unsigned int wait_hint_ns;
 };
@@ -93,7 +94,8 @@ __global__ void __launch_bounds__(kAttThreads, 1)
   using L = AttnSmem<D>;
   extern __shared__ unsigned char att_smem[];
   __shared__ __align__(8) unsigned long long q_full, q_empty, o_free;
-  __shared__ __align__(8) unsigned long long kv_full[2], kv_empty[2], s_full[2], s_free[2];
+  __shared__ __align__(8) unsigned long long k_full[2], k_empty[2], v_full[2], v_empty[2];
+  __shared__ __align__(8) unsigned long long s_full[2], s_free[2];
   __shared__ __align__(8) unsigned long long p_full[2], pv_done[2];
   __shared__ uint32_t tmem_slot;
 
@@ -101,8 +103,9 @@ __global__ void __launch_bounds__(kAttThreads, 1)
   const int lane = threadIdx.x & 31;
   const uint32_t base = (smem_u32(att_smem) + 1023u) & ~1023u;  // swizzle atoms need 1024 B
   const uint32_t sq = base;
-  const uint32_t skv = sq + L::kQ;
-  const uint32_t sp = skv + 2 * L::kStage;  // two P buffers
+  const uint32_t sk0 = sq + L::kQ;         // two K stages
+  const uint32_t sv0 = sk0 + 2 * L::kK;     // two V stages
+  const uint32_t sp = sv0 + 2 * L::kV;      // two P buffers
   bool failed = false;
   const unsigned int hint = p.wait_hint_ns;
 
@@ -111,8 +114,10 @@ __global__ void __launch_bounds__(kAttThreads, 1)
     mbar_init(smem_u32(&q_empty), 1);
     mbar_init(smem_u32(&o_free), 128);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(smem_u32(&kv_full[s]), 1);
-      mbar_init(smem_u32(&kv_empty[s]), 1);
+      mbar_init(smem_u32(&k_full[s]), 1);
+      mbar_init(smem_u32(&k_empty[s]), 1);
+      mbar_init(smem_u32(&v_full[s]), 1);
+      mbar_init(smem_u32(&v_empty[s]), 1);
       mbar_init(smem_u32(&s_full[s]), 1);
       mbar_init(smem_u32(&s_free[s]), 128);
       mbar_init(smem_u32(&p_full[s]), 128);
@@ -132,11 +137,26 @@ __global__ void __launch_bounds__(kAttThreads, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
 
-  // work item w: head bh, query tile qt; the causal items with the most key
-  // tiles come first so the persistent grid ends evenly
-  auto item_of = [&](int w, int& bh, int& qt) {
-    bh = w % p.BH;
-    qt = p.q_tiles - 1 - w / p.BH;
+  // Work units, handed out round-robin to the persistent CTAs.  Neighbouring
+  // units belong to the same head, so the CTAs running together share that
+  // head's K and V through L2.  Without the causal mask a unit is one
+  // (head, query tile) item.  With it, unit u of a head pairs query tile
+  // q_tiles - 1 - u (u + 1 key tiles from the end) with query tile u, so
+  // every unit costs q_tiles + 1 key tiles and the grid ends evenly.
+  auto items_in = [&](int u) {
+    if (!p.causal) return 1;
+    const int pr = u % p.n_pairs;
+    return (p.q_tiles - 1 - pr != pr) ? 2 : 1;
+  };
+  auto item_of = [&](int u, int sub, int& bh, int& qt) {
+    if (!p.causal) {
+      bh = u / p.q_tiles;
+      qt = u % p.q_tiles;
+      return;
+    }
+    bh = u / p.n_pairs;
+    const int pr = u % p.n_pairs;
+    qt = sub == 0 ? p.q_tiles - 1 - pr : pr;
   };
   auto tiles_of = [&](int qt) {
     const int kv_end = p.causal ? min(p.T, (qt + 1) * kAttBQ) : p.T;
@@ -146,45 +166,63 @@ __global__ void __launch_bounds__(kAttThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ---------------- TMA producer ----------------
+      // K tile g is issued before V tile g - 1: S = Q K^T runs ahead of O += P V,
+      // so each K stage is refilled as soon as its score MMA has read it
       long long g = 0;  // key tiles loaded, over all items
       int it = 0;
-      for (int w = blockIdx.x; w < p.n_items; w += gridDim.x, ++it) {
-        int bh, qt;
-        item_of(w, bh, qt);
-        const int n = tiles_of(qt);
-        // the previous item's score MMAs have read its Q
-        if (it > 0)
-          mbar_wait<false>(smem_u32(&q_empty), static_cast<uint32_t>((it - 1) & 1), p.err, failed,
-                           WAIT_LIMIT_NS, hint);
-        mbar_arrive_expect_tx(smem_u32(&q_full), L::kQ);
-        for (int kb = 0; kb < D / 64; ++kb)
-          tma_load_3d(sq + kb * 16384, &map_q, 64 * kb, qt * kAttBQ, bh, smem_u32(&q_full));
-        for (int j = 0; j < n; ++j, ++g) {
-          const int st = static_cast<int>(g & 1);
-          if (g >= 2)
-            mbar_wait<false>(smem_u32(&kv_empty[st]), static_cast<uint32_t>(((g >> 1) - 1) & 1),
-                             p.err, failed, WAIT_LIMIT_NS, hint);
-          const uint32_t sk = skv + st * L::kStage;
-          const uint32_t sv = sk + L::kK;
-          const uint32_t fb = smem_u32(&kv_full[st]);
-          mbar_arrive_expect_tx(fb, L::kStage);
+      int v_bh = -1, v_j = 0;  // the V tile still to load (tile g - 1)
+      auto load_v = [&](long long t, int bh, int j) {
+        const int st = static_cast<int>(t & 1);
+        if (t >= 2)
+          mbar_wait<false>(smem_u32(&v_empty[st]), static_cast<uint32_t>(((t >> 1) - 1) & 1),
+                           p.err, failed, WAIT_LIMIT_NS, hint);
+        const uint32_t fb = smem_u32(&v_full[st]);
+        mbar_arrive_expect_tx(fb, L::kV);
+        for (int db = 0; db < D / 64; ++db)
+          for (int kh = 0; kh < 2; ++kh)
+            tma_load_3d(sv0 + st * L::kV + db * 16384 + kh * 8192, &map_v, 64 * db,
+                        j * kAttBK + 64 * kh, bh, fb);
+      };
+      for (int u = blockIdx.x; u < p.n_units; u += gridDim.x) {
+        for (int sub = 0; sub < items_in(u); ++sub, ++it) {
+          int bh, qt;
+          item_of(u, sub, bh, qt);
+          const int n = tiles_of(qt);
+          // the previous item's score MMAs have read its Q
+          if (it > 0)
+            mbar_wait<false>(smem_u32(&q_empty), static_cast<uint32_t>((it - 1) & 1), p.err,
+                             failed, WAIT_LIMIT_NS, hint);
+          mbar_arrive_expect_tx(smem_u32(&q_full), L::kQ);
           for (int kb = 0; kb < D / 64; ++kb)
-            tma_load_3d(sk + kb * 16384, &map_k, 64 * kb, j * kAttBK, bh, fb);
-          for (int db = 0; db < D / 64; ++db)
-            for (int kh = 0; kh < 2; ++kh)
-              tma_load_3d(sv + db * 16384 + kh * 8192, &map_v, 64 * db, j * kAttBK + 64 * kh, bh,
-                          fb);
+            tma_load_3d(sq + kb * 16384, &map_q, 64 * kb, qt * kAttBQ, bh, smem_u32(&q_full));
+          for (int j = 0; j < n; ++j, ++g) {
+            const int st = static_cast<int>(g & 1);
+            if (g >= 2)
+              mbar_wait<false>(smem_u32(&k_empty[st]), static_cast<uint32_t>(((g >> 1) - 1) & 1),
+                               p.err, failed, WAIT_LIMIT_NS, hint);
+            const uint32_t fb = smem_u32(&k_full[st]);
+            mbar_arrive_expect_tx(fb, L::kK);
+            for (int kb = 0; kb < D / 64; ++kb)
+              tma_load_3d(sk0 + st * L::kK + kb * 16384, &map_k, 64 * kb, j * kAttBK, bh, fb);
+            if (v_bh >= 0) load_v(g - 1, v_bh, v_j);
+            v_bh = bh;
+            v_j = j;
+          }
         }
       }
+      if (v_bh >= 0) load_v(g - 1, v_bh, v_j);
       // drain: no copy into this CTA's shared memory is in flight when it exits
       // (the MMA thread has waited on these phases already unless a wait failed)
       bool drain_failed = false;
       if (it > 0)
         mbar_wait<false>(smem_u32(&q_full), static_cast<uint32_t>((it - 1) & 1), p.err,
                          drain_failed, WAIT_LIMIT_NS, hint);
-      for (long long t = g - 2 < 0 ? 0 : g - 2; t < g; ++t)
-        mbar_wait<false>(smem_u32(&kv_full[t & 1]), static_cast<uint32_t>((t >> 1) & 1), p.err,
+      for (long long t = g - 2 < 0 ? 0 : g - 2; t < g; ++t) {
+        mbar_wait<false>(smem_u32(&k_full[t & 1]), static_cast<uint32_t>((t >> 1) & 1), p.err,
                          drain_failed, WAIT_LIMIT_NS, hint);
+        mbar_wait<false>(smem_u32(&v_full[t & 1]), static_cast<uint32_t>((t >> 1) & 1), p.err,
+                         drain_failed, WAIT_LIMIT_NS, hint);
+      }
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -199,14 +237,14 @@ __global__ void __launch_bounds__(kAttThreads, 1)
       long long gp = 0;  // P V tiles issued, over all items
       int it = 0;
       auto issue_s = [&](long long gs) {
-        const int st = static_cast<int>(gs & 1);  // key stage and score buffer alternate alike
-        mbar_wait<false>(smem_u32(&kv_full[st]), static_cast<uint32_t>((gs >> 1) & 1), p.err,
+        const int st = static_cast<int>(gs & 1);  // K stage and score buffer alternate alike
+        mbar_wait<false>(smem_u32(&k_full[st]), static_cast<uint32_t>((gs >> 1) & 1), p.err,
                          failed, WAIT_LIMIT_NS, hint);
         if (gs >= 2)
           mbar_wait<false>(smem_u32(&s_free[st]), static_cast<uint32_t>(((gs >> 1) - 1) & 1),
                            p.err, failed, WAIT_LIMIT_NS, hint);
         tc_fence_after();
-        const uint32_t sk = skv + st * L::kStage;
+        const uint32_t sk = sk0 + st * L::kK;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
@@ -214,10 +252,12 @@ __global__ void __launch_bounds__(kAttThreads, 1)
                     kk > 0 ? 1u : 0u);
         }
         umma_commit(smem_u32(&s_full[st]));
+        umma_commit(smem_u32(&k_empty[st]));
       };
-      for (int w = blockIdx.x; w < p.n_items; w += gridDim.x, ++it) {
+      for (int u = blockIdx.x; u < p.n_units; u += gridDim.x)
+      for (int sub = 0; sub < items_in(u); ++sub, ++it) {
         int bh, qt;
-        item_of(w, bh, qt);
+        item_of(u, sub, bh, qt);
         const int n = tiles_of(qt);
         mbar_wait<false>(smem_u32(&q_full), static_cast<uint32_t>(it & 1), p.err, failed,
                          WAIT_LIMIT_NS, hint);
@@ -230,11 +270,13 @@ __global__ void __launch_bounds__(kAttThreads, 1)
           if (j == 0 && it > 0)
             mbar_wait<false>(smem_u32(&o_free), static_cast<uint32_t>((it - 1) & 1), p.err, failed,
                              WAIT_LIMIT_NS, hint);
-          const int pb = static_cast<int>(gp & 1);  // P buffer, and the K/V stage of this tile
+          const int pb = static_cast<int>(gp & 1);  // P buffer, and the V stage of this tile
           mbar_wait<false>(smem_u32(&p_full[pb]), static_cast<uint32_t>((gp >> 1) & 1), p.err,
                            failed, WAIT_LIMIT_NS, hint);
+          mbar_wait<false>(smem_u32(&v_full[pb]), static_cast<uint32_t>((gp >> 1) & 1), p.err,
+                           failed, WAIT_LIMIT_NS, hint);
           tc_fence_after();
-          const uint32_t sv = skv + pb * L::kStage + L::kK;
+          const uint32_t sv = sv0 + pb * L::kV;
           const uint32_t pbase = sp + pb * L::kP;
 #pragma unroll
           for (int kk = 0; kk < kAttBK / 16; ++kk) {
@@ -244,7 +286,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
                       idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
           }
           umma_commit(smem_u32(&pv_done[pb]));
-          umma_commit(smem_u32(&kv_empty[pb]));
+          umma_commit(smem_u32(&v_empty[pb]));
           ++gp;
         }
       }
@@ -268,9 +310,10 @@ __global__ void __launch_bounds__(kAttThreads, 1)
     };
     long long g = 0;  // score tiles consumed, over all items
     int it = 0;
-    for (int w = blockIdx.x; w < p.n_items; w += gridDim.x, ++it) {
+    for (int u = blockIdx.x; u < p.n_units; u += gridDim.x)
+    for (int sub = 0; sub < items_in(u); ++sub, ++it) {
       int bh, qt;
-      item_of(w, bh, qt);
+      item_of(u, sub, bh, qt);
       const int n = tiles_of(qt);
       const int row = qt * kAttBQ + r;
       const bool row_ok = row < p.T;
@@ -468,7 +511,8 @@ static ce_status attention_launch(const void* Q, const void* K, const void* V, c
   p.scale_log2 = sm_scale * kLog2e;
   p.inv_scale = 1.f / sm_scale;
   p.q_tiles = (T + kAttBQ - 1) / kAttBQ;
-  p.n_items = BH * p.q_tiles;
+  p.n_pairs = (p.q_tiles + 1) / 2;
+  p.n_units = BH * (causal ? p.n_pairs : p.q_tiles);
   p.err = err;
   p.wait_hint_ns = wait_hint_ns;
   if (BH == 0 || T == 0) return CE_OK;
@@ -485,7 +529,7 @@ static ce_status attention_launch(const void* Q, const void* K, const void* V, c
     return CE_ERR_CUDA;
   if (per_sm != 1) return CE_ERR_UNSUPPORTED;
   long long grid = sm_count;
-  if (grid > p.n_items) grid = p.n_items;
+  if (grid > p.n_units) grid = p.n_units;
   attention_fwd_kernel<D><<<static_cast<int>(grid), kAttThreads, smem, stream>>>(mq, mk, mv, mo, p);
   return cudaGetLastError() == cudaSuccess ? CE_OK : CE_ERR_CUDA;
 }
