@@ -11,22 +11,26 @@
 //     lse_i = log sum_j exp(S_ij)                    (fp32, optional)
 //
 // Design (persistent, one CTA per SM, 192 threads; a work item is 128 query
-// rows of one head):
-//  * warp 0 (one thread) loads the item's Q tile and streams K and V tiles of
-//    128 keys into a two-stage ring with TMA (128-byte swizzle; K K-major for
-//    S = Q K^T, V MN-major for O = P V, so neither is transposed);
-//  * warp 1 allocates 512 TMEM columns -- two 128 x 128 fp32 score buffers
-//    and the D-column output accumulator -- and one thread issues the MMAs:
-//    S_{j+1} = Q K_{j+1}^T is issued before O += P_j V_j, so the tensor cores
-//    compute the next scores while the softmax warps work on these;
-//  * warps 2..5 own one query row per thread (TMEM lane = row): from S_j they
-//    take the row max, the correction alpha = 2^(m_old - m_new), rescale the
-//    row of O in TMEM when some alpha != 1 (after the previous O += P V has
-//    finished), write P = 2^(s - m_new) as bf16 into a 128-byte swizzled
-//    shared tile (the K-major A operand of O += P V), and keep the running
-//    normaliser l = alpha l + sum P in fp32.  At the end of the item they
-//    divide O by l and store it through shared memory with TMA tensor stores
-//    (rows past T are clipped by the tensor map), and write lse.
+// rows of one head; neighbouring CTAs work on the same head so its K and V
+// are read from L2; under the causal mask query tiles are paired so every
+// work unit costs the same):
+//  * warp 0 (one thread) loads each item's Q tile (two buffers: the next
+//    item's Q arrives while this one computes) and streams K and V tiles of
+//    128 keys into two-stage rings with TMA (128-byte swizzle; K K-major for
+//    S = Q K^T, V MN-major for O = P V, so neither is transposed); K runs one
+//    tile ahead of V, each K stage refilled once its score MMA has read it;
+//  * warp 1 allocates all 512 TMEM columns -- two 128 x 128 fp32 score
+//    buffers, the D-column output accumulator, two bf16 weight buffers P --
+//    and one thread issues the MMAs: S_{j+1} = Q K_{j+1}^T before
+//    O += P_j V_j (A operand P read from TMEM), so the tensor cores compute
+//    the next scores while the softmax warps work on these;
+//  * warps 2..5 own one query row per thread (TMEM lane = row): they load the
+//    128 scores of a tile into registers (freeing the score buffer), take the
+//    tile max, move the row's reference max only when the tile max exceeds it
+//    by more than 2^8 (then the row of O is rescaled in TMEM after the previous
+//    P V has run), write P = 2^(s c - ref) as bf16 into TMEM and add it to the
+//    running normaliser l.  At the end of the item they stage O / l in shared
+//    memory (two 32 x 32 blocks per warp) for TMA tensor stores, and write lse.
 //  * exp is exp2 of the score in log2 units: s * sm_scale * log2(e).
 // Every mbarrier wait is bounded; TMEM is freed on every path.
 #include <cstring>
@@ -43,7 +47,12 @@ namespace ce {
 constexpr int kAttBQ = 128;  // query rows of a work item
 constexpr int kAttBK = 128;  // keys of a tile
 constexpr int kAttThreads = 192;
-constexpr uint32_t kAttTmemCols = 512;  // S0 [0, 128), S1 [128, 256), O [256, 256 + D)
+// TMEM columns: scores S0 [0, 128) and S1 [128, 256), the output accumulator
+// O [256, 256 + D), the bf16 weights P0 [384, 448) and P1 [448, 512) (two to
+// a 32-bit column)
+constexpr uint32_t kAttTmemCols = 512;
+constexpr uint32_t kAttTmemO = 256;
+constexpr uint32_t kAttTmemP = 384;
 
 struct AttnParams {
   const float* mask;   // [T, T] additive, or null
@@ -61,12 +70,11 @@ struct AttnParams {
 
 template <int D>
 struct AttnSmem {
-  static constexpr int kQ = kAttBQ * D * 2;       // Q: D / 64 K-major blocks of 128 rows x 128 B
-  static constexpr int kK = kAttBK * D * 2;       // K: the same layout
-  static constexpr int kV = kAttBK * D * 2;       // V: D / 64 MN-major blocks of 128 keys x 128 B
-  static constexpr int kStage = kK + kV;
-  static constexpr int kP = kAttBQ * kAttBK * 2;  // P: 2 K-major blocks of 128 rows x 128 B
-  static constexpr int kTotal = kQ + 2 * kStage + 2 * kP + 1024;  // + alignment slack
+  static constexpr int kQ = kAttBQ * D * 2;  // Q: D / 64 K-major blocks of 128 rows x 128 B
+  static constexpr int kK = kAttBK * D * 2;  // K: the same layout
+  static constexpr int kV = kAttBK * D * 2;  // V: D / 64 MN-major blocks of 128 keys x 128 B
+  static constexpr int kStage = 4 * 2 * 4096;  // output staging: 4 warps x 2 x (32 rows x 128 B)
+  static constexpr int kTotal = 2 * (kQ + kK + kV) + kStage + 1024;  // + alignment slack
 };
 
 // The reference max of a row moves only when a tile's max exceeds it by more
@@ -74,16 +82,6 @@ struct AttnSmem {
 // exact enough in fp32 and bf16, and the accumulator is not rescaled.
 constexpr float kRescaleLog2 = 8.f;
 
-__device__ __forceinline__ uint4 pack8_bf16(const float* v) {
-  uint4 w;
-  __nv_bfloat162 h0 = __floats2bfloat162_rn(v[0], v[1]), h1 = __floats2bfloat162_rn(v[2], v[3]);
-  __nv_bfloat162 h2 = __floats2bfloat162_rn(v[4], v[5]), h3 = __floats2bfloat162_rn(v[6], v[7]);
-  w.x = *reinterpret_cast<uint32_t*>(&h0);
-  w.y = *reinterpret_cast<uint32_t*>(&h1);
-  w.z = *reinterpret_cast<uint32_t*>(&h2);
-  w.w = *reinterpret_cast<uint32_t*>(&h3);
-  return w;
-}
 
 template <int D>
 __global__ void __launch_bounds__(kAttThreads, 1)
@@ -93,7 +91,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
                          const __grid_constant__ CUtensorMap map_o, const AttnParams p) {
   using L = AttnSmem<D>;
   extern __shared__ unsigned char att_smem[];
-  __shared__ __align__(8) unsigned long long q_full, q_empty, o_free;
+  __shared__ __align__(8) unsigned long long q_full[2], q_empty[2], o_free;
   __shared__ __align__(8) unsigned long long k_full[2], k_empty[2], v_full[2], v_empty[2];
   __shared__ __align__(8) unsigned long long s_full[2], s_free[2];
   __shared__ __align__(8) unsigned long long p_full[2], pv_done[2];
@@ -102,18 +100,18 @@ __global__ void __launch_bounds__(kAttThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t base = (smem_u32(att_smem) + 1023u) & ~1023u;  // swizzle atoms need 1024 B
-  const uint32_t sq = base;
-  const uint32_t sk0 = sq + L::kQ;         // two K stages
+  const uint32_t sq0 = base;                // two Q buffers (items alternate)
+  const uint32_t sk0 = sq0 + 2 * L::kQ;     // two K stages
   const uint32_t sv0 = sk0 + 2 * L::kK;     // two V stages
-  const uint32_t sp = sv0 + 2 * L::kV;      // two P buffers
+  const uint32_t so0 = sv0 + 2 * L::kV;     // output staging
   bool failed = false;
   const unsigned int hint = p.wait_hint_ns;
 
   if (threadIdx.x == 0) {
-    mbar_init(smem_u32(&q_full), 1);
-    mbar_init(smem_u32(&q_empty), 1);
     mbar_init(smem_u32(&o_free), 128);
     for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_u32(&q_full[s]), 1);
+      mbar_init(smem_u32(&q_empty[s]), 1);
       mbar_init(smem_u32(&k_full[s]), 1);
       mbar_init(smem_u32(&k_empty[s]), 1);
       mbar_init(smem_u32(&v_full[s]), 1);
@@ -188,13 +186,15 @@ __global__ void __launch_bounds__(kAttThreads, 1)
           int bh, qt;
           item_of(u, sub, bh, qt);
           const int n = tiles_of(qt);
-          // the previous item's score MMAs have read its Q
-          if (it > 0)
-            mbar_wait<false>(smem_u32(&q_empty), static_cast<uint32_t>((it - 1) & 1), p.err,
-                             failed, WAIT_LIMIT_NS, hint);
-          mbar_arrive_expect_tx(smem_u32(&q_full), L::kQ);
+          // Q buffer it % 2: the score MMAs of item it - 2 have read it
+          const int qb = it & 1;
+          if (it >= 2)
+            mbar_wait<false>(smem_u32(&q_empty[qb]), static_cast<uint32_t>(((it >> 1) - 1) & 1),
+                             p.err, failed, WAIT_LIMIT_NS, hint);
+          mbar_arrive_expect_tx(smem_u32(&q_full[qb]), L::kQ);
           for (int kb = 0; kb < D / 64; ++kb)
-            tma_load_3d(sq + kb * 16384, &map_q, 64 * kb, qt * kAttBQ, bh, smem_u32(&q_full));
+            tma_load_3d(sq0 + qb * L::kQ + kb * 16384, &map_q, 64 * kb, qt * kAttBQ, bh,
+                        smem_u32(&q_full[qb]));
           for (int j = 0; j < n; ++j, ++g) {
             const int st = static_cast<int>(g & 1);
             if (g >= 2)
@@ -214,8 +214,8 @@ __global__ void __launch_bounds__(kAttThreads, 1)
       // drain: no copy into this CTA's shared memory is in flight when it exits
       // (the MMA thread has waited on these phases already unless a wait failed)
       bool drain_failed = false;
-      if (it > 0)
-        mbar_wait<false>(smem_u32(&q_full), static_cast<uint32_t>((it - 1) & 1), p.err,
+      for (int t = it - 2 < 0 ? 0 : it - 2; t < it; ++t)
+        mbar_wait<false>(smem_u32(&q_full[t & 1]), static_cast<uint32_t>((t >> 1) & 1), p.err,
                          drain_failed, WAIT_LIMIT_NS, hint);
       for (long long t = g - 2 < 0 ? 0 : g - 2; t < g; ++t) {
         mbar_wait<false>(smem_u32(&k_full[t & 1]), static_cast<uint32_t>((t >> 1) & 1), p.err,
@@ -230,12 +230,13 @@ __global__ void __launch_bounds__(kAttThreads, 1)
       // S = Q K^T: M = 128 queries, N = 128 keys, both operands K-major (K = D)
       constexpr uint32_t idesc_s = (1u << 4) | (1u << 7) | (1u << 10) | ((128u >> 3) << 17) |
                                    ((128u >> 4) << 24);
-      // O += P V: M = 128 queries, N = D, A = P K-major (K = keys), B = V MN-major
+      // O += P V: M = 128 queries, N = D, A = P in TMEM (K = keys), B = V MN-major
       constexpr uint32_t idesc_o = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) |
                                    ((static_cast<uint32_t>(D) >> 3) << 17) | ((128u >> 4) << 24);
       long long g = 0;   // score tiles issued, over all items
       long long gp = 0;  // P V tiles issued, over all items
       int it = 0;
+      uint32_t sq = sq0;  // this item's Q buffer
       auto issue_s = [&](long long gs) {
         const int st = static_cast<int>(gs & 1);  // K stage and score buffer alternate alike
         mbar_wait<false>(smem_u32(&k_full[st]), static_cast<uint32_t>((gs >> 1) & 1), p.err,
@@ -259,31 +260,33 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         int bh, qt;
         item_of(u, sub, bh, qt);
         const int n = tiles_of(qt);
-        mbar_wait<false>(smem_u32(&q_full), static_cast<uint32_t>(it & 1), p.err, failed,
-                         WAIT_LIMIT_NS, hint);
+        const int qb = it & 1;
+        sq = sq0 + qb * L::kQ;
+        mbar_wait<false>(smem_u32(&q_full[qb]), static_cast<uint32_t>((it >> 1) & 1), p.err,
+                         failed, WAIT_LIMIT_NS, hint);
         tc_fence_after();
         issue_s(g++);
         for (int j = 0; j < n; ++j) {
           if (j + 1 < n) issue_s(g++);
-          if (j + 1 == n) umma_commit(smem_u32(&q_empty));  // every MMA reading Q is issued
+          if (j + 1 == n) umma_commit(smem_u32(&q_empty[qb]));  // every MMA reading Q is issued
           // the previous item's output has been read out of TMEM
           if (j == 0 && it > 0)
             mbar_wait<false>(smem_u32(&o_free), static_cast<uint32_t>((it - 1) & 1), p.err, failed,
                              WAIT_LIMIT_NS, hint);
-          const int pb = static_cast<int>(gp & 1);  // P buffer, and the V stage of this tile
+          const int pb = static_cast<int>(gp & 1);  // P buffer and V stage of this tile
           mbar_wait<false>(smem_u32(&p_full[pb]), static_cast<uint32_t>((gp >> 1) & 1), p.err,
                            failed, WAIT_LIMIT_NS, hint);
           mbar_wait<false>(smem_u32(&v_full[pb]), static_cast<uint32_t>((gp >> 1) & 1), p.err,
                            failed, WAIT_LIMIT_NS, hint);
           tc_fence_after();
           const uint32_t sv = sv0 + pb * L::kV;
-          const uint32_t pbase = sp + pb * L::kP;
 #pragma unroll
           for (int kk = 0; kk < kAttBK / 16; ++kk) {
-            const uint32_t pa = pbase + (kk >> 2) * 16384 + (kk & 3) * 32;
-            // V: 64-wide D blocks 128 keys x 128 B = 16 KB apart, 16 keys = 2 KB
-            umma_bf16(tmem + 256, smem_desc_sw128(pa), smem_desc_sw128_mn(sv + kk * 2048, 16384),
-                      idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+            // P: 16 keys = 8 columns; V: 64-wide D blocks of 128 keys x 128 B
+            // 16 KB apart, 16 keys = 2 KB
+            umma_bf16_ts(tmem + kAttTmemO, tmem + kAttTmemP + 64 * pb + 8 * kk,
+                         smem_desc_sw128_mn(sv + kk * 2048, 16384), idesc_o,
+                         (j > 0 || kk > 0) ? 1u : 0u);
           }
           umma_commit(smem_u32(&pv_done[pb]));
           umma_commit(smem_u32(&v_empty[pb]));
@@ -301,7 +304,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
     const int q = warp & 3;  // the TMEM lane quarter this warp may access
     const int r = 32 * q + lane;
     const uint32_t lane_off = static_cast<uint32_t>(32 * q) << 16;
-    const uint32_t ebuf = sp + q * 4096;  // this warp's output staging block (inside P buffer 0)
+    const uint32_t ebuf = so0 + q * 8192;  // this warp's two output staging blocks
     const float c = p.scale_log2;          // > 0: the max of s * c is c * max(s)
     // wait until P V of global tile t has finished
     auto wait_pv = [&](long long t) {
@@ -378,10 +381,10 @@ __global__ void __launch_bounds__(kAttThreads, 1)
 #pragma unroll 1
           for (int cc = 0; cc < D / 32; ++cc) {
             float o[32];
-            tmem_ld32(tmem + 256 + 32 * cc + lane_off, o);
+            tmem_ld32(tmem + kAttTmemO + 32 * cc + lane_off, o);
 #pragma unroll
             for (int i = 0; i < 32; ++i) o[i] *= alpha;
-            tmem_st32(tmem + 256 + 32 * cc + lane_off, o);
+            tmem_st32(tmem + kAttTmemO + 32 * cc + lane_off, o);
           }
           l *= alpha;
           m_ref = m_new;
@@ -396,25 +399,24 @@ __global__ void __launch_bounds__(kAttThreads, 1)
           sm[i & 7] += x[i];
         }
         l += ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
-        // P buffer g % 2 is free once P V of tile g - 2 has finished; at an
-        // item's first tile the previous item's output stores (staged in P
-        // buffer 0) have also read their rows
-        if (g >= 2) wait_pv(g - 2);
-        if (j == 0 && it > 0) {
-          if (lane == 0) bulk_wait_read<0>();
-          __syncwarp();
-        }
-        const uint32_t pbase = sp + st * L::kP;
-        // keys 8u .. 8u + 7 of row r: K-block u / 8, 16-byte chunk (u % 8) ^ (r % 8)
-        // -- the 128-byte swizzle
+        // P, rounded to bf16, two keys to a column (the lower key in the low
+        // half), into TMEM buffer g % 2 -- free once P V of tile g - 2 has run
+        uint32_t pk[64];
 #pragma unroll
-        for (int u = 0; u < 16; ++u)
-          sts128(pbase + (u >> 3) * 16384 + r * 128 + 16 * ((u & 7) ^ (r & 7)), pack8_bf16(x + 8 * u));
-        fence_proxy_async_smem();  // P is read by the tensor cores (async proxy)
+        for (int i = 0; i < 64; ++i) {
+          __nv_bfloat162 h = __floats2bfloat162_rn(x[2 * i], x[2 * i + 1]);
+          pk[i] = *reinterpret_cast<uint32_t*>(&h);
+        }
+        if (g >= 2) wait_pv(g - 2);
+        tc_fence_after();
+        const uint32_t tp = tmem + kAttTmemP + 64 * st + lane_off;
+        tmem_st32_nowait(tp, pk);
+        tmem_st32_nowait(tp + 32, pk + 32);
+        tmem_wait_st();
         tc_fence_before();
         mbar_arrive(smem_u32(&p_full[st]));
       }
-      // ---- the item's output: O / l through shared memory and TMA ----
+      // ---- the item's output: O / l through shared memory and TMA stores ----
       wait_pv(g - 1);
       tc_fence_after();
       if (p.lse != nullptr && row_ok) {
@@ -425,22 +427,22 @@ __global__ void __launch_bounds__(kAttThreads, 1)
 #pragma unroll 1
       for (int cc = 0; cc < D / 32; ++cc) {
         float o[32];
-        tmem_ld32(tmem + 256 + 32 * cc + lane_off, o);
-        if (cc > 0) {
-          if (lane == 0) bulk_wait_read<0>();
-          __syncwarp();
-        }
+        tmem_ld32(tmem + kAttTmemO + 32 * cc + lane_off, o);
+        // staging block cc % 2: the store issued two chunks ago has read it
+        if (lane == 0) bulk_wait_read<1>();
+        __syncwarp();
+        const uint32_t eb = ebuf + (cc & 1) * 4096;
 #pragma unroll
         for (int jj = 0; jj < 8; ++jj)
           asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(
-                           ebuf + lane * 128 + 16 * (jj ^ (lane & 7))),
+                           eb + lane * 128 + 16 * (jj ^ (lane & 7))),
                        "f"(o[4 * jj] * inv_l), "f"(o[4 * jj + 1] * inv_l),
                        "f"(o[4 * jj + 2] * inv_l), "f"(o[4 * jj + 3] * inv_l)
                        : "memory");
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0 && qt * kAttBQ + 32 * q < p.T) {  // blocks wholly past T are not stored
-          tma_store_3d(&map_o, ebuf, 32 * cc, qt * kAttBQ + 32 * q, bh);
+          tma_store_3d(&map_o, eb, 32 * cc, qt * kAttBQ + 32 * q, bh);
           bulk_commit();
         }
       }
