@@ -530,6 +530,26 @@ def run_linear(args):
 # blockwise attention forward (the flash-attention page's benchmark shape)
 # ---------------------------------------------------------------------------
 ATTN_SHAPES = {"attn_causal_32x96x512x128": (32, 96, 512, 128, True)}
+ATTN_SOURCES = ("ce_attention.cu", "ce_tc.cuh")
+# DRAM traffic of the attention kernel per launch on the workload above, from
+# `ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum` (summarised under
+# profiles/), valid only for the attention sources it was taken on.
+ATTN_NCU_TRAFFIC = {}
+
+
+def attention_digest() -> str:
+    d = os.path.join(ROOT, "softmax_cross_entropy_online_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in ATTN_SOURCES:
+        with open(os.path.join(d, f), "rb") as fh:
+            h.update(f.encode() + b"\0" + fh.read())
+    return h.hexdigest()
+
+
+def attention_bytes(B: int, NH: int, T: int, D: int) -> int:
+    """Bytes the method must move: one read of the bf16 q, k and v, one write of
+    the fp32 output and lse."""
+    return 3 * B * NH * T * D * 2 + B * NH * T * D * 4 + B * NH * T * 4
 
 
 def attention_flops(B: int, NH: int, T: int, D: int, causal: bool, heads: int | None = None) -> float:
@@ -645,6 +665,14 @@ def run_attention(args):
     value = ws * flops / (ms * 1e-3) / 1e12
     assert api.ce_check_errors() == 0
     peak, peak_kind = measured_tflops(burst=True)
+    hbm_peak, hbm_kind = measured_peaks()
+    abytes = attention_bytes(B, NH, T, D)
+    tflops = flops / (ms * 1e-3) / 1e12
+    gbs = abytes / (ms * 1e-3) / 1e9
+    # the bound that binds: HBM time of the algorithmic bytes against tensor
+    # time of the algorithmic flops, both at the measured peaks
+    hbm_bound = abytes / (hbm_peak * 1e9) >= flops / (peak * 1e12)
+    tr = ATTN_NCU_TRAFFIC.get(attention_digest())
     # end to end: q, k, v from pinned host memory, the call, out and lse back
     out_host = torch.empty((B, NH, T, D), dtype=torch.float32).pin_memory()
     lse_host = torch.empty((B, NH, T), dtype=torch.float32).pin_memory()
@@ -674,10 +702,16 @@ def run_attention(args):
             "data": "synthetic",
             "config": {"workload": desc, "B": B, "NH": NH, "T": T, "D": D, "causal": causal,
                        "l2": "inputs (3 x 403 MB) larger than L2"},
-            "roofline": {"bound": "tensor", "achieved": flops / (ms * 1e-3) / 1e12, "peak": peak,
-                         "unit": "TFLOP/s", "frac": flops / (ms * 1e-3) / 1e12 / peak,
-                         "peak_source": peak_kind, "traffic": None,
-                         "kernel": "attention_fwd_kernel<128>", "ms_per_launch": ms},
+            "roofline": ({"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
+                          "frac": gbs / hbm_peak, "peak_source": hbm_kind,
+                          "algorithmic_bytes": abytes}
+                         if hbm_bound else
+                         {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
+                          "frac": tflops / peak, "peak_source": peak_kind})
+            | {"traffic": None if tr is None else tr["bytes_per_launch"],
+               "tensor": {"achieved": tflops, "peak": peak, "unit": "TFLOP/s",
+                          "frac": tflops / peak, "peak_source": peak_kind},
+               "kernel": f"attention_fwd_kernel<{D}>", "ms_per_launch": ms},
             "e2e": {"value": ws * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                     "h2d_bytes_per_step": 3 * B * NH * T * D * 2,
                     "d2h_bytes_per_step": B * NH * T * (D + 1) * 4, "ms_per_step": e2e_ms},
