@@ -46,7 +46,9 @@ namespace ce {
 
 constexpr int kAttBQ = 128;  // query rows of a work item
 constexpr int kAttBK = 128;  // keys of a tile
-constexpr int kAttThreads = 192;
+constexpr int kAttSoftmaxWarps = 8;  // two per TMEM lane quarter, 64 keys of a tile each
+constexpr int kAttSoftmax = 32 * kAttSoftmaxWarps;
+constexpr int kAttThreads = 64 + kAttSoftmax;
 // TMEM columns: scores S0 [0, 128) and S1 [128, 256), the output accumulator
 // O [256, 256 + D), the bf16 weights P0 [384, 448) and P1 [448, 512) (two to
 // a 32-bit column)
@@ -73,7 +75,7 @@ struct AttnSmem {
   static constexpr int kQ = kAttBQ * D * 2;  // Q: D / 64 K-major blocks of 128 rows x 128 B
   static constexpr int kK = kAttBK * D * 2;  // K: the same layout
   static constexpr int kV = kAttBK * D * 2;  // V: D / 64 MN-major blocks of 128 keys x 128 B
-  static constexpr int kStage = 4 * 2 * 4096;  // output staging: 4 warps x 2 x (32 rows x 128 B)
+  static constexpr int kStage = kAttSoftmaxWarps * 4096;  // output staging: 32 rows x 128 B a warp
   static constexpr int kTotal = 2 * (kQ + kK + kV) + kStage + 1024;  // + alignment slack
 };
 
@@ -96,6 +98,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
   __shared__ __align__(8) unsigned long long s_full[2], s_free[2];
   __shared__ __align__(8) unsigned long long p_full[2], pv_done[2];
   __shared__ uint32_t tmem_slot;
+  __shared__ float red[2][kAttBQ];  // [key half][row]: a row's two partial maxima or normalisers
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -108,7 +111,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
   const unsigned int hint = p.wait_hint_ns;
 
   if (threadIdx.x == 0) {
-    mbar_init(smem_u32(&o_free), 128);
+    mbar_init(smem_u32(&o_free), kAttSoftmax);
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&q_full[s]), 1);
       mbar_init(smem_u32(&q_empty[s]), 1);
@@ -117,8 +120,8 @@ __global__ void __launch_bounds__(kAttThreads, 1)
       mbar_init(smem_u32(&v_full[s]), 1);
       mbar_init(smem_u32(&v_empty[s]), 1);
       mbar_init(smem_u32(&s_full[s]), 1);
-      mbar_init(smem_u32(&s_free[s]), 128);
-      mbar_init(smem_u32(&p_full[s]), 128);
+      mbar_init(smem_u32(&s_free[s]), kAttSoftmax);
+      mbar_init(smem_u32(&p_full[s]), kAttSoftmax);
       mbar_init(smem_u32(&pv_done[s]), 1);
     }
     fence_mbar_init_cluster();
@@ -300,16 +303,27 @@ __global__ void __launch_bounds__(kAttThreads, 1)
                          p.err, drain_failed, WAIT_LIMIT_NS, hint);
     }
   } else {
-    // ---------------- softmax warps 2..5: one query row per thread ----------------
-    const int q = warp & 3;  // the TMEM lane quarter this warp may access
+    // ------- softmax warps 2..9: one query row and 64 keys of a tile per thread -------
+    const int q = warp & 3;           // the TMEM lane quarter this warp may access
+    const int h = (warp - 2) >> 2;    // which 64 keys of each tile (and half of O's columns)
     const int r = 32 * q + lane;
     const uint32_t lane_off = static_cast<uint32_t>(32 * q) << 16;
-    const uint32_t ebuf = so0 + q * 8192;  // this warp's two output staging blocks
-    const float c = p.scale_log2;          // > 0: the max of s * c is c * max(s)
+    const uint32_t ebuf = so0 + (warp - 2) * 4096;  // this warp's output staging block
+    const float c = p.scale_log2;                   // > 0: the max of s * c is c * max(s)
+    constexpr int kOC = D / 64;                     // output chunks of 32 columns per thread
     // wait until P V of global tile t has finished
     auto wait_pv = [&](long long t) {
       mbar_wait<false>(smem_u32(&pv_done[t & 1]), static_cast<uint32_t>((t >> 1) & 1), p.err,
                        failed, WAIT_LIMIT_NS, hint);
+    };
+    // the two threads of a row swap a value through red[][r]: the first meeting
+    // makes sure the partner has read the previous value, the second that the
+    // new one is written (one named barrier per lane quarter)
+    auto swap = [&](float v) {
+      group_sync(1 + q, 64);
+      red[h][r] = v;
+      group_sync(1 + q, 64);
+      return red[h ^ 1][r];
     };
     long long g = 0;  // score tiles consumed, over all items
     int it = 0;
@@ -322,69 +336,68 @@ __global__ void __launch_bounds__(kAttThreads, 1)
       const bool row_ok = row < p.T;
       const float* mrow = (p.mask != nullptr && row_ok) ? p.mask + static_cast<long long>(row) * p.T
                                                         : nullptr;
-      float m_ref = -INFINITY;  // reference max of O and l (log2 units)
-      float l = 0.f;            // running normaliser, relative to m_ref
+      float m_ref = -INFINITY;  // reference max of O and l (log2 units), the same in both threads
+      float l = 0.f;            // this thread's share of the normaliser, relative to m_ref
       for (int j = 0; j < n; ++j, ++g) {
         const int st = static_cast<int>(g & 1);
         mbar_wait<false>(smem_u32(&s_full[st]), static_cast<uint32_t>((g >> 1) & 1), p.err,
                          failed, WAIT_LIMIT_NS, hint);
         tc_fence_after();
-        uint32_t sr[128];
-        const uint32_t ts = tmem + st * 128 + lane_off;
-#pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) tmem_ld32_nowait(ts + 32 * c4, sr + 32 * c4);
-        tmem_wait_ld<128>(sr);
+        uint32_t sr[64];
+        const uint32_t ts = tmem + st * 128 + 64 * h + lane_off;
+        tmem_ld32_nowait(ts, sr);
+        tmem_ld32_nowait(ts + 32, sr + 32);
+        tmem_wait_ld<64>(sr);
         // the scores are in registers: the buffer may take the next tile's scores
         tc_fence_before();
         mbar_arrive(smem_u32(&s_free[st]));
         float* x = reinterpret_cast<float*>(sr);
-        const int kv0 = j * kAttBK;
+        const int kv0 = j * kAttBK + 64 * h;  // this thread's first key
         // one decision for the whole CTA: does any key of this tile need a mask?
-        const bool masked =
-            p.mask != nullptr || kv0 + kAttBK > p.T || (p.causal && kv0 + kAttBK - 1 > qt * kAttBQ);
-        float mt;  // the tile's max (log2 units)
+        const bool masked = p.mask != nullptr || j * kAttBK + kAttBK > p.T ||
+                            (p.causal && j * kAttBK + kAttBK - 1 > qt * kAttBQ);
+        float mx[8];
         if (!masked) {
-          float mx[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) mx[i] = x[i];
 #pragma unroll
-          for (int i = 8; i < 128; ++i) mx[i & 7] = fmaxf(mx[i & 7], x[i]);
-          mt = c * fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                         fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+          for (int i = 8; i < 64; ++i) mx[i & 7] = fmaxf(mx[i & 7], x[i]);
         } else {
           // keys kv0 + i with i > lim are hidden (past T, or after the query);
           // the additive mask joins the unscaled score as mask / sm_scale, so
           // both paths share one exponent, and a zero entry changes no bit
           const int lim = (p.causal ? min(row, p.T - 1) : p.T - 1) - kv0;
-          float mx[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
 #pragma unroll
-          for (int i = 0; i < 128; ++i) {
+          for (int i = 0; i < 64; ++i) {
             float y = x[i];
             if (mrow != nullptr) y = fmaf(__ldg(mrow + min(kv0 + i, p.T - 1)), p.inv_scale, y);
             x[i] = (i > lim) ? -INFINITY : y;
             mx[i & 7] = fmaxf(mx[i & 7], x[i]);
           }
-          mt = c * fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                         fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
         }
+        const float pm = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        const float mt = c * fmaxf(pm, swap(pm));  // the row's tile max (log2 units)
         if (j == 0) {
           m_ref = mt;  // this tile's P V overwrites O
         } else if (__any_sync(0xffffffffu, mt > m_ref + kRescaleLog2)) {
           // move the reference: O and l are rescaled by alpha = 2^(old - new),
           // after the previous P V has finished and before this tile's is issued
+          // (the partner warp takes the same decision: it sees the same maxima)
           const float m_new = fmaxf(m_ref, mt);
           const float alpha = (m_ref == -INFINITY) ? 0.f : ex2(m_ref - m_new);
           wait_pv(g - 1);
           tc_fence_after();
 #pragma unroll 1
-          for (int cc = 0; cc < D / 32; ++cc) {
+          for (int cc = 0; cc < kOC; ++cc) {
+            const uint32_t to = tmem + kAttTmemO + 32 * (kOC * h + cc) + lane_off;
             float o[32];
-            tmem_ld32(tmem + kAttTmemO + 32 * cc + lane_off, o);
+            tmem_ld32(to, o);
 #pragma unroll
             for (int i = 0; i < 32; ++i) o[i] *= alpha;
-            tmem_st32(tmem + kAttTmemO + 32 * cc + lane_off, o);
+            tmem_st32(to, o);
           }
           l *= alpha;
           m_ref = m_new;
@@ -394,55 +407,54 @@ __global__ void __launch_bounds__(kAttThreads, 1)
 #pragma unroll
         for (int i = 0; i < 8; ++i) sm[i] = 0.f;
 #pragma unroll
-        for (int i = 0; i < 128; ++i) {
+        for (int i = 0; i < 64; ++i) {
           x[i] = ex2(fmaf(x[i], c, -ref));
           sm[i & 7] += x[i];
         }
         l += ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
         // P, rounded to bf16, two keys to a column (the lower key in the low
         // half), into TMEM buffer g % 2 -- free once P V of tile g - 2 has run
-        uint32_t pk[64];
+        uint32_t pk[32];
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          __nv_bfloat162 h = __floats2bfloat162_rn(x[2 * i], x[2 * i + 1]);
-          pk[i] = *reinterpret_cast<uint32_t*>(&h);
+        for (int i = 0; i < 32; ++i) {
+          __nv_bfloat162 hv = __floats2bfloat162_rn(x[2 * i], x[2 * i + 1]);
+          pk[i] = *reinterpret_cast<uint32_t*>(&hv);
         }
         if (g >= 2) wait_pv(g - 2);
         tc_fence_after();
-        const uint32_t tp = tmem + kAttTmemP + 64 * st + lane_off;
-        tmem_st32_nowait(tp, pk);
-        tmem_st32_nowait(tp + 32, pk + 32);
+        tmem_st32_nowait(tmem + kAttTmemP + 64 * st + 32 * h + lane_off, pk);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(smem_u32(&p_full[st]));
       }
       // ---- the item's output: O / l through shared memory and TMA stores ----
+      const float lt = l + swap(l);
       wait_pv(g - 1);
       tc_fence_after();
-      if (p.lse != nullptr && row_ok) {
+      if (h == 0 && p.lse != nullptr && row_ok) {
         const float mref = (m_ref == -INFINITY) ? 0.f : m_ref;
-        p.lse[static_cast<long long>(bh) * p.T + row] = (mref + lg2(l)) * 0.6931471805599453f;
+        p.lse[static_cast<long long>(bh) * p.T + row] = (mref + lg2(lt)) * 0.6931471805599453f;
       }
-      const float inv_l = 1.f / l;
+      const float inv_l = 1.f / lt;
 #pragma unroll 1
-      for (int cc = 0; cc < D / 32; ++cc) {
+      for (int cc = 0; cc < kOC; ++cc) {
+        const int col = 32 * (kOC * h + cc);
         float o[32];
-        tmem_ld32(tmem + kAttTmemO + 32 * cc + lane_off, o);
-        // staging block cc % 2: the store issued two chunks ago has read it
-        if (lane == 0) bulk_wait_read<1>();
+        tmem_ld32(tmem + kAttTmemO + col + lane_off, o);
+        // the staging block: the store issued before has read it
+        if (lane == 0) bulk_wait_read<0>();
         __syncwarp();
-        const uint32_t eb = ebuf + (cc & 1) * 4096;
 #pragma unroll
         for (int jj = 0; jj < 8; ++jj)
           asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(
-                           eb + lane * 128 + 16 * (jj ^ (lane & 7))),
+                           ebuf + lane * 128 + 16 * (jj ^ (lane & 7))),
                        "f"(o[4 * jj] * inv_l), "f"(o[4 * jj + 1] * inv_l),
                        "f"(o[4 * jj + 2] * inv_l), "f"(o[4 * jj + 3] * inv_l)
                        : "memory");
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0 && qt * kAttBQ + 32 * q < p.T) {  // blocks wholly past T are not stored
-          tma_store_3d(&map_o, eb, 32 * cc, qt * kAttBQ + 32 * q, bh);
+          tma_store_3d(&map_o, ebuf, col, qt * kAttBQ + 32 * q, bh);
           bulk_commit();
         }
       }
