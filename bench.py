@@ -46,8 +46,8 @@ FALLBACK_HBM_GBS = 6800.0
 # digest of the row-kernel sources at that time.  Any change to them nulls it.
 NCU_TRAFFIC = {
     # profiles/ce_rows_fwd_bwd_f32_32768x4096.md: a 16384-row capture, scaled 2x
-    "acdd8d5f9c9cbbd481dbc05dec43658f00e6ae5d2efe98b244de9a43c0944029": {
-        "workload": "f32_32768x4096", "bytes_per_launch": 953288704},
+    "85f8fb43e3b9160227a84ceed1f00d6093d1b19e463ec0546ac01bfe7c2b359e": {
+        "workload": "f32_32768x4096", "bytes_per_launch": 950148096},
 }
 
 
@@ -534,7 +534,11 @@ ATTN_SOURCES = ("ce_attention.cu", "ce_tc.cuh")
 # DRAM traffic of the attention kernel per launch on the workload above, from
 # `ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum` (summarised under
 # profiles/), valid only for the attention sources it was taken on.
-ATTN_NCU_TRAFFIC = {}
+ATTN_NCU_TRAFFIC = {
+    # profiles/attention_fwd_bf16_32x96x512x128_causal.md
+    "e11801a593a18bf18676b7679cfc2f4d1314bb762e54ddb16aff6b357e7c9bef": {
+        "workload": "attn_causal_32x96x512x128", "bytes_per_launch": 1978001664},
+}
 
 
 def attention_digest() -> str:
@@ -594,7 +598,10 @@ def run_attention(args):
 
     ws, rank, local = dist_env()
     B, NH, T, D, causal = ATTN_SHAPES[args.workload]
-    desc = attention_desc(args.workload, B, NH, T, D, causal)
+    name = args.workload
+    if args.heads is not None:  # a smaller case of the same shape (profiling)
+        B, NH, name = 1, args.heads, f"{args.workload}[heads={args.heads}]"
+    desc = attention_desc(name, B, NH, T, D, causal)
     metric = "blockwise attention forward TFLOP/s (4 D per visible query-key pair)"
     if args.impl == "reference":
         if rank != 0:
@@ -701,7 +708,9 @@ def run_attention(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
             "config": {"workload": desc, "B": B, "NH": NH, "T": T, "D": D, "causal": causal,
-                       "l2": "inputs (3 x 403 MB) larger than L2"},
+                       "l2": f"inputs (3 x {B * NH * T * D * 2 / 1e6:.0f} MB) "
+                             + ("larger than L2" if 3 * B * NH * T * D * 2 > 129e6 else
+                                "within L2")},
             "roofline": ({"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
                           "frac": gbs / hbm_peak, "peak_source": hbm_kind,
                           "algorithmic_bytes": abytes}
@@ -737,6 +746,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--rows", type=int, default=None,
                     help="override the workload's row count (smaller cases for profiling)")
+    ap.add_argument("--heads", type=int, default=None,
+                    help="attention workloads: run B = 1 with this many heads instead")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps, always
     if args.workload in ATTN_SHAPES:
