@@ -325,7 +325,7 @@ def run_native(args, w):
     traffic = rec.get("bytes_per_launch") if rec.get("workload") == w.name else None
 
     # forward-only pass on the same workload (the first half of the config)
-    fwd_ms = None
+    fwd_ms = sm_ms = None
     if rank == 0:
         for b in bufs[:2]:
             b.copy_(pristine)
@@ -343,6 +343,19 @@ def run_native(args, w):
         fe1.record(stream)
         torch.cuda.synchronize()
         fwd_ms = fe0.elapsed_time(fe1) / nf
+        # the fused softmax (probabilities written over the logits, one read and
+        # one write per element) on the same buffers
+        for i in range(3):
+            L.ce_softmax_forward(bufs[i % n_bufs].data_ptr(), bufs[i % n_bufs].data_ptr(), M, V,
+                                 code, None, sh)
+        fe0.record(stream)
+        for i in range(nf):
+            L.ce_softmax_forward(bufs[i % n_bufs].data_ptr(), bufs[i % n_bufs].data_ptr(), M, V,
+                                 code, None, sh)
+        fe1.record(stream)
+        torch.cuda.synchronize()
+        sm_ms = fe0.elapsed_time(fe1) / nf
+        assert api.ce_check_errors() == 0
 
     # end to end: host logits -> device, the call, loss -> host, every step
     loss_host = torch.empty((), dtype=torch.float32).pin_memory()
@@ -387,6 +400,10 @@ def run_native(args, w):
             "forward_only": None if fwd_ms is None else {
                 "ms_per_call": fwd_ms,
                 "gb_s": algorithmic_bytes(M, V, es, False) / (fwd_ms * 1e-3) / 1e9},
+            "softmax": None if sm_ms is None else {
+                "call": "ce_softmax_forward (in place)", "ms_per_call": sm_ms,
+                "gb_s": 2 * M * V * es / (sm_ms * 1e-3) / 1e9,
+                "frac": 2 * M * V * es / (sm_ms * 1e-3) / 1e9 / peak},
             "e2e": {"value": e2e_value, "unit": "GB/s",
                     "h2d_bytes_per_step": step_bytes + M * 8, "d2h_bytes_per_step": 4,
                     "ms_per_step": e2e_ms},
