@@ -553,7 +553,7 @@ ATTN_SOURCES = ("ce_attention.cu", "ce_tc.cuh")
 # profiles/), valid only for the attention sources it was taken on.
 ATTN_NCU_TRAFFIC = {
     # profiles/attention_fwd_bf16_32x96x512x128_causal.md
-    "e11801a593a18bf18676b7679cfc2f4d1314bb762e54ddb16aff6b357e7c9bef": {
+    "cff57136d22565bada4ffd5f62f884aa582e97704709de84767aa8777c6461dd": {
         "workload": "attn_causal_32x96x512x128", "bytes_per_launch": 1978001664},
 }
 

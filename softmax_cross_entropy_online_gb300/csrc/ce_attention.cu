@@ -10,7 +10,7 @@
 //     O = softmax(Q K^T * sm_scale + mask) V        (fp32)
 //     lse_i = log sum_j exp(S_ij)                    (fp32, optional)
 //
-// Design (persistent, one CTA per SM, 192 threads; a work item is 128 query
+// Design (persistent, one CTA per SM, 320 threads; a work item is 128 query
 // rows of one head; neighbouring CTAs work on the same head so its K and V
 // are read from L2; under the causal mask query tiles are paired so every
 // work unit costs the same):
@@ -24,13 +24,16 @@
 //    and one thread issues the MMAs: S_{j+1} = Q K_{j+1}^T before
 //    O += P_j V_j (A operand P read from TMEM), so the tensor cores compute
 //    the next scores while the softmax warps work on these;
-//  * warps 2..5 own one query row per thread (TMEM lane = row): they load the
-//    128 scores of a tile into registers (freeing the score buffer), take the
-//    tile max, move the row's reference max only when the tile max exceeds it
-//    by more than 2^8 (then the row of O is rescaled in TMEM after the previous
-//    P V has run), write P = 2^(s c - ref) as bf16 into TMEM and add it to the
-//    running normaliser l.  At the end of the item they stage O / l in shared
-//    memory (two 32 x 32 blocks per warp) for TMA tensor stores, and write lse.
+//  * warps 2..9 give each query row two threads (TMEM lane = row; two warps
+//    per lane quarter), each with 64 of a tile's 128 keys: they load those
+//    scores into registers (freeing the score buffer), swap partial maxima
+//    through shared memory for the tile max, move the row's reference max only
+//    when the tile max exceeds it by more than 2^8 (then each rescales its half
+//    of the row of O in TMEM after the previous P V has run), write
+//    P = 2^(s c - ref) as bf16 into TMEM and add it to their share of the
+//    normaliser l.  At the end of the item the two shares are summed and each
+//    thread stages its half of O / l in shared memory (one 32 x 32 block per
+//    warp at a time) for TMA tensor stores; lse is written by the first.
 //  * exp is exp2 of the score in log2 units: s * sm_scale * log2(e).
 // Every mbarrier wait is bounded; TMEM is freed on every path.
 #include <cstring>
