@@ -72,3 +72,28 @@ def test_reference_arm_under_torchrun_prints_from_rank_zero_only():
     assert d["impl"] == "reference" and d["n_gpus"] == 2
     assert d["cpu_baseline"]["kind"] == "oracle"
     assert d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_attention_reference_arm_prints_one_line():
+    cmd = [sys.executable, "bench.py", "--impl", "reference", "--steps", "1", "--warmup", "3",
+           "--cpu-budget-s", "0.4", "--workload", "attn_causal_32x96x512x128"]
+    r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "TFLOP/s" and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
+    assert d["config"]["T"] == 512 and d["config"]["D"] == 128
+
+
+def test_attention_flop_and_byte_counts():
+    sys.path.insert(0, ROOT)
+    import bench
+    # 4 D flops per visible (query, key) pair: T (T + 1) / 2 pairs per head under the causal mask
+    assert bench.attention_flops(1, 1, 4, 8, True) == 4 * 8 * 10
+    assert bench.attention_flops(2, 3, 4, 8, False) == 4 * 8 * 16 * 6
+    # one read of bf16 q, k, v and one write of the fp32 output and lse
+    assert bench.attention_bytes(1, 1, 4, 8) == 3 * 32 * 2 + 32 * 4 + 4 * 4
