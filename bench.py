@@ -772,7 +772,8 @@ def main():
     if args.workload in LINEAR_SHAPES:
         if args.impl == "reference":
             print(json.dumps({"impl": "reference", "unavailable":
-                              "the float64 linear+CE oracle is timed only on the CE workloads"}))
+                              "the float64 linear+CE oracle holds dW [128256, 4096] in float64 "
+                              "(4.2 GB) for any row sample; it is timed on the CE workloads"}))
             return 0
         return run_linear(args)
     w = synthetic.WORKLOADS[args.workload]
