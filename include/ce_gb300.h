@@ -235,8 +235,8 @@ ce_status ce_gemm_bf16_tn(const void* A, int64_t lda, const void* B, int64_t ldb
  * bf16 for P V, accumulated in fp32.  A row whose every key is hidden gives
  * NaN outputs and lse = -inf (the definition's 0/0).
  * Errors: null pointers, B, NH or T < 0, causal outside {0, 1}, sm_scale not
- * positive with a finite reciprocal, misaligned pointers -> CE_ERR_INVALID_ARG; D not 64 or 128, or T
- * or B*NH above 2^31-1 -> CE_ERR_UNSUPPORTED.
+ * positive with a finite reciprocal, misaligned pointers -> CE_ERR_INVALID_ARG; D not 64 or 128, or T,
+ * B*NH or B*NH*ceil(T/128) above 2^31-1 -> CE_ERR_UNSUPPORTED.
  */
 ce_status ce_attention_forward(const void* q, const void* k, const void* v, const float* mask,
                                int causal, int64_t B, int64_t NH, int64_t T, int64_t D,

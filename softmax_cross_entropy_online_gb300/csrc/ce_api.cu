@@ -756,6 +756,8 @@ ce_status ce_attention_forward(const void* q, const void* k, const void* v, cons
   if (BH == 0 || T == 0) return CE_OK;
   if (q == nullptr || k == nullptr || v == nullptr || out == nullptr) return CE_ERR_INVALID_ARG;
   if (T > INT32_MAX || BH > INT32_MAX || (B > 0 && BH / B != NH)) return CE_ERR_UNSUPPORTED;
+  // the kernel counts (head, 128-row query tile) items in 32-bit integers
+  if (BH * ((T + 127) / 128) > INT32_MAX) return CE_ERR_UNSUPPORTED;
   auto mis = [](const void* ptr, uintptr_t a) { return reinterpret_cast<uintptr_t>(ptr) % a != 0; };
   if (mis(q, 16) || mis(k, 16) || mis(v, 16) || mis(out, 16) || (mask && mis(mask, 4)) ||
       (lse && mis(lse, 4)))

@@ -135,6 +135,7 @@ def test_product_path_never_imports_the_oracle():
     ((16, 16, 16, 18, 0, 1, 1, 8, 64, 0.125, 16, None), 1),             # mask misaligned
     ((16, 16, 16, None, 0, 1, 1, 8, 64, 0.125, 16, 18), 1),             # lse misaligned
     ((16, 16, 16, None, 0, 1, 1, 1 << 31, 64, 0.125, 16, None), 2),     # T above 2^31 - 1
+    ((16, 16, 16, None, 0, 1, 1 << 30, 1024, 64, 0.125, 16, None), 2),  # 2^33 query tiles
     ((None, None, None, None, 0, 0, 4, 8, 64, 0.125, None, None), 0),   # B = 0: nothing to do
     ((None, None, None, None, 1, 2, 4, 0, 128, 0.125, None, None), 0),  # T = 0: nothing to do
 ])
