@@ -154,3 +154,43 @@ def test_linear_ce_full_width_sampled(api):
     dW_ref = G[:, vs].T @ h64
     eW = np.abs(dW[torch.from_numpy(vs).cuda()].cpu().numpy().astype(np.float64) - dW_ref)
     assert np.all(eW <= 2.0**-8 * (np.abs(G[:, vs]).T @ np.abs(h64)) + 1e-30)
+
+
+def test_linear_ce_bench_size_sampled(api):
+    # the bench workload itself (h [8192, 4096], W [128256, 4096], seed 0) through the
+    # same call, so four row chunks of 2048 with dW accumulated across them: the loss
+    # in full, and rows of dH and dW on both sides of every chunk border, against
+    # float64 logits formed 512 rows at a time
+    M, H, V = 8192, 4096, 128256
+    h, W, t = synthetic.make_linear_ce_inputs(M, H, V, seed=0)
+    loss, dH, dW = api.linear_ce_fwd_bwd(bf16_dev(h), bf16_dev(W), torch.from_numpy(t).cuda())
+    torch.cuda.synchronize()
+    assert api.ce_check_errors() == 0
+    h64, W64 = oracle.decode_bf16(h), oracle.decode_bf16(W)
+    rng = np.random.default_rng(2)
+    rows = np.unique(np.concatenate([rng.choice(M, 16, replace=False),
+                                     [0, 2047, 2048, 4095, 4096, 6143, 6144, M - 1]]))
+    vs = np.unique(np.concatenate([t[:32], rng.choice(V, 32, replace=False), [0, V - 1]]))
+    total = 0.0
+    dW_ref = np.zeros((len(vs), H))
+    dW_bnd = np.zeros((len(vs), H))
+    dH_ref, dH_bnd = {}, {}
+    for b0 in range(0, M, 512):
+        hb = h64[b0:b0 + 512]
+        x = hb @ W64.T
+        f = oracle.ce_forward(x, t[b0:b0 + 512], "sum")
+        total += f["loss"]
+        G = oracle.ce_grad(x, t[b0:b0 + 512], f["lse"], 1.0 / M)
+        dW_ref += G[:, vs].T @ hb
+        dW_bnd += np.abs(G[:, vs]).T @ np.abs(hb)
+        for r in rows[(rows >= b0) & (rows < b0 + 512)]:
+            dH_ref[r] = G[r - b0] @ W64
+            dH_bnd[r] = np.abs(G[r - b0]) @ np.abs(W64)
+    assert abs(loss.item() - total / M) <= 2e-3
+    got_H = dH[torch.from_numpy(rows).cuda()].cpu().numpy().astype(np.float64)
+    for k, r in enumerate(rows):
+        e = np.abs(got_H[k] - dH_ref[r])
+        assert np.all(e <= 2.0**-8 * dH_bnd[r] + 1e-30), f"dH row {r}: worst {np.max(e / (2.0**-8 * dH_bnd[r] + 1e-30)):.3g} x bound"
+    got_W = dW[torch.from_numpy(vs).cuda()].cpu().numpy().astype(np.float64)
+    eW = np.abs(got_W - dW_ref)
+    assert np.all(eW <= 2.0**-8 * dW_bnd + 1e-30), f"dW worst {np.max(eW / (2.0**-8 * dW_bnd + 1e-30)):.3g} x bound"
