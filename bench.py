@@ -325,7 +325,7 @@ def run_native(args, w):
     traffic = rec.get("bytes_per_launch") if rec.get("workload") == w.name else None
 
     # forward-only pass on the same workload (the first half of the config)
-    fwd_ms = sm_ms = None
+    fwd_ms = sm_ms = probe = None
     if rank == 0:
         for b in bufs[:2]:
             b.copy_(pristine)
@@ -356,6 +356,22 @@ def run_native(args, w):
         torch.cuda.synchronize()
         sm_ms = fe0.elapsed_time(fe1) / nf
         assert api.ce_check_errors() == 0
+        # stream probes over the same buffers with PyTorch's own kernels (not the
+        # library's): an in-place read + write pass (x *= 1) and a read-only pass
+        # (the max), the achievable ceilings beside the fused pass
+        probe = {}
+        for name, fn, nbytes in (("inplace_rw", lambda b: b.mul_(1), 2 * M * V * es),
+                                 ("read_only", lambda b: torch.amax(b), M * V * es)):
+            for i in range(3):
+                fn(bufs[i % n_bufs])
+            fe0.record(stream)
+            for i in range(nf):
+                fn(bufs[i % n_bufs])
+            fe1.record(stream)
+            torch.cuda.synchronize()
+            pms = fe0.elapsed_time(fe1) / nf
+            probe[name] = {"ms": pms, "gb_s": nbytes / (pms * 1e-3) / 1e9,
+                           "frac": nbytes / (pms * 1e-3) / 1e9 / peak}
 
     # end to end: host logits -> device, the call, loss -> host, every step
     loss_host = torch.empty((), dtype=torch.float32).pin_memory()
@@ -400,6 +416,7 @@ def run_native(args, w):
             "forward_only": None if fwd_ms is None else {
                 "ms_per_call": fwd_ms,
                 "gb_s": algorithmic_bytes(M, V, es, False) / (fwd_ms * 1e-3) / 1e9},
+            "stream_probes": probe,
             "softmax": None if sm_ms is None else {
                 "call": "ce_softmax_forward (in place)", "ms_per_call": sm_ms,
                 "gb_s": 2 * M * V * es / (sm_ms * 1e-3) / 1e9,
