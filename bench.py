@@ -568,11 +568,7 @@ ATTN_SOURCES = ("ce_attention.cu", "ce_tc.cuh")
 # DRAM traffic of the attention kernel per launch on the workload above, from
 # `ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum` (summarised under
 # profiles/), valid only for the attention sources it was taken on.
-ATTN_NCU_TRAFFIC = {
-    # profiles/attention_fwd_bf16_32x96x512x128_causal.md
-    "cff57136d22565bada4ffd5f62f884aa582e97704709de84767aa8777c6461dd": {
-        "workload": "attn_causal_32x96x512x128", "bytes_per_launch": 1978001664},
-}
+ATTN_NCU_TRAFFIC = {}
 
 
 def attention_digest() -> str:
@@ -584,10 +580,10 @@ def attention_digest() -> str:
     return h.hexdigest()
 
 
-def attention_bytes(B: int, NH: int, T: int, D: int) -> int:
+def attention_bytes(B: int, NH: int, T: int, D: int, out_bytes: int = 2) -> int:
     """Bytes the method must move: one read of the bf16 q, k and v, one write of
-    the fp32 output and lse."""
-    return 3 * B * NH * T * D * 2 + B * NH * T * D * 4 + B * NH * T * 4
+    the output (bf16 like q: 2 bytes an element; fp32: 4) and the fp32 lse."""
+    return 3 * B * NH * T * D * 2 + B * NH * T * D * out_bytes + B * NH * T * 4
 
 
 def attention_flops(B: int, NH: int, T: int, D: int, causal: bool, heads: int | None = None) -> float:
@@ -600,7 +596,8 @@ def attention_flops(B: int, NH: int, T: int, D: int, causal: bool, heads: int | 
 
 def attention_desc(name, B, NH, T, D, causal):
     return (f"{name}: q, k, v bf16 [{B}, {NH}, {T}, {D}] N(0,1), "
-            f"{'causal' if causal else 'no'} mask, sm_scale 1/sqrt({D}); out fp32 + lse")
+            f"{'causal' if causal else 'no'} mask, sm_scale 1/sqrt({D}); "
+            "out bf16 (allocated like q, as the page does) + fp32 lse")
 
 
 def attention_oracle_sample(B, NH, T, D, causal, budget_s):
@@ -670,14 +667,16 @@ def run_attention(args):
     hosts = [as_bf16(a).pin_memory() for a in (qb, kb, vb)]
     del qb, kb, vb
     q, k, v = (h.to(dev) for h in hosts)
-    out = torch.empty((B, NH, T, D), dtype=torch.float32, device=dev)
+    out = torch.empty((B, NH, T, D), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((B, NH, T), dtype=torch.float32, device=dev)
     sh = torch.cuda.current_stream(dev).cuda_stream
     scale = 1.0 / float(np.sqrt(D))
+    CE_BF16 = 2
 
     def step():
         st = L.ce_attention_forward(q.data_ptr(), k.data_ptr(), v.data_ptr(), None, int(causal),
-                                    B, NH, T, D, scale, out.data_ptr(), lse.data_ptr(), sh)
+                                    B, NH, T, D, scale, out.data_ptr(), CE_BF16, lse.data_ptr(),
+                                    sh)
         if st != 0:
             raise api.CEError(st, "ce_attention_forward")
 
@@ -715,7 +714,7 @@ def run_attention(args):
     hbm_bound = abytes / (hbm_peak * 1e9) >= flops / (peak * 1e12)
     tr = ATTN_NCU_TRAFFIC.get(attention_digest())
     # end to end: q, k, v from pinned host memory, the call, out and lse back
-    out_host = torch.empty((B, NH, T, D), dtype=torch.float32).pin_memory()
+    out_host = torch.empty((B, NH, T, D), dtype=torch.bfloat16).pin_memory()
     lse_host = torch.empty((B, NH, T), dtype=torch.float32).pin_memory()
     x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e2e_steps = max(2, min(args.steps, 5))
@@ -757,7 +756,7 @@ def run_attention(args):
                "kernel": f"attention_fwd_kernel<{D}>", "ms_per_launch": ms},
             "e2e": {"value": ws * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                     "h2d_bytes_per_step": 3 * B * NH * T * D * 2,
-                    "d2h_bytes_per_step": B * NH * T * (D + 1) * 4, "ms_per_step": e2e_ms},
+                    "d2h_bytes_per_step": B * NH * T * (D * 2 + 4), "ms_per_step": e2e_ms},
             "cpu_baseline": cpu, "gpu_launches": launches, "clocks": clocks}), flush=True)
     if ws > 1:
         dist.barrier()

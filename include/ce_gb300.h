@@ -228,19 +228,23 @@ ce_status ce_gemm_bf16_tn(const void* A, int64_t lda, const void* B, int64_t ldb
  *   sm_scale the score scale (the page uses 1/sqrt(D)); positive, with a finite
  *            reciprocal (a mask entry enters as mask / sm_scale on the unscaled
  *            score, so finite entries must stay below 2^127 sm_scale in size).
- *   out      [B, NH, T, D] fp32, 16-byte aligned (device, caller-owned).
+ *   out      [B, NH, T, D] of out_dtype, 16-byte aligned (device, caller-owned).
+ *   out_dtype CE_F32, or CE_BF16 (the page's output is allocated like q).
  *   lse      [B, NH, T] fp32 (device) or NULL.
  * Arithmetic: bf16 products with fp32 accumulation for Q K^T; the softmax in
  * fp32 (exponentials in base 2 of the score times log2(e)); P is rounded to
- * bf16 for P V, accumulated in fp32.  A row whose every key is hidden gives
- * NaN outputs and lse = -inf (the definition's 0/0).
+ * bf16 for P V, accumulated in fp32; out = O / l in fp32, rounded to nearest
+ * even for CE_BF16.  A row whose every key is hidden gives NaN outputs and
+ * lse = -inf (the definition's 0/0).
  * Errors: null pointers, B, NH or T < 0, causal outside {0, 1}, sm_scale not
- * positive with a finite reciprocal, misaligned pointers -> CE_ERR_INVALID_ARG; D not 64 or 128, or T,
+ * positive with a finite reciprocal, out_dtype not a ce_dtype, misaligned
+ * pointers -> CE_ERR_INVALID_ARG; D not 64 or 128, out_dtype CE_F16, or T,
  * B*NH or B*NH*ceil(T/128) above 2^31-1 -> CE_ERR_UNSUPPORTED.
  */
 ce_status ce_attention_forward(const void* q, const void* k, const void* v, const float* mask,
                                int causal, int64_t B, int64_t NH, int64_t T, int64_t D,
-                               float sm_scale, float* out, float* lse, void* stream);
+                               float sm_scale, void* out, ce_dtype out_dtype, float* lse,
+                               void* stream);
 
 /*
  * ce_check_errors -- wait (at most timeout_ms) for `stream` to drain, then

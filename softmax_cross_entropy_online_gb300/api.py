@@ -42,7 +42,7 @@ SIGNATURES = {
     "ce_gemm_bf16": (_i32, [_vp, _i64, _i32, _vp, _i64, _i32, _vp, _i64, _i64, _i64, _i64, _f32,
                             _vp]),
     "ce_attention_forward": (_i32, [_vp, _vp, _vp, _vp, _i32, _i64, _i64, _i64, _i64, _f32,
-                                    _vp, _vp, _vp]),
+                                    _vp, _i32, _vp, _vp]),
     "ce_check_errors": (_i32, [_vp, _i32]),
     "ce_status_string": (ctypes.c_char_p, [_i32]),
     "ce_max_vocab": (_i64, [_i32]),
@@ -255,12 +255,13 @@ def ce_gemm_bf16(A: torch.Tensor, B: torch.Tensor, D: torch.Tensor | None = None
 def ce_attention_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
                          mask: torch.Tensor | None = None, *, causal: bool = False,
                          sm_scale: float | None = None, lse: bool = True, out=None,
-                         stream=None):
+                         out_dtype=torch.float32, stream=None):
     """Blockwise attention forward: softmax(Q K^T * sm_scale + mask [+ causal]) V.
 
     q, k, v: contiguous bf16 CUDA tensors [B, NH, T, D] (D 64 or 128); mask: fp32
-    [T, T] or None; sm_scale defaults to 1/sqrt(D).  Returns (out fp32
-    [B, NH, T, D], lse fp32 [B, NH, T] or None)."""
+    [T, T] or None; sm_scale defaults to 1/sqrt(D); out_dtype float32 or bfloat16
+    (ignored when `out` is given).  Returns (out [B, NH, T, D], lse fp32
+    [B, NH, T] or None)."""
     for name, t in (("q", q), ("k", k), ("v", v)):
         if (not t.is_cuda or t.dtype != torch.bfloat16 or t.dim() != 4 or not t.is_contiguous()
                 or t.shape != q.shape or t.device != q.device):
@@ -273,14 +274,15 @@ def ce_attention_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
     if sm_scale is None:
         sm_scale = 1.0 / math.sqrt(D)
     if out is None:
-        out = torch.empty((B, NH, T, D), dtype=torch.float32, device=q.device)
-    if (out.dtype != torch.float32 or tuple(out.shape) != (B, NH, T, D)
+        out = torch.empty((B, NH, T, D), dtype=out_dtype, device=q.device)
+    if (out.dtype not in (torch.float32, torch.bfloat16) or tuple(out.shape) != (B, NH, T, D)
             or not out.is_contiguous()):
-        raise ValueError("out must be a contiguous fp32 tensor [B, NH, T, D]")
+        raise ValueError("out must be a contiguous fp32 or bf16 tensor [B, NH, T, D]")
     lse_t = torch.empty((B, NH, T), dtype=torch.float32, device=q.device) if lse else None
     st = lib().ce_attention_forward(q.data_ptr(), k.data_ptr(), v.data_ptr(), _ptr(mask),
                                     int(bool(causal)), B, NH, T, D, float(sm_scale),
-                                    out.data_ptr(), _ptr(lse_t), _stream_handle(stream, q.device))
+                                    out.data_ptr(), _DTYPES[out.dtype], _ptr(lse_t),
+                                    _stream_handle(stream, q.device))
     _check(st, "ce_attention_forward")
     return out, lse_t
 

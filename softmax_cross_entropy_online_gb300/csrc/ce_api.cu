@@ -38,9 +38,9 @@ ce_status gemm_bf16(const void* A, long long lda, bool a_mn, const void* B, long
                     unsigned int wait_hint_ns);
 ce_status launch_mean_rows(const float* rl, long long M, float* loss, cudaStream_t st);
 ce_status attention_forward(const void* Q, const void* K, const void* V, const float* mask,
-                            int causal, int BH, int T, int D, float sm_scale, float* O, float* lse,
-                            cudaStream_t stream, unsigned int* err, int sm_count,
-                            unsigned int wait_hint_ns);
+                            int causal, int BH, int T, int D, float sm_scale, void* O,
+                            bool out_bf16, float* lse, cudaStream_t stream, unsigned int* err,
+                            int sm_count, unsigned int wait_hint_ns);
 }  // namespace ce
 
 namespace ce {
@@ -747,11 +747,14 @@ ce_status ce_gemm_bf16(const void* A, int64_t lda, int a_mn, const void* B, int6
 
 ce_status ce_attention_forward(const void* q, const void* k, const void* v, const float* mask,
                                int causal, int64_t B, int64_t NH, int64_t T, int64_t D,
-                               float sm_scale, float* out, float* lse, void* stream) {
+                               float sm_scale, void* out, ce_dtype out_dtype, float* lse,
+                               void* stream) {
   if (B < 0 || NH < 0 || T < 0 || (causal != 0 && causal != 1) || !std::isfinite(sm_scale) ||
       !(sm_scale > 0.f) || !std::isfinite(1.f / sm_scale))
     return CE_ERR_INVALID_ARG;
+  if (out_dtype != CE_F32 && out_dtype != CE_F16 && out_dtype != CE_BF16) return CE_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return CE_ERR_UNSUPPORTED;
+  if (out_dtype == CE_F16) return CE_ERR_UNSUPPORTED;
   const int64_t BH = B * NH;
   if (BH == 0 || T == 0) return CE_OK;
   if (q == nullptr || k == nullptr || v == nullptr || out == nullptr) return CE_ERR_INVALID_ARG;
@@ -767,7 +770,7 @@ ce_status ce_attention_forward(const void* q, const void* k, const void* v, cons
   ce_status st = device_info(di, &dev);
   if (st != CE_OK) return st;
   st = ce::attention_forward(q, k, v, mask, causal, static_cast<int>(BH), static_cast<int>(T),
-                             static_cast<int>(D), sm_scale, out, lse,
+                             static_cast<int>(D), sm_scale, out, out_dtype == CE_BF16, lse,
                              static_cast<cudaStream_t>(stream), di.err, di.sm_count,
                              wait_hint_ns());
   if (st == CE_OK) g_launches.fetch_add(1, std::memory_order_relaxed);

@@ -32,8 +32,9 @@
 //    of the row of O in TMEM after the previous P V has run), write
 //    P = 2^(s c - ref) as bf16 into TMEM and add it to their share of the
 //    normaliser l.  At the end of the item the two shares are summed and each
-//    thread stages its half of O / l in shared memory (one 32 x 32 block per
-//    warp at a time) for TMA tensor stores; lse is written by the first.
+//    thread stages its half of O / l (fp32, or rounded to bf16) in shared
+//    memory (one block per warp at a time) for TMA tensor stores; lse is
+//    written by the first.
 //  * exp is exp2 of the score in log2 units: s * sm_scale * log2(e).
 // Every mbarrier wait is bounded; TMEM is freed on every path.
 #include <cstring>
@@ -88,7 +89,8 @@ struct AttnSmem {
 constexpr float kRescaleLog2 = 8.f;
 
 
-template <int D>
+// OUT16: the output is rounded to bf16 (else fp32)
+template <int D, bool OUT16>
 __global__ void __launch_bounds__(kAttThreads, 1)
     attention_fwd_kernel(const __grid_constant__ CUtensorMap map_q,
                          const __grid_constant__ CUtensorMap map_k,
@@ -439,26 +441,58 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         p.lse[static_cast<long long>(bh) * p.T + row] = (mref + lg2(lt)) * 0.6931471805599453f;
       }
       const float inv_l = 1.f / lt;
-#pragma unroll 1
-      for (int cc = 0; cc < kOC; ++cc) {
-        const int col = 32 * (kOC * h + cc);
-        float o[32];
-        tmem_ld32(tmem + kAttTmemO + col + lane_off, o);
+      if constexpr (OUT16) {
+        // this thread's half of the row, rounded to bf16: D bytes, one staging
+        // row (128-byte rows with the 128-byte swizzle for D = 128, plain
+        // 64-byte rows for D = 64) and one TMA store per warp
+        uint32_t pk[D / 4];
+#pragma unroll
+        for (int cc = 0; cc < kOC; ++cc) {
+          float o[32];
+          tmem_ld32(tmem + kAttTmemO + 32 * (kOC * h + cc) + lane_off, o);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            __nv_bfloat162 hv = __floats2bfloat162_rn(o[2 * i] * inv_l, o[2 * i + 1] * inv_l);
+            pk[16 * cc + i] = *reinterpret_cast<uint32_t*>(&hv);
+          }
+        }
         // the staging block: the store issued before has read it
         if (lane == 0) bulk_wait_read<0>();
         __syncwarp();
 #pragma unroll
-        for (int jj = 0; jj < 8; ++jj)
-          asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(
-                           ebuf + lane * 128 + 16 * (jj ^ (lane & 7))),
-                       "f"(o[4 * jj] * inv_l), "f"(o[4 * jj + 1] * inv_l),
-                       "f"(o[4 * jj + 2] * inv_l), "f"(o[4 * jj + 3] * inv_l)
-                       : "memory");
+        for (int jj = 0; jj < D / 16; ++jj) {
+          const uint32_t a = (D == 128) ? ebuf + lane * 128 + 16 * (jj ^ (lane & 7))
+                                        : ebuf + lane * 64 + 16 * jj;
+          sts128(a, make_uint4(pk[4 * jj], pk[4 * jj + 1], pk[4 * jj + 2], pk[4 * jj + 3]));
+        }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0 && qt * kAttBQ + 32 * q < p.T) {  // blocks wholly past T are not stored
-          tma_store_3d(&map_o, ebuf, col, qt * kAttBQ + 32 * q, bh);
+          tma_store_3d(&map_o, ebuf, (D / 2) * h, qt * kAttBQ + 32 * q, bh);
           bulk_commit();
+        }
+      } else {
+#pragma unroll 1
+        for (int cc = 0; cc < kOC; ++cc) {
+          const int col = 32 * (kOC * h + cc);
+          float o[32];
+          tmem_ld32(tmem + kAttTmemO + col + lane_off, o);
+          // the staging block: the store issued before has read it
+          if (lane == 0) bulk_wait_read<0>();
+          __syncwarp();
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj)
+            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(
+                             ebuf + lane * 128 + 16 * (jj ^ (lane & 7))),
+                         "f"(o[4 * jj] * inv_l), "f"(o[4 * jj + 1] * inv_l),
+                         "f"(o[4 * jj + 2] * inv_l), "f"(o[4 * jj + 3] * inv_l)
+                         : "memory");
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0 && qt * kAttBQ + 32 * q < p.T) {  // blocks wholly past T are not stored
+            tma_store_3d(&map_o, ebuf, col, qt * kAttBQ + 32 * q, bh);
+            bulk_commit();
+          }
         }
       }
       tc_fence_before();
@@ -494,7 +528,8 @@ static PFN_cuTensorMapEncodeTiled_v12000 att_encode_fn() {
 
 // 3-D map over [BH, T, D] (D contiguous) with a box of box_d x box_t x 1
 static bool att_map(CUtensorMap* map, CUtensorMapDataType type, int esize, const void* base,
-                    int BH, int T, int D, int box_d, int box_t) {
+                    int BH, int T, int D, int box_d, int box_t,
+                    CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   auto fn = att_encode_fn();
   if (fn == nullptr) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(T),
@@ -504,20 +539,22 @@ static bool att_map(CUtensorMap* map, CUtensorMapDataType type, int esize, const
   cuuint32_t box[3] = {static_cast<cuuint32_t>(box_d), static_cast<cuuint32_t>(box_t), 1u};
   cuuint32_t estr[3] = {1, 1, 1};
   return fn(map, type, 3, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D>
+template <int D, bool OUT16>
 static ce_status attention_launch(const void* Q, const void* K, const void* V, const float* mask,
-                                  int causal, int BH, int T, float sm_scale, float* O, float* lse,
+                                  int causal, int BH, int T, float sm_scale, void* O, float* lse,
                                   cudaStream_t stream, unsigned int* err, int sm_count,
                                   unsigned int wait_hint_ns) {
   CUtensorMap mq, mk, mv, mo;
   if (!att_map(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Q, BH, T, D, 64, kAttBQ) ||
       !att_map(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, BH, T, D, 64, kAttBK) ||
       !att_map(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, V, BH, T, D, 64, 64) ||
-      !att_map(&mo, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, O, BH, T, D, 32, 32))
+      !(OUT16 ? att_map(&mo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, O, BH, T, D, D / 2, 32,
+                        D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE)
+              : att_map(&mo, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, O, BH, T, D, 32, 32)))
     return CE_ERR_CUDA;
   AttnParams p;
   p.mask = mask;
@@ -536,31 +573,35 @@ static ce_status attention_launch(const void* Q, const void* K, const void* V, c
   // 512 TMEM columns per CTA: the shared-memory request keeps one CTA per SM,
   // so no CTA ever waits in tcgen05.alloc for a neighbour to finish
   const int smem = AttnSmem<D>::kTotal > (128 << 10) ? AttnSmem<D>::kTotal : (128 << 10);
-  if (cudaFuncSetAttribute(attention_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(attention_fwd_kernel<D, OUT16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            smem) != cudaSuccess)
     return CE_ERR_CUDA;
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attention_fwd_kernel<D>, kAttThreads,
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attention_fwd_kernel<D, OUT16>, kAttThreads,
                                                     smem) != cudaSuccess ||
       per_sm < 1)
     return CE_ERR_CUDA;
   if (per_sm != 1) return CE_ERR_UNSUPPORTED;
   long long grid = sm_count;
   if (grid > p.n_units) grid = p.n_units;
-  attention_fwd_kernel<D><<<static_cast<int>(grid), kAttThreads, smem, stream>>>(mq, mk, mv, mo, p);
+  attention_fwd_kernel<D, OUT16><<<static_cast<int>(grid), kAttThreads, smem, stream>>>(mq, mk, mv, mo, p);
   return cudaGetLastError() == cudaSuccess ? CE_OK : CE_ERR_CUDA;
 }
 
 ce_status attention_forward(const void* Q, const void* K, const void* V, const float* mask,
-                            int causal, int BH, int T, int D, float sm_scale, float* O, float* lse,
-                            cudaStream_t stream, unsigned int* err, int sm_count,
-                            unsigned int wait_hint_ns) {
+                            int causal, int BH, int T, int D, float sm_scale, void* O,
+                            bool out_bf16, float* lse, cudaStream_t stream, unsigned int* err,
+                            int sm_count, unsigned int wait_hint_ns) {
   if (D == 64)
-    return attention_launch<64>(Q, K, V, mask, causal, BH, T, sm_scale, O, lse, stream, err,
-                                sm_count, wait_hint_ns);
+    return out_bf16 ? attention_launch<64, true>(Q, K, V, mask, causal, BH, T, sm_scale, O, lse,
+                                                 stream, err, sm_count, wait_hint_ns)
+                    : attention_launch<64, false>(Q, K, V, mask, causal, BH, T, sm_scale, O, lse,
+                                                  stream, err, sm_count, wait_hint_ns);
   if (D == 128)
-    return attention_launch<128>(Q, K, V, mask, causal, BH, T, sm_scale, O, lse, stream, err,
-                                 sm_count, wait_hint_ns);
+    return out_bf16 ? attention_launch<128, true>(Q, K, V, mask, causal, BH, T, sm_scale, O, lse,
+                                                  stream, err, sm_count, wait_hint_ns)
+                    : attention_launch<128, false>(Q, K, V, mask, causal, BH, T, sm_scale, O,
+                                                   lse, stream, err, sm_count, wait_hint_ns);
   return CE_ERR_UNSUPPORTED;
 }
 

@@ -117,27 +117,30 @@ def test_product_path_never_imports_the_oracle():
 
 
 @pytest.mark.parametrize("args, status", [
-    # (q, k, v, mask, causal, B, NH, T, D, sm_scale, out, lse) -> status, before any CUDA call
-    ((16, 16, 16, None, 2, 1, 1, 8, 64, 0.125, 16, None), 1),           # causal not 0/1
-    ((16, 16, 16, None, 0, -1, 1, 8, 64, 0.125, 16, None), 1),          # B < 0
-    ((16, 16, 16, None, 0, 1, 1, -8, 64, 0.125, 16, None), 1),          # T < 0
-    ((16, 16, 16, None, 0, 1, 1, 8, 64, float("nan"), 16, None), 1),    # sm_scale not finite
-    ((16, 16, 16, None, 0, 1, 1, 8, 64, float("inf"), 16, None), 1),
-    ((16, 16, 16, None, 0, 1, 1, 8, 64, 0.0, 16, None), 1),             # sm_scale not > 0
-    ((16, 16, 16, None, 0, 1, 1, 8, 64, -0.125, 16, None), 1),
-    ((16, 16, 16, None, 0, 1, 1, 8, 64, 1e-39, 16, None), 1),           # 1 / sm_scale overflows
-    ((16, 16, 16, None, 0, 1, 1, 8, 96, 0.125, 16, None), 2),           # D not 64 / 128
-    ((16, 16, 16, None, 0, 1, 1, 8, 32, 0.125, 16, None), 2),
-    ((None, 16, 16, None, 0, 1, 1, 8, 64, 0.125, 16, None), 1),         # null q
-    ((16, 16, 16, None, 0, 1, 1, 8, 64, 0.125, None, None), 1),         # null out
-    ((24, 16, 16, None, 0, 1, 1, 8, 64, 0.125, 16, None), 1),           # q not 16-byte aligned
-    ((16, 16, 16, None, 0, 1, 1, 8, 64, 0.125, 40, None), 1),           # out not 16-byte aligned
-    ((16, 16, 16, 18, 0, 1, 1, 8, 64, 0.125, 16, None), 1),             # mask misaligned
-    ((16, 16, 16, None, 0, 1, 1, 8, 64, 0.125, 16, 18), 1),             # lse misaligned
-    ((16, 16, 16, None, 0, 1, 1, 1 << 31, 64, 0.125, 16, None), 2),     # T above 2^31 - 1
-    ((16, 16, 16, None, 0, 1, 1 << 30, 1024, 64, 0.125, 16, None), 2),  # 2^33 query tiles
-    ((None, None, None, None, 0, 0, 4, 8, 64, 0.125, None, None), 0),   # B = 0: nothing to do
-    ((None, None, None, None, 1, 2, 4, 0, 128, 0.125, None, None), 0),  # T = 0: nothing to do
+    # (q, k, v, mask, causal, B, NH, T, D, sm_scale, out, out_dtype, lse) -> status,
+    # before any CUDA call
+    ((16, 16, 16, None, 2, 1, 1, 8, 64, 0.125, 16, 0, None), 1),           # causal not 0/1
+    ((16, 16, 16, None, 0, -1, 1, 8, 64, 0.125, 16, 0, None), 1),          # B < 0
+    ((16, 16, 16, None, 0, 1, 1, -8, 64, 0.125, 16, 0, None), 1),          # T < 0
+    ((16, 16, 16, None, 0, 1, 1, 8, 64, float("nan"), 16, 0, None), 1),    # sm_scale not finite
+    ((16, 16, 16, None, 0, 1, 1, 8, 64, float("inf"), 16, 0, None), 1),
+    ((16, 16, 16, None, 0, 1, 1, 8, 64, 0.0, 16, 0, None), 1),             # sm_scale not > 0
+    ((16, 16, 16, None, 0, 1, 1, 8, 64, -0.125, 16, 0, None), 1),
+    ((16, 16, 16, None, 0, 1, 1, 8, 64, 1e-39, 16, 0, None), 1),           # 1 / sm_scale overflows
+    ((16, 16, 16, None, 0, 1, 1, 8, 96, 0.125, 16, 0, None), 2),           # D not 64 / 128
+    ((16, 16, 16, None, 0, 1, 1, 8, 32, 0.125, 16, 0, None), 2),
+    ((None, 16, 16, None, 0, 1, 1, 8, 64, 0.125, 16, 0, None), 1),         # null q
+    ((16, 16, 16, None, 0, 1, 1, 8, 64, 0.125, None, 0, None), 1),         # null out
+    ((24, 16, 16, None, 0, 1, 1, 8, 64, 0.125, 16, 0, None), 1),           # q not 16-byte aligned
+    ((16, 16, 16, None, 0, 1, 1, 8, 64, 0.125, 40, 0, None), 1),           # out not 16-byte aligned
+    ((16, 16, 16, 18, 0, 1, 1, 8, 64, 0.125, 16, 0, None), 1),             # mask misaligned
+    ((16, 16, 16, None, 0, 1, 1, 8, 64, 0.125, 16, 0, 18), 1),             # lse misaligned
+    ((16, 16, 16, None, 0, 1, 1, 1 << 31, 64, 0.125, 16, 0, None), 2),     # T above 2^31 - 1
+    ((16, 16, 16, None, 0, 1, 1 << 30, 1024, 64, 0.125, 16, 0, None), 2),  # 2^33 query tiles
+    ((None, None, None, None, 0, 0, 4, 8, 64, 0.125, None, 0, None), 0),   # B = 0: nothing to do
+    ((None, None, None, None, 1, 2, 4, 0, 128, 0.125, None, 0, None), 0),  # T = 0: nothing to do
+    ((16, 16, 16, None, 0, 1, 1, 8, 64, 0.125, 16, 7, None), 1),         # out_dtype not a ce_dtype
+    ((16, 16, 16, None, 0, 1, 1, 8, 64, 0.125, 16, 1, None), 2),         # fp16 output
 ])
 def test_attention_host_validation(cdll, args, status):
     assert cdll.ce_attention_forward(*args, None) == status

@@ -95,5 +95,6 @@ def test_attention_flop_and_byte_counts():
     # 4 D flops per visible (query, key) pair: T (T + 1) / 2 pairs per head under the causal mask
     assert bench.attention_flops(1, 1, 4, 8, True) == 4 * 8 * 10
     assert bench.attention_flops(2, 3, 4, 8, False) == 4 * 8 * 16 * 6
-    # one read of bf16 q, k, v and one write of the fp32 output and lse
-    assert bench.attention_bytes(1, 1, 4, 8) == 3 * 32 * 2 + 32 * 4 + 4 * 4
+    # one read of bf16 q, k, v and one write of the output (bf16 by default) and fp32 lse
+    assert bench.attention_bytes(1, 1, 4, 8) == 3 * 32 * 2 + 32 * 2 + 4 * 4
+    assert bench.attention_bytes(1, 1, 4, 8, out_bytes=4) == 3 * 32 * 2 + 32 * 4 + 4 * 4
