@@ -568,7 +568,11 @@ ATTN_SOURCES = ("ce_attention.cu", "ce_tc.cuh")
 # DRAM traffic of the attention kernel per launch on the workload above, from
 # `ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum` (summarised under
 # profiles/), valid only for the attention sources it was taken on.
-ATTN_NCU_TRAFFIC = {}
+ATTN_NCU_TRAFFIC = {
+    # profiles/attention_fwd_bf16_32x96x512x128_causal.md
+    "16de8cae8d85bb884168924649d0aff882936177a8c64a1ef1f20e5987193f9c": {
+        "workload": "attn_causal_32x96x512x128", "bytes_per_launch": 1598912512},
+}
 
 
 def attention_digest() -> str:
