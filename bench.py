@@ -492,6 +492,8 @@ def run_linear(args):
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
     sampler = ClockSampler(local) if rank == 0 else None
     if sampler:
         sampler.start()
@@ -505,7 +507,7 @@ def run_linear(args):
     torch.cuda.synchronize()
     launches = api.ce_launch_count() - n0
     clocks = sampler.stop() if sampler else None
-    ms = e0.elapsed_time(e1) / args.steps
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dev)
     flops = 6.0 * M * V * H  # logits, dH and dW GEMMs
     value = ws * flops / (ms * 1e-3) / 1e12
     assert api.ce_check_errors() == 0
@@ -537,7 +539,7 @@ def run_linear(args):
         loss_host.copy_(loss, non_blocking=True)
     x1.record()
     torch.cuda.synchronize()
-    e2e_ms = x0.elapsed_time(x1) / e2e_steps
+    e2e_ms = max_over_ranks(x0.elapsed_time(x1) / e2e_steps, dev)
     if rank == 0:
         line = {
             "metric": "fused linear+CE fwd+bwd TFLOP/s (6 M V H per step)", "value": value,
@@ -557,6 +559,9 @@ def run_linear(args):
             "gpu_launches": launches, "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.barrier()
+        dist.destroy_process_group()
     return 0
 
 
