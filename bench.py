@@ -46,7 +46,7 @@ FALLBACK_HBM_GBS = 6800.0
 # digest of the row-kernel sources at that time.  Any change to them nulls it.
 NCU_TRAFFIC = {
     # profiles/ce_rows_fwd_bwd_f32_32768x4096.md: a 16384-row capture, scaled 2x
-    "fe1f47a1fdc6a8a4b946069de7e0f2ff6fb94d3d9d4ea86ab50c670791ec8fa8": {
+    "a97261e124c3c92b0b799fbd3601857d99454c30818709898eb0b4e655ccceee": {
         "workload": "f32_32768x4096", "bytes_per_launch": 950148096},
 }
 
