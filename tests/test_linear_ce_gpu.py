@@ -5,9 +5,13 @@ linear_ce for the fused path).
 Tolerances.  h and W are exact bf16 values, so every product is exact in
 fp32; the GEMM accumulates in fp32 on the tensor cores: |D - D_ref| <=
 1e-5 * (|A| |B|^T) covers K up to several thousand terms at 2^-24 per step.
-The gradients use G rounded to bf16 (relative 2^-9) and fp32 accumulation:
+The gradients use G rounded to bf16 (relative error at most 2^-8, the unit
+roundoff of an 8-bit significand) and fp32 accumulation:
 |dH - dH_ref| <= 2^-8 (|G| |W|) and |dW - dW_ref| <= 2^-8 (|G|^T |h|),
-elementwise, with G the float64 reference gradient.  The loss follows the
+elementwise, with G the float64 reference gradient: the bound is the worst case
+of the rounding alone; the fp32 errors of the logits and of the accumulations
+(up to 128256 terms) stay far below theirs, because the terms' rounding errors
+do not all share one sign, and the float64 comparison shows it.  The loss follows the
 16-bit-input rule (2e-3).
 """
 
