@@ -24,6 +24,7 @@ import dataclasses
 import hashlib
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -197,12 +198,28 @@ def run_reference(args, w):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
         "config": {"workload": workload_desc(w), "M": w.M, "V": w.V, "sample_rows": sample_rows},
-        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle", **host_info(),
                          "sample": sample},
         "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+def host_info() -> dict:
+    """The host the oracle ran on: its CPU count and model (recorded beside the
+    single-thread figure)."""
+    model = platform.processor() or platform.machine()
+    try:
+        with open("/proc/cpuinfo") as fh:
+            for line in fh:
+                key = line.split(":")[0].strip().lower()
+                if key in ("model name", "cpu part", "hardware"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    return {"host_cpus": os.cpu_count(), "host_cpu": model, "host_arch": platform.machine()}
 
 
 def workload_desc(w):
@@ -226,7 +243,7 @@ def cpu_baseline(w, budget_s: float):
     oracle.ce_fwd_bwd(oracle.to_f64(x, w.dtype), t, "mean")
     dt = time.perf_counter() - t0
     gbs = algorithmic_bytes(rows, w.V, es, True) / dt / 1e9
-    return {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+    return {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle", **host_info(),
             "sample": f"{rows} of {w.M} rows of {w.name}, fwd+bwd in float64 numpy "
                       f"({dt:.1f} s on 1 host thread)"}
 
@@ -659,7 +676,7 @@ def run_attention(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": desc, "B": B, "NH": NH, "T": T, "D": D},
-            "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+            "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": 1, "kind": "oracle", **host_info(),
                              "sample": sample},
             "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}), flush=True)
@@ -740,7 +757,7 @@ def run_attention(args):
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         cv, hs, secs = attention_oracle_sample(B, NH, T, D, causal, args.cpu_budget_s)
-        cpu = {"value": cv, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+        cpu = {"value": cv, "unit": "TFLOP/s", "cores": 1, "kind": "oracle", **host_info(),
                "sample": f"{hs} of {B * NH} heads in float64 numpy ({secs:.1f} s on 1 host "
                          "thread)"}
     if rank == 0:
