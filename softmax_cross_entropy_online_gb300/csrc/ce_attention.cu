@@ -15,15 +15,17 @@
 // are read from L2; under the causal mask query tiles are paired so every
 // work unit costs the same):
 //  * warp 0 (one thread) loads each item's Q tile (two buffers: the next
-//    item's Q arrives while this one computes) and streams K and V tiles of
-//    128 keys into two-stage rings with TMA (128-byte swizzle; K K-major for
-//    S = Q K^T, V MN-major for O = P V, so neither is transposed); K runs one
-//    tile ahead of V, each K stage refilled once its score MMA has read it;
+//    item's Q arrives while this one computes) and streams K tiles of 128
+//    keys into a three-stage ring and V tiles into a two-stage ring with TMA
+//    (128-byte swizzle; K K-major for S = Q K^T, V MN-major for O = P V, so
+//    neither is transposed); K runs one tile ahead of V, each K stage
+//    refilled once its score MMA has read it;
 //  * warp 1 allocates all 512 TMEM columns -- two 128 x 128 fp32 score
 //    buffers, the D-column output accumulator, two bf16 weight buffers P --
-//    and one thread issues the MMAs: S_{j+1} = Q K_{j+1}^T before
-//    O += P_j V_j (A operand P read from TMEM), so the tensor cores compute
-//    the next scores while the softmax warps work on these;
+//    and one thread issues the MMAs: scores run two tiles ahead, S_{j+2} =
+//    Q K_{j+2}^T issued as soon as the softmax holds S_j in registers and
+//    before O += P_j V_j (A operand P read from TMEM), so the tensor cores
+//    always have the next scores queued while the softmax warps work;
 //  * warps 2..9 give each query row two threads (TMEM lane = row; two warps
 //    per lane quarter), each with 64 of a tile's 128 keys: they load those
 //    scores into registers (freeing the score buffer), swap partial maxima
@@ -34,7 +36,9 @@
 //    normaliser l.  At the end of the item the two shares are summed and each
 //    thread stages its half of O / l (fp32, or rounded to bf16) in shared
 //    memory (one block per warp at a time) for TMA tensor stores; lse is
-//    written by the first.
+//    written by the first.  For D = 128 the staging blocks are the item's own
+//    Q buffer (its score MMAs have all run by then), which the producer
+//    reloads only after each warp's stores have read it.
 //  * exp is exp2 of the score in log2 units: s * sm_scale * log2(e).
 // Every mbarrier wait is bounded; TMEM is freed on every path.
 #include <cstring>
@@ -74,13 +78,18 @@ struct AttnParams {
   unsigned int wait_hint_ns;
 };
 
+constexpr int kAttKStages = 3;  // K ring depth: scores run two tiles ahead
 template <int D>
 struct AttnSmem {
   static constexpr int kQ = kAttBQ * D * 2;  // Q: D / 64 K-major blocks of 128 rows x 128 B
   static constexpr int kK = kAttBK * D * 2;  // K: the same layout
   static constexpr int kV = kAttBK * D * 2;  // V: D / 64 MN-major blocks of 128 keys x 128 B
-  static constexpr int kStage = kAttSoftmaxWarps * 4096;  // output staging: 32 rows x 128 B a warp
-  static constexpr int kTotal = 2 * (kQ + kK + kV) + kStage + 1024;  // + alignment slack
+  // output staging: 32 rows x 128 B a warp, in the item's own Q buffer when it
+  // is large enough (its score MMAs have all run by then), else a region of its own
+  static constexpr int kStageNeed = kAttSoftmaxWarps * 4096;
+  static constexpr bool kStageInQ = kQ >= kStageNeed;
+  static constexpr int kStage = kStageInQ ? 0 : kStageNeed;
+  static constexpr int kTotal = 2 * kQ + kAttKStages * kK + 2 * kV + kStage + 1024;  // + slack
 };
 
 // The reference max of a row moves only when a tile's max exceeds it by more
@@ -99,7 +108,8 @@ __global__ void __launch_bounds__(kAttThreads, 1)
   using L = AttnSmem<D>;
   extern __shared__ unsigned char att_smem[];
   __shared__ __align__(8) unsigned long long q_full[2], q_empty[2], o_free;
-  __shared__ __align__(8) unsigned long long k_full[2], k_empty[2], v_full[2], v_empty[2];
+  __shared__ __align__(8) unsigned long long k_full[kAttKStages], k_empty[kAttKStages];
+  __shared__ __align__(8) unsigned long long v_full[2], v_empty[2];
   __shared__ __align__(8) unsigned long long s_full[2], s_free[2];
   __shared__ __align__(8) unsigned long long p_full[2], pv_done[2];
   __shared__ uint32_t tmem_slot;
@@ -108,10 +118,10 @@ __global__ void __launch_bounds__(kAttThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t base = (smem_u32(att_smem) + 1023u) & ~1023u;  // swizzle atoms need 1024 B
-  const uint32_t sq0 = base;                // two Q buffers (items alternate)
-  const uint32_t sk0 = sq0 + 2 * L::kQ;     // two K stages
-  const uint32_t sv0 = sk0 + 2 * L::kK;     // two V stages
-  const uint32_t so0 = sv0 + 2 * L::kV;     // output staging
+  const uint32_t sq0 = base;                      // two Q buffers (items alternate)
+  const uint32_t sk0 = sq0 + 2 * L::kQ;           // three K stages
+  const uint32_t sv0 = sk0 + kAttKStages * L::kK; // two V stages
+  const uint32_t so0 = sv0 + 2 * L::kV;           // output staging (when not in Q)
   bool failed = false;
   const unsigned int hint = p.wait_hint_ns;
 
@@ -119,15 +129,19 @@ __global__ void __launch_bounds__(kAttThreads, 1)
     mbar_init(smem_u32(&o_free), kAttSoftmax);
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&q_full[s]), 1);
-      mbar_init(smem_u32(&q_empty[s]), 1);
-      mbar_init(smem_u32(&k_full[s]), 1);
-      mbar_init(smem_u32(&k_empty[s]), 1);
+      // the score MMAs' commit and, when the output is staged in the Q buffer,
+      // each softmax warp once its stores have read it
+      mbar_init(smem_u32(&q_empty[s]), 1 + (L::kStageInQ ? kAttSoftmaxWarps : 0));
       mbar_init(smem_u32(&v_full[s]), 1);
       mbar_init(smem_u32(&v_empty[s]), 1);
       mbar_init(smem_u32(&s_full[s]), 1);
       mbar_init(smem_u32(&s_free[s]), kAttSoftmax);
       mbar_init(smem_u32(&p_full[s]), kAttSoftmax);
       mbar_init(smem_u32(&pv_done[s]), 1);
+    }
+    for (int s = 0; s < kAttKStages; ++s) {
+      mbar_init(smem_u32(&k_full[s]), 1);
+      mbar_init(smem_u32(&k_empty[s]), 1);
     }
     fence_mbar_init_cluster();
   }
@@ -194,7 +208,8 @@ __global__ void __launch_bounds__(kAttThreads, 1)
           int bh, qt;
           item_of(u, sub, bh, qt);
           const int n = tiles_of(qt);
-          // Q buffer it % 2: the score MMAs of item it - 2 have read it
+          // Q buffer it % 2: the score MMAs of item it - 2 have read it (and the
+          // stores of that item's output, staged there, have read it)
           const int qb = it & 1;
           if (it >= 2)
             mbar_wait<false>(smem_u32(&q_empty[qb]), static_cast<uint32_t>(((it >> 1) - 1) & 1),
@@ -204,10 +219,11 @@ __global__ void __launch_bounds__(kAttThreads, 1)
             tma_load_3d(sq0 + qb * L::kQ + kb * 16384, &map_q, 64 * kb, qt * kAttBQ, bh,
                         smem_u32(&q_full[qb]));
           for (int j = 0; j < n; ++j, ++g) {
-            const int st = static_cast<int>(g & 1);
-            if (g >= 2)
-              mbar_wait<false>(smem_u32(&k_empty[st]), static_cast<uint32_t>(((g >> 1) - 1) & 1),
-                               p.err, failed, WAIT_LIMIT_NS, hint);
+            const int st = static_cast<int>(g % kAttKStages);
+            if (g >= kAttKStages)
+              mbar_wait<false>(smem_u32(&k_empty[st]),
+                               static_cast<uint32_t>((g / kAttKStages - 1) & 1), p.err, failed,
+                               WAIT_LIMIT_NS, hint);
             const uint32_t fb = smem_u32(&k_full[st]);
             mbar_arrive_expect_tx(fb, L::kK);
             for (int kb = 0; kb < D / 64; ++kb)
@@ -225,12 +241,13 @@ __global__ void __launch_bounds__(kAttThreads, 1)
       for (int t = it - 2 < 0 ? 0 : it - 2; t < it; ++t)
         mbar_wait<false>(smem_u32(&q_full[t & 1]), static_cast<uint32_t>((t >> 1) & 1), p.err,
                          drain_failed, WAIT_LIMIT_NS, hint);
-      for (long long t = g - 2 < 0 ? 0 : g - 2; t < g; ++t) {
-        mbar_wait<false>(smem_u32(&k_full[t & 1]), static_cast<uint32_t>((t >> 1) & 1), p.err,
-                         drain_failed, WAIT_LIMIT_NS, hint);
+      for (long long t = g - kAttKStages < 0 ? 0 : g - kAttKStages; t < g; ++t)
+        mbar_wait<false>(smem_u32(&k_full[t % kAttKStages]),
+                         static_cast<uint32_t>((t / kAttKStages) & 1), p.err, drain_failed,
+                         WAIT_LIMIT_NS, hint);
+      for (long long t = g - 2 < 0 ? 0 : g - 2; t < g; ++t)
         mbar_wait<false>(smem_u32(&v_full[t & 1]), static_cast<uint32_t>((t >> 1) & 1), p.err,
                          drain_failed, WAIT_LIMIT_NS, hint);
-      }
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -245,15 +262,18 @@ __global__ void __launch_bounds__(kAttThreads, 1)
       long long gp = 0;  // P V tiles issued, over all items
       int it = 0;
       uint32_t sq = sq0;  // this item's Q buffer
+      // S_gs into score buffer gs % 2 from K stage gs % 3, once the softmax holds
+      // the buffer's previous scores (tile gs - 2) in registers
       auto issue_s = [&](long long gs) {
-        const int st = static_cast<int>(gs & 1);  // K stage and score buffer alternate alike
-        mbar_wait<false>(smem_u32(&k_full[st]), static_cast<uint32_t>((gs >> 1) & 1), p.err,
-                         failed, WAIT_LIMIT_NS, hint);
+        const int st = static_cast<int>(gs & 1);
+        const int ks = static_cast<int>(gs % kAttKStages);
+        mbar_wait<false>(smem_u32(&k_full[ks]), static_cast<uint32_t>((gs / kAttKStages) & 1),
+                         p.err, failed, WAIT_LIMIT_NS, hint);
         if (gs >= 2)
           mbar_wait<false>(smem_u32(&s_free[st]), static_cast<uint32_t>(((gs >> 1) - 1) & 1),
                            p.err, failed, WAIT_LIMIT_NS, hint);
         tc_fence_after();
-        const uint32_t sk = sk0 + st * L::kK;
+        const uint32_t sk = sk0 + ks * L::kK;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
@@ -261,7 +281,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
                     kk > 0 ? 1u : 0u);
         }
         umma_commit(smem_u32(&s_full[st]));
-        umma_commit(smem_u32(&k_empty[st]));
+        umma_commit(smem_u32(&k_empty[ks]));
       };
       for (int u = blockIdx.x; u < p.n_units; u += gridDim.x)
       for (int sub = 0; sub < items_in(u); ++sub, ++it) {
@@ -273,10 +293,16 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         mbar_wait<false>(smem_u32(&q_full[qb]), static_cast<uint32_t>((it >> 1) & 1), p.err,
                          failed, WAIT_LIMIT_NS, hint);
         tc_fence_after();
+        // scores run two tiles ahead of P V: S_{j+2} is issued as soon as the
+        // softmax has read S_j, before P V of tile j
         issue_s(g++);
+        if (n > 1) issue_s(g++);
+        if (n <= 2) umma_commit(smem_u32(&q_empty[qb]));  // every MMA reading Q is issued
         for (int j = 0; j < n; ++j) {
-          if (j + 1 < n) issue_s(g++);
-          if (j + 1 == n) umma_commit(smem_u32(&q_empty[qb]));  // every MMA reading Q is issued
+          if (j + 2 < n) {
+            issue_s(g++);
+            if (j + 3 == n) umma_commit(smem_u32(&q_empty[qb]));
+          }
           // the previous item's output has been read out of TMEM
           if (j == 0 && it > 0)
             mbar_wait<false>(smem_u32(&o_free), static_cast<uint32_t>((it - 1) & 1), p.err, failed,
@@ -313,7 +339,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
     const int h = (warp - 2) >> 2;    // which 64 keys of each tile (and half of O's columns)
     const int r = 32 * q + lane;
     const uint32_t lane_off = static_cast<uint32_t>(32 * q) << 16;
-    const uint32_t ebuf = so0 + (warp - 2) * 4096;  // this warp's output staging block
+    const uint32_t eoff = (warp - 2) * 4096;  // this warp's output staging block
     const float c = p.scale_log2;                   // > 0: the max of s * c is c * max(s)
     constexpr int kOC = D / 64;                     // output chunks of 32 columns per thread
     // wait until P V of global tile t has finished
@@ -343,6 +369,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
                                                         : nullptr;
       float m_ref = -INFINITY;  // reference max of O and l (log2 units), the same in both threads
       float l = 0.f;            // this thread's share of the normaliser, relative to m_ref
+      const uint32_t ebuf = (L::kStageInQ ? sq0 + (it & 1) * L::kQ : so0) + eoff;
       for (int j = 0; j < n; ++j, ++g) {
         const int st = static_cast<int>(g & 1);
         mbar_wait<false>(smem_u32(&s_full[st]), static_cast<uint32_t>((g >> 1) & 1), p.err,
@@ -356,6 +383,14 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         // the scores are in registers: the buffer may take the next tile's scores
         tc_fence_before();
         mbar_arrive(smem_u32(&s_free[st]));
+        if (L::kStageInQ && j == 0 && it > 0) {
+          // the previous item's output stores have read its Q buffer: release it
+          if (lane == 0) {
+            bulk_wait_read<0>();
+            mbar_arrive(smem_u32(&q_empty[(it - 1) & 1]));
+          }
+          __syncwarp();
+        }
         float* x = reinterpret_cast<float*>(sr);
         const int kv0 = j * kAttBK + 64 * h;  // this thread's first key
         // one decision for the whole CTA: does any key of this tile need a mask?
