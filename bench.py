@@ -592,8 +592,8 @@ ATTN_SOURCES = ("ce_attention.cu", "ce_tc.cuh")
 # profiles/), valid only for the attention sources it was taken on.
 ATTN_NCU_TRAFFIC = {
     # profiles/attention_fwd_bf16_32x96x512x128_causal.md
-    "7d2cd03735f517f920a7202f11b9a6814b27c9a0fcd5e6b62f2afb8adce21486": {
-        "workload": "attn_causal_32x96x512x128", "bytes_per_launch": 1592968448},
+    "16dab2fec8146bfc2035d7edd17ebeba680df01bf7b477ce2a3d748dcfad31fb": {
+        "workload": "attn_causal_32x96x512x128", "bytes_per_launch": 1592443392},
 }
 
 

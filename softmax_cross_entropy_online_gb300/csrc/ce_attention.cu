@@ -39,7 +39,11 @@
 //    written by the first.  For D = 128 the staging blocks are the item's own
 //    Q buffer (its score MMAs have all run by then), which the producer
 //    reloads only after each warp's stores have read it.
-//  * exp is exp2 of the score in log2 units: s * sm_scale * log2(e).
+//  * exp is exp2 of the score in log2 units: s * sm_scale * log2(e).  The
+//    softmax warps issue the most instructions per tile, so the exponent
+//    arguments and the normaliser's partial sums use paired fp32 instructions
+//    (fma / add .f32x2, rounded as the scalar ones) and the tile max a
+//    three-input max: the same results from fewer instructions.
 // Every mbarrier wait is bounded; TMEM is freed on every path.
 #include <cstring>
 
@@ -97,6 +101,29 @@ struct AttnSmem {
 // exact enough in fp32 and bf16, and the accumulator is not rescaled.
 constexpr float kRescaleLog2 = 8.f;
 
+// two fp32 FMAs (or adds) in one instruction, each rounded as the scalar one
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n .reg .b64 ra, rb, rc, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+      " mov.b64 rc, {%6, %7};\n fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+      " add.rn.f32x2 rd, ra, rb;\n mov.b64 {%0, %1}, rd;\n}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+// max of three floats in one instruction
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
 
 // OUT16: the output is rounded to bf16 (else fp32)
 template <int D, bool OUT16>
@@ -401,7 +428,10 @@ __global__ void __launch_bounds__(kAttThreads, 1)
 #pragma unroll
           for (int i = 0; i < 8; ++i) mx[i] = x[i];
 #pragma unroll
-          for (int i = 8; i < 64; ++i) mx[i & 7] = fmaxf(mx[i & 7], x[i]);
+          for (int i = 8; i < 64; i += 16)  // two more scores per partial max and instruction
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              mx[k] = (i + 8 < 64) ? fmax3(mx[k], x[i + k], x[i + 8 + k]) : fmaxf(mx[k], x[i + k]);
         } else {
           // keys kv0 + i with i > lim are hidden (past T, or after the query);
           // the additive mask joins the unscaled score as mask / sm_scale, so
@@ -417,8 +447,8 @@ __global__ void __launch_bounds__(kAttThreads, 1)
             mx[i & 7] = fmaxf(mx[i & 7], x[i]);
           }
         }
-        const float pm = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        const float pm = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
+                               fmaxf(mx[6], mx[7]));
         const float mt = c * fmaxf(pm, swap(pm));  // the row's tile max (log2 units)
         if (j == 0) {
           m_ref = mt;  // this tile's P V overwrites O
@@ -443,15 +473,19 @@ __global__ void __launch_bounds__(kAttThreads, 1)
           m_ref = m_new;
         }
         const float ref = (m_ref == -INFINITY) ? 0.f : m_ref;
-        float sm[8];
+        float2 sm2[4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) sm[i] = 0.f;
+        for (int i = 0; i < 4; ++i) sm2[i] = make_float2(0.f, 0.f);
+        const float2 c2 = make_float2(c, c), nr2 = make_float2(-ref, -ref);
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          x[i] = ex2(fmaf(x[i], c, -ref));
-          sm[i & 7] += x[i];
+        for (int i = 0; i < 64; i += 2) {
+          const float2 y = ffma2(make_float2(x[i], x[i + 1]), c2, nr2);
+          x[i] = ex2(y.x);
+          x[i + 1] = ex2(y.y);
+          sm2[(i & 7) >> 1] = fadd2(sm2[(i & 7) >> 1], make_float2(x[i], x[i + 1]));
         }
-        l += ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
+        l += ((sm2[0].x + sm2[0].y) + (sm2[1].x + sm2[1].y)) +
+             ((sm2[2].x + sm2[2].y) + (sm2[3].x + sm2[3].y));
         // P, rounded to bf16, two keys to a column (the lower key in the low
         // half), into TMEM buffer g % 2 -- free once P V of tile g - 2 has run
         uint32_t pk[32];
