@@ -98,3 +98,17 @@ def test_attention_flop_and_byte_counts():
     # one read of bf16 q, k, v and one write of the output (bf16 by default) and fp32 lse
     assert bench.attention_bytes(1, 1, 4, 8) == 3 * 32 * 2 + 32 * 2 + 4 * 4
     assert bench.attention_bytes(1, 1, 4, 8, out_bytes=4) == 3 * 32 * 2 + 32 * 4 + 4 * 4
+
+
+def test_cpu_baseline_times_one_thread_and_all_cores():
+    # the oracle baseline: its value on one host thread, and the same sample split
+    # over every host core (a spawn pool) beside it
+    sys.path.insert(0, ROOT)
+    import bench
+    from softmax_cross_entropy_online_gb300 import synthetic
+    d = bench.cpu_baseline(synthetic.WORKLOADS["small_f32_256x1024"], 0.2)
+    assert d["kind"] == "oracle" and d["cores"] == 1 and d["value"] > 0
+    n = os.cpu_count() or 1
+    if n > 1:
+        a = d["all_cores"]
+        assert a["cores"] == n and a["value"] > 0 and a["unit"] == d["unit"]
