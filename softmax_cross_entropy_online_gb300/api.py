@@ -113,6 +113,20 @@ def _outputs(logits, reduction, row_loss, lse):
     return loss_t, rl_t, lse_t
 
 
+def _check_buffer(t, name, device, dtype, shape=None, numel=None):
+    """A caller's buffer the kernels read or write: a contiguous CUDA tensor of
+    `dtype` on `device` with the given shape (or element count).  Anything else
+    is refused before a launch, since a kernel would write through a pointer of
+    another device (or of the host) or past the end."""
+    if (not isinstance(t, torch.Tensor) or not t.is_cuda or t.device != device
+            or t.dtype != dtype or not t.is_contiguous()
+            or (shape is not None and tuple(t.shape) != tuple(shape))
+            or (numel is not None and t.numel() != numel)):
+        want = f"shape {tuple(shape)}" if shape is not None else f"{numel} elements"
+        raise ValueError(f"{name} must be a contiguous {dtype} CUDA tensor on {device} with "
+                         f"{want}")
+
+
 def _ptr(t):
     return None if t is None else t.data_ptr()
 
@@ -152,10 +166,9 @@ def ce_fwd_bwd_inplace_noalloc(logits: torch.Tensor, targets: torch.Tensor,
     (fp32 loss [], row_loss [M], lse [M]; any may be None).  Returns them."""
     _check_inputs(logits, targets)
     M, V = logits.shape
-    for t_, n in ((loss, 1), (row_loss, M), (lse, M)):
-        if t_ is not None and (not t_.is_cuda or t_.dtype != torch.float32
-                               or t_.numel() != n or not t_.is_contiguous()):
-            raise ValueError("outputs must be contiguous fp32 CUDA tensors of the right size")
+    for t_, n, name in ((loss, 1, "loss"), (row_loss, M, "row_loss"), (lse, M, "lse")):
+        if t_ is not None:
+            _check_buffer(t_, name, logits.device, torch.float32, numel=n)
     st = lib().ce_fwd_bwd_inplace_noalloc(logits.data_ptr(), targets.data_ptr(), M, V,
                                           _DTYPES[logits.dtype], _REDUCTIONS[reduction],
                                           _ptr(loss), _ptr(row_loss), _ptr(lse),
@@ -168,9 +181,7 @@ def ce_backward_from_lse(logits: torch.Tensor, targets: torch.Tensor, lse: torch
                          scale: float, *, stream=None):
     """Gradient from a stored lse, written over `logits`."""
     _check_inputs(logits, targets)
-    if (not lse.is_cuda or lse.dtype != torch.float32 or not lse.is_contiguous()
-            or lse.numel() != logits.shape[0]):
-        raise ValueError("lse must be a contiguous fp32 CUDA tensor [M]")
+    _check_buffer(lse, "lse", logits.device, torch.float32, numel=logits.shape[0])
     M, V = logits.shape
     st = lib().ce_backward_from_lse(logits.data_ptr(), targets.data_ptr(), lse.data_ptr(), M, V,
                                     _DTYPES[logits.dtype], float(scale),
@@ -183,8 +194,9 @@ def linear_ce_fwd_bwd(h: torch.Tensor, W: torch.Tensor, targets: torch.Tensor, *
     """Fused linear + cross-entropy: returns (loss, dH, dW) for bf16 h [M, H] and
     W [V, H]; the mean loss's gradients are fp32.  The workspace (uint8 CUDA
     tensor) defaults to linear_ce_workspace_size(M, H, V) bytes."""
-    if h.dtype != torch.bfloat16 or W.dtype != torch.bfloat16 or not h.is_cuda or not W.is_cuda:
-        raise ValueError("h and W must be bf16 CUDA tensors")
+    if (h.dtype != torch.bfloat16 or W.dtype != torch.bfloat16 or not h.is_cuda or not W.is_cuda
+            or W.device != h.device):
+        raise ValueError("h and W must be bf16 CUDA tensors on one device")
     if h.dim() != 2 or W.dim() != 2 or h.shape[1] != W.shape[1]:
         raise ValueError("h must be [M, H] and W [V, H]")
     if not h.is_contiguous() or not W.is_contiguous():
@@ -192,12 +204,15 @@ def linear_ce_fwd_bwd(h: torch.Tensor, W: torch.Tensor, targets: torch.Tensor, *
     M, H = h.shape
     V = W.shape[0]
     if (targets.dtype != torch.int64 or targets.numel() != M or not targets.is_cuda
-            or not targets.is_contiguous()):
-        raise ValueError("targets must be a contiguous int64 CUDA tensor [M]")
+            or not targets.is_contiguous() or targets.device != h.device):
+        raise ValueError("targets must be a contiguous int64 CUDA tensor [M] on h's device")
     dev = h.device
     if workspace is None:
         workspace = torch.empty(int(lib().linear_ce_workspace_size(M, H, V)), dtype=torch.uint8,
                                 device=dev)
+    else:
+        # its size in bytes is its element count: uint8 only
+        _check_buffer(workspace, "workspace", dev, torch.uint8, numel=workspace.numel())
     loss = torch.empty((), dtype=torch.float32, device=dev)
     dH = torch.empty((M, H), dtype=torch.float32, device=dev)
     dW = torch.empty((V, H), dtype=torch.float32, device=dev)
@@ -213,15 +228,35 @@ def linear_ce_workspace_size(M: int, H: int, V: int) -> int:
     return int(lib().linear_ce_workspace_size(M, H, V))
 
 
+def _check_operands(A, B):
+    if not A.is_cuda or not B.is_cuda or A.device != B.device:
+        raise ValueError("A and B must be CUDA tensors on one device")
+    if A.stride(1) != 1 or B.stride(1) != 1:
+        raise ValueError("A and B must have contiguous rows")
+
+
+def _gemm_out(D, M, N, device):
+    """The fp32 output [M, N] (rows contiguous, any row stride the ABI accepts)."""
+    if D is None:
+        return torch.empty((M, N), dtype=torch.float32, device=device)
+    if (not isinstance(D, torch.Tensor) or not D.is_cuda or D.device != device
+            or D.dtype != torch.float32 or D.dim() != 2 or tuple(D.shape) != (M, N)
+            or D.stride(1) != 1):
+        raise ValueError(f"D must be an fp32 CUDA tensor [{M}, {N}] with contiguous rows on "
+                         f"{device}")
+    return D
+
+
 def ce_gemm_bf16_tn(A: torch.Tensor, B: torch.Tensor, D: torch.Tensor | None = None,
                     beta: float = 0.0, *, stream=None) -> torch.Tensor:
     """D = A B^T (beta 0) or D += A B^T (beta 1): A [M, K], B [N, K] bf16, D fp32."""
-    if A.dtype != torch.bfloat16 or B.dtype != torch.bfloat16 or A.shape[1] != B.shape[1]:
+    if (A.dtype != torch.bfloat16 or B.dtype != torch.bfloat16 or A.dim() != 2 or B.dim() != 2
+            or A.shape[1] != B.shape[1]):
         raise ValueError("A [M, K] and B [N, K] must be bf16 with the same K")
+    _check_operands(A, B)
     M, K = A.shape
     N = B.shape[0]
-    if D is None:
-        D = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    D = _gemm_out(D, M, N, A.device)
     st = lib().ce_gemm_bf16_tn(A.data_ptr(), A.stride(0), B.data_ptr(), B.stride(0),
                                D.data_ptr(), D.stride(0), M, N, K, float(beta),
                                _stream_handle(stream, A.device))
@@ -243,8 +278,8 @@ def ce_gemm_bf16(A: torch.Tensor, B: torch.Tensor, D: torch.Tensor | None = None
     Kb, N = B.shape if b_mn else (B.shape[1], B.shape[0])
     if Kb != K:
         raise ValueError("A and B must share K")
-    if D is None:
-        D = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    _check_operands(A, B)
+    D = _gemm_out(D, M, N, A.device)
     st = lib().ce_gemm_bf16(A.data_ptr(), A.stride(0), int(a_mn), B.data_ptr(), B.stride(0),
                             int(b_mn), D.data_ptr(), D.stride(0), M, N, K, float(beta),
                             _stream_handle(stream, A.device))
@@ -275,9 +310,9 @@ def ce_attention_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
         sm_scale = 1.0 / math.sqrt(D)
     if out is None:
         out = torch.empty((B, NH, T, D), dtype=out_dtype, device=q.device)
-    if (out.dtype not in (torch.float32, torch.bfloat16) or tuple(out.shape) != (B, NH, T, D)
-            or not out.is_contiguous()):
-        raise ValueError("out must be a contiguous fp32 or bf16 tensor [B, NH, T, D]")
+    if out.dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError("out must be fp32 or bf16")
+    _check_buffer(out, "out", q.device, out.dtype, shape=(B, NH, T, D))
     lse_t = torch.empty((B, NH, T), dtype=torch.float32, device=q.device) if lse else None
     st = lib().ce_attention_forward(q.data_ptr(), k.data_ptr(), v.data_ptr(), _ptr(mask),
                                     int(bool(causal)), B, NH, T, D, float(sm_scale),
@@ -297,8 +332,7 @@ def ce_softmax_forward(logits: torch.Tensor, probs: torch.Tensor | None = None, 
         raise ValueError(f"unsupported logits dtype {logits.dtype}")
     if probs is None:
         probs = torch.empty_like(logits)
-    if probs.shape != logits.shape or probs.dtype != logits.dtype or not probs.is_contiguous():
-        raise ValueError("probs must match logits")
+    _check_buffer(probs, "probs", logits.device, logits.dtype, shape=logits.shape)
     M, V = logits.shape
     lse_t = torch.empty(M, dtype=torch.float32, device=logits.device) if lse else None
     st = lib().ce_softmax_forward(logits.data_ptr(), probs.data_ptr(), M, V,

@@ -144,3 +144,59 @@ def test_product_path_never_imports_the_oracle():
 ])
 def test_attention_host_validation(cdll, args, status):
     assert cdll.ce_attention_forward(*args, None) == status
+
+
+# --- the Python binding refuses caller buffers it cannot hand to a kernel -----
+
+def test_binding_buffer_checks_on_the_host():
+    # host-side checks of the binding's helpers: a buffer off the GPU, of another
+    # dtype or of the wrong size is refused before any call into the library
+    torch = pytest.importorskip("torch")
+    from softmax_cross_entropy_online_gb300 import api
+    dev = torch.device("cuda", 0)
+    with pytest.raises(ValueError):
+        api._check_buffer(torch.empty(3), "x", dev, torch.float32, numel=3)
+    with pytest.raises(ValueError):
+        api._gemm_out(torch.empty(2, 3), 2, 3, dev)
+    assert api._gemm_out(None, 2, 3, torch.device("cpu")).shape == (2, 3)
+    a = torch.zeros(4, 8, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        api.ce_gemm_bf16_tn(a, a)
+    with pytest.raises(ValueError, match="CUDA"):
+        api.ce_gemm_bf16(a, a)
+    with pytest.raises(ValueError):
+        api.ce_attention_forward(*(torch.zeros(1, 1, 4, 64, dtype=torch.bfloat16),) * 3)
+
+
+@pytest.mark.gpu
+def test_binding_refuses_buffers_off_the_device(cdll):
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from softmax_cross_entropy_online_gb300 import api
+    dev = torch.device("cuda", 0)
+    n0 = api.ce_launch_count()
+    q = torch.zeros(1, 2, 8, 64, dtype=torch.bfloat16, device=dev)
+    with pytest.raises(ValueError, match="out"):
+        api.ce_attention_forward(q, q, q, out=torch.empty(1, 2, 8, 64))            # host
+    with pytest.raises(ValueError, match="out"):
+        api.ce_attention_forward(q, q, q, out=torch.empty(1, 2, 8, 32, device=dev))  # shape
+    x = torch.zeros(4, 16, device=dev)
+    with pytest.raises(ValueError, match="probs"):
+        api.ce_softmax_forward(x, torch.empty(4, 16))
+    t = torch.zeros(4, dtype=torch.int64, device=dev)
+    with pytest.raises(ValueError, match="lse"):
+        api.ce_backward_from_lse(x, t, torch.zeros(4), 0.25)
+    with pytest.raises(ValueError, match="row_loss"):
+        api.ce_fwd_bwd_inplace_noalloc(x, t, row_loss=torch.empty(4))
+    a = torch.zeros(128, 64, dtype=torch.bfloat16, device=dev)
+    with pytest.raises(ValueError, match="D must be"):
+        api.ce_gemm_bf16_tn(a, a, torch.empty(64, 128, device=dev))
+    with pytest.raises(ValueError, match="D must be"):
+        api.ce_gemm_bf16(a, a, torch.empty(128, 128))
+    h = torch.zeros(8, 64, dtype=torch.bfloat16, device=dev)
+    with pytest.raises(ValueError, match="workspace"):
+        api.linear_ce_fwd_bwd(h, h, torch.zeros(8, dtype=torch.int64, device=dev),
+                              workspace=torch.empty(16, dtype=torch.float32, device=dev))
+    torch.cuda.synchronize()
+    assert api.ce_launch_count() == n0  # nothing was launched
