@@ -19,10 +19,15 @@
  * "9 Triton kernels in 9 weeks", week seven.
  *
  * Conventions shared by every entry point:
- *  - Pointers named logits/targets/loss/row_loss/lse are DEVICE pointers on
- *    the current CUDA device.  The caller owns all of them; the library
- *    never frees or keeps them.  `stream` is a cudaStream_t (NULL = legacy
- *    default stream); every call is asynchronous and stream-ordered.
+ *  - Every buffer pointer (logits, targets, loss, row_loss, lse, and the
+ *    operands and outputs of the GEMM, linear+CE and attention calls) is a
+ *    DEVICE pointer on the current CUDA device.  The caller owns all of them;
+ *    the library never frees or keeps them.  The library does not look up
+ *    where a pointer lives: a host pointer, or one into another device's
+ *    memory, is the caller's error and faults the kernel (the Python binding
+ *    refuses such tensors before calling).  `stream` is a cudaStream_t
+ *    (NULL = legacy default stream); every call is asynchronous and
+ *    stream-ordered.
  *  - logits must be aligned to the element size, targets to 8 bytes and
  *    the float outputs to 4 bytes.  Rows need not be 16-byte aligned.
  *  - Arithmetic is fp32 (16-bit inputs widen exactly); loss, row_loss and
