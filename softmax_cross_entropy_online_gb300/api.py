@@ -104,7 +104,14 @@ def _check_inputs(logits: torch.Tensor, targets: torch.Tensor):
         raise ValueError("targets must be a contiguous int64 CUDA tensor [M] on the logits' device")
 
 
+def _reduction_code(reduction: str) -> int:
+    if reduction not in _REDUCTIONS:
+        raise ValueError(f"reduction must be one of {sorted(_REDUCTIONS)}, not {reduction!r}")
+    return _REDUCTIONS[reduction]
+
+
 def _outputs(logits, reduction, row_loss, lse):
+    _reduction_code(reduction)
     M = logits.shape[0]
     dev = logits.device
     loss_t = torch.empty((), dtype=torch.float32, device=dev) if reduction != "none" else None
@@ -138,7 +145,7 @@ def ce_forward(logits: torch.Tensor, targets: torch.Tensor, reduction: str = "me
     loss_t, rl_t, lse_t = _outputs(logits, reduction, row_loss, lse)
     M, V = logits.shape
     st = lib().ce_forward(logits.data_ptr(), targets.data_ptr(), M, V, _DTYPES[logits.dtype],
-                          _REDUCTIONS[reduction], _ptr(loss_t), _ptr(rl_t), _ptr(lse_t),
+                          _reduction_code(reduction), _ptr(loss_t), _ptr(rl_t), _ptr(lse_t),
                           _stream_handle(stream, logits.device))
     _check(st, "ce_forward")
     return loss_t, rl_t, lse_t
@@ -151,7 +158,7 @@ def ce_fwd_bwd_inplace(logits: torch.Tensor, targets: torch.Tensor, reduction: s
     loss_t, rl_t, lse_t = _outputs(logits, reduction, row_loss, lse)
     M, V = logits.shape
     st = lib().ce_fwd_bwd_inplace(logits.data_ptr(), targets.data_ptr(), M, V,
-                                  _DTYPES[logits.dtype], _REDUCTIONS[reduction], _ptr(loss_t),
+                                  _DTYPES[logits.dtype], _reduction_code(reduction), _ptr(loss_t),
                                   _ptr(rl_t), _ptr(lse_t), _stream_handle(stream, logits.device))
     _check(st, "ce_fwd_bwd_inplace")
     return loss_t, rl_t, lse_t
@@ -170,7 +177,7 @@ def ce_fwd_bwd_inplace_noalloc(logits: torch.Tensor, targets: torch.Tensor,
         if t_ is not None:
             _check_buffer(t_, name, logits.device, torch.float32, numel=n)
     st = lib().ce_fwd_bwd_inplace_noalloc(logits.data_ptr(), targets.data_ptr(), M, V,
-                                          _DTYPES[logits.dtype], _REDUCTIONS[reduction],
+                                          _DTYPES[logits.dtype], _reduction_code(reduction),
                                           _ptr(loss), _ptr(row_loss), _ptr(lse),
                                           _stream_handle(stream, logits.device))
     _check(st, "ce_fwd_bwd_inplace_noalloc")

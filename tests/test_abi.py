@@ -200,3 +200,11 @@ def test_binding_refuses_buffers_off_the_device(cdll):
                               workspace=torch.empty(16, dtype=torch.float32, device=dev))
     torch.cuda.synchronize()
     assert api.ce_launch_count() == n0  # nothing was launched
+
+
+def test_binding_rejects_an_unknown_reduction():
+    torch = pytest.importorskip("torch")
+    from softmax_cross_entropy_online_gb300 import api
+    assert api._reduction_code("sum") == 1
+    with pytest.raises(ValueError, match="reduction"):
+        api._reduction_code("average")
