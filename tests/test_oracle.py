@@ -222,6 +222,74 @@ def test_linear_ce_against_torch_float64():
     np.testing.assert_allclose(f["dW"], Wt.grad.numpy(), rtol=0, atol=1e-15)
 
 
+def test_linear_ce_equal_weight_rows_closed_form():
+    # every row of W equal: each row of logits is constant, so the loss is ln V
+    # exactly, G = (1/V - onehot) / M, dH = G W = 0 (G's rows sum to 0) and
+    # dW_j = (sum_i h_i / V - sum_{i: t_i = j} h_i) / M
+    M, H, V = 6, 5, 7
+    rng = np.random.default_rng(7)
+    h = rng.normal(size=(M, H))
+    W = np.tile(rng.normal(size=H), (V, 1))
+    t = np.array([0, 3, 3, 6, 1, 0])
+    f = oracle.linear_ce(h, W, t, "mean")
+    assert abs(f["loss"] - math.log(V)) < 1e-14
+    np.testing.assert_allclose(f["dH"], 0.0, rtol=0, atol=1e-15)
+    expect = np.empty((V, H))
+    for j in range(V):
+        expect[j] = (h.sum(axis=0) / V - h[t == j].sum(axis=0)) / M
+    np.testing.assert_allclose(f["dW"], expect, rtol=0, atol=1e-15)
+
+
+def _linear_ce_fd_ok(fn, M=3, H=4, V=5, seed=8):
+    """Central differences of the mean loss against fn's dH and dW."""
+    rng = np.random.default_rng(seed)
+    h = rng.normal(size=(M, H))
+    W = rng.normal(0, 0.5, size=(V, H))
+    t = rng.integers(0, V, M)
+    f = fn(h, W, t, "mean")
+    eps = 1e-6
+    ok = True
+    for A, dA in ((h, f["dH"]), (W, f["dW"])):
+        num = np.zeros_like(A)
+        for idx in np.ndindex(A.shape):
+            save = A[idx]
+            A[idx] = save + eps
+            up = oracle.linear_ce(h, W, t, "mean")["loss"]
+            A[idx] = save - eps
+            dn = oracle.linear_ce(h, W, t, "mean")["loss"]
+            A[idx] = save
+            num[idx] = (up - dn) / (2 * eps)
+        ok = ok and dA.shape == num.shape and np.allclose(dA, num, rtol=0, atol=1e-8)
+    return ok
+
+
+def test_linear_ce_finite_differences():
+    assert _linear_ce_fd_ok(oracle.linear_ce)
+
+
+@pytest.mark.parametrize("kind", ["no_mean_scale", "no_one_hot", "dW_from_W"])
+def test_linear_ce_planted_mistakes_are_caught(kind, monkeypatch):
+    # each mistake is planted in the oracle (on the CPU) and must fail the
+    # finite-difference pin above
+    real_grad = ce_oracle.ce_grad
+
+    def broken(h, W, t, reduction="mean"):
+        with monkeypatch.context() as mp:
+            if kind == "no_mean_scale":
+                mp.setattr(ce_oracle, "grad_scale", lambda reduction, M: 1.0)
+            elif kind == "no_one_hot":
+                mp.setattr(ce_oracle, "ce_grad",
+                           lambda x, t_, lse, scale: real_grad(x, np.full_like(t_, -1), lse, scale))
+            f = ce_oracle.linear_ce(h, W, t, reduction)
+        if kind == "dW_from_W":
+            # the weight gradient taken against the wrong operand (W's first M
+            # rows in place of h)
+            f["dW"] = f["grad"].T @ np.asarray(W, dtype=np.float64)[:len(t)]
+        return f
+
+    assert not _linear_ce_fd_ok(broken), kind
+
+
 def test_online_recurrence_reaches_definition():
     # the streaming pass and any merge tree give the defined lse
     for V in [1, 2, 17, 300]:
