@@ -431,3 +431,52 @@ def test_softmax_matches_torch_float64():
     x = RNG.normal(0, 5, size=(17, 301))
     ref = torch.softmax(torch.tensor(x, dtype=torch.float64), dim=1).numpy()
     np.testing.assert_allclose(oracle.softmax_rows(x), ref, rtol=1e-13, atol=1e-300)
+
+
+def test_softmax_closed_forms():
+    # uniform rows give 1/V for any offset; two classes give the logistic
+    # function of the difference; a row with one entry 50 above the rest puts
+    # 1 / (1 + (V - 1) e^-50) on it; and rows are shift-invariant
+    for V, c in ((1, 0.0), (7, -3.5), (4096, 1e4)):
+        # the exponent x - lse carries lse's rounding, up to an ulp of |c| + ln V
+        tol = 4 * np.finfo(np.float64).eps * (abs(c) + math.log(V) + 1)
+        np.testing.assert_allclose(oracle.softmax_rows(np.full((3, V), c)), 1.0 / V, rtol=tol)
+    a = RNG.normal(size=(9, 2)) * 4
+    p = oracle.softmax_rows(a)
+    np.testing.assert_allclose(p[:, 0], 1.0 / (1.0 + np.exp(a[:, 1] - a[:, 0])), rtol=1e-14)
+    V = 1000
+    x = np.zeros((1, V))
+    x[0, 17] = 50.0
+    p = oracle.softmax_rows(x)
+    np.testing.assert_allclose(p[0, 17], 1.0 / (1.0 + (V - 1) * math.exp(-50.0)), rtol=1e-15)
+    np.testing.assert_allclose(p[0, 0], math.exp(-50.0) / (1.0 + (V - 1) * math.exp(-50.0)),
+                               rtol=1e-13)
+    x = RNG.normal(size=(5, 33))
+    np.testing.assert_allclose(oracle.softmax_rows(x + RNG.normal(size=(5, 1)) * 100),
+                               oracle.softmax_rows(x), rtol=1e-12)
+
+
+@pytest.mark.parametrize("kind", ["unstabilised_lse", "lse_over_columns", "lse_missing_log"])
+def test_softmax_planted_mistakes_are_caught(kind, monkeypatch):
+    # each mistake is planted in the oracle's log-sum-exp (on the CPU) and must
+    # fail the closed forms above
+    def unstabilised(x):
+        with np.errstate(over="ignore"):
+            return np.log(np.sum(np.exp(np.asarray(x, dtype=np.float64)), axis=1))
+
+    def over_columns(x):
+        x = np.asarray(x, dtype=np.float64)
+        m = np.max(x, axis=0)
+        r = m + np.log(np.sum(np.exp(x - m[None, :]), axis=0))
+        return np.resize(r, x.shape[0])
+
+    def missing_log(x):
+        x = np.asarray(x, dtype=np.float64)
+        m = np.max(x, axis=1)
+        return m + np.sum(np.exp(x - m[:, None]), axis=1)
+
+    fake = {"unstabilised_lse": unstabilised, "lse_over_columns": over_columns,
+            "lse_missing_log": missing_log}[kind]
+    monkeypatch.setattr(ce_oracle, "logsumexp_rows", fake)
+    with pytest.raises(AssertionError), np.errstate(all="ignore"):
+        test_softmax_closed_forms()
