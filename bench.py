@@ -160,6 +160,17 @@ def aggregate_gbs(world_size: int, bytes_per_step: int, ms_per_step: float) -> f
     return world_size * bytes_per_step / (ms_per_step * 1e-3) / 1e9
 
 
+def rate_figures(ws: int, M: int, ms_per_step: float, kernel_ms: float, bytes_per_step: int,
+                 peak_gbs: float) -> dict:
+    """Absolute figures beside the GB/s: microseconds per call, rows per second
+    for the whole job, and whether the call is so small that its bytes at the
+    peak rate take less than a few microseconds, so launch latency bounds it
+    and its roofline fraction says little."""
+    return {"us_per_call": kernel_ms * 1e3,
+            "rows_per_s": ws * M / (ms_per_step * 1e-3),
+            "latency_bound": bytes_per_step / (peak_gbs * 1e9) < 4e-6}
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -465,6 +476,7 @@ def run_native(args, w):
                        "parallelism": f"replicas x{ws}"},
             "pct_of_hbm_roofline": 100.0 * achieved / peak,
             "ms_per_call": avg_kernel_ms,
+            "rates": rate_figures(ws, M, ms_per_step, avg_kernel_ms, b_step, peak),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_source": peak_kind,
                          "traffic": traffic,

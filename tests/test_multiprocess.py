@@ -112,3 +112,17 @@ def test_cpu_baseline_times_one_thread_and_all_cores():
     if n > 1:
         a = d["all_cores"]
         assert a["cores"] == n and a["value"] > 0 and a["unit"] == d["unit"]
+
+
+def test_rate_figures():
+    sys.path.insert(0, ROOT)
+    import bench
+    # fp32 [256, 1024] forward+backward: ~2.1 MB, far below a few microseconds at
+    # 6.8 TB/s, so launch latency bounds it; [32768, 4096] (1.07 GB) does not
+    small = bench.algorithmic_bytes(256, 1024, 4, True)
+    r = bench.rate_figures(1, 256, 0.005, 0.004, small, 6800.0)
+    assert r["latency_bound"] and abs(r["us_per_call"] - 4.0) < 1e-12
+    assert abs(r["rows_per_s"] - 256 / 5e-6) < 1e-3
+    big = bench.algorithmic_bytes(32768, 4096, 4, True)
+    r = bench.rate_figures(2, 32768, 0.18, 0.18, big, 6800.0)
+    assert not r["latency_bound"] and abs(r["rows_per_s"] - 2 * 32768 / 0.18e-3) < 1
