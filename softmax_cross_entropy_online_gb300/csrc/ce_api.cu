@@ -755,10 +755,11 @@ ce_status ce_attention_forward(const void* q, const void* k, const void* v, cons
   if (out_dtype != CE_F32 && out_dtype != CE_F16 && out_dtype != CE_BF16) return CE_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return CE_ERR_UNSUPPORTED;
   if (out_dtype == CE_F16) return CE_ERR_UNSUPPORTED;
-  const int64_t BH = B * NH;
+  int64_t BH = 0;
+  if (__builtin_mul_overflow(B, NH, &BH)) return CE_ERR_UNSUPPORTED;
   if (BH == 0 || T == 0) return CE_OK;
   if (q == nullptr || k == nullptr || v == nullptr || out == nullptr) return CE_ERR_INVALID_ARG;
-  if (T > INT32_MAX || BH > INT32_MAX || (B > 0 && BH / B != NH)) return CE_ERR_UNSUPPORTED;
+  if (T > INT32_MAX || BH > INT32_MAX) return CE_ERR_UNSUPPORTED;
   // the kernel counts (head, 128-row query tile) items in 32-bit integers
   if (BH * ((T + 127) / 128) > INT32_MAX) return CE_ERR_UNSUPPORTED;
   auto mis = [](const void* ptr, uintptr_t a) { return reinterpret_cast<uintptr_t>(ptr) % a != 0; };

@@ -137,6 +137,8 @@ def test_product_path_never_imports_the_oracle():
     ((16, 16, 16, None, 0, 1, 1, 8, 64, 0.125, 16, 0, 18), 1),             # lse misaligned
     ((16, 16, 16, None, 0, 1, 1, 1 << 31, 64, 0.125, 16, 0, None), 2),     # T above 2^31 - 1
     ((16, 16, 16, None, 0, 1, 1 << 30, 1024, 64, 0.125, 16, 0, None), 2),  # 2^33 query tiles
+    ((16, 16, 16, None, 0, 1 << 32, 1 << 32, 8, 64, 0.125, 16, 0, None), 2),  # B NH wraps to 0
+    ((16, 16, 16, None, 0, 1 << 40, 1 << 30, 8, 64, 0.125, 16, 0, None), 2),  # B NH overflows
     ((None, None, None, None, 0, 0, 4, 8, 64, 0.125, None, 0, None), 0),   # B = 0: nothing to do
     ((None, None, None, None, 1, 2, 4, 0, 128, 0.125, None, 0, None), 0),  # T = 0: nothing to do
     ((16, 16, 16, None, 0, 1, 1, 8, 64, 0.125, 16, 7, None), 1),         # out_dtype not a ce_dtype
