@@ -626,10 +626,98 @@ def run_linear(args):
                     "ms_per_step": e2e_ms},
             "gpu_launches": launches, "clocks": clocks,
         }
+        if ws == 1 and not args.no_cpu_baseline:
+            try:
+                line["cpu_baseline"] = linear_cpu_baseline(h_np, W_np, t_np, M, H, V,
+                                                           args.cpu_budget_s)
+            except Exception as e:  # never costs the line its GPU figures
+                line["cpu_baseline"] = {"kind": "oracle", "error": f"{type(e).__name__}: {e}"[:200]}
         print(json.dumps(line), flush=True)
     if ws > 1:
         dist.barrier()
         dist.destroy_process_group()
+    return 0
+
+
+def blas_threads() -> int:
+    """Threads numpy's BLAS uses for a matmul (threadpoolctl when present, else
+    the host's CPU count, the BLAS default)."""
+    try:
+        from threadpoolctl import threadpool_info
+        n = [d.get("num_threads", 0) for d in threadpool_info() if d.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def linear_cpu_baseline(h_bits, W_bits, t, M: int, H: int, V: int, budget_s: float) -> dict:
+    """The float64 oracle as it stands (logits = h W^T, the CE pass, dH, dW) on
+    a bounded sample of the workload: its first rows of h against the whole W,
+    6 V H flops a row as in the full step.  The bf16 decoding is done once,
+    outside the timed region."""
+    import oracle
+    W64 = oracle.to_f64(W_bits, "bf16")
+    h64 = oracle.to_f64(h_bits, "bf16")
+    t0 = time.perf_counter()
+    oracle.linear_ce(h64[:1], W64, t[:1], "mean")
+    dt = time.perf_counter() - t0
+    rows = int(min(M, max(1, budget_s / max(dt, 1e-6))))
+    t0 = time.perf_counter()
+    oracle.linear_ce(h64[:rows], W64, t[:rows], "mean")
+    dt = time.perf_counter() - t0
+    n = blas_threads()
+    return {"value": 6.0 * rows * V * H / dt / 1e12, "unit": "TFLOP/s", "cores": n,
+            "kind": "oracle", **host_info(),
+            "sample": f"{rows} of {M} rows of h against the whole W [{V}, {H}], loss, dH "
+                      f"and dW in float64 numpy ({dt:.1f} s, {n} BLAS threads)"}
+
+
+def run_linear_reference(args):
+    """The reference arm of the linear + CE workload: the float64 oracle on the
+    host, each step on a bounded sample (the first rows of h against the whole
+    W, 6 V H flops a row as in the full step); rank 0 alone."""
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    M, H, V = LINEAR_SHAPES[args.workload]
+    if args.rows is not None:
+        M = args.rows
+    h_np, W_np, t_np = synthetic.make_linear_ce_inputs(M, H, V, seed=0)
+    W64 = oracle.to_f64(W_np, "bf16")
+    for _ in range(args.warmup):
+        t0 = time.perf_counter()
+        oracle.linear_ce(oracle.to_f64(h_np[:1], "bf16"), W64, t_np[:1], "mean")
+        one_row_s = time.perf_counter() - t0
+    # rows per step: the steps together take about a minute (at least one row)
+    step_budget = max(0.5, 60.0 / max(1, args.steps))
+    rows = int(max(1, min(M, args.ref_rows, step_budget / max(one_row_s, 1e-6))))
+    h64 = oracle.to_f64(h_np[:rows], "bf16")
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.linear_ce(h64, W64, t_np[:rows], "mean")
+        times.append(time.perf_counter() - t0)
+    step_s = sum(times) / len(times)
+    tf = 6.0 * rows * V * H / step_s / 1e12
+    n = blas_threads()
+    sample = (f"{rows} of {M} rows of h against the whole W [{V}, {H}] per step, loss, dH "
+              f"and dW in float64 numpy ({n} BLAS threads); bf16 decoding outside the steps")
+    print(json.dumps({
+        "impl": "reference", "metric": "fused linear+CE fwd+bwd TFLOP/s (6 M V H per step)",
+        "value": tf, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{args.workload}: bf16 h [{M}, {H}] N(0,1), W [{V}, {H}] "
+                               "N(0, 0.02^2), int64 targets; loss, dH, dW",
+                   "M": M, "H": H, "V": V, "sample_rows": rows},
+        "cpu_baseline": {"value": tf, "unit": "TFLOP/s", "cores": n, "kind": "oracle",
+                         **host_info(), "sample": sample},
+        "e2e": {"value": tf, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
     return 0
 
 
@@ -864,10 +952,7 @@ def main():
         return run_attention(args)
     if args.workload in LINEAR_SHAPES:
         if args.impl == "reference":
-            print(json.dumps({"impl": "reference", "unavailable":
-                              "the float64 linear+CE oracle holds dW [128256, 4096] in float64 "
-                              "(4.2 GB) for any row sample; it is timed on the CE workloads"}))
-            return 0
+            return run_linear_reference(args)
         return run_linear(args)
     w = synthetic.WORKLOADS[args.workload]
     if args.rows is not None:

@@ -126,3 +126,31 @@ def test_rate_figures():
     big = bench.algorithmic_bytes(32768, 4096, 4, True)
     r = bench.rate_figures(2, 32768, 0.18, 0.18, big, 6800.0)
     assert not r["latency_bound"] and abs(r["rows_per_s"] - 2 * 32768 / 0.18e-3) < 1
+
+
+def test_linear_cpu_baseline_on_a_small_shape():
+    sys.path.insert(0, ROOT)
+    import bench
+    from softmax_cross_entropy_online_gb300 import synthetic
+    M, H, V = 64, 32, 96
+    h, W, t = synthetic.make_linear_ce_inputs(M, H, V, seed=0)
+    d = bench.linear_cpu_baseline(h, W, t, M, H, V, 0.05)
+    assert d["kind"] == "oracle" and d["unit"] == "TFLOP/s" and d["value"] > 0
+    assert d["cores"] >= 1 and "rows of h" in d["sample"]
+
+
+def test_linear_reference_arm_prints_one_line(monkeypatch, capsys):
+    # the reference arm of the linear + CE workload on a small stand-in shape
+    sys.path.insert(0, ROOT)
+    import bench
+    monkeypatch.setitem(bench.LINEAR_SHAPES, "linear_ce_8192x4096x128256", (64, 32, 96))
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--impl", "reference", "--workload",
+                                      "linear_ce_8192x4096x128256", "--steps", "2"])
+    assert bench.main() == 0
+    lines = [ln for ln in capsys.readouterr().out.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "TFLOP/s" and d["value"] > 0
+    assert d["cpu_baseline"]["value"] == d["value"] and d["config"]["sample_rows"] >= 1
+    assert d["e2e"] == {"value": d["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
