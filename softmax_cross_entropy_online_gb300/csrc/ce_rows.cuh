@@ -56,6 +56,7 @@ constexpr unsigned ERR_TARGET_RANGE = 1u;
 constexpr unsigned ERR_WAIT_TIMEOUT = 2u;
 constexpr unsigned long long WAIT_LIMIT_NS = 4000000000ull;  // 4 s per wait
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
 
 // SOFTMAX: p = exp(x - lse) (the fused softmax of "9 Triton kernels in 9
 // weeks", week one), written over the logits or into a second buffer.
@@ -238,6 +239,94 @@ __device__ __forceinline__ float lg2(float x) {
   asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+// e^u - 1 for the target's gradient, u = x_t - lse (<= 0 up to rounding).  Below
+// u = -1/2 the difference ex2(u log2 e) - 1 loses nothing to cancellation (the
+// result is at most -0.39).  Above it the Taylor series of e^u - 1 is summed
+// through the u^8/8! term by Horner's rule: on |u| <= 1/2 the first omitted term
+// is below 2^-26 of the result, so a target that holds nearly all the
+// probability keeps its small gradient.  Branch-free; -inf gives -1, NaN stays
+// NaN.
+__device__ __forceinline__ float expm1_target(float u) {
+  float p = fmaf(u, 1.f / 40320.f, 1.f / 5040.f);
+  p = fmaf(u, p, 1.f / 720.f);
+  p = fmaf(u, p, 1.f / 120.f);
+  p = fmaf(u, p, 1.f / 24.f);
+  p = fmaf(u, p, 1.f / 6.f);
+  p = fmaf(u, p, 0.5f);
+  p = fmaf(u, p, 1.f);
+  const float series = u * p;
+  const float diff = ex2(u * kLog2e) - 1.f;
+  return u < -0.5f ? diff : series;
+}
+
+// Sum of a double over the warp by butterflies: every lane ends with the same
+// bits (each step adds the same two operands on both lanes of a pair).
+__device__ __forceinline__ double warp_sum_f64(double v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// A running sum of row losses kept as an unevaluated pair hi + lo of floats:
+// each step is Knuth's error-free TwoSum (the rounding error of hi + x goes
+// into lo), so the pair carries about twice a float's precision and no
+// double-precision instruction sits on a row's path.  A non-finite sum (an
+// infinite or NaN row loss) is kept in hi with no error term.
+struct PairSum {
+  float hi = 0.f, lo = 0.f;
+  __device__ __forceinline__ void add(float x) {
+    const float s = hi + x;
+    const float bb = s - hi;
+    const float e = (hi - (s - bb)) + (x - bb);
+    lo += isfinite(s) ? e : 0.f;
+    hi = s;
+  }
+  __device__ __forceinline__ double value() const {
+    return static_cast<double>(hi) + static_cast<double>(lo);
+  }
+};
+
+// Deterministic reduction of the loss over the grid, run by one whole warp of
+// each CTA after the CTA's row-group sums sit in group_sums[0, n).  Lane j adds
+// group sums j, j + 32, ... in order, a butterfly combines the lanes, and lane 0
+// stores the CTA's partial and takes an integer ticket.  The CTA that takes the
+// last ticket sums every partial the same way, with its loads all in flight at
+// once (one L2 round trip, not one per CTA), writes the loss and re-arms the
+// ticket.  Every addition's order is fixed by the launch shape, so the loss is
+// bit-reproducible; no floating-point atomics are used.
+__device__ __forceinline__ void loss_tail_warp(const double* group_sums, int n,
+                                               double* partials, unsigned int* ticket,
+                                               float* loss, long long M, int mean, int lane) {
+  double part = 0.0;
+  for (int j = lane; j < n; j += 32) part += group_sums[j];
+  part = warp_sum_f64(part);
+  unsigned int prev = 0;
+  if (lane == 0) {
+    partials[blockIdx.x] = part;
+    __threadfence();
+    prev = atomicAdd(ticket, 1u);
+  }
+  prev = __shfl_sync(0xffffffffu, prev, 0);
+  if (prev != gridDim.x - 1) return;
+  __threadfence();
+  const int G = static_cast<int>(gridDim.x);
+  double s = 0.0;
+  int j = lane;
+  for (; j + 32 * 7 < G; j += 32 * 8) {
+    double v[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) v[k] = __ldcg(partials + j + 32 * k);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) s += v[k];
+  }
+  for (; j < G; j += 32) s += __ldcg(partials + j);
+  s = warp_sum_f64(s);
+  if (lane == 0) {
+    *loss = static_cast<float>(mean ? s / static_cast<double>(M) : s);
+    *ticket = 0u;  // ready for the next launch that uses this scratch
+  }
+}
+
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -574,7 +663,7 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
     const int gt = tid & (GT - 1);
     const int V = static_cast<int>(p.V);          // the host caps V * sizeof(T) far below 2^31
     const int rb = static_cast<int>(p.row_bytes);
-    double acc = 0.0;  // this group's running loss sum (leader only)
+    PairSum acc;  // this group's running loss sum (leader only)
     const bool leader = (gt == 0) && (rank == 0);
 
     int s = -1;
@@ -713,7 +802,7 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
         }
         if (owner) {
           // exp(x_t - lse) - 1 without cancellation when the target dominates
-          const float gval = expm1f(xt - lse_given) * sc;
+          const float gval = expm1_target(xt - lse_given) * sc;
           if (t_smem) E::st(smem_ptr(tbo), gval);
           else E::st(elem_ptr_global(static_cast<int>(t)), gval);
         }
@@ -894,13 +983,13 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
 
       // ---- row outputs (one thread per row) ----
       if (leader && row_ok) {
-        const float lnS = logf(Sg);
+        const float lnS = lg2(Sg) * kLn2;
         const float lse = Mg + lnS;
         // (m - x_t) + log S keeps the loss accurate when m and x_t are large
         const float rl = t_ok ? (Mg - xrow) + lnS : __int_as_float(0x7fc00000);
         if (p.row_loss) p.row_loss[row] = rl;
         if (p.lse_out) p.lse_out[row] = lse;
-        acc += static_cast<double>(rl);
+        acc.add(rl);
         if (!t_ok && MODE != SOFTMAX) atomicOr(p.err, ERR_TARGET_RANGE);
       }
 
@@ -954,7 +1043,7 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
         }
         if (owner) {
           // exp(x_t - lse) - 1 without cancellation when the target dominates
-          const float gval = expm1f((xt - Mg) - logf(Sg)) * sc;
+          const float gval = expm1_target((xt - Mg) - lg2(Sg) * kLn2) * sc;
           if (t_smem) E::st(smem_ptr(tbo), gval);
           else E::st(elem_ptr_global(static_cast<int>(t)), gval);
         }
@@ -965,22 +1054,9 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
 
     // ---- deterministic reduction of the loss ----
     if (p.loss != nullptr) {
-      if (gt == 0) acc_slot[grp] = acc;
+      if (gt == 0) acc_slot[grp] = acc.value();
       group_sync(15, NC);  // an id no row group uses
-      if (tid == 0) {
-        double part = 0.0;
-        for (int j = 0; j < R; ++j) part += acc_slot[j];
-        p.partials[blockIdx.x] = part;
-        __threadfence();
-        const unsigned prev = atomicAdd(p.ticket, 1u);
-        if (prev == gridDim.x - 1) {
-          __threadfence();
-          double total = 0.0;
-          for (unsigned j = 0; j < gridDim.x; ++j) total += __ldcg(p.partials + j);
-          *p.loss = static_cast<float>(p.mean ? total / static_cast<double>(p.M) : total);
-          *p.ticket = 0u;  // ready for the next launch on this stream
-        }
-      }
+      if (warp == 0) loss_tail_warp(acc_slot, R, p.partials, p.ticket, p.loss, p.M, p.mean, lane);
     }
   }
 

@@ -162,8 +162,6 @@ __device__ __forceinline__ void online_rescale(float lm, float& m, float& mh, fl
   }
 }
 
-constexpr float kLn2 = 0.6931471805599453f;
-
 // KRES > 0 (FWD_BWD, SOFTMAX): "resident" rows.  Each lane copies its chunks
 // of the piece (at most KRES, lane + 32 k) from the ring into registers and
 // releases the slots at once; the gradient is computed from those registers
@@ -301,7 +299,7 @@ __global__ void __launch_bounds__(kStreamMaxWarps * 32, 1) ce_stream_kernel(cons
     }
   };
 
-  double acc = 0.0;  // the group's loss sum (warp kw == 0, lane 0)
+  PairSum acc;  // the group's loss sum (warp kw == 0, lane 0)
   // Targets (and, for BWD, the stored lse) of the group's rows are fetched 32
   // rows at a time, lane j holding row ri0 + j, one batch ahead, so their
   // latency never sits on a row's path.
@@ -511,6 +509,8 @@ __global__ void __launch_bounds__(kStreamMaxWarps * 32, 1) ce_stream_kernel(cons
       if (G == 1) {
         Mrow = mw;
         Srow = sw;
+        // the target logit, read by lane 0, for every lane
+        if (TARGETS) xt = __shfl_sync(0xffffffffu, xt, 0);
       } else {
         if (lane == 0) red[b][warp] = make_float4(mw, sw, xt, have_xt ? 1.f : 0.f);
         group_sync(1 + grp, G * 32);
@@ -532,7 +532,7 @@ __global__ void __launch_bounds__(kStreamMaxWarps * 32, 1) ce_stream_kernel(cons
         const float rl = t_ok ? (Mrow - xt) + lnS : __int_as_float(0x7fc00000);
         if (p.row_loss) p.row_loss[r] = rl;
         if (p.lse_out) p.lse_out[r] = Mrow + lnS;
-        acc += static_cast<double>(rl);
+        acc.add(rl);
         if (TARGETS && !t_ok) atomicOr(p.err, ERR_TARGET_RANGE);
       }
     } else if (row_leader && !t_ok) {
@@ -563,7 +563,8 @@ __global__ void __launch_bounds__(kStreamMaxWarps * 32, 1) ce_stream_kernel(cons
       const float scf = ex2(-Lc) * sc;
       // g_t = expm1(x_t - lse) * scale, evaluated from the target's own value
       auto target_grad = [&](float x) -> float {
-        return MODE == BWD ? expm1f(x - lse_given) * sc : expm1f((x - Mrow) - lnS) * sc;
+        return MODE == BWD ? expm1_target(x - lse_given) * sc
+                           : expm1_target((x - Mrow) - lnS) * sc;
       };
       char* const out_row = reinterpret_cast<char*>(g.as) + p.out_delta;
       // bf16 gradient rows (fp32 logits): chunk c holds elements e0 .. e0 + 3,
@@ -608,14 +609,13 @@ __global__ void __launch_bounds__(kStreamMaxWarps * 32, 1) ce_stream_kernel(cons
             E::unpack(qr[k], x);
 #pragma unroll
             for (int e = 0; e < EPC; ++e) gv[e] = ex2(fmaf(x[e], kLog2e, -mh)) * f;
-            if (c == tc) {
-#pragma unroll
-              for (int e = 0; e < EPC; ++e)
-                if (e == tq) gv[e] = target_grad(x[e]);
-            }
             store_chunk(o0 + 16LL * c, c, gv);
           }
         }
+        // the target's element: the lane that stored its chunk overwrites it
+        // (the same thread, so the two stores stay in program order)
+        if (t_ok && tc >= fa_row && tc < fb_row && lane == ((tc - g.p0) & 31))
+          store_elem(static_cast<int>(t), target_grad(xt));
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int c = h ? g.nI + 1 : 0;
@@ -647,7 +647,6 @@ __global__ void __launch_bounds__(kStreamMaxWarps * 32, 1) ce_stream_kernel(cons
           const int cl = cb + lane;
           const uint32_t a0 = sbase + 16 * (cl - c0);
           char* const o0 = out_row + (g.hb - 16 + 16LL * cl);
-          const bool t_here = tc >= cb && tc < cb + 128;  // the target's chunk is in this block
           uint4 q[4];
 #pragma unroll
           for (int j = 0; j < 4; ++j)
@@ -659,11 +658,6 @@ __global__ void __launch_bounds__(kStreamMaxWarps * 32, 1) ce_stream_kernel(cons
               E::unpack(q[j], x);
 #pragma unroll
               for (int e = 0; e < EPC; ++e) gv[e] = ex2(fmaf(x[e], kLog2e, -Lh)) * scf;
-              if (t_here && cl + 32 * j == tc) {
-#pragma unroll
-                for (int e = 0; e < EPC; ++e)
-                  if (e == tq) gv[e] = target_grad(x[e]);
-              }
               store_chunk(o0 + 512 * j, cl + 32 * j, gv);
             }
           }
@@ -671,6 +665,15 @@ __global__ void __launch_bounds__(kStreamMaxWarps * 32, 1) ce_stream_kernel(cons
         int cb = fa;
         for (; cb + 128 <= fb; cb += 128) grad_block(cb, kTrue{});
         if (cb < fb) grad_block(cb, kFalse{});
+        // the target's element, when its chunk is a full chunk of this segment:
+        // lane (tc - fa) mod 32 stored that chunk above and now overwrites the one
+        // element (the same thread, so the two stores stay in program order); no
+        // test of the target sits in the blocks' inner loops
+        if (t_ok && tc >= fa && tc < fb && lane == ((tc - fa) & 31)) {
+          const float xv = E::ld(static_cast<const char*>(
+              __cvta_shared_to_generic(sbase + 16 * (tc - c0) + tq * ES)));
+          store_elem(static_cast<int>(t), target_grad(xv));
+        }
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int c = h ? g.nI + 1 : 0;
@@ -698,22 +701,10 @@ __global__ void __launch_bounds__(kStreamMaxWarps * 32, 1) ce_stream_kernel(cons
 
   // ---- deterministic reduction of the loss ----
   if (STATS && p.loss != nullptr) {
-    if (kw == 0 && lane == 0) acc_slot[grp] = acc;
+    if (kw == 0 && lane == 0) acc_slot[grp] = acc.value();
     __syncthreads();
-    if (threadIdx.x == 0) {
-      double part = 0.0;
-      for (int j = 0; j < ngrp_cta; ++j) part += acc_slot[j];
-      p.partials[blockIdx.x] = part;
-      __threadfence();
-      const unsigned prev = atomicAdd(p.ticket, 1u);
-      if (prev == gridDim.x - 1) {
-        __threadfence();
-        double total = 0.0;
-        for (unsigned j = 0; j < gridDim.x; ++j) total += __ldcg(p.partials + j);
-        *p.loss = static_cast<float>(p.mean ? total / static_cast<double>(p.M) : total);
-        *p.ticket = 0u;  // ready for the next launch on this stream
-      }
-    }
+    if (warp == 0)
+      loss_tail_warp(acc_slot, ngrp_cta, p.partials, p.ticket, p.loss, p.M, p.mean, lane);
   }
 }
 

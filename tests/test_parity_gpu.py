@@ -344,7 +344,30 @@ def test_large_workloads_sampled(name):
     w = synthetic.WORKLOADS[name]
     x, t = synthetic.make_workload(w)
     rows = P.sample_rows(w.M, 128)
-    check_case(x, t, w.dtype, rows=rows)
+    out = check_case(x, t, w.dtype, rows=rows)
+    # the deterministic mean over every row against the float64 oracle's mean
+    # over every row (the per-row definition, reduced by a separate sum)
+    ref = P.workload_full_loss(name)
+    P.check_loss(out["loss_f"].item(), ref, w.dtype, w.M)
+    P.check_loss(out["loss_b"].item(), ref, w.dtype, w.M)
+
+
+@pytest.mark.parametrize("kernel", ["unit", "stream"])
+@pytest.mark.parametrize("dtype,V", [("f32", 1000), ("bf16", 4099), ("f16", 50257),
+                                     ("f32", 131072)])
+def test_target_gradient_across_probability(kernel, dtype, V, monkeypatch):
+    # rows whose target holds from almost none to almost all of the probability:
+    # u = x_t - lse sweeps (-25, 0], across the switch at u = -1/2 between the
+    # two forms of exp(u) - 1 used for the target's gradient
+    monkeypatch.setenv("CE_KERNEL", kernel)
+    M = 96
+    x = synthetic.make_logits(M, V, "f32", 0.5, seed=V + 31)
+    t = synthetic.make_targets(M, V, seed=V + 32)
+    lift = np.linspace(-12.0, 12.0 + np.log(V), M)
+    x[np.arange(M), t] = (np.max(x, axis=1) + lift).astype(np.float32)
+    xs = (x if dtype == "f32" else x.astype(np.float16) if dtype == "f16"
+          else synthetic.f32_to_bf16_bits(x))
+    check_case(xs, t, dtype, "sum")
 
 
 @pytest.mark.parametrize("plan", ["3,1,1,1", "2,2,1,1", "0,1,1,1", "3,1,2,1"])

@@ -251,4 +251,8 @@ def test_stream_softmax(dtype, inplace, V):
 def test_stream_workloads_sampled(name):
     w = synthetic.WORKLOADS[name]
     x, t = synthetic.make_workload(w)
-    check_case(x, t, w.dtype, rows=P.sample_rows(w.M, 128))
+    out = check_case(x, t, w.dtype, rows=P.sample_rows(w.M, 128))
+    # the mean over every row against the float64 oracle's
+    ref = P.workload_full_loss(name)
+    P.check_loss(out["loss_f"].item(), ref, w.dtype, w.M)
+    P.check_loss(out["loss_b"].item(), ref, w.dtype, w.M)
