@@ -41,14 +41,12 @@ from softmax_cross_entropy_online_gb300 import synthetic  # noqa: E402
 METRIC = "CE fwd+bwd GB/s and % of GB300 HBM roofline (ms per call) at 1 GPU"
 FALLBACK_HBM_GBS = 6800.0
 
-# DRAM traffic of the fused fwd+bwd kernel per launch on f32 [32768, 4096],
-# from `ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum` (summarised
-# under profiles/), valid only for the kernel source it was taken on: the
-# digest of the row-kernel sources at that time.  Any change to them nulls it.
-NCU_TRAFFIC = {
-    # profiles/ce_rows_fwd_bwd_f32_32768x4096.md: a 16384-row capture, scaled 2x
-    "212491ab2683c7ad7d0428a7e08da2c8857bbc3bd6549cdc51cb282f1b2e3e0e": {
-        "workload": "f32_32768x4096", "bytes_per_launch": 950148096},
+# DRAM traffic per launch of each workload's default kernel, from one
+# `ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum` capture (a reduced
+# row count, scaled to the full launch by the rows processed), keyed by the
+# digest of the row-kernel sources the counters were taken on: any change to
+# those sources nulls every record until it is captured again.
+NCU_TRAFFIC: dict[str, dict[str, int]] = {
 }
 
 
@@ -113,6 +111,39 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.lines.append(line.strip())
 
+    def mark(self) -> int:
+        """Index of the next sample (to delimit a window of samples)."""
+        return len(self.lines)
+
+    @staticmethod
+    def summarize(lines) -> dict:
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            try:
+                power.append(float(parts[3]))
+            except ValueError:
+                pass
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_median": statistics.median(power) if power else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+    def window(self, i0: int, i1: int) -> dict:
+        """Summary of the samples taken between two marks."""
+        return self.summarize(list(self.lines[i0:i1]))
+
     def stop(self):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
@@ -123,23 +154,7 @@ class ClockSampler:
             self.proc.kill()
         if self.thread:
             self.thread.join(timeout=5)
-        sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                smax.append(float(parts[2]))
-            except ValueError:
-                continue
-            for name, val in zip(names, parts[5:9]):
-                if val.lower() == "active":
-                    reasons.add(name)
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        return self.summarize(self.lines)
 
 
 def max_over_ranks(x: float, device) -> float:
@@ -301,6 +316,105 @@ def cpu_baseline(w, budget_s: float):
 # ---------------------------------------------------------------------------
 # native arm
 # ---------------------------------------------------------------------------
+def flush_l2(scratch) -> None:
+    """Write a buffer larger than the L2 (129 MB), so no input starts warm."""
+    scratch.fill_(1)
+
+
+def time_per_call(fn, bufs, pristine, flush, reps: int = 3, warmup: int = 3, refresh=True):
+    """Device time of one call (ms): the calls run back to back, one per
+    distinct buffer, bracketed by CUDA events on the launch stream; before each
+    rep the buffers get fresh inputs and the L2 is flushed (both untimed).
+    Returns the median over reps and the per-rep times."""
+    import torch
+    for i in range(warmup):
+        fn(bufs[i % len(bufs)])
+    times = []
+    for _ in range(reps):
+        if refresh:
+            for b in bufs:
+                b.copy_(pristine)
+        flush()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record()
+        for b in bufs:
+            fn(b)
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1) / len(bufs))
+    return statistics.median(times), times
+
+
+def traffic_record(workload: str):
+    """ncu DRAM bytes per launch of a workload's default kernel, when the row-kernel
+    sources are the ones the counters were taken on; else None."""
+    rec = NCU_TRAFFIC.get(csrc_digest(), {})
+    return rec.get(workload)
+
+
+def workload_tensors(w, dev):
+    import torch
+    x_np = synthetic.make_logits(w.M, w.V, w.dtype, w.sigma, w.spike_prob, w.spike_value, w.seed)
+    t_np = synthetic.make_targets(w.M, w.V, w.seed)
+    if w.dtype == "bf16":
+        host = torch.from_numpy(x_np.view(np.int16)).view(torch.bfloat16)
+    else:
+        host = torch.from_numpy(x_np)
+    return host, torch.from_numpy(t_np)
+
+
+def sub_record(L, api, w, dev, sh, flush, peak, bwd: bool, n_bufs: int):
+    """One more workload timed beside the headline one: ms per call of the
+    default kernel (fused fwd+bwd in place, or the forward), GB/s of the
+    algorithmic bytes, the roofline fraction, rows/s, and ncu traffic."""
+    import torch
+    host, t_host = workload_tensors(w, dev)
+    pristine = host.to(dev)
+    targets = t_host.to(dev)
+    del host
+    M, V = w.M, w.V
+    es = synthetic.ELEM_BYTES[w.dtype]
+    code = {"f32": 0, "f16": 1, "bf16": 2}[w.dtype]
+    bufs = [pristine.clone() for _ in range(n_bufs)]
+    loss = torch.empty((), dtype=torch.float32, device=dev)
+    rl = torch.empty(M, dtype=torch.float32, device=dev)
+    lse = torch.empty(M, dtype=torch.float32, device=dev)
+    entry = L.ce_fwd_bwd_inplace if bwd else L.ce_forward
+
+    def fn(b):
+        st = entry(b.data_ptr(), targets.data_ptr(), M, V, code, 0, loss.data_ptr(),
+                   rl.data_ptr(), lse.data_ptr(), sh)
+        if st != 0:
+            raise api.CEError(st, entry.__name__)
+
+    ms, reps = time_per_call(fn, bufs, pristine, flush, refresh=bwd)
+    assert api.ce_check_errors() == 0
+    nbytes = algorithmic_bytes(M, V, es, bwd)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    out = {"workload": workload_desc(w), "call": ("ce_fwd_bwd_inplace (mean)" if bwd
+                                                  else "ce_forward (mean, row loss, lse)"),
+           "M": M, "V": V, "dtype": w.dtype, "ms_per_call": ms, "us_per_call": ms * 1e3,
+           "gb_s": gbs, "rows_per_s": M / (ms * 1e-3),
+           "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                        "frac": gbs / peak, "bytes_per_launch": nbytes,
+                        "traffic": traffic_record(w.name)},
+           "latency_bound": nbytes / (peak * 1e9) < 4e-6,
+           "timing": f"{len(bufs)} distinct buffers back to back, L2 flushed, median of "
+                     f"{len(reps)} reps"}
+    del bufs, pristine
+    torch.cuda.empty_cache()
+    return out
+
+
+# The workloads timed beside the headline one in the default run: (name, fused
+# fwd+bwd?, distinct buffers).  The small fp32 case is forward only and bound
+# by launch latency; its 300 buffers (> L2) keep every call cold.
+SIDE_WORKLOADS = (("small_f32_256x1024", False, 300), ("f16_8192x131072_spiked", True, 6),
+                  ("bf16_16384x50257", True, 6))
+
+
 def run_native(args, w):
     import torch
     import torch.distributed as dist
@@ -317,17 +431,11 @@ def run_native(args, w):
 
     M, V = w.M, w.V
     es = synthetic.ELEM_BYTES[w.dtype]
-    tdt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[w.dtype]
     code = {"f32": 0, "f16": 1, "bf16": 2}[w.dtype]
 
-    x_np = synthetic.make_logits(M, V, w.dtype, w.sigma, w.spike_prob, w.spike_value, w.seed)
-    t_np = synthetic.make_targets(M, V, w.seed)
-    if w.dtype == "bf16":
-        host = torch.from_numpy(x_np.view(np.int16)).view(torch.bfloat16)
-    else:
-        host = torch.from_numpy(x_np)
+    host, t_cpu = workload_tensors(w, dev)
     host = host.pin_memory()
-    t_host = torch.from_numpy(t_np).pin_memory()
+    t_host = t_cpu.pin_memory()
     pristine = host.to(dev)
     targets = t_host.to(dev)
     step_bytes = M * V * es
@@ -340,6 +448,10 @@ def run_native(args, w):
     lse = torch.empty(M, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
+    l2_scratch = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def flush():
+        flush_l2(l2_scratch)
 
     def step(buf):
         st = L.ce_fwd_bwd_inplace(buf.data_ptr(), targets.data_ptr(), M, V, code, 0,
@@ -352,6 +464,7 @@ def run_native(args, w):
     # refresh every timed buffer with the pristine logits (untimed)
     for b in bufs:
         b.copy_(pristine)
+    flush()
     torch.cuda.synchronize()
     if ws > 1:
         dist.barrier()
@@ -360,68 +473,79 @@ def run_native(args, w):
     if sampler:
         sampler.start()
         time.sleep(0.3)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
     region0 = torch.cuda.Event(enable_timing=True)
     region1 = torch.cuda.Event(enable_timing=True)
     launches0 = api.ce_launch_count()
     torch.cuda.synchronize()
     if ws > 1:
         dist.barrier()
+    # the K calls back to back between two events on the launch stream (an event
+    # between calls would make each call wait for the previous one to drain)
     region0.record(stream)
     for i in range(args.steps):
-        ev[i][0].record(stream)
         step(bufs[i % n_bufs])
-        ev[i][1].record(stream)
     region1.record(stream)
     torch.cuda.synchronize()
     launches = api.ce_launch_count() - launches0
+    # a sustained window of the same call over the resident buffers (their contents
+    # are by now earlier calls' gradients: the same work per call), long enough for
+    # the clock sampler to see it; outside the events that time `value`
+    sustained = None
+    if rank == 0 and args.sustained_s > 0:
+        avg = region0.elapsed_time(region1) / args.steps
+        n_sus = max(1, int(args.sustained_s / (avg * 1e-3)))
+        mark0 = sampler.mark()
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for i in range(n_sus):
+            step(bufs[i % n_bufs])
+        s1.record(stream)
+        torch.cuda.synchronize()
+        mark1 = sampler.mark()
+        sus_ms = s0.elapsed_time(s1) / n_sus
+        sustained = {"calls": n_sus, "seconds": s0.elapsed_time(s1) * 1e-3,
+                     "ms_per_call": sus_ms,
+                     "gb_s": algorithmic_bytes(M, V, es, True) / (sus_ms * 1e-3) / 1e9,
+                     "clocks": sampler.window(mark0, mark1)}
     clocks = sampler.stop() if sampler else None
+    if clocks is not None and sustained is not None and sustained["clocks"]["samples"]:
+        # the clocks under load: the samples of the sustained window, with the
+        # whole run's count and reasons beside them
+        whole = clocks
+        clocks = dict(sustained["clocks"])
+        clocks["window"] = "the sustained window of back-to-back calls"
+        clocks["samples_whole_run"] = whole["samples"]
+        clocks["reasons"] = sorted(set(clocks["reasons"]) | set(whole["reasons"]))
     region_ms = region0.elapsed_time(region1)
-    kernel_ms = [a.elapsed_time(b) for a, b in ev]
+    local_kernel_ms = region_ms / args.steps  # this rank's mean time per launch
     region_ms = max_over_ranks(region_ms, dev)
     assert api.ce_check_errors() == 0
 
     ms_per_step = region_ms / args.steps
     b_step = algorithmic_bytes(M, V, es, True)
     value = aggregate_gbs(ws, b_step, ms_per_step)
-    avg_kernel_ms = sum(kernel_ms) / len(kernel_ms)
+    avg_kernel_ms = local_kernel_ms
     peak, peak_kind = measured_peaks()
     achieved = b_step / (avg_kernel_ms * 1e-3) / 1e9
-    rec = NCU_TRAFFIC.get(csrc_digest(), {})
-    traffic = rec.get("bytes_per_launch") if rec.get("workload") == w.name else None
+    traffic = traffic_record(w.name)
+    if sustained is not None:
+        sustained["frac"] = sustained["gb_s"] / peak
 
     # forward-only pass on the same workload (the first half of the config)
     fwd_ms = sm_ms = probe = None
     if rank == 0:
-        for b in bufs[:2]:
-            b.copy_(pristine)
-        torch.cuda.synchronize()
-        fe0 = torch.cuda.Event(enable_timing=True)
-        fe1 = torch.cuda.Event(enable_timing=True)
         nf = min(args.steps, n_bufs)
-        for i in range(3):
-            L.ce_forward(bufs[i % n_bufs].data_ptr(), targets.data_ptr(), M, V, code, 0,
-                         loss.data_ptr(), row_loss.data_ptr(), lse.data_ptr(), sh)
-        fe0.record(stream)
-        for i in range(nf):
-            L.ce_forward(bufs[i % n_bufs].data_ptr(), targets.data_ptr(), M, V, code, 0,
-                         loss.data_ptr(), row_loss.data_ptr(), lse.data_ptr(), sh)
-        fe1.record(stream)
-        torch.cuda.synchronize()
-        fwd_ms = fe0.elapsed_time(fe1) / nf
+        fbufs = bufs[:nf]
+        fwd_ms, _ = time_per_call(
+            lambda b: L.ce_forward(b.data_ptr(), targets.data_ptr(), M, V, code, 0,
+                                   loss.data_ptr(), row_loss.data_ptr(), lse.data_ptr(), sh),
+            fbufs, pristine, flush, reps=3)
         # the fused softmax (probabilities written over the logits, one read and
         # one write per element) on the same buffers
-        for i in range(3):
-            L.ce_softmax_forward(bufs[i % n_bufs].data_ptr(), bufs[i % n_bufs].data_ptr(), M, V,
-                                 code, None, sh)
-        fe0.record(stream)
-        for i in range(nf):
-            L.ce_softmax_forward(bufs[i % n_bufs].data_ptr(), bufs[i % n_bufs].data_ptr(), M, V,
-                                 code, None, sh)
-        fe1.record(stream)
-        torch.cuda.synchronize()
-        sm_ms = fe0.elapsed_time(fe1) / nf
+        sm_ms, _ = time_per_call(
+            lambda b: L.ce_softmax_forward(b.data_ptr(), b.data_ptr(), M, V, code, None, sh),
+            fbufs, pristine, flush, reps=3)
         assert api.ce_check_errors() == 0
         # stream probes over the same buffers with PyTorch's own kernels (not the
         # library's): an in-place read + write pass (x *= 1) and a read-only pass
@@ -429,39 +553,52 @@ def run_native(args, w):
         probe = {}
         for name, fn, nbytes in (("inplace_rw", lambda b: b.mul_(1), 2 * M * V * es),
                                  ("read_only", lambda b: torch.amax(b), M * V * es)):
-            for i in range(3):
-                fn(bufs[i % n_bufs])
-            fe0.record(stream)
-            for i in range(nf):
-                fn(bufs[i % n_bufs])
-            fe1.record(stream)
-            torch.cuda.synchronize()
-            pms = fe0.elapsed_time(fe1) / nf
+            pms, _ = time_per_call(fn, fbufs, pristine, flush, reps=3)
             probe[name] = {"ms": pms, "gb_s": nbytes / (pms * 1e-3) / 1e9,
                            "frac": nbytes / (pms * 1e-3) / 1e9 / peak}
 
-    # end to end: host logits -> device, the call, loss -> host, every step
+    # end to end through the public call: host logits and targets -> device, the
+    # call, then the call's outputs -> host: the gradient it wrote over the
+    # logits and the loss, every step
     loss_host = torch.empty((), dtype=torch.float32).pin_memory()
+    grad_host = torch.empty_like(host).pin_memory()
     dbuf = bufs[0]
-    for _ in range(2):
+
+    def e2e_step():
         dbuf.copy_(host, non_blocking=True)
+        targets.copy_(t_host, non_blocking=True)
         step(dbuf)
+        grad_host.copy_(dbuf, non_blocking=True)
         loss_host.copy_(loss, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e2e_steps = max(3, min(args.steps, 10))
     e0.record(stream)
     for _ in range(e2e_steps):
-        dbuf.copy_(host, non_blocking=True)
-        targets.copy_(t_host, non_blocking=True)
-        step(dbuf)
-        loss_host.copy_(loss, non_blocking=True)
+        e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
     e2e_ms = max_over_ranks(e2e_ms, dev)
     e2e_value = aggregate_gbs(ws, b_step, e2e_ms)
+    del grad_host
+
+    side = None
+    if rank == 0 and not args.no_side_workloads and args.rows is None:
+        del bufs
+        torch.cuda.empty_cache()
+        side = {}
+        for name, bwd, nb in SIDE_WORKLOADS:
+            if name == w.name:
+                continue
+            side[name] = sub_record(L, api, synthetic.WORKLOADS[name], dev, sh, flush, peak,
+                                    bwd, nb)
+        if not args.no_linear_side:
+            side["linear_ce_8192x4096x128256"] = linear_side_record(L, api, dev, sh)
 
     if rank == 0:
         line = {
@@ -483,17 +620,23 @@ def run_native(args, w):
                          "bytes_per_launch": b_step},
             "forward_only": None if fwd_ms is None else {
                 "ms_per_call": fwd_ms,
-                "gb_s": algorithmic_bytes(M, V, es, False) / (fwd_ms * 1e-3) / 1e9},
+                "gb_s": algorithmic_bytes(M, V, es, False) / (fwd_ms * 1e-3) / 1e9,
+                "frac": algorithmic_bytes(M, V, es, False) / (fwd_ms * 1e-3) / 1e9 / peak},
             "stream_probes": probe,
             "softmax": None if sm_ms is None else {
                 "call": "ce_softmax_forward (in place)", "ms_per_call": sm_ms,
                 "gb_s": 2 * M * V * es / (sm_ms * 1e-3) / 1e9,
                 "frac": 2 * M * V * es / (sm_ms * 1e-3) / 1e9 / peak},
             "e2e": {"value": e2e_value, "unit": "GB/s",
-                    "h2d_bytes_per_step": step_bytes + M * 8, "d2h_bytes_per_step": 4,
-                    "ms_per_step": e2e_ms},
+                    "h2d_bytes_per_step": step_bytes + M * 8,
+                    "d2h_bytes_per_step": step_bytes + 4,
+                    "ms_per_step": e2e_ms,
+                    "what": "pinned host logits + targets -> device, ce_fwd_bwd_inplace, "
+                            "the gradient (written over the logits) + loss -> pinned host"},
             "gpu_launches": launches,
             "clocks": clocks,
+            "sustained": sustained,
+            "side_workloads": side,
         }
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(w, args.cpu_budget_s)
@@ -521,6 +664,55 @@ def measured_tflops(burst: bool = False):
         if d.get(key):
             return float(d[key]), f"measured ({'burst' if burst else 'sustained'})"
     return (1900.0, "fallback (burst)") if burst else (1700.0, "fallback (sustained)")
+
+
+def linear_side_record(L, api, dev, sh, steps: int = 5, warmup: int = 3) -> dict:
+    """The fused linear + cross-entropy step on its full workload (bf16 h
+    [8192, 4096], W [128256, 4096]), timed beside the headline line: ms per
+    step and TFLOP/s of the three GEMMs (6 M H V), against the sustained bf16
+    peak."""
+    import torch
+    M, H, V = LINEAR_SHAPES["linear_ce_8192x4096x128256"]
+    h_np, W_np, t_np = synthetic.make_linear_ce_inputs(M, H, V, seed=0)
+    as_bf16 = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)  # noqa: E731
+    h, W, t = as_bf16(h_np).to(dev), as_bf16(W_np).to(dev), torch.from_numpy(t_np).to(dev)
+    del h_np, W_np
+    wsb = int(L.linear_ce_workspace_size(M, H, V))
+    work = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    loss = torch.empty((), dtype=torch.float32, device=dev)
+    dH = torch.empty((M, H), dtype=torch.float32, device=dev)
+    dW = torch.empty((V, H), dtype=torch.float32, device=dev)
+
+    def step():
+        st = L.linear_ce_fwd_bwd(h.data_ptr(), W.data_ptr(), t.data_ptr(), M, H, V,
+                                 loss.data_ptr(), dH.data_ptr(), dW.data_ptr(),
+                                 work.data_ptr(), wsb, sh)
+        if st != 0:
+            raise api.CEError(st, "linear_ce_fwd_bwd")
+
+    for _ in range(warmup):
+        step()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    assert api.ce_check_errors() == 0
+    ms = e0.elapsed_time(e1) / steps
+    flops = 6.0 * M * V * H
+    peak, kind = measured_tflops()
+    tf = flops / (ms * 1e-3) / 1e12
+    out = {"workload": f"linear_ce_8192x4096x128256: bf16 h [{M}, {H}] N(0,1), W [{V}, {H}] "
+                       "N(0, 0.02^2), int64 targets; loss, dH, dW (fp32)",
+           "call": "linear_ce_fwd_bwd", "ms_per_step": ms, "tflop_s": tf,
+           "roofline": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s",
+                        "frac": tf / peak, "peak_source": kind},
+           "loss": loss.item(), "steps": steps, "workspace_bytes": wsb}
+    del h, W, t, work, dH, dW
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_linear(args):
@@ -688,9 +880,12 @@ def run_linear_reference(args):
     h_np, W_np, t_np = synthetic.make_linear_ce_inputs(M, H, V, seed=0)
     W64 = oracle.to_f64(W_np, "bf16")
     for _ in range(args.warmup):
-        t0 = time.perf_counter()
         oracle.linear_ce(oracle.to_f64(h_np[:1], "bf16"), W64, t_np[:1], "mean")
-        one_row_s = time.perf_counter() - t0
+    # a one-row probe sizes the steps (timed apart from the warm-up calls, so it
+    # exists whatever the warm-up count)
+    t0 = time.perf_counter()
+    oracle.linear_ce(oracle.to_f64(h_np[:1], "bf16"), W64, t_np[:1], "mean")
+    one_row_s = time.perf_counter() - t0
     # rows per step: the steps together take about a minute (at least one row)
     step_budget = max(0.5, 60.0 / max(1, args.steps))
     rows = int(max(1, min(M, args.ref_rows, step_budget / max(one_row_s, 1e-6))))
@@ -727,10 +922,10 @@ def run_linear_reference(args):
 ATTN_SHAPES = {"attn_causal_32x96x512x128": (32, 96, 512, 128, True)}
 ATTN_SOURCES = ("ce_attention.cu", "ce_tc.cuh")
 # DRAM traffic of the attention kernel per launch on the workload above, from
-# `ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum` (summarised under
-# profiles/), valid only for the attention sources it was taken on.
+# `ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum`, valid only for
+# the attention sources it was taken on.
 ATTN_NCU_TRAFFIC = {
-    # profiles/attention_fwd_bf16_32x96x512x128_causal.md
+    # bf16 [32, 96, 512, 128] causal, bf16 output
     "16dab2fec8146bfc2035d7edd17ebeba680df01bf7b477ce2a3d748dcfad31fb": {
         "workload": "attn_causal_32x96x512x128", "bytes_per_launch": 1592443392},
 }
@@ -942,6 +1137,12 @@ def main():
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     ap.add_argument("--ref-rows", type=int, default=1024)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-side-workloads", action="store_true",
+                    help="time only the headline workload (no fp16/bf16/small side records)")
+    ap.add_argument("--no-linear-side", action="store_true",
+                    help="leave the fused linear + CE step out of the side records")
+    ap.add_argument("--sustained-s", type=float, default=2.0,
+                    help="seconds of back-to-back calls during which the clocks are sampled")
     ap.add_argument("--rows", type=int, default=None,
                     help="override the workload's row count (smaller cases for profiling)")
     ap.add_argument("--heads", type=int, default=None,
