@@ -730,6 +730,8 @@ def run_linear(args):
     M, H, V = LINEAR_SHAPES[args.workload]
     if args.rows is not None:
         M = args.rows
+    if args.vocab is not None:
+        V = args.vocab
     h_np, W_np, t_np = synthetic.make_linear_ce_inputs(M, H, V, seed=0)
     as_bf16 = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)  # noqa: E731
     h_host, W_host = as_bf16(h_np).pin_memory(), as_bf16(W_np).pin_memory()
@@ -1145,6 +1147,8 @@ def main():
                     help="seconds of back-to-back calls during which the clocks are sampled")
     ap.add_argument("--rows", type=int, default=None,
                     help="override the workload's row count (smaller cases for profiling)")
+    ap.add_argument("--vocab", type=int, default=None,
+                    help="linear + CE workload: override V (smaller cases for profiling)")
     ap.add_argument("--heads", type=int, default=None,
                     help="attention workloads: run B = 1 with this many heads instead")
     args = ap.parse_args()

@@ -165,19 +165,24 @@ ce_status ce_backward_from_lse(void* logits, const int64_t* targets, const float
  *     dH   = G W          [M, H]      G = (softmax(logits) - onehot) / M
  *     dW   = G^T h        [V, H]
  *
- * Rows are processed in chunks: each chunk's logits are produced by a
- * tcgen05 GEMM into the workspace, turned by the row kernel into the bf16
- * gradient rows G (never written in fp32), and contracted into dH and dW
- * (accumulated over chunks) by two more tcgen05 GEMMs that read W, G and h in
- * their stored layouts, with fp32 accumulation.
+ * Rows are processed in chunks: each chunk's fp32 logits are produced by a
+ * tcgen05 GEMM into the workspace (one chunk at a time: the [M, V] logits
+ * never exist at once) and turned by the row kernel into the bf16 gradient
+ * rows G and the row losses.  With a workspace that holds G for every row
+ * (the size linear_ce_workspace_size returns), dH and dW are then each one
+ * tcgen05 GEMM over all rows, dW written once.  With a smaller workspace,
+ * each chunk's G is contracted into dH and dW before the next chunk (dW
+ * accumulated over the chunks).  The GEMMs read W, G and h in their stored
+ * layouts, with fp32 accumulation.
  *
  *   h        [M, H] bf16, row-major; W [V, H] bf16, row-major (device).
  *            H must be a multiple of 8; h and W 16-byte aligned.
  *   targets  [M] int64.   loss [1] fp32.   dH [M, H] fp32.   dW [V, H] fp32.
- *   workspace  device memory of workspace_bytes >= linear_ce_workspace_size
- *            for some chunk size (256-byte aligned, owned by the caller); a
- *            smaller workspace is used with a smaller row chunk, down to 128
- *            rows, else CE_ERR_INVALID_ARG.
+ *   workspace  device memory (256-byte aligned, owned by the caller) of
+ *            workspace_bytes: at least linear_ce_workspace_size(M, H, V) for
+ *            the whole-G schedule; less selects a smaller row chunk and then
+ *            the per-chunk schedule, down to 128-row chunks (about
+ *            128 * V * 6 + 4 * M bytes), else CE_ERR_INVALID_ARG.
  *   G is rounded to bf16 before the two gradient GEMMs; logits, the loss
  *   and every accumulation are fp32.
  */
@@ -185,7 +190,9 @@ ce_status linear_ce_fwd_bwd(const void* h, const void* W, const int64_t* targets
                             int64_t H, int64_t V, float* loss, float* dH, float* dW,
                             void* workspace, size_t workspace_bytes, void* stream);
 
-/* Workspace bytes of linear_ce_fwd_bwd at its default row chunk (0 on bad sizes). */
+/* Workspace bytes of linear_ce_fwd_bwd's whole-G schedule at its default row
+ * chunk of 2048 (or M) rows: one fp32 logits chunk, bf16 G [M, V rounded up to
+ * a multiple of 8] and the fp32 row losses (0 on bad sizes). */
 size_t linear_ce_workspace_size(int64_t M, int64_t H, int64_t V);
 
 /*

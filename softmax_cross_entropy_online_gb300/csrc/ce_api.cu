@@ -653,22 +653,27 @@ ce_status launch_rows(int mode, const void* logits, const int64_t* targets, cons
 }
 
 // Workspace of the fused linear + cross-entropy for row chunks of `mc` rows:
-// logits [mc, V] fp32, G16 [mc, ldv] bf16 (ldv = V rounded up to a multiple of
-// 8), row losses [M] fp32.  The GEMMs read W, G16 and h in their stored
-// layouts (MN-major operands where K is not contiguous), so nothing is
-// transposed.
+// logits [mc, V] fp32 (one chunk at a time), the bf16 gradient rows G [g_rows,
+// ldv] (ldv = V rounded up to a multiple of 8), row losses [M] fp32.  With
+// g_rows = M ("whole G") every chunk's G rows stay, and dH and dW are each one
+// GEMM over all rows after the last chunk: dW is written once, with no
+// read-modify-write per chunk, and dH's tiles fill the machine.  With g_rows =
+// mc (the fallback for a smaller workspace) each chunk's G is contracted before
+// the next chunk overwrites it, dW accumulating over the chunks.  The GEMMs read
+// W, G and h in their stored layouts (MN-major operands where K is not
+// contiguous), so nothing is transposed.
 struct LinearWs {
   size_t logits, g16, rl, total;
 };
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
-LinearWs linear_ws_layout(long long M, long long V, long long mc) {
+LinearWs linear_ws_layout(long long M, long long V, long long mc, long long g_rows) {
   const long long ldv = (V + 7) / 8 * 8;
   LinearWs w;
   size_t off = 0;
   w.logits = off;
   off += round256(static_cast<size_t>(mc) * V * 4);
   w.g16 = off;
-  off += round256(static_cast<size_t>(mc) * ldv * 2);
+  off += round256(static_cast<size_t>(g_rows) * ldv * 2);
   w.rl = off;
   off += round256(static_cast<size_t>(M) * 4);
   w.total = off;
@@ -788,7 +793,7 @@ size_t linear_ce_workspace_size(int64_t M, int64_t H, int64_t V) {
   if (M < 0 || H < 1 || V < 1) return 0;
   const long long mc = M < kLinearDefaultChunk ? (M > 0 ? M : 1) : kLinearDefaultChunk;
   (void)H;
-  return linear_ws_layout(M, V, mc).total;
+  return linear_ws_layout(M, V, mc, M > 0 ? M : 1).total;
 }
 
 ce_status linear_ce_fwd_bwd(const void* h, const void* W, const int64_t* targets, int64_t M,
@@ -803,17 +808,26 @@ ce_status linear_ce_fwd_bwd(const void* h, const void* W, const int64_t* targets
       (reinterpret_cast<uintptr_t>(loss) % 4))
     return CE_ERR_INVALID_ARG;
   if (M > INT32_MAX || H > INT32_MAX || V > INT32_MAX) return CE_ERR_UNSUPPORTED;
-  // the largest row chunk (a multiple of 128, or all of M) whose workspace fits
+  // the schedule and row chunk: the largest chunk (a multiple of 128, or all of
+  // M) whose workspace fits with the whole of G, else the largest that fits with
+  // one chunk of G
   long long mc = M < kLinearDefaultChunk ? M : kLinearDefaultChunk;
-  while (linear_ws_layout(M, V, mc).total > workspace_bytes) {
-    if (mc <= 128) return CE_ERR_INVALID_ARG;
+  bool whole_g = true;
+  while (linear_ws_layout(M, V, mc, M).total > workspace_bytes && mc > 128)
     mc = (mc / 2 + 127) / 128 * 128;
+  if (linear_ws_layout(M, V, mc, M).total > workspace_bytes) {
+    whole_g = false;
+    mc = M < kLinearDefaultChunk ? M : kLinearDefaultChunk;
+    while (linear_ws_layout(M, V, mc, mc).total > workspace_bytes) {
+      if (mc <= 128) return CE_ERR_INVALID_ARG;
+      mc = (mc / 2 + 127) / 128 * 128;
+    }
   }
   DeviceInfo di;
   int dev = 0;
   ce_status st = device_info(di, &dev);
   if (st != CE_OK) return st;
-  const LinearWs L = linear_ws_layout(M, V, mc);
+  const LinearWs L = linear_ws_layout(M, V, mc, whole_g ? M : mc);
   char* ws = static_cast<char*>(workspace);
   auto* logits = reinterpret_cast<float*>(ws + L.logits);
   auto* g16 = reinterpret_cast<__nv_bfloat16*>(ws + L.g16);
@@ -823,34 +837,50 @@ ce_status linear_ce_fwd_bwd(const void* h, const void* W, const int64_t* targets
   const unsigned hint = wait_hint_ns();
   const int sms = di.sm_count;
   const auto* Wb = static_cast<const __nv_bfloat16*>(W);
+  const auto* hb = static_cast<const __nv_bfloat16*>(h);
   uint64_t launches = 0;
   const float scale = 1.0f / static_cast<float>(M);
   for (long long m0 = 0; m0 < M; m0 += mc) {
     const long long rows = (M - m0) < mc ? (M - m0) : mc;
-    const auto* hc = static_cast<const __nv_bfloat16*>(h) + m0 * H;
+    const auto* hc = hb + m0 * H;
+    __nv_bfloat16* const gc = whole_g ? g16 + m0 * ldv : g16;
     // logits[rows, V] = h_c W^T: both operands K-major (K = H)
     if ((st = ce::gemm_bf16(hc, H, false, Wb, H, false, logits, V, static_cast<int>(rows),
                             static_cast<int>(V), static_cast<int>(H), 0.f, s, di.err, sms,
                             hint)) != CE_OK)
       return st;
-    // row losses, and G16 [rows, ldv] = bf16 of G = (softmax - onehot) / M
+    // row losses, and G rows [rows, ldv] = bf16 of G = (softmax - onehot) / M
     // written by the row kernel straight from the fp32 logits
     if ((st = launch_rows(ce::FWD_BWD, logits, targets + m0, nullptr, rows, V, CE_F32,
                           CE_RED_NONE, nullptr, rl + m0, nullptr, scale, stream, false, nullptr,
-                          g16, ldv)) != CE_OK)
+                          gc, ldv)) != CE_OK)
       return st;
-    // dH[rows] = G W: A = G16 K-major (K = V), B = W read MN-major ([V, H], H contiguous)
-    if ((st = ce::gemm_bf16(g16, ldv, false, Wb, H, true, dH + m0 * H, H, static_cast<int>(rows),
+    ++launches;  // the GEMM (the row kernel counts itself)
+    if (whole_g) continue;
+    // dH[rows] = G W: A = G K-major (K = V), B = W read MN-major ([V, H], H contiguous)
+    if ((st = ce::gemm_bf16(gc, ldv, false, Wb, H, true, dH + m0 * H, H, static_cast<int>(rows),
                             static_cast<int>(H), static_cast<int>(V), 0.f, s, di.err, sms,
                             hint)) != CE_OK)
       return st;
-    // dW (+)= G^T h_c: A = G16 read MN-major ([rows, V], V contiguous), B = h_c read
+    // dW (+)= G^T h_c: A = G read MN-major ([rows, V], V contiguous), B = h_c read
     // MN-major ([rows, H], H contiguous), K = rows
-    if ((st = ce::gemm_bf16(g16, ldv, true, hc, H, true, dW, H, static_cast<int>(V),
+    if ((st = ce::gemm_bf16(gc, ldv, true, hc, H, true, dW, H, static_cast<int>(V),
                             static_cast<int>(H), static_cast<int>(rows), m0 == 0 ? 0.f : 1.f, s,
                             di.err, sms, hint)) != CE_OK)
       return st;
-    launches += 3;  // the row kernel counts itself
+    launches += 2;
+  }
+  if (whole_g) {
+    // dH = G W over every row at once (K = V), dW = G^T h written once (K = M)
+    if ((st = ce::gemm_bf16(g16, ldv, false, Wb, H, true, dH, H, static_cast<int>(M),
+                            static_cast<int>(H), static_cast<int>(V), 0.f, s, di.err, sms,
+                            hint)) != CE_OK)
+      return st;
+    if ((st = ce::gemm_bf16(g16, ldv, true, hb, H, true, dW, H, static_cast<int>(V),
+                            static_cast<int>(H), static_cast<int>(M), 0.f, s, di.err, sms,
+                            hint)) != CE_OK)
+      return st;
+    launches += 2;
   }
   if ((st = ce::launch_mean_rows(rl, M, loss, s)) != CE_OK) return st;
   ++launches;
