@@ -39,9 +39,19 @@
  *    target outside [0, V) does not stop the call: that row's loss is NaN,
  *    its gradient is softmax*scale (no one-hot term), and a device error
  *    word is set; ce_check_errors reports it.  Nothing traps.
- *  - The reducing calls use a small library-owned device buffer (one per
- *    device and stream, created by cudaMalloc on the first reducing call
- *    on that stream).  Make that first call outside CUDA graph capture.
+ *  - The reducing calls (a mean or sum loss) use a small library-owned device
+ *    buffer, one per (device, stream) pair: 256 + 8 * 8192 bytes (about
+ *    64 KB), created by cudaMalloc on the first reducing call on that stream
+ *    and kept until the process exits (the library never frees it).  A caller
+ *    that reduces on many short-lived streams therefore holds 64 KB per
+ *    stream it has used; reduce on a few long-lived streams, or use
+ *    ce_fwd_bwd_inplace_noalloc.  Make the first reducing call on a stream
+ *    outside CUDA graph capture.
+ *  - Per device, the library looks up and keeps device addresses (its error
+ *    word, its static scratch) and launch shapes on first use.  After
+ *    cudaDeviceReset, or any other teardown of the device's primary context,
+ *    those kept addresses are stale: do not call the library again in that
+ *    process after a reset.
  */
 #ifndef CE_GB300_H
 #define CE_GB300_H
@@ -145,9 +155,14 @@ ce_status ce_fwd_bwd_inplace_noalloc(void* logits, const int64_t* targets, int64
 
 /*
  * ce_backward_from_lse -- gradient only, from a stored per-row lse:
- * g = (exp(x - lse_i) - onehot) * scale written over the logits.  Use it
- * when the forward ran earlier (ce_forward with lse != NULL); `scale` is
- * the upstream gradient of each row loss (1/M for a mean).
+ * g = (exp(x - lse_i) - onehot) * scale written over the logits.  This is
+ * the backward half of the fused kernel of "9 Triton kernels in 9 weeks",
+ * week seven (the gradient of the mean loss, softmax minus the one-hot
+ * target over M, written into the logits buffer), run from an lse saved by
+ * the forward of "POPCORNBENCH level-1 problem 95 transcript"'s definition
+ * (log_sum_exp per row).  Use it when the forward ran earlier (ce_forward
+ * with lse != NULL); `scale` is the upstream gradient of each row loss (1/M
+ * for a mean).  Each logit is read once and written once.
  *
  *   logits [M, V] read and overwritten; targets [M] int64; lse [M] fp32.
  */

@@ -17,10 +17,14 @@ needs; the listing keeps it as the running max plus the log of the running
 normaliser).  ``attention_forward`` is this definition, evaluated directly in
 float64 (a row of all -inf scores gives NaN, as the definition does).
 
-``attention_blockwise`` restates the listing's algorithm -- blocks of keys,
-a running row max, a running normaliser rescaled by ``exp(old max - new
-max)``, an output accumulator rescaled by the same factor, one division at the
-end -- only so that tests can show it reaches the definition's values.
+``attention_blockwise`` is the blockwise form of the same definition, kept
+only so that tests can show it reaches the definition's values: every block
+of keys gets its own (max, normaliser, accumulator) triple, and the triples
+are combined by the associative pairwise merge of the online softmax (the
+"This is associative" passage of the "POPCORNBENCH level-1 problem 95
+transcript", extended to the value accumulator, which is rescaled by the same
+factor as the normaliser).  The flash-attention forward of the Triton
+discussion applies that merge one key block after another.
 
 Parity status: pinned by tests/test_attention_oracle.py (closed forms for one
 key and for constant scores, a float64 library cross-check, the blockwise
@@ -65,41 +69,51 @@ def attention_forward(q: np.ndarray, k: np.ndarray, v: np.ndarray, mask=None,
     return {"out": out, "lse": lse}
 
 
+def block_triple(s: np.ndarray, v: np.ndarray):
+    """(max, normaliser, accumulator) of one block of scores s [..., T, nb] and
+    values v [..., nb, D]: m = max_j s_ij, l = sum_j exp(s_ij - m),
+    a = sum_j exp(s_ij - m) v_j (a row with no finite score gives (-inf, 0, 0))."""
+    m = np.max(s, axis=-1)
+    ref = np.where(np.isfinite(m), m, 0.0)
+    e = np.exp(s - ref[..., None])
+    return m, np.sum(e, axis=-1), np.einsum("...ij,...jd->...id", e, v)
+
+
+def merge_triples(x, y):
+    """Combine two partial triples: the larger max is kept and each side's
+    normaliser and accumulator are rescaled by exp(its max - the larger max)."""
+    (m1, l1, a1), (m2, l2, a2) = x, y
+    m = np.maximum(m1, m2)
+    ref = np.where(np.isfinite(m), m, 0.0)
+    f1 = np.exp(m1 - ref)  # exp(-inf) = 0 for a side with no finite score
+    f2 = np.exp(m2 - ref)
+    return m, f1 * l1 + f2 * l2, f1[..., None] * a1 + f2[..., None] * a2
+
+
 def attention_blockwise(q: np.ndarray, k: np.ndarray, v: np.ndarray, mask=None,
                         sm_scale: float | None = None, block: int = 16) -> dict:
-    """The listing's blockwise recurrence over key blocks, in float64 (test aid).
-
-    For each block of `block` keys: the block's scores, the new running max,
-    the correction exp(old max - new max) applied to the running normaliser
-    and to the output accumulator, then the block's exp-scores added to both;
-    the output is divided by the normaliser once at the end.
-    """
+    """The definition evaluated block by block (test aid): one triple per block
+    of `block` keys, merged pairwise (a balanced tree) by merge_triples; the
+    output is the merged accumulator over the merged normaliser and lse the
+    merged max plus the normaliser's log."""
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
     v = np.asarray(v, dtype=np.float64)
-    T, D = q.shape[-2], q.shape[-1]
+    D = q.shape[-1]
     Tk = k.shape[-2]
     if sm_scale is None:
         sm_scale = 1.0 / np.sqrt(D)
-    lead = q.shape[:-2]
-    run_max = np.full(lead + (T,), -np.inf)
-    run_norm = np.zeros(lead + (T,))
-    acc = np.zeros(lead + (T, D))
+    parts = []
     for j0 in range(0, Tk, block):
-        kb = k[..., j0:j0 + block, :]
-        vb = v[..., j0:j0 + block, :]
-        s = np.einsum("...id,...jd->...ij", q, kb) * sm_scale
+        s = np.einsum("...id,...jd->...ij", q, k[..., j0:j0 + block, :]) * sm_scale
         if mask is not None:
             s = s + np.asarray(mask, dtype=np.float64)[:, j0:j0 + block]
-        new_max = np.maximum(run_max, np.max(s, axis=-1))
-        # -inf - -inf would be NaN: a row with no finite score so far keeps 0
-        ref = np.where(np.isfinite(new_max), new_max, 0.0)
-        corr = np.exp(np.where(np.isfinite(run_max), run_max - ref, -np.inf))
-        e = np.exp(s - ref[..., None])
-        run_norm = corr * run_norm + np.sum(e, axis=-1)
-        acc = corr[..., None] * acc + np.einsum("...ij,...jd->...id", e, vb)
-        run_max = new_max
+        parts.append(block_triple(s, v[..., j0:j0 + block, :]))
+    while len(parts) > 1:
+        parts = [merge_triples(parts[i], parts[i + 1]) if i + 1 < len(parts) else parts[i]
+                 for i in range(0, len(parts), 2)]
+    m, l, a = parts[0]
     with np.errstate(invalid="ignore", divide="ignore"):
-        out = acc / run_norm[..., None]
-        lse = np.where(np.isfinite(run_max), run_max, 0.0) + np.log(run_norm)
+        out = a / l[..., None]
+        lse = np.where(np.isfinite(m), m, 0.0) + np.log(l)
     return {"out": out, "lse": lse}

@@ -1,5 +1,5 @@
 """Pins of the float64 attention oracle (CPU): closed forms, a library
-cross-check, the page's blockwise recurrence against the definition, and a
+cross-check, the blockwise (pairwise-merge) form against the definition, and a
 planted mistake the checks must catch."""
 
 import numpy as np
@@ -116,29 +116,20 @@ def test_large_score_offsets_stay_finite():
 
 
 def test_planted_mistake_dropped_rescale_is_caught(monkeypatch):
-    # a recurrence that forgets to rescale the accumulator when the max grows
-    # must disagree with the definition on rows whose max rises across blocks
+    # a merge that forgets to rescale the side with the smaller max must disagree
+    # with the definition on rows whose max differs between key blocks
     B, H, T, D = 1, 1, 24, 8
     q, k, v = rand((B, H, T, D), 13) * 4, rand((B, H, T, D), 14) * 4, rand((B, H, T, D), 15)
-    real_exp = np.exp
 
-    def broken_blockwise(*args, **kw):
-        calls = {"n": 0}
-
-        def exp_without_correction(x):
-            calls["n"] += 1
-            # the correction factor is the first exp of every block
-            return np.ones_like(x) if calls["n"] % 2 == 1 else real_exp(x)
-
-        monkeypatch.setattr(A.np, "exp", exp_without_correction)
-        try:
-            return A.attention_blockwise(*args, **kw)
-        finally:
-            monkeypatch.setattr(A.np, "exp", real_exp)
+    def merge_without_rescale(x, y):
+        (m1, l1, a1), (m2, l2, a2) = x, y
+        return np.maximum(m1, m2), l1 + l2, a1 + a2
 
     good = A.attention_forward(q, k, v)
-    bad = broken_blockwise(q, k, v, block=4)
+    monkeypatch.setattr(A, "merge_triples", merge_without_rescale)
+    bad = A.attention_blockwise(q, k, v, block=4)
     assert not np.allclose(bad["out"], good["out"], rtol=1e-6, atol=1e-6)
+    assert not np.allclose(bad["lse"], good["lse"], rtol=1e-6, atol=1e-6)
 
 
 def mutated_forward(kind):
