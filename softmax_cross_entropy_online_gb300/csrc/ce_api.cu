@@ -16,6 +16,7 @@
 #include <utility>
 
 #include "../../include/ce_gb300.h"
+#include "ce_lce.cuh"
 #include "ce_rows.cuh"
 #include "ce_stream.cuh"
 
@@ -35,8 +36,9 @@ constexpr int kStreamKRes = 16;  // as in ce_launch.cuh
 ce_status gemm_bf16(const void* A, long long lda, bool a_mn, const void* B, long long ldb,
                     bool b_mn, float* D, long long ldd, int M, int N, int K, float beta,
                     cudaStream_t stream, unsigned int* err, int sm_count,
-                    unsigned int wait_hint_ns);
+                    unsigned int wait_hint_ns, const LceArgs* lce = nullptr);
 ce_status launch_mean_rows(const float* rl, long long M, float* loss, cudaStream_t st);
+ce_status launch_lce_grad_rows(const LceArgs& a, cudaStream_t st, int sm_count);
 ce_status attention_forward(const void* Q, const void* K, const void* V, const float* mask,
                             int causal, int BH, int T, int D, float sm_scale, void* O,
                             bool out_bf16, float* lse, cudaStream_t stream, unsigned int* err,
@@ -652,28 +654,49 @@ ce_status launch_rows(int mode, const void* logits, const int64_t* targets, cons
   return CE_OK;
 }
 
-// Workspace of the fused linear + cross-entropy for row chunks of `mc` rows:
-// logits [mc, V] fp32 (one chunk at a time), the bf16 gradient rows G [g_rows,
-// ldv] (ldv = V rounded up to a multiple of 8), row losses [M] fp32.  With
-// g_rows = M ("whole G") every chunk's G rows stay, and dH and dW are each one
-// GEMM over all rows after the last chunk: dW is written once, with no
-// read-modify-write per chunk, and dH's tiles fill the machine.  With g_rows =
-// mc (the fallback for a smaller workspace) each chunk's G is contracted before
-// the next chunk overwrites it, dW accumulating over the chunks.  The GEMMs read
-// W, G and h in their stored layouts (MN-major operands where K is not
-// contiguous), so nothing is transposed.
+// Workspace of the fused linear + cross-entropy for row chunks of `mc` rows.
+//
+// Fused schedule (the default): two fp32 logits buffers [mc, ldl] (ldl = V
+// rounded up to a multiple of 4), two per-tile pair buffers [mc, n_tiles] and
+// two target-logit buffers [mc], the bf16 gradient rows G [M, ldv] of every
+// row (ldv = V rounded up to a multiple of 8) and the row losses [M].  The
+// logits GEMM of chunk k writes buffer k % 2 and its epilogue reduces each row
+// over each tile to a (max, sum) pair; its epilogue warps form chunk k - 1's
+// gradient rows from buffer (k - 1) % 2 meanwhile; a standalone pass forms the
+// last chunk's.  dH and dW are then each one GEMM over all rows.
+//
+// Per-chunk schedule (the fallback for a smaller workspace): one logits chunk,
+// the row kernel turning it into that chunk's G [mc, ldv] and row losses, and
+// dH and dW contracted before the next chunk (dW accumulated over the chunks).
+//
+// The GEMMs read W, G and h in their stored layouts (MN-major operands where K
+// is not contiguous), so nothing is transposed.
 struct LinearWs {
-  size_t logits, g16, rl, total;
+  size_t logits[2], part[2], xt[2], g16, rl, total;
 };
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
-LinearWs linear_ws_layout(long long M, long long V, long long mc, long long g_rows) {
+LinearWs linear_ws_layout(long long M, long long V, long long mc, bool fused) {
   const long long ldv = (V + 7) / 8 * 8;
+  const long long ldl = (V + 3) / 4 * 4;
+  const long long nt = (V + ce::kLceTileCols - 1) / ce::kLceTileCols;
   LinearWs w;
+  std::memset(&w, 0, sizeof(w));
   size_t off = 0;
-  w.logits = off;
-  off += round256(static_cast<size_t>(mc) * V * 4);
+  const int nbuf = fused ? 2 : 1;
+  for (int b = 0; b < nbuf; ++b) {
+    w.logits[b] = off;
+    off += round256(static_cast<size_t>(mc) * (fused ? ldl : V) * 4);
+  }
+  if (fused) {
+    for (int b = 0; b < 2; ++b) {
+      w.part[b] = off;
+      off += round256(static_cast<size_t>(mc) * nt * 8);
+      w.xt[b] = off;
+      off += round256(static_cast<size_t>(mc) * 4);
+    }
+  }
   w.g16 = off;
-  off += round256(static_cast<size_t>(g_rows) * ldv * 2);
+  off += round256(static_cast<size_t>(fused ? M : mc) * ldv * 2);
   w.rl = off;
   off += round256(static_cast<size_t>(M) * 4);
   w.total = off;
@@ -793,7 +816,7 @@ size_t linear_ce_workspace_size(int64_t M, int64_t H, int64_t V) {
   if (M < 0 || H < 1 || V < 1) return 0;
   const long long mc = M < kLinearDefaultChunk ? (M > 0 ? M : 1) : kLinearDefaultChunk;
   (void)H;
-  return linear_ws_layout(M, V, mc, M > 0 ? M : 1).total;
+  return linear_ws_layout(M > 0 ? M : 1, V, mc, true).total;
 }
 
 ce_status linear_ce_fwd_bwd(const void* h, const void* W, const int64_t* targets, int64_t M,
@@ -809,16 +832,16 @@ ce_status linear_ce_fwd_bwd(const void* h, const void* W, const int64_t* targets
     return CE_ERR_INVALID_ARG;
   if (M > INT32_MAX || H > INT32_MAX || V > INT32_MAX) return CE_ERR_UNSUPPORTED;
   // the schedule and row chunk: the largest chunk (a multiple of 128, or all of
-  // M) whose workspace fits with the whole of G, else the largest that fits with
-  // one chunk of G
+  // M) whose workspace fits the fused schedule, else the largest that fits the
+  // per-chunk one
   long long mc = M < kLinearDefaultChunk ? M : kLinearDefaultChunk;
-  bool whole_g = true;
-  while (linear_ws_layout(M, V, mc, M).total > workspace_bytes && mc > 128)
+  bool fused = true;
+  while (linear_ws_layout(M, V, mc, true).total > workspace_bytes && mc > 128)
     mc = (mc / 2 + 127) / 128 * 128;
-  if (linear_ws_layout(M, V, mc, M).total > workspace_bytes) {
-    whole_g = false;
+  if (linear_ws_layout(M, V, mc, true).total > workspace_bytes) {
+    fused = false;
     mc = M < kLinearDefaultChunk ? M : kLinearDefaultChunk;
-    while (linear_ws_layout(M, V, mc, mc).total > workspace_bytes) {
+    while (linear_ws_layout(M, V, mc, false).total > workspace_bytes) {
       if (mc <= 128) return CE_ERR_INVALID_ARG;
       mc = (mc / 2 + 127) / 128 * 128;
     }
@@ -827,50 +850,66 @@ ce_status linear_ce_fwd_bwd(const void* h, const void* W, const int64_t* targets
   int dev = 0;
   ce_status st = device_info(di, &dev);
   if (st != CE_OK) return st;
-  const LinearWs L = linear_ws_layout(M, V, mc, whole_g ? M : mc);
+  const LinearWs L = linear_ws_layout(M, V, mc, fused);
   char* ws = static_cast<char*>(workspace);
-  auto* logits = reinterpret_cast<float*>(ws + L.logits);
   auto* g16 = reinterpret_cast<__nv_bfloat16*>(ws + L.g16);
   auto* rl = reinterpret_cast<float*>(ws + L.rl);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const long long ldv = (V + 7) / 8 * 8;
+  const long long ldl = (V + 3) / 4 * 4;
   const unsigned hint = wait_hint_ns();
   const int sms = di.sm_count;
   const auto* Wb = static_cast<const __nv_bfloat16*>(W);
   const auto* hb = static_cast<const __nv_bfloat16*>(h);
   uint64_t launches = 0;
   const float scale = 1.0f / static_cast<float>(M);
-  for (long long m0 = 0; m0 < M; m0 += mc) {
-    const long long rows = (M - m0) < mc ? (M - m0) : mc;
-    const auto* hc = hb + m0 * H;
-    __nv_bfloat16* const gc = whole_g ? g16 + m0 * ldv : g16;
-    // logits[rows, V] = h_c W^T: both operands K-major (K = H)
-    if ((st = ce::gemm_bf16(hc, H, false, Wb, H, false, logits, V, static_cast<int>(rows),
-                            static_cast<int>(V), static_cast<int>(H), 0.f, s, di.err, sms,
-                            hint)) != CE_OK)
-      return st;
-    // row losses, and G rows [rows, ldv] = bf16 of G = (softmax - onehot) / M
-    // written by the row kernel straight from the fp32 logits
-    if ((st = launch_rows(ce::FWD_BWD, logits, targets + m0, nullptr, rows, V, CE_F32,
-                          CE_RED_NONE, nullptr, rl + m0, nullptr, scale, stream, false, nullptr,
-                          gc, ldv)) != CE_OK)
-      return st;
-    ++launches;  // the GEMM (the row kernel counts itself)
-    if (whole_g) continue;
-    // dH[rows] = G W: A = G K-major (K = V), B = W read MN-major ([V, H], H contiguous)
-    if ((st = ce::gemm_bf16(gc, ldv, false, Wb, H, true, dH + m0 * H, H, static_cast<int>(rows),
-                            static_cast<int>(H), static_cast<int>(V), 0.f, s, di.err, sms,
-                            hint)) != CE_OK)
-      return st;
-    // dW (+)= G^T h_c: A = G read MN-major ([rows, V], V contiguous), B = h_c read
-    // MN-major ([rows, H], H contiguous), K = rows
-    if ((st = ce::gemm_bf16(gc, ldv, true, hc, H, true, dW, H, static_cast<int>(V),
-                            static_cast<int>(H), static_cast<int>(rows), m0 == 0 ? 0.f : 1.f, s,
-                            di.err, sms, hint)) != CE_OK)
-      return st;
-    launches += 2;
-  }
-  if (whole_g) {
+  if (fused) {
+    const int nt = static_cast<int>((V + ce::kLceTileCols - 1) / ce::kLceTileCols);
+    ce::LceArgs prev;  // the chunk whose gradient rows are still to be formed
+    std::memset(&prev, 0, sizeof(prev));
+    int k = 0;
+    for (long long m0 = 0; m0 < M; m0 += mc, ++k) {
+      const long long rows = (M - m0) < mc ? (M - m0) : mc;
+      const int b = k & 1;
+      auto* logits = reinterpret_cast<float*>(ws + L.logits[b]);
+      ce::LceArgs a;
+      std::memset(&a, 0, sizeof(a));
+      a.part = reinterpret_cast<float2*>(ws + L.part[b]);
+      a.xt = reinterpret_cast<float*>(ws + L.xt[b]);
+      a.targets = targets + m0;
+      a.rows = static_cast<int>(rows);
+      a.V = static_cast<int>(V);
+      a.n_tiles = nt;
+      a.ldl = ldl;
+      a.ldv = ldv;
+      a.scale = scale;
+      a.err = di.err;
+      // the previous chunk's gradient rows, formed by this GEMM's epilogue warps
+      a.bg_logits = prev.bg_logits;
+      a.bg_part = prev.bg_part;
+      a.bg_xt = prev.bg_xt;
+      a.bg_targets = prev.bg_targets;
+      a.bg_g16 = prev.bg_g16;
+      a.bg_rl = prev.bg_rl;
+      a.bg_rows = prev.bg_rows;
+      // logits[rows, V] = h_c W^T: both operands K-major (K = H)
+      if ((st = ce::gemm_bf16(hb + m0 * H, H, false, Wb, H, false, logits, ldl,
+                              static_cast<int>(rows), static_cast<int>(V), static_cast<int>(H),
+                              0.f, s, di.err, sms, hint, &a)) != CE_OK)
+        return st;
+      ++launches;
+      prev = a;
+      prev.bg_logits = logits;
+      prev.bg_part = a.part;
+      prev.bg_xt = a.xt;
+      prev.bg_targets = targets + m0;
+      prev.bg_g16 = g16 + m0 * ldv;
+      prev.bg_rl = rl + m0;
+      prev.bg_rows = static_cast<int>(rows);
+    }
+    // the last chunk's gradient rows
+    if ((st = ce::launch_lce_grad_rows(prev, s, sms)) != CE_OK) return st;
+    ++launches;
     // dH = G W over every row at once (K = V), dW = G^T h written once (K = M)
     if ((st = ce::gemm_bf16(g16, ldv, false, Wb, H, true, dH, H, static_cast<int>(M),
                             static_cast<int>(H), static_cast<int>(V), 0.f, s, di.err, sms,
@@ -881,6 +920,35 @@ ce_status linear_ce_fwd_bwd(const void* h, const void* W, const int64_t* targets
                             hint)) != CE_OK)
       return st;
     launches += 2;
+  } else {
+    auto* logits = reinterpret_cast<float*>(ws + L.logits[0]);
+    for (long long m0 = 0; m0 < M; m0 += mc) {
+      const long long rows = (M - m0) < mc ? (M - m0) : mc;
+      const auto* hc = hb + m0 * H;
+      // logits[rows, V] = h_c W^T: both operands K-major (K = H)
+      if ((st = ce::gemm_bf16(hc, H, false, Wb, H, false, logits, V, static_cast<int>(rows),
+                              static_cast<int>(V), static_cast<int>(H), 0.f, s, di.err, sms,
+                              hint)) != CE_OK)
+        return st;
+      // row losses, and G rows [rows, ldv] = bf16 of G = (softmax - onehot) / M
+      // written by the row kernel straight from the fp32 logits
+      if ((st = launch_rows(ce::FWD_BWD, logits, targets + m0, nullptr, rows, V, CE_F32,
+                            CE_RED_NONE, nullptr, rl + m0, nullptr, scale, stream, false, nullptr,
+                            g16, ldv)) != CE_OK)
+        return st;
+      // dH[rows] = G W: A = G K-major (K = V), B = W read MN-major ([V, H], H contiguous)
+      if ((st = ce::gemm_bf16(g16, ldv, false, Wb, H, true, dH + m0 * H, H,
+                              static_cast<int>(rows), static_cast<int>(H), static_cast<int>(V),
+                              0.f, s, di.err, sms, hint)) != CE_OK)
+        return st;
+      // dW (+)= G^T h_c: A = G read MN-major ([rows, V], V contiguous), B = h_c read
+      // MN-major ([rows, H], H contiguous), K = rows
+      if ((st = ce::gemm_bf16(g16, ldv, true, hc, H, true, dW, H, static_cast<int>(V),
+                              static_cast<int>(H), static_cast<int>(rows), m0 == 0 ? 0.f : 1.f,
+                              s, di.err, sms, hint)) != CE_OK)
+        return st;
+      launches += 3;  // the row kernel counts itself
+    }
   }
   if ((st = ce::launch_mean_rows(rl, M, loss, s)) != CE_OK) return st;
   ++launches;

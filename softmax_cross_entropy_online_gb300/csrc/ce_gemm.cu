@@ -30,6 +30,7 @@
 #include <cudaTypedefs.h>
 
 #include "../../include/ce_gb300.h"
+#include "ce_lce.cuh"
 #include "ce_rows.cuh"
 #include "ce_tc.cuh"
 
@@ -59,6 +60,7 @@ struct GemmParams {
   int a_3d, b_3d; // MN-major operand loaded by one 3-D box per stage (M / N % 64 == 0)
   unsigned int* err;
   unsigned int wait_hint_ns;
+  LceArgs lce;    // the fused linear + CE epilogue's work (LCE kernels only)
 };
 
 // instruction descriptor of kind::f16: D fp32, A and B bf16, N=256, M=128; bits
@@ -80,9 +82,179 @@ __device__ __forceinline__ void tile_coords(const GemmParams& p, int tile, int& 
 }
 
 
+// ---------------------------------------------------------------------------
+// The fused linear + CE's gradient rows, formed by one warp per row from the
+// stored fp32 logits and the row's per-tile (max, sum) pairs (ce_lce.cuh).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n"
+      " mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Merge of two (max, sum of exp(x - max)) pairs: the larger max is kept and
+// the other sum rescaled by exp(its max - the larger max); two empty pairs
+// (-inf, 0) stay empty.
+__device__ __forceinline__ void merge_pair(float& m, float& s, float m2, float s2) {
+  const float mn = fmaxf(m, m2);
+  const float f1 = (m == -INFINITY) ? 0.f : ex2((m - mn) * kLog2e);
+  const float f2 = (m2 == -INFINITY) ? 0.f : ex2((m2 - mn) * kLog2e);
+  s = s * f1 + s2 * f2;
+  m = mn;
+}
+
+// One warp's share of the gradient rows: a contiguous range of the chunk's
+// 4-logit chunks (row-major over the rows), so every warp gets the same amount
+// of work whatever the row count.  The warp walks it row by row: r the current
+// row (done once r >= bg_rows), pos the next chunk in it (-1 until the row's
+// pairs are merged), end_r / end_pos where the range stops, and the row's
+// constants.
+struct BgRow {
+  int r, pos;           // the current row, and its next chunk (-1: pairs not merged yet)
+  int start;            // where the warp's work in the next row to merge begins
+  int end_r, end_pos;   // the range ends before chunk end_pos of row end_r
+  long long t;          // the row's target
+  float Lh, scf, gt;    // lse log2e = Lh + (correction in scf); scf = 2^-correction * scale; g_t
+};
+
+// Warp `gw` of `nwarps`: its range [gw * total / nwarps, (gw + 1) * total / nwarps)
+// of the rows * ceil(V / 4) chunks.
+__device__ __forceinline__ void bg_range(const LceArgs& a, BgRow& w, int gw, int nwarps) {
+  const long long nch = (a.V + 3) >> 2;
+  const long long total = static_cast<long long>(a.bg_rows) * nch;
+  const long long g0 = total * gw / nwarps, g1 = total * (gw + 1) / nwarps;
+  w.r = static_cast<int>(g0 / nch);
+  w.start = static_cast<int>(g0 % nch);
+  w.pos = -1;
+  w.end_r = static_cast<int>(g1 / nch);
+  w.end_pos = static_cast<int>(g1 % nch);
+  if (g0 >= g1) w.r = w.end_r = a.bg_rows;  // an empty range
+  w.t = -1;
+  w.Lh = w.scf = w.gt = 0.f;
+}
+
+__device__ __forceinline__ bool bg_active(const LceArgs& a, const BgRow& w) {
+  return w.r < w.end_r ||
+         (w.r == w.end_r && w.r < a.bg_rows && w.end_pos > 0 && (w.pos < 0 || w.pos < w.end_pos));
+}
+
+// Merge row w.r's tile pairs into its log-sum-exp, write its row loss (the warp
+// whose range holds the row's first chunk), and prepare the constants of its
+// gradient; `start` is the chunk the warp's work in this row begins at.
+__device__ __forceinline__ void bg_merge(const LceArgs& a, BgRow& w, int lane, int start) {
+  const float2* pp = a.bg_part + static_cast<long long>(w.r) * a.n_tiles;
+  float m = -INFINITY, s = 0.f;
+  for (int j = lane; j < a.n_tiles; j += 32) {
+    const float2 q = __ldcg(pp + j);
+    merge_pair(m, s, q.x, q.y);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+    const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+    merge_pair(m, s, m2, s2);
+  }
+  const long long t = __ldg(a.bg_targets + w.r);
+  const bool t_ok = t >= 0 && t < a.V;
+  const float xt = t_ok ? __ldcg(a.bg_xt + w.r) : 0.f;
+  // lse log2e = Lh + Lc, Lc a small correction taken once into the scale
+  const float mref = (m == -INFINITY) ? 0.f : m;
+  const float mhr = mref * kLog2e;
+  const float mlr = fmaf(mref, kLog2e, -mhr);
+  const float l2s = lg2(s);
+  const float Lh = mhr + l2s;
+  const float bv = Lh - mhr;
+  const float Lc = mlr + ((mhr - (Lh - bv)) + (l2s - bv));
+  const float lnS = l2s * kLn2;
+  w.t = t_ok ? t : -1;
+  w.Lh = Lh;
+  w.scf = ex2(-Lc) * a.scale;
+  // exp(x_t - lse) - 1 without cancellation when the target dominates
+  w.gt = expm1_target((xt - m) - lnS) * a.scale;
+  if (lane == 0 && start == 0) {
+    a.bg_rl[w.r] = t_ok ? (m - xt) + lnS : __int_as_float(0x7fc00000);
+    if (!t_ok) atomicOr(a.err, ERR_TARGET_RANGE);
+  }
+  w.pos = start;
+}
+
+// Up to NL x 32 consecutive 4-logit chunks of row w.r from w.pos on (not past
+// the warp's range): g = exp(x - lse) * scale in bf16, the target's element
+// overwritten by the lane that stored its chunk.  Moves w to the next row at
+// the row's end.
+template <int NL>
+__device__ __forceinline__ void bg_chunks(const LceArgs& a, BgRow& w, int lane) {
+  const int nrow = (a.V + 3) >> 2;
+  const int nch = (w.r == w.end_r) ? w.end_pos : nrow;  // this row's last chunk + 1 for the warp
+  const float* row = a.bg_logits + static_cast<long long>(w.r) * a.ldl;
+  __nv_bfloat16* grow = a.bg_g16 + static_cast<long long>(w.r) * a.ldv;
+  float4 x[NL];
+#pragma unroll
+  for (int k = 0; k < NL; ++k) {
+    const int c = w.pos + lane + 32 * k;
+    if (c < nch) x[k] = __ldcs(reinterpret_cast<const float4*>(row) + c);
+  }
+  const int tc = w.t >= 0 ? static_cast<int>(w.t >> 2) : -1;
+#pragma unroll
+  for (int k = 0; k < NL; ++k) {
+    const int c = w.pos + lane + 32 * k;
+    if (c < nch) {
+      float g[4] = {ex2(fmaf(x[k].x, kLog2e, -w.Lh)) * w.scf, ex2(fmaf(x[k].y, kLog2e, -w.Lh)) * w.scf,
+                    ex2(fmaf(x[k].z, kLog2e, -w.Lh)) * w.scf, ex2(fmaf(x[k].w, kLog2e, -w.Lh)) * w.scf};
+      if (4 * c + 4 > a.V) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (4 * c + e >= a.V) g[e] = 0.f;  // columns past V (never read as data)
+      }
+      const __nv_bfloat162 lo = __floats2bfloat162_rn(g[0], g[1]);
+      const __nv_bfloat162 hi = __floats2bfloat162_rn(g[2], g[3]);
+      uint2 u;
+      u.x = *reinterpret_cast<const uint32_t*>(&lo);
+      u.y = *reinterpret_cast<const uint32_t*>(&hi);
+      *reinterpret_cast<uint2*>(grow + 4LL * c) = u;
+      if (c == tc) grow[w.t] = __float2bfloat16_rn(w.gt);
+    }
+  }
+  w.pos += 32 * NL;
+  if (w.pos >= nch) {
+    ++w.r;
+    w.pos = -1;
+  }
+}
+
+// One step of a warp's share: merge the next row's pairs, or form a slice.
+template <int NL>
+__device__ __forceinline__ void bg_step(const LceArgs& a, BgRow& w, int lane) {
+  if (w.pos < 0) {
+    bg_merge(a, w, lane, w.start);
+    w.start = 0;  // every later row of the range starts at its first chunk
+  } else {
+    bg_chunks<NL>(a, w, lane);
+  }
+}
+
+// A standalone pass over one chunk's rows (the last chunk of a call): a warp
+// per row, rows r = warp, warp + nwarps, ...
+__global__ void __launch_bounds__(256) lce_grad_rows_kernel(const LceArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int nwarps = static_cast<int>((gridDim.x * blockDim.x) >> 5);
+  BgRow w;
+  bg_range(a, w, static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5), nwarps);
+  while (bg_active(a, w)) bg_step<16>(a, w, lane);
+}
+
 // A_MN / B_MN: the operands' layouts, fixed at compile time so that the
-// K-major form runs exactly the code it would alone
-template <bool A_MN, bool B_MN>
+// K-major form runs exactly the code it would alone.  LCE (K-major operands
+// only): the fused linear + CE's logits GEMM, whose epilogue also reduces each
+// row over each tile to a (max, sum) pair, keeps the target logit, and forms
+// the previous chunk's gradient rows while it waits for accumulators.
+template <bool A_MN, bool B_MN, bool LCE = false>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap tma_a,
                         const __grid_constant__ CUtensorMap tma_b,
@@ -214,12 +386,36 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint32_t ebuf = sbase + kGemmStages * kStageBytes + q * kEpiBytes;
     int a = 0;
     uint32_t aph = 0;
+    // LCE: this warp's background rows of the previous chunk
+    BgRow bg;
+    const bool bg_on = LCE && p.lce.bg_rows > 0;
+    if (bg_on) bg_range(p.lce, bg, static_cast<int>(blockIdx.x) * 4 + q, static_cast<int>(gridDim.x) * 4);
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
       int tm, tn;
       tile_coords(p, tile, tm, tn);
-      mbar_wait<false>(smem_u32(&accf_bar[a]), aph, p.err, failed, WAIT_LIMIT_NS, hint);
+      if (LCE) {
+        // while the accumulator fills, form background gradient rows (a slice
+        // takes a few microseconds; a tile's MMAs take about 25); once they run
+        // out, wait as usual (bounded)
+        while (!mbar_test_wait(smem_u32(&accf_bar[a]), aph)) {
+          if (bg_on && bg_active(p.lce, bg)) {
+            bg_step<8>(p.lce, bg, lane);
+          } else {
+            mbar_wait<false>(smem_u32(&accf_bar[a]), aph, p.err, failed, WAIT_LIMIT_NS, hint);
+            break;
+          }
+        }
+      } else {
+        mbar_wait<false>(smem_u32(&accf_bar[a]), aph, p.err, failed, WAIT_LIMIT_NS, hint);
+      }
       tc_fence_after();
       const int rbase = tm * kGemmBM + 32 * q;  // this warp's 32 rows of the tile
+      // LCE: this thread's row (TMEM lane) and its running pair over the tile
+      const int my_row = rbase + lane;
+      long long my_t = -1;
+      if (LCE && my_row < p.lce.rows) my_t = __ldg(p.lce.targets + my_row);
+      float sm = -INFINITY, smh = 0.f, ss = 0.f, xtv = 0.f;
+      bool hx = false;
 #pragma unroll 1
       for (int cc = 0; cc < kGemmBN / 32; ++cc) {
         float v[32];
@@ -227,6 +423,37 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                       (static_cast<uint32_t>(32 * q) << 16),
                   v);
         const int col0 = tn * kGemmBN + cc * 32;
+        if (LCE) {
+          // the row's pair over these 32 columns (those past V excluded): the
+          // max first, then one exp2 per value against the running reference
+          const int nv = p.lce.V - col0;
+          if (nv > 0) {
+            float cm = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (nv >= 32 || j < nv) cm = fmaxf(cm, v[j]);
+            if (cm > sm) {
+              const float nh = cm * kLog2e;
+              ss = (sm == -INFINITY) ? 0.f : ss * ex2(smh - nh);
+              sm = cm;
+              smh = nh;
+            }
+            if (sm != -INFINITY) {
+              float a4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (nv >= 32 || j < nv) a4[j & 3] += ex2(fmaf(v[j], kLog2e, -smh));
+              ss += (a4[0] + a4[1]) + (a4[2] + a4[3]);
+            }
+            if (my_t >= col0 && my_t < col0 + 32) {
+              const int o = static_cast<int>(my_t - col0);
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (j == o) xtv = v[j];
+              hx = true;
+            }
+          }
+        }
         if (p.use_tma) {
           // the previous block's store has read the buffer
           if (lane == 0) bulk_wait_read<0>();
@@ -278,8 +505,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       tc_fence_before();
       mbar_arrive(smem_u32(&acce_bar[a]));
+      if (LCE && my_row < p.lce.rows) {
+        // the pair in natural units: ss counts 2^(x log2e - smh), smh rounded
+        const float ml = (sm == -INFINITY) ? 0.f : fmaf(sm, kLog2e, -smh);
+        p.lce.part[static_cast<long long>(my_row) * p.lce.n_tiles + tn] =
+            make_float2(sm, (sm == -INFINITY) ? 0.f : ss * ex2(-ml));
+        if (hx) p.lce.xt[my_row] = xtv;
+      }
       a ^= 1;
       if (a == 0) aph ^= 1u;
+    }
+    // the rest of this warp's background rows
+    if (bg_on) {
+      while (bg_active(p.lce, bg)) bg_step<8>(p.lce, bg, lane);
     }
     // no CTA exits while a TMA store still reads its shared memory
     if (p.use_tma && lane == 0) bulk_wait_all();
@@ -362,11 +600,14 @@ static bool make_map_f32(CUtensorMap* map, void* base, long long rows, long long
 // (the transpose of a K-major A).  The same for B with N.  Requires lda, ldb
 // multiples of 8 (16-byte row strides for TMA) and 16-byte aligned A and B;
 // tiles reaching past M, N or K are zero-filled by TMA.
+// lce (both operands K-major, beta = 0, D rows on the 16-byte grid): the fused
+// linear + CE's logits GEMM, with the epilogue work of ce_lce.cuh.
 ce_status gemm_bf16(const void* A, long long lda, bool a_mn, const void* B, long long ldb,
                     bool b_mn, float* D, long long ldd, int M, int N, int K, float beta,
                     cudaStream_t stream, unsigned int* err, int sm_count,
-                    unsigned int wait_hint_ns) {
+                    unsigned int wait_hint_ns, const LceArgs* lce) {
   if (M <= 0 || N <= 0 || K <= 0) return CE_OK;
+  if (lce != nullptr && (a_mn || b_mn || beta != 0.f)) return CE_ERR_UNSUPPORTED;
   if ((lda % 8) || (ldb % 8) || ldd < N) return CE_ERR_UNSUPPORTED;
   if ((a_mn ? lda < M : lda < K) || (b_mn ? ldb < N : ldb < K)) return CE_ERR_UNSUPPORTED;
   if ((reinterpret_cast<uintptr_t>(A) & 15) || (reinterpret_cast<uintptr_t>(B) & 15))
@@ -401,8 +642,15 @@ ce_status gemm_bf16(const void* A, long long lda, bool a_mn, const void* B, long
   p.b_3d = b_3d ? 1 : 0;
   p.err = err;
   p.wait_hint_ns = wait_hint_ns;
-  auto kern = a_mn ? (b_mn ? gemm_bf16_kernel<true, true> : gemm_bf16_kernel<true, false>)
-                   : (b_mn ? gemm_bf16_kernel<false, true> : gemm_bf16_kernel<false, false>);
+  std::memset(&p.lce, 0, sizeof(p.lce));
+  if (lce != nullptr) {
+    if (!use_tma || lce->n_tiles != p.tiles_n || lce->rows != M || lce->V != N)
+      return CE_ERR_UNSUPPORTED;
+    p.lce = *lce;
+  }
+  auto kern = lce != nullptr ? gemm_bf16_kernel<false, false, true>
+              : a_mn ? (b_mn ? gemm_bf16_kernel<true, true> : gemm_bf16_kernel<true, false>)
+                     : (b_mn ? gemm_bf16_kernel<false, true> : gemm_bf16_kernel<false, false>);
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem) !=
       cudaSuccess)
     return CE_ERR_CUDA;
@@ -435,6 +683,16 @@ __global__ void mean_rows_kernel(const float* __restrict__ rl, long long M, floa
 
 ce_status launch_mean_rows(const float* rl, long long M, float* loss, cudaStream_t st) {
   mean_rows_kernel<<<1, 1024, 0, st>>>(rl, M, loss);
+  return cudaGetLastError() == cudaSuccess ? CE_OK : CE_ERR_CUDA;
+}
+
+// The gradient rows of a.bg_rows rows (the last chunk of a fused linear + CE
+// call), a warp per row, 8 warps a CTA.
+ce_status launch_lce_grad_rows(const LceArgs& a, cudaStream_t st, int sm_count) {
+  if (a.bg_rows <= 0) return CE_OK;
+  int grid = (a.bg_rows + 7) / 8;
+  if (grid > sm_count * 8) grid = sm_count * 8;
+  lce_grad_rows_kernel<<<grid, 256, 0, st>>>(a);
   return cudaGetLastError() == cudaSuccess ? CE_OK : CE_ERR_CUDA;
 }
 

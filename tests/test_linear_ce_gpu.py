@@ -124,6 +124,14 @@ def test_linear_ce_against_oracle(api, M, H, V):
     check_linear(api, M, H, V, seed=M + H + V)
 
 
+@pytest.mark.parametrize("M,H,V", [(5000, 256, 3001), (4224, 64, 1027), (2049, 128, 256)])
+def test_linear_ce_fused_chunks_against_oracle(api, M, H, V):
+    # several 2048-row chunks with the default (fused) workspace: each chunk's
+    # gradient rows are formed by the next chunk's GEMM epilogue, the last
+    # chunk's by the standalone pass; V off the 4- and 256-column grids
+    check_linear(api, M, H, V, seed=M + V)
+
+
 def test_linear_ce_in_row_chunks(api):
     # a workspace too small for one chunk: rows go through in chunks of 128
     M, H, V = 700, 128, 1500
