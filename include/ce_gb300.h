@@ -180,24 +180,30 @@ ce_status ce_backward_from_lse(void* logits, const int64_t* targets, const float
  *     dH   = G W          [M, H]      G = (softmax(logits) - onehot) / M
  *     dW   = G^T h        [V, H]
  *
- * Rows are processed in chunks: each chunk's fp32 logits are produced by a
- * tcgen05 GEMM into the workspace (one chunk at a time: the [M, V] logits
- * never exist at once) and turned by the row kernel into the bf16 gradient
- * rows G and the row losses.  With a workspace that holds G for every row
- * (the size linear_ce_workspace_size returns), dH and dW are then each one
- * tcgen05 GEMM over all rows, dW written once.  With a smaller workspace,
- * each chunk's G is contracted into dH and dW before the next chunk (dW
- * accumulated over the chunks).  The GEMMs read W, G and h in their stored
- * layouts, with fp32 accumulation.
+ * Rows are processed in chunks of 2048.  Each chunk's fp32 logits are
+ * produced by a tcgen05 GEMM into the workspace (two chunk buffers, used in
+ * turn: the [M, V] logits never exist at once).  Its epilogue also reduces
+ * each row over each 256-column tile to a (max, sum of exp) pair.  While the
+ * next chunk's GEMM runs, its epilogue warps merge the previous chunk's pairs
+ * into each row's log-sum-exp and form that chunk's bf16 gradient rows G and
+ * row losses.  A short pass does the last chunk's.  dH and dW are then each
+ * one tcgen05 GEMM over all rows, dW written once.  With a workspace too
+ * small for that (fused) schedule, a smaller chunk and then a per-chunk
+ * schedule are used: the row kernel turns each chunk's logits into its G,
+ * which is contracted into dH and dW before the next chunk (dW accumulated
+ * over the chunks).  The GEMMs read W, G and h in their stored layouts, with
+ * fp32 accumulation.
  *
  *   h        [M, H] bf16, row-major; W [V, H] bf16, row-major (device).
  *            H must be a multiple of 8; h and W 16-byte aligned.
  *   targets  [M] int64.   loss [1] fp32.   dH [M, H] fp32.   dW [V, H] fp32.
  *   workspace  device memory (256-byte aligned, owned by the caller) of
  *            workspace_bytes: at least linear_ce_workspace_size(M, H, V) for
- *            the whole-G schedule; less selects a smaller row chunk and then
+ *            the fused schedule; less selects a smaller row chunk and then
  *            the per-chunk schedule, down to 128-row chunks (about
  *            128 * V * 6 + 4 * M bytes), else CE_ERR_INVALID_ARG.
+ *   A target outside [0, V) gives that row a NaN loss (so the mean is NaN),
+ *   drops its one-hot term and sets the device error word (ce_check_errors).
  *   G is rounded to bf16 before the two gradient GEMMs; logits, the loss
  *   and every accumulation are fp32.
  */
@@ -205,9 +211,11 @@ ce_status linear_ce_fwd_bwd(const void* h, const void* W, const int64_t* targets
                             int64_t H, int64_t V, float* loss, float* dH, float* dW,
                             void* workspace, size_t workspace_bytes, void* stream);
 
-/* Workspace bytes of linear_ce_fwd_bwd's whole-G schedule at its default row
- * chunk of 2048 (or M) rows: one fp32 logits chunk, bf16 G [M, V rounded up to
- * a multiple of 8] and the fp32 row losses (0 on bad sizes). */
+/* Workspace bytes of linear_ce_fwd_bwd's fused schedule at its default row
+ * chunk of 2048 (or M) rows: two fp32 logits chunks [2048, V rounded up to a
+ * multiple of 4], their per-tile pairs and target logits, bf16 G [M, V
+ * rounded up to a multiple of 8] and the fp32 row losses; about 4.2 GB for
+ * M = 8192, V = 128256 (0 on bad sizes). */
 size_t linear_ce_workspace_size(int64_t M, int64_t H, int64_t V);
 
 /*
