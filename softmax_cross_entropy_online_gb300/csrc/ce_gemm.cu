@@ -399,7 +399,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // out, wait as usual (bounded)
         while (!mbar_test_wait(smem_u32(&accf_bar[a]), aph)) {
           if (bg_on && bg_active(p.lce, bg)) {
-            bg_step<8>(p.lce, bg, lane);
+            bg_step<16>(p.lce, bg, lane);
           } else {
             mbar_wait<false>(smem_u32(&accf_bar[a]), aph, p.err, failed, WAIT_LIMIT_NS, hint);
             break;
@@ -517,7 +517,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     // the rest of this warp's background rows
     if (bg_on) {
-      while (bg_active(p.lce, bg)) bg_step<8>(p.lce, bg, lane);
+      while (bg_active(p.lce, bg)) bg_step<16>(p.lce, bg, lane);
     }
     // no CTA exits while a TMA store still reads its shared memory
     if (p.use_tma && lane == 0) bulk_wait_all();
