@@ -132,6 +132,36 @@ def test_linear_ce_fused_chunks_against_oracle(api, M, H, V):
     check_linear(api, M, H, V, seed=M + V)
 
 
+@pytest.mark.parametrize("small_workspace", [False, True])
+def test_linear_ce_out_of_range_targets(api, small_workspace):
+    # targets outside [0, V) in the first and the last row chunk (the last one's
+    # gradient rows come from the standalone pass): those rows' losses are NaN, so
+    # the mean is NaN, their gradient rows drop the one-hot term, and the device
+    # error word is set; every other row is unaffected
+    M, H, V = 4500, 64, 1003
+    h, W, t = synthetic.make_linear_ce_inputs(M, H, V, seed=17)
+    t[7] = V
+    t[4400] = -2
+    ws = None
+    if small_workspace:
+        ws = torch.empty(api.linear_ce_workspace_size(128, H, V) + 4 * M + 4096,
+                         dtype=torch.uint8, device="cuda")
+    assert api.ce_check_errors() == 0
+    loss, dH, dW = api.linear_ce_fwd_bwd(bf16_dev(h), bf16_dev(W), torch.from_numpy(t).cuda(),
+                                         workspace=ws)
+    torch.cuda.synchronize()
+    assert api.ce_check_errors() == api.CE_ERR_TARGET_RANGE
+    assert api.ce_check_errors() == 0
+    h64, W64 = oracle.decode_bf16(h), oracle.decode_bf16(W)
+    ref = oracle.linear_ce(h64, W64, t, "mean")
+    assert np.isnan(ref["loss"]) and np.isnan(loss.item())
+    G = np.abs(ref["grad"])
+    eH = np.abs(dH.cpu().numpy().astype(np.float64) - ref["dH"])
+    assert np.all(eH <= 2.0**-8 * (G @ np.abs(W64)) + 1e-30)
+    eW = np.abs(dW.cpu().numpy().astype(np.float64) - ref["dW"])
+    assert np.all(eW <= 2.0**-8 * (G.T @ np.abs(h64)) + 1e-30)
+
+
 def test_linear_ce_in_row_chunks(api):
     # a workspace too small for one chunk: rows go through in chunks of 128
     M, H, V = 700, 128, 1500
