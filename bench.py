@@ -693,7 +693,9 @@ def run_native(args, w):
             side[name] = sub_record(L, api, synthetic.WORKLOADS[name], dev, sh, flush, peak,
                                     bwd, nb)
         if not args.no_linear_side:
-            side["linear_ce_8192x4096x128256"] = linear_side_record(L, api, dev, sh)
+            side["linear_ce_8192x4096x128256"] = linear_side_record(L, api, dev, sh, "lean")
+            side["linear_ce_8192x4096x128256_fused"] = linear_side_record(L, api, dev, sh,
+                                                                          "fused")
 
     if rank == 0:
         line = {
@@ -764,18 +766,31 @@ def measured_tflops(burst: bool = False):
     return (1900.0, "fallback (burst)") if burst else (1700.0, "fallback (sustained)")
 
 
-def linear_side_record(L, api, dev, sh, steps: int = 5, warmup: int = 3) -> dict:
+def linear_workspace_bytes(L, schedule: str, M: int, H: int, V: int) -> int:
+    """The workspace that selects a schedule of linear_ce_fwd_bwd: "lean" (the
+    default: no logits stored) or "fused" (fp32 logits chunks, G kept whole)."""
+    fn = L.linear_ce_workspace_size if schedule == "lean" else L.linear_ce_workspace_size_fused
+    return int(fn(M, H, V))
+
+
+# the schedules' executed GEMM work per step in units of 2 M V H: the lean one
+# computes the logits twice (statistics, then G), the fused one once
+LINEAR_GEMMS = {"lean": 4, "fused": 3}
+
+
+def linear_side_record(L, api, dev, sh, schedule: str, steps: int = 5, warmup: int = 3) -> dict:
     """The fused linear + cross-entropy step on its full workload (bf16 h
-    [8192, 4096], W [128256, 4096]), timed beside the headline line: ms per
-    step and TFLOP/s of the three GEMMs (6 M H V), against the sustained bf16
-    peak."""
+    [8192, 4096], W [128256, 4096]) in one schedule, timed beside the headline
+    line: ms per step and TFLOP/s of the three GEMMs the loss and its gradients
+    need (6 M H V; the lean schedule also recomputes the logits, its executed
+    rate is given beside), against the sustained bf16 peak."""
     import torch
     M, H, V = LINEAR_SHAPES["linear_ce_8192x4096x128256"]
     h_np, W_np, t_np = synthetic.make_linear_ce_inputs(M, H, V, seed=0)
     as_bf16 = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)  # noqa: E731
     h, W, t = as_bf16(h_np).to(dev), as_bf16(W_np).to(dev), torch.from_numpy(t_np).to(dev)
     del h_np, W_np
-    wsb = int(L.linear_ce_workspace_size(M, H, V))
+    wsb = linear_workspace_bytes(L, schedule, M, H, V)
     work = torch.empty(wsb, dtype=torch.uint8, device=dev)
     loss = torch.empty((), dtype=torch.float32, device=dev)
     dH = torch.empty((M, H), dtype=torch.float32, device=dev)
@@ -802,11 +817,15 @@ def linear_side_record(L, api, dev, sh, steps: int = 5, warmup: int = 3) -> dict
     flops = 6.0 * M * V * H
     peak, kind = measured_tflops()
     tf = flops / (ms * 1e-3) / 1e12
+    executed = LINEAR_GEMMS[schedule] * 2.0 * M * V * H / (ms * 1e-3) / 1e12
     out = {"workload": f"linear_ce_8192x4096x128256: bf16 h [{M}, {H}] N(0,1), W [{V}, {H}] "
                        "N(0, 0.02^2), int64 targets; loss, dH, dW (fp32)",
-           "call": "linear_ce_fwd_bwd", "ms_per_step": ms, "tflop_s": tf,
+           "call": "linear_ce_fwd_bwd", "schedule": schedule,
+           "logits_stored": schedule == "fused", "ms_per_step": ms, "tflop_s": tf,
+           "executed_tflop_s": executed,
            "roofline": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s",
-                        "frac": tf / peak, "peak_source": kind},
+                        "frac": tf / peak, "peak_source": kind,
+                        "executed_frac": executed / peak},
            "loss": loss.item(), "steps": steps, "workspace_bytes": wsb}
     del h, W, t, work, dH, dW
     torch.cuda.empty_cache()
@@ -835,7 +854,7 @@ def run_linear(args):
     h_host, W_host = as_bf16(h_np).pin_memory(), as_bf16(W_np).pin_memory()
     t_host = torch.from_numpy(t_np).pin_memory()
     h, W, t = h_host.to(dev), W_host.to(dev), t_host.to(dev)
-    wsb = int(L.linear_ce_workspace_size(M, H, V))
+    wsb = linear_workspace_bytes(L, args.schedule, M, H, V)
     work = torch.empty(wsb, dtype=torch.uint8, device=dev)
     loss = torch.empty((), dtype=torch.float32, device=dev)
     dH = torch.empty((M, H), dtype=torch.float32, device=dev)
@@ -868,8 +887,9 @@ def run_linear(args):
     launches = api.ce_launch_count() - n0
     clocks = sampler.stop() if sampler else None
     ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dev)
-    flops = 6.0 * M * V * H  # logits, dH and dW GEMMs
+    flops = 6.0 * M * V * H  # the logits, dH and dW GEMMs the step needs
     value = ws * flops / (ms * 1e-3) / 1e12
+    executed = ws * LINEAR_GEMMS[args.schedule] * 2.0 * M * V * H / (ms * 1e-3) / 1e12
     assert api.ce_check_errors() == 0
     # the dominant kernel (the logits GEMM of one row chunk), timed live
     mc = min(M, 2048)
@@ -908,7 +928,9 @@ def run_linear(args):
             "dtype": "bf16", "data": "synthetic",
             "config": {"workload": f"{args.workload}: bf16 h [{M}, {H}] N(0,1), W [{V}, {H}] "
                                    "N(0, 0.02^2), int64 targets; loss, dH, dW (fp32)",
-                       "M": M, "H": H, "V": V, "workspace_bytes": wsb, "row_chunk": mc},
+                       "M": M, "H": H, "V": V, "workspace_bytes": wsb,
+                       "schedule": args.schedule, "logits_stored": args.schedule == "fused"},
+            "executed_tflop_s": executed,
             "roofline": {"bound": "tensor", "achieved": gemm_tf, "peak": peak,
                          "unit": "TFLOP/s", "frac": gemm_tf / peak, "peak_source": peak_kind,
                          "traffic": None, "kernel": f"logits GEMM [{mc}, {V}, {H}]",
@@ -1247,6 +1269,9 @@ def main():
                     help="override the workload's row count (smaller cases for profiling)")
     ap.add_argument("--vocab", type=int, default=None,
                     help="linear + CE workload: override V (smaller cases for profiling)")
+    ap.add_argument("--schedule", choices=["lean", "fused"], default="lean",
+                    help="linear + CE workload: the lean schedule (no logits stored, the "
+                         "default) or the fused one (fp32 logits chunks)")
     ap.add_argument("--heads", type=int, default=None,
                     help="attention workloads: run B = 1 with this many heads instead")
     args = ap.parse_args()

@@ -172,36 +172,41 @@ ce_status ce_backward_from_lse(void* logits, const int64_t* targets, const float
 
 /*
  * linear_ce_fwd_bwd -- fused linear + cross-entropy ("9 Triton kernels in 9
- * weeks", week eight: the lm_head projection chunked into the loss so the
- * full logits matrix never exists).  For hidden states h [M, H] and the
- * lm_head weight W [V, H], with logits = h W^T:
+ * weeks", week eight: the lm_head projection chunked into the loss to cut its
+ * activation memory).  For hidden states h [M, H] and the lm_head weight
+ * W [V, H], with logits = h W^T:
  *
  *     loss = mean_i CE(logits_i, t_i)
  *     dH   = G W          [M, H]      G = (softmax(logits) - onehot) / M
  *     dW   = G^T h        [V, H]
  *
- * Rows are processed in chunks of 2048.  Each chunk's fp32 logits are
- * produced by a tcgen05 GEMM into the workspace (two chunk buffers, used in
- * turn: the [M, V] logits never exist at once).  Its epilogue also reduces
- * each row over each 256-column tile to a (max, sum of exp) pair.  While the
- * next chunk's GEMM runs, its epilogue warps merge the previous chunk's pairs
- * into each row's log-sum-exp and form that chunk's bf16 gradient rows G and
- * row losses.  A short pass does the last chunk's.  dH and dW are then each
- * one tcgen05 GEMM over all rows, dW written once.  With a workspace too
- * small for that (fused) schedule, a smaller chunk and then a per-chunk
- * schedule are used: the row kernel turns each chunk's logits into its G,
- * which is contracted into dH and dW before the next chunk (dW accumulated
- * over the chunks).  The GEMMs read W, G and h in their stored layouts, with
- * fp32 accumulation.
+ * Rows are processed in chunks; the schedule follows the workspace.
+ *  * Lean schedule (linear_ce_workspace_size bytes, the default): the logits
+ *    are never stored.  Per chunk, a tcgen05 logits GEMM reduces each row
+ *    over each 256-column tile of its accumulator to a (max, sum of exp) pair
+ *    and keeps the target logit; a pass merges each row's pairs into its
+ *    log-sum-exp and loss; a second logits GEMM recomputes the tiles and its
+ *    epilogue writes the chunk's bf16 G straight from the accumulator; then
+ *    dH rows = G W and dW (+)= G^T h.  Four GEMMs' work, about 0.66 GB of
+ *    workspace for M = 8192, V = 128256 (the unfused fp32 logits and their
+ *    gradient would take 8.4 GB).
+ *  * Fused schedule (linear_ce_workspace_size_fused bytes or more): each
+ *    2048-row chunk's fp32 logits go to one of two chunk buffers (the [M, V]
+ *    logits never exist at once) while the epilogue forms the same pairs; the
+ *    next chunk's GEMM epilogue warps turn them into the previous chunk's bf16
+ *    G rows and row losses from the stored logits; G is kept whole and dH and
+ *    dW are each one GEMM over all rows.  Three GEMMs' work, about 4.2 GB.
+ *    A workspace between the two takes the fused schedule with a smaller
+ *    chunk while it fits (down to 128 rows), else the lean one.
+ * The GEMMs read W, G and h in their stored layouts, with fp32 accumulation.
  *
  *   h        [M, H] bf16, row-major; W [V, H] bf16, row-major (device).
  *            H must be a multiple of 8; h and W 16-byte aligned.
  *   targets  [M] int64.   loss [1] fp32.   dH [M, H] fp32.   dW [V, H] fp32.
  *   workspace  device memory (256-byte aligned, owned by the caller) of
- *            workspace_bytes: at least linear_ce_workspace_size(M, H, V) for
- *            the fused schedule; less selects a smaller row chunk and then
- *            the per-chunk schedule, down to 128-row chunks (about
- *            128 * V * 6 + 4 * M bytes), else CE_ERR_INVALID_ARG.
+ *            workspace_bytes: at least the lean schedule's need for 128-row
+ *            chunks (about 128 * (2 V + 8 V / 256 + 20) + 4 M bytes), else
+ *            CE_ERR_INVALID_ARG.
  *   A target outside [0, V) gives that row a NaN loss (so the mean is NaN),
  *   drops its one-hot term and sets the device error word (ce_check_errors).
  *   G is rounded to bf16 before the two gradient GEMMs; logits, the loss
@@ -211,12 +216,19 @@ ce_status linear_ce_fwd_bwd(const void* h, const void* W, const int64_t* targets
                             int64_t H, int64_t V, float* loss, float* dH, float* dW,
                             void* workspace, size_t workspace_bytes, void* stream);
 
-/* Workspace bytes of linear_ce_fwd_bwd's fused schedule at its default row
- * chunk of 2048 (or M) rows: two fp32 logits chunks [2048, V rounded up to a
- * multiple of 4], their per-tile pairs and target logits, bf16 G [M, V
- * rounded up to a multiple of 8] and the fp32 row losses; about 4.2 GB for
- * M = 8192, V = 128256 (0 on bad sizes). */
+/* Workspace bytes of linear_ce_fwd_bwd's lean schedule at its largest row
+ * chunk (2560, or M, rows): the chunk's bf16 G [rows, V rounded up to a
+ * multiple of 8], its per-tile pairs, target logits and row constants, and the
+ * fp32 row losses [M]; about 0.66 GB for M = 8192, V = 128256 (0 on bad
+ * sizes). */
 size_t linear_ce_workspace_size(int64_t M, int64_t H, int64_t V);
+
+/* Workspace bytes of linear_ce_fwd_bwd's fused schedule at its row chunk of
+ * 2048 (or M) rows: two fp32 logits chunks [2048, V rounded up to a multiple
+ * of 4], their per-tile pairs and target logits, bf16 G [M, V rounded up to a
+ * multiple of 8] and the fp32 row losses; about 4.2 GB for M = 8192,
+ * V = 128256 (0 on bad sizes). */
+size_t linear_ce_workspace_size_fused(int64_t M, int64_t H, int64_t V);
 
 /*
  * ce_gemm_bf16 -- the tensor-core contraction under linear_ce_fwd_bwd, exposed

@@ -38,6 +38,7 @@ SIGNATURES = {
     "linear_ce_fwd_bwd": (_i32, [_vp, _vp, _vp, _i64, _i64, _i64, _vp, _vp, _vp, _vp,
                                  ctypes.c_size_t, _vp]),
     "linear_ce_workspace_size": (ctypes.c_size_t, [_i64, _i64, _i64]),
+    "linear_ce_workspace_size_fused": (ctypes.c_size_t, [_i64, _i64, _i64]),
     "ce_gemm_bf16_tn": (_i32, [_vp, _i64, _vp, _i64, _vp, _i64, _i64, _i64, _i64, _f32, _vp]),
     "ce_gemm_bf16": (_i32, [_vp, _i64, _i32, _vp, _i64, _i32, _vp, _i64, _i64, _i64, _i64, _f32,
                             _vp]),
@@ -197,10 +198,15 @@ def ce_backward_from_lse(logits: torch.Tensor, targets: torch.Tensor, lse: torch
 
 
 def linear_ce_fwd_bwd(h: torch.Tensor, W: torch.Tensor, targets: torch.Tensor, *,
-                      workspace: torch.Tensor | None = None, stream=None):
+                      workspace: torch.Tensor | None = None, schedule: str = "lean",
+                      stream=None):
     """Fused linear + cross-entropy: returns (loss, dH, dW) for bf16 h [M, H] and
     W [V, H]; the mean loss's gradients are fp32.  The workspace (uint8 CUDA
-    tensor) defaults to linear_ce_workspace_size(M, H, V) bytes."""
+    tensor, whose size picks the schedule) defaults to
+    linear_ce_workspace_size(M, H, V) bytes for schedule "lean" (no logits
+    stored) and linear_ce_workspace_size_fused(M, H, V) for "fused"."""
+    if schedule not in ("lean", "fused"):
+        raise ValueError("schedule must be 'lean' or 'fused'")
     if (h.dtype != torch.bfloat16 or W.dtype != torch.bfloat16 or not h.is_cuda or not W.is_cuda
             or W.device != h.device):
         raise ValueError("h and W must be bf16 CUDA tensors on one device")
@@ -215,8 +221,9 @@ def linear_ce_fwd_bwd(h: torch.Tensor, W: torch.Tensor, targets: torch.Tensor, *
         raise ValueError("targets must be a contiguous int64 CUDA tensor [M] on h's device")
     dev = h.device
     if workspace is None:
-        workspace = torch.empty(int(lib().linear_ce_workspace_size(M, H, V)), dtype=torch.uint8,
-                                device=dev)
+        size = (lib().linear_ce_workspace_size(M, H, V) if schedule == "lean"
+                else lib().linear_ce_workspace_size_fused(M, H, V))
+        workspace = torch.empty(int(size), dtype=torch.uint8, device=dev)
     else:
         # its size in bytes is its element count: uint8 only
         _check_buffer(workspace, "workspace", dev, torch.uint8, numel=workspace.numel())
@@ -233,6 +240,10 @@ def linear_ce_fwd_bwd(h: torch.Tensor, W: torch.Tensor, targets: torch.Tensor, *
 
 def linear_ce_workspace_size(M: int, H: int, V: int) -> int:
     return int(lib().linear_ce_workspace_size(M, H, V))
+
+
+def linear_ce_workspace_size_fused(M: int, H: int, V: int) -> int:
+    return int(lib().linear_ce_workspace_size_fused(M, H, V))
 
 
 def _check_operands(A, B):

@@ -39,6 +39,7 @@ ce_status gemm_bf16(const void* A, long long lda, bool a_mn, const void* B, long
                     unsigned int wait_hint_ns, const LceArgs* lce = nullptr);
 ce_status launch_mean_rows(const float* rl, long long M, float* loss, cudaStream_t st);
 ce_status launch_lce_grad_rows(const LceArgs& a, cudaStream_t st, int sm_count);
+ce_status launch_lce_merge_rows(const LceArgs& a, cudaStream_t st, int sm_count);
 ce_status attention_forward(const void* Q, const void* K, const void* V, const float* mask,
                             int causal, int BH, int T, int D, float sm_scale, void* O,
                             bool out_bf16, float* lse, cudaStream_t stream, unsigned int* err,
@@ -656,23 +657,28 @@ ce_status launch_rows(int mode, const void* logits, const int64_t* targets, cons
 
 // Workspace of the fused linear + cross-entropy for row chunks of `mc` rows.
 //
-// Fused schedule (the default): two fp32 logits buffers [mc, ldl] (ldl = V
-// rounded up to a multiple of 4), two per-tile pair buffers [mc, n_tiles] and
-// two target-logit buffers [mc], the bf16 gradient rows G [M, ldv] of every
-// row (ldv = V rounded up to a multiple of 8) and the row losses [M].  The
-// logits GEMM of chunk k writes buffer k % 2 and its epilogue reduces each row
-// over each tile to a (max, sum) pair; its epilogue warps form chunk k - 1's
-// gradient rows from buffer (k - 1) % 2 meanwhile; a standalone pass forms the
-// last chunk's.  dH and dW are then each one GEMM over all rows.
+// Fused schedule (a workspace of linear_ce_workspace_size_fused bytes): two
+// fp32 logits buffers [mc, ldl] (ldl = V rounded up to a multiple of 4), two
+// per-tile pair buffers [mc, n_tiles] and two target-logit buffers [mc], the
+// bf16 gradient rows G [M, ldv] of every row (ldv = V rounded up to a multiple
+// of 8) and the row losses [M].  The logits GEMM of chunk k writes buffer
+// k % 2 and its epilogue reduces each row over each tile to a (max, sum) pair;
+// its epilogue warps form chunk k - 1's gradient rows from buffer (k - 1) % 2
+// meanwhile; a standalone pass forms the last chunk's.  dH and dW are then
+// each one GEMM over all rows.
 //
-// Per-chunk schedule (the fallback for a smaller workspace): one logits chunk,
-// the row kernel turning it into that chunk's G [mc, ldv] and row losses, and
-// dH and dW contracted before the next chunk (dW accumulated over the chunks).
+// Lean schedule (the default, and any workspace short of the fused one): no
+// logits are stored.  Per chunk, one pair buffer [mc, n_tiles], one target-
+// logit buffer [mc], the row constants [mc] and the chunk's bf16 G [mc, ldv],
+// plus the row losses [M]: the logits GEMM keeps only the pairs, a merge pass
+// turns them into the row constants and losses, a second logits GEMM writes G
+// from its accumulators, and dH and dW are contracted before the next chunk
+// (dW accumulated over the chunks).
 //
 // The GEMMs read W, G and h in their stored layouts (MN-major operands where K
 // is not contiguous), so nothing is transposed.
 struct LinearWs {
-  size_t logits[2], part[2], xt[2], g16, rl, total;
+  size_t logits[2], part[2], xt[2], rowc, g16, rl, total;
 };
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 LinearWs linear_ws_layout(long long M, long long V, long long mc, bool fused) {
@@ -683,17 +689,21 @@ LinearWs linear_ws_layout(long long M, long long V, long long mc, bool fused) {
   std::memset(&w, 0, sizeof(w));
   size_t off = 0;
   const int nbuf = fused ? 2 : 1;
-  for (int b = 0; b < nbuf; ++b) {
-    w.logits[b] = off;
-    off += round256(static_cast<size_t>(mc) * (fused ? ldl : V) * 4);
-  }
   if (fused) {
     for (int b = 0; b < 2; ++b) {
-      w.part[b] = off;
-      off += round256(static_cast<size_t>(mc) * nt * 8);
-      w.xt[b] = off;
-      off += round256(static_cast<size_t>(mc) * 4);
+      w.logits[b] = off;
+      off += round256(static_cast<size_t>(mc) * ldl * 4);
     }
+  }
+  for (int b = 0; b < nbuf; ++b) {
+    w.part[b] = off;
+    off += round256(static_cast<size_t>(mc) * nt * 8);
+    w.xt[b] = off;
+    off += round256(static_cast<size_t>(mc) * 4);
+  }
+  if (!fused) {
+    w.rowc = off;
+    off += round256(static_cast<size_t>(mc) * 16);
   }
   w.g16 = off;
   off += round256(static_cast<size_t>(fused ? M : mc) * ldv * 2);
@@ -702,7 +712,33 @@ LinearWs linear_ws_layout(long long M, long long V, long long mc, bool fused) {
   w.total = off;
   return w;
 }
-constexpr long long kLinearDefaultChunk = 2048;
+constexpr long long kLinearDefaultChunk = 2048;   // the fused schedule's row chunk
+constexpr long long kLinearLeanMaxChunk = 2560;   // the lean schedule's largest row chunk
+
+// The lean schedule's row chunk: among the multiples of 128 up to the largest
+// that fits the workspace (and kLinearLeanMaxChunk), or all of M, the one whose
+// per-chunk dH GEMMs (ceil(rows / 128) x ceil(H / 256) tiles each) take the
+// fewest waves over the SMs, then the fewest chunks; 0 if none fits.
+long long lean_chunk(long long M, long long H, long long V, int sms, size_t ws) {
+  const long long tn = (H + 255) / 256;
+  long long best = 0, best_waves = 0, best_chunks = 0;
+  auto consider = [&](long long mc) {
+    if (linear_ws_layout(M, V, mc, false).total > ws) return;
+    long long waves = 0, chunks = 0;
+    for (long long m0 = 0; m0 < M; m0 += mc, ++chunks) {
+      const long long rows = (M - m0) < mc ? (M - m0) : mc;
+      waves += ((rows + 127) / 128 * tn + sms - 1) / sms;
+    }
+    if (best == 0 || waves < best_waves || (waves == best_waves && chunks < best_chunks)) {
+      best = mc;
+      best_waves = waves;
+      best_chunks = chunks;
+    }
+  };
+  if (M <= kLinearLeanMaxChunk) consider(M);
+  for (long long mc = 128; mc <= kLinearLeanMaxChunk && mc < M; mc += 128) consider(mc);
+  return best;
+}
 
 }  // namespace
 
@@ -814,9 +850,16 @@ ce_status ce_gemm_bf16_tn(const void* A, int64_t lda, const void* B, int64_t ldb
 
 size_t linear_ce_workspace_size(int64_t M, int64_t H, int64_t V) {
   if (M < 0 || H < 1 || V < 1) return 0;
-  const long long mc = M < kLinearDefaultChunk ? (M > 0 ? M : 1) : kLinearDefaultChunk;
-  (void)H;
-  return linear_ws_layout(M > 0 ? M : 1, V, mc, true).total;
+  const long long Mr = M > 0 ? M : 1;
+  const long long mc = Mr < kLinearLeanMaxChunk ? Mr : kLinearLeanMaxChunk;
+  return linear_ws_layout(Mr, V, mc, false).total;
+}
+
+size_t linear_ce_workspace_size_fused(int64_t M, int64_t H, int64_t V) {
+  if (M < 0 || H < 1 || V < 1) return 0;
+  const long long Mr = M > 0 ? M : 1;
+  const long long mc = Mr < kLinearDefaultChunk ? Mr : kLinearDefaultChunk;
+  return linear_ws_layout(Mr, V, mc, true).total;
 }
 
 ce_status linear_ce_fwd_bwd(const void* h, const void* W, const int64_t* targets, int64_t M,
@@ -831,26 +874,23 @@ ce_status linear_ce_fwd_bwd(const void* h, const void* W, const int64_t* targets
       (reinterpret_cast<uintptr_t>(loss) % 4))
     return CE_ERR_INVALID_ARG;
   if (M > INT32_MAX || H > INT32_MAX || V > INT32_MAX) return CE_ERR_UNSUPPORTED;
+  DeviceInfo di;
+  int dev = 0;
+  ce_status st = device_info(di, &dev);
+  if (st != CE_OK) return st;
   // the schedule and row chunk: the largest chunk (a multiple of 128, or all of
-  // M) whose workspace fits the fused schedule, else the largest that fits the
-  // per-chunk one
+  // M) whose workspace fits the fused schedule, else the lean schedule's chunk
   long long mc = M < kLinearDefaultChunk ? M : kLinearDefaultChunk;
   bool fused = true;
   while (linear_ws_layout(M, V, mc, true).total > workspace_bytes && mc > 128)
     mc = (mc / 2 + 127) / 128 * 128;
   if (linear_ws_layout(M, V, mc, true).total > workspace_bytes) {
     fused = false;
-    mc = M < kLinearDefaultChunk ? M : kLinearDefaultChunk;
-    while (linear_ws_layout(M, V, mc, false).total > workspace_bytes) {
-      if (mc <= 128) return CE_ERR_INVALID_ARG;
-      mc = (mc / 2 + 127) / 128 * 128;
-    }
+    mc = lean_chunk(M, H, V, di.sm_count, workspace_bytes);
+    if (mc == 0) return CE_ERR_INVALID_ARG;
   }
-  DeviceInfo di;
-  int dev = 0;
-  ce_status st = device_info(di, &dev);
-  if (st != CE_OK) return st;
   const LinearWs L = linear_ws_layout(M, V, mc, fused);
+  const int nt = static_cast<int>((V + ce::kLceTileCols - 1) / ce::kLceTileCols);
   char* ws = static_cast<char*>(workspace);
   auto* g16 = reinterpret_cast<__nv_bfloat16*>(ws + L.g16);
   auto* rl = reinterpret_cast<float*>(ws + L.rl);
@@ -864,7 +904,6 @@ ce_status linear_ce_fwd_bwd(const void* h, const void* W, const int64_t* targets
   uint64_t launches = 0;
   const float scale = 1.0f / static_cast<float>(M);
   if (fused) {
-    const int nt = static_cast<int>((V + ce::kLceTileCols - 1) / ce::kLceTileCols);
     ce::LceArgs prev;  // the chunk whose gradient rows are still to be formed
     std::memset(&prev, 0, sizeof(prev));
     int k = 0;
@@ -880,6 +919,8 @@ ce_status linear_ce_fwd_bwd(const void* h, const void* W, const int64_t* targets
       a.rows = static_cast<int>(rows);
       a.V = static_cast<int>(V);
       a.n_tiles = nt;
+      a.mode = ce::kLceStats;
+      a.store = 1;
       a.ldl = ldl;
       a.ldv = ldv;
       a.scale = scale;
@@ -921,20 +962,37 @@ ce_status linear_ce_fwd_bwd(const void* h, const void* W, const int64_t* targets
       return st;
     launches += 2;
   } else {
-    auto* logits = reinterpret_cast<float*>(ws + L.logits[0]);
     for (long long m0 = 0; m0 < M; m0 += mc) {
       const long long rows = (M - m0) < mc ? (M - m0) : mc;
       const auto* hc = hb + m0 * H;
-      // logits[rows, V] = h_c W^T: both operands K-major (K = H)
-      if ((st = ce::gemm_bf16(hc, H, false, Wb, H, false, logits, V, static_cast<int>(rows),
-                              static_cast<int>(V), static_cast<int>(H), 0.f, s, di.err, sms,
-                              hint)) != CE_OK)
+      ce::LceArgs a;
+      std::memset(&a, 0, sizeof(a));
+      a.part = reinterpret_cast<float2*>(ws + L.part[0]);
+      a.xt = reinterpret_cast<float*>(ws + L.xt[0]);
+      a.targets = targets + m0;
+      a.rows = static_cast<int>(rows);
+      a.V = static_cast<int>(V);
+      a.n_tiles = nt;
+      a.mode = ce::kLceStats;
+      a.store = 0;
+      a.rowc = reinterpret_cast<float4*>(ws + L.rowc);
+      a.rl = rl + m0;
+      a.g16 = g16;
+      a.ldv = ldv;
+      a.scale = scale;
+      a.err = di.err;
+      // the logits' per-tile pairs and target logits (logits = h_c W^T, K = H), no logits
+      if ((st = ce::gemm_bf16(hc, H, false, Wb, H, false, nullptr, 0, static_cast<int>(rows),
+                              static_cast<int>(V), static_cast<int>(H), 0.f, s, di.err, sms, hint,
+                              &a)) != CE_OK)
         return st;
-      // row losses, and G rows [rows, ldv] = bf16 of G = (softmax - onehot) / M
-      // written by the row kernel straight from the fp32 logits
-      if ((st = launch_rows(ce::FWD_BWD, logits, targets + m0, nullptr, rows, V, CE_F32,
-                            CE_RED_NONE, nullptr, rl + m0, nullptr, scale, stream, false, nullptr,
-                            g16, ldv)) != CE_OK)
+      // each row's log-sum-exp constants and loss
+      if ((st = ce::launch_lce_merge_rows(a, s, sms)) != CE_OK) return st;
+      // the logits again, their epilogue writing G [rows, ldv] in bf16
+      a.mode = ce::kLceGrad;
+      if ((st = ce::gemm_bf16(hc, H, false, Wb, H, false, nullptr, 0, static_cast<int>(rows),
+                              static_cast<int>(V), static_cast<int>(H), 0.f, s, di.err, sms, hint,
+                              &a)) != CE_OK)
         return st;
       // dH[rows] = G W: A = G K-major (K = V), B = W read MN-major ([V, H], H contiguous)
       if ((st = ce::gemm_bf16(g16, ldv, false, Wb, H, true, dH + m0 * H, H,
@@ -947,7 +1005,7 @@ ce_status linear_ce_fwd_bwd(const void* h, const void* W, const int64_t* targets
                               static_cast<int>(H), static_cast<int>(rows), m0 == 0 ? 0.f : 1.f,
                               s, di.err, sms, hint)) != CE_OK)
         return st;
-      launches += 3;  // the row kernel counts itself
+      launches += 5;
     }
   }
   if ((st = ce::launch_mean_rows(rl, M, loss, s)) != CE_OK) return st;

@@ -144,13 +144,18 @@ __device__ __forceinline__ bool bg_active(const LceArgs& a, const BgRow& w) {
          (w.r == w.end_r && w.r < a.bg_rows && w.end_pos > 0 && (w.pos < 0 || w.pos < w.end_pos));
 }
 
-// Merge row w.r's tile pairs into its log-sum-exp, write its row loss (the warp
-// whose range holds the row's first chunk), and prepare the constants of its
-// gradient; `start` is the chunk the warp's work in this row begins at.
-__device__ __forceinline__ void bg_merge(const LceArgs& a, BgRow& w, int lane, int start) {
-  const float2* pp = a.bg_part + static_cast<long long>(w.r) * a.n_tiles;
+// A row's constants from its per-tile pairs, the warp's lanes sharing the
+// merge: the merged (m, s), ln s, lse log2e split into Lh + Lc (Lc a small
+// correction taken once into the scale: scf = 2^-Lc * scale), and the target's
+// gradient exp(x_t - lse) - 1 times the scale, without cancellation when the
+// target dominates.
+struct RowConsts {
+  float m, lnS, Lh, scf, gt;
+};
+__device__ __forceinline__ RowConsts lce_row_consts(const float2* pp, int n_tiles, float xt,
+                                                    float scale, int lane) {
   float m = -INFINITY, s = 0.f;
-  for (int j = lane; j < a.n_tiles; j += 32) {
+  for (int j = lane; j < n_tiles; j += 32) {
     const float2 q = __ldcg(pp + j);
     merge_pair(m, s, q.x, q.y);
   }
@@ -160,10 +165,6 @@ __device__ __forceinline__ void bg_merge(const LceArgs& a, BgRow& w, int lane, i
     const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
     merge_pair(m, s, m2, s2);
   }
-  const long long t = __ldg(a.bg_targets + w.r);
-  const bool t_ok = t >= 0 && t < a.V;
-  const float xt = t_ok ? __ldcg(a.bg_xt + w.r) : 0.f;
-  // lse log2e = Lh + Lc, Lc a small correction taken once into the scale
   const float mref = (m == -INFINITY) ? 0.f : m;
   const float mhr = mref * kLog2e;
   const float mlr = fmaf(mref, kLog2e, -mhr);
@@ -171,14 +172,30 @@ __device__ __forceinline__ void bg_merge(const LceArgs& a, BgRow& w, int lane, i
   const float Lh = mhr + l2s;
   const float bv = Lh - mhr;
   const float Lc = mlr + ((mhr - (Lh - bv)) + (l2s - bv));
-  const float lnS = l2s * kLn2;
+  RowConsts c;
+  c.m = m;
+  c.lnS = l2s * kLn2;
+  c.Lh = Lh;
+  c.scf = ex2(-Lc) * scale;
+  c.gt = expm1_target((xt - m) - c.lnS) * scale;
+  return c;
+}
+
+// Merge row w.r's tile pairs into its log-sum-exp, write its row loss (the warp
+// whose range holds the row's first chunk), and prepare the constants of its
+// gradient; `start` is the chunk the warp's work in this row begins at.
+__device__ __forceinline__ void bg_merge(const LceArgs& a, BgRow& w, int lane, int start) {
+  const long long t = __ldg(a.bg_targets + w.r);
+  const bool t_ok = t >= 0 && t < a.V;
+  const float xt = t_ok ? __ldcg(a.bg_xt + w.r) : 0.f;
+  const RowConsts c =
+      lce_row_consts(a.bg_part + static_cast<long long>(w.r) * a.n_tiles, a.n_tiles, xt, a.scale, lane);
   w.t = t_ok ? t : -1;
-  w.Lh = Lh;
-  w.scf = ex2(-Lc) * a.scale;
-  // exp(x_t - lse) - 1 without cancellation when the target dominates
-  w.gt = expm1_target((xt - m) - lnS) * a.scale;
+  w.Lh = c.Lh;
+  w.scf = c.scf;
+  w.gt = c.gt;
   if (lane == 0 && start == 0) {
-    a.bg_rl[w.r] = t_ok ? (m - xt) + lnS : __int_as_float(0x7fc00000);
+    a.bg_rl[w.r] = t_ok ? (c.m - xt) + c.lnS : __int_as_float(0x7fc00000);
     if (!t_ok) atomicOr(a.err, ERR_TARGET_RANGE);
   }
   w.pos = start;
@@ -249,16 +266,44 @@ __global__ void __launch_bounds__(256) lce_grad_rows_kernel(const LceArgs a) {
   while (bg_active(a, w)) bg_step<16>(a, w, lane);
 }
 
+// The lean schedule's merge pass: a warp per row of the chunk turns the row's
+// pairs into its constants (a.rowc) and loss (a.rl); a target outside [0, V)
+// gives a NaN loss, no one-hot term (-1 in the constants) and the error word.
+__global__ void __launch_bounds__(256) lce_merge_rows_kernel(const LceArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int nwarps = static_cast<int>((gridDim.x * blockDim.x) >> 5);
+  for (int r = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5); r < a.rows;
+       r += nwarps) {
+    const long long t = __ldg(a.targets + r);
+    const bool t_ok = t >= 0 && t < a.V;
+    const float xt = t_ok ? __ldcg(a.xt + r) : 0.f;
+    const RowConsts c =
+        lce_row_consts(a.part + static_cast<long long>(r) * a.n_tiles, a.n_tiles, xt, a.scale, lane);
+    if (lane == 0) {
+      a.rowc[r] = make_float4(c.Lh, c.scf, c.gt, __int_as_float(t_ok ? static_cast<int>(t) : -1));
+      a.rl[r] = t_ok ? (c.m - xt) + c.lnS : __int_as_float(0x7fc00000);
+      if (!t_ok) atomicOr(a.err, ERR_TARGET_RANGE);
+    }
+  }
+}
+
 // A_MN / B_MN: the operands' layouts, fixed at compile time so that the
-// K-major form runs exactly the code it would alone.  LCE (K-major operands
-// only): the fused linear + CE's logits GEMM, whose epilogue also reduces each
-// row over each tile to a (max, sum) pair, keeps the target logit, and forms
-// the previous chunk's gradient rows while it waits for accumulators.
-template <bool A_MN, bool B_MN, bool LCE = false>
+// K-major form runs exactly the code it would alone.  EPI (K-major operands
+// only) extends the epilogue for the fused linear + CE:
+//  * kLceStats: the logits GEMM, whose epilogue also reduces each row over each
+//    tile to a (max, sum) pair and keeps the target logit; with p.lce.store it
+//    stores the logits too and forms the previous chunk's gradient rows while
+//    it waits for accumulators, without it stores nothing else;
+//  * kLceGrad: the logits GEMM again, whose epilogue writes the bf16 gradient
+//    exp(x - lse) * scale (the target's from the row's constants) instead of
+//    the logits.
+template <bool A_MN, bool B_MN, int EPI = 0>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap tma_a,
                         const __grid_constant__ CUtensorMap tma_b,
                         const __grid_constant__ CUtensorMap tma_d, const GemmParams p) {
+  constexpr bool LCE = EPI == kLceStats;
+  constexpr bool GRAD = EPI == kLceGrad;
   extern __shared__ unsigned char gsm[];
   __shared__ __align__(8) unsigned long long full_bar[kGemmStages];
   __shared__ __align__(8) unsigned long long empty_bar[kGemmStages];
@@ -410,6 +455,56 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       tc_fence_after();
       const int rbase = tm * kGemmBM + 32 * q;  // this warp's 32 rows of the tile
+      if constexpr (GRAD) {
+        // this thread's row (TMEM lane): g = 2^(x log2e - Lh) * scf, the
+        // target's element from the row's constants; 64 columns (one
+        // 128-byte swizzled row of bf16 per thread) per TMA store
+        const int my_row = rbase + lane;
+        float4 rc = make_float4(0.f, 0.f, 0.f, __int_as_float(-1));
+        if (my_row < p.lce.rows) rc = __ldg(p.lce.rowc + my_row);
+        const int my_t = __float_as_int(rc.w);
+#pragma unroll 1
+        for (int cc = 0; cc < kGemmBN / 64; ++cc) {
+          uint32_t r[64];
+          const uint32_t ta = tmem + static_cast<uint32_t>(a * kGemmBN + cc * 64) +
+                              (static_cast<uint32_t>(32 * q) << 16);
+          tmem_ld32_nowait(ta, r);
+          tmem_ld32_nowait(ta + 32, r + 32);
+          tmem_wait_ld<64>(r);
+          const int col0 = tn * kGemmBN + cc * 64;
+          const int o = my_t - col0;  // the target's place in this block (none outside [0, 64))
+          uint32_t pk[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            float g0 = ex2(fmaf(__uint_as_float(r[2 * j]), kLog2e, -rc.x)) * rc.y;
+            float g1 = ex2(fmaf(__uint_as_float(r[2 * j + 1]), kLog2e, -rc.x)) * rc.y;
+            if (o == 2 * j) g0 = rc.z;
+            if (o == 2 * j + 1) g1 = rc.z;
+            __nv_bfloat162 hv = __floats2bfloat162_rn(g0, g1);
+            pk[j] = *reinterpret_cast<uint32_t*>(&hv);
+          }
+          // the previous block's store has read the buffer
+          if (lane == 0) bulk_wait_read<0>();
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                             ebuf + lane * 128 + 16 * (j ^ (lane & 7))),
+                         "r"(pk[4 * j]), "r"(pk[4 * j + 1]), "r"(pk[4 * j + 2]), "r"(pk[4 * j + 3])
+                         : "memory");
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tma_d, ebuf, col0, rbase);
+            bulk_commit();
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(smem_u32(&acce_bar[a]));
+        a ^= 1;
+        if (a == 0) aph ^= 1u;
+        continue;
+      }
       // LCE: this thread's row (TMEM lane) and its running pair over the tile
       const int my_row = rbase + lane;
       long long my_t = -1;
@@ -454,6 +549,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
           }
         }
+        if (LCE && !p.lce.store) continue;  // the pairs only: nothing is stored
         if (p.use_tma) {
           // the previous block's store has read the buffer
           if (lane == 0) bulk_wait_read<0>();
@@ -595,20 +691,39 @@ static bool make_map_f32(CUtensorMap* map, void* base, long long rows, long long
             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D bf16 tensor map over the gradient rows G (rows x cols, row stride ld
+// elements, a multiple of 8) with a box of 64 x 32 and 128-byte swizzle: the
+// gradient epilogue's blocks (one 128-byte row of bf16 per thread)
+static bool make_map_g16(CUtensorMap* map, void* base, long long rows, long long cols,
+                         long long ld) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+  cuuint32_t box[2] = {64, 32};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // D[M,N] = op(A) op(B)^T (+ beta D), bf16 inputs, fp32 D.  a_mn = false: A is
 // [M, lda] with K contiguous; a_mn = true: A is stored [K, lda] with M contiguous
 // (the transpose of a K-major A).  The same for B with N.  Requires lda, ldb
 // multiples of 8 (16-byte row strides for TMA) and 16-byte aligned A and B;
 // tiles reaching past M, N or K are zero-filled by TMA.
-// lce (both operands K-major, beta = 0, D rows on the 16-byte grid): the fused
-// linear + CE's logits GEMM, with the epilogue work of ce_lce.cuh.
+// lce (both operands K-major, beta = 0): the fused linear + CE's logits GEMM,
+// with the epilogue work of ce_lce.cuh.  lce->mode kLceStats with lce->store
+// needs D with rows on the 16-byte grid; without it, and in kLceGrad (which
+// writes lce->g16, row stride lce->ldv, a multiple of 8), D is not used.
 ce_status gemm_bf16(const void* A, long long lda, bool a_mn, const void* B, long long ldb,
                     bool b_mn, float* D, long long ldd, int M, int N, int K, float beta,
                     cudaStream_t stream, unsigned int* err, int sm_count,
                     unsigned int wait_hint_ns, const LceArgs* lce) {
   if (M <= 0 || N <= 0 || K <= 0) return CE_OK;
   if (lce != nullptr && (a_mn || b_mn || beta != 0.f)) return CE_ERR_UNSUPPORTED;
-  if ((lda % 8) || (ldb % 8) || ldd < N) return CE_ERR_UNSUPPORTED;
+  const bool lce_d = lce == nullptr || (lce->mode == kLceStats && lce->store);  // D written
+  if ((lda % 8) || (ldb % 8) || (lce_d && ldd < N)) return CE_ERR_UNSUPPORTED;
   if ((a_mn ? lda < M : lda < K) || (b_mn ? ldb < N : ldb < K)) return CE_ERR_UNSUPPORTED;
   if ((reinterpret_cast<uintptr_t>(A) & 15) || (reinterpret_cast<uintptr_t>(B) & 15))
     return CE_ERR_UNSUPPORTED;
@@ -621,9 +736,16 @@ ce_status gemm_bf16(const void* A, long long lda, bool a_mn, const void* B, long
                          : (b_mn ? make_map(&mb, B, K, N, ldb, 64) : make_map(&mb, B, N, K, ldb, kGemmBN));
   if (!ok_a || !ok_b) return CE_ERR_CUDA;
   // D by TMA when its rows sit on the 16-byte grid (the tensor map's stride rule)
-  const bool use_tma = (ldd % 4 == 0) && ((reinterpret_cast<uintptr_t>(D) & 15) == 0);
+  bool use_tma = lce_d && (ldd % 4 == 0) && ((reinterpret_cast<uintptr_t>(D) & 15) == 0);
   std::memset(&md, 0, sizeof(md));
   if (use_tma && !make_map_f32(&md, D, M, N, ldd)) return CE_ERR_CUDA;
+  if (lce != nullptr && lce->mode == kLceGrad) {
+    if (lce->g16 == nullptr || (lce->ldv % 8) || lce->ldv < N ||
+        (reinterpret_cast<uintptr_t>(lce->g16) & 15))
+      return CE_ERR_UNSUPPORTED;
+    if (!make_map_g16(&md, lce->g16, M, N, lce->ldv)) return CE_ERR_CUDA;
+    use_tma = true;  // the gradient blocks leave by TMA stores
+  }
   GemmParams p;
   p.M = M;
   p.N = N;
@@ -644,11 +766,13 @@ ce_status gemm_bf16(const void* A, long long lda, bool a_mn, const void* B, long
   p.wait_hint_ns = wait_hint_ns;
   std::memset(&p.lce, 0, sizeof(p.lce));
   if (lce != nullptr) {
-    if (!use_tma || lce->n_tiles != p.tiles_n || lce->rows != M || lce->V != N)
+    if ((lce_d && !use_tma) || lce->n_tiles != p.tiles_n || lce->rows != M || lce->V != N ||
+        (lce->mode != kLceStats && lce->mode != kLceGrad))
       return CE_ERR_UNSUPPORTED;
     p.lce = *lce;
   }
-  auto kern = lce != nullptr ? gemm_bf16_kernel<false, false, true>
+  auto kern = lce != nullptr ? (lce->mode == kLceGrad ? gemm_bf16_kernel<false, false, kLceGrad>
+                                                      : gemm_bf16_kernel<false, false, kLceStats>)
               : a_mn ? (b_mn ? gemm_bf16_kernel<true, true> : gemm_bf16_kernel<true, false>)
                      : (b_mn ? gemm_bf16_kernel<false, true> : gemm_bf16_kernel<false, false>);
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem) !=
@@ -688,6 +812,14 @@ ce_status launch_mean_rows(const float* rl, long long M, float* loss, cudaStream
 
 // The gradient rows of a.bg_rows rows (the last chunk of a fused linear + CE
 // call), a warp per row, 8 warps a CTA.
+ce_status launch_lce_merge_rows(const LceArgs& a, cudaStream_t st, int sm_count) {
+  if (a.rows <= 0) return CE_OK;
+  int grid = (a.rows + 7) / 8;
+  if (grid > sm_count * 8) grid = sm_count * 8;
+  lce_merge_rows_kernel<<<grid, 256, 0, st>>>(a);
+  return cudaGetLastError() == cudaSuccess ? CE_OK : CE_ERR_CUDA;
+}
+
 ce_status launch_lce_grad_rows(const LceArgs& a, cudaStream_t st, int sm_count) {
   if (a.bg_rows <= 0) return CE_OK;
   int grid = (a.bg_rows + 7) / 8;

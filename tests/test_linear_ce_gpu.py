@@ -15,6 +15,8 @@ do not all share one sign, and the float64 comparison shows it.  The loss follow
 16-bit-input rule (2e-3).
 """
 
+import functools
+
 import numpy as np
 import pytest
 
@@ -97,13 +99,13 @@ def test_gemm_operand_layouts_against_float64(api, a_mn, b_mn, M, N, K):
     assert api.ce_check_errors() == 0
 
 
-def check_linear(api, M, H, V, seed, workspace_bytes=None):
+def check_linear(api, M, H, V, seed, workspace_bytes=None, schedule="lean"):
     h, W, t = synthetic.make_linear_ce_inputs(M, H, V, seed=seed)
     ws = None
     if workspace_bytes is not None:
         ws = torch.empty(workspace_bytes, dtype=torch.uint8, device="cuda")
     loss, dH, dW = api.linear_ce_fwd_bwd(bf16_dev(h), bf16_dev(W), torch.from_numpy(t).cuda(),
-                                         workspace=ws)
+                                         workspace=ws, schedule=schedule)
     torch.cuda.synchronize()
     assert api.ce_check_errors() == 0
     h64, W64 = oracle.decode_bf16(h), oracle.decode_bf16(W)
@@ -118,37 +120,48 @@ def check_linear(api, M, H, V, seed, workspace_bytes=None):
     assert np.all(eW <= bW), f"dW worst {np.max(eW / bW):.3g} x bound"
 
 
+@pytest.mark.parametrize("schedule", ["lean", "fused"])
 @pytest.mark.parametrize("M,H,V", [(300, 256, 1000), (257, 64, 777), (128, 4096, 2048),
                                    (1, 8, 3), (64, 512, 50257)])
-def test_linear_ce_against_oracle(api, M, H, V):
-    check_linear(api, M, H, V, seed=M + H + V)
+def test_linear_ce_against_oracle(api, M, H, V, schedule):
+    check_linear(api, M, H, V, seed=M + H + V, schedule=schedule)
 
 
 @pytest.mark.parametrize("M,H,V", [(5000, 256, 3001), (4224, 64, 1027), (2049, 128, 256)])
 def test_linear_ce_fused_chunks_against_oracle(api, M, H, V):
-    # several 2048-row chunks with the default (fused) workspace: each chunk's
-    # gradient rows are formed by the next chunk's GEMM epilogue, the last
-    # chunk's by the standalone pass; V off the 4- and 256-column grids
-    check_linear(api, M, H, V, seed=M + V)
+    # several 2048-row chunks with the fused workspace: each chunk's gradient
+    # rows are formed by the next chunk's GEMM epilogue, the last chunk's by the
+    # standalone pass; V off the 4- and 256-column grids
+    check_linear(api, M, H, V, seed=M + V, schedule="fused")
 
 
-@pytest.mark.parametrize("small_workspace", [False, True])
-def test_linear_ce_out_of_range_targets(api, small_workspace):
-    # targets outside [0, V) in the first and the last row chunk (the last one's
-    # gradient rows come from the standalone pass): those rows' losses are NaN, so
-    # the mean is NaN, their gradient rows drop the one-hot term, and the device
-    # error word is set; every other row is unaffected
+@pytest.mark.parametrize("M,H,V", [(5000, 256, 3001), (6000, 64, 1027), (2561, 128, 256),
+                                   (3000, 4096, 300)])
+def test_linear_ce_lean_chunks_against_oracle(api, M, H, V):
+    # several row chunks with the default (lean) workspace: each chunk's pairs,
+    # merged row constants and recomputed bf16 G, dW accumulated across the
+    # chunks; V off the 4- and 256-column grids; H = 4096 takes 16 dH column tiles
+    check_linear(api, M, H, V, seed=M + V + 1)
+
+
+@pytest.mark.parametrize("workspace", ["lean", "fused", "lean_128_row_chunks"])
+def test_linear_ce_out_of_range_targets(api, workspace):
+    # targets outside [0, V) in the first and the last row chunk (in the fused
+    # schedule the last one's gradient rows come from the standalone pass): those
+    # rows' losses are NaN, so the mean is NaN, their gradient rows drop the
+    # one-hot term, and the device error word is set; every other row is unaffected
     M, H, V = 4500, 64, 1003
     h, W, t = synthetic.make_linear_ce_inputs(M, H, V, seed=17)
     t[7] = V
     t[4400] = -2
     ws = None
-    if small_workspace:
+    if workspace == "lean_128_row_chunks":
         ws = torch.empty(api.linear_ce_workspace_size(128, H, V) + 4 * M + 4096,
                          dtype=torch.uint8, device="cuda")
     assert api.ce_check_errors() == 0
     loss, dH, dW = api.linear_ce_fwd_bwd(bf16_dev(h), bf16_dev(W), torch.from_numpy(t).cuda(),
-                                         workspace=ws)
+                                         workspace=ws,
+                                         schedule="fused" if workspace == "fused" else "lean")
     torch.cuda.synchronize()
     assert api.ce_check_errors() == api.CE_ERR_TARGET_RANGE
     assert api.ce_check_errors() == 0
@@ -163,7 +176,7 @@ def test_linear_ce_out_of_range_targets(api, small_workspace):
 
 
 def test_linear_ce_in_row_chunks(api):
-    # a workspace too small for one chunk: rows go through in chunks of 128
+    # a workspace with room for 128 rows at a time: the lean schedule in chunks of 128
     M, H, V = 700, 128, 1500
     ws = api.linear_ce_workspace_size(128, H, V) + 4 * M + 4096
     check_linear(api, M, H, V, seed=5, workspace_bytes=ws)
@@ -177,11 +190,13 @@ def test_linear_ce_rejects_bad_layouts(api):
         api.linear_ce_fwd_bwd(h, W, t)
 
 
-def test_linear_ce_full_width_sampled(api):
+@pytest.mark.parametrize("schedule", ["lean", "fused"])
+def test_linear_ce_full_width_sampled(api, schedule):
     # the bench shapes' H and V at 512 rows: all of loss and dH, sampled rows of dW
     M, H, V = 512, 4096, 128256
     h, W, t = synthetic.make_linear_ce_inputs(M, H, V, seed=0)
-    loss, dH, dW = api.linear_ce_fwd_bwd(bf16_dev(h), bf16_dev(W), torch.from_numpy(t).cuda())
+    loss, dH, dW = api.linear_ce_fwd_bwd(bf16_dev(h), bf16_dev(W), torch.from_numpy(t).cuda(),
+                                         schedule=schedule)
     torch.cuda.synchronize()
     assert api.ce_check_errors() == 0
     h64, W64 = oracle.decode_bf16(h), oracle.decode_bf16(W)
@@ -198,20 +213,20 @@ def test_linear_ce_full_width_sampled(api):
     assert np.all(eW <= 2.0**-8 * (np.abs(G[:, vs]).T @ np.abs(h64)) + 1e-30)
 
 
-def test_linear_ce_bench_size_sampled(api):
-    # the bench workload itself (h [8192, 4096], W [128256, 4096], seed 0) through the
-    # same call, so four row chunks of 2048 with dW accumulated across them: the loss
-    # in full, and rows of dH and dW on both sides of every chunk border, against
-    # float64 logits formed 512 rows at a time
+@functools.lru_cache(maxsize=1)
+def bench_size_reference():
+    """float64 loss, and rows of dH and dW, of the bench workload (h [8192, 4096],
+    W [128256, 4096], seed 0), its logits formed 512 rows at a time: the rows
+    straddle every chunk border of both schedules (2048-row chunks in the fused
+    one; 2432 rows in the lean one on 152 SMs, where 19 x 16 dH tiles fill two
+    waves)."""
     M, H, V = 8192, 4096, 128256
     h, W, t = synthetic.make_linear_ce_inputs(M, H, V, seed=0)
-    loss, dH, dW = api.linear_ce_fwd_bwd(bf16_dev(h), bf16_dev(W), torch.from_numpy(t).cuda())
-    torch.cuda.synchronize()
-    assert api.ce_check_errors() == 0
     h64, W64 = oracle.decode_bf16(h), oracle.decode_bf16(W)
     rng = np.random.default_rng(2)
     rows = np.unique(np.concatenate([rng.choice(M, 16, replace=False),
-                                     [0, 2047, 2048, 4095, 4096, 6143, 6144, M - 1]]))
+                                     [0, 2047, 2048, 2431, 2432, 4095, 4096, 4863, 4864, 6143,
+                                      6144, 7295, 7296, M - 1]]))
     vs = np.unique(np.concatenate([t[:32], rng.choice(V, 32, replace=False), [0, V - 1]]))
     total = 0.0
     dW_ref = np.zeros((len(vs), H))
@@ -228,7 +243,20 @@ def test_linear_ce_bench_size_sampled(api):
         for r in rows[(rows >= b0) & (rows < b0 + 512)]:
             dH_ref[r] = G[r - b0] @ W64
             dH_bnd[r] = np.abs(G[r - b0]) @ np.abs(W64)
-    assert abs(loss.item() - total / M) <= 2e-3
+    return (h, W, t), rows, vs, total / M, dH_ref, dH_bnd, dW_ref, dW_bnd
+
+
+@pytest.mark.parametrize("schedule", ["lean", "fused"])
+def test_linear_ce_bench_size_sampled(api, schedule):
+    # the bench workload itself through the same call, in both schedules (dW
+    # accumulated across the chunks in the lean one): the loss in full, and rows
+    # of dH and dW, against the float64 reference
+    (h, W, t), rows, vs, loss_ref, dH_ref, dH_bnd, dW_ref, dW_bnd = bench_size_reference()
+    loss, dH, dW = api.linear_ce_fwd_bwd(bf16_dev(h), bf16_dev(W), torch.from_numpy(t).cuda(),
+                                         schedule=schedule)
+    torch.cuda.synchronize()
+    assert api.ce_check_errors() == 0
+    assert abs(loss.item() - loss_ref) <= 2e-3
     got_H = dH[torch.from_numpy(rows).cuda()].cpu().numpy().astype(np.float64)
     for k, r in enumerate(rows):
         e = np.abs(got_H[k] - dH_ref[r])
