@@ -1048,8 +1048,8 @@ ATTN_SOURCES = ("ce_attention.cu", "ce_tc.cuh")
 # the attention sources it was taken on.
 ATTN_NCU_TRAFFIC = {
     # bf16 [32, 96, 512, 128] causal, bf16 output
-    "16dab2fec8146bfc2035d7edd17ebeba680df01bf7b477ce2a3d748dcfad31fb": {
-        "workload": "attn_causal_32x96x512x128", "bytes_per_launch": 1592443392},
+    "603aa2f3596a7a82a56875484783db1fcbc3d614f2c151ca2bf3e97f87b580a1": {
+        "workload": "attn_causal_32x96x512x128", "bytes_per_launch": 1208148736 + 383880960},
 }
 
 

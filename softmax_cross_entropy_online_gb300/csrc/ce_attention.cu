@@ -289,6 +289,11 @@ __global__ void __launch_bounds__(kAttThreads, 1)
       long long gp = 0;  // P V tiles issued, over all items
       int it = 0;
       uint32_t sq = sq0;  // this item's Q buffer
+      // shared-memory descriptors built once: a buffer's descriptor advances by
+      // (bytes >> 4) in its start-address field (the buffers sit below 256 KB
+      // on 16-byte boundaries, so the field never carries)
+      const uint64_t dk = smem_desc_sw128(sk0);
+      const uint64_t dv = smem_desc_sw128_mn(sv0, 16384);
       // S_gs into score buffer gs % 2 from K stage gs % 3, once the softmax holds
       // the buffer's previous scores (tile gs - 2) in registers
       auto issue_s = [&](long long gs) {
@@ -300,12 +305,12 @@ __global__ void __launch_bounds__(kAttThreads, 1)
           mbar_wait<false>(smem_u32(&s_free[st]), static_cast<uint32_t>(((gs >> 1) - 1) & 1),
                            p.err, failed, WAIT_LIMIT_NS, hint);
         tc_fence_after();
-        const uint32_t sk = sk0 + ks * L::kK;
+        const uint64_t da = smem_desc_sw128(sq);
+        const uint64_t db = dk + static_cast<uint64_t>(ks * (L::kK >> 4));
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          umma_bf16(tmem + st * 128, smem_desc_sw128(sq + off), smem_desc_sw128(sk + off), idesc_s,
-                    kk > 0 ? 1u : 0u);
+          const uint64_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+          umma_bf16(tmem + st * 128, da + off, db + off, idesc_s, kk > 0 ? 1u : 0u);
         }
         umma_commit(smem_u32(&s_full[st]));
         umma_commit(smem_u32(&k_empty[ks]));
@@ -340,14 +345,15 @@ __global__ void __launch_bounds__(kAttThreads, 1)
           mbar_wait<false>(smem_u32(&v_full[pb]), static_cast<uint32_t>((gp >> 1) & 1), p.err,
                            failed, WAIT_LIMIT_NS, hint);
           tc_fence_after();
-          const uint32_t sv = sv0 + pb * L::kV;
+          const uint64_t dbv = dv + static_cast<uint64_t>(pb * (L::kV >> 4));
+          const uint32_t acc0 = j > 0 ? 1u : 0u;
 #pragma unroll
           for (int kk = 0; kk < kAttBK / 16; ++kk) {
             // P: 16 keys = 8 columns; V: 64-wide D blocks of 128 keys x 128 B
             // 16 KB apart, 16 keys = 2 KB
             umma_bf16_ts(tmem + kAttTmemO, tmem + kAttTmemP + 64 * pb + 8 * kk,
-                         smem_desc_sw128_mn(sv + kk * 2048, 16384), idesc_o,
-                         (j > 0 || kk > 0) ? 1u : 0u);
+                         dbv + static_cast<uint64_t>(kk * (2048 >> 4)), idesc_o,
+                         kk > 0 ? 1u : acc0);
           }
           umma_commit(smem_u32(&pv_done[pb]));
           umma_commit(smem_u32(&v_empty[pb]));

@@ -86,17 +86,6 @@ __device__ __forceinline__ void tile_coords(const GemmParams& p, int tile, int& 
 // The fused linear + CE's gradient rows, formed by one warp per row from the
 // stored fp32 logits and the row's per-tile (max, sum) pairs (ce_lce.cuh).
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n"
-      " mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
 
 // Merge of two (max, sum of exp(x - max)) pairs: the larger max is kept and
 // the other sum rescaled by exp(its max - the larger max); two empty pairs
