@@ -832,6 +832,85 @@ def linear_side_record(L, api, dev, sh, schedule: str, steps: int = 5, warmup: i
     return out
 
 
+def linear_e2e(L, api, host_in, dev_set, work, wsb: int, M: int, H: int, V: int, steps: int):
+    """Milliseconds per step of the linear + CE end-to-end leg: every step copies
+    h, W and the targets from pinned host memory, calls linear_ce_fwd_bwd, and
+    copies the loss, dH and dW (the call's products) back to pinned host memory.
+    Pipelined as a caller streaming batches would run it: two device buffer sets
+    alternate, the input copies run on one copy stream and the output copies on
+    another, so one step's input copies overlap the previous step's output
+    copies.  Also returns the same steps run one after another on one stream."""
+    import torch
+    h_host, W_host, t_host = host_in
+    h0, W0, t0, dH0, dW0, loss0 = dev_set
+    dev = h0.device
+    sets = [(h0, W0, t0, dH0, dW0, loss0),
+            (torch.empty_like(h0), torch.empty_like(W0), torch.empty_like(t0),
+             torch.empty_like(dH0), torch.empty_like(dW0), torch.empty_like(loss0))]
+    dH_host = torch.empty(dH0.shape, dtype=dH0.dtype).pin_memory()
+    dW_host = torch.empty(dW0.shape, dtype=dW0.dtype).pin_memory()
+    loss_host = torch.empty((), dtype=torch.float32).pin_memory()
+    comp = torch.cuda.current_stream(dev)
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in sets]
+    ev_done = [torch.cuda.Event() for _ in sets]
+    ev_free = [torch.cuda.Event() for _ in sets]
+
+    def call(bs, stream):
+        h, W, t, dH, dW, loss = bs
+        st = L.linear_ce_fwd_bwd(h.data_ptr(), W.data_ptr(), t.data_ptr(), M, H, V,
+                                 loss.data_ptr(), dH.data_ptr(), dW.data_ptr(),
+                                 work.data_ptr(), wsb, stream.cuda_stream)
+        if st != 0:
+            raise api.CEError(st, "linear_ce_fwd_bwd")
+
+    def pipelined(n):
+        for i in range(n):
+            b = i % 2
+            h, W, t, dH, dW, loss = sets[b]
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(ev_free[b])  # the set's previous products are out
+                h.copy_(h_host, non_blocking=True)
+                W.copy_(W_host, non_blocking=True)
+                t.copy_(t_host, non_blocking=True)
+                ev_in[b].record(s_in)
+            comp.wait_event(ev_in[b])
+            call(sets[b], comp)
+            ev_done[b].record(comp)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_done[b])
+                loss_host.copy_(loss, non_blocking=True)
+                dH_host.copy_(dH, non_blocking=True)
+                dW_host.copy_(dW, non_blocking=True)
+                ev_free[b].record(s_out)
+        comp.wait_stream(s_out)
+
+    def serial(n):
+        h, W, t, dH, dW, loss = sets[0]
+        for _ in range(n):
+            h.copy_(h_host, non_blocking=True)
+            W.copy_(W_host, non_blocking=True)
+            t.copy_(t_host, non_blocking=True)
+            call(sets[0], comp)
+            loss_host.copy_(loss, non_blocking=True)
+            dH_host.copy_(dH, non_blocking=True)
+            dW_host.copy_(dW, non_blocking=True)
+
+    out = []
+    for fn in (pipelined, serial):
+        fn(1)  # warm: pinned pages, streams
+        torch.cuda.synchronize()
+        x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        x0.record(comp)
+        fn(steps)
+        x1.record(comp)
+        torch.cuda.synchronize()
+        out.append(x0.elapsed_time(x1) / steps)
+    del sets[1]
+    return out[0], out[1]
+
+
 def run_linear(args):
     import torch
     from softmax_cross_entropy_online_gb300 import api, build
@@ -906,20 +985,11 @@ def run_linear(args):
     gemm_tf = 2.0 * mc * V * H / (gemm_ms * 1e-3) / 1e12
     peak, peak_kind = measured_tflops()
     del logits
-    # end to end: host h, W, targets -> device, the call, loss -> host
-    loss_host = torch.empty((), dtype=torch.float32).pin_memory()
-    x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    x0.record()
-    e2e_steps = max(2, min(args.steps, 4))
-    for _ in range(e2e_steps):
-        h.copy_(h_host, non_blocking=True)
-        W.copy_(W_host, non_blocking=True)
-        t.copy_(t_host, non_blocking=True)
-        step()
-        loss_host.copy_(loss, non_blocking=True)
-    x1.record()
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(x0.elapsed_time(x1) / e2e_steps, dev)
+    # end to end: host h, W, targets -> device, the call, loss, dH and dW -> host
+    e2e_steps = max(3, min(args.steps, 6))
+    e2e_ms, e2e_serial_ms = linear_e2e(L, api, (h_host, W_host, t_host), (h, W, t, dH, dW, loss),
+                                       work, wsb, M, H, V, e2e_steps)
+    e2e_ms = max_over_ranks(e2e_ms, dev)
     if rank == 0:
         line = {
             "metric": "fused linear+CE fwd+bwd TFLOP/s (6 M V H per step)", "value": value,
@@ -936,8 +1006,12 @@ def run_linear(args):
                          "traffic": None, "kernel": f"logits GEMM [{mc}, {V}, {H}]",
                          "ms_per_launch": gemm_ms},
             "e2e": {"value": ws * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-                    "h2d_bytes_per_step": (M * H + V * H) * 2 + M * 8, "d2h_bytes_per_step": 4,
-                    "ms_per_step": e2e_ms},
+                    "h2d_bytes_per_step": (M * H + V * H) * 2 + M * 8,
+                    "d2h_bytes_per_step": 4 + (M * H + V * H) * 4,
+                    "ms_per_step": e2e_ms, "serial_ms_per_step": e2e_serial_ms,
+                    "what": "pinned host h, W, targets -> device, linear_ce_fwd_bwd, loss + dH + "
+                            "dW -> pinned host, every step; two device buffer sets in turn, "
+                            "copies on their own streams"},
             "gpu_launches": launches, "clocks": clocks,
         }
         if ws == 1 and not args.no_cpu_baseline:
