@@ -48,10 +48,10 @@ FALLBACK_HBM_GBS = 6800.0
 # those sources nulls every record until it is captured again.
 NCU_TRAFFIC: dict[str, dict[str, int]] = {
     # full-size captures, one launch each (dram__bytes_read.sum + dram__bytes_write.sum)
-    "8e7c1ee4423e094e5f1ccd5ab75ec2ed53dd5f6ef9aea1e3e0976d7af49439e7": {
-        "f32_32768x4096": 537300992 + 475473920,
-        "f16_8192x131072_spiked": 2178680064 + 2066690048,
-        "bf16_16384x50257": 1647468800 + 1585123072,
+    "672d6922993523b3e0096b00d163bf04e911922213c881643b90e89f9699cf66": {
+        "f32_32768x4096": 537248512 + 475613696,
+        "f16_8192x131072_spiked": 2170206464 + 2066579712,
+        "bf16_16384x50257": 1647763200 + 1585092352,
     },
 }
 
@@ -1122,8 +1122,8 @@ ATTN_SOURCES = ("ce_attention.cu", "ce_tc.cuh")
 # the attention sources it was taken on.
 ATTN_NCU_TRAFFIC = {
     # bf16 [32, 96, 512, 128] causal, bf16 output
-    "603aa2f3596a7a82a56875484783db1fcbc3d614f2c151ca2bf3e97f87b580a1": {
-        "workload": "attn_causal_32x96x512x128", "bytes_per_launch": 1208148736 + 383880960},
+    "f19a00c2d8914ebbbf8558354d4a93234429f425948c7d295369b06fcc658883": {
+        "workload": "attn_causal_32x96x512x128", "bytes_per_launch": 1208313856 + 383944960},
 }
 
 

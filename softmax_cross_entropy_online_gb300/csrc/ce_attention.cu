@@ -299,10 +299,10 @@ __global__ void __launch_bounds__(kAttThreads, 1)
       auto issue_s = [&](long long gs) {
         const int st = static_cast<int>(gs & 1);
         const int ks = static_cast<int>(gs % kAttKStages);
-        mbar_wait<false>(smem_u32(&k_full[ks]), static_cast<uint32_t>((gs / kAttKStages) & 1),
+        mbar_wait_fast(smem_u32(&k_full[ks]), static_cast<uint32_t>((gs / kAttKStages) & 1),
                          p.err, failed, WAIT_LIMIT_NS, hint);
         if (gs >= 2)
-          mbar_wait<false>(smem_u32(&s_free[st]), static_cast<uint32_t>(((gs >> 1) - 1) & 1),
+          mbar_wait_fast(smem_u32(&s_free[st]), static_cast<uint32_t>(((gs >> 1) - 1) & 1),
                            p.err, failed, WAIT_LIMIT_NS, hint);
         tc_fence_after();
         const uint64_t da = smem_desc_sw128(sq);
@@ -322,7 +322,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         const int n = tiles_of(qt);
         const int qb = it & 1;
         sq = sq0 + qb * L::kQ;
-        mbar_wait<false>(smem_u32(&q_full[qb]), static_cast<uint32_t>((it >> 1) & 1), p.err,
+        mbar_wait_fast(smem_u32(&q_full[qb]), static_cast<uint32_t>((it >> 1) & 1), p.err,
                          failed, WAIT_LIMIT_NS, hint);
         tc_fence_after();
         // scores run two tiles ahead of P V: S_{j+2} is issued as soon as the
@@ -337,12 +337,12 @@ __global__ void __launch_bounds__(kAttThreads, 1)
           }
           // the previous item's output has been read out of TMEM
           if (j == 0 && it > 0)
-            mbar_wait<false>(smem_u32(&o_free), static_cast<uint32_t>((it - 1) & 1), p.err, failed,
+            mbar_wait_fast(smem_u32(&o_free), static_cast<uint32_t>((it - 1) & 1), p.err, failed,
                              WAIT_LIMIT_NS, hint);
           const int pb = static_cast<int>(gp & 1);  // P buffer and V stage of this tile
-          mbar_wait<false>(smem_u32(&p_full[pb]), static_cast<uint32_t>((gp >> 1) & 1), p.err,
+          mbar_wait_fast(smem_u32(&p_full[pb]), static_cast<uint32_t>((gp >> 1) & 1), p.err,
                            failed, WAIT_LIMIT_NS, hint);
-          mbar_wait<false>(smem_u32(&v_full[pb]), static_cast<uint32_t>((gp >> 1) & 1), p.err,
+          mbar_wait_fast(smem_u32(&v_full[pb]), static_cast<uint32_t>((gp >> 1) & 1), p.err,
                            failed, WAIT_LIMIT_NS, hint);
           tc_fence_after();
           const uint64_t dbv = dv + static_cast<uint64_t>(pb * (L::kV >> 4));
@@ -363,7 +363,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
       // drain: every MMA has finished before TMEM is released
       bool drain_failed = false;
       if (gp > 0)
-        mbar_wait<false>(smem_u32(&pv_done[(gp - 1) & 1]), static_cast<uint32_t>(((gp - 1) >> 1) & 1),
+        mbar_wait_fast(smem_u32(&pv_done[(gp - 1) & 1]), static_cast<uint32_t>(((gp - 1) >> 1) & 1),
                          p.err, drain_failed, WAIT_LIMIT_NS, hint);
     }
   } else {

@@ -286,8 +286,8 @@ __global__ void __launch_bounds__(kStreamMaxWarps * 32, 1) ce_stream_kernel(cons
   int c_slot = 0;
   uint32_t c_phase = 0;
   auto wait_segment = [&]() -> uint32_t {
-    mbar_wait<false>(smem_u32(&full_bar[warp][c_slot]), c_phase, p.err, failed, WAIT_LIMIT_NS,
-                     p.wait_hint_ns);
+    mbar_wait_fast(smem_u32(&full_bar[warp][c_slot]), c_phase, p.err, failed, WAIT_LIMIT_NS,
+                   p.wait_hint_ns);
     return ring + c_slot * SB;
   };
   auto release_segment = [&]() {
