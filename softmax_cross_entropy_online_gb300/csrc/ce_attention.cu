@@ -439,18 +439,28 @@ __global__ void __launch_bounds__(kAttThreads, 1)
             for (int k = 0; k < 8; ++k)
               mx[k] = (i + 8 < 64) ? fmax3(mx[k], x[i + k], x[i + 8 + k]) : fmaxf(mx[k], x[i + k]);
         } else {
-          // keys kv0 + i with i > lim are hidden (past T, or after the query);
-          // the additive mask joins the unscaled score as mask / sm_scale, so
-          // both paths share one exponent, and a zero entry changes no bit
+          // keys kv0 + i with i > lim are hidden (past T, or after the query).
+          // Two loops, with and without the additive mask: a test of the mask
+          // pointer inside the unrolled loop made every causal diagonal tile
+          // about twice as slow as a clear one.
           const int lim = (p.causal ? min(row, p.T - 1) : p.T - 1) - kv0;
 #pragma unroll
           for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
+          if (mrow != nullptr) {
+            // the additive mask joins the unscaled score as mask / sm_scale, so
+            // both paths share one exponent, and a zero entry changes no bit
 #pragma unroll
-          for (int i = 0; i < 64; ++i) {
-            float y = x[i];
-            if (mrow != nullptr) y = fmaf(__ldg(mrow + min(kv0 + i, p.T - 1)), p.inv_scale, y);
-            x[i] = (i > lim) ? -INFINITY : y;
-            mx[i & 7] = fmaxf(mx[i & 7], x[i]);
+            for (int i = 0; i < 64; ++i) {
+              const float y = fmaf(__ldg(mrow + min(kv0 + i, p.T - 1)), p.inv_scale, x[i]);
+              x[i] = (i > lim) ? -INFINITY : y;
+              mx[i & 7] = fmaxf(mx[i & 7], x[i]);
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 64; ++i) {
+              x[i] = (i > lim) ? -INFINITY : x[i];
+              mx[i & 7] = fmaxf(mx[i & 7], x[i]);
+            }
           }
         }
         const float pm = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
