@@ -18,8 +18,9 @@
 //    item's Q arrives while this one computes) and streams K tiles of 128
 //    keys into a three-stage ring and V tiles into a two-stage ring with TMA
 //    (128-byte swizzle; K K-major for S = Q K^T, V MN-major for O = P V, so
-//    neither is transposed); K runs one tile ahead of V, each K stage
-//    refilled once its score MMA has read it;
+//    neither is transposed); K runs one tile ahead of V within an item (an
+//    item's last V is loaded with it), each K stage refilled once its score
+//    MMA has read it;
 //  * warp 1 allocates all 512 TMEM columns -- two 128 x 128 fp32 score
 //    buffers, the D-column output accumulator, two bf16 weight buffers P --
 //    and one thread issues the MMAs: scores run two tiles ahead, S_{j+2} =
@@ -259,9 +260,13 @@ __global__ void __launch_bounds__(kAttThreads, 1)
             v_bh = bh;
             v_j = j;
           }
+          // the item's last V now, not after the next item's Q: that Q buffer
+          // may still hold an output being stored, and a one-tile item's P V
+          // would wait for this V behind it
+          load_v(g - 1, bh, n - 1);
+          v_bh = -1;
         }
       }
-      if (v_bh >= 0) load_v(g - 1, v_bh, v_j);
       // drain: no copy into this CTA's shared memory is in flight when it exits
       // (the MMA thread has waited on these phases already unless a wait failed)
       bool drain_failed = false;

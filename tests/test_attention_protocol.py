@@ -152,8 +152,10 @@ def run_cta(rng, items, T, causal, stage_in_q, W, mutation):
                 pending_v = g
                 g += 1
                 yield None
-        if pending_v is not None:
+            # the item's last V before the next item's Q (whose buffer may still
+            # hold an output being stored)
             yield from load_v(pending_v)
+            pending_v = None
         # drain: nothing in flight into shared memory when the CTA ends
         for t in range(max(0, len(items) - 2), len(items)):
             yield wait(f"q_full{t & 1}", t >> 1)
