@@ -13,6 +13,18 @@ namespace ce {
 // no runtime call (defined in ce_api.cu).
 cudaError_t ensure_max_smem(const void* fn, int smem_bytes);
 
+// Programmatic dependent launch: a row kernel may be scheduled while the
+// previous kernel on its stream finishes (its CTAs take SMs as that kernel's
+// CTAs exit), and waits in griddep_wait() for that kernel's completion before
+// it touches global memory.  Back-to-back calls overlap launch and scheduling
+// with the previous call's tail (fp32 [32768, 4096] fwd+bwd: 167.7 -> 165.8 us).
+// Writes the attribute into *a; returns the number of attributes written.
+static inline int pdl_attr(cudaLaunchAttribute* a) {
+  a->id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  a->val.programmaticStreamSerializationAllowed = 1;
+  return 1;
+}
+
 // Instantiated shapes: NC consumer threads x CPT register-resident 16-byte
 // chunks per thread.  Both hold 2048 chunks (32 KB) of a row slice per CTA.
 //   NC = 256, CPT = 8: 9 warps, fewer threads with more elements each
@@ -60,15 +72,18 @@ cudaError_t rows_launch(int mode, int variant, const RowParams& p, int grid, int
   cfg.blockDim = dim3(static_cast<unsigned>(NC + 32), 1, 1);
   cfg.dynamicSmemBytes = static_cast<size_t>(smem_bytes);
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
+  int na = 0;
   if (p.CL > 1) {
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(p.CL);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = static_cast<unsigned>(p.CL);
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
   }
+  na += pdl_attr(attr + na);
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
   void* args[] = {const_cast<RowParams*>(&p)};
   return cudaLaunchKernelExC(&cfg, fn, args);
 }
@@ -138,6 +153,9 @@ cudaError_t stream_launch(int mode, bool resident, const StreamParams& p, int gr
   cfg.blockDim = dim3(static_cast<unsigned>(nwarps * 32), 1, 1);
   cfg.dynamicSmemBytes = static_cast<size_t>(smem_bytes);
   cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  cfg.numAttrs = pdl_attr(attr);
+  cfg.attrs = attr;
   void* args[] = {const_cast<StreamParams*>(&p)};
   return cudaLaunchKernelExC(&cfg, fn, args);
 }

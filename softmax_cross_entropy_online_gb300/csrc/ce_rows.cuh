@@ -196,6 +196,14 @@ __device__ __forceinline__ bool mbar_wait_fast(uint32_t bar, uint32_t parity, un
   if (mbar_test_wait(bar, parity)) return true;
   return mbar_wait<false>(bar, parity, err, failed, limit_ns, hint_ns);
 }
+// Programmatically dependent launch (see ce_launch.cuh): let the next kernel
+// on the stream be scheduled as this grid's CTAs exit, and wait until the
+// previous kernel has completed and its writes are visible.  Called by every
+// thread before any access to global memory.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -543,6 +551,7 @@ struct MinBlocks {
 template <typename T, int MODE, int NC, int CPT>
 __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
     ce_rows_kernel(const RowParams p) {
+  griddep_wait();
   using E = Elem<T>;
   constexpr int EPC = E::EPC;
   constexpr int ES = E::ES;

@@ -169,6 +169,7 @@ __device__ __forceinline__ void online_rescale(float lm, float& m, float& mh, fl
 // row meanwhile.  The host picks it when the row's pieces fit, with 4 KB slots.
 template <typename T, int MODE, int KRES>
 __global__ void __launch_bounds__(kStreamMaxWarps * 32, 1) ce_stream_kernel(const StreamParams p) {
+  griddep_wait();
   using E = Elem<T>;
   constexpr int EPC = E::EPC;
   constexpr int ES = E::ES;
