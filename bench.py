@@ -48,10 +48,10 @@ FALLBACK_HBM_GBS = 6800.0
 # those sources nulls every record until it is captured again.
 NCU_TRAFFIC: dict[str, dict[str, int]] = {
     # full-size captures, one launch each (dram__bytes_read.sum + dram__bytes_write.sum)
-    "672d6922993523b3e0096b00d163bf04e911922213c881643b90e89f9699cf66": {
-        "f32_32768x4096": 537248512 + 475613696,
-        "f16_8192x131072_spiked": 2170206464 + 2066579712,
-        "bf16_16384x50257": 1647763200 + 1585092352,
+    "d2228c4e85fdd7aa39005d7a798dca1bcce553e58ecd3148e88a58a854e2e25a": {
+        "f32_32768x4096": 537208320 + 475370752,
+        "f16_8192x131072_spiked": 2180331264 + 2066549760,
+        "bf16_16384x50257": 1647631616 + 1584869120,
     },
 }
 
