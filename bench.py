@@ -1122,8 +1122,8 @@ ATTN_SOURCES = ("ce_attention.cu", "ce_tc.cuh")
 # the attention sources it was taken on.
 ATTN_NCU_TRAFFIC = {
     # bf16 [32, 96, 512, 128] causal, bf16 output
-    "491f335c9895829195c971ecd5c023d4824eba073c05feda94555684baae71a4": {
-        "workload": "attn_causal_32x96x512x128", "bytes_per_launch": 1208168448 + 383885056},
+    "746c88baa1ac7d48c0f7702660dee8e8bab000522315844a0589b92b11403ed7": {
+        "workload": "attn_causal_32x96x512x128", "bytes_per_launch": 1208036096 + 383832064},
 }
 
 

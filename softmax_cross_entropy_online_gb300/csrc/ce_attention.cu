@@ -133,6 +133,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
                          const __grid_constant__ CUtensorMap map_k,
                          const __grid_constant__ CUtensorMap map_v,
                          const __grid_constant__ CUtensorMap map_o, const AttnParams p) {
+  griddep_wait();  // the previous kernel on the stream has completed (dependent launch)
   using L = AttnSmem<D>;
   extern __shared__ unsigned char att_smem[];
   __shared__ __align__(8) unsigned long long q_full[2], q_empty[2], o_free;
@@ -674,8 +675,21 @@ static ce_status attention_launch(const void* Q, const void* K, const void* V, c
   if (per_sm != 1) return CE_ERR_UNSUPPORTED;
   long long grid = sm_count;
   if (grid > p.n_units) grid = p.n_units;
-  attention_fwd_kernel<D, OUT16><<<static_cast<int>(grid), kAttThreads, smem, stream>>>(mq, mk, mv, mo, p);
-  return cudaGetLastError() == cudaSuccess ? CE_OK : CE_ERR_CUDA;
+  // launched as programmatically dependent, like the row kernels: the next
+  // call's CTAs take SMs as this call's exit, and wait before touching memory
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(kAttThreads, 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, attention_fwd_kernel<D, OUT16>, mq, mk, mv, mo, p) == cudaSuccess
+             ? CE_OK
+             : CE_ERR_CUDA;
 }
 
 ce_status attention_forward(const void* Q, const void* K, const void* V, const float* mask,
