@@ -48,10 +48,10 @@ FALLBACK_HBM_GBS = 6800.0
 # those sources nulls every record until it is captured again.
 NCU_TRAFFIC: dict[str, dict[str, int]] = {
     # full-size captures, one launch each (dram__bytes_read.sum + dram__bytes_write.sum)
-    "d2228c4e85fdd7aa39005d7a798dca1bcce553e58ecd3148e88a58a854e2e25a": {
-        "f32_32768x4096": 537208320 + 475370752,
-        "f16_8192x131072_spiked": 2180331264 + 2066549760,
-        "bf16_16384x50257": 1647631616 + 1584869120,
+    "a6b98fd3d850ff945570fa6fa1c0febbc9223a727ee1a603ba188e54cd384970": {
+        "f32_32768x4096": 537215488 + 475834624,
+        "f16_8192x131072_spiked": 2181138432 + 2066735872,
+        "bf16_16384x50257": 1647658752 + 1584876288,
     },
 }
 
@@ -1116,14 +1116,14 @@ def run_linear_reference(args):
 # blockwise attention forward (the flash-attention page's benchmark shape)
 # ---------------------------------------------------------------------------
 ATTN_SHAPES = {"attn_causal_32x96x512x128": (32, 96, 512, 128, True)}
-ATTN_SOURCES = ("ce_attention.cu", "ce_tc.cuh")
+ATTN_SOURCES = ("ce_attention.cu", "ce_tc.cuh", "ce_rows.cuh")
 # DRAM traffic of the attention kernel per launch on the workload above, from
 # `ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum`, valid only for
 # the attention sources it was taken on.
 ATTN_NCU_TRAFFIC = {
     # bf16 [32, 96, 512, 128] causal, bf16 output
-    "746c88baa1ac7d48c0f7702660dee8e8bab000522315844a0589b92b11403ed7": {
-        "workload": "attn_causal_32x96x512x128", "bytes_per_launch": 1208036096 + 383832064},
+    "10c15293d41d72d987172ca13ce4a6b5b77c9bac3cdd1f8da8e7c304174320af": {
+        "workload": "attn_causal_32x96x512x128", "bytes_per_launch": 1208035072 + 383947264},
 }
 
 

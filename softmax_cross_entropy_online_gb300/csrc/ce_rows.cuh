@@ -37,6 +37,10 @@
 //    shuffles, then across the row's warps through shared memory, then
 //    across the cluster through distributed shared memory (each CTA stores
 //    its pair into every peer's slot and arrives on the peer's mbarrier).
+//  * Issue slots are the scarce resource once the stream runs at the copy
+//    rate, so the streaming passes use the packed fp32 pair instructions
+//    (fma/add/mul .f32x2: two rn operations, the same results, one issue)
+//    and three-input maxima.
 //  * Mean: each CTA sums its rows' losses in row order (fp64); the last CTA
 //    to finish (integer ticket) adds the per-CTA partials in index order.
 //    No floating-point atomics, bit-reproducible for a given grid.
@@ -271,6 +275,52 @@ __device__ __forceinline__ float lg2(float x) {
   asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+// max of three floats in one instruction (NaN-ignoring, like fmaxf)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+// Packed fp32 pairs: one fma/add/mul.rn.f32x2 does the work of two rn scalar
+// operations with the same results, in one issue slot.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+  float2 d;
+  asm("{.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+  float2 d;
+  asm("{.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+// 2^(a log2e - h), 2^(b log2e - h): one packed FFMA and two EX2
+__device__ __forceinline__ float2 ex2_pair(float a, float b, float h) {
+  const float2 u = ffma2(make_float2(a, b), make_float2(kLog2e, kLog2e), make_float2(-h, -h));
+  return make_float2(ex2(u.x), ex2(u.y));
+}
+// the same, times f (the gradient's row factor)
+__device__ __forceinline__ void grad_pair(const float* x, float* g, float h, float f) {
+  const float2 r = fmul2(ex2_pair(x[0], x[1], h), make_float2(f, f));
+  g[0] = r.x;
+  g[1] = r.y;
+}
 // e^u - 1 for the target's gradient, u = x_t - lse (<= 0 up to rounding).  Below
 // u = -1/2 the difference ex2(u log2 e) - 1 loses nothing to cancellation (the
 // result is at most -0.39).  Above it the Taylor series of e^u - 1 is summed
@@ -396,8 +446,18 @@ struct Elem<float> {
     return *static_cast<const volatile float*>(p);
   }
   __device__ static __forceinline__ float chunk_max(uint4 q) {
-    return fmaxf(fmaxf(__uint_as_float(q.x), __uint_as_float(q.y)),
+    return fmax3(__uint_as_float(q.x), __uint_as_float(q.y),
                  fmaxf(__uint_as_float(q.z), __uint_as_float(q.w)));
+  }
+  // max of m and four chunks: a tree of three-input maxima
+  __device__ static __forceinline__ float max4(uint4 a, uint4 b, uint4 c, uint4 d, float m) {
+    const float m1 = fmax3(__uint_as_float(a.x), __uint_as_float(a.y), __uint_as_float(a.z));
+    const float m2 = fmax3(__uint_as_float(a.w), __uint_as_float(b.x), __uint_as_float(b.y));
+    const float m3 = fmax3(__uint_as_float(b.z), __uint_as_float(b.w), __uint_as_float(c.x));
+    const float m4 = fmax3(__uint_as_float(c.y), __uint_as_float(c.z), __uint_as_float(c.w));
+    const float m5 = fmax3(__uint_as_float(d.x), __uint_as_float(d.y), __uint_as_float(d.z));
+    const float m6 = fmax3(__uint_as_float(d.w), m, m1);
+    return fmax3(fmax3(m2, m3, m4), m5, m6);
   }
   __device__ static __forceinline__ void st(void* p, float g) { *static_cast<float*>(p) = g; }
 };
@@ -432,6 +492,9 @@ struct Elem<__half> {
     __half2 c = *reinterpret_cast<__half2*>(&q.z), d = *reinterpret_cast<__half2*>(&q.w);
     __half2 m = __hmax2(__hmax2(a, b), __hmax2(c, d));
     return fmaxf(__low2float(m), __high2float(m));
+  }
+  __device__ static __forceinline__ float max4(uint4 a, uint4 b, uint4 c, uint4 d, float m) {
+    return fmaxf(m, fmaxf(fmaxf(chunk_max(a), chunk_max(b)), fmaxf(chunk_max(c), chunk_max(d))));
   }
   __device__ static __forceinline__ void st(void* p, float g) {
     *static_cast<unsigned short*>(p) = __half_as_ushort(__float2half_rn(g));
@@ -468,6 +531,9 @@ struct Elem<__nv_bfloat16> {
     __nv_bfloat162 d = *reinterpret_cast<__nv_bfloat162*>(&q.w);
     __nv_bfloat162 m = __hmax2(__hmax2(a, b), __hmax2(c, d));
     return fmaxf(__low2float(m), __high2float(m));
+  }
+  __device__ static __forceinline__ float max4(uint4 a, uint4 b, uint4 c, uint4 d, float m) {
+    return fmaxf(m, fmaxf(fmaxf(chunk_max(a), chunk_max(b)), fmaxf(chunk_max(c), chunk_max(d))));
   }
   __device__ static __forceinline__ void st(void* p, float g) {
     *static_cast<unsigned short*>(p) = __bfloat16_as_ushort(__float2bfloat16_rn(g));
@@ -819,7 +885,7 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
           float x[EPC], gv[EPC];
           E::unpack(lds128(sbase + 16 * c), x);
 #pragma unroll
-          for (int q = 0; q < EPC; ++q) gv[q] = ex2(fmaf(x[q], kLog2e, -lh)) * scf;
+          for (int q = 0; q < EPC; q += 2) grad_pair(x + q, gv + q, lh, scf);
           sts128(sbase + 16 * c, E::pack(gv));
         }
 #pragma unroll
@@ -867,8 +933,7 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
         for (; c + 3 * GT < f1; c += 4 * GT) {
           const uint4 q0 = lds128(sbase + 16 * c), q1 = lds128(sbase + 16 * (c + GT));
           const uint4 q2 = lds128(sbase + 16 * (c + 2 * GT)), q3 = lds128(sbase + 16 * (c + 3 * GT));
-          mt = fmaxf(mt, fmaxf(fmaxf(E::chunk_max(q0), E::chunk_max(q1)),
-                               fmaxf(E::chunk_max(q2), E::chunk_max(q3))));
+          mt = E::max4(q0, q1, q2, q3, mt);
         }
         for (; c < f1; c += GT) mt = fmaxf(mt, E::chunk_max(lds128(sbase + 16 * c)));
       }
@@ -904,7 +969,8 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
           }
       } else {
         int c = f0 + gt;
-        float st1 = 0.f;  // a second partial sum shortens the dependency chain
+        // two packed partial sums: short dependency chains, half the adds
+        float2 sa = make_float2(0.f, 0.f), sb = make_float2(0.f, 0.f);
         for (; c + 3 * GT < f1; c += 4 * GT) {
           float x0[EPC], x1[EPC], x2[EPC], x3[EPC];
           E::unpack(lds128(sbase + 16 * c), x0);
@@ -912,18 +978,18 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
           E::unpack(lds128(sbase + 16 * (c + 2 * GT)), x2);
           E::unpack(lds128(sbase + 16 * (c + 3 * GT)), x3);
 #pragma unroll
-          for (int q = 0; q < EPC; ++q) {
-            st += ex2(fmaf(x0[q], kLog2e, -mh)) + ex2(fmaf(x1[q], kLog2e, -mh));
-            st1 += ex2(fmaf(x2[q], kLog2e, -mh)) + ex2(fmaf(x3[q], kLog2e, -mh));
+          for (int q = 0; q < EPC; q += 2) {
+            sa = fadd2(sa, fadd2(ex2_pair(x0[q], x0[q + 1], mh), ex2_pair(x1[q], x1[q + 1], mh)));
+            sb = fadd2(sb, fadd2(ex2_pair(x2[q], x2[q + 1], mh), ex2_pair(x3[q], x3[q + 1], mh)));
           }
         }
         for (; c < f1; c += GT) {
           float x[EPC];
           E::unpack(lds128(sbase + 16 * c), x);
 #pragma unroll
-          for (int q = 0; q < EPC; ++q) st += ex2(fmaf(x[q], kLog2e, -mh));
+          for (int q = 0; q < EPC; q += 2) sa = fadd2(sa, ex2_pair(x[q], x[q + 1], mh));
         }
-        st += st1;
+        st += (sa.x + sa.y) + (sb.x + sb.y);
       }
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -1051,7 +1117,7 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
             for (int u = 0; u < 4; ++u) {
               float gv[EPC];
 #pragma unroll
-              for (int q = 0; q < EPC; ++q) gv[q] = ex2(fmaf(x[u][q], kLog2e, -mh)) * f;
+              for (int q = 0; q < EPC; q += 2) grad_pair(x[u] + q, gv + q, mh, f);
               sts128(sbase + 16 * (c + u * GT), E::pack(gv));
             }
           }
@@ -1059,7 +1125,7 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
             float x[EPC], gv[EPC];
             E::unpack(lds128(sbase + 16 * c), x);
 #pragma unroll
-            for (int q = 0; q < EPC; ++q) gv[q] = ex2(fmaf(x[q], kLog2e, -mh)) * f;
+            for (int q = 0; q < EPC; q += 2) grad_pair(x + q, gv + q, mh, f);
             sts128(sbase + 16 * c, E::pack(gv));
           }
         }
