@@ -48,10 +48,10 @@ FALLBACK_HBM_GBS = 6800.0
 # those sources nulls every record until it is captured again.
 NCU_TRAFFIC: dict[str, dict[str, int]] = {
     # full-size captures, one launch each (dram__bytes_read.sum + dram__bytes_write.sum)
-    "a6b98fd3d850ff945570fa6fa1c0febbc9223a727ee1a603ba188e54cd384970": {
-        "f32_32768x4096": 537215488 + 475834624,
-        "f16_8192x131072_spiked": 2181138432 + 2066735872,
-        "bf16_16384x50257": 1647658752 + 1584876288,
+    "8c71097c4f7b299746e8a72f6eaf555928aa66924cc0cd27f64765b7a6085a09": {
+        "f32_32768x4096": 537248768 + 476203264,
+        "f16_8192x131072_spiked": 2182995456 + 2066819328,
+        "bf16_16384x50257": 1647309056 + 1585424896,
     },
 }
 
@@ -1122,8 +1122,8 @@ ATTN_SOURCES = ("ce_attention.cu", "ce_tc.cuh", "ce_rows.cuh")
 # the attention sources it was taken on.
 ATTN_NCU_TRAFFIC = {
     # bf16 [32, 96, 512, 128] causal, bf16 output
-    "10c15293d41d72d987172ca13ce4a6b5b77c9bac3cdd1f8da8e7c304174320af": {
-        "workload": "attn_causal_32x96x512x128", "bytes_per_launch": 1208035072 + 383947264},
+    "f85bda929c1ef721cc191afdb6f7f76fa0fc05c1ad46b827b1f2b09128439210": {
+        "workload": "attn_causal_32x96x512x128", "bytes_per_launch": 1208034048 + 384181760},
 }
 
 

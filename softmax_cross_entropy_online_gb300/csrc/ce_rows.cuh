@@ -30,10 +30,12 @@
 //    (0) and tail chunk (nI + 1) are read and written element by element by
 //    the consumer thread that owns them.  No byte outside the unit is ever
 //    touched, so neighbouring units never race.
-//  * Each consumer thread keeps its elements in registers: it takes its own
-//    max m_t first, so every element costs one exp2 (not two), keeps
-//    e = exp(x - m_t), and after the row's lse is known writes
-//    g = e * exp(m_t - lse) * scale.  Thread pairs (m_t, s_t) merge by warp
+//  * Each consumer thread reads its chunks of the stage once for the row's
+//    statistics: blocks of four chunks update an online pair (m_t, s_t), the
+//    sum rescaled by exp(m_old - m_new) when a block raises the max, so every
+//    element costs one exp2.  After the row's lse is known it reads them again
+//    and writes g = exp(x - m_t) * exp(m_t - lse) * scale.  (The register-
+//    resident shapes hold the row's chunks instead: max first, then the sum.)  Thread pairs (m_t, s_t) merge by warp
 //    shuffles, then across the row's warps through shared memory, then
 //    across the cluster through distributed shared memory (each CTA stores
 //    its pair into every peer's slot and arrives on the peer's mbarrier).
@@ -911,9 +913,14 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
         continue;
       }
 
-      // ---- per-thread max ----
+      // ---- per-thread (max, sum) ----
+      // e' = 2^(x log2e - mh) with mh = RN(m_t log2e) is a single FFMA + EX2.
+      // Since x log2e - mh = (x - m_t) log2e + ml exactly up to the FFMA's own
+      // rounding (ml = m_t log2e - mh, the same for every element of the
+      // thread), e' = e * 2^ml: the common factor is divided out once per
+      // thread, so logits sharing a large offset lose no accuracy.
       float v[KR][EPC];
-      float mt = -INFINITY;
+      float mt = -INFINITY, mh = 0.f, ml = 0.f, st = 0.f;
       if (RESIDENT) {
 #pragma unroll
         for (int k = 0; k < KR; ++k) {
@@ -927,38 +934,19 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
             for (int q = 0; q < EPC; ++q) v[k][q] = -INFINITY;
           }
         }
-      } else {
-        // four chunks per iteration: independent shared-memory loads in flight
-        int c = f0 + gt;
-        for (; c + 3 * GT < f1; c += 4 * GT) {
-          const uint4 q0 = lds128(sbase + 16 * c), q1 = lds128(sbase + 16 * (c + GT));
-          const uint4 q2 = lds128(sbase + 16 * (c + 2 * GT)), q3 = lds128(sbase + 16 * (c + 3 * GT));
-          mt = E::max4(q0, q1, q2, q3, mt);
-        }
-        for (; c < f1; c += GT) mt = fmaxf(mt, E::chunk_max(lds128(sbase + 16 * c)));
-      }
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int c = h ? ce_back : ce_front;
-        if (c >= 0) {
-          float x[EPC];
-          edge_load(c, x);
+        for (int h = 0; h < 2; ++h) {
+          const int c = h ? ce_back : ce_front;
+          if (c >= 0) {
+            float x[EPC];
+            edge_load(c, x);
 #pragma unroll
-          for (int q = 0; q < EPC; ++q) mt = fmaxf(mt, x[q]);
+            for (int q = 0; q < EPC; ++q) mt = fmaxf(mt, x[q]);
+          }
         }
-      }
-
-      // ---- one exp2 per element ----
-      // e' = 2^(x log2e - mh) with mh = RN(m_t log2e) is a single FFMA + EX2.
-      // Since x log2e - mh = (x - m_t) log2e + ml exactly up to the FFMA's own
-      // rounding (ml = m_t log2e - mh, the same for every element of the
-      // thread), e' = e * 2^ml: the common factor is divided out once per
-      // thread, so logits sharing a large offset lose no accuracy.
-      const float mref = (mt == -INFINITY) ? 0.f : mt;
-      const float mh = mref * kLog2e;
-      const float ml = fmaf(mref, kLog2e, -mh);
-      float st = 0.f;
-      if (RESIDENT) {
+        const float mref = (mt == -INFINITY) ? 0.f : mt;
+        mh = mref * kLog2e;
+        ml = fmaf(mref, kLog2e, -mh);
 #pragma unroll
         for (int k = 0; k < KR; ++k)
 #pragma unroll
@@ -967,16 +955,39 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
             v[k][q] = e;
             st += e;
           }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int c = h ? ce_back : ce_front;
+          if (c >= 0) {
+            float x[EPC];
+            edge_load(c, x);
+#pragma unroll
+            for (int q = 0; q < EPC; ++q) st += ex2(fmaf(x[q], kLog2e, -mh));
+          }
+        }
       } else {
-        int c = f0 + gt;
-        // two packed partial sums: short dependency chains, half the adds
+        // one pass over the stage: each block of four chunks updates an online
+        // pair (m_t, s_t), the running sums rescaled by 2^(mh_old - mh_new)
+        // (a factor 1 when the block does not raise the max: branch-free)
         float2 sa = make_float2(0.f, 0.f), sb = make_float2(0.f, 0.f);
+        auto rescale_to = [&](float mn) {
+          const float mhn = (mn == -INFINITY) ? 0.f : mn * kLog2e;
+          const float r = (mt == -INFINITY) ? 0.f : ex2(mh - mhn);
+          sa = fmul2(sa, make_float2(r, r));
+          sb = fmul2(sb, make_float2(r, r));
+          mt = mn;
+          mh = mhn;
+        };
+        int c = f0 + gt;
         for (; c + 3 * GT < f1; c += 4 * GT) {
+          const uint4 q0 = lds128(sbase + 16 * c), q1 = lds128(sbase + 16 * (c + GT));
+          const uint4 q2 = lds128(sbase + 16 * (c + 2 * GT)), q3 = lds128(sbase + 16 * (c + 3 * GT));
+          rescale_to(E::max4(q0, q1, q2, q3, mt));
           float x0[EPC], x1[EPC], x2[EPC], x3[EPC];
-          E::unpack(lds128(sbase + 16 * c), x0);
-          E::unpack(lds128(sbase + 16 * (c + GT)), x1);
-          E::unpack(lds128(sbase + 16 * (c + 2 * GT)), x2);
-          E::unpack(lds128(sbase + 16 * (c + 3 * GT)), x3);
+          E::unpack(q0, x0);
+          E::unpack(q1, x1);
+          E::unpack(q2, x2);
+          E::unpack(q3, x3);
 #pragma unroll
           for (int q = 0; q < EPC; q += 2) {
             sa = fadd2(sa, fadd2(ex2_pair(x0[q], x0[q + 1], mh), ex2_pair(x1[q], x1[q + 1], mh)));
@@ -984,22 +995,30 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
           }
         }
         for (; c < f1; c += GT) {
+          const uint4 q0 = lds128(sbase + 16 * c);
+          rescale_to(fmaxf(mt, E::chunk_max(q0)));
           float x[EPC];
-          E::unpack(lds128(sbase + 16 * c), x);
+          E::unpack(q0, x);
 #pragma unroll
           for (int q = 0; q < EPC; q += 2) sa = fadd2(sa, ex2_pair(x[q], x[q + 1], mh));
         }
-        st += (sa.x + sa.y) + (sb.x + sb.y);
-      }
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int c = h ? ce_back : ce_front;
-        if (c >= 0) {
-          float x[EPC];
-          edge_load(c, x);
+        for (int h = 0; h < 2; ++h) {
+          const int ce = h ? ce_back : ce_front;
+          if (ce >= 0) {
+            float x[EPC];
+            edge_load(ce, x);
+            float em = mt;
 #pragma unroll
-          for (int q = 0; q < EPC; ++q) st += ex2(fmaf(x[q], kLog2e, -mh));
+            for (int q = 0; q < EPC; ++q) em = fmaxf(em, x[q]);
+            rescale_to(em);
+#pragma unroll
+            for (int q = 0; q < EPC; q += 2) sa = fadd2(sa, ex2_pair(x[q], x[q + 1], mh));
+          }
         }
+        st = (sa.x + sa.y) + (sb.x + sb.y);
+        const float mref = (mt == -INFINITY) ? 0.f : mt;
+        ml = fmaf(mref, kLog2e, -mh);
       }
       if (MODE == FWD) {
         // every read of the stage is done: hand it back to the producer early

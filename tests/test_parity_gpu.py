@@ -212,6 +212,44 @@ def test_negative_infinity_entries(dtype):
     check_case(xs, t, dtype)
 
 
+@pytest.mark.parametrize("kernel", ["unit", "stream"])
+@pytest.mark.parametrize("dtype,V", [("f32", 3001), ("f16", 4099), ("bf16", 50257)])
+def test_degenerate_rows(kernel, dtype, V, monkeypatch):
+    # The method's degenerate rows, beside ordinary ones:
+    #  * a row with no finite logit: the sum of exponentials is empty, so its
+    #    lse is log 0 = -inf, and lse - x_t = -inf - (-inf) makes its loss and
+    #    every gradient element NaN;
+    #  * a row with one NaN logit: the NaN reaches the sum, so the row's lse,
+    #    loss and gradient are NaN (the NaN-ignoring maxima must not hide it).
+    # The other rows are unaffected and match the oracle; the mean is NaN.
+    monkeypatch.setenv("CE_KERNEL", kernel)
+    M = 6
+    x = synthetic.make_logits(M, V, "f32", 1.0, seed=V + 41)
+    x[1, :] = -np.inf
+    x[3, V // 3] = np.nan
+    t = synthetic.make_targets(M, V, seed=V + 42)
+    xs = (x if dtype == "f32" else x.astype(np.float16) if dtype == "f16"
+          else synthetic.f32_to_bf16_bits(x))
+    out = run_all(xs, t, dtype, "mean")
+    ok = np.array([0, 2, 4, 5])
+    x64 = P.widen(xs[ok], dtype)
+    ref = oracle.ce_forward(x64, t[ok], "sum")
+    tol = P.ROW_TOL[dtype]
+    for key in ("rl_f", "rl_b"):
+        got = out[key].cpu().numpy()
+        P.check_rows(key, got[ok], ref["row_loss"], tol)
+        assert np.isnan(got[1]) and np.isnan(got[3]), (key, got)
+    for key in ("lse_f", "lse_b"):
+        got = out[key].cpu().numpy()
+        P.check_lse(key, got[ok], ref["lse"], tol, None)
+        assert got[1] == -np.inf and np.isnan(got[3]), (key, got)
+    assert math.isnan(out["loss_f"].item()) and math.isnan(out["loss_b"].item())
+    g = P.to_host(out["grad_b"], dtype)
+    gw = oracle.to_f64(g, dtype)
+    assert np.isnan(gw[1]).all() and np.isnan(gw[3]).all()
+    P.check_grad(g[ok], x64, t[ok], ref["lse"], 1.0 / M, dtype)
+
+
 def test_one_hot_dominant_and_large_offsets():
     M, V = 6, 3000
     x = np.zeros((M, V), dtype=np.float32)
