@@ -35,10 +35,11 @@
 //    sum rescaled by exp(m_old - m_new) when a block raises the max, so every
 //    element costs one exp2.  After the row's lse is known it reads them again
 //    and writes g = exp(x - m_t) * exp(m_t - lse) * scale.  (The register-
-//    resident shapes hold the row's chunks instead: max first, then the sum.)  Thread pairs (m_t, s_t) merge by warp
-//    shuffles, then across the row's warps through shared memory, then
-//    across the cluster through distributed shared memory (each CTA stores
-//    its pair into every peer's slot and arrives on the peer's mbarrier).
+//    resident shapes hold the row's chunks instead: max first, then the
+//    sum.)  Thread pairs (m_t, s_t) merge by warp shuffles, then across the
+//    row's warps through shared memory, then across the cluster through
+//    distributed shared memory (each CTA stores its pair into every peer's
+//    slot and arrives on the peer's mbarrier).
 //  * Issue slots are the scarce resource once the stream runs at the copy
 //    rate, so the streaming passes use the packed fp32 pair instructions
 //    (fma/add/mul .f32x2: two rn operations, the same results, one issue)
@@ -607,8 +608,9 @@ __device__ __forceinline__ void load_range(const UnitGeo& g, int& lo, int& hi) {
 // ---------------------------------------------------------------------------
 // CPT > 0: each consumer thread keeps up to CPT full chunks of exp values in
 // registers (one exp2 per element).  CPT == 0: the stage in shared memory is
-// re-read for the backward (two exp2 per element, few registers, several CTAs
-// per SM, and no register limit on the slice length).
+// read once for the statistics and again for the backward (two exp2 per
+// element, few registers, several CTAs per SM, and no register limit on the
+// slice length).
 template <int NC, int CPT>
 struct MinBlocks {
   // streaming consumers: registers capped so that 5 (128 threads) or 3 (256
@@ -1004,10 +1006,10 @@ __global__ void __launch_bounds__(NC + 32, (MinBlocks<NC, CPT>::value))
         }
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          const int ce = h ? ce_back : ce_front;
-          if (ce >= 0) {
+          const int ec = h ? ce_back : ce_front;
+          if (ec >= 0) {
             float x[EPC];
-            edge_load(ce, x);
+            edge_load(ec, x);
             float em = mt;
 #pragma unroll
             for (int q = 0; q < EPC; ++q) em = fmaxf(em, x[q]);
