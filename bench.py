@@ -814,6 +814,19 @@ def linear_side_record(L, api, dev, sh, schedule: str, steps: int = 5, warmup: i
     torch.cuda.synchronize()
     assert api.ce_check_errors() == 0
     ms = e0.elapsed_time(e1) / steps
+    # the clocks under this step's load: about a second of back-to-back steps
+    # after the timed ones (untimed), sampled by nvidia-smi, so the record
+    # shows whether the tensor-bound step ran at a power-capped clock
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    sampler.start()
+    time.sleep(0.3)
+    i0 = sampler.mark()
+    for _ in range(max(1, int(1200.0 / ms))):
+        step()
+    torch.cuda.synchronize()
+    i1 = sampler.mark()
+    sampler.stop()
+    clocks = sampler.window(i0, i1)
     flops = 6.0 * M * V * H
     peak, kind = measured_tflops()
     tf = flops / (ms * 1e-3) / 1e12
@@ -826,7 +839,8 @@ def linear_side_record(L, api, dev, sh, schedule: str, steps: int = 5, warmup: i
            "roofline": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s",
                         "frac": tf / peak, "peak_source": kind,
                         "executed_frac": executed / peak},
-           "loss": loss.item(), "steps": steps, "workspace_bytes": wsb}
+           "loss": loss.item(), "steps": steps, "workspace_bytes": wsb,
+           "clocks": dict(clocks, window="about 1.2 s of back-to-back steps after the timed ones")}
     del h, W, t, work, dH, dW
     torch.cuda.empty_cache()
     return out
