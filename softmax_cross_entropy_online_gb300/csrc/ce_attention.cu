@@ -30,7 +30,8 @@
 //  * warps 2..9 give each query row two threads (TMEM lane = row; two warps
 //    per lane quarter), each with 64 of a tile's 128 keys: they load those
 //    scores into registers (freeing the score buffer), swap partial maxima
-//    through shared memory for the tile max, move the row's reference max only
+//    through shared memory for the tile max (one named barrier per swap: each
+//    thread writes the slot it read at the previous swap), move the row's reference max only
 //    when the tile max exceeds it by more than 2^8 (then each rescales its half
 //    of the row of O in TMEM after the previous P V has run), write
 //    P = 2^(s c - ref) as bf16 into TMEM and add it to their share of the
@@ -362,14 +363,18 @@ __global__ void __launch_bounds__(kAttThreads, 1)
       mbar_wait<false>(smem_u32(&pv_done[t & 1]), static_cast<uint32_t>((t >> 1) & 1), p.err,
                        failed, WAIT_LIMIT_NS, hint);
     };
-    // the two threads of a row swap a value through red[][r]: the first meeting
-    // makes sure the partner has read the previous value, the second that the
-    // new one is written (one named barrier per lane quarter)
+    // the two threads of a row swap a value through red[][r] with one meeting
+    // (a named barrier per lane quarter) after the writes.  Each thread writes
+    // the slot it read at the previous swap, whose value the partner wrote for
+    // it alone, so no write can overtake the partner's pending read: that read
+    // is of the other slot
+    int par = 0;
     auto swap = [&](float v) {
+      red[h ^ par][r] = v;
       group_sync(1 + q, 64);
-      red[h][r] = v;
-      group_sync(1 + q, 64);
-      return red[h ^ 1][r];
+      const float w = red[h ^ par ^ 1][r];
+      par ^= 1;
+      return w;
     };
     long long g = 0;  // score tiles consumed, over all items
     int it = 0;

@@ -329,3 +329,51 @@ def test_o_free_wait_is_implied_by_the_next_p_full():
     for seed in range(300):
         rng, bh, T, causal, grid = random_case(seed)
         simulate(rng, bh, T, causal, grid, True, mutation="no_o_free_wait")
+
+
+# ---------------------------------------------------------------------------
+# The swap of a row's two partial values between its two softmax threads
+# (csrc/ce_attention.cu, `swap`): two slots per row and one named barrier per
+# swap.  At swap k thread h writes slot h ^ (k % 2), meets its partner at the
+# barrier, and reads slot h ^ (k % 2) ^ 1: each thread overwrites only the slot
+# it read at the previous swap, so no write overtakes the partner's pending
+# read.  The model runs the two threads under random schedules; a thread at a
+# barrier waits until both have arrived there.
+# ---------------------------------------------------------------------------
+def run_swaps(rng, n, slot_of):
+    slots = [None, None]
+    arrived = [0, 0]          # barriers each thread has reached
+    pc = [0, 0]               # 0: write, 1: at the barrier, 2: read (per swap)
+    k = [0, 0]
+    while k[0] < n or k[1] < n:
+        ready = [t for t in (0, 1) if k[t] < n and (pc[t] != 1 or arrived[1 - t] > k[t])]
+        check(ready, "deadlock")
+        t = rng.choice(ready)
+        w, r = slot_of(t, k[t])
+        if pc[t] == 0:
+            slots[w] = (t, k[t])
+            arrived[t] += 1
+            pc[t] = 1
+        elif pc[t] == 1:
+            pc[t] = 2
+        else:
+            check(slots[r] == (1 - t, k[t]),
+                  f"thread {t} at swap {k[t]} read {slots[r]} from slot {r}")
+            pc[t] = 0
+            k[t] += 1
+
+
+def test_row_swap_with_one_barrier():
+    rng = random.Random(7)
+    for _ in range(500):
+        run_swaps(rng, 12, lambda h, k: (h ^ (k & 1), h ^ (k & 1) ^ 1))
+
+
+def test_row_swap_planted_mistake_is_found():
+    # each thread always writing its own slot needs a second barrier (before
+    # the write): with one, a fast thread overwrites a value its partner has
+    # not read yet
+    rng = random.Random(7)
+    with pytest.raises(ProtocolError):
+        for _ in range(500):
+            run_swaps(rng, 12, lambda h, k: (h, h ^ 1))
