@@ -48,10 +48,10 @@ FALLBACK_HBM_GBS = 6800.0
 # those sources nulls every record until it is captured again.
 NCU_TRAFFIC: dict[str, dict[str, int]] = {
     # full-size captures, one launch each (dram__bytes_read.sum + dram__bytes_write.sum)
-    "8c71097c4f7b299746e8a72f6eaf555928aa66924cc0cd27f64765b7a6085a09": {
-        "f32_32768x4096": 537248768 + 476203264,
-        "f16_8192x131072_spiked": 2182995456 + 2066819328,
-        "bf16_16384x50257": 1647309056 + 1585424896,
+    "64be446b00a875428fedd74795b8543b144316b107c705a77d476e7c30138998": {
+        "f32_32768x4096": 537308160 + 476059648,
+        "f16_8192x131072_spiked": 2176604160 + 2066951680,
+        "bf16_16384x50257": 1647397376 + 1584967168,
     },
 }
 
@@ -1136,8 +1136,8 @@ ATTN_SOURCES = ("ce_attention.cu", "ce_tc.cuh", "ce_rows.cuh")
 # the attention sources it was taken on.
 ATTN_NCU_TRAFFIC = {
     # bf16 [32, 96, 512, 128] causal, bf16 output
-    "f85bda929c1ef721cc191afdb6f7f76fa0fc05c1ad46b827b1f2b09128439210": {
-        "workload": "attn_causal_32x96x512x128", "bytes_per_launch": 1208034048 + 384181760},
+    "9a59bd1f46a665591a8092ac661dbed087c0e348b35beef0c476b0da869b5981": {
+        "workload": "attn_causal_32x96x512x128", "bytes_per_launch": 1208061696 + 383948288},
 }
 
 
