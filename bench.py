@@ -48,10 +48,10 @@ FALLBACK_HBM_GBS = 6800.0
 # those sources nulls every record until it is captured again.
 NCU_TRAFFIC: dict[str, dict[str, int]] = {
     # full-size captures, one launch each (dram__bytes_read.sum + dram__bytes_write.sum)
-    "64be446b00a875428fedd74795b8543b144316b107c705a77d476e7c30138998": {
-        "f32_32768x4096": 537308160 + 476059648,
-        "f16_8192x131072_spiked": 2176604160 + 2066951680,
-        "bf16_16384x50257": 1647397376 + 1584967168,
+    "91288ced712945cb0207ef6500f2f2fc0c69b1aa000eecf6058c9d14e97f0c6e": {
+        "f32_32768x4096": 537206528 + 476305664,
+        "f16_8192x131072_spiked": 2183476992 + 2066646272,
+        "bf16_16384x50257": 1647271168 + 1585052416,
     },
 }
 
