@@ -48,10 +48,10 @@ FALLBACK_HBM_GBS = 6800.0
 # those sources nulls every record until it is captured again.
 NCU_TRAFFIC: dict[str, dict[str, int]] = {
     # full-size captures, one launch each (dram__bytes_read.sum + dram__bytes_write.sum)
-    "91288ced712945cb0207ef6500f2f2fc0c69b1aa000eecf6058c9d14e97f0c6e": {
-        "f32_32768x4096": 537206528 + 476305664,
-        "f16_8192x131072_spiked": 2183476992 + 2066646272,
-        "bf16_16384x50257": 1647271168 + 1585052416,
+    "d87fca6c7ad3c81b4d3691c53b03664c8905388105be045da367c706607f86ef": {
+        "f32_32768x4096": 537223168 + 475344640,
+        "f16_8192x131072_spiked": 2170441728 + 2066544640,
+        "bf16_16384x50257": 1647281152 + 1585064704,
     },
 }
 
