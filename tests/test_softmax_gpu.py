@@ -67,3 +67,28 @@ def test_softmax_rejects_other_phase(api):
     buf = torch.zeros(4 * 9 + 1, dtype=torch.float16, device="cuda")
     with pytest.raises(api.CEError):
         api.ce_softmax_forward(x, buf[1:].view(4, 9))
+
+
+@pytest.mark.parametrize("kernel", ["unit", "stream"])
+@pytest.mark.parametrize("dtype,V", [("f32", 3001), ("bf16", 50257)])
+def test_softmax_degenerate_rows(api, kernel, dtype, V, monkeypatch):
+    # A row with no finite logit has an empty sum (lse = log 0 = -inf, and
+    # 0/0 probabilities: NaN); a row with one NaN logit carries the NaN into
+    # its sum, so its lse and every probability are NaN.  The other rows are
+    # unaffected.
+    monkeypatch.setenv("CE_KERNEL", kernel)
+    M = 6
+    x = synthetic.make_logits(M, V, "f32", 2.0, seed=V + 7)
+    x[2, :] = -np.inf
+    x[4, V // 2] = np.nan
+    xs = x if dtype == "f32" else synthetic.f32_to_bf16_bits(x)
+    xd = P.to_device(xs, dtype)
+    probs, lse = api.ce_softmax_forward(xd, xd, lse=True)
+    torch.cuda.synchronize()
+    p = oracle.to_f64(P.to_host(probs, dtype), dtype)
+    ok = np.array([0, 1, 3, 5])
+    check(P.to_host(probs, dtype)[ok], xs[ok], dtype)
+    assert np.isnan(p[2]).all() and np.isnan(p[4]).all()
+    lse = lse.cpu().numpy()
+    assert lse[2] == -np.inf and np.isnan(lse[4])
+    P.check_lse("lse", lse[ok], oracle.logsumexp_rows(P.widen(xs[ok], dtype)), P.ROW_TOL[dtype])
